@@ -1,0 +1,176 @@
+/*
+ * qdec.h -- C ABI of libqdec: the attention block of one GQA decode
+ * layer-step over a paged bf16 KV cache, on one NVIDIA GB300 (sm_103a).
+ *
+ * What the block computes (for every sequence b of the batch, with
+ * L_b = seq_lens[b] tokens including the new one, G = 4 query heads per KV
+ * head, D = 128, page size P = 16):
+ *
+ *   1. QK RMSNorm -- every new-token head row x (Hq query rows, Hkv key rows)
+ *      becomes x * rsqrt(mean(x^2) + eps) * w, with one weight vector w_q for
+ *      the query rows and one w_k for the key rows.  ("Qwen3 GPU optimisation"
+ *      blog by yuzheng310, part 6, fused RMSNorm after the Q/K projection.)
+ *   2. NeoX RoPE -- rotate-half at position positions[b]: for i < D/2 the pair
+ *      (i, i + D/2) turns by pos * rope_theta^(-2i/D).  (Same blog, part 6,
+ *      fused NeoX RoPE with interleave=False.)
+ *   3. Paged append -- slot t = L_b - 1 lives in page block_table[b][t / P],
+ *      row t % P; it receives bf16(k_rot) (round-to-nearest-even) and v (bits
+ *      copied).  ("What happens inside an inference engine", PagedAttention
+ *      section: 16-token blocks reached through a per-request block table.)
+ *   4. Split-KV GQA decode attention -- query head h reads KV head h / G;
+ *      out = softmax(q_rot K^T * sm_scale) V over the L_b tokens, the new one
+ *      included.  The KV sequence of each (b, KV head) is cut into pieces
+ *      processed by different CTAs, each piece yields a local softmax, and
+ *      the pieces are reduced with the exact log-sum-exp merge.  (Blog part 8,
+ *      split-KV; Qwen3-8B engine article, section 4.4.2, grouped decode.)
+ *
+ * Pool layout (one pool per layer; the blog's part-4 shape with K and V in
+ * one tensor):   kv_pool[num_pages][2][Hkv][P][D] bf16, plane 0 = K, 1 = V.
+ * Every (page, plane, head) tile is 4 KiB contiguous.
+ *
+ * Conventions shared by every call:
+ *   - bf16 tensors are passed as qdec_bf16 (raw IEEE bfloat16 bits).
+ *   - Every pointer except `shape` and `err_flag`-less calls is a DEVICE
+ *     pointer on the current CUDA device; the caller allocates and owns all
+ *     of them.  The library never allocates or frees device memory and holds
+ *     no per-call state; it caches only per-device attributes.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call is asynchronous on that stream; only
+ *     qdec_check_error synchronises.
+ *   - Host-detectable errors return a status and launch nothing.  A failed
+ *     launch returns QDEC_ERR_CUDA.  Device-detected faults (a block-table
+ *     entry outside the pool, a seq_len outside [1, max_blocks_per_seq * P],
+ *     a bounded wait that ran out) never trap: the kernel skips the affected
+ *     work, ORs a QDEC_FLAG_* bit into *err_flag (when err_flag is not NULL)
+ *     and the outputs of the affected sequences are unspecified.
+ *   - Alignment: q, k, v, kv_pool, out, q_rot and workspace must be 16-byte
+ *     aligned; q_stride, k_stride and v_stride (elements between consecutive
+ *     sequences) must be multiples of 8.  Within a sequence the heads of q
+ *     (and of k, of v) are contiguous rows of D elements, so q/k/v may be
+ *     strided views of one fused qkv buffer [B][Hq + 2 Hkv][D].
+ *   - The 36 layers of a model share block_table, seq_lens and positions;
+ *     each layer brings its own kv_pool and norm weights.
+ */
+#ifndef QDEC_H
+#define QDEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t qdec_bf16;
+
+typedef enum {
+    QDEC_OK = 0,
+    QDEC_ERR_INVALID_ARG = 1,    /* null pointer, bad size, misalignment       */
+    QDEC_ERR_UNSUPPORTED = 2,    /* shape outside what the kernels implement    */
+    QDEC_ERR_WORKSPACE = 3,      /* workspace missing or smaller than required  */
+    QDEC_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed           */
+    QDEC_ERR_DEVICE_BOUNDS = 5,  /* qdec_check_error: device saw bad page/len   */
+    QDEC_ERR_TIMEOUT = 6         /* qdec_check_error: a bounded wait gave up    */
+} qdec_status;
+
+/* Bits a kernel ORs into *err_flag. */
+#define QDEC_FLAG_BAD_PAGE   1   /* block-table entry outside [0, num_pages)   */
+#define QDEC_FLAG_BAD_SEQLEN 2   /* seq_len outside [1, max_blocks_per_seq*P]  */
+#define QDEC_FLAG_TIMEOUT    4   /* an mbarrier wait exceeded its time limit   */
+
+/* Problem description.  Supported: head_dim 128, page_size 16,
+ * num_q_heads == 4 * num_kv_heads, 1 <= batch <= 1024. */
+typedef struct {
+    int32_t batch;               /* B                                            */
+    int32_t num_q_heads;         /* Hq                                           */
+    int32_t num_kv_heads;        /* Hkv                                          */
+    int32_t head_dim;            /* D (128)                                      */
+    int32_t page_size;           /* P (16)                                       */
+    int32_t num_pages;           /* pages in kv_pool (device bounds checks)      */
+    int32_t max_blocks_per_seq;  /* row stride of block_table                    */
+    int32_t max_seq_len;         /* host upper bound of seq_lens; sizes the grid */
+    float rope_theta;            /* RoPE base, e.g. 1e6                          */
+    float eps;                   /* RMSNorm epsilon, e.g. 1e-6                   */
+    float sm_scale;              /* softmax scale; 0 selects 1/sqrt(head_dim)    */
+    int32_t num_ctas;            /* attention grid size; 0 = automatic (a whole
+                                    number of CTAs per SM).  Results do not
+                                    depend on it beyond fp32 rounding.          */
+} qdec_shape;
+
+/* Bytes of device workspace that qdec_attn_split / qdec_attn_merge /
+ * qdec_step need for `shape` on the current device (0 on an invalid shape).
+ * The workspace holds the per-piece partial results (o, lse) of the split
+ * and one arrival counter per (sequence, KV head). */
+size_t qdec_workspace_bytes(const qdec_shape *shape);
+
+/* Zero the arrival counters of a fresh workspace.  Call once after
+ * allocating it (the kernels leave the counters at zero again when they
+ * finish), and again after any call that reported a device error. */
+qdec_status qdec_workspace_init(const qdec_shape *shape, void *workspace,
+                                size_t workspace_bytes, void *stream);
+
+/* Steps 1-3 for every sequence: RMSNorm + NeoX RoPE of the new q and k rows,
+ * then the append of bf16(k_rot) and v into kv_pool at slot seq_lens[b]-1.
+ *   q [B][Hq][D] (sequence stride q_stride), k, v [B][Hkv][D] (k_stride,
+ *   v_stride); q_norm_w, k_norm_w [D]; positions, seq_lens [B] int32;
+ *   block_table [B][max_blocks_per_seq] int32; kv_pool as above (written at
+ *   one slot per (sequence, KV head) only); q_rot [B][Hq][D] fp32 output, the
+ *   normed and rotated query rows, unscaled and unrounded. */
+qdec_status qdec_append_rope(const qdec_shape *shape,
+                             const qdec_bf16 *q, int64_t q_stride,
+                             const qdec_bf16 *k, int64_t k_stride,
+                             const qdec_bf16 *v, int64_t v_stride,
+                             const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                             const int32_t *positions, const int32_t *seq_lens,
+                             const int32_t *block_table, qdec_bf16 *kv_pool,
+                             float *q_rot, int32_t *err_flag, void *stream);
+
+/* Step 4, first half: split-KV attention of q_rot (from qdec_append_rope)
+ * over the pool.  A (sequence, KV head) handled by one piece gets its bf16
+ * output written to `out` [B][Hq][D] directly; the others leave partial
+ * (o, lse) pairs in the workspace for qdec_attn_merge. */
+qdec_status qdec_attn_split(const qdec_shape *shape, const float *q_rot,
+                            const qdec_bf16 *kv_pool, const int32_t *block_table,
+                            const int32_t *seq_lens, void *workspace,
+                            size_t workspace_bytes, qdec_bf16 *out,
+                            int32_t *err_flag, void *stream);
+
+/* Step 4, second half: log-sum-exp merge of the partials qdec_attn_split left
+ * in the workspace (same shape and seq_lens), bf16 result into `out`. */
+qdec_status qdec_attn_merge(const qdec_shape *shape, const int32_t *seq_lens,
+                            const void *workspace, size_t workspace_bytes,
+                            qdec_bf16 *out, int32_t *err_flag, void *stream);
+
+/* The whole layer-step (steps 1-4) in ONE kernel launch: every CTA norms and
+ * rotates the four query rows of the (sequence, KV head) it works on, the CTA
+ * that holds the last page of a (sequence, KV head) also norms, rotates and
+ * appends the new key/value, and the last CTA to finish a split (sequence,
+ * KV head) merges its pieces.  Same arguments as qdec_append_rope plus the
+ * workspace and `out`; no q_rot buffer is needed.  The workspace counters
+ * must be zero on entry (qdec_workspace_init once). */
+qdec_status qdec_step(const qdec_shape *shape,
+                      const qdec_bf16 *q, int64_t q_stride,
+                      const qdec_bf16 *k, int64_t k_stride,
+                      const qdec_bf16 *v, int64_t v_stride,
+                      const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                      const int32_t *positions, const int32_t *seq_lens,
+                      const int32_t *block_table, qdec_bf16 *kv_pool,
+                      void *workspace, size_t workspace_bytes, qdec_bf16 *out,
+                      int32_t *err_flag, void *stream);
+
+/* Synchronise `stream`, read *err_flag (device), clear it, and map it to a
+ * status: QDEC_OK, QDEC_ERR_DEVICE_BOUNDS or QDEC_ERR_TIMEOUT (QDEC_ERR_CUDA
+ * if the stream itself failed).  The raw bits go to *flags_out if not NULL. */
+qdec_status qdec_check_error(int32_t *err_flag, void *stream, int32_t *flags_out);
+
+/* Static, human-readable name of a status. */
+const char *qdec_status_string(qdec_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t qdec_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QDEC_H */

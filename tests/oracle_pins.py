@@ -1,0 +1,409 @@
+"""Pins of the fp64 oracle against what the mathematics fixes.
+
+Each ``pin_*`` takes an :class:`oracle.Oracle` and raises AssertionError if
+the oracle disagrees with a closed form, an invariant, a special case that
+reduces to a library routine, or brute force on tiny inputs.  The pages print
+no worked numeric example for this path, so these are the oracle's anchors.
+
+They are written so that a plausible slip anywhere in the oracle fails at
+least one of them; ``test_oracle_mutants.py`` plants such slips in a copy of
+the oracle source and checks exactly that.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import scipy.special
+import torch
+
+import oracle as oracle_pkg
+from oracle import OracleError
+
+
+# ------------------------------------------------------------ tiny inputs --
+
+def bits_of(x) -> np.ndarray:
+    """bf16 bits of values that are exactly representable in bf16."""
+    f = np.asarray(x, dtype=np.float32)
+    u = f.view(np.uint32)
+    assert np.all((u & 0xFFFF) == 0), "value not exact in bf16"
+    return (u >> 16).astype(np.uint16)
+
+
+def random_bits(rng, shape, scale=1.0) -> np.ndarray:
+    """Random bf16 bit patterns (normal draws truncated to bf16)."""
+    f = (rng.standard_normal(shape) * scale).astype(np.float32)
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def f64(bits) -> np.ndarray:
+    return oracle_pkg.bf16_bits_to_f64(bits)
+
+
+class Paged:
+    """A tiny paged problem: pool [pages][2][Hkv][P][D] plus block table."""
+
+    def __init__(self, rng, seq_lens, Hq=8, Hkv=2, D=16, P=4, extra_pages=3, pool=None):
+        self.seq_lens = np.asarray(seq_lens, np.int32)
+        self.Hq, self.Hkv, self.D, self.P = Hq, Hkv, D, P
+        n = (self.seq_lens + P - 1) // P
+        self.mb = int(n.max())
+        total = int(n.sum()) + extra_pages
+        perm = rng.permutation(total)
+        self.bt = np.full((len(seq_lens), self.mb), -1, np.int32)
+        off = 0
+        for b in range(len(seq_lens)):
+            self.bt[b, :n[b]] = perm[off:off + n[b]]
+            off += int(n[b])
+        self.pool = random_bits(rng, (total, 2, Hkv, P, D)) if pool is None else pool
+        self.q = rng.standard_normal((len(seq_lens), Hq, D))
+
+    def gather(self, b, kv, g):
+        """Contiguous [L][D] rows of sequence b, plane kv, head g (numpy indexing)."""
+        L = int(self.seq_lens[b])
+        t = np.arange(L)
+        pages = self.bt[b, t // self.P]
+        return f64(self.pool[pages, kv, g, t % self.P, :])
+
+
+def _close(a, b, tol, what):
+    a, b = np.asarray(a), np.asarray(b)
+    err = np.max(np.abs(a - b)) if a.size else 0.0
+    assert np.all(np.isfinite(a)) and err <= tol, f"{what}: max |diff| {err:.3e} > {tol:.1e}"
+
+
+# ------------------------------------------------------------------- bf16 --
+
+def pin_bf16_roundtrip(orc):
+    """Every finite bf16 pattern survives widening and re-rounding exactly."""
+    for h in range(0, 1 << 16, 7):
+        e = (h >> 7) & 0xFF
+        if e == 0xFF:
+            continue
+        assert orc.double_to_bf16(orc.bf16_to_double(h)) == h, hex(h)
+
+
+def pin_bf16_rne_matches_library(orc):
+    """For binary32 inputs, the double->bf16 rounding equals torch's
+    float32->bf16 conversion (round to nearest even) bit for bit."""
+    rng = np.random.default_rng(7)
+    x = np.concatenate([
+        rng.standard_normal(3000).astype(np.float32),
+        (rng.standard_normal(1000) * 1e-38).astype(np.float32),   # subnormal range
+        (rng.standard_normal(1000) * 1e37).astype(np.float32),
+        np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 2 ** -133, 2 ** -134,
+                  3.3e38, -3.3e38], np.float32)])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = orc.f64_to_bf16_bits(x.astype(np.float64))
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, f"{bad.size} mismatches, first x={x[bad[0]]!r}"
+
+
+def pin_bf16_single_rounding(orc):
+    """Ties go to even; a double just above a tie rounds up (one rounding,
+    not double rounding through binary32); overflow gives infinity."""
+    assert orc.double_to_bf16(1 + 2 ** -8) == 0x3F80
+    assert orc.double_to_bf16(1 + 3 * 2 ** -8) == 0x3F82
+    assert orc.double_to_bf16(1 + 2 ** -8 + 2 ** -40) == 0x3F81
+    assert orc.double_to_bf16(-(1 + 2 ** -8 + 2 ** -40)) == 0xBF81
+    assert orc.double_to_bf16(3.4e38) == 0x7F80
+    assert orc.double_to_bf16(2.0 ** -133) == 0x0001
+    assert orc.double_to_bf16(2.0 ** -134) == 0x0000
+
+
+# ---------------------------------------------------------------- RMSNorm --
+
+def pin_rmsnorm_closed_form(orc):
+    x = np.array([1.0, 2.0, 3.0, 4.0])
+    _close(orc.rmsnorm(x, np.ones(4), 0.0), x / math.sqrt(7.5), 1e-15, "rmsnorm [1,2,3,4]")
+    w = np.array([1.0, 0.5, 2.0, 1.0])
+    _close(orc.rmsnorm(x, w, 0.5), x * w / math.sqrt(8.0), 1e-15, "rmsnorm weighted, eps")
+
+
+def pin_rmsnorm_invariants(orc):
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal(128)
+    y = orc.rmsnorm(x, np.ones(128), 0.0)
+    _close(np.sqrt(np.mean(y * y)), 1.0, 1e-14, "unit RMS")
+    _close(orc.rmsnorm(3.7 * x, np.ones(128), 0.0), y, 1e-14, "scale invariance")
+
+
+def pin_rmsnorm_eps_inside_root(orc):
+    x = np.full(4, 1e-3)
+    # mean(x^2) = 1e-6; with eps = 1e-6 inside the root: 1e-3 / sqrt(2e-6)
+    _close(orc.rmsnorm(x, np.ones(4), 1e-6), np.full(4, 1e-3 / math.sqrt(2e-6)), 1e-12,
+           "eps inside the root")
+    _close(orc.rmsnorm(np.zeros(4), np.ones(4), 1e-6), np.zeros(4), 0.0, "zero row")
+
+
+# ------------------------------------------------------------------- RoPE --
+
+def _rot2(x, a):
+    R = np.array([[math.cos(a), -math.sin(a)], [math.sin(a), math.cos(a)]])
+    return R @ np.asarray(x, float)
+
+
+def pin_rope_2d_is_rotation(orc):
+    """D = 2: one pair, frequency theta^0 = 1, so RoPE is the plane rotation
+    by `pos` radians (counter-clockwise)."""
+    _close(orc.rope_neox([1.0, 0.0], math.pi / 2, 1e6), [0.0, 1.0], 1e-15, "quarter turn")
+    for pos in (0.3, 7.0, 1000.0):
+        _close(orc.rope_neox([0.6, -1.2], pos, 1e6), _rot2([0.6, -1.2], pos), 1e-12, "2-D")
+
+
+def pin_rope_d4_rotate_half_pairs(orc):
+    """D = 4, theta = 10000: pair (0, 2) turns by pos, pair (1, 3) by
+    pos * 10000^(-1/2) = pos / 100 (rotate-half pairing, not interleaved)."""
+    x = np.array([0.5, -1.0, 2.0, 0.25])
+    pos = 3.0
+    y = orc.rope_neox(x, pos, 1e4)
+    a = _rot2([x[0], x[2]], pos)
+    b = _rot2([x[1], x[3]], pos / 100.0)
+    _close(y, [a[0], b[0], a[1], b[1]], 1e-14, "D=4 pairs")
+
+
+def pin_rope_invariants(orc):
+    rng = np.random.default_rng(2)
+    q, k = rng.standard_normal(128), rng.standard_normal(128)
+    _close(np.linalg.norm(orc.rope_neox(q, 12345, 1e6)), np.linalg.norm(q), 1e-12, "norm")
+    _close(orc.rope_neox(q, 0, 1e6), q, 0.0, "pos 0 identity")
+    _close(orc.rope_neox(orc.rope_neox(q, 777, 1e6), -777, 1e6), q, 1e-12, "R(p)R(-p)")
+    for m, n, c in ((5, 2, 9), (100, 40, 1000), (0, 16383, 3)):
+        d1 = orc.rope_neox(q, m, 1e6) @ orc.rope_neox(k, n, 1e6)
+        d2 = orc.rope_neox(q, m + c, 1e6) @ orc.rope_neox(k, n + c, 1e6)
+        _close(d1, d2, 1e-10, "relative position")
+
+
+# -------------------------------------------------------------- attention --
+
+def pin_attention_single_token(orc):
+    """L = 1: softmax over one token is 1, so out = V_0 and lse = s_0."""
+    rng = np.random.default_rng(3)
+    pb = Paged(rng, [1, 1], Hq=8, Hkv=2, D=16, P=4)
+    scale = 0.25
+    out, lse = orc.attention(pb.pool, pb.bt, pb.seq_lens, pb.q, scale)
+    for b in range(2):
+        for h in range(8):
+            g = h // 4
+            K, V = pb.gather(b, 0, g), pb.gather(b, 1, g)
+            _close(out[b, h], V[0], 1e-15, "out = V_0")
+            _close(lse[b, h], scale * (pb.q[b, h] @ K[0]), 1e-13, "lse = s_0")
+
+
+def pin_attention_equal_keys(orc):
+    """All keys equal: uniform weights, out = mean of V, lse = s + ln L."""
+    rng = np.random.default_rng(4)
+    pb = Paged(rng, [13, 37], Hq=4, Hkv=1, D=16, P=4)
+    krow = random_bits(rng, 16)
+    pb.pool[:, 0] = krow
+    out, lse = orc.attention(pb.pool, pb.bt, pb.seq_lens, pb.q, 0.3)
+    for b, L in enumerate(pb.seq_lens):
+        V = pb.gather(b, 1, 0)
+        for h in range(4):
+            _close(out[b, h], V.mean(axis=0), 1e-14, "mean of V")
+            _close(lse[b, h], 0.3 * (pb.q[b, h] @ f64(krow)) + math.log(L), 1e-12, "lse")
+
+
+def pin_attention_two_tokens(orc):
+    """L = 2: out = sigma V_0 + (1 - sigma) V_1 with sigma = 1 / (1 + e^(s1 - s0))."""
+    rng = np.random.default_rng(5)
+    pb = Paged(rng, [2], Hq=4, Hkv=1, D=16, P=4)
+    scale = 0.5
+    out, lse = orc.attention(pb.pool, pb.bt, pb.seq_lens, pb.q, scale)
+    K, V = pb.gather(0, 0, 0), pb.gather(0, 1, 0)
+    for h in range(4):
+        s0, s1 = scale * (pb.q[0, h] @ K[0]), scale * (pb.q[0, h] @ K[1])
+        sig = 1.0 / (1.0 + math.exp(s1 - s0))
+        _close(out[0, h], sig * V[0] + (1 - sig) * V[1], 1e-14, "two tokens")
+        _close(lse[0, h], math.log(math.exp(s0) + math.exp(s1)), 1e-13, "two-token lse")
+
+
+def pin_attention_dense_equivalence(orc):
+    """Against dense contiguous attention: rows gathered with numpy indexing,
+    scipy's softmax, numpy matmul.  Lengths straddle page boundaries."""
+    rng = np.random.default_rng(6)
+    pb = Paged(rng, [1, 3, 4, 5, 8, 15, 17, 40], Hq=8, Hkv=2, D=16, P=4)
+    scale = 1 / 4
+    out, lse = orc.attention(pb.pool, pb.bt, pb.seq_lens, pb.q, scale)
+    for b in range(len(pb.seq_lens)):
+        for h in range(8):
+            g = h // 4
+            K, V = pb.gather(b, 0, g), pb.gather(b, 1, g)
+            s = scale * (K @ pb.q[b, h])
+            _close(out[b, h], scipy.special.softmax(s) @ V, 1e-13, f"dense b={b} h={h}")
+            _close(lse[b, h], scipy.special.logsumexp(s), 1e-12, "dense lse")
+
+
+def pin_attention_page_relabel(orc):
+    """Relabelling physical pages (pool and block table together) changes nothing."""
+    rng = np.random.default_rng(8)
+    pb = Paged(rng, [9, 30, 17], Hq=8, Hkv=2, D=16, P=4, extra_pages=5)
+    out0, lse0 = orc.attention(pb.pool, pb.bt, pb.seq_lens, pb.q, 0.25)
+    perm = rng.permutation(pb.pool.shape[0])
+    pool2 = np.empty_like(pb.pool)
+    pool2[perm] = pb.pool
+    bt2 = np.where(pb.bt >= 0, perm[np.maximum(pb.bt, 0)], -1).astype(np.int32)
+    out1, lse1 = orc.attention(pool2, bt2, pb.seq_lens, pb.q, 0.25)
+    assert np.array_equal(out0, out1) and np.array_equal(lse0, lse1), "page relabel"
+
+
+def pin_attention_token_permutation(orc):
+    """Permuting (K_t, V_t) pairs jointly within a sequence changes nothing."""
+    rng = np.random.default_rng(9)
+    pb = Paged(rng, [23], Hq=4, Hkv=1, D=16, P=4)
+    out0, lse0 = orc.attention(pb.pool, pb.bt, pb.seq_lens, pb.q, 0.25)
+    L, P = 23, 4
+    t = np.arange(L)
+    rows = (pb.bt[0, t // P], t % P)
+    K = pb.pool[rows[0], 0, 0, rows[1]].copy()
+    V = pb.pool[rows[0], 1, 0, rows[1]].copy()
+    pi = rng.permutation(L)
+    pool2 = pb.pool.copy()
+    pool2[rows[0], 0, 0, rows[1]] = K[pi]
+    pool2[rows[0], 1, 0, rows[1]] = V[pi]
+    out1, lse1 = orc.attention(pool2, pb.bt, pb.seq_lens, pb.q, 0.25)
+    _close(out1, out0, 1e-13, "token permutation")
+    _close(lse1, lse0, 1e-12, "token permutation lse")
+
+
+def pin_attention_key_shift(orc):
+    """K_t + c for one c shared by all tokens shifts every score by q.c: out unchanged."""
+    rng = np.random.default_rng(10)
+    pb = Paged(rng, [11, 29], Hq=4, Hkv=1, D=16, P=4)
+    ints = rng.integers(-8, 8, size=pb.pool.shape).astype(np.float32) / 4
+    pb.pool = bits_of(ints)
+    out0, _ = orc.attention(pb.pool, pb.bt, pb.seq_lens, pb.q, 0.25)
+    c = rng.integers(-4, 4, size=16).astype(np.float32)
+    pool2 = pb.pool.copy()
+    pool2[:, 0] = bits_of(ints[:, 0] + c)     # exact in bf16 (small quarter-integers)
+    out1, _ = orc.attention(pool2, pb.bt, pb.seq_lens, pb.q, 0.25)
+    _close(out1, out0, 1e-12, "key shift")
+
+
+def pin_attention_value_affine(orc):
+    """V -> a V + b gives out -> a out + b (weights sum to one)."""
+    rng = np.random.default_rng(11)
+    pb = Paged(rng, [7, 18], Hq=4, Hkv=1, D=16, P=4)
+    ints = rng.integers(-8, 8, size=pb.pool.shape).astype(np.float32)
+    pb.pool = bits_of(ints)
+    out0, lse0 = orc.attention(pb.pool, pb.bt, pb.seq_lens, pb.q, 0.25)
+    pool2 = pb.pool.copy()
+    pool2[:, 1] = bits_of(2 * ints[:, 1] + 3)
+    out1, lse1 = orc.attention(pool2, pb.bt, pb.seq_lens, pb.q, 0.25)
+    _close(out1, 2 * out0 + 3, 1e-12, "value affine")
+    _close(lse1, lse0, 0.0, "lse independent of V")
+
+
+def pin_gqa_equals_replicated_mha(orc):
+    """Hq = 8 over Hkv = 2 equals Hq = 8 over Hkv = 8 with KV head g copied to
+    heads 4g..4g+3 (query head h reads KV head h / 4)."""
+    rng = np.random.default_rng(12)
+    pb = Paged(rng, [5, 21], Hq=8, Hkv=2, D=16, P=4)
+    out0, lse0 = orc.attention(pb.pool, pb.bt, pb.seq_lens, pb.q, 0.25)
+    rep = np.repeat(pb.pool, 4, axis=2)
+    out1, lse1 = orc.attention(np.ascontiguousarray(rep), pb.bt, pb.seq_lens, pb.q, 0.25)
+    assert np.array_equal(out0, out1) and np.array_equal(lse0, lse1), "GQA vs MHA"
+
+
+def pin_split_merge_exact(orc):
+    """Any chunking followed by the log-sum-exp merge equals the unsplit result."""
+    rng = np.random.default_rng(13)
+    pb = Paged(rng, [1, 16, 17, 45, 64], Hq=8, Hkv=2, D=16, P=4)
+    out0, lse0 = orc.attention(pb.pool, pb.bt, pb.seq_lens, pb.q, 0.25)
+    for chunk in (1, 2, 3, 16):
+        out1, lse1 = orc.attention_split(pb.pool, pb.bt, pb.seq_lens, pb.q, 0.25, chunk)
+        _close(out1, out0, 1e-13, f"split chunk={chunk}")
+        _close(lse1, lse0, 1e-12, f"split lse chunk={chunk}")
+
+
+def pin_nan_outside_context_is_ignored(orc):
+    """NaN in slots past the end and in unreferenced pages never reaches out."""
+    rng = np.random.default_rng(14)
+    pb = Paged(rng, [6, 13], Hq=4, Hkv=1, D=16, P=4, extra_pages=2)
+    out0, _ = orc.attention(pb.pool, pb.bt, pb.seq_lens, pb.q, 0.25)
+    pool2 = pb.pool.copy()
+    used = set(int(p) for p in pb.bt.ravel() if p >= 0)
+    for p in range(pool2.shape[0]):
+        if p not in used:
+            pool2[p] = 0x7FC0
+    for b, L in enumerate(pb.seq_lens):
+        pool2[pb.bt[b, (L - 1) // 4], :, :, (L - 1) % 4 + 1:] = 0x7FC0
+    out1, _ = orc.attention(pool2, pb.bt, pb.seq_lens, pb.q, 0.25)
+    assert np.array_equal(out0, out1), "NaN poison"
+
+
+def pin_errors(orc):
+    rng = np.random.default_rng(15)
+    pb = Paged(rng, [5], Hq=4, Hkv=1, D=16, P=4)
+    bad = pb.bt.copy()
+    bad[0, 1] = pb.pool.shape[0]
+    for bt, sl in ((bad, pb.seq_lens), (pb.bt, np.array([0], np.int32)),
+                   (pb.bt, np.array([pb.mb * 4 + 1], np.int32))):
+        try:
+            orc.attention(pb.pool, bt, sl, pb.q, 0.25)
+        except OracleError:
+            continue
+        raise AssertionError("bad input accepted")
+
+
+# ------------------------------------------------------------- layer-step --
+
+def _layer_problem(rng, seq_lens, Hq=8, Hkv=2, D=16, P=4):
+    pb = Paged(rng, seq_lens, Hq=Hq, Hkv=Hkv, D=D, P=P, extra_pages=4)
+    B = len(seq_lens)
+    q = random_bits(rng, (B, Hq, D))
+    k = random_bits(rng, (B, Hkv, D))
+    v = random_bits(rng, (B, Hkv, D))
+    wq = bits_of((rng.integers(2, 6, D) / 4).astype(np.float32))
+    wk = bits_of((rng.integers(2, 6, D) / 4).astype(np.float32))
+    pos = (pb.seq_lens - 1).astype(np.int32)
+    return pb, q, k, v, wq, wk, pos
+
+
+def pin_layer_append_one_slot(orc):
+    """The append changes exactly slot L-1 of every (sequence, KV head, plane):
+    K gets bf16(k_rot) rounded to nearest even, V gets v's bits."""
+    rng = np.random.default_rng(16)
+    pb, q, k, v, wq, wk, pos = _layer_problem(rng, [1, 4, 5, 16, 22])
+    before = pb.pool.copy()
+    res = orc.decode_layer(q, k, v, wq, wk, pos, pb.seq_lens, pb.bt, pb.pool, 1e6, 1e-6)
+    changed = np.zeros(before.shape, bool)
+    for b, L in enumerate(pb.seq_lens):
+        page, off = pb.bt[b, (L - 1) // 4], (L - 1) % 4
+        for g in range(2):
+            assert np.array_equal(pb.pool[page, 0, g, off], orc.f64_to_bf16_bits(res["k_rot"][b, g]))
+            assert np.array_equal(pb.pool[page, 1, g, off], v[b, g])
+        changed[page, :, :, off] = True
+    assert np.array_equal(pb.pool[~changed], before[~changed]), "append touched another slot"
+
+
+def pin_layer_composition(orc):
+    """The layer-step is norm -> rope per row, append, then attention over the
+    appended pool; and each stage uses the right weight vector."""
+    rng = np.random.default_rng(17)
+    pb, q, k, v, wq, wk, pos = _layer_problem(rng, [3, 17, 31])
+    res = orc.decode_layer(q, k, v, wq, wk, pos, pb.seq_lens, pb.bt, pb.pool, 1e6, 1e-6)
+    for b in range(3):
+        for h in range(8):
+            want = orc.rope_neox(orc.rmsnorm(f64(q[b, h]), f64(wq), 1e-6), pos[b], 1e6)
+            _close(res["q_rot"][b, h], want, 0.0, "q_rot")
+        for g in range(2):
+            want = orc.rope_neox(orc.rmsnorm(f64(k[b, g]), f64(wk), 1e-6), pos[b], 1e6)
+            _close(res["k_rot"][b, g], want, 0.0, "k_rot")
+    out, lse = orc.attention(pb.pool, pb.bt, pb.seq_lens, res["q_rot"], 1 / math.sqrt(16))
+    _close(res["out"], out, 0.0, "out after append")
+    _close(res["lse"], lse, 0.0, "lse after append")
+
+
+def pin_layer_new_token_attends_itself(orc):
+    """L = 1: the only token is the new one, so out = v (exactly, as double)."""
+    rng = np.random.default_rng(18)
+    pb, q, k, v, wq, wk, pos = _layer_problem(rng, [1, 1])
+    res = orc.decode_layer(q, k, v, wq, wk, pos, pb.seq_lens, pb.bt, pb.pool, 1e6, 1e-6)
+    for b in range(2):
+        for h in range(8):
+            _close(res["out"][b, h], f64(v[b, h // 4]), 0.0, "out = v")
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,70 @@
+"""Plausible slips planted in a copy of the oracle must each fail a pin.
+
+Every mutant is a one-line textual change of qdec_oracle.c (a dropped term, a
+wrong sign or index, a transposed layout), compiled into a temporary
+library on the CPU.  The pin suite that guards the real oracle must reject
+every one of them; if a mutant survives, the pins have a blind spot.
+"""
+import os
+import tempfile
+
+import pytest
+
+import oracle
+import oracle_pins
+
+MUTANTS = [
+    ("rope sign of the first half", "y[i] = x1 * c - x2 * s;", "y[i] = x1 * c + x2 * s;"),
+    ("rope sign of the second half", "y[i + half] = x2 * c + x1 * s;",
+     "y[i + half] = x2 * c - x1 * s;"),
+    ("rope interleaved pairs", "double x1 = x[i], x2 = x[i + half];",
+     "double x1 = x[(2 * i) % D], x2 = x[(2 * i + 1) % D];"),
+    ("rope frequency exponent", "-2.0 * (double)i / (double)D", "-1.0 * (double)i / (double)D"),
+    ("rmsnorm eps outside the root", "1.0 / sqrt(ss / (double)D + eps)",
+     "1.0 / (sqrt(ss / (double)D) + eps)"),
+    ("rmsnorm sum instead of mean", "1.0 / sqrt(ss / (double)D + eps)", "1.0 / sqrt(ss + eps)"),
+    ("rmsnorm weight dropped", "y[i] = x[i] * r * w[i];", "y[i] = x[i] * r;"),
+    ("gqa head mapping", "int g = h / G;", "int g = h % Hkv;"),
+    ("softmax scale dropped", "s[t - t0] = scale * dot;", "s[t - t0] = dot;"),
+    ("max not subtracted", "double w = exp(s[t - t0] - m);", "double w = exp(s[t - t0]);"),
+    ("normalisation dropped", "out[i] /= l;", "out[i] /= 1.0;"),
+    ("merge weight", "double w = exp(lse_s[s] - M);", "double w = exp(-M);"),
+    ("merge lse", "lse[(long)b * Hq + h] = M + log(den);", "lse[(long)b * Hq + h] = M;"),
+    ("append slot off by one", "long rk = pool_row(&d, block_table, b, L - 1, 0, h);",
+     "long rk = pool_row(&d, block_table, b, L > 1 ? L - 2 : 0, 0, h);"),
+    ("append v from k", "pool[rv + i] = v[o + i];", "pool[rv + i] = k[o + i];"),
+    ("append k unrounded bits", "pool[rk + i] = oracle_double_to_bf16(k_rot[o + i]);",
+     "pool[rk + i] = oracle_double_to_bf16(k_rot[o + i] * 1.001);"),
+    ("pool layout head/plane transposed", "((((long)page * 2 + kv) * d->Hkv + h)",
+     "((((long)page * d->Hkv + h) * 2 + kv)"),
+    ("page index within block", "t / d->P];", "t % d->P];"),
+    ("bf16 truncation", "nearbyint(x / ulp)", "trunc(x / ulp)"),
+    ("bf16 spacing", "ldexp(1.0, e - 8)", "ldexp(1.0, e - 9)"),
+    ("q normed with the k weight", "oracle_rmsnorm(x, wq, D, eps, xn);",
+     "oracle_rmsnorm(x, wk, D, eps, xn);"),
+    ("rope at position + 1", "double pos = (double)positions[b];",
+     "double pos = (double)positions[b] + 1.0;"),
+]
+
+
+@pytest.fixture(scope="module")
+def source():
+    with open(oracle.SOURCE) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(source, name, old, new):
+    assert source.count(old) >= 1, f"mutation site not found: {old!r}"
+    with tempfile.TemporaryDirectory() as d:
+        src = os.path.join(d, "mutant.c")
+        with open(src, "w") as f:
+            f.write(source.replace(old, new))
+        orc = oracle.Oracle(oracle.build(force=True, src=src, out=os.path.join(d, "libm.so")))
+        failed = []
+        for pin in oracle_pins.ALL_PINS:
+            try:
+                pin(orc)
+            except (AssertionError, oracle.OracleError):
+                failed.append(pin.__name__)
+        assert failed, f"mutant '{name}' passed every pin"
