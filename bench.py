@@ -1,0 +1,411 @@
+#!/usr/bin/env python3
+"""Decode-attention benchmark: one JSON line on rank 0.
+
+A step is one decode step of the attention block of a 36-layer model: 36
+back-to-back layer-steps (qdec_step: QK RMSNorm + NeoX RoPE + paged append +
+split-KV GQA attention with the log-sum-exp merge, one kernel launch each),
+each layer with its own KV pool, all layers sharing the block table.  The 36
+launches are captured once in a CUDA graph and replayed per step.
+
+value   = KV GB/s: algorithmic bytes (KV read at token granularity plus the
+          q/k/v inputs and the output) / device time, over all ranks.
+e2e     = the same metric with, every step, the host->device copy of the
+          step's new-token inputs and metadata from pinned memory and the
+          device->host copy of the outputs inside the timed region.
+roofline = the fused kernel against the measured HBM copy bandwidth.
+cpu_baseline / --impl reference = the fp64 CPU oracle on a bounded sample.
+
+Multi-GPU: the path shards without any exchange, so N ranks run N
+independent replicas (weak scaling); value sums their work over the slowest
+rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gqa_paged_kv_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "decode-attn µs/layer-step and KV GB/s (% of GB300 HBM peak) per batch×ctx"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ("gqa_paged_kv_gb300/csrc/qdec_kernels.cu", "gqa_paged_kv_gb300/csrc/qdec_internal.h")
+
+# DRAM bytes per launch of the fused kernel measured with ncu (see
+# profiles/), keyed by workload; used only while the kernel source hash
+# still matches the one the counters were taken on.
+TRAFFIC = {}
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", type=int, default=2, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch the 36 calls eagerly")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ infra --
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            torch.cuda.set_device(self.local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class Clocks:
+    """nvidia-smi samples of this GPU's clocks and throttle reasons."""
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.bus = None
+        try:
+            props = torch.cuda.get_device_properties(device)
+            self.bus = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id,
+                                             props.pci_device_id)
+        except Exception:
+            pass
+        self.proc = None
+        self.path = None
+
+    def _cmd(self, loop_ms=None):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits"]
+        if self.bus:
+            cmd += ["-i", self.bus]
+        if loop_ms:
+            cmd += ["-lms", str(loop_ms)]
+        return cmd
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(self._cmd(50), stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        rows = []
+        try:
+            snap = subprocess.run(self._cmd(), capture_output=True, text=True, timeout=20).stdout
+        except (OSError, subprocess.SubprocessError):
+            snap = ""
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait(timeout=10)
+        text = (open(self.path).read() if self.path else "") + snap
+        for line in text.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                rows.append((float(f[2]), float(f[3]), f[5:]))
+            except ValueError:
+                continue
+        if self.path:
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ("active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2])
+                          if i > 0 and v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------ CPU oracle --
+def oracle_sample(w: wl.Workload, seconds: float, per_seq: bool):
+    """Time the fp64 oracle (as it stands, one thread) on a bounded sample of
+    the workload: layer-steps in order (one sequence at a time when per_seq),
+    until `seconds` have passed.  Returns (GB/s, description, steps, elapsed)."""
+    import oracle
+    B = w.spec.batch
+    units = ([(l, [b]) for l in range(w.spec.layers) for b in range(B)] if per_seq
+             else [(l, None) for l in range(w.spec.layers)])
+    bytes_done, n, t_total = 0, 0, 0.0
+    i = 0
+    while t_total < seconds or n == 0:
+        layer, seqs = units[i % len(units)]
+        inp = wl.oracle_inputs(w, layer, seqs)
+        pool = inp["pool"].copy()
+        t0 = time.perf_counter()
+        oracle.decode_layer(inp["q"], inp["k"], inp["v"], inp["w_q"], inp["w_k"],
+                            inp["positions"], inp["seq_lens"], inp["block_table"], pool,
+                            inp["rope_theta"], inp["eps"])
+        t_total += time.perf_counter() - t0
+        sl = inp["seq_lens"].astype(np.int64)
+        bytes_done += int(sl.sum()) * w.spec.kv_bytes_per_token() + len(sl) * w.spec.io_bytes_per_seq()
+        n += 1
+        i += 1
+    what = "one sequence of one layer" if per_seq else "one layer (all sequences)"
+    return bytes_done / t_total / 1e9, what, n, t_total
+
+
+def run_reference(args, dist: Dist):
+    """The reference arm: the CPU oracle, timed as it stands on the host."""
+    if dist.rank != 0:
+        return
+    spec = wl.WORKLOADS[args.workload]
+    w = wl.build(spec, "cpu")
+    # warm-up steps, then exactly K timed steps; a step is one sequence of one layer
+    oracle_steps(w, args.warmup)
+    t0 = time.perf_counter()
+    gbs_bytes = oracle_steps(w, args.steps)
+    dt = time.perf_counter() - t0
+    value = gbs_bytes / dt / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": spec.name, "batch": spec.batch, "layers": spec.layers,
+                   "step": "fp64 oracle, one sequence of one layer-step per step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} steps of one sequence x one layer, "
+                                   f"{dt:.1f} s"},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def oracle_steps(w: wl.Workload, k: int) -> int:
+    import oracle
+    B = w.spec.batch
+    done = 0
+    for i in range(k):
+        layer, b = (i // B) % w.spec.layers, i % B
+        inp = wl.oracle_inputs(w, layer, [b])
+        pool = inp["pool"].copy()
+        oracle.decode_layer(inp["q"], inp["k"], inp["v"], inp["w_q"], inp["w_k"],
+                            inp["positions"], inp["seq_lens"], inp["block_table"], pool,
+                            inp["rope_theta"], inp["eps"])
+        done += int(inp["seq_lens"][0]) * w.spec.kv_bytes_per_token() + w.spec.io_bytes_per_seq()
+    return done
+
+
+# -------------------------------------------------------------- our path --
+def run_ours(args, dist: Dist):
+    from gqa_paged_kv_gb300 import build as qbuild
+    qbuild.build()
+    from gqa_paged_kv_gb300 import qdec
+
+    dev = dist.local
+    torch.cuda.set_device(dev)
+    spec = wl.WORKLOADS[args.workload]
+    w = wl.build(spec, f"cuda:{dev}")
+    L = spec.layers
+    shape = qdec.shape_for(w)
+    stream = torch.cuda.Stream()
+    ws = qdec.alloc_workspace(shape)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty((L, spec.batch, spec.num_q_heads, spec.head_dim), dtype=torch.bfloat16,
+                      device="cuda")
+    torch.cuda.synchronize()
+
+    def layers():
+        for l in range(L):
+            qdec.qdec_step(shape, w.q(l), w.k(l), w.v(l), w.w_q[l], w.w_k[l], w.positions,
+                           w.seq_lens, w.block_table, w.pool(l), ws, out[l], err, stream=stream)
+
+    with torch.cuda.stream(stream):
+        layers()  # first launch configures the kernels outside capture
+    stream.synchronize()
+    if args.no_graph:
+        run = layers
+    else:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                layers()
+        run = graph.replay
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            run()
+    stream.synchronize()
+    st, flags = qdec.qdec_check_error(err, stream)
+    assert st == 0, f"device error flags {flags:#x}"
+
+    # ---- device-timed region
+    clocks = Clocks(dev)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            run()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    ck = clocks.stop()
+    t_ms = e0.elapsed_time(e1)
+    t_ms_max = dist.max(t_ms)
+    st, flags = qdec.qdec_check_error(err, stream)
+    assert st == 0, f"device error flags {flags:#x}"
+
+    bytes_layer = w.algorithmic_bytes_per_layer()
+    bytes_step = bytes_layer * L
+    ms_step = t_ms_max / args.steps
+    value = dist.world * bytes_step * args.steps / (t_ms_max * 1e-3) / 1e9
+    launch_us = t_ms / args.steps / L * 1e3           # per launch, this rank
+    achieved = bytes_layer / (launch_us * 1e-6) / 1e9
+    peak, peak_kind = measured_peaks()
+
+    # ---- end to end: pinned host inputs in, outputs out, every step
+    qkv_h = w.qkv.cpu().pin_memory()
+    meta = [w.seq_lens, w.positions, w.block_table]
+    meta_h = [m.cpu().pin_memory() for m in meta]
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step():
+        w.qkv.copy_(qkv_h, non_blocking=True)
+        for d, h in zip(meta, meta_h):
+            d.copy_(h, non_blocking=True)
+        run()
+        out_h.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup // 4)):
+            e2e_step()
+    stream.synchronize()
+    k_e2e = max(1, args.steps // 4)
+    dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    t_e2e = dist.max(e0.elapsed_time(e1))
+    h2d = qkv_h.numel() * qkv_h.element_size() + sum(m.numel() * m.element_size() for m in meta_h)
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_value = dist.world * bytes_step * k_e2e / (t_e2e * 1e-3) / 1e9
+    st, flags = qdec.qdec_check_error(err, stream)
+    assert st == 0, f"device error flags {flags:#x}"
+
+    traffic = None
+    tr = TRAFFIC.get(spec.name)
+    if tr and tr["kernel_sha"] == kernel_sha():
+        traffic = tr["bytes_per_launch"]
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        w_cpu = wl.build(spec, "cpu")
+        gbs, what, n, secs = oracle_sample(w_cpu, args.cpu_seconds, per_seq=False)
+        cpu = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} x {what} of {spec.name}, fp64, {secs:.1f} s"}
+
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 q/k/v and KV pages)",
+            "us_per_layer_step": round(ms_step * 1e3 / L, 4),
+            "pct_of_hbm_peak": round(100 * value / dist.world / peak, 2),
+            "config": {"workload": spec.name, "batch": spec.batch,
+                       "ctx": f"{int(w.seq_lens_host.min())}-{int(w.seq_lens_host.max())}",
+                       "heads": f"{spec.num_q_heads}q/{spec.num_kv_heads}kv",
+                       "head_dim": spec.head_dim, "page_size": spec.page_size, "layers": L,
+                       "pool_pages_per_layer": spec.pool_pages,
+                       "kv_bytes_per_step": bytes_step,
+                       "l2": f"inputs larger than L2: each step reads {bytes_step / 1e9:.3f} GB "
+                             "of KV across 36 per-layer pools" if not spec.shared_pool else
+                             f"{bytes_layer / 1e9:.3f} GB per layer from one shared pool",
+                       "launch": "eager" if args.no_graph else "CUDA graph of 36 qdec_step",
+                       "parallelism": f"replicas x{dist.world}"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_kind == "measured" else "fallback",
+                         "kernel": "attention_kernel<fused>", "launch_us": round(launch_us, 3),
+                         "bytes_per_launch": bytes_layer},
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": k_e2e},
+            "gpu_launches": L * args.steps,
+            "clocks": ck,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, dist)
+        else:
+            run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,349 @@
+// qdec_api.cu -- host side of the libqdec C ABI: argument checks, workspace
+// layout, the TMA descriptor of the KV pool, and kernel launches.  No call
+// here allocates device memory; the only host-side arithmetic is the RoPE
+// frequency table rope_theta^(-2i/D), a per-shape constant passed to the
+// kernels by value.
+#include "qdec_internal.h"
+#include "qdec.h"
+
+#include <math.h>
+#include <mutex>
+
+namespace {
+
+using qdec::Params;
+
+constexpr int kVersion = 10000;  // 1.0.0
+
+// ----------------------------------------------------------- device info --
+int sm_count_of_current_device() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// ------------------------------------------------------------ validation --
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+qdec_status check_shape(const qdec_shape *s) {
+    if (!s) return QDEC_ERR_INVALID_ARG;
+    if (s->batch < 1 || s->num_q_heads < 1 || s->num_kv_heads < 1 || s->head_dim < 1 ||
+        s->page_size < 1 || s->num_pages < 1 || s->max_blocks_per_seq < 1 ||
+        s->max_seq_len < 1 || s->num_ctas < 0)
+        return QDEC_ERR_INVALID_ARG;
+    if (!(s->rope_theta > 0.f) || !(s->eps >= 0.f) || !(s->sm_scale >= 0.f) ||
+        !isfinite(s->rope_theta) || !isfinite(s->eps) || !isfinite(s->sm_scale))
+        return QDEC_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(s->max_seq_len) >
+        static_cast<int64_t>(s->max_blocks_per_seq) * s->page_size)
+        return QDEC_ERR_INVALID_ARG;
+    if (s->head_dim != qdec::kHeadDim || s->page_size != qdec::kPageSize ||
+        s->num_q_heads != qdec::kGroup * s->num_kv_heads || s->batch > qdec::kMaxBatch)
+        return QDEC_ERR_UNSUPPORTED;
+    // TMA row coordinates of the pool are 32-bit
+    if (static_cast<int64_t>(s->num_pages) * 2 * s->num_kv_heads * qdec::kPageSize >= (1ll << 31))
+        return QDEC_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(s->max_blocks_per_seq) * qdec::kPageSize >= (1ll << 31))
+        return QDEC_ERR_UNSUPPORTED;
+    return QDEC_OK;
+}
+
+qdec_status check_row_input(const void *p, int64_t stride, int rows) {
+    if (!p) return QDEC_ERR_INVALID_ARG;
+    if (!aligned16(p) || stride % 8 != 0 || stride < static_cast<int64_t>(rows) * qdec::kHeadDim)
+        return QDEC_ERR_INVALID_ARG;
+    return QDEC_OK;
+}
+
+// ----------------------------------------------------------------- plan --
+// Attention grid: a whole number of CTAs per SM, never more than the page
+// tiles a launch can have.  The kernels re-derive the piece layout from the
+// grid and the device-side seq_lens, so this depends on the shape only.
+int attention_grid(const qdec_shape *s) {
+    if (s->num_ctas > 0) return s->num_ctas;
+    int sms = sm_count_of_current_device();
+    if (sms <= 0) sms = 1;
+    const int64_t max_tiles = static_cast<int64_t>(s->batch) * s->num_kv_heads *
+                              ((s->max_seq_len + qdec::kPageSize - 1) / qdec::kPageSize);
+    const int64_t g = static_cast<int64_t>(sms) * qdec::kCtasPerSm;
+    return static_cast<int>(g < max_tiles ? g : max_tiles);
+}
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WorkspaceLayout {
+    size_t cnt, lse, o, total;
+};
+
+// counters [B*Hkv] int32 | partial lse [pieces][G] f32 | partial o [pieces][G][D] f32
+// with pieces <= grid + B*Hkv (each CTA adds at most one piece per segment it
+// starts in, plus its first).
+WorkspaceLayout workspace_layout(const qdec_shape *s) {
+    const size_t segs = static_cast<size_t>(s->batch) * s->num_kv_heads;
+    const size_t pieces = static_cast<size_t>(attention_grid(s)) + segs;
+    WorkspaceLayout l;
+    l.cnt = 0;
+    l.lse = round256(segs * sizeof(int32_t));
+    l.o = l.lse + round256(pieces * qdec::kGroup * sizeof(float));
+    l.total = l.o + pieces * qdec::kGroup * qdec::kHeadDim * sizeof(float);
+    return l;
+}
+
+// RoPE frequencies rope_theta^(-2i/D) in double, cached per theta.
+void fill_inv_freq(double *dst, float theta) {
+    static std::mutex mu;
+    static float cached_theta = -1.f;
+    static double table[qdec::kRotPairs];
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached_theta != theta) {
+        for (int i = 0; i < qdec::kRotPairs; ++i)
+            table[i] = pow(static_cast<double>(theta), -2.0 * i / qdec::kHeadDim);
+        cached_theta = theta;
+    }
+    for (int i = 0; i < qdec::kRotPairs; ++i) dst[i] = table[i];
+}
+
+void fill_common(Params &p, const qdec_shape *s) {
+    p.B = s->batch;
+    p.Hq = s->num_q_heads;
+    p.Hkv = s->num_kv_heads;
+    p.num_pages = s->num_pages;
+    p.max_blocks = s->max_blocks_per_seq;
+    p.eps = s->eps;
+    const double scale =
+        s->sm_scale > 0.f ? s->sm_scale : 1.0 / sqrt(static_cast<double>(s->head_dim));
+    p.qscale = static_cast<float>(scale * 1.4426950408889634074);  // * log2(e)
+    p.grid = attention_grid(s);
+    fill_inv_freq(p.inv_freq, s->rope_theta);
+}
+
+void bind_workspace(Params &p, const qdec_shape *s, void *ws) {
+    const WorkspaceLayout l = workspace_layout(s);
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    p.ws_cnt = reinterpret_cast<int32_t *>(base + l.cnt);
+    p.ws_lse = reinterpret_cast<float *>(base + l.lse);
+    p.ws_o = reinterpret_cast<float *>(base + l.o);
+}
+
+// ------------------------------------------------------- TMA descriptor --
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// The pool as a 2-D tensor of rows of D bf16 (one row per token slot of one
+// (page, plane, head)); a box is 16 rows x 64 dims (128 B), 128-byte
+// swizzled so the tile math reads shared memory without bank conflicts.
+qdec_status encode_pool_map(CUtensorMap *map, const qdec_shape *s, const void *pool) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return QDEC_ERR_CUDA;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(qdec::kHeadDim),
+                                static_cast<cuuint64_t>(s->num_pages) * 2 * s->num_kv_heads *
+                                    qdec::kPageSize};
+    const cuuint64_t strides[1] = {qdec::kHeadDim * sizeof(uint16_t)};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(qdec::kPageSize)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? QDEC_OK : QDEC_ERR_CUDA;
+}
+
+qdec_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QDEC_OK : QDEC_ERR_CUDA; }
+
+qdec_status check_new_token_args(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_stride,
+                                 const qdec_bf16 *k, int64_t k_stride, const qdec_bf16 *v,
+                                 int64_t v_stride, const qdec_bf16 *q_norm_w,
+                                 const qdec_bf16 *k_norm_w, const int32_t *positions,
+                                 const int32_t *seq_lens, const int32_t *block_table,
+                                 const qdec_bf16 *kv_pool) {
+    qdec_status st = check_shape(shape);
+    if (st != QDEC_OK) return st;
+    if ((st = check_row_input(q, q_stride, shape->num_q_heads)) != QDEC_OK) return st;
+    if ((st = check_row_input(k, k_stride, shape->num_kv_heads)) != QDEC_OK) return st;
+    if ((st = check_row_input(v, v_stride, shape->num_kv_heads)) != QDEC_OK) return st;
+    if (!q_norm_w || !k_norm_w || !positions || !seq_lens || !block_table || !kv_pool)
+        return QDEC_ERR_INVALID_ARG;
+    if (!aligned16(q_norm_w) || !aligned16(k_norm_w) || !aligned16(kv_pool))
+        return QDEC_ERR_INVALID_ARG;
+    return QDEC_OK;
+}
+
+qdec_status check_workspace(const qdec_shape *shape, const void *ws, size_t bytes) {
+    if (!ws || !aligned16(ws)) return QDEC_ERR_WORKSPACE;
+    if (bytes < workspace_layout(shape).total) return QDEC_ERR_WORKSPACE;
+    return QDEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t qdec_workspace_bytes(const qdec_shape *shape) {
+    if (check_shape(shape) != QDEC_OK) return 0;
+    return workspace_layout(shape).total;
+}
+
+qdec_status qdec_workspace_init(const qdec_shape *shape, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    qdec_status st = check_shape(shape);
+    if (st != QDEC_OK) return st;
+    if ((st = check_workspace(shape, workspace, workspace_bytes)) != QDEC_OK) return st;
+    const size_t n = static_cast<size_t>(shape->batch) * shape->num_kv_heads * sizeof(int32_t);
+    return cuda_status(cudaMemsetAsync(workspace, 0, n, static_cast<cudaStream_t>(stream)));
+}
+
+qdec_status qdec_append_rope(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_stride,
+                             const qdec_bf16 *k, int64_t k_stride, const qdec_bf16 *v,
+                             int64_t v_stride, const qdec_bf16 *q_norm_w,
+                             const qdec_bf16 *k_norm_w, const int32_t *positions,
+                             const int32_t *seq_lens, const int32_t *block_table,
+                             qdec_bf16 *kv_pool, float *q_rot, int32_t *err_flag, void *stream) {
+    qdec_status st = check_new_token_args(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w,
+                                          k_norm_w, positions, seq_lens, block_table, kv_pool);
+    if (st != QDEC_OK) return st;
+    if (!q_rot || !aligned16(q_rot)) return QDEC_ERR_INVALID_ARG;
+    Params p{};
+    fill_common(p, shape);
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    p.k = reinterpret_cast<const __nv_bfloat16 *>(k);
+    p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
+    p.q_stride = q_stride;
+    p.k_stride = k_stride;
+    p.v_stride = v_stride;
+    p.w_q = reinterpret_cast<const __nv_bfloat16 *>(q_norm_w);
+    p.w_k = reinterpret_cast<const __nv_bfloat16 *>(k_norm_w);
+    p.positions = positions;
+    p.seq_lens = seq_lens;
+    p.block_table = block_table;
+    p.pool = reinterpret_cast<__nv_bfloat16 *>(kv_pool);
+    p.q_rot_out = q_rot;
+    p.err = err_flag;
+    return cuda_status(qdec::launch_append_rope(p, static_cast<cudaStream_t>(stream)));
+}
+
+qdec_status qdec_attn_split(const qdec_shape *shape, const float *q_rot, const qdec_bf16 *kv_pool,
+                            const int32_t *block_table, const int32_t *seq_lens, void *workspace,
+                            size_t workspace_bytes, qdec_bf16 *out, int32_t *err_flag,
+                            void *stream) {
+    qdec_status st = check_shape(shape);
+    if (st != QDEC_OK) return st;
+    if (!q_rot || !kv_pool || !block_table || !seq_lens || !out) return QDEC_ERR_INVALID_ARG;
+    if (!aligned16(q_rot) || !aligned16(kv_pool) || !aligned16(out)) return QDEC_ERR_INVALID_ARG;
+    if ((st = check_workspace(shape, workspace, workspace_bytes)) != QDEC_OK) return st;
+    Params p{};
+    fill_common(p, shape);
+    p.q_rot_in = q_rot;
+    p.seq_lens = seq_lens;
+    p.block_table = block_table;
+    p.pool = reinterpret_cast<__nv_bfloat16 *>(const_cast<qdec_bf16 *>(kv_pool));
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.err = err_flag;
+    bind_workspace(p, shape, workspace);
+    CUtensorMap map;
+    if ((st = encode_pool_map(&map, shape, kv_pool)) != QDEC_OK) return st;
+    return cuda_status(qdec::launch_attention(p, map, false, static_cast<cudaStream_t>(stream)));
+}
+
+qdec_status qdec_attn_merge(const qdec_shape *shape, const int32_t *seq_lens,
+                            const void *workspace, size_t workspace_bytes, qdec_bf16 *out,
+                            int32_t *err_flag, void *stream) {
+    qdec_status st = check_shape(shape);
+    if (st != QDEC_OK) return st;
+    if (!seq_lens || !out || !aligned16(out)) return QDEC_ERR_INVALID_ARG;
+    if ((st = check_workspace(shape, workspace, workspace_bytes)) != QDEC_OK) return st;
+    Params p{};
+    fill_common(p, shape);
+    p.seq_lens = seq_lens;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.err = err_flag;
+    bind_workspace(p, shape, const_cast<void *>(workspace));
+    return cuda_status(qdec::launch_merge(p, static_cast<cudaStream_t>(stream)));
+}
+
+qdec_status qdec_step(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_stride,
+                      const qdec_bf16 *k, int64_t k_stride, const qdec_bf16 *v, int64_t v_stride,
+                      const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                      const int32_t *positions, const int32_t *seq_lens,
+                      const int32_t *block_table, qdec_bf16 *kv_pool, void *workspace,
+                      size_t workspace_bytes, qdec_bf16 *out, int32_t *err_flag, void *stream) {
+    qdec_status st = check_new_token_args(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w,
+                                          k_norm_w, positions, seq_lens, block_table, kv_pool);
+    if (st != QDEC_OK) return st;
+    if (!out || !aligned16(out)) return QDEC_ERR_INVALID_ARG;
+    if ((st = check_workspace(shape, workspace, workspace_bytes)) != QDEC_OK) return st;
+    Params p{};
+    fill_common(p, shape);
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    p.k = reinterpret_cast<const __nv_bfloat16 *>(k);
+    p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
+    p.q_stride = q_stride;
+    p.k_stride = k_stride;
+    p.v_stride = v_stride;
+    p.w_q = reinterpret_cast<const __nv_bfloat16 *>(q_norm_w);
+    p.w_k = reinterpret_cast<const __nv_bfloat16 *>(k_norm_w);
+    p.positions = positions;
+    p.seq_lens = seq_lens;
+    p.block_table = block_table;
+    p.pool = reinterpret_cast<__nv_bfloat16 *>(kv_pool);
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.err = err_flag;
+    bind_workspace(p, shape, workspace);
+    CUtensorMap map;
+    if ((st = encode_pool_map(&map, shape, kv_pool)) != QDEC_OK) return st;
+    return cuda_status(qdec::launch_attention(p, map, true, static_cast<cudaStream_t>(stream)));
+}
+
+qdec_status qdec_check_error(int32_t *err_flag, void *stream, int32_t *flags_out) {
+    if (!err_flag) return QDEC_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t flags = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return QDEC_ERR_CUDA;
+    if (cudaMemcpyAsync(&flags, err_flag, sizeof flags, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return QDEC_ERR_CUDA;
+    if (cudaMemsetAsync(err_flag, 0, sizeof flags, s) != cudaSuccess) return QDEC_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return QDEC_ERR_CUDA;
+    if (flags_out) *flags_out = flags;
+    if (flags & QDEC_FLAG_TIMEOUT) return QDEC_ERR_TIMEOUT;
+    if (flags & (QDEC_FLAG_BAD_PAGE | QDEC_FLAG_BAD_SEQLEN)) return QDEC_ERR_DEVICE_BOUNDS;
+    return QDEC_OK;
+}
+
+const char *qdec_status_string(qdec_status status) {
+    switch (status) {
+        case QDEC_OK: return "ok";
+        case QDEC_ERR_INVALID_ARG: return "invalid argument";
+        case QDEC_ERR_UNSUPPORTED: return "unsupported shape";
+        case QDEC_ERR_WORKSPACE: return "workspace missing or too small";
+        case QDEC_ERR_CUDA: return "CUDA call failed";
+        case QDEC_ERR_DEVICE_BOUNDS: return "device saw a block-table entry or seq_len out of range";
+        case QDEC_ERR_TIMEOUT: return "a bounded device wait gave up";
+    }
+    return "unknown status";
+}
+
+int32_t qdec_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// qdec_internal.h -- what the host API (qdec_api.cu) and the kernels
+// (qdec_kernels.cu) of libqdec share.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qdec {
+
+// Shapes the kernels are written for.
+constexpr int kHeadDim = 128;       // D
+constexpr int kPageSize = 16;       // P (tokens per page)
+constexpr int kGroup = 4;           // query heads per KV head
+constexpr int kMaxBatch = 1024;     // sequence prefix sums live in shared memory
+constexpr int kRotPairs = kHeadDim / 2;
+
+// Attention kernel geometry.
+constexpr int kConsumerWarps = 4;                          // tile math
+constexpr int kThreads = (kConsumerWarps + 1) * 32;        // + one TMA producer warp
+constexpr int kStages = 8;                                 // ring of page tiles
+constexpr int kTileHalfBytes = kPageSize * 64 * 2;         // 16 rows x 64 dims bf16 = 2 KiB
+constexpr int kPlaneBytes = 2 * kTileHalfBytes;            // one (page, plane, head) = 4 KiB
+constexpr int kTileBytes = 2 * kPlaneBytes;                // K + V = 8 KiB
+constexpr int kCtasPerSm = 2;
+
+// Everything a launch needs, passed by value (__grid_constant__).
+struct Params {
+    int B, Hq, Hkv, num_pages, max_blocks;
+    float eps;
+    float qscale;            // sm_scale * log2(e): scores come out in log2 units
+    const __nv_bfloat16 *q, *k, *v;
+    int64_t q_stride, k_stride, v_stride;   // elements between sequences
+    const __nv_bfloat16 *w_q, *w_k;
+    const int32_t *positions, *seq_lens, *block_table;
+    __nv_bfloat16 *pool;
+    const float *q_rot_in;   // split kernel (unfused): normed + rotated q rows
+    float *q_rot_out;        // append kernel: normed + rotated q rows
+    float *ws_o;             // [pieces][G][D] partial outputs (normalised)
+    float *ws_lse;           // [pieces][G] partial log2-sum-exp
+    int32_t *ws_cnt;         // [B * Hkv] arrival counters (fused merge)
+    __nv_bfloat16 *out;      // [B][Hq][D]
+    int32_t *err;            // device error flag (may be null)
+    int grid;                // attention grid size the piece layout is built for
+    double inv_freq[kRotPairs];  // rope_theta^(-2i/D), i < D/2
+};
+
+size_t attention_smem_bytes();
+
+cudaError_t launch_append_rope(const Params &p, cudaStream_t s);
+cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, bool fused,
+                             cudaStream_t s);
+cudaError_t launch_merge(const Params &p, cudaStream_t s);
+
+}  // namespace qdec

@@ -1,0 +1,211 @@
+"""Python binding of libqdec (ctypes): argument marshalling only.
+
+Every function here has the name of the C entry point it calls, takes torch
+tensors that already live on the current CUDA device, passes their raw
+pointers and the current stream, and raises :class:`QdecError` on a non-OK
+status.  All arithmetic runs in the library's kernels; if the library is
+missing or cannot be loaded, importing this module fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqdec.so")
+
+QDEC_OK = 0
+QDEC_ERR_INVALID_ARG = 1
+QDEC_ERR_UNSUPPORTED = 2
+QDEC_ERR_WORKSPACE = 3
+QDEC_ERR_CUDA = 4
+QDEC_ERR_DEVICE_BOUNDS = 5
+QDEC_ERR_TIMEOUT = 6
+
+QDEC_FLAG_BAD_PAGE = 1
+QDEC_FLAG_BAD_SEQLEN = 2
+QDEC_FLAG_TIMEOUT = 4
+
+# Every symbol include/qdec.h declares.
+EXPORTS = ("qdec_workspace_bytes", "qdec_workspace_init", "qdec_append_rope", "qdec_attn_split",
+           "qdec_attn_merge", "qdec_step", "qdec_check_error", "qdec_status_string",
+           "qdec_version")
+
+
+class QdecShape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
+                ("rope_theta", ctypes.c_float), ("eps", ctypes.c_float),
+                ("sm_scale", ctypes.c_float), ("num_ctas", ctypes.c_int32)]
+
+
+@dataclass
+class Shape:
+    batch: int
+    num_pages: int
+    max_blocks_per_seq: int
+    max_seq_len: int
+    num_q_heads: int = 32
+    num_kv_heads: int = 8
+    head_dim: int = 128
+    page_size: int = 16
+    rope_theta: float = 1.0e6
+    eps: float = 1.0e-6
+    sm_scale: float = 0.0
+    num_ctas: int = 0
+
+    def c(self) -> QdecShape:
+        return QdecShape(self.batch, self.num_q_heads, self.num_kv_heads, self.head_dim,
+                         self.page_size, self.num_pages, self.max_blocks_per_seq,
+                         self.max_seq_len, self.rope_theta, self.eps, self.sm_scale,
+                         self.num_ctas)
+
+
+class QdecError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"libqdec.so not built ({_LIB_PATH}); run gqa_paged_kv_gb300/build.py")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    sp = ctypes.POINTER(QdecShape)
+    st = ctypes.c_int
+    lib.qdec_workspace_bytes.argtypes = [sp]
+    lib.qdec_workspace_bytes.restype = sz
+    lib.qdec_workspace_init.argtypes = [sp, vp, sz, vp]
+    lib.qdec_workspace_init.restype = st
+    lib.qdec_append_rope.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp,
+                                     vp, vp]
+    lib.qdec_append_rope.restype = st
+    lib.qdec_attn_split.argtypes = [sp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+    lib.qdec_attn_split.restype = st
+    lib.qdec_attn_merge.argtypes = [sp, vp, vp, sz, vp, vp, vp]
+    lib.qdec_attn_merge.restype = st
+    lib.qdec_step.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp,
+                              vp, vp]
+    lib.qdec_step.restype = st
+    lib.qdec_check_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.qdec_check_error.restype = st
+    lib.qdec_status_string.argtypes = [st]
+    lib.qdec_status_string.restype = ctypes.c_char_p
+    lib.qdec_version.argtypes = []
+    lib.qdec_version.restype = ctypes.c_int32
+    return lib
+
+
+_lib = _load()
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def status_string(status: int) -> str:
+    return _lib.qdec_status_string(int(status)).decode()
+
+
+def qdec_version() -> int:
+    return int(_lib.qdec_version())
+
+
+def _ptr(t) -> int:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _rows(t: torch.Tensor, what: str) -> int:
+    """Sequence stride (elements) of a [B][H][D] view whose head rows are contiguous."""
+    if t.dtype != torch.bfloat16 or t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError(f"{what}: expected a bf16 [B][H][D] view with contiguous head rows")
+    return t.stride(0)
+
+
+def _raise(status: int, what: str):
+    if status != QDEC_OK:
+        raise QdecError(status, what)
+
+
+def qdec_workspace_bytes(shape: Shape) -> int:
+    return int(_lib.qdec_workspace_bytes(ctypes.byref(shape.c())))
+
+
+def qdec_workspace_init(shape: Shape, workspace: torch.Tensor, stream=None):
+    _raise(_lib.qdec_workspace_init(ctypes.byref(shape.c()), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(),
+                                    _stream(stream)), "qdec_workspace_init")
+
+
+def qdec_append_rope(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, seq_lens,
+                     block_table, kv_pool, q_rot, err_flag=None, stream=None):
+    _raise(_lib.qdec_append_rope(
+        ctypes.byref(shape.c()), _ptr(q), _rows(q, "q"), _ptr(k), _rows(k, "k"), _ptr(v),
+        _rows(v, "v"), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions), _ptr(seq_lens),
+        _ptr(block_table), _ptr(kv_pool), _ptr(q_rot), _ptr(err_flag), _stream(stream)),
+        "qdec_append_rope")
+
+
+def qdec_attn_split(shape: Shape, q_rot, kv_pool, block_table, seq_lens, workspace, out,
+                    err_flag=None, stream=None):
+    _raise(_lib.qdec_attn_split(
+        ctypes.byref(shape.c()), _ptr(q_rot), _ptr(kv_pool), _ptr(block_table), _ptr(seq_lens),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
+        _ptr(err_flag), _stream(stream)), "qdec_attn_split")
+
+
+def qdec_attn_merge(shape: Shape, seq_lens, workspace, out, err_flag=None, stream=None):
+    _raise(_lib.qdec_attn_merge(
+        ctypes.byref(shape.c()), _ptr(seq_lens), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(err_flag),
+        _stream(stream)), "qdec_attn_merge")
+
+
+def qdec_step(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, seq_lens, block_table,
+              kv_pool, workspace, out, err_flag=None, stream=None):
+    _raise(_lib.qdec_step(
+        ctypes.byref(shape.c()), _ptr(q), _rows(q, "q"), _ptr(k), _rows(k, "k"), _ptr(v),
+        _rows(v, "v"), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions), _ptr(seq_lens),
+        _ptr(block_table), _ptr(kv_pool), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(err_flag),
+        _stream(stream)), "qdec_step")
+
+
+def qdec_check_error(err_flag, stream=None):
+    """Synchronise, read and clear the device error flag: (status, flag bits)."""
+    flags = ctypes.c_int32(0)
+    st = _lib.qdec_check_error(_ptr(err_flag), _stream(stream), ctypes.byref(flags))
+    return int(st), int(flags.value)
+
+
+# ------------------------------------------------------------- conveniences --
+
+def shape_for(workload, num_ctas: int = 0) -> Shape:
+    """The Shape of a workloads.Workload (one layer's pool)."""
+    s = workload.spec
+    return Shape(batch=s.batch, num_pages=s.pool_pages,
+                 max_blocks_per_seq=workload.max_blocks,
+                 max_seq_len=int(workload.max_blocks * s.page_size),
+                 num_q_heads=s.num_q_heads, num_kv_heads=s.num_kv_heads,
+                 head_dim=s.head_dim, page_size=s.page_size, num_ctas=num_ctas)
+
+
+def alloc_workspace(shape: Shape, device=None, stream=None) -> torch.Tensor:
+    """A zero-initialised workspace of the size `shape` needs (caller owns it)."""
+    n = qdec_workspace_bytes(shape)
+    if n == 0:
+        raise QdecError(QDEC_ERR_INVALID_ARG, "qdec_workspace_bytes")
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    qdec_workspace_init(shape, ws, stream)
+    return ws

@@ -1,0 +1,116 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C
+ABI, run the oracle on the same seeded inputs, compare element by element.
+
+Tolerances (stated for bf16 outputs of an fp32 pipeline against fp64):
+  out     |gpu - ref| <= 2e-2 + 1e-2 |ref|        (ref: unrounded double)
+  k slot  |gpu - ref| <= 1 bf16 ulp of ref         (ref: unrounded k_rot)
+  v slot  bit-equal to the input v
+  q_rot   |gpu - ref| <= 2e-5 (1 + |ref|)          (fp32 output, unrounded)
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from gqa_paged_kv_gb300 import workloads as wl
+
+OUT_ATOL, OUT_RTOL = 2e-2, 1e-2
+QROT_TOL = 2e-5
+
+
+def qdec():
+    from gqa_paged_kv_gb300 import qdec as q
+    return q
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 numbers at |x| (8 significant bits, min normal 2^-126)."""
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.maximum(ax, 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return oracle.bf16_bits_to_f64(wl.bf16_bits(t))
+
+
+class Runner:
+    """Device buffers for running a workload's layers through qdec_step."""
+
+    def __init__(self, w: wl.Workload, num_ctas: int = 0):
+        q = qdec()
+        self.w = w
+        self.shape = q.shape_for(w, num_ctas=num_ctas)
+        self.ws = q.alloc_workspace(self.shape)
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        s = w.spec
+        self.out = torch.empty((s.layers, s.batch, s.num_q_heads, s.head_dim),
+                               dtype=torch.bfloat16, device="cuda")
+        self.q_rot = torch.empty((s.batch, s.num_q_heads, s.head_dim), dtype=torch.float32,
+                                 device="cuda")
+
+    def step(self, layer: int):
+        q, w = qdec(), self.w
+        q.qdec_step(self.shape, w.q(layer), w.k(layer), w.v(layer), w.w_q[layer], w.w_k[layer],
+                    w.positions, w.seq_lens, w.block_table, w.pool(layer), self.ws,
+                    self.out[layer], self.err)
+
+    def unfused(self, layer: int):
+        q, w = qdec(), self.w
+        q.qdec_append_rope(self.shape, w.q(layer), w.k(layer), w.v(layer), w.w_q[layer],
+                           w.w_k[layer], w.positions, w.seq_lens, w.block_table, w.pool(layer),
+                           self.q_rot, self.err)
+        q.qdec_attn_split(self.shape, self.q_rot, w.pool(layer), w.block_table, w.seq_lens,
+                          self.ws, self.out[layer], self.err)
+        q.qdec_attn_merge(self.shape, w.seq_lens, self.ws, self.out[layer], self.err)
+
+    def check_flags(self):
+        st, flags = qdec().qdec_check_error(self.err)
+        assert st == 0 and flags == 0, f"device error flags {flags:#x} (status {st})"
+
+
+def run_oracle(inputs: dict) -> dict:
+    """One layer on the oracle; `inputs` from workloads.oracle_inputs (pool copied)."""
+    pool = inputs["pool"].copy()
+    res = oracle.decode_layer(inputs["q"], inputs["k"], inputs["v"], inputs["w_q"],
+                              inputs["w_k"], inputs["positions"], inputs["seq_lens"],
+                              inputs["block_table"], pool, inputs["rope_theta"],
+                              float(np.float32(inputs["eps"])))
+    res["pool_after"] = pool
+    return res
+
+
+def assert_out_close(gpu: torch.Tensor, ref: np.ndarray, what: str = "out"):
+    g = to_f64(gpu)
+    assert g.shape == ref.shape, (g.shape, ref.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    err = np.abs(g - ref)
+    bound = OUT_ATOL + OUT_RTOL * np.abs(ref)
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} elements out of tolerance, "
+                           f"max err {err.max():.3e}")
+    return float(err.max())
+
+
+def assert_slots(w: wl.Workload, layer: int, seqs, res: dict):
+    """The appended k rows are within 1 bf16 ulp of the unrounded oracle k_rot
+    and the v rows carry v's bits; returns the count of k elements that are
+    not bit-identical to the oracle's own rounding."""
+    s = w.spec
+    P = s.page_size
+    pool = w.pool(layer)
+    v_in = wl.bf16_bits(w.v(layer))
+    not_exact = 0
+    for i, b in enumerate(seqs):
+        L = int(w.seq_lens_host[b])
+        page = int(w.block_table_host[b, (L - 1) // P])
+        row = wl.bf16_bits(pool[page, :, :, (L - 1) % P, :])       # [2][Hkv][D]
+        k_ref = res["k_rot"][i]
+        k_gpu = oracle.bf16_bits_to_f64(row[0])
+        assert np.all(np.abs(k_gpu - k_ref) <= bf16_ulp(k_ref)), f"k slot seq {b}"
+        not_exact += int(np.sum(row[0] != oracle.f64_to_bf16_bits(k_ref)))
+        assert np.array_equal(row[1], v_in[b]), f"v slot seq {b}"
+    return not_exact

@@ -1,0 +1,169 @@
+"""GPU vs oracle, element by element, through the C ABI (marked gpu).
+
+Small cases span several page tiles, ragged last pages, forced grid sizes
+(one CTA for everything, odd counts, more CTAs than tiles) and both the
+fused single-launch step and the three-call path.  Pools are NaN-poisoned
+wherever the attention must not read.  The five benchmark workloads run at
+full size in the launch configuration the benchmark times; their outputs are
+compared on every sequence of a few layers (sampled sequences for the
+ragged 64-sequence batch).
+"""
+import numpy as np
+import pytest
+import torch
+
+from gqa_paged_kv_gb300 import workloads as wl
+import parity
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    ([1], 0), ([2], 0), ([15, 16, 17], 0), ([31, 33, 1, 100], 0), ([1000], 0),
+    ([17, 1, 300, 64, 16, 2, 999], 0),
+    ([15, 16, 17], 1), ([31, 33, 1, 100], 3), ([1000, 1], 7), ([17, 1, 300, 64], 1000),
+    ([513], 0), ([4096, 3, 777], 5),
+]
+
+
+def _small(lens, seed=11, hq=32, hkv=8, chan=False, spikes=0.0):
+    pages = sum((l + 15) // 16 for l in lens) + 9
+    spec = wl.custom(len(lens), lens, pool_pages=pages, seed=seed, num_q_heads=hq,
+                     num_kv_heads=hkv, chan_scale=chan, spike_frac=spikes)
+    return wl.build(spec, "cuda", poison=True)
+
+
+@pytest.mark.parametrize("lens,num_ctas", SMALL, ids=lambda x: str(x))
+def test_step_small(lens, num_ctas):
+    w = _small(lens)
+    ref = parity.run_oracle(wl.oracle_inputs(w, 0))
+    r = parity.Runner(w, num_ctas=num_ctas)
+    r.step(0)
+    r.check_flags()
+    parity.assert_out_close(r.out[0], ref["out"])
+    parity.assert_slots(w, 0, range(len(lens)), ref)
+
+
+@pytest.mark.parametrize("lens,num_ctas", SMALL[:8], ids=lambda x: str(x))
+def test_unfused_three_calls(lens, num_ctas):
+    w = _small(lens, seed=12)
+    inputs = wl.oracle_inputs(w, 0)
+    ref = parity.run_oracle(inputs)
+    r = parity.Runner(w, num_ctas=num_ctas)
+    r.unfused(0)
+    r.check_flags()
+    q_rot = r.q_rot.double().cpu().numpy()
+    err = np.abs(q_rot - ref["q_rot"])
+    assert np.all(err <= parity.QROT_TOL * (1 + np.abs(ref["q_rot"]))), err.max()
+    parity.assert_out_close(r.out[0], ref["out"])
+    parity.assert_slots(w, 0, range(len(lens)), ref)
+
+
+def test_fused_equals_unfused_closely():
+    w = _small([17, 1, 300, 64, 16, 2, 999], seed=13)
+    r1 = parity.Runner(w)
+    r1.step(0)
+    a = r1.out[0].float().clone()
+    r1.unfused(0)
+    r1.check_flags()
+    b = r1.out[0].float()
+    # both round the same fp32 attention once to bf16; allow one bf16 step
+    assert torch.allclose(a, b, rtol=2 ** -7, atol=1e-3)
+
+
+def test_mqa_group_of_four_single_kv_head():
+    w = _small([15, 16, 17, 200], seed=14, hq=4, hkv=1)
+    ref = parity.run_oracle(wl.oracle_inputs(w, 0))
+    r = parity.Runner(w)
+    r.step(0)
+    r.check_flags()
+    parity.assert_out_close(r.out[0], ref["out"])
+    parity.assert_slots(w, 0, range(4), ref)
+
+
+def test_channel_scales_and_spikes_small():
+    w = _small([300, 1000, 37], seed=15, chan=True, spikes=0.01)
+    ref = parity.run_oracle(wl.oracle_inputs(w, 0))
+    r = parity.Runner(w, num_ctas=5)
+    r.step(0)
+    r.check_flags()
+    parity.assert_out_close(r.out[0], ref["out"])
+
+
+def test_deterministic_bits():
+    w = _small([17, 1, 300, 64, 16, 2, 999], seed=16)
+    r = parity.Runner(w)
+    r.step(0)
+    a = r.out[0].clone()
+    for _ in range(3):
+        r.step(0)
+        assert torch.equal(a, r.out[0])
+
+
+def test_counters_return_to_zero():
+    w = _small([1000, 3, 2000], seed=17)
+    r = parity.Runner(w, num_ctas=9)
+    r.step(0)
+    torch.cuda.synchronize()
+    n = w.spec.batch * w.spec.num_kv_heads
+    assert torch.count_nonzero(r.ws[:4 * n].view(torch.int32)).item() == 0
+
+
+def test_graph_capture_replays_identically():
+    w = _small([17, 1, 300, 64], seed=18)
+    spec = wl.custom(4, [17, 1, 300, 64], pool_pages=40, layers=3, seed=18)
+    w = wl.build(spec, "cuda", poison=True)
+    r = parity.Runner(w)
+    for layer in range(3):
+        r.step(layer)
+    torch.cuda.synchronize()
+    eager = r.out.clone()
+    r.out.zero_()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for layer in range(3):
+                r.step(layer)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(eager, r.out)
+
+
+# ------------------------------------------------------ benchmark workloads --
+
+def _check_layers(w, layers, seqs=None, num_ctas=0):
+    """Run every layer of w in order (as the benchmark does); compare the
+    given layers (pool snapshots taken before any layer ran)."""
+    seqs = list(range(w.spec.batch)) if seqs is None else list(seqs)
+    snaps = {l: wl.oracle_inputs(w, l, seqs) for l in layers}
+    r = parity.Runner(w, num_ctas=num_ctas)
+    for layer in range(w.spec.layers):
+        r.step(layer)
+    r.check_flags()
+    sel = torch.as_tensor(seqs, device="cuda")
+    for l in layers:
+        ref = parity.run_oracle(snaps[l])
+        parity.assert_out_close(r.out[l].index_select(0, sel), ref["out"], f"layer {l}")
+        if w.spec.shared_pool and l != w.spec.layers - 1:
+            continue  # later layers overwrote this layer's slot in the shared pool
+        parity.assert_slots(w, l, seqs, ref)
+
+
+def test_workload_1_full():
+    w = wl.build(wl.WORKLOADS[1], "cuda", poison=True)
+    _check_layers(w, [0])
+
+
+@pytest.mark.parametrize("cid", [2, 3, 4])
+def test_workloads_2_to_4_full(cid):
+    w = wl.build(wl.WORKLOADS[cid], "cuda", poison=True)
+    _check_layers(w, [0, 17, 35])
+
+
+def test_workload_5_sampled():
+    w = wl.build(wl.WORKLOADS[5], "cuda", poison=False)
+    lens = w.seq_lens_host
+    order = np.argsort(lens)
+    seqs = sorted(set([int(order[0]), int(order[1]), int(order[-1]), int(order[-2]),
+                       int(order[len(order) // 2]), 0, 63]))
+    _check_layers(w, [0, 35], seqs)
