@@ -1,11 +1,14 @@
 #!/usr/bin/env python3
 """Decode-attention benchmark: one JSON line on rank 0.
 
-A step is one decode step of the attention block of a 36-layer model: 36
+A step is one decode step of the attention block of a 36-layer model: the
+step's RoPE cos/sin table (one launch, shared by every layer) and 36
 back-to-back layer-steps (qdec_step: QK RMSNorm + NeoX RoPE + paged append +
 split-KV GQA attention with the log-sum-exp merge, one kernel launch each),
-each layer with its own KV pool, all layers sharing the block table.  The 36
-launches are captured once in a CUDA graph and replayed per step.
+each layer with its own KV pool, all layers sharing the block table.  Each
+layer may start streaming its cached pages while the previous layer
+finishes (programmatic dependent launch).  The launches are captured once in
+CUDA graphs and replayed per step.
 
 value   = KV GB/s: algorithmic bytes (KV read at token granularity plus the
           q/k/v inputs and the output) / device time, over all ranks.
@@ -67,6 +70,11 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the 36 calls eagerly")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="launch each layer only after the previous one completed")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: run fewer layers than the workload has")
     return ap.parse_args()
 
 
@@ -254,32 +262,46 @@ def run_ours(args, dist: Dist):
     dev = dist.local
     torch.cuda.set_device(dev)
     spec = wl.WORKLOADS[args.workload]
-    w = wl.build(spec, f"cuda:{dev}")
+    w = wl.build(spec, f"cuda:{dev}", layers=args.layers or None)
+    spec = w.spec
     L = spec.layers
-    shape = qdec.shape_for(w)
+    shape = qdec.shape_for(w, launch_flags=0 if args.no_overlap
+                           else qdec.QDEC_LAUNCH_OVERLAP_PREVIOUS)
     stream = torch.cuda.Stream()
     ws = qdec.alloc_workspace(shape)
+    rope = qdec.alloc_rope_table(shape)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = torch.empty((L, spec.batch, spec.num_q_heads, spec.head_dim), dtype=torch.bfloat16,
                       device="cuda")
     torch.cuda.synchronize()
 
+    def rope_step():
+        qdec.qdec_rope_table(shape, w.positions, rope, stream=stream)
+
     def layers():
         for l in range(L):
             qdec.qdec_step(shape, w.q(l), w.k(l), w.v(l), w.w_q[l], w.w_k[l], w.positions,
-                           w.seq_lens, w.block_table, w.pool(l), ws, out[l], err, stream=stream)
+                           w.seq_lens, w.block_table, w.pool(l), ws, out[l], err, stream=stream,
+                           rope_table=rope)
 
     with torch.cuda.stream(stream):
+        rope_step()
         layers()  # first launch configures the kernels outside capture
     stream.synchronize()
     if args.no_graph:
-        run = layers
+        run_rope, run_layers = rope_step, layers
     else:
-        graph = torch.cuda.CUDAGraph()
+        g_rope, g_layers = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
-            with torch.cuda.graph(graph, stream=stream):
+            with torch.cuda.graph(g_rope, stream=stream):
+                rope_step()
+            with torch.cuda.graph(g_layers, stream=stream):
                 layers()
-        run = graph.replay
+        run_rope, run_layers = g_rope.replay, g_layers.replay
+
+    def run():
+        run_rope()
+        run_layers()
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -292,17 +314,23 @@ def run_ours(args, dist: Dist):
     clocks = Clocks(dev)
     clocks.start()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     dist.barrier()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for _ in range(args.steps):
-            run()
+        for k in range(args.steps):
+            run_rope()
+            mids[k].record(stream)
+            run_layers()
+            ends[k].record(stream)
         e1.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
     ck = clocks.stop()
     t_ms = e0.elapsed_time(e1)
+    t_layers_ms = sum(m.elapsed_time(e) for m, e in zip(mids, ends))
     t_ms_max = dist.max(t_ms)
     st, flags = qdec.qdec_check_error(err, stream)
     assert st == 0, f"device error flags {flags:#x}"
@@ -311,7 +339,7 @@ def run_ours(args, dist: Dist):
     bytes_step = bytes_layer * L
     ms_step = t_ms_max / args.steps
     value = dist.world * bytes_step * args.steps / (t_ms_max * 1e-3) / 1e9
-    launch_us = t_ms / args.steps / L * 1e3           # per launch, this rank
+    launch_us = t_layers_ms / args.steps / L * 1e3    # per attention launch, this rank
     achieved = bytes_layer / (launch_us * 1e-6) / 1e9
     peak, peak_kind = measured_peaks()
 
@@ -328,24 +356,25 @@ def run_ours(args, dist: Dist):
         run()
         out_h.copy_(out, non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup // 4)):
-            e2e_step()
-    stream.synchronize()
-    k_e2e = max(1, args.steps // 4)
-    dist.barrier()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(k_e2e):
-            e2e_step()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    dist.barrier()
-    t_e2e = dist.max(e0.elapsed_time(e1))
+    k_e2e = 0 if args.no_e2e else max(1, args.steps // 4)
+    if k_e2e:
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup // 4)):
+                e2e_step()
+        stream.synchronize()
+        dist.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(k_e2e):
+                e2e_step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        t_e2e = dist.max(e0.elapsed_time(e1))
     h2d = qkv_h.numel() * qkv_h.element_size() + sum(m.numel() * m.element_size() for m in meta_h)
     d2h = out_h.numel() * out_h.element_size()
-    e2e_value = dist.world * bytes_step * k_e2e / (t_e2e * 1e-3) / 1e9
+    e2e_value = dist.world * bytes_step * k_e2e / (t_e2e * 1e-3) / 1e9 if k_e2e else None
     st, flags = qdec.qdec_check_error(err, stream)
     assert st == 0, f"device error flags {flags:#x}"
 
@@ -378,17 +407,22 @@ def run_ours(args, dist: Dist):
                        "l2": f"inputs larger than L2: each step reads {bytes_step / 1e9:.3f} GB "
                              "of KV across 36 per-layer pools" if not spec.shared_pool else
                              f"{bytes_layer / 1e9:.3f} GB per layer from one shared pool",
-                       "launch": "eager" if args.no_graph else "CUDA graph of 36 qdec_step",
+                       "launch": ("eager" if args.no_graph else "CUDA graphs: rope table + "
+                                  "36 qdec_step") + ("" if args.no_overlap else
+                                                     ", programmatic dependent launch"),
                        "parallelism": f"replicas x{dist.world}"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_kind == "measured" else "fallback",
                          "kernel": "attention_kernel<fused>", "launch_us": round(launch_us, 3),
+                         "launch_us_how": "CUDA events around the 36-launch graph each step "
+                                          "(inter-launch gaps included) / 36",
                          "bytes_per_launch": bytes_layer},
-            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": e2e_value and round(e2e_value, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": k_e2e},
-            "gpu_launches": L * args.steps,
+            "gpu_launches": (L + 1) * args.steps,
             "clocks": ck,
             "cpu_baseline": cpu,
         }

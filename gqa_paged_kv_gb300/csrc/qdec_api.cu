@@ -38,6 +38,7 @@ qdec_status check_shape(const qdec_shape *s) {
         s->page_size < 1 || s->num_pages < 1 || s->max_blocks_per_seq < 1 ||
         s->max_seq_len < 1 || s->num_ctas < 0)
         return QDEC_ERR_INVALID_ARG;
+    if ((s->launch_flags & ~QDEC_LAUNCH_OVERLAP_PREVIOUS) != 0) return QDEC_ERR_INVALID_ARG;
     if (!(s->rope_theta > 0.f) || !(s->eps >= 0.f) || !(s->sm_scale >= 0.f) ||
         !isfinite(s->rope_theta) || !isfinite(s->eps) || !isfinite(s->sm_scale))
         return QDEC_ERR_INVALID_ARG;
@@ -62,18 +63,130 @@ qdec_status check_row_input(const void *p, int64_t stride, int rows) {
     return QDEC_OK;
 }
 
+int smem_per_sm_of_current_device() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess)
+            return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 // ----------------------------------------------------------------- plan --
-// Attention grid: a whole number of CTAs per SM, never more than the page
-// tiles a launch can have.  The kernels re-derive the piece layout from the
-// grid and the device-side seq_lens, so this depends on the shape only.
-int attention_grid(const qdec_shape *s) {
-    if (s->num_ctas > 0) return s->num_ctas;
+int64_t max_tiles(const qdec_shape *s) {
+    return static_cast<int64_t>(s->batch) * s->num_kv_heads *
+           ((s->max_seq_len + qdec::kPageSize - 1) / qdec::kPageSize);
+}
+
+// Work layout of the attention kernel (see qdec_kernels.cu): a function of
+// the shape and the device only, never of the lengths in seq_lens.
+struct Plan {
+    int grid;        // CTAs launched
+    int stages;      // ring depth
+    int cluster;     // 0 = flat partition, else CTAs per cluster
+    int chunks;      // cluster layout: chunks (clusters) per segment
+};
+
+// Below this many tiles per CTA the per-CTA stream is too short to hide the
+// global merge, so the cluster layout is used.
+constexpr int64_t kFlatMinTilesPerCta = 32;
+
+// Deepest ring (a multiple of the 4 consumer warps) that still lets two
+// CTAs share an SM.
+int ring_cap(const qdec_shape *s, bool cluster) {
+    int per_sm = smem_per_sm_of_current_device();
+    if (per_sm <= 0) per_sm = 228 * 1024;
+    const int w = qdec::kConsumerWarps;
+    int cap = qdec::kMaxStages / w * w;
+    while (cap > w && static_cast<int64_t>(qdec::kCtasPerSm) *
+                              (qdec::attention_smem_bytes(s->batch, cap, cluster) + 1024) >
+                          static_cast<int64_t>(per_sm))
+        cap -= w;
+    return cap;
+}
+
+// Ring depth: a CTA's whole share of tiles when that is small (so a launch
+// can prefetch everything before its inputs are ready), else the cap; always
+// a multiple of the consumer warp count (see the attention kernel).
+int clamp_stages(int64_t want, int cap) {
+    const int w = qdec::kConsumerWarps;
+    int64_t st = (want + w - 1) / w * w;
+    if (st < w) st = w;
+    return static_cast<int>(st < cap ? st : cap);
+}
+
+// CTAs of cluster size c that fit on the device at once (cached per device).
+int64_t cluster_capacity(const qdec_shape *s, int c, int cap) {
+    static std::mutex mu;
+    static int cache[64][qdec::kMaxCluster + 1];
+    static size_t cache_smem[64][qdec::kMaxCluster + 1];
+    const size_t smem = qdec::attention_smem_bytes(s->batch, cap, true);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = -1;
+    int n = 0;
+    if (dev >= 0) {
+        std::lock_guard<std::mutex> lock(mu);
+        n = cache_smem[dev][c] == smem ? cache[dev][c] : 0;
+        if (n == 0) {
+            n = qdec::max_active_clusters(c, smem);
+            cudaGetLastError();  // a failed query leaves no sticky state behind
+            if (n <= 0) n = -1;
+            cache[dev][c] = n;
+            cache_smem[dev][c] = smem;
+        }
+    }
+    if (n > 0) return static_cast<int64_t>(n) * c;
     int sms = sm_count_of_current_device();
     if (sms <= 0) sms = 1;
-    const int64_t max_tiles = static_cast<int64_t>(s->batch) * s->num_kv_heads *
-                              ((s->max_seq_len + qdec::kPageSize - 1) / qdec::kPageSize);
-    const int64_t g = static_cast<int64_t>(sms) * qdec::kCtasPerSm;
-    return static_cast<int>(g < max_tiles ? g : max_tiles);
+    return static_cast<int64_t>(sms) * qdec::kCtasPerSm / c * c;  // no device: plain estimate
+}
+
+// allow_cluster = false for the three-call path, whose merge kernel reads
+// the flat layout.  num_ctas > 0 forces the flat layout on that grid.
+// Cluster layout: the fewest tiles per CTA T whose grid still fits on the
+// device in one wave (a second wave would double the latency).
+Plan plan_for(const qdec_shape *s, bool allow_cluster) {
+    int sms = sm_count_of_current_device();
+    if (sms <= 0) sms = 1;
+    const int64_t target = static_cast<int64_t>(sms) * qdec::kCtasPerSm;
+    const int64_t wmax = max_tiles(s);
+    Plan pl{};
+    const int64_t per_cta = (wmax + target - 1) / target;
+    const int64_t segs = static_cast<int64_t>(s->batch) * s->num_kv_heads;
+    const int64_t nmax = (s->max_seq_len + qdec::kPageSize - 1) / qdec::kPageSize;
+    if (s->num_ctas == 0 && allow_cluster && per_cta < kFlatMinTilesPerCta) {
+        const int cap = ring_cap(s, true);
+        // T = tiles per CTA; a segment of nmax tiles gets C = ceil(nmax/T) CTAs
+        // (at most a portable cluster) per chunk and K = ceil(nmax/(C*T)) chunks
+        for (int64_t t = per_cta < 1 ? 1 : per_cta; t <= nmax && t < kFlatMinTilesPerCta; ++t) {
+            int64_t c = (nmax + t - 1) / t;
+            if (c > qdec::kMaxCluster) c = qdec::kMaxCluster;
+            const int64_t chunks = (nmax + c * t - 1) / (c * t);
+            const int64_t grid = c * segs * chunks;
+            if (grid <= cluster_capacity(s, static_cast<int>(c), cap)) {
+                pl.cluster = static_cast<int>(c);
+                pl.chunks = static_cast<int>(chunks);
+                pl.grid = static_cast<int>(grid);
+                pl.stages = clamp_stages(t + 1, cap);
+                return pl;
+            }
+        }
+    }
+    const int64_t g = s->num_ctas > 0 ? s->num_ctas : (target < wmax ? target : wmax);
+    pl.grid = static_cast<int>(g);
+    pl.stages = clamp_stages((wmax + g - 1) / g, ring_cap(s, false));
+    return pl;
+}
+
+// Grid bound covering both layouts (sizes the workspace).
+int attention_grid(const qdec_shape *s) {
+    const Plan a = plan_for(s, true), b = plan_for(s, false);
+    return a.grid > b.grid ? a.grid : b.grid;
 }
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -83,8 +196,9 @@ struct WorkspaceLayout {
 };
 
 // counters [B*Hkv] int32 | partial lse [pieces][G] f32 | partial o [pieces][G][D] f32
-// with pieces <= grid + B*Hkv (each CTA adds at most one piece per segment it
-// starts in, plus its first).
+// with pieces <= grid + B*Hkv for either layout (flat: each CTA adds at most
+// one piece per segment it starts in, plus its first; cluster: one per
+// cluster).
 WorkspaceLayout workspace_layout(const qdec_shape *s) {
     const size_t segs = static_cast<size_t>(s->batch) * s->num_kv_heads;
     const size_t pieces = static_cast<size_t>(attention_grid(s)) + segs;
@@ -110,7 +224,7 @@ void fill_inv_freq(double *dst, float theta) {
     for (int i = 0; i < qdec::kRotPairs; ++i) dst[i] = table[i];
 }
 
-void fill_common(Params &p, const qdec_shape *s) {
+void fill_common(Params &p, const qdec_shape *s, bool allow_cluster) {
     p.B = s->batch;
     p.Hq = s->num_q_heads;
     p.Hkv = s->num_kv_heads;
@@ -120,7 +234,12 @@ void fill_common(Params &p, const qdec_shape *s) {
     const double scale =
         s->sm_scale > 0.f ? s->sm_scale : 1.0 / sqrt(static_cast<double>(s->head_dim));
     p.qscale = static_cast<float>(scale * 1.4426950408889634074);  // * log2(e)
-    p.grid = attention_grid(s);
+    const Plan pl = plan_for(s, allow_cluster);
+    p.grid = pl.grid;
+    p.stages = pl.stages;
+    p.cluster = pl.cluster;
+    p.chunks = pl.chunks;
+    p.pdl = (s->launch_flags & QDEC_LAUNCH_OVERLAP_PREVIOUS) != 0;
     fill_inv_freq(p.inv_freq, s->rope_theta);
 }
 
@@ -130,6 +249,8 @@ void bind_workspace(Params &p, const qdec_shape *s, void *ws) {
     p.ws_cnt = reinterpret_cast<int32_t *>(base + l.cnt);
     p.ws_lse = reinterpret_cast<float *>(base + l.lse);
     p.ws_o = reinterpret_cast<float *>(base + l.o);
+    p.ws_pieces = static_cast<long long>((l.total - l.o) /
+                                         (qdec::kGroup * qdec::kHeadDim * sizeof(float)));
 }
 
 // ------------------------------------------------------- TMA descriptor --
@@ -201,6 +322,23 @@ qdec_status check_workspace(const qdec_shape *shape, const void *ws, size_t byte
 
 extern "C" {
 
+size_t qdec_rope_table_bytes(const qdec_shape *shape) {
+    if (check_shape(shape) != QDEC_OK) return 0;
+    return static_cast<size_t>(shape->batch) * qdec::kRotPairs * sizeof(qdec::RopeEntry);
+}
+
+qdec_status qdec_rope_table(const qdec_shape *shape, const int32_t *positions, void *rope_table,
+                            void *stream) {
+    qdec_status st = check_shape(shape);
+    if (st != QDEC_OK) return st;
+    if (!positions || !rope_table || !aligned16(rope_table)) return QDEC_ERR_INVALID_ARG;
+    Params p{};
+    fill_common(p, shape, false);
+    p.positions = positions;
+    p.rope_out = static_cast<qdec::RopeEntry *>(rope_table);
+    return cuda_status(qdec::launch_rope_table(p, static_cast<cudaStream_t>(stream)));
+}
+
 size_t qdec_workspace_bytes(const qdec_shape *shape) {
     if (check_shape(shape) != QDEC_OK) return 0;
     return workspace_layout(shape).total;
@@ -220,13 +358,15 @@ qdec_status qdec_append_rope(const qdec_shape *shape, const qdec_bf16 *q, int64_
                              int64_t v_stride, const qdec_bf16 *q_norm_w,
                              const qdec_bf16 *k_norm_w, const int32_t *positions,
                              const int32_t *seq_lens, const int32_t *block_table,
-                             qdec_bf16 *kv_pool, float *q_rot, int32_t *err_flag, void *stream) {
+                             const void *rope_table, qdec_bf16 *kv_pool, float *q_rot,
+                             int32_t *err_flag, void *stream) {
     qdec_status st = check_new_token_args(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w,
                                           k_norm_w, positions, seq_lens, block_table, kv_pool);
     if (st != QDEC_OK) return st;
+    if (rope_table && !aligned16(rope_table)) return QDEC_ERR_INVALID_ARG;
     if (!q_rot || !aligned16(q_rot)) return QDEC_ERR_INVALID_ARG;
     Params p{};
-    fill_common(p, shape);
+    fill_common(p, shape, false);
     p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
     p.k = reinterpret_cast<const __nv_bfloat16 *>(k);
     p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
@@ -240,6 +380,7 @@ qdec_status qdec_append_rope(const qdec_shape *shape, const qdec_bf16 *q, int64_
     p.block_table = block_table;
     p.pool = reinterpret_cast<__nv_bfloat16 *>(kv_pool);
     p.q_rot_out = q_rot;
+    p.rope = static_cast<const qdec::RopeEntry *>(rope_table);
     p.err = err_flag;
     return cuda_status(qdec::launch_append_rope(p, static_cast<cudaStream_t>(stream)));
 }
@@ -254,13 +395,14 @@ qdec_status qdec_attn_split(const qdec_shape *shape, const float *q_rot, const q
     if (!aligned16(q_rot) || !aligned16(kv_pool) || !aligned16(out)) return QDEC_ERR_INVALID_ARG;
     if ((st = check_workspace(shape, workspace, workspace_bytes)) != QDEC_OK) return st;
     Params p{};
-    fill_common(p, shape);
+    fill_common(p, shape, false);
     p.q_rot_in = q_rot;
     p.seq_lens = seq_lens;
     p.block_table = block_table;
     p.pool = reinterpret_cast<__nv_bfloat16 *>(const_cast<qdec_bf16 *>(kv_pool));
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
     p.err = err_flag;
+    p.pdl = 0;  // reads what qdec_append_rope just wrote: no overlap
     bind_workspace(p, shape, workspace);
     CUtensorMap map;
     if ((st = encode_pool_map(&map, shape, kv_pool)) != QDEC_OK) return st;
@@ -275,7 +417,7 @@ qdec_status qdec_attn_merge(const qdec_shape *shape, const int32_t *seq_lens,
     if (!seq_lens || !out || !aligned16(out)) return QDEC_ERR_INVALID_ARG;
     if ((st = check_workspace(shape, workspace, workspace_bytes)) != QDEC_OK) return st;
     Params p{};
-    fill_common(p, shape);
+    fill_common(p, shape, false);
     p.seq_lens = seq_lens;
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
     p.err = err_flag;
@@ -287,15 +429,17 @@ qdec_status qdec_step(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_str
                       const qdec_bf16 *k, int64_t k_stride, const qdec_bf16 *v, int64_t v_stride,
                       const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
                       const int32_t *positions, const int32_t *seq_lens,
-                      const int32_t *block_table, qdec_bf16 *kv_pool, void *workspace,
-                      size_t workspace_bytes, qdec_bf16 *out, int32_t *err_flag, void *stream) {
+                      const int32_t *block_table, const void *rope_table, qdec_bf16 *kv_pool,
+                      void *workspace, size_t workspace_bytes, qdec_bf16 *out,
+                      int32_t *err_flag, void *stream) {
     qdec_status st = check_new_token_args(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w,
                                           k_norm_w, positions, seq_lens, block_table, kv_pool);
     if (st != QDEC_OK) return st;
+    if (rope_table && !aligned16(rope_table)) return QDEC_ERR_INVALID_ARG;
     if (!out || !aligned16(out)) return QDEC_ERR_INVALID_ARG;
     if ((st = check_workspace(shape, workspace, workspace_bytes)) != QDEC_OK) return st;
     Params p{};
-    fill_common(p, shape);
+    fill_common(p, shape, true);
     p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
     p.k = reinterpret_cast<const __nv_bfloat16 *>(k);
     p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
@@ -309,6 +453,7 @@ qdec_status qdec_step(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_str
     p.block_table = block_table;
     p.pool = reinterpret_cast<__nv_bfloat16 *>(kv_pool);
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.rope = static_cast<const qdec::RopeEntry *>(rope_table);
     p.err = err_flag;
     bind_workspace(p, shape, workspace);
     CUtensorMap map;
@@ -327,7 +472,8 @@ qdec_status qdec_check_error(int32_t *err_flag, void *stream, int32_t *flags_out
     if (cudaStreamSynchronize(s) != cudaSuccess) return QDEC_ERR_CUDA;
     if (flags_out) *flags_out = flags;
     if (flags & QDEC_FLAG_TIMEOUT) return QDEC_ERR_TIMEOUT;
-    if (flags & (QDEC_FLAG_BAD_PAGE | QDEC_FLAG_BAD_SEQLEN)) return QDEC_ERR_DEVICE_BOUNDS;
+    if (flags & (QDEC_FLAG_BAD_PAGE | QDEC_FLAG_BAD_SEQLEN | QDEC_FLAG_BAD_INDEX))
+        return QDEC_ERR_DEVICE_BOUNDS;
     return QDEC_OK;
 }
 

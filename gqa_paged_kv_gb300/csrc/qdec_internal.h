@@ -19,11 +19,18 @@ constexpr int kRotPairs = kHeadDim / 2;
 // Attention kernel geometry.
 constexpr int kConsumerWarps = 4;                          // tile math
 constexpr int kThreads = (kConsumerWarps + 1) * 32;        // + one TMA producer warp
-constexpr int kStages = 8;                                 // ring of page tiles
+constexpr int kMaxStages = 24;                             // ring of page tiles (runtime depth)
 constexpr int kTileHalfBytes = kPageSize * 64 * 2;         // 16 rows x 64 dims bf16 = 2 KiB
 constexpr int kPlaneBytes = 2 * kTileHalfBytes;            // one (page, plane, head) = 4 KiB
 constexpr int kTileBytes = 2 * kPlaneBytes;                // K + V = 8 KiB
 constexpr int kCtasPerSm = 2;
+constexpr int kMaxCluster = 8;                             // portable cluster size
+
+// One RoPE angle of one sequence: cos and sin as unevaluated float pairs
+// (hi + lo), i.e. about 48 significant bits.
+struct RopeEntry {
+    float c_hi, c_lo, s_hi, s_lo;
+};
 
 // Everything a launch needs, passed by value (__grid_constant__).
 struct Params {
@@ -34,6 +41,8 @@ struct Params {
     int64_t q_stride, k_stride, v_stride;   // elements between sequences
     const __nv_bfloat16 *w_q, *w_k;
     const int32_t *positions, *seq_lens, *block_table;
+    const RopeEntry *rope;   // [B][D/2] per-step table, or null: angles computed in-kernel
+    RopeEntry *rope_out;     // rope-table kernel output
     __nv_bfloat16 *pool;
     const float *q_rot_in;   // split kernel (unfused): normed + rotated q rows
     float *q_rot_out;        // append kernel: normed + rotated q rows
@@ -43,11 +52,23 @@ struct Params {
     __nv_bfloat16 *out;      // [B][Hq][D]
     int32_t *err;            // device error flag (may be null)
     int grid;                // attention grid size the piece layout is built for
+    int stages;              // ring depth: a multiple of kConsumerWarps, <= kMaxStages
+    int pdl;                 // launched as a programmatic dependent of the previous kernel
+    int cluster;             // 0: flat tile partition; C > 0: segment chunks on C-CTA clusters
+    int chunks;              // cluster mode: chunks (clusters) per segment
+    long long ws_pieces;     // partial slots the workspace holds (device bounds checks)
     double inv_freq[kRotPairs];  // rope_theta^(-2i/D), i < D/2
 };
 
-size_t attention_smem_bytes();
+// Dynamic shared memory of the attention kernel for batch B, `stages` ring
+// slots and the given layout.
+size_t attention_smem_bytes(int B, int stages, bool cluster);
 
+// Clusters of `cluster` CTAs (each with `smem` bytes of dynamic shared
+// memory) that can be resident at once on the current device (0 if unknown).
+int max_active_clusters(int cluster, size_t smem);
+
+cudaError_t launch_rope_table(const Params &p, cudaStream_t s);
 cudaError_t launch_append_rope(const Params &p, cudaStream_t s);
 cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, bool fused,
                              cudaStream_t s);

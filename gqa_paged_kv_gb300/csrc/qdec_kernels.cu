@@ -1,24 +1,42 @@
 // qdec_kernels.cu -- sm_103a kernels of libqdec.
 //
-// Work layout.  The KV work of one launch is the flat list of page tiles
+// Work layout.  The KV work of one launch is the list of page tiles
 // (sequence b, KV head g, page) in that order; a "segment" is the run of
-// tiles of one (b, g).  CTA j of G takes tiles [j*W/G, (j+1)*W/G) of the W
-// tiles, so every CTA streams the same number of pages whatever the mix of
-// context lengths (the ragged batch needs no host-side planning and the grid
-// never depends on the lengths, so a launch can be captured in a graph).
-// The part of a segment one CTA holds is a "piece": it gets a local softmax
-// state and, when the segment is split over several CTAs, its (o, lse)
-// pair goes to the workspace and is merged with the exact log-sum-exp rule
-// (blog "Qwen3 GPU optimisation", part 8, split-KV: local softmax per CTA,
-// then a reduction).
+// tiles of one (b, g).  The part of a segment one CTA holds is a "piece": it
+// gets a local softmax state, and the pieces of a segment are reduced with
+// the exact log-sum-exp rule (blog "Qwen3 GPU optimisation", part 8,
+// split-KV: local softmax per CTA, then a reduction).  Two layouts, chosen
+// by the host from the shape:
+//   flat    -- CTA j of G takes tiles [j*W/G, (j+1)*W/G) of the W tiles, so
+//              every CTA streams the same number of pages whatever the mix of
+//              context lengths; pieces of a split segment meet in the
+//              workspace and the last CTA to finish merges them.  For large
+//              per-CTA work (long ragged batches), where the merge is cheap
+//              next to the stream.
+//   cluster -- every segment is cut into K equal chunks (K fixed by the
+//              shape), one chunk per cluster of C CTAs, one piece per CTA;
+//              each CTA pushes its piece into rank 0's shared memory
+//              (distributed shared memory) and one cluster barrier later
+//              rank 0 merges them; with K > 1 the chunks then meet in the
+//              workspace.  A CTA needs only its own sequence's length and
+//              block-table row.  For short per-CTA work (small or moderate
+//              batches), where global round trips would dominate.
+// In both, the grid depends on the shape only (the lengths are read on the
+// device), so a launch can be captured in a CUDA graph.
 //
-// Inside a CTA one producer thread streams page tiles (K and V of one page
-// and one KV head, 4 KiB each) from HBM into an 8-deep shared-memory ring
-// with TMA, 128-byte swizzled; four consumer warps take tiles round-robin.
-// Per tile a warp forms S^T = K q^T for the 4 query heads of the group and
+// Inside a CTA one producer warp streams page tiles (K and V of one page and
+// one KV head, 4 KiB each) from HBM into a shared-memory ring with TMA,
+// 128-byte swizzled; four consumer warps take tiles round-robin.  Per tile a
+// warp forms S^T = K q^T for the 4 query heads of the group and
 // O^T += V^T P^T with bf16 mma.sync (fp32 accumulate).  q and P are fed as
 // bf16 hi + lo pairs, so the products carry ~16 mantissa bits while K and V
 // enter exactly; the softmax statistics stay in fp32.
+//
+// The producer reads only data that no kernel of the step writes (seq_lens,
+// the block table, cached pool pages), so when the launch is a programmatic
+// dependent of the previous layer it streams pages while that layer is still
+// finishing; the consumers wait for the previous kernel before they touch q,
+// k, v, the pool slot they append to, the workspace or `out`.
 #include "qdec_internal.h"
 #include "qdec.h"
 
@@ -29,7 +47,7 @@ namespace {
 
 constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;          // log2 units: p <= 2^8 between rescales
-constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;
+constexpr long long kWaitTimeoutCycles = 4000000000ll;  // ~2 s at the 2.07 GHz max clock
 constexpr unsigned kFull = 0xffffffffu;
 
 // Cody-Waite split of 2*pi for the double-precision angle reduction.
@@ -42,27 +60,32 @@ constexpr int kQbStride = kHeadDim + 8;  // bf16 per q-operand row (272 B: no ba
 // prologue buffers (also the whole shared memory of the append kernel)
 constexpr int kOffQb = 0;                                        // bf16 [8][kQbStride]
 constexpr int kOffKvNew = kOffQb + 8 * kQbStride * 2;            // bf16 [2][D]
-constexpr int kOffCs = kOffKvNew + 2 * kHeadDim * 2;             // float2 [D/2]
-constexpr int kOffKcs = kOffCs + kRotPairs * 8;                  // double2 [D/2]
-constexpr int kOffKx = kOffKcs + kRotPairs * 16;                 // double [D]
-constexpr int kOffKss = kOffKx + kHeadDim * 8;                   // double [4]
-constexpr int kPrologueBytes = kOffKss + 4 * 8;
+constexpr int kOffRope = kOffKvNew + 2 * kHeadDim * 2;           // RopeEntry [D/2]
+constexpr int kPrologueBytes = kOffRope + kRotPairs * 16;
 // attention-only buffers
 constexpr int kOffBar = kPrologueBytes;                          // full[S], empty[S]
-constexpr int kOffSlotOk = kOffBar + 2 * kStages * 8;
-constexpr int kOffMisc = kOffSlotOk + kStages * 4;               // abort, last, issued
+constexpr int kOffSlotOk = kOffBar + 2 * kMaxStages * 8;
+constexpr int kOffMisc = kOffSlotOk + kMaxStages * 4;            // abort, last, issued
 constexpr int kOffPbuf = kOffMisc + 8 * 4;                       // bf16 [warps][8][16]
 constexpr int kOffMs = kOffPbuf + kConsumerWarps * 8 * 16 * 2;   // float [warps][G]
 constexpr int kOffLs = kOffMs + kConsumerWarps * kGroup * 4;     // float [warps][G]
 constexpr int kOffOs = kOffLs + kConsumerWarps * kGroup * 4;     // float [warps][G][D]
-constexpr int kOffPre = kOffOs + kConsumerWarps * kGroup * kHeadDim * 4;  // int [B+1]
-constexpr int kOffSl = kOffPre + (kMaxBatch + 1) * 4;                     // int [B]
-constexpr int kOffRing = (kOffSl + kMaxBatch * 4 + 1023) / 1024 * 1024;  // 128B-swizzle atoms
-constexpr int kSmemUsed = kOffRing + kStages * kTileBytes;
-constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base to 1024
-static_assert(kOffKvNew % 16 == 0 && kOffKcs % 16 == 0 && kOffKx % 8 == 0 &&
-              kOffBar % 8 == 0 && kOffOs % 16 == 0 && kOffPbuf % 4 == 0, "smem alignment");
-static_assert(kSmemBytes * kCtasPerSm <= 227 * 1024, "two CTAs per SM must fit");
+constexpr int kPartStride = kHeadDim + 4;                        // num[D], M, den, pad
+// flat layout: int pre[B+1], sl[B] follow os; cluster layout: a receive
+// buffer float [C][G][D+4] for the peers' pieces comes first
+constexpr int kOffRecv = kOffOs + kConsumerWarps * kGroup * kHeadDim * 4;
+constexpr int kRecvBytes = kMaxCluster * kGroup * kPartStride * 4;
+static_assert(kOffKvNew % 16 == 0 && kOffRope % 16 == 0 && kOffBar % 8 == 0 &&
+              kOffOs % 16 == 0 && kOffRecv % 16 == 0 && kOffPbuf % 4 == 0, "smem alignment");
+
+__host__ __device__ constexpr int pre_offset(bool cluster) {
+    return kOffRecv + (cluster ? kRecvBytes : 0);
+}
+// the ring starts at the first 1024-byte boundary after the prefix arrays
+// (128-byte swizzle atoms); +1024 for aligning the dynamic base itself
+__host__ __device__ constexpr int ring_offset(int B, bool cluster) {
+    return (pre_offset(cluster) + 4 * (2 * B + 1) + 1023) / 1024 * 1024;
+}
 
 // ------------------------------------------------------------ PTX helpers --
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -92,20 +115,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-// Wait for a barrier phase; give up after kWaitTimeoutNs or when another
-// thread of the CTA has already given up.  Never spins without bound.
+// Wait for a barrier phase; give up after kWaitTimeoutCycles SM cycles (about
+// two seconds) or when another thread of the CTA has already given up.  Never
+// spins without bound.  The budget is counted with clock64(), which is
+// monotonic on the SM the thread runs on (the global nanosecond timer is
+// not: it can step backwards, which would end a wait at once).
 __device__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer();
+    const long long t0 = clock64();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer() - t0 > kWaitTimeoutNs) return false;
+        if (clock64() - t0 > kWaitTimeoutCycles) return false;
     }
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -141,16 +162,29 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
 __device__ __forceinline__ void consumer_sync() {  // the 128 consumer threads only
     asm volatile("bar.sync 1, 128;" ::: "memory");
 }
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Release/acquire fence at GPU scope (lighter than the sequentially
+// consistent one __threadfence issues).
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
 
 __device__ __forceinline__ void flag_error(int32_t *err, int bits) {
     if (err) atomicOr(err, bits);
 }
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    return v;
+// Defensive bounds check on an index derived inside the kernel: a failure
+// means an internal inconsistency; the access is skipped and flagged.
+__device__ __forceinline__ bool in_bounds(const Params &p, bool ok) {
+    if (!ok) flag_error(p.err, QDEC_FLAG_BAD_INDEX);
+    return ok;
 }
-__device__ __forceinline__ double warp_sum(double v) {
+__device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
     return v;
@@ -158,6 +192,85 @@ __device__ __forceinline__ double warp_sum(double v) {
 __device__ __forceinline__ uint32_t pack_bf16(__nv_bfloat16 lo, __nv_bfloat16 hi) {
     return static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
            (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
+}
+
+// ----------------------------------------------------- float-float math --
+// Unevaluated sums hi + lo of two floats (Dekker 1971; Knuth's TwoSum):
+// ~48 significant bits from fp32 arithmetic, so the appended key can be
+// rounded to bf16 as if from the exact value without fp64 (which GB300
+// executes at a small fraction of its fp32 rate).
+struct ff {
+    float hi, lo;
+};
+__device__ __forceinline__ ff two_sum(float a, float b) {
+    const float s = a + b;
+    const float bb = s - a;
+    return {s, (a - (s - bb)) + (b - bb)};
+}
+__device__ __forceinline__ ff fast_two_sum(float a, float b) {  // |a| >= |b|
+    const float s = a + b;
+    return {s, b - (s - a)};
+}
+__device__ __forceinline__ ff two_prod(float a, float b) {
+    const float p = a * b;
+    return {p, fmaf(a, b, -p)};
+}
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+    ff s = two_sum(a.hi, b.hi);
+    const ff t = two_sum(a.lo, b.lo);
+    s.lo += t.hi;
+    s = fast_two_sum(s.hi, s.lo);
+    s.lo += t.lo;
+    return fast_two_sum(s.hi, s.lo);
+}
+__device__ __forceinline__ ff ff_neg(ff a) { return {-a.hi, -a.lo}; }
+__device__ __forceinline__ ff ff_mul(ff a, ff b) {
+    ff p = two_prod(a.hi, b.hi);
+    p.lo += a.hi * b.lo + a.lo * b.hi;
+    return fast_two_sum(p.hi, p.lo);
+}
+__device__ __forceinline__ ff ff_mul_f(ff a, float b) {
+    ff p = two_prod(a.hi, b);
+    p.lo += a.lo * b;
+    return fast_two_sum(p.hi, p.lo);
+}
+// Round hi + lo to bf16, nearest-even: hi is the float nearest to the exact
+// sum, so the two differ in bf16 only when hi sits exactly on a bf16
+// midpoint, where the sign of lo decides.
+__device__ __forceinline__ __nv_bfloat16 ff_to_bf16(ff y) {
+    const uint32_t u = __float_as_uint(y.hi);
+    if ((u & 0xFFFFu) == 0x8000u && y.lo != 0.0f) {
+        const uint32_t toward_zero = u & 0xFFFF0000u;
+        const bool away = (y.lo > 0.0f) == (y.hi > 0.0f);
+        return __ushort_as_bfloat16(
+            static_cast<unsigned short>((away ? toward_zero + 0x10000u : toward_zero) >> 16));
+    }
+    return __float2bfloat16_rn(y.hi);
+}
+
+// ------------------------------------------------------------ RoPE angles --
+// Angle i of position pos is pos * theta^(-2i/D), formed in double (the
+// frequency comes in as a double).  precise: cos/sin from double sincos,
+// split into float pairs; otherwise the angle is reduced modulo 2 pi in
+// double and sin/cos are taken in fp32 (the lo parts are then zero).
+__device__ RopeEntry rope_entry(int pos, double inv_freq, bool precise) {
+    const double th = static_cast<double>(pos) * inv_freq;
+    RopeEntry e;
+    if (precise) {
+        double sn, cn;
+        sincos(th, &sn, &cn);
+        e.c_hi = static_cast<float>(cn);
+        e.c_lo = static_cast<float>(cn - static_cast<double>(e.c_hi));
+        e.s_hi = static_cast<float>(sn);
+        e.s_lo = static_cast<float>(sn - static_cast<double>(e.s_hi));
+    } else {
+        const double kq = rint(th * kInvTwoPi);
+        double red = fma(-kq, kTwoPiHi, th);
+        red = fma(-kq, kTwoPiLo, red);
+        sincosf(static_cast<float>(red), &e.s_hi, &e.c_hi);
+        e.c_lo = e.s_lo = 0.f;
+    }
+    return e;
 }
 
 // ------------------------------------------------------ sequence metadata --
@@ -204,11 +317,6 @@ __device__ __forceinline__ int cta_of(long long f, long long W, int G) {
     return static_cast<int>(((f + 1) * G - 1) / W);
 }
 
-// Walks the pieces of one CTA's tile range in order.
-struct Walk {
-    int b, g, pg;
-    long long f, hi;
-};
 __device__ int seq_of(const int *pre, int B, int Hkv, long long f) {
     int lo = 0, hi = B - 1;  // largest b with Hkv * pre[b] <= f
     while (lo < hi) {
@@ -220,17 +328,31 @@ __device__ int seq_of(const int *pre, int B, int Hkv, long long f) {
     }
     return lo;
 }
+// (b, g, page index) of flat tile f
+__device__ __forceinline__ void tile_coords(const int *pre, int B, int Hkv, long long f, int &b,
+                                            int &g, int &pg) {
+    b = seq_of(pre, B, Hkv, f);
+    const int n = pre[b + 1] - pre[b];
+    if (n <= 0) {  // cannot happen for f inside the tile range; defensive
+        g = 0;
+        pg = -1;
+        return;
+    }
+    const long long rem = f - static_cast<long long>(Hkv) * pre[b];
+    g = static_cast<int>(rem / n);
+    pg = static_cast<int>(rem % n);
+}
+
+// Walks the pieces of one CTA's tile range in order.
+struct Walk {
+    int b, g, pg;
+    long long f, hi;
+};
 __device__ void walk_start(Walk &w, const int *pre, int B, int Hkv, long long lo, long long hi) {
     w.f = lo;
     w.hi = hi;
     w.b = w.g = w.pg = 0;
-    if (lo >= hi) return;
-    const int b = seq_of(pre, B, Hkv, lo);
-    const int n = pre[b + 1] - pre[b];
-    const long long rem = lo - static_cast<long long>(Hkv) * pre[b];
-    w.b = b;
-    w.g = static_cast<int>(rem / n);
-    w.pg = static_cast<int>(rem % n);
+    if (lo < hi) tile_coords(pre, B, Hkv, lo, w.b, w.g, w.pg);
 }
 __device__ __forceinline__ int piece_len(const Walk &w, const int *pre) {
     const int n = pre[w.b + 1] - pre[w.b];
@@ -250,15 +372,41 @@ __device__ void walk_next(Walk &w, const int *pre, int Hkv, int cnt) {
 }
 
 // ------------------------------------------------------------ row math --
-// The new-token rows of (sequence b, KV head g): the 4 query rows 4g..4g+3
-// and, when need_k, the key row g with the value row g.  Run by the 128
-// consumer threads (warp w owns query row 4g + w; lane l holds dims 2l, 2l+1,
-// 64+2l, 65+2l, i.e. both members of two rotate-half pairs).
-//
-// Query rows: RMSNorm and RoPE in fp32; the angle pos * theta^(-2i/D) is
-// formed and reduced modulo 2 pi in double, then sin/cos are taken in fp32.
-// Key row: RMSNorm and RoPE in double with double sin/cos, so the one bf16
-// rounding on append matches a correctly rounded result of the exact math.
+// The new key row (sequence b, KV head g) on one warp, lane l holding dims
+// 2l, 2l+1, 64+2l, 65+2l: RMSNorm and RoPE in float-float arithmetic, then
+// one rounding to bf16.  x*w is exact in fp32 (two bf16 values), so is x^2.
+__device__ void key_row(const Params &p, __nv_bfloat162 ka, __nv_bfloat162 kc, __nv_bfloat162 wa,
+                        __nv_bfloat162 wc, const RopeEntry &e0, const RopeEntry &e1,
+                        __nv_bfloat16 (&kb)[4]) {
+    const float x[4] = {__low2float(ka), __high2float(ka), __low2float(kc), __high2float(kc)};
+    const float wv[4] = {__low2float(wa), __high2float(wa), __low2float(wc), __high2float(wc)};
+    ff ss = {x[0] * x[0], 0.f};
+#pragma unroll
+    for (int e = 1; e < 4; ++e) ss = ff_add(ss, ff{x[e] * x[e], 0.f});
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+        ss = ff_add(ss, ff{__shfl_xor_sync(kFull, ss.hi, o), __shfl_xor_sync(kFull, ss.lo, o)});
+    const ff v = ff_add(ff{ss.hi * (1.0f / kHeadDim), ss.lo * (1.0f / kHeadDim)}, ff{p.eps, 0.f});
+    // r = 1/sqrt(v): one Newton step from rsqrtf in float-float
+    const float r0 = rsqrtf(v.hi);
+    const ff t = ff_mul(v, two_prod(r0, r0));          // v * r0^2, close to 1
+    const float h = (1.0f - t.hi) - t.lo;              // 1 - t.hi is exact there
+    const ff r = fast_two_sum(r0, 0.5f * r0 * h);
+    ff xh[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) xh[e] = ff_mul_f(r, x[e] * wv[e]);
+    const ff c0 = {e0.c_hi, e0.c_lo}, s0 = {e0.s_hi, e0.s_lo};
+    const ff c1 = {e1.c_hi, e1.c_lo}, s1 = {e1.s_hi, e1.s_lo};
+    kb[0] = ff_to_bf16(ff_add(ff_mul(xh[0], c0), ff_neg(ff_mul(xh[2], s0))));
+    kb[2] = ff_to_bf16(ff_add(ff_mul(xh[2], c0), ff_mul(xh[0], s0)));
+    kb[1] = ff_to_bf16(ff_add(ff_mul(xh[1], c1), ff_neg(ff_mul(xh[3], s1))));
+    kb[3] = ff_to_bf16(ff_add(ff_mul(xh[3], c1), ff_mul(xh[1], s1)));
+}
+
+// The new-token rows of (sequence b, KV head g), on the 128 consumer threads:
+// warp w norms and rotates query row 4g + w in fp32; when need_k, warp 0 also
+// produces the key row (float-float) and appends key and value.  Lane l
+// holds dims 2l, 2l+1, 64+2l, 65+2l: both members of two rotate-half pairs.
 //
 // Q_OUT = 0: scaled bf16 hi/lo operand rows into shared memory (qb);
 // Q_OUT = 1: fp32 rows to p.q_rot_out (unscaled).
@@ -266,108 +414,97 @@ __device__ void walk_next(Walk &w, const int *pre, int Hkv, int cnt) {
 template <int Q_OUT>
 __device__ void new_token_rows(const Params &p, int b, int g, int L, bool need_k, uint8_t *sm) {
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
-    const int pos = p.positions[b];
-    float2 *cs = reinterpret_cast<float2 *>(sm + kOffCs);
-    double2 *kcs = reinterpret_cast<double2 *>(sm + kOffKcs);
-    double *kx = reinterpret_cast<double *>(sm + kOffKx);
-    double *kss = reinterpret_cast<double *>(sm + kOffKss);
-    __nv_bfloat16 *kv_new = reinterpret_cast<__nv_bfloat16 *>(sm + kOffKvNew);
+    // warp 0 fetches the key/value rows and the slot's page up front, so
+    // their latency overlaps the query work
+    if (!in_bounds(p, b >= 0 && b < p.B && g >= 0 && g < p.Hkv && L >= 1 &&
+                          (L - 1) / kPageSize < p.max_blocks))
+        return;  // uniform over the CTA
+    const bool do_k = need_k && w == 0;
+    __nv_bfloat162 ka{}, kc{}, wka{}, wkc{};
+    uint32_t va = 0, vc = 0;
+    int page = -1;
+    if (do_k) {
+        const __nv_bfloat16 *krow = p.k + b * p.k_stride + static_cast<int64_t>(g) * kHeadDim;
+        const __nv_bfloat16 *vrow = p.v + b * p.v_stride + static_cast<int64_t>(g) * kHeadDim;
+        ka = reinterpret_cast<const __nv_bfloat162 *>(krow)[lane];
+        kc = reinterpret_cast<const __nv_bfloat162 *>(krow + 64)[lane];
+        wka = reinterpret_cast<const __nv_bfloat162 *>(p.w_k)[lane];
+        wkc = reinterpret_cast<const __nv_bfloat162 *>(p.w_k + 64)[lane];
+        va = reinterpret_cast<const uint32_t *>(vrow)[lane];
+        vc = reinterpret_cast<const uint32_t *>(vrow + 64)[lane];
+        page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + (L - 1) / kPageSize];
+    }
+    const RopeEntry *rope;
+    if (p.rope) {
+        rope = p.rope + static_cast<int64_t>(b) * kRotPairs;
+    } else {
+        RopeEntry *rs = reinterpret_cast<RopeEntry *>(sm + kOffRope);
+        if (t < kRotPairs) rs[t] = rope_entry(p.positions[b], p.inv_freq[t], need_k);
+        consumer_sync();
+        rope = rs;
+    }
+    const RopeEntry e0 = rope[2 * lane], e1 = rope[2 * lane + 1];
 
-    // Phase A: per-row sums of squares, the rotation angles.
     const int hq = g * kGroup + w;
     const __nv_bfloat16 *qrow = p.q + b * p.q_stride + static_cast<int64_t>(hq) * kHeadDim;
     const __nv_bfloat162 qa = reinterpret_cast<const __nv_bfloat162 *>(qrow)[lane];
-    const __nv_bfloat162 qb2 = reinterpret_cast<const __nv_bfloat162 *>(qrow + 64)[lane];
-    float x[4] = {__low2float(qa), __high2float(qa), __low2float(qb2), __high2float(qb2)};
+    const __nv_bfloat162 qc = reinterpret_cast<const __nv_bfloat162 *>(qrow + 64)[lane];
+    const __nv_bfloat162 wa = reinterpret_cast<const __nv_bfloat162 *>(p.w_q)[lane];
+    const __nv_bfloat162 wc = reinterpret_cast<const __nv_bfloat162 *>(p.w_q + 64)[lane];
+    float x[4] = {__low2float(qa), __high2float(qa), __low2float(qc), __high2float(qc)};
     const float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
     const float r = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
-    {
-        const __nv_bfloat162 wa = reinterpret_cast<const __nv_bfloat162 *>(p.w_q)[lane];
-        const __nv_bfloat162 wb = reinterpret_cast<const __nv_bfloat162 *>(p.w_q + 64)[lane];
-        x[0] = x[0] * r * __low2float(wa);
-        x[1] = x[1] * r * __high2float(wa);
-        x[2] = x[2] * r * __low2float(wb);
-        x[3] = x[3] * r * __high2float(wb);
-    }
-    if (t < kRotPairs) {
-        const double th = static_cast<double>(pos) * p.inv_freq[t];
-        const double kq = rint(th * kInvTwoPi);
-        double red = fma(-kq, kTwoPiHi, th);
-        red = fma(-kq, kTwoPiLo, red);
-        float sn, cn;
-        sincosf(static_cast<float>(red), &sn, &cn);
-        cs[t] = make_float2(cn, sn);
-    }
-    double kxv = 0.0;
-    if (need_k) {
-        if (t >= kRotPairs) {
-            const double th = static_cast<double>(pos) * p.inv_freq[t - kRotPairs];
-            double sn, cn;
-            sincos(th, &sn, &cn);
-            kcs[t - kRotPairs] = make_double2(cn, sn);
-        }
-        const __nv_bfloat16 *krow =
-            p.k + b * p.k_stride + static_cast<int64_t>(g) * kHeadDim;
-        kxv = static_cast<double>(__bfloat162float(krow[t]));
-        const double part = warp_sum(kxv * kxv);
-        if (lane == 0) kss[w] = part;
-    }
-    consumer_sync();
-
-    // Phase B: rotate the query rows; normalise the key row.
-    {
-        const float2 c0 = cs[2 * lane], c1 = cs[2 * lane + 1];
-        const float y0 = x[0] * c0.x - x[2] * c0.y;
-        const float y2 = x[2] * c0.x + x[0] * c0.y;
-        const float y1 = x[1] * c1.x - x[3] * c1.y;
-        const float y3 = x[3] * c1.x + x[1] * c1.y;
-        if (Q_OUT == 0) {
-            __nv_bfloat16 *qb = reinterpret_cast<__nv_bfloat16 *>(sm + kOffQb);
-            const float ys[4] = {y0 * p.qscale, y1 * p.qscale, y2 * p.qscale, y3 * p.qscale};
-            __nv_bfloat16 hi[4], lo[4];
+    x[0] = x[0] * r * __low2float(wa);
+    x[1] = x[1] * r * __high2float(wa);
+    x[2] = x[2] * r * __low2float(wc);
+    x[3] = x[3] * r * __high2float(wc);
+    const float y0 = x[0] * e0.c_hi - x[2] * e0.s_hi;
+    const float y2 = x[2] * e0.c_hi + x[0] * e0.s_hi;
+    const float y1 = x[1] * e1.c_hi - x[3] * e1.s_hi;
+    const float y3 = x[3] * e1.c_hi + x[1] * e1.s_hi;
+    if (Q_OUT == 0) {
+        __nv_bfloat16 *qb = reinterpret_cast<__nv_bfloat16 *>(sm + kOffQb);
+        const float ys[4] = {y0 * p.qscale, y1 * p.qscale, y2 * p.qscale, y3 * p.qscale};
+        __nv_bfloat16 hi[4], lo[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                hi[e] = __float2bfloat16_rn(ys[e]);
-                lo[e] = __float2bfloat16_rn(ys[e] - __bfloat162float(hi[e]));
-            }
-            uint32_t *hrow = reinterpret_cast<uint32_t *>(qb + w * kQbStride);
-            uint32_t *lrow = reinterpret_cast<uint32_t *>(qb + (kGroup + w) * kQbStride);
-            hrow[lane] = pack_bf16(hi[0], hi[1]);
-            hrow[32 + lane] = pack_bf16(hi[2], hi[3]);
-            lrow[lane] = pack_bf16(lo[0], lo[1]);
-            lrow[32 + lane] = pack_bf16(lo[2], lo[3]);
-        } else {
-            float *dst = p.q_rot_out + (static_cast<int64_t>(b) * p.Hq + hq) * kHeadDim;
-            reinterpret_cast<float2 *>(dst)[lane] = make_float2(y0, y1);
-            reinterpret_cast<float2 *>(dst + 64)[lane] = make_float2(y2, y3);
+        for (int e = 0; e < 4; ++e) {
+            hi[e] = __float2bfloat16_rn(ys[e]);
+            lo[e] = __float2bfloat16_rn(ys[e] - __bfloat162float(hi[e]));
         }
+        uint32_t *hrow = reinterpret_cast<uint32_t *>(qb + w * kQbStride);
+        uint32_t *lrow = reinterpret_cast<uint32_t *>(qb + (kGroup + w) * kQbStride);
+        hrow[lane] = pack_bf16(hi[0], hi[1]);
+        hrow[32 + lane] = pack_bf16(hi[2], hi[3]);
+        lrow[lane] = pack_bf16(lo[0], lo[1]);
+        lrow[32 + lane] = pack_bf16(lo[2], lo[3]);
+    } else {
+        float *dst = p.q_rot_out + (static_cast<int64_t>(b) * p.Hq + hq) * kHeadDim;
+        reinterpret_cast<float2 *>(dst)[lane] = make_float2(y0, y1);
+        reinterpret_cast<float2 *>(dst + 64)[lane] = make_float2(y2, y3);
     }
-    if (!need_k) return;
-    {
-        const double tot = kss[0] + kss[1] + kss[2] + kss[3];
-        const double rk = 1.0 / sqrt(tot / kHeadDim + static_cast<double>(p.eps));
-        kx[t] = kxv * rk * static_cast<double>(__bfloat162float(p.w_k[t]));
-    }
-    consumer_sync();
 
-    // Phase C: rotate the key row (double), round once, append k and v.
-    const int i = t & (kRotPairs - 1);
-    const double2 c = kcs[i];
-    const double y = t < kRotPairs ? kx[t] * c.x - kx[t + kRotPairs] * c.y
-                                   : kx[t] * c.x + kx[t - kRotPairs] * c.y;
-    const __nv_bfloat16 kb = __double2bfloat16(y);
-    const __nv_bfloat16 vb = (p.v + b * p.v_stride + static_cast<int64_t>(g) * kHeadDim)[t];
-    kv_new[t] = kb;
-    kv_new[kHeadDim + t] = vb;
+    if (!do_k) return;
+    __nv_bfloat16 kb[4];
+    key_row(p, ka, kc, wka, wkc, e0, e1, kb);
+    const uint32_t k0 = pack_bf16(kb[0], kb[1]), k1 = pack_bf16(kb[2], kb[3]);
+    uint32_t *kv_new = reinterpret_cast<uint32_t *>(sm + kOffKvNew);
+    kv_new[lane] = k0;
+    kv_new[32 + lane] = k1;
+    kv_new[64 + lane] = va;
+    kv_new[96 + lane] = vc;
     const int slot = L - 1;
-    const int page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + slot / kPageSize];
     if (page >= 0 && page < p.num_pages) {
         const int64_t row =
             ((static_cast<int64_t>(page) * 2 * p.Hkv + g) * kPageSize + slot % kPageSize) *
             kHeadDim;
-        p.pool[row + t] = kb;
-        p.pool[row + static_cast<int64_t>(p.Hkv) * kPageSize * kHeadDim + t] = vb;
-    } else if (t == 0) {
+        uint32_t *kdst = reinterpret_cast<uint32_t *>(p.pool + row);
+        uint32_t *vdst =
+            reinterpret_cast<uint32_t *>(p.pool + row + static_cast<int64_t>(p.Hkv) * kPageSize * kHeadDim);
+        kdst[lane] = k0;
+        kdst[32 + lane] = k1;
+        vdst[lane] = va;
+        vdst[32 + lane] = vc;
+    } else if (lane == 0) {
         flag_error(p.err, QDEC_FLAG_BAD_PAGE);
     }
 }
@@ -494,27 +631,50 @@ __device__ void fix_tile(uint8_t *tile, int ntok, bool patch, const __nv_bfloat1
     __syncwarp();
 }
 
-// Log-sum-exp merge of the np pieces of segment sigma (piece ids sigma + j,
-// j = j0 .. j0 + np - 1) into out.  128 threads: head t/32, dims 4(t%32)...
-__device__ void merge_pieces(const Params &p, int sigma, int b, int g, int j0, int np) {
-    const int t = threadIdx.x, h = t >> 5, d0 = (t & 31) * 4;
+// Log-sum-exp merge of the np partials with workspace ids pid0 .. pid0+np-1
+// into out[b][4g..4g+3].  128 threads: warp h merges head h, lane l owns
+// dims 4l..4l+3.  The lse values are fetched one per lane and the partial
+// rows eight at a time, so the L2 round trips overlap.
+__device__ void merge_pieces(const Params &p, int64_t pid0, int b, int g, int np) {
+    const int t = threadIdx.x, h = t >> 5, lane = t & 31, d0 = lane * 4;
+    if (!in_bounds(p, pid0 >= 0 && np >= 1 && pid0 + np <= p.ws_pieces && b >= 0 && b < p.B &&
+                          g >= 0 && g < p.Hkv))
+        return;
     float M = kNegInf;
-    for (int j = 0; j < np; ++j)
-        M = fmaxf(M, __ldcg(p.ws_lse + static_cast<int64_t>(sigma + j0 + j) * kGroup + h));
+    for (int j = lane; j < np; j += 32) M = fmaxf(M, __ldcg(p.ws_lse + (pid0 + j) * kGroup + h));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
     float den = 0.f;
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != kNegInf) {
-        for (int j = 0; j < np; ++j) {
-            const int64_t pid = sigma + j0 + j;
-            const float e = exp2f(__ldcg(p.ws_lse + pid * kGroup + h) - M);
-            const float4 o = __ldcg(
-                reinterpret_cast<const float4 *>(p.ws_o + (pid * kGroup + h) * kHeadDim + d0));
+        for (int base = 0; base < np; base += 32) {
+            const int j = base + lane;
+            const float e = j < np ? exp2f(__ldcg(p.ws_lse + (pid0 + j) * kGroup + h) - M) : 0.f;
             den += e;
-            num.x += e * o.x;
-            num.y += e * o.y;
-            num.z += e * o.z;
-            num.w += e * o.w;
+            const int cnt = min(32, np - base);
+            for (int k0 = 0; k0 < cnt; k0 += 8) {
+                float4 o[8];
+                float ek[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    ek[u] = __shfl_sync(kFull, e, (k0 + u) & 31);
+                    o[u] = k0 + u < cnt
+                               ? __ldcg(reinterpret_cast<const float4 *>(
+                                     p.ws_o + ((pid0 + base + k0 + u) * kGroup + h) * kHeadDim + d0))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float w = k0 + u < cnt ? ek[u] : 0.f;
+                    num.x += w * o[u].x;
+                    num.y += w * o[u].y;
+                    num.z += w * o[u].z;
+                    num.w += w * o[u].w;
+                }
+            }
         }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) den += __shfl_xor_sync(kFull, den, o);
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
     __nv_bfloat16 *dst =
@@ -524,24 +684,237 @@ __device__ void merge_pieces(const Params &p, int sigma, int b, int g, int j0, i
                    pack_bf16(__float2bfloat16_rn(num.z * inv), __float2bfloat16_rn(num.w * inv)));
 }
 
-// ------------------------------------------------------ attention kernel --
+// -------------------------------------------------------- piece processing --
+// The 128 consumer threads process pages [pg0, pg0+cnt) of segment (b, g):
+// prologue (the group's query rows as MMA operands; with has_last also the
+// new key/value), then the tiles, round-robin over the 4 warps by the CTA's
+// running tile counter i (shared with the producer).
 template <bool kFused>
+__device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint32_t full0,
+                              uint32_t empty0, volatile int *slot_ok, volatile int *misc, int b,
+                              int g, int pg0, int cnt, int L, int n, uint32_t &i,
+                              WarpState &st) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tg = lane >> 2, c = lane & 3;
+    const int NS = p.stages;
+    __nv_bfloat16 *qb = reinterpret_cast<__nv_bfloat16 *>(sm + kOffQb);
+    const __nv_bfloat16 *kv_new = reinterpret_cast<const __nv_bfloat16 *>(sm + kOffKvNew);
+    __nv_bfloat16 *pbuf = reinterpret_cast<__nv_bfloat16 *>(sm + kOffPbuf) + warp * 8 * 16;
+    const bool has_last = pg0 + cnt == n;
+
+    if (kFused) {
+        new_token_rows<0>(p, b, g, L, has_last, sm);
+    } else {
+        const float *src =
+            p.q_rot_in + (static_cast<int64_t>(b) * p.Hq + g * kGroup + warp) * kHeadDim;
+        const float2 ya = reinterpret_cast<const float2 *>(src)[lane];
+        const float2 yb = reinterpret_cast<const float2 *>(src + 64)[lane];
+        const float ys[4] = {ya.x * p.qscale, ya.y * p.qscale, yb.x * p.qscale, yb.y * p.qscale};
+        __nv_bfloat16 h4[4], l4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            h4[e] = __float2bfloat16_rn(ys[e]);
+            l4[e] = __float2bfloat16_rn(ys[e] - __bfloat162float(h4[e]));
+        }
+        uint32_t *hrow = reinterpret_cast<uint32_t *>(qb + warp * kQbStride);
+        uint32_t *lrow = reinterpret_cast<uint32_t *>(qb + (kGroup + warp) * kQbStride);
+        hrow[lane] = pack_bf16(h4[0], h4[1]);
+        hrow[32 + lane] = pack_bf16(h4[2], h4[3]);
+        lrow[lane] = pack_bf16(l4[0], l4[1]);
+        lrow[32 + lane] = pack_bf16(l4[2], l4[3]);
+    }
+    consumer_sync();
+    uint32_t qf[8][2];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const __nv_bfloat16 *row = qb + tg * kQbStride + 16 * j + 2 * c;
+        qf[j][0] = *reinterpret_cast<const uint32_t *>(row);
+        qf[j][1] = *reinterpret_cast<const uint32_t *>(row + 8);
+    }
+    for (int k = 0; k < cnt; ++k, ++i) {
+        if (static_cast<int>(i & 3) != warp) continue;
+        const int slot = i % NS;
+        const bool ok = mbar_wait_bounded(full0 + 8 * slot, (i / NS) & 1, misc);
+        if (!ok && lane == 0) {
+            misc[0] = 1;
+            flag_error(p.err, QDEC_FLAG_TIMEOUT);
+        }
+        const int pg = pg0 + k;
+        const int ntok = min(kPageSize, L - pg * kPageSize);
+        if (ok && slot_ok[slot]) {
+            uint8_t *tile = ring + slot * kTileBytes;
+            const bool patch = kFused && pg == n - 1;
+            if (patch || ntok < kPageSize) fix_tile(tile, ntok, patch, kv_new, lane);
+            const uint32_t ks = smem_u32(tile);
+            tile_math(ks, ks + kPlaneBytes, qf, ntok, lane, st, pbuf);
+        }
+        __syncwarp();
+        // a slot whose copy may still be landing is never handed back
+        if (ok && lane == 0) mbar_arrive(empty0 + 8 * slot);
+    }
+}
+
+__device__ __forceinline__ void reset_state(WarpState &st) {
+    st.mA = st.mB = kNegInf;
+    st.lA = st.lB = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) st.o[mt][0] = st.o[mt][1] = st.o[mt][2] = st.o[mt][3] = 0.f;
+}
+
+// The four warps' states of one piece, merged: thread t ends with head
+// t/32's max M (log2 units), sum den and numerator num for dims 4(t%32)..
+struct PieceResult {
+    float M, den;
+    float4 num;
+};
+__device__ PieceResult combine_warps(WarpState &st, uint8_t *sm) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tg = lane >> 2, c = lane & 3;
+    float *ms = reinterpret_cast<float *>(sm + kOffMs);
+    float *ls = reinterpret_cast<float *>(sm + kOffLs);
+    float *os = reinterpret_cast<float *>(sm + kOffOs);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        st.lA += __shfl_xor_sync(kFull, st.lA, o);
+        st.lB += __shfl_xor_sync(kFull, st.lB, o);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st.o[mt][e] += __shfl_xor_sync(kFull, st.o[mt][e], 2);
+    if (c < 2) {
+        const int hA = 2 * c, hB = hA + 1;
+        float *oA = os + (warp * kGroup + hA) * kHeadDim;
+        float *oB = os + (warp * kGroup + hB) * kHeadDim;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            oA[16 * mt + tg] = st.o[mt][0];
+            oB[16 * mt + tg] = st.o[mt][1];
+            oA[16 * mt + tg + 8] = st.o[mt][2];
+            oB[16 * mt + tg + 8] = st.o[mt][3];
+        }
+        if (tg == 0) {
+            ms[warp * kGroup + hA] = st.mA;
+            ms[warp * kGroup + hB] = st.mB;
+            ls[warp * kGroup + hA] = st.lA;
+            ls[warp * kGroup + hB] = st.lB;
+        }
+    }
+    consumer_sync();
+    const int h = tid >> 5, d0 = (tid & 31) * 4;
+    PieceResult r;
+    r.M = kNegInf;
+#pragma unroll
+    for (int q = 0; q < kConsumerWarps; ++q) r.M = fmaxf(r.M, ms[q * kGroup + h]);
+    r.den = 0.f;
+    r.num = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r.M != kNegInf) {
+#pragma unroll
+        for (int q = 0; q < kConsumerWarps; ++q) {
+            const float mq = ms[q * kGroup + h];
+            const float e = mq == kNegInf ? 0.f : exp2f(mq - r.M);
+            const float4 o4 =
+                *reinterpret_cast<const float4 *>(os + (q * kGroup + h) * kHeadDim + d0);
+            r.den += e * ls[q * kGroup + h];
+            r.num.x += e * o4.x;
+            r.num.y += e * o4.y;
+            r.num.z += e * o4.z;
+            r.num.w += e * o4.w;
+        }
+    }
+    return r;
+}
+
+__device__ __forceinline__ void store_out(const Params &p, int b, int g, const PieceResult &r) {
+    const int tid = threadIdx.x, h = tid >> 5, d0 = (tid & 31) * 4;
+    const float inv = r.den > 0.f ? 1.f / r.den : 0.f;
+    if (!in_bounds(p, b >= 0 && b < p.B && g >= 0 && g < p.Hkv)) return;
+    __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(b) * p.Hq + g * kGroup + h) * kHeadDim + d0;
+    reinterpret_cast<uint2 *>(dst)[0] = make_uint2(
+        pack_bf16(__float2bfloat16_rn(r.num.x * inv), __float2bfloat16_rn(r.num.y * inv)),
+        pack_bf16(__float2bfloat16_rn(r.num.z * inv), __float2bfloat16_rn(r.num.w * inv)));
+}
+
+// Write this piece's (o, lse) as workspace partial `pid`; in the fused
+// kernel count it against segment sigma's np partials, and if it is the
+// last to arrive merge all of them (ids pid0 .. pid0+np-1) into out.
+template <bool kFused>
+__device__ void store_partial(const Params &p, volatile int *misc, int64_t pid, int sigma,
+                              int64_t pid0, int np, int b, int g, const PieceResult &r) {
+    const int tid = threadIdx.x, h = tid >> 5, d0 = (tid & 31) * 4;
+    const float inv = r.den > 0.f ? 1.f / r.den : 0.f;
+    if (!in_bounds(p, pid >= 0 && pid < p.ws_pieces && sigma >= 0 && sigma < p.B * p.Hkv))
+        return;  // uniform over the CTA
+    *reinterpret_cast<float4 *>(p.ws_o + (pid * kGroup + h) * kHeadDim + d0) =
+        make_float4(r.num.x * inv, r.num.y * inv, r.num.z * inv, r.num.w * inv);
+    if ((tid & 31) == 0) p.ws_lse[pid * kGroup + h] = r.den > 0.f ? r.M + log2f(r.den) : kNegInf;
+    if (!kFused) return;
+    // release the partial (all 128 threads' stores, ordered by the barrier),
+    // count it; the last piece in acquires all of them
+    consumer_sync();
+    if (tid == 0) {
+        fence_acq_rel_gpu();
+        const int prev = atomicAdd(p.ws_cnt + sigma, 1);
+        fence_acq_rel_gpu();
+        misc[1] = prev == np - 1;
+    }
+    consumer_sync();
+    if (misc[1]) {
+        merge_pieces(p, pid0, b, g, np);
+        if (tid == 0) p.ws_cnt[sigma] = 0;  // ready for the next launch
+    }
+}
+
+// Split cluster barrier: every thread of every CTA of the cluster arrives,
+// then waits for all arrivals.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Generic address of the same shared-memory location in CTA `rank` of this
+// cluster (distributed shared memory).
+__device__ __forceinline__ float *cluster_peer(float *ptr, int rank) {
+    uint64_t r;
+    asm volatile("mapa.u64 %0, %1, %2;"
+                 : "=l"(r)
+                 : "l"(reinterpret_cast<uint64_t>(ptr)), "r"(rank));
+    return reinterpret_cast<float *>(r);
+}
+
+// ------------------------------------------------------ attention kernel --
+template <bool kFused, bool kCluster>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     attention_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *ring = sm + kOffRing;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (p.pdl && tid == 0) launch_dependents();
+
+    uint8_t *ring = sm + ring_offset(p.B, kCluster);
     const uint32_t full0 = smem_u32(sm + kOffBar);
-    const uint32_t empty0 = full0 + kStages * 8;
+    const uint32_t empty0 = full0 + kMaxStages * 8;
     volatile int *slot_ok = reinterpret_cast<volatile int *>(sm + kOffSlotOk);
     volatile int *misc = reinterpret_cast<volatile int *>(sm + kOffMisc);  // 0 abort, 1 last, 2 issued
-    int *pre = reinterpret_cast<int *>(sm + kOffPre);
-    int *sl = reinterpret_cast<int *>(sm + kOffSl);
+    int *pre = reinterpret_cast<int *>(sm + pre_offset(kCluster));
+    int *sl = pre + p.B + 1;
+    const int NS = p.stages;
+    // Ring slot s is always consumed by warp s % 4 only when NS is a multiple
+    // of the consumer warp count; then each warp waits on its slots' phases in
+    // order.  Otherwise two warps could wait on consecutive phases of one slot
+    // and the parity wait of the later one would pass on the earlier phase.
+    if (NS < kConsumerWarps || NS % kConsumerWarps != 0 || NS > kMaxStages) {
+        if (tid == 0) flag_error(p.err, QDEC_FLAG_BAD_INDEX);
+        return;  // uniform: no barrier has been touched yet
+    }
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
@@ -550,41 +923,86 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         misc[2] = 0;
         fence_mbar_init();
     }
-    if (warp == 0) build_prefix(p, pre, sl, blockIdx.x == 0);
-    __syncthreads();
 
-    const long long W = static_cast<long long>(p.Hkv) * pre[p.B];
-    if (W == 0) return;
-    const int G = static_cast<int>(min(static_cast<long long>(p.grid), W));
-    if (static_cast<int>(blockIdx.x) >= G) return;  // the whole CTA leaves together
-    const long long lo = static_cast<long long>(blockIdx.x) * W / G;
-    const long long hi = static_cast<long long>(blockIdx.x + 1) * W / G;
+    // ---- this CTA's tiles: pages [pg_lo, pg_hi) of segment (cb, cg) in the
+    // cluster layout; the flat range [lo, hi) of the (b, g, page) order in
+    // the flat layout
+    long long W = 0, lo = 0, hi = 0;
+    int G = 1;
+    int cb = 0, cg = 0, cn = 0, cL = 0, crank = 0, pg_lo = 0, pg_hi = 0;
+    long long cid = 0;
+    if (kCluster) {
+        const int C = p.cluster, K = p.chunks;
+        cid = blockIdx.x / C;
+        crank = static_cast<int>(blockIdx.x % C);
+        const int sigma = static_cast<int>(cid / K), ck = static_cast<int>(cid % K);
+        cb = sigma / p.Hkv;
+        cg = sigma % p.Hkv;
+        cL = p.seq_lens[cb];
+        if (cL < 1 || cL > p.max_blocks * kPageSize) {
+            if (tid == 0 && crank == 0 && ck == 0 && cg == 0) flag_error(p.err, QDEC_FLAG_BAD_SEQLEN);
+            cL = 0;
+        }
+        cn = (cL + kPageSize - 1) / kPageSize;
+        const int c0 = static_cast<int>(static_cast<long long>(ck) * cn / K);
+        const int c1 = static_cast<int>(static_cast<long long>(ck + 1) * cn / K);
+        pg_lo = c0 + crank * (c1 - c0) / C;
+        pg_hi = c0 + (crank + 1) * (c1 - c0) / C;
+        __syncthreads();  // barrier initialisation
+        // first cluster phase: every CTA has started (its shared memory may be
+        // written by peers once this phase completes); waited for before the
+        // push below, by which time it has long completed
+        cluster_arrive_relaxed();
+    } else {
+        if (warp == kConsumerWarps) build_prefix(p, pre, sl, blockIdx.x == 0);
+        __syncthreads();
+        W = static_cast<long long>(p.Hkv) * pre[p.B];
+        if (W == 0) return;
+        G = static_cast<int>(min(static_cast<long long>(p.grid), W));
+        if (static_cast<int>(blockIdx.x) >= G) return;  // the whole CTA leaves together
+        lo = static_cast<long long>(blockIdx.x) * W / G;
+        hi = static_cast<long long>(blockIdx.x + 1) * W / G;
+    }
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------ TMA producer --
-        if (lane == 0) {
-            Walk w;
-            walk_start(w, pre, p.B, p.Hkv, lo, hi);
-            uint32_t i = 0;
-            bool stop = false;
-            while (!stop && w.f < w.hi) {
-                const int cnt = piece_len(w, pre);
-                const int32_t *bt = p.block_table + static_cast<int64_t>(w.b) * p.max_blocks;
-                for (int k = 0; k < cnt; ++k, ++i) {
-                    const int slot = i % kStages;
+        // 32 tiles at a time: every lane looks up one tile's page, lane 0
+        // issues the copies in order as ring slots come free.
+        const long long ntiles = kCluster ? pg_hi - pg_lo : hi - lo;
+        uint32_t i = 0;
+        bool stop = false;
+        for (long long base = 0; base < ntiles && !stop; base += 32) {
+            int page = -1, g = cg;
+            if (base + lane < ntiles) {
+                int b, pg;
+                if (kCluster) {
+                    b = cb;
+                    pg = pg_lo + static_cast<int>(base) + lane;
+                } else {
+                    tile_coords(pre, p.B, p.Hkv, lo + base + lane, b, g, pg);
+                }
+                if (in_bounds(p, b >= 0 && b < p.B && pg >= 0 && pg < p.max_blocks && g >= 0 &&
+                                     g < p.Hkv))
+                    page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg];
+            }
+            const int cnt = static_cast<int>(min(32ll, ntiles - base));
+            for (int j = 0; j < cnt; ++j, ++i) {
+                const int pj = __shfl_sync(kFull, page, j);
+                const int gj = __shfl_sync(kFull, g, j);
+                if (lane == 0) {
+                    const int slot = i % NS;
                     const uint32_t full = full0 + 8 * slot;
-                    if (i >= kStages &&
-                        !mbar_wait_bounded(empty0 + 8 * slot, ((i / kStages) - 1) & 1, misc)) {
+                    if (misc[0]) {
+                        stop = true;  // another thread gave up: issue nothing more
+                    } else if (i >= static_cast<uint32_t>(NS) &&
+                        !mbar_wait_bounded(empty0 + 8 * slot, ((i / NS) - 1) & 1, misc)) {
                         misc[0] = 1;
                         flag_error(p.err, QDEC_FLAG_TIMEOUT);
                         stop = true;
-                        break;
-                    }
-                    const int page = bt[w.pg + k];
-                    if (page >= 0 && page < p.num_pages) {
+                    } else if (pj >= 0 && pj < p.num_pages && gj >= 0 && gj < p.Hkv) {
                         slot_ok[slot] = 1;
                         mbar_arrive_expect_tx(full, kTileBytes);
-                        const int yk = (page * 2 * p.Hkv + w.g) * kPageSize;
+                        const int yk = (pj * 2 * p.Hkv + gj) * kPageSize;
                         const int yv = yk + p.Hkv * kPageSize;
                         const uint32_t dst = smem_u32(ring + slot * kTileBytes);
                         tma_load_2d(dst, &kv_map, 0, yk, full);
@@ -597,175 +1015,91 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         mbar_arrive(full);
                     }
                 }
-                if (!stop) walk_next(w, pre, p.Hkv, cnt);
+                stop = __shfl_sync(kFull, stop, 0);
+                if (stop) break;
             }
-            misc[2] = static_cast<int>(i);
         }
-    } else {
-        // ---------------------------------------------- consumer warps --
-        __nv_bfloat16 *qb = reinterpret_cast<__nv_bfloat16 *>(sm + kOffQb);
-        const __nv_bfloat16 *kv_new = reinterpret_cast<const __nv_bfloat16 *>(sm + kOffKvNew);
-        __nv_bfloat16 *pbuf = reinterpret_cast<__nv_bfloat16 *>(sm + kOffPbuf) + warp * 8 * 16;
-        float *ms = reinterpret_cast<float *>(sm + kOffMs);
-        float *ls = reinterpret_cast<float *>(sm + kOffLs);
-        float *os = reinterpret_cast<float *>(sm + kOffOs);
-        const int tg = lane >> 2, c = lane & 3;
-
+        if (lane == 0) misc[2] = static_cast<int>(i);
+        if (kCluster) {  // the producer warp takes part in both cluster phases
+            cluster_wait();
+            cluster_sync_all();
+        }
+    } else if (!kCluster) {
+        // -------------------------------------- consumer warps, flat layout --
+        if (p.pdl) grid_dependency_wait();  // q/k/v, pool slot, workspace, out
         Walk w;
         walk_start(w, pre, p.B, p.Hkv, lo, hi);
         uint32_t i = 0;
         while (w.f < w.hi) {
             const int cnt = piece_len(w, pre);
-            const int b = w.b, g = w.g, pg0 = w.pg;
-            const int L = sl[b];
+            const int b = w.b, g = w.g;
             const int n = pre[b + 1] - pre[b];
-            const bool has_last = pg0 + cnt == n;
-
-            // prologue: the group's 4 query rows as bf16 hi/lo MMA operands
-            if (kFused) {
-                new_token_rows<0>(p, b, g, L, has_last, sm);
-            } else {
-                const float *src =
-                    p.q_rot_in + (static_cast<int64_t>(b) * p.Hq + g * kGroup + warp) * kHeadDim;
-                const float2 ya = reinterpret_cast<const float2 *>(src)[lane];
-                const float2 yb = reinterpret_cast<const float2 *>(src + 64)[lane];
-                const float ys[4] = {ya.x * p.qscale, ya.y * p.qscale, yb.x * p.qscale,
-                                     yb.y * p.qscale};
-                __nv_bfloat16 h4[4], l4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    h4[e] = __float2bfloat16_rn(ys[e]);
-                    l4[e] = __float2bfloat16_rn(ys[e] - __bfloat162float(h4[e]));
-                }
-                uint32_t *hrow = reinterpret_cast<uint32_t *>(qb + warp * kQbStride);
-                uint32_t *lrow = reinterpret_cast<uint32_t *>(qb + (kGroup + warp) * kQbStride);
-                hrow[lane] = pack_bf16(h4[0], h4[1]);
-                hrow[32 + lane] = pack_bf16(h4[2], h4[3]);
-                lrow[lane] = pack_bf16(l4[0], l4[1]);
-                lrow[32 + lane] = pack_bf16(l4[2], l4[3]);
-            }
-            consumer_sync();
-            uint32_t qf[8][2];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const __nv_bfloat16 *row = qb + tg * kQbStride + 16 * j + 2 * c;
-                qf[j][0] = *reinterpret_cast<const uint32_t *>(row);
-                qf[j][1] = *reinterpret_cast<const uint32_t *>(row + 8);
-            }
-
             WarpState st;
-            st.mA = st.mB = kNegInf;
-            st.lA = st.lB = 0.f;
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt)
-                st.o[mt][0] = st.o[mt][1] = st.o[mt][2] = st.o[mt][3] = 0.f;
-
-            for (int k = 0; k < cnt; ++k, ++i) {
-                if (static_cast<int>(i & 3) != warp) continue;
-                const int slot = i % kStages;
-                const bool ok = mbar_wait_bounded(full0 + 8 * slot, (i / kStages) & 1, misc);
-                if (!ok && lane == 0) {
-                    misc[0] = 1;
-                    flag_error(p.err, QDEC_FLAG_TIMEOUT);
-                }
-                const int pg = pg0 + k;
-                const int ntok = min(kPageSize, L - pg * kPageSize);
-                if (ok && slot_ok[slot]) {
-                    uint8_t *tile = ring + slot * kTileBytes;
-                    const bool patch = kFused && pg == n - 1;
-                    if (patch || ntok < kPageSize) fix_tile(tile, ntok, patch, kv_new, lane);
-                    const uint32_t ks = smem_u32(tile);
-                    tile_math(ks, ks + kPlaneBytes, qf, ntok, lane, st, pbuf);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-            }
-
-            // epilogue: combine hi/lo columns, then the four warps' states
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                st.lA += __shfl_xor_sync(kFull, st.lA, o);
-                st.lB += __shfl_xor_sync(kFull, st.lB, o);
-            }
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) st.o[mt][e] += __shfl_xor_sync(kFull, st.o[mt][e], 2);
-            if (c < 2) {
-                const int hA = 2 * c, hB = hA + 1;
-                float *oA = os + (warp * kGroup + hA) * kHeadDim;
-                float *oB = os + (warp * kGroup + hB) * kHeadDim;
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    oA[16 * mt + tg] = st.o[mt][0];
-                    oB[16 * mt + tg] = st.o[mt][1];
-                    oA[16 * mt + tg + 8] = st.o[mt][2];
-                    oB[16 * mt + tg + 8] = st.o[mt][3];
-                }
-                if (tg == 0) {
-                    ms[warp * kGroup + hA] = st.mA;
-                    ms[warp * kGroup + hB] = st.mB;
-                    ls[warp * kGroup + hA] = st.lA;
-                    ls[warp * kGroup + hB] = st.lB;
-                }
-            }
-            consumer_sync();
-            {
-                const int h = tid >> 5, d0 = (tid & 31) * 4;
-                float M = kNegInf;
-#pragma unroll
-                for (int q = 0; q < kConsumerWarps; ++q) M = fmaxf(M, ms[q * kGroup + h]);
-                float den = 0.f;
-                float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (M != kNegInf) {
-#pragma unroll
-                    for (int q = 0; q < kConsumerWarps; ++q) {
-                        const float mq = ms[q * kGroup + h];
-                        const float e = mq == kNegInf ? 0.f : exp2f(mq - M);
-                        const float4 o4 =
-                            *reinterpret_cast<const float4 *>(os + (q * kGroup + h) * kHeadDim + d0);
-                        den += e * ls[q * kGroup + h];
-                        num.x += e * o4.x;
-                        num.y += e * o4.y;
-                        num.z += e * o4.z;
-                        num.w += e * o4.w;
-                    }
-                }
-                const float inv = den > 0.f ? 1.f / den : 0.f;
-                const long long seg0 = static_cast<long long>(p.Hkv) * pre[b] +
-                                       static_cast<long long>(g) * n;
-                const int j0 = cta_of(seg0, W, G);
-                const int np = cta_of(seg0 + n - 1, W, G) - j0 + 1;
-                const int sigma = b * p.Hkv + g;
-                if (np == 1) {
-                    __nv_bfloat16 *dst =
-                        p.out + (static_cast<int64_t>(b) * p.Hq + g * kGroup + h) * kHeadDim + d0;
-                    reinterpret_cast<uint2 *>(dst)[0] = make_uint2(
-                        pack_bf16(__float2bfloat16_rn(num.x * inv), __float2bfloat16_rn(num.y * inv)),
-                        pack_bf16(__float2bfloat16_rn(num.z * inv), __float2bfloat16_rn(num.w * inv)));
-                } else {
-                    const int64_t pid = sigma + static_cast<int64_t>(blockIdx.x);
-                    *reinterpret_cast<float4 *>(p.ws_o + (pid * kGroup + h) * kHeadDim + d0) =
-                        make_float4(num.x * inv, num.y * inv, num.z * inv, num.w * inv);
-                    if ((tid & 31) == 0)
-                        p.ws_lse[pid * kGroup + h] = den > 0.f ? M + log2f(den) : kNegInf;
-                    if (kFused) {
-                        __threadfence();
-                        consumer_sync();
-                        if (tid == 0) {
-                            const int prev = atomicAdd(p.ws_cnt + sigma, 1);
-                            misc[1] = prev == np - 1;
-                        }
-                        consumer_sync();
-                        if (misc[1]) {
-                            __threadfence();
-                            merge_pieces(p, sigma, b, g, j0, np);
-                            if (tid == 0) p.ws_cnt[sigma] = 0;  // ready for the next launch
-                        }
-                    }
-                }
-            }
+            reset_state(st);
+            process_piece<kFused>(p, sm, ring, full0, empty0, slot_ok, misc, b, g, w.pg, cnt, sl[b],
+                                  n, i, st);
+            const PieceResult r = combine_warps(st, sm);
+            const long long seg0 = static_cast<long long>(p.Hkv) * pre[b] + static_cast<long long>(g) * n;
+            const int j0 = cta_of(seg0, W, G);
+            const int np = cta_of(seg0 + n - 1, W, G) - j0 + 1;
+            const int sigma = b * p.Hkv + g;
+            if (np == 1)
+                store_out(p, b, g, r);
+            else
+                store_partial<kFused>(p, misc, sigma + static_cast<int64_t>(blockIdx.x), sigma,
+                                      sigma + static_cast<int64_t>(j0), np, b, g, r);
+            consumer_sync();  // the shared scratch is reused by the next piece
             walk_next(w, pre, p.Hkv, cnt);
+        }
+    } else {
+        // ----------------------------------- consumer warps, cluster layout --
+        if (p.pdl) grid_dependency_wait();
+        const int C = p.cluster, K = p.chunks;
+        const int cnt = pg_hi - pg_lo;
+        WarpState st;
+        reset_state(st);
+        uint32_t i = 0;
+        if (cnt > 0)
+            process_piece<kFused>(p, sm, ring, full0, empty0, slot_ok, misc, cb, cg, pg_lo, cnt, cL,
+                                  cn, i, st);
+        PieceResult r = combine_warps(st, sm);
+        // push this CTA's piece into slot `crank` of rank 0's receive buffer
+        cluster_wait();
+        const int h = tid >> 5, d0 = (tid & 31) * 4;
+        float *recv = reinterpret_cast<float *>(sm + kOffRecv);
+        float *dst = cluster_peer(recv, 0) + (crank * kGroup + h) * kPartStride;
+        *reinterpret_cast<float4 *>(dst + d0) = r.num;
+        if ((tid & 31) == 0) {
+            dst[kHeadDim] = r.M;
+            dst[kHeadDim + 1] = r.den;
+        }
+        cluster_sync_all();
+        if (crank == 0) {
+            PieceResult m;
+            m.M = kNegInf;
+            for (int q = 0; q < C; ++q) m.M = fmaxf(m.M, recv[(q * kGroup + h) * kPartStride + kHeadDim]);
+            m.den = 0.f;
+            m.num = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (m.M != kNegInf) {
+                for (int q = 0; q < C; ++q) {
+                    const float *pp = recv + (q * kGroup + h) * kPartStride;
+                    const float mq = pp[kHeadDim];
+                    const float e = mq == kNegInf ? 0.f : exp2f(mq - m.M);
+                    const float4 o4 = *reinterpret_cast<const float4 *>(pp + d0);
+                    m.den += e * pp[kHeadDim + 1];
+                    m.num.x += e * o4.x;
+                    m.num.y += e * o4.y;
+                    m.num.z += e * o4.z;
+                    m.num.w += e * o4.w;
+                }
+            }
+            if (K == 1) {
+                store_out(p, cb, cg, m);
+            } else {
+                const int sigma = cb * p.Hkv + cg;
+                store_partial<kFused>(p, misc, cid, sigma, static_cast<int64_t>(sigma) * K, K, cb,
+                                      cg, m);
+            }
         }
     }
     __syncthreads();
@@ -773,11 +1107,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // (bounded) before the CTA's shared memory is released.
     if (tid == 0 && misc[0]) {
         const uint32_t issued = static_cast<uint32_t>(misc[2]);
-        const uint32_t first = issued > kStages ? issued - kStages : 0;
+        const uint32_t first = issued > static_cast<uint32_t>(NS) ? issued - NS : 0;
         volatile int never = 0;
         for (uint32_t t = first; t < issued; ++t)
-            mbar_wait_bounded(full0 + 8 * (t % kStages), (t / kStages) & 1, &never);
+            mbar_wait_bounded(full0 + 8 * (t % NS), (t / NS) & 1, &never);
     }
+}
+
+// ------------------------------------------------------------ rope table --
+// cos/sin of every (sequence, frequency) of the step, computed once and
+// shared by all layers (the angles depend on the positions only).
+__global__ void __launch_bounds__(256) rope_table_kernel(const __grid_constant__ Params p) {
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= p.B * kRotPairs) return;
+    const int b = idx / kRotPairs, i = idx % kRotPairs;
+    p.rope_out[idx] = rope_entry(p.positions[b], p.inv_freq[i], true);
 }
 
 // ---------------------------------------------------------- append kernel --
@@ -810,14 +1154,52 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Para
     const int j0 = cta_of(seg0, W, G);
     const int np = cta_of(seg0 + n - 1, W, G) - j0 + 1;
     if (np == 1) return;  // the split kernel wrote this output itself
-    merge_pieces(p, sigma, b, g, j0, np);
+    merge_pieces(p, static_cast<int64_t>(sigma) + j0, b, g, np);
 }
 
-bool g_attr_set[2][64];
+size_t g_smem_attr[4][64];
+
+template <bool kFused, bool kCluster>
+cudaError_t launch_one(const Params &p, const CUtensorMap &kv_map, size_t smem, int dev,
+                       cudaStream_t s) {
+    auto kern = attention_kernel<kFused, kCluster>;
+    size_t &attr = g_smem_attr[(kFused ? 2 : 0) + (kCluster ? 1 : 0)][dev];
+    if (attr < smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        attr = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (kCluster) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = p.cluster;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (p.pdl) {
+        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, kv_map, p);
+}
 
 }  // namespace
 
-size_t attention_smem_bytes() { return kSmemBytes; }
+size_t attention_smem_bytes(int B, int stages, bool cluster) {
+    return static_cast<size_t>(ring_offset(B, cluster)) + static_cast<size_t>(stages) * kTileBytes +
+           1024;
+}
 
 static int current_device() {
     int d = 0;
@@ -825,23 +1207,43 @@ static int current_device() {
     return d < 64 ? d : 63;
 }
 
+int max_active_clusters(int cluster, size_t smem) {
+    auto kern = attention_kernel<true, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return 0;
+    const int dev = current_device();
+    if (g_smem_attr[3][dev] < smem) g_smem_attr[3][dev] = smem;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cluster * 64);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = cluster;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+    return n;
+}
+
 cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, bool fused,
                              cudaStream_t s) {
+    const size_t smem = attention_smem_bytes(p.B, p.stages, p.cluster != 0);
     const int dev = current_device();
-    if (!g_attr_set[fused][dev]) {
-        cudaError_t e = fused ? cudaFuncSetAttribute(attention_kernel<true>,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     kSmemBytes)
-                              : cudaFuncSetAttribute(attention_kernel<false>,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     kSmemBytes);
-        if (e != cudaSuccess) return e;
-        g_attr_set[fused][dev] = true;
-    }
     if (fused)
-        attention_kernel<true><<<p.grid, kThreads, kSmemBytes, s>>>(kv_map, p);
-    else
-        attention_kernel<false><<<p.grid, kThreads, kSmemBytes, s>>>(kv_map, p);
+        return p.cluster ? launch_one<true, true>(p, kv_map, smem, dev, s)
+                         : launch_one<true, false>(p, kv_map, smem, dev, s);
+    return p.cluster ? launch_one<false, true>(p, kv_map, smem, dev, s)
+                     : launch_one<false, false>(p, kv_map, smem, dev, s);
+}
+
+cudaError_t launch_rope_table(const Params &p, cudaStream_t s) {
+    const int n = p.B * kRotPairs;
+    rope_table_kernel<<<(n + 255) / 256, 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

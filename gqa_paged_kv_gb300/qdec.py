@@ -24,14 +24,17 @@ QDEC_ERR_CUDA = 4
 QDEC_ERR_DEVICE_BOUNDS = 5
 QDEC_ERR_TIMEOUT = 6
 
+QDEC_LAUNCH_OVERLAP_PREVIOUS = 1
+
 QDEC_FLAG_BAD_PAGE = 1
 QDEC_FLAG_BAD_SEQLEN = 2
 QDEC_FLAG_TIMEOUT = 4
+QDEC_FLAG_BAD_INDEX = 8
 
 # Every symbol include/qdec.h declares.
-EXPORTS = ("qdec_workspace_bytes", "qdec_workspace_init", "qdec_append_rope", "qdec_attn_split",
-           "qdec_attn_merge", "qdec_step", "qdec_check_error", "qdec_status_string",
-           "qdec_version")
+EXPORTS = ("qdec_workspace_bytes", "qdec_workspace_init", "qdec_rope_table_bytes",
+           "qdec_rope_table", "qdec_append_rope", "qdec_attn_split", "qdec_attn_merge",
+           "qdec_step", "qdec_check_error", "qdec_status_string", "qdec_version")
 
 
 class QdecShape(ctypes.Structure):
@@ -40,7 +43,8 @@ class QdecShape(ctypes.Structure):
                 ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32),
                 ("max_blocks_per_seq", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
                 ("rope_theta", ctypes.c_float), ("eps", ctypes.c_float),
-                ("sm_scale", ctypes.c_float), ("num_ctas", ctypes.c_int32)]
+                ("sm_scale", ctypes.c_float), ("num_ctas", ctypes.c_int32),
+                ("launch_flags", ctypes.c_int32)]
 
 
 @dataclass
@@ -57,12 +61,13 @@ class Shape:
     eps: float = 1.0e-6
     sm_scale: float = 0.0
     num_ctas: int = 0
+    launch_flags: int = 0
 
     def c(self) -> QdecShape:
         return QdecShape(self.batch, self.num_q_heads, self.num_kv_heads, self.head_dim,
                          self.page_size, self.num_pages, self.max_blocks_per_seq,
                          self.max_seq_len, self.rope_theta, self.eps, self.sm_scale,
-                         self.num_ctas)
+                         self.num_ctas, self.launch_flags)
 
 
 class QdecError(RuntimeError):
@@ -82,15 +87,19 @@ def _load():
     lib.qdec_workspace_bytes.restype = sz
     lib.qdec_workspace_init.argtypes = [sp, vp, sz, vp]
     lib.qdec_workspace_init.restype = st
+    lib.qdec_rope_table_bytes.argtypes = [sp]
+    lib.qdec_rope_table_bytes.restype = sz
+    lib.qdec_rope_table.argtypes = [sp, vp, vp, vp]
+    lib.qdec_rope_table.restype = st
     lib.qdec_append_rope.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp,
-                                     vp, vp]
+                                     vp, vp, vp]
     lib.qdec_append_rope.restype = st
     lib.qdec_attn_split.argtypes = [sp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     lib.qdec_attn_split.restype = st
     lib.qdec_attn_merge.argtypes = [sp, vp, vp, sz, vp, vp, vp]
     lib.qdec_attn_merge.restype = st
-    lib.qdec_step.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp,
-                              vp, vp]
+    lib.qdec_step.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+                              vp, vp, vp]
     lib.qdec_step.restype = st
     lib.qdec_check_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
     lib.qdec_check_error.restype = st
@@ -148,13 +157,22 @@ def qdec_workspace_init(shape: Shape, workspace: torch.Tensor, stream=None):
                                     _stream(stream)), "qdec_workspace_init")
 
 
+def qdec_rope_table_bytes(shape: Shape) -> int:
+    return int(_lib.qdec_rope_table_bytes(ctypes.byref(shape.c())))
+
+
+def qdec_rope_table(shape: Shape, positions, rope_table, stream=None):
+    _raise(_lib.qdec_rope_table(ctypes.byref(shape.c()), _ptr(positions), _ptr(rope_table),
+                                _stream(stream)), "qdec_rope_table")
+
+
 def qdec_append_rope(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, seq_lens,
-                     block_table, kv_pool, q_rot, err_flag=None, stream=None):
+                     block_table, kv_pool, q_rot, err_flag=None, stream=None, rope_table=None):
     _raise(_lib.qdec_append_rope(
         ctypes.byref(shape.c()), _ptr(q), _rows(q, "q"), _ptr(k), _rows(k, "k"), _ptr(v),
         _rows(v, "v"), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions), _ptr(seq_lens),
-        _ptr(block_table), _ptr(kv_pool), _ptr(q_rot), _ptr(err_flag), _stream(stream)),
-        "qdec_append_rope")
+        _ptr(block_table), _ptr(rope_table), _ptr(kv_pool), _ptr(q_rot), _ptr(err_flag),
+        _stream(stream)), "qdec_append_rope")
 
 
 def qdec_attn_split(shape: Shape, q_rot, kv_pool, block_table, seq_lens, workspace, out,
@@ -173,11 +191,11 @@ def qdec_attn_merge(shape: Shape, seq_lens, workspace, out, err_flag=None, strea
 
 
 def qdec_step(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, seq_lens, block_table,
-              kv_pool, workspace, out, err_flag=None, stream=None):
+              kv_pool, workspace, out, err_flag=None, stream=None, rope_table=None):
     _raise(_lib.qdec_step(
         ctypes.byref(shape.c()), _ptr(q), _rows(q, "q"), _ptr(k), _rows(k, "k"), _ptr(v),
         _rows(v, "v"), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions), _ptr(seq_lens),
-        _ptr(block_table), _ptr(kv_pool), _ptr(workspace),
+        _ptr(block_table), _ptr(rope_table), _ptr(kv_pool), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), _ptr(err_flag),
         _stream(stream)), "qdec_step")
 
@@ -191,14 +209,23 @@ def qdec_check_error(err_flag, stream=None):
 
 # ------------------------------------------------------------- conveniences --
 
-def shape_for(workload, num_ctas: int = 0) -> Shape:
+def shape_for(workload, num_ctas: int = 0, launch_flags: int = 0) -> Shape:
     """The Shape of a workloads.Workload (one layer's pool)."""
     s = workload.spec
     return Shape(batch=s.batch, num_pages=s.pool_pages,
                  max_blocks_per_seq=workload.max_blocks,
                  max_seq_len=int(workload.max_blocks * s.page_size),
                  num_q_heads=s.num_q_heads, num_kv_heads=s.num_kv_heads,
-                 head_dim=s.head_dim, page_size=s.page_size, num_ctas=num_ctas)
+                 head_dim=s.head_dim, page_size=s.page_size, num_ctas=num_ctas,
+                 launch_flags=launch_flags)
+
+
+def alloc_rope_table(shape: Shape, device=None) -> torch.Tensor:
+    """A device buffer for qdec_rope_table (caller owns it)."""
+    n = qdec_rope_table_bytes(shape)
+    if n == 0:
+        raise QdecError(QDEC_ERR_INVALID_ARG, "qdec_rope_table_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 
 def alloc_workspace(shape: Shape, device=None, stream=None) -> torch.Tensor:

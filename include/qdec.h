@@ -40,7 +40,8 @@
  *   - Host-detectable errors return a status and launch nothing.  A failed
  *     launch returns QDEC_ERR_CUDA.  Device-detected faults (a block-table
  *     entry outside the pool, a seq_len outside [1, max_blocks_per_seq * P],
- *     a bounded wait that ran out) never trap: the kernel skips the affected
+ *     a bounded wait that ran out, an internal index that fails its bounds
+ *     check) never trap: the kernel skips the affected
  *     work, ORs a QDEC_FLAG_* bit into *err_flag (when err_flag is not NULL)
  *     and the outputs of the affected sequences are unspecified.
  *   - Alignment: q, k, v, kv_pool, out, q_rot and workspace must be 16-byte
@@ -73,10 +74,21 @@ typedef enum {
     QDEC_ERR_TIMEOUT = 6         /* qdec_check_error: a bounded wait gave up    */
 } qdec_status;
 
+/* qdec_shape.launch_flags */
+#define QDEC_LAUNCH_OVERLAP_PREVIOUS 1
+/* qdec_step may be launched as a programmatic dependent of the kernel before
+ * it on the stream: it starts streaming cached KV pages (reading seq_lens,
+ * block_table and kv_pool) while that kernel is still finishing, and waits
+ * for it before reading q, k, v, positions, the norm weights, the rope table
+ * or writing anything.  Set it only when the immediately preceding kernel
+ * does not write seq_lens, block_table or kv_pool pages other than the
+ * append slots of this step (e.g. the previous layer's qdec_step). */
+
 /* Bits a kernel ORs into *err_flag. */
 #define QDEC_FLAG_BAD_PAGE   1   /* block-table entry outside [0, num_pages)   */
 #define QDEC_FLAG_BAD_SEQLEN 2   /* seq_len outside [1, max_blocks_per_seq*P]  */
 #define QDEC_FLAG_TIMEOUT    4   /* an mbarrier wait exceeded its time limit   */
+#define QDEC_FLAG_BAD_INDEX  8   /* an internal index failed its bounds check  */
 
 /* Problem description.  Supported: head_dim 128, page_size 16,
  * num_q_heads == 4 * num_kv_heads, 1 <= batch <= 1024. */
@@ -95,6 +107,7 @@ typedef struct {
     int32_t num_ctas;            /* attention grid size; 0 = automatic (a whole
                                     number of CTAs per SM).  Results do not
                                     depend on it beyond fp32 rounding.          */
+    int32_t launch_flags;        /* QDEC_LAUNCH_* bits (qdec_step only)          */
 } qdec_shape;
 
 /* Bytes of device workspace that qdec_attn_split / qdec_attn_merge /
@@ -102,6 +115,19 @@ typedef struct {
  * The workspace holds the per-piece partial results (o, lse) of the split
  * and one arrival counter per (sequence, KV head). */
 size_t qdec_workspace_bytes(const qdec_shape *shape);
+
+/* Bytes of the per-step RoPE table for `shape` (B * D/2 entries of 16 B). */
+size_t qdec_rope_table_bytes(const qdec_shape *shape);
+
+/* cos and sin of every RoPE angle positions[b] * rope_theta^(-2i/D) of the
+ * step, each kept as an unevaluated pair of floats (about 48 bits), into
+ * rope_table (device, qdec_rope_table_bytes).  The angles depend on the
+ * positions only, so one table serves all layers of a decode step (the
+ * blog's part 3: build per-step metadata once, share it across the 36
+ * layers).  Pass it to qdec_step / qdec_append_rope; recompute it whenever
+ * positions change. */
+qdec_status qdec_rope_table(const qdec_shape *shape, const int32_t *positions,
+                            void *rope_table, void *stream);
 
 /* Zero the arrival counters of a fresh workspace.  Call once after
  * allocating it (the kernels leave the counters at zero again when they
@@ -113,17 +139,20 @@ qdec_status qdec_workspace_init(const qdec_shape *shape, void *workspace,
  * then the append of bf16(k_rot) and v into kv_pool at slot seq_lens[b]-1.
  *   q [B][Hq][D] (sequence stride q_stride), k, v [B][Hkv][D] (k_stride,
  *   v_stride); q_norm_w, k_norm_w [D]; positions, seq_lens [B] int32;
- *   block_table [B][max_blocks_per_seq] int32; kv_pool as above (written at
- *   one slot per (sequence, KV head) only); q_rot [B][Hq][D] fp32 output, the
- *   normed and rotated query rows, unscaled and unrounded. */
+ *   block_table [B][max_blocks_per_seq] int32; rope_table from qdec_rope_table
+ *   for these positions, or NULL (the angles are then computed in the kernel,
+ *   partly in slow fp64); kv_pool as above (written at one slot per
+ *   (sequence, KV head) only); q_rot [B][Hq][D] fp32 output, the normed and
+ *   rotated query rows, unscaled and unrounded. */
 qdec_status qdec_append_rope(const qdec_shape *shape,
                              const qdec_bf16 *q, int64_t q_stride,
                              const qdec_bf16 *k, int64_t k_stride,
                              const qdec_bf16 *v, int64_t v_stride,
                              const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
                              const int32_t *positions, const int32_t *seq_lens,
-                             const int32_t *block_table, qdec_bf16 *kv_pool,
-                             float *q_rot, int32_t *err_flag, void *stream);
+                             const int32_t *block_table, const void *rope_table,
+                             qdec_bf16 *kv_pool, float *q_rot, int32_t *err_flag,
+                             void *stream);
 
 /* Step 4, first half: split-KV attention of q_rot (from qdec_append_rope)
  * over the pool.  A (sequence, KV head) handled by one piece gets its bf16
@@ -147,16 +176,17 @@ qdec_status qdec_attn_merge(const qdec_shape *shape, const int32_t *seq_lens,
  * appends the new key/value, and the last CTA to finish a split (sequence,
  * KV head) merges its pieces.  Same arguments as qdec_append_rope plus the
  * workspace and `out`; no q_rot buffer is needed.  The workspace counters
- * must be zero on entry (qdec_workspace_init once). */
+ * must be zero on entry (qdec_workspace_init once).  See
+ * QDEC_LAUNCH_OVERLAP_PREVIOUS for overlapping consecutive layers. */
 qdec_status qdec_step(const qdec_shape *shape,
                       const qdec_bf16 *q, int64_t q_stride,
                       const qdec_bf16 *k, int64_t k_stride,
                       const qdec_bf16 *v, int64_t v_stride,
                       const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
                       const int32_t *positions, const int32_t *seq_lens,
-                      const int32_t *block_table, qdec_bf16 *kv_pool,
-                      void *workspace, size_t workspace_bytes, qdec_bf16 *out,
-                      int32_t *err_flag, void *stream);
+                      const int32_t *block_table, const void *rope_table,
+                      qdec_bf16 *kv_pool, void *workspace, size_t workspace_bytes,
+                      qdec_bf16 *out, int32_t *err_flag, void *stream);
 
 /* Synchronise `stream`, read *err_flag (device), clear it, and map it to a
  * status: QDEC_OK, QDEC_ERR_DEVICE_BOUNDS or QDEC_ERR_TIMEOUT (QDEC_ERR_CUDA

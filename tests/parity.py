@@ -40,11 +40,17 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
 class Runner:
     """Device buffers for running a workload's layers through qdec_step."""
 
-    def __init__(self, w: wl.Workload, num_ctas: int = 0):
+    def __init__(self, w: wl.Workload, num_ctas: int = 0, rope: bool = True,
+                 overlap: bool = False):
         q = qdec()
         self.w = w
-        self.shape = q.shape_for(w, num_ctas=num_ctas)
+        self.shape = q.shape_for(w, num_ctas=num_ctas,
+                                 launch_flags=q.QDEC_LAUNCH_OVERLAP_PREVIOUS if overlap else 0)
         self.ws = q.alloc_workspace(self.shape)
+        self.rope = None
+        if rope:
+            self.rope = q.alloc_rope_table(self.shape)
+            q.qdec_rope_table(self.shape, w.positions, self.rope)
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
         s = w.spec
         self.out = torch.empty((s.layers, s.batch, s.num_q_heads, s.head_dim),
@@ -56,13 +62,13 @@ class Runner:
         q, w = qdec(), self.w
         q.qdec_step(self.shape, w.q(layer), w.k(layer), w.v(layer), w.w_q[layer], w.w_k[layer],
                     w.positions, w.seq_lens, w.block_table, w.pool(layer), self.ws,
-                    self.out[layer], self.err)
+                    self.out[layer], self.err, rope_table=self.rope)
 
     def unfused(self, layer: int):
         q, w = qdec(), self.w
         q.qdec_append_rope(self.shape, w.q(layer), w.k(layer), w.v(layer), w.w_q[layer],
                            w.w_k[layer], w.positions, w.seq_lens, w.block_table, w.pool(layer),
-                           self.q_rot, self.err)
+                           self.q_rot, self.err, rope_table=self.rope)
         q.qdec_attn_split(self.shape, self.q_rot, w.pool(layer), w.block_table, w.seq_lens,
                           self.ws, self.out[layer], self.err)
         q.qdec_attn_merge(self.shape, w.seq_lens, self.ws, self.out[layer], self.err)
@@ -113,4 +119,5 @@ def assert_slots(w: wl.Workload, layer: int, seqs, res: dict):
         assert np.all(np.abs(k_gpu - k_ref) <= bf16_ulp(k_ref)), f"k slot seq {b}"
         not_exact += int(np.sum(row[0] != oracle.f64_to_bf16_bits(k_ref)))
         assert np.array_equal(row[1], v_in[b]), f"v slot seq {b}"
+    assert not_exact == 0, f"{not_exact} k elements differ from the oracle's rounding"
     return not_exact

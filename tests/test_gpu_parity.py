@@ -32,23 +32,25 @@ def _small(lens, seed=11, hq=32, hkv=8, chan=False, spikes=0.0):
     return wl.build(spec, "cuda", poison=True)
 
 
+@pytest.mark.parametrize("rope", [True, False], ids=["rope_table", "in_kernel_angles"])
 @pytest.mark.parametrize("lens,num_ctas", SMALL, ids=lambda x: str(x))
-def test_step_small(lens, num_ctas):
+def test_step_small(lens, num_ctas, rope):
     w = _small(lens)
     ref = parity.run_oracle(wl.oracle_inputs(w, 0))
-    r = parity.Runner(w, num_ctas=num_ctas)
+    r = parity.Runner(w, num_ctas=num_ctas, rope=rope)
     r.step(0)
     r.check_flags()
     parity.assert_out_close(r.out[0], ref["out"])
     parity.assert_slots(w, 0, range(len(lens)), ref)
 
 
+@pytest.mark.parametrize("rope", [True, False], ids=["rope_table", "in_kernel_angles"])
 @pytest.mark.parametrize("lens,num_ctas", SMALL[:8], ids=lambda x: str(x))
-def test_unfused_three_calls(lens, num_ctas):
+def test_unfused_three_calls(lens, num_ctas, rope):
     w = _small(lens, seed=12)
     inputs = wl.oracle_inputs(w, 0)
     ref = parity.run_oracle(inputs)
-    r = parity.Runner(w, num_ctas=num_ctas)
+    r = parity.Runner(w, num_ctas=num_ctas, rope=rope)
     r.unfused(0)
     r.check_flags()
     q_rot = r.q_rot.double().cpu().numpy()
@@ -108,8 +110,38 @@ def test_counters_return_to_zero():
     assert torch.count_nonzero(r.ws[:4 * n].view(torch.int32)).item() == 0
 
 
+def test_rope_table_values():
+    """The table's float pairs carry cos/sin of pos * theta^(-2i/D) to ~1e-14."""
+    w = _small([1, 17, 300, 16384], seed=19)
+    r = parity.Runner(w)
+    torch.cuda.synchronize()
+    t = r.rope.view(torch.float32).view(4, 64, 4).double().cpu().numpy()
+    pos = w.positions.cpu().numpy().astype(np.float64)
+    inv = 1e6 ** (-2.0 * np.arange(64) / 128)
+    ang = pos[:, None] * inv[None, :]
+    assert np.max(np.abs(t[..., 0] + t[..., 1] - np.cos(ang))) < 1e-13
+    assert np.max(np.abs(t[..., 2] + t[..., 3] - np.sin(ang))) < 1e-13
+
+
+@pytest.mark.parametrize("num_ctas", [0, 5])
+def test_overlapped_layers_match_serial_layers(num_ctas):
+    """Programmatic dependent launch of consecutive layers changes no bit,
+    also when the layers share one pool (each layer rewrites the same slots)."""
+    for shared in (False, True):
+        spec = wl.custom(5, [17, 1, 300, 64, 1000], pool_pages=120, layers=6, seed=20,
+                         shared_pool=shared)
+        w = wl.build(spec, "cuda", poison=True)
+        outs = []
+        for overlap in (False, True):
+            r = parity.Runner(w, num_ctas=num_ctas, overlap=overlap)
+            for layer in range(6):
+                r.step(layer)
+            r.check_flags()
+            outs.append(r.out.clone())
+        assert torch.equal(outs[0], outs[1])
+
+
 def test_graph_capture_replays_identically():
-    w = _small([17, 1, 300, 64], seed=18)
     spec = wl.custom(4, [17, 1, 300, 64], pool_pages=40, layers=3, seed=18)
     w = wl.build(spec, "cuda", poison=True)
     r = parity.Runner(w)
@@ -132,11 +164,13 @@ def test_graph_capture_replays_identically():
 # ------------------------------------------------------ benchmark workloads --
 
 def _check_layers(w, layers, seqs=None, num_ctas=0):
-    """Run every layer of w in order (as the benchmark does); compare the
-    given layers (pool snapshots taken before any layer ran)."""
+    """Run every layer of w in order as the benchmark does (rope table, then
+    overlapped layer launches); compare the given layers (pool snapshots
+    taken before any layer ran)."""
     seqs = list(range(w.spec.batch)) if seqs is None else list(seqs)
     snaps = {l: wl.oracle_inputs(w, l, seqs) for l in layers}
-    r = parity.Runner(w, num_ctas=num_ctas)
+    torch.cuda.synchronize()
+    r = parity.Runner(w, num_ctas=num_ctas, overlap=True)
     for layer in range(w.spec.layers):
         r.step(layer)
     r.check_flags()

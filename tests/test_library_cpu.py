@@ -58,32 +58,41 @@ def test_workspace_bytes_rejects_bad_shapes(q):
 def test_entry_points_reject_null_and_misaligned_arguments(q):
     lib = q._lib
     sh = ctypes.byref(_shape(q).c())
-    ok_ptr = ctypes.c_void_p(1 << 20)      # never dereferenced: rejected earlier
-    bad_ptr = ctypes.c_void_p((1 << 20) + 2)
+    ok = ctypes.c_void_p(1 << 20)      # never dereferenced: rejected earlier
+    bad = ctypes.c_void_p((1 << 20) + 2)
     z = ctypes.c_void_p(0)
-    # null shape
-    assert lib.qdec_step(None, *([z, 0] * 3), *([z] * 6), z, 0, z, z, z) == q.QDEC_ERR_INVALID_ARG
-    # null q
-    assert lib.qdec_step(sh, z, 48 * 128, ok_ptr, 48 * 128, ok_ptr, 48 * 128, *([ok_ptr] * 6),
-                         ok_ptr, 1 << 30, ok_ptr, z, z) == q.QDEC_ERR_INVALID_ARG
-    # misaligned q
-    assert lib.qdec_step(sh, bad_ptr, 48 * 128, ok_ptr, 48 * 128, ok_ptr, 48 * 128,
-                         *([ok_ptr] * 6), ok_ptr, 1 << 30, ok_ptr, z, z) == q.QDEC_ERR_INVALID_ARG
-    # stride not a multiple of 8 / shorter than the heads
-    assert lib.qdec_step(sh, ok_ptr, 48 * 128 + 4, ok_ptr, 48 * 128, ok_ptr, 48 * 128,
-                         *([ok_ptr] * 6), ok_ptr, 1 << 30, ok_ptr, z, z) == q.QDEC_ERR_INVALID_ARG
-    assert lib.qdec_step(sh, ok_ptr, 16 * 128, ok_ptr, 48 * 128, ok_ptr, 48 * 128,
-                         *([ok_ptr] * 6), ok_ptr, 1 << 30, ok_ptr, z, z) == q.QDEC_ERR_INVALID_ARG
-    # workspace too small / missing
-    assert lib.qdec_step(sh, *([ok_ptr, 48 * 128] * 3), *([ok_ptr] * 6), ok_ptr, 16, ok_ptr,
-                         z, z) == q.QDEC_ERR_WORKSPACE
-    assert lib.qdec_attn_split(sh, ok_ptr, ok_ptr, ok_ptr, ok_ptr, z, 1 << 30, ok_ptr, z,
-                               z) == q.QDEC_ERR_WORKSPACE
-    assert lib.qdec_attn_merge(sh, z, ok_ptr, 1 << 30, ok_ptr, z, z) == q.QDEC_ERR_INVALID_ARG
-    assert lib.qdec_append_rope(sh, *([ok_ptr, 48 * 128] * 3), *([ok_ptr] * 6), z, z,
+    S = 48 * 128
+
+    def step(shape=sh, qp=ok, qs=S, rope=z, ws=ok, ws_bytes=1 << 30, out=ok):
+        # shape, q, q_stride, k, k_stride, v, v_stride, w_q, w_k, positions,
+        # seq_lens, block_table, rope_table, kv_pool, workspace, bytes, out, err, stream
+        return lib.qdec_step(shape, qp, qs, ok, S, ok, S, ok, ok, ok, ok, ok, rope, ok, ws,
+                             ws_bytes, out, z, z)
+
+    assert step(shape=None) == q.QDEC_ERR_INVALID_ARG
+    assert step(qp=z) == q.QDEC_ERR_INVALID_ARG
+    assert step(qp=bad) == q.QDEC_ERR_INVALID_ARG
+    assert step(qs=S + 4) == q.QDEC_ERR_INVALID_ARG          # not a multiple of 8
+    assert step(qs=16 * 128) == q.QDEC_ERR_INVALID_ARG       # shorter than the heads
+    assert step(rope=bad) == q.QDEC_ERR_INVALID_ARG
+    assert step(out=z) == q.QDEC_ERR_INVALID_ARG
+    assert step(ws_bytes=16) == q.QDEC_ERR_WORKSPACE
+    assert step(ws=z) == q.QDEC_ERR_WORKSPACE
+    assert lib.qdec_attn_split(sh, ok, ok, ok, ok, z, 1 << 30, ok, z, z) == q.QDEC_ERR_WORKSPACE
+    assert lib.qdec_attn_merge(sh, z, ok, 1 << 30, ok, z, z) == q.QDEC_ERR_INVALID_ARG
+    # append without a q_rot output
+    assert lib.qdec_append_rope(sh, ok, S, ok, S, ok, S, ok, ok, ok, ok, ok, z, ok, z, z,
                                 z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_rope_table(sh, z, ok, z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_rope_table(sh, ok, bad, z) == q.QDEC_ERR_INVALID_ARG
     assert lib.qdec_check_error(None, z, None) == q.QDEC_ERR_INVALID_ARG
-    # unsupported group size
+    # unsupported group size; unknown launch flag
     sh2 = ctypes.byref(_shape(q, num_q_heads=8, num_kv_heads=8).c())
-    assert lib.qdec_step(sh2, *([ok_ptr, 48 * 128] * 3), *([ok_ptr] * 6), ok_ptr, 1 << 30,
-                         ok_ptr, z, z) == q.QDEC_ERR_UNSUPPORTED
+    assert step(shape=sh2) == q.QDEC_ERR_UNSUPPORTED
+    sh3 = ctypes.byref(_shape(q, launch_flags=2).c())
+    assert step(shape=sh3) == q.QDEC_ERR_INVALID_ARG
+
+
+def test_rope_table_bytes(q):
+    assert q.qdec_rope_table_bytes(_shape(q, batch=3)) == 3 * 64 * 16
+    assert q.qdec_rope_table_bytes(_shape(q, head_dim=64)) == 0
