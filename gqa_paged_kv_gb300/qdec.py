@@ -34,7 +34,10 @@ QDEC_FLAG_BAD_INDEX = 8
 # Every symbol include/qdec.h declares.
 EXPORTS = ("qdec_workspace_bytes", "qdec_workspace_init", "qdec_rope_table_bytes",
            "qdec_rope_table", "qdec_append_rope", "qdec_attn_split", "qdec_attn_merge",
-           "qdec_step", "qdec_check_error", "qdec_status_string", "qdec_version")
+           "qdec_step", "qdec_step_static_scratch", "qdec_check_error", "qdec_status_string",
+           "qdec_version")
+
+QDEC_STATIC_SCRATCH_BYTES = 4 << 20
 
 
 class QdecShape(ctypes.Structure):
@@ -101,6 +104,9 @@ def _load():
     lib.qdec_step.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                               vp, vp, vp]
     lib.qdec_step.restype = st
+    lib.qdec_step_static_scratch.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp,
+                                             vp, vp, vp, vp, vp]
+    lib.qdec_step_static_scratch.restype = st
     lib.qdec_check_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
     lib.qdec_check_error.restype = st
     lib.qdec_status_string.argtypes = [st]
@@ -198,6 +204,18 @@ def qdec_step(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, seq_lens, bl
         _ptr(block_table), _ptr(rope_table), _ptr(kv_pool), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), _ptr(err_flag),
         _stream(stream)), "qdec_step")
+
+
+def qdec_step_static_scratch(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, seq_lens,
+                             block_table, kv_pool, out, err_flag=None, stream=None,
+                             rope_table=None):
+    """qdec_step with the library's own fixed scratch array as the workspace
+    (for callers that cannot allocate device memory)."""
+    _raise(_lib.qdec_step_static_scratch(
+        ctypes.byref(shape.c()), _ptr(q), _rows(q, "q"), _ptr(k), _rows(k, "k"), _ptr(v),
+        _rows(v, "v"), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions), _ptr(seq_lens),
+        _ptr(block_table), _ptr(rope_table), _ptr(kv_pool), _ptr(out), _ptr(err_flag),
+        _stream(stream)), "qdec_step_static_scratch")
 
 
 def qdec_check_error(err_flag, stream=None):

@@ -188,6 +188,35 @@ qdec_status qdec_step(const qdec_shape *shape,
                       qdec_bf16 *kv_pool, void *workspace, size_t workspace_bytes,
                       qdec_bf16 *out, int32_t *err_flag, void *stream);
 
+/* qdec_step without a caller-provided workspace, for callers that cannot
+ * allocate device memory (e.g. a serving loop that must not call
+ * cudaMalloc/cudaFree once running, or a plugin whose host runtime owns all
+ * device allocations).  No counterpart in the pages: it is a deployment
+ * convenience, not part of the method.  The scratch is a fixed array of
+ * QDEC_STATIC_SCRATCH_BYTES in the library's own device memory, reserved on
+ * every device that loads the library and held until the process exits.
+ *   - Same arguments as qdec_step minus workspace/workspace_bytes; the caller
+ *     still passes every input and output.  Allocates nothing.
+ *   - Returns QDEC_ERR_WORKSPACE when the shape needs more scratch than
+ *     QDEC_STATIC_SCRATCH_BYTES (qdec_workspace_bytes tells how much).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call, on any stream, uses the same array, which keeps the
+ *     previous call's contents; each call clears the counters it needs on its
+ *     stream before the kernel runs.  Calls that can overlap on the GPU (other
+ *     streams, other threads) race on the array: serialise them. */
+#define QDEC_STATIC_SCRATCH_BYTES (4u << 20)
+qdec_status qdec_step_static_scratch(const qdec_shape *shape,
+                                     const qdec_bf16 *q, int64_t q_stride,
+                                     const qdec_bf16 *k, int64_t k_stride,
+                                     const qdec_bf16 *v, int64_t v_stride,
+                                     const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                                     const int32_t *positions, const int32_t *seq_lens,
+                                     const int32_t *block_table, const void *rope_table,
+                                     qdec_bf16 *kv_pool, qdec_bf16 *out, int32_t *err_flag,
+                                     void *stream);
+
 /* Synchronise `stream`, read *err_flag (device), clear it, and map it to a
  * status: QDEC_OK, QDEC_ERR_DEVICE_BOUNDS or QDEC_ERR_TIMEOUT (QDEC_ERR_CUDA
  * if the stream itself failed).  The raw bits go to *flags_out if not NULL. */
