@@ -51,6 +51,11 @@ KERNEL_SOURCES = ("gqa_paged_kv_gb300/csrc/qdec_kernels.cu", "gqa_paged_kv_gb300
 # still matches the one the counters were taken on.
 TRAFFIC = {}
 
+# The CPU timings sample the first few layers of a workload (same shapes and
+# lengths; fewer per-layer pools to materialise in host memory).
+CPU_SAMPLE_LAYERS = 4
+L2_BYTES_NOMINAL = 126 << 20
+
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
@@ -181,6 +186,42 @@ class Clocks:
                 "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
 
 
+def l2_bytes(dev=None) -> int:
+    if dev is not None:
+        n = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)
+        if n:
+            return int(n)
+    return L2_BYTES_NOMINAL
+
+
+def workload_config(spec, seq_lens_host, args, world: int, l2: int = L2_BYTES_NOMINAL) -> dict:
+    """The `config` object of the JSON line (the same for both arms)."""
+    L = spec.layers
+    bytes_layer = (int(seq_lens_host.sum()) * spec.kv_bytes_per_token()
+                   + spec.batch * spec.io_bytes_per_seq())
+    bytes_step = bytes_layer * L
+    if bytes_step < 2 * l2:
+        l2_note = (f"L2 flushed: a {2 * l2 / 2**20:.0f} MiB buffer is rewritten before each "
+                   f"timed step (untimed); a step reads {bytes_step / 1e6:.1f} MB")
+    elif spec.shared_pool:
+        l2_note = (f"inputs larger than L2: {bytes_layer / 1e9:.3f} GB per layer-step from "
+                   "one shared pool")
+    else:
+        l2_note = (f"inputs larger than L2: each step reads {bytes_step / 1e9:.3f} GB of KV "
+                   f"across {L} per-layer pools")
+    return {"workload": spec.name, "batch": spec.batch,
+            "ctx": f"{int(seq_lens_host.min())}-{int(seq_lens_host.max())}",
+            "heads": f"{spec.num_q_heads}q/{spec.num_kv_heads}kv",
+            "head_dim": spec.head_dim, "page_size": spec.page_size, "layers": L,
+            "pool_pages_per_layer": spec.pool_pages,
+            "kv_bytes_per_step": bytes_step,
+            "l2": l2_note,
+            "launch": ("eager" if args.no_graph else f"CUDA graphs: rope table + "
+                       f"{L} qdec_step") + ("" if args.no_overlap else
+                                            ", programmatic dependent launch"),
+            "parallelism": f"replicas x{world}"}
+
+
 # ------------------------------------------------------------ CPU oracle --
 def oracle_sample(w: wl.Workload, seconds: float, per_seq: bool):
     """Time the fp64 oracle (as it stands, one thread) on a bounded sample of
@@ -214,7 +255,7 @@ def run_reference(args, dist: Dist):
     if dist.rank != 0:
         return
     spec = wl.WORKLOADS[args.workload]
-    w = wl.build(spec, "cpu")
+    w = wl.build(spec, "cpu", layers=min(spec.layers, CPU_SAMPLE_LAYERS))
     # warm-up steps, then exactly K timed steps; a step is one sequence of one layer
     oracle_steps(w, args.warmup)
     t0 = time.perf_counter()
@@ -226,8 +267,7 @@ def run_reference(args, dist: Dist):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": {"workload": spec.name, "batch": spec.batch, "layers": spec.layers,
-                   "step": "fp64 oracle, one sequence of one layer-step per step"},
+        "config": workload_config(spec, w.seq_lens_host, args, 1),
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} steps of one sequence x one layer, "
                                    f"{dt:.1f} s"},
@@ -310,10 +350,17 @@ def run_ours(args, dist: Dist):
     st, flags = qdec.qdec_check_error(err, stream)
     assert st == 0, f"device error flags {flags:#x}"
 
+    # Steps whose inputs fit in L2 twice over are timed L2-cold: a buffer
+    # larger than L2 is rewritten before each one, outside the timed steps.
+    l2 = l2_bytes(dev)
+    flush = (torch.empty(2 * l2 // 4, dtype=torch.int32, device="cuda")
+             if w.algorithmic_bytes_per_layer() * L < 2 * l2 else None)
+
     # ---- device-timed region
     clocks = Clocks(dev)
     clocks.start()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     dist.barrier()
@@ -321,6 +368,9 @@ def run_ours(args, dist: Dist):
     with torch.cuda.stream(stream):
         e0.record(stream)
         for k in range(args.steps):
+            if flush is not None:
+                flush.add_(1)   # evict the previous step's lines from L2 (not timed)
+            starts[k].record(stream)
             run_rope()
             mids[k].record(stream)
             run_layers()
@@ -329,7 +379,9 @@ def run_ours(args, dist: Dist):
     torch.cuda.synchronize()
     dist.barrier()
     ck = clocks.stop()
-    t_ms = e0.elapsed_time(e1)
+    # the steps themselves: without a flush this is the whole region
+    t_ms = (sum(a.elapsed_time(e) for a, e in zip(starts, ends)) if flush is not None
+            else e0.elapsed_time(e1))
     t_layers_ms = sum(m.elapsed_time(e) for m, e in zip(mids, ends))
     t_ms_max = dist.max(t_ms)
     st, flags = qdec.qdec_check_error(err, stream)
@@ -385,10 +437,11 @@ def run_ours(args, dist: Dist):
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        w_cpu = wl.build(spec, "cpu")
+        w_cpu = wl.build(spec, "cpu", layers=min(spec.layers, CPU_SAMPLE_LAYERS))
         gbs, what, n, secs = oracle_sample(w_cpu, args.cpu_seconds, per_seq=False)
         cpu = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n} x {what} of {spec.name}, fp64, {secs:.1f} s"}
+               "sample": f"{n} x {what} of {spec.name} (layers 0-{w_cpu.spec.layers - 1}), "
+                             f"fp64, {secs:.1f} s"}
 
     if dist.rank == 0:
         line = {
@@ -398,26 +451,14 @@ def run_ours(args, dist: Dist):
             "data": "synthetic (seeded N(0,1) bf16 q/k/v and KV pages)",
             "us_per_layer_step": round(ms_step * 1e3 / L, 4),
             "pct_of_hbm_peak": round(100 * value / dist.world / peak, 2),
-            "config": {"workload": spec.name, "batch": spec.batch,
-                       "ctx": f"{int(w.seq_lens_host.min())}-{int(w.seq_lens_host.max())}",
-                       "heads": f"{spec.num_q_heads}q/{spec.num_kv_heads}kv",
-                       "head_dim": spec.head_dim, "page_size": spec.page_size, "layers": L,
-                       "pool_pages_per_layer": spec.pool_pages,
-                       "kv_bytes_per_step": bytes_step,
-                       "l2": f"inputs larger than L2: each step reads {bytes_step / 1e9:.3f} GB "
-                             "of KV across 36 per-layer pools" if not spec.shared_pool else
-                             f"{bytes_layer / 1e9:.3f} GB per layer from one shared pool",
-                       "launch": ("eager" if args.no_graph else "CUDA graphs: rope table + "
-                                  "36 qdec_step") + ("" if args.no_overlap else
-                                                     ", programmatic dependent launch"),
-                       "parallelism": f"replicas x{dist.world}"},
+            "config": workload_config(spec, w.seq_lens_host, args, dist.world, l2_bytes(dev)),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_kind == "measured" else "fallback",
                          "kernel": "attention_kernel<fused>", "launch_us": round(launch_us, 3),
-                         "launch_us_how": "CUDA events around the 36-launch graph each step "
-                                          "(inter-launch gaps included) / 36",
+                         "launch_us_how": f"CUDA events around the {L}-launch graph each step "
+                                          f"(inter-launch gaps included) / {L}",
                          "bytes_per_launch": bytes_layer},
             "e2e": {"value": e2e_value and round(e2e_value, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d,

@@ -98,7 +98,7 @@ constexpr int64_t kFlatMinTilesPerCta = 32;
 
 // Deepest ring (a multiple of the 4 consumer warps) that still lets two
 // CTAs share an SM.
-int ring_cap(const qdec_shape *s, bool cluster) {
+int ring_cap(const qdec_shape *s, int cluster) {
     int per_sm = smem_per_sm_of_current_device();
     if (per_sm <= 0) per_sm = 228 * 1024;
     const int w = qdec::kConsumerWarps;
@@ -125,7 +125,7 @@ int64_t cluster_capacity(const qdec_shape *s, int c, int cap) {
     static std::mutex mu;
     static int cache[64][qdec::kMaxCluster + 1];
     static size_t cache_smem[64][qdec::kMaxCluster + 1];
-    const size_t smem = qdec::attention_smem_bytes(s->batch, cap, true);
+    const size_t smem = qdec::attention_smem_bytes(s->batch, cap, c);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = -1;
     int n = 0;
@@ -160,12 +160,12 @@ Plan plan_for(const qdec_shape *s, bool allow_cluster) {
     const int64_t segs = static_cast<int64_t>(s->batch) * s->num_kv_heads;
     const int64_t nmax = (s->max_seq_len + qdec::kPageSize - 1) / qdec::kPageSize;
     if (s->num_ctas == 0 && allow_cluster && per_cta < kFlatMinTilesPerCta) {
-        const int cap = ring_cap(s, true);
         // T = tiles per CTA; a segment of nmax tiles gets C = ceil(nmax/T) CTAs
         // (at most a portable cluster) per chunk and K = ceil(nmax/(C*T)) chunks
         for (int64_t t = per_cta < 1 ? 1 : per_cta; t <= nmax && t < kFlatMinTilesPerCta; ++t) {
             int64_t c = (nmax + t - 1) / t;
             if (c > qdec::kMaxCluster) c = qdec::kMaxCluster;
+            const int cap = ring_cap(s, static_cast<int>(c));
             const int64_t chunks = (nmax + c * t - 1) / (c * t);
             const int64_t grid = c * segs * chunks;
             if (grid <= cluster_capacity(s, static_cast<int>(c), cap)) {
@@ -179,7 +179,7 @@ Plan plan_for(const qdec_shape *s, bool allow_cluster) {
     }
     const int64_t g = s->num_ctas > 0 ? s->num_ctas : (target < wmax ? target : wmax);
     pl.grid = static_cast<int>(g);
-    pl.stages = clamp_stages((wmax + g - 1) / g, ring_cap(s, false));
+    pl.stages = clamp_stages((wmax + g - 1) / g, ring_cap(s, 0));
     return pl;
 }
 
@@ -273,19 +273,24 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// The pool as a 2-D tensor of rows of D bf16 (one row per token slot of one
-// (page, plane, head)); a box is 16 rows x 64 dims (128 B), 128-byte
+// The pool as a 5-D tensor whose box is one page tile: dims (64 of D,
+// token [16], half of D [2], plane K/V [2], page*2*Hkv + head), strides
+// (2, 256, 128, Hkv*4096, 4096) bytes.  The plane and head dimensions
+// address the same bytes two ways (the K/V plane step is Hkv heads), which
+// the hardware allows; every box stays inside the pool because the last
+// coordinate is page*2*Hkv + head with head < Hkv.  128-byte rows are
 // swizzled so the tile math reads shared memory without bank conflicts.
 qdec_status encode_pool_map(CUtensorMap *map, const qdec_shape *s, const void *pool) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return QDEC_ERR_CUDA;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(qdec::kHeadDim),
-                                static_cast<cuuint64_t>(s->num_pages) * 2 * s->num_kv_heads *
-                                    qdec::kPageSize};
-    const cuuint64_t strides[1] = {qdec::kHeadDim * sizeof(uint16_t)};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(qdec::kPageSize)};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims,
+    const cuuint64_t plane = static_cast<cuuint64_t>(qdec::kPageSize) * qdec::kHeadDim * 2;
+    const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(qdec::kPageSize), 2, 2,
+                                static_cast<cuuint64_t>(s->num_pages) * 2 * s->num_kv_heads};
+    const cuuint64_t strides[4] = {qdec::kHeadDim * 2, 128,
+                                   static_cast<cuuint64_t>(s->num_kv_heads) * plane, plane};
+    const cuuint32_t box[5] = {64, static_cast<cuuint32_t>(qdec::kPageSize), 2, 2, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(pool), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

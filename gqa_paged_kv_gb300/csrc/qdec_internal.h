@@ -61,8 +61,8 @@ struct Params {
 };
 
 // Dynamic shared memory of the attention kernel for batch B, `stages` ring
-// slots and the given layout.
-size_t attention_smem_bytes(int B, int stages, bool cluster);
+// slots and the given layout (cluster = 0: flat; C > 0: C-CTA clusters).
+size_t attention_smem_bytes(int B, int stages, int cluster);
 
 // Clusters of `cluster` CTAs (each with `smem` bytes of dynamic shared
 // memory) that can be resident at once on the current device (0 if unknown).

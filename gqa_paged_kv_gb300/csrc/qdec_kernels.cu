@@ -42,6 +42,8 @@
 
 #include <math.h>
 
+#include <mutex>
+
 namespace qdec {
 namespace {
 
@@ -69,22 +71,29 @@ constexpr int kOffMisc = kOffSlotOk + kMaxStages * 4;            // abort, last,
 constexpr int kOffPbuf = kOffMisc + 8 * 4;                       // bf16 [warps][8][16]
 constexpr int kOffMs = kOffPbuf + kConsumerWarps * 8 * 16 * 2;   // float [warps][G]
 constexpr int kOffLs = kOffMs + kConsumerWarps * kGroup * 4;     // float [warps][G]
-constexpr int kOffOs = kOffLs + kConsumerWarps * kGroup * 4;     // float [warps][G][D]
+constexpr int kOffOs = kOffLs + kConsumerWarps * kGroup * 4;     // see below
+constexpr int kOsBytes = kConsumerWarps * kGroup * kHeadDim * 4;  // float [warps][G][D]
 constexpr int kPartStride = kHeadDim + 4;                        // num[D], M, den, pad
-// flat layout: int pre[B+1], sl[B] follow os; cluster layout: a receive
-// buffer float [C][G][D+4] for the peers' pieces comes first
-constexpr int kOffRecv = kOffOs + kConsumerWarps * kGroup * kHeadDim * 4;
-constexpr int kRecvBytes = kMaxCluster * kGroup * kPartStride * 4;
+constexpr int kRecvSlotBytes = kGroup * kPartStride * 4;         // one peer's piece
 static_assert(kOffKvNew % 16 == 0 && kOffRope % 16 == 0 && kOffBar % 8 == 0 &&
-              kOffOs % 16 == 0 && kOffRecv % 16 == 0 && kOffPbuf % 4 == 0, "smem alignment");
+              kOffOs % 16 == 0 && kOffPbuf % 4 == 0 && kRecvSlotBytes % 16 == 0,
+              "smem alignment");
+static_assert(kOsBytes <= kTileBytes, "the warp-combine scratch fits in one ring slot");
 
-__host__ __device__ constexpr int pre_offset(bool cluster) {
-    return kOffRecv + (cluster ? kRecvBytes : 0);
+// From kOffOs on, the two layouts differ:
+//   flat (C = 0):  os[warps][G][D] (the warp combine of each piece), then
+//                  int pre[B+1], sl[B], then the ring;
+//   cluster (C):   the receive buffer float [C-1][G][D+4] for the peers'
+//                  pieces, then the ring.  One piece per CTA, so the warp
+//                  combine runs once the ring has drained and uses ring
+//                  slot 0 as its scratch.
+__host__ __device__ constexpr int pre_offset(int C) {
+    return kOffOs + (C == 0 ? kOsBytes : (C - 1) * kRecvSlotBytes);
 }
-// the ring starts at the first 1024-byte boundary after the prefix arrays
-// (128-byte swizzle atoms); +1024 for aligning the dynamic base itself
-__host__ __device__ constexpr int ring_offset(int B, bool cluster) {
-    return (pre_offset(cluster) + 4 * (2 * B + 1) + 1023) / 1024 * 1024;
+// the ring starts at a 1024-byte boundary (128-byte swizzle atoms); the
+// dynamic base itself is aligned with 1024 bytes of slack
+__host__ __device__ constexpr int ring_offset(int B, int C) {
+    return (pre_offset(C) + (C == 0 ? 4 * (2 * B + 1) : 0) + 1023) / 1024 * 1024;
 }
 
 // ------------------------------------------------------------ PTX helpers --
@@ -132,12 +141,16 @@ __device__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int *a
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar) {
+// One whole page tile: the K and V planes of one (page, KV head), 8 KiB,
+// landing as [plane][half of D][token][64 dims] in 128-byte swizzled rows.
+// The pool's tensor map is 5-D (dims, token, half, plane, page*2*Hkv + head);
+// only the last coordinate varies.
+__device__ __forceinline__ void tma_load_tile(uint32_t dst, const CUtensorMap *map, int plane_row,
+                                              uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %2, %2, %2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(plane_row), "r"(bar)
         : "memory");
 }
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
@@ -767,12 +780,12 @@ struct PieceResult {
     float M, den;
     float4 num;
 };
-__device__ PieceResult combine_warps(WarpState &st, uint8_t *sm) {
+// `os` is the scratch for the warps' accumulators (kOsBytes).
+__device__ PieceResult combine_warps(WarpState &st, uint8_t *sm, float *os) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tg = lane >> 2, c = lane & 3;
     float *ms = reinterpret_cast<float *>(sm + kOffMs);
     float *ls = reinterpret_cast<float *>(sm + kOffLs);
-    float *os = reinterpret_cast<float *>(sm + kOffOs);
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
         st.lA += __shfl_xor_sync(kFull, st.lA, o);
@@ -896,12 +909,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (p.pdl && tid == 0) launch_dependents();
 
-    uint8_t *ring = sm + ring_offset(p.B, kCluster);
+    uint8_t *ring = sm + ring_offset(p.B, kCluster ? p.cluster : 0);
     const uint32_t full0 = smem_u32(sm + kOffBar);
     const uint32_t empty0 = full0 + kMaxStages * 8;
     volatile int *slot_ok = reinterpret_cast<volatile int *>(sm + kOffSlotOk);
     volatile int *misc = reinterpret_cast<volatile int *>(sm + kOffMisc);  // 0 abort, 1 last, 2 issued
-    int *pre = reinterpret_cast<int *>(sm + pre_offset(kCluster));
+    int *pre = reinterpret_cast<int *>(sm + pre_offset(kCluster ? p.cluster : 0));
     int *sl = pre + p.B + 1;
     const int NS = p.stages;
     // Ring slot s is always consumed by warp s % 4 only when NS is a multiple
@@ -1002,13 +1015,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     } else if (pj >= 0 && pj < p.num_pages && gj >= 0 && gj < p.Hkv) {
                         slot_ok[slot] = 1;
                         mbar_arrive_expect_tx(full, kTileBytes);
-                        const int yk = (pj * 2 * p.Hkv + gj) * kPageSize;
-                        const int yv = yk + p.Hkv * kPageSize;
-                        const uint32_t dst = smem_u32(ring + slot * kTileBytes);
-                        tma_load_2d(dst, &kv_map, 0, yk, full);
-                        tma_load_2d(dst + kTileHalfBytes, &kv_map, 64, yk, full);
-                        tma_load_2d(dst + kPlaneBytes, &kv_map, 0, yv, full);
-                        tma_load_2d(dst + kPlaneBytes + kTileHalfBytes, &kv_map, 64, yv, full);
+                        tma_load_tile(smem_u32(ring + slot * kTileBytes), &kv_map,
+                                      pj * 2 * p.Hkv + gj, full);
                     } else {
                         slot_ok[slot] = 0;
                         flag_error(p.err, QDEC_FLAG_BAD_PAGE);
@@ -1038,7 +1046,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             reset_state(st);
             process_piece<kFused>(p, sm, ring, full0, empty0, slot_ok, misc, b, g, w.pg, cnt, sl[b],
                                   n, i, st);
-            const PieceResult r = combine_warps(st, sm);
+            const PieceResult r = combine_warps(st, sm, reinterpret_cast<float *>(sm + kOffOs));
             const long long seg0 = static_cast<long long>(p.Hkv) * pre[b] + static_cast<long long>(g) * n;
             const int j0 = cta_of(seg0, W, G);
             const int np = cta_of(seg0 + n - 1, W, G) - j0 + 1;
@@ -1062,26 +1070,38 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (cnt > 0)
             process_piece<kFused>(p, sm, ring, full0, empty0, slot_ok, misc, cb, cg, pg_lo, cnt, cL,
                                   cn, i, st);
-        PieceResult r = combine_warps(st, sm);
-        // push this CTA's piece into slot `crank` of rank 0's receive buffer
+        // every tile has been consumed (so no copy is landing in the ring)
+        // before ring slot 0 becomes the combine scratch
+        consumer_sync();
+        PieceResult r = combine_warps(st, sm, reinterpret_cast<float *>(ring));
+        // a peer pushes its piece into slot crank - 1 of rank 0's receive
+        // buffer; rank 0 keeps its own in registers
         cluster_wait();
         const int h = tid >> 5, d0 = (tid & 31) * 4;
-        float *recv = reinterpret_cast<float *>(sm + kOffRecv);
-        float *dst = cluster_peer(recv, 0) + (crank * kGroup + h) * kPartStride;
-        *reinterpret_cast<float4 *>(dst + d0) = r.num;
-        if ((tid & 31) == 0) {
-            dst[kHeadDim] = r.M;
-            dst[kHeadDim + 1] = r.den;
+        float *recv = reinterpret_cast<float *>(sm + kOffOs);
+        if (crank > 0) {
+            float *dst = cluster_peer(recv, 0) + ((crank - 1) * kGroup + h) * kPartStride;
+            *reinterpret_cast<float4 *>(dst + d0) = r.num;
+            if ((tid & 31) == 0) {
+                dst[kHeadDim] = r.M;
+                dst[kHeadDim + 1] = r.den;
+            }
         }
         cluster_sync_all();
         if (crank == 0) {
             PieceResult m;
-            m.M = kNegInf;
-            for (int q = 0; q < C; ++q) m.M = fmaxf(m.M, recv[(q * kGroup + h) * kPartStride + kHeadDim]);
+            m.M = r.M;
+            for (int q = 0; q + 1 < C; ++q)
+                m.M = fmaxf(m.M, recv[(q * kGroup + h) * kPartStride + kHeadDim]);
             m.den = 0.f;
             m.num = make_float4(0.f, 0.f, 0.f, 0.f);
             if (m.M != kNegInf) {
-                for (int q = 0; q < C; ++q) {
+                if (r.M != kNegInf) {
+                    const float e = exp2f(r.M - m.M);
+                    m.den = e * r.den;
+                    m.num = make_float4(e * r.num.x, e * r.num.y, e * r.num.z, e * r.num.w);
+                }
+                for (int q = 0; q + 1 < C; ++q) {
                     const float *pp = recv + (q * kGroup + h) * kPartStride;
                     const float mq = pp[kHeadDim];
                     const float e = mq == kNegInf ? 0.f : exp2f(mq - m.M);
@@ -1157,19 +1177,31 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Para
     merge_pieces(p, static_cast<int64_t>(sigma) + j0, b, g, np);
 }
 
+// Largest dynamic shared memory each attention kernel variant has been
+// allowed on each device.  The attribute only ever grows: a launch (or an
+// occupancy query) that needs less leaves it as it is, so a later launch
+// that needs more than a smaller request in between still finds it set.
+std::mutex g_smem_mu;
 size_t g_smem_attr[4][64];
+
+template <bool kFused, bool kCluster>
+cudaError_t allow_smem(int dev, size_t smem) {
+    std::lock_guard<std::mutex> lock(g_smem_mu);
+    size_t &attr = g_smem_attr[(kFused ? 2 : 0) + (kCluster ? 1 : 0)][dev];
+    if (attr >= smem) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(attention_kernel<kFused, kCluster>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+    if (e == cudaSuccess) attr = smem;
+    return e;
+}
 
 template <bool kFused, bool kCluster>
 cudaError_t launch_one(const Params &p, const CUtensorMap &kv_map, size_t smem, int dev,
                        cudaStream_t s) {
     auto kern = attention_kernel<kFused, kCluster>;
-    size_t &attr = g_smem_attr[(kFused ? 2 : 0) + (kCluster ? 1 : 0)][dev];
-    if (attr < smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        attr = smem;
-    }
+    const cudaError_t e = allow_smem<kFused, kCluster>(dev, smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid);
     cfg.blockDim = dim3(kThreads);
@@ -1196,7 +1228,7 @@ cudaError_t launch_one(const Params &p, const CUtensorMap &kv_map, size_t smem, 
 
 }  // namespace
 
-size_t attention_smem_bytes(int B, int stages, bool cluster) {
+size_t attention_smem_bytes(int B, int stages, int cluster) {
     return static_cast<size_t>(ring_offset(B, cluster)) + static_cast<size_t>(stages) * kTileBytes +
            1024;
 }
@@ -1209,11 +1241,7 @@ static int current_device() {
 
 int max_active_clusters(int cluster, size_t smem) {
     auto kern = attention_kernel<true, true>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-        return 0;
-    const int dev = current_device();
-    if (g_smem_attr[3][dev] < smem) g_smem_attr[3][dev] = smem;
+    if (allow_smem<true, true>(current_device(), smem) != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cluster * 64);
     cfg.blockDim = dim3(kThreads);
@@ -1232,7 +1260,7 @@ int max_active_clusters(int cluster, size_t smem) {
 
 cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, bool fused,
                              cudaStream_t s) {
-    const size_t smem = attention_smem_bytes(p.B, p.stages, p.cluster != 0);
+    const size_t smem = attention_smem_bytes(p.B, p.stages, p.cluster);
     const int dev = current_device();
     if (fused)
         return p.cluster ? launch_one<true, true>(p, kv_map, smem, dev, s)

@@ -201,3 +201,36 @@ def test_workload_5_sampled():
     seqs = sorted(set([int(order[0]), int(order[1]), int(order[-1]), int(order[-2]),
                        int(order[len(order) // 2]), 0, 63]))
     _check_layers(w, [0, 35], seqs)
+
+
+_SHAPE_SWITCH = r"""
+import sys, torch
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+from gqa_paged_kv_gb300 import workloads as wl
+import parity
+
+def make(lens, seed):
+    pages = sum((l + 15) // 16 for l in lens) + 9
+    return wl.build(wl.custom(len(lens), lens, pool_pages=pages, seed=seed), "cuda")
+
+big = parity.Runner(make([100] * 32, 31))    # 32 sequences: larger shared-memory layout
+big.step(0); big.check_flags()
+first = big.out[0].clone()
+small = parity.Runner(make([20, 21], 32))    # first use of a smaller layout in this process
+small.step(0); small.check_flags()
+big.step(0); big.check_flags()               # the larger layout again
+assert torch.equal(first, big.out[0])
+print("ok")
+"""
+
+
+def test_shapes_with_different_shared_memory_alternate():
+    """A shape whose launch needs more shared memory still launches after a
+    shape needing less was planned for the first time in between."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = _SHAPE_SWITCH.format(root=os.path.dirname(here), tests=here)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
