@@ -49,7 +49,12 @@ KERNEL_SOURCES = ("gqa_paged_kv_gb300/csrc/qdec_kernels.cu", "gqa_paged_kv_gb300
 # DRAM bytes per launch of the fused kernel measured with ncu (see
 # profiles/), keyed by workload; used only while the kernel source hash
 # still matches the one the counters were taken on.
-TRAFFIC = {}
+TRAFFIC = {
+    "b8-ctx256to384-36layer": {"kernel_sha": "8fb4f96fb7bf12e9", "bytes_per_launch": 10900352},
+    "b1-ctx8192-spikes-36layer": {"kernel_sha": "8fb4f96fb7bf12e9", "bytes_per_launch": 33632128},
+    "b64-ragged128to16384-sharedpool-36layer": {"kernel_sha": "8fb4f96fb7bf12e9",
+                                                "bytes_per_launch": 1036990000},
+}
 
 # The CPU timings sample the first few layers of a workload (same shapes and
 # lengths; fewer per-layer pools to materialise in host memory).
