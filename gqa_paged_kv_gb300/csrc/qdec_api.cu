@@ -7,6 +7,8 @@
 #include "qdec.h"
 
 #include <math.h>
+
+#include <algorithm>
 #include <mutex>
 
 namespace {
@@ -148,8 +150,17 @@ int64_t cluster_capacity(const qdec_shape *s, int c, int cap) {
 
 // allow_cluster = false for the three-call path, whose merge kernel reads
 // the flat layout.  num_ctas > 0 forces the flat layout on that grid.
-// Cluster layout: the fewest tiles per CTA T whose grid still fits on the
-// device in one wave (a second wave would double the latency).
+//
+// Cluster layout: each (sequence, KV head) is cut into K chunks of C CTAs.
+// Chunks meet through the workspace (a fence, an atomic and a second pass:
+// the costly merge), CTAs of a cluster through distributed shared memory.
+// So the fewest chunks K that still give enough CTAs to stream the pages:
+// about kBytesPerCta each, or 60% of the resident CTAs, whichever is fewer
+// (a smaller grid also leaves room for the next launch to start early).  For
+// that K the largest cluster that fits on the device in one wave.
+constexpr double kBytesPerCta = 96.0 * 1024;
+constexpr double kGridShare = 0.6;
+
 Plan plan_for(const qdec_shape *s, bool allow_cluster) {
     int sms = sm_count_of_current_device();
     if (sms <= 0) sms = 1;
@@ -160,22 +171,29 @@ Plan plan_for(const qdec_shape *s, bool allow_cluster) {
     const int64_t segs = static_cast<int64_t>(s->batch) * s->num_kv_heads;
     const int64_t nmax = (s->max_seq_len + qdec::kPageSize - 1) / qdec::kPageSize;
     if (s->num_ctas == 0 && allow_cluster && per_cta < kFlatMinTilesPerCta) {
-        // T = tiles per CTA; a segment of nmax tiles gets C = ceil(nmax/T) CTAs
-        // (at most a portable cluster) per chunk and K = ceil(nmax/(C*T)) chunks
-        for (int64_t t = per_cta < 1 ? 1 : per_cta; t <= nmax && t < kFlatMinTilesPerCta; ++t) {
-            int64_t c = (nmax + t - 1) / t;
-            if (c > qdec::kMaxCluster) c = qdec::kMaxCluster;
-            const int cap = ring_cap(s, static_cast<int>(c));
-            const int64_t chunks = (nmax + c * t - 1) / (c * t);
-            const int64_t grid = c * segs * chunks;
-            if (grid <= cluster_capacity(s, static_cast<int>(c), cap)) {
-                pl.cluster = static_cast<int>(c);
-                pl.chunks = static_cast<int>(chunks);
-                pl.grid = static_cast<int>(grid);
-                pl.stages = clamp_stages(t + 1, cap);
-                return pl;
+        const double bytes = static_cast<double>(wmax) * qdec::kTileBytes;
+        const double want = std::min(kGridShare * static_cast<double>(target), bytes / kBytesPerCta);
+        Plan widest{};
+        for (int64_t k = 1; k <= nmax && pl.grid == 0; ++k) {
+            if (segs * k > target) break;  // not even one CTA per chunk fits
+            for (int c = qdec::kMaxCluster; c >= 1; --c) {
+                if (c * k > nmax && c > 1) continue;  // every CTA gets a page
+                const int64_t t = (nmax + c * k - 1) / (c * k);
+                const int64_t grid = c * segs * k;
+                const int cap = ring_cap(s, c);
+                if (grid > cluster_capacity(s, c, cap)) continue;
+                Plan cand{};
+                cand.cluster = c;
+                cand.chunks = static_cast<int>(k);
+                cand.grid = static_cast<int>(grid);
+                cand.stages = clamp_stages(t + 1, cap);
+                if (grid > widest.grid) widest = cand;
+                if (static_cast<double>(grid) >= want) pl = cand;
+                break;  // the largest cluster that fits, for this k
             }
         }
+        if (pl.grid == 0 && widest.grid > 0 && per_cta < kFlatMinTilesPerCta / 2) pl = widest;
+        if (pl.grid > 0) return pl;
     }
     const int64_t g = s->num_ctas > 0 ? s->num_ctas : (target < wmax ? target : wmax);
     pl.grid = static_cast<int>(g);

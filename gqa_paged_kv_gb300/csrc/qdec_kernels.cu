@@ -68,6 +68,7 @@ constexpr int kPrologueBytes = kOffRope + kRotPairs * 16;
 constexpr int kOffBar = kPrologueBytes;                          // full[S], empty[S]
 constexpr int kOffSlotOk = kOffBar + 2 * kMaxStages * 8;
 constexpr int kOffMisc = kOffSlotOk + kMaxStages * 4;            // abort, last, issued
+constexpr int kOffKvReady = kOffMisc + 16;                       // mbarrier: new key/value ready
 constexpr int kOffPbuf = kOffMisc + 8 * 4;                       // bf16 [warps][8][16]
 constexpr int kOffMs = kOffPbuf + kConsumerWarps * 8 * 16 * 2;   // float [warps][G]
 constexpr int kOffLs = kOffMs + kConsumerWarps * kGroup * 4;     // float [warps][G]
@@ -79,16 +80,24 @@ static_assert(kOffKvNew % 16 == 0 && kOffRope % 16 == 0 && kOffBar % 8 == 0 &&
               kOffOs % 16 == 0 && kOffPbuf % 4 == 0 && kRecvSlotBytes % 16 == 0,
               "smem alignment");
 static_assert(kOsBytes <= kTileBytes, "the warp-combine scratch fits in one ring slot");
+static_assert(kTileBytes + (kMaxCluster - 1) * kRecvSlotBytes <= 4 * kTileBytes,
+              "the receive buffer fits in ring slots 1..3");
 
-// From kOffOs on, the two layouts differ:
-//   flat (C = 0):  os[warps][G][D] (the warp combine of each piece), then
-//                  int pre[B+1], sl[B], then the ring;
-//   cluster (C):   the receive buffer float [C-1][G][D+4] for the peers'
-//                  pieces, then the ring.  One piece per CTA, so the warp
-//                  combine runs once the ring has drained and uses ring
-//                  slot 0 as its scratch.
+// From kOffOs on, the layouts differ:
+//   flat (C = 0):   os[warps][G][D] (the warp combine of each piece), then
+//                   int pre[B+1], sl[B], then the ring;
+//   cluster, C <= kMaxDirectRecv:  the receive buffer float [C-1][G][D+4]
+//                   for the peers' pieces, then the ring;
+//   cluster, larger C: the ring right away; rank 0 receives in its drained
+//                   ring from slot 1 on (peers push only after rank 0 has
+//                   arrived on the cluster barrier with its tiles consumed).
+// In both cluster layouts one piece per CTA, so once the ring has drained
+// slot 0 is the warp-combine scratch.  kMaxDirectRecv is the largest C whose
+// receive buffer still leaves room for a 12-slot ring at 2 CTAs per SM.
+constexpr int kMaxDirectRecv = 6;
+__host__ __device__ constexpr bool ring_receives(int C) { return C > kMaxDirectRecv; }
 __host__ __device__ constexpr int pre_offset(int C) {
-    return kOffOs + (C == 0 ? kOsBytes : (C - 1) * kRecvSlotBytes);
+    return kOffOs + (C == 0 ? kOsBytes : ring_receives(C) ? 0 : (C - 1) * kRecvSlotBytes);
 }
 // the ring starts at a 1024-byte boundary (128-byte swizzle atoms); the
 // dynamic base itself is aligned with 1024 bytes of slack
@@ -416,43 +425,79 @@ __device__ void key_row(const Params &p, __nv_bfloat162 ka, __nv_bfloat162 kc, _
     kb[3] = ff_to_bf16(ff_add(ff_mul(xh[3], c1), ff_mul(xh[1], s1)));
 }
 
-// The new-token rows of (sequence b, KV head g), on the 128 consumer threads:
-// warp w norms and rotates query row 4g + w in fp32; when need_k, warp 0 also
-// produces the key row (float-float) and appends key and value.  Lane l
-// holds dims 2l, 2l+1, 64+2l, 65+2l: both members of two rotate-half pairs.
+// The new key/value row of (sequence b, KV head g), on one warp: lane l holds
+// dims 2l, 2l+1, 64+2l, 65+2l.  bf16(k_rot) (float-float norm and rotation,
+// one rounding) and v go to kv_new in shared memory and to the pool slot of
+// token L-1.
+__device__ void key_value_row(const Params &p, int b, int g, int L, uint8_t *sm) {
+    const int lane = threadIdx.x & 31;
+    const __nv_bfloat16 *krow = p.k + b * p.k_stride + static_cast<int64_t>(g) * kHeadDim;
+    const __nv_bfloat16 *vrow = p.v + b * p.v_stride + static_cast<int64_t>(g) * kHeadDim;
+    const __nv_bfloat162 ka = reinterpret_cast<const __nv_bfloat162 *>(krow)[lane];
+    const __nv_bfloat162 kc = reinterpret_cast<const __nv_bfloat162 *>(krow + 64)[lane];
+    const __nv_bfloat162 wka = reinterpret_cast<const __nv_bfloat162 *>(p.w_k)[lane];
+    const __nv_bfloat162 wkc = reinterpret_cast<const __nv_bfloat162 *>(p.w_k + 64)[lane];
+    const uint32_t va = reinterpret_cast<const uint32_t *>(vrow)[lane];
+    const uint32_t vc = reinterpret_cast<const uint32_t *>(vrow + 64)[lane];
+    const int page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + (L - 1) / kPageSize];
+    RopeEntry e0, e1;
+    if (p.rope) {
+        const RopeEntry *rope = p.rope + static_cast<int64_t>(b) * kRotPairs;
+        e0 = rope[2 * lane];
+        e1 = rope[2 * lane + 1];
+    } else {
+        const int pos = p.positions[b];
+        e0 = rope_entry(pos, p.inv_freq[2 * lane], true);
+        e1 = rope_entry(pos, p.inv_freq[2 * lane + 1], true);
+    }
+    __nv_bfloat16 kb[4];
+    key_row(p, ka, kc, wka, wkc, e0, e1, kb);
+    const uint32_t k0 = pack_bf16(kb[0], kb[1]), k1 = pack_bf16(kb[2], kb[3]);
+    uint32_t *kv_new = reinterpret_cast<uint32_t *>(sm + kOffKvNew);
+    kv_new[lane] = k0;
+    kv_new[32 + lane] = k1;
+    kv_new[64 + lane] = va;
+    kv_new[96 + lane] = vc;
+    const int slot = L - 1;
+    if (page >= 0 && page < p.num_pages) {
+        const int64_t row =
+            ((static_cast<int64_t>(page) * 2 * p.Hkv + g) * kPageSize + slot % kPageSize) *
+            kHeadDim;
+        uint32_t *kdst = reinterpret_cast<uint32_t *>(p.pool + row);
+        uint32_t *vdst =
+            reinterpret_cast<uint32_t *>(p.pool + row + static_cast<int64_t>(p.Hkv) * kPageSize * kHeadDim);
+        kdst[lane] = k0;
+        kdst[32 + lane] = k1;
+        vdst[lane] = va;
+        vdst[32 + lane] = vc;
+    } else if (lane == 0) {
+        flag_error(p.err, QDEC_FLAG_BAD_PAGE);
+    }
+}
+
+// Bounds of the new-token work of (sequence b, KV head g) with L tokens.
+__device__ __forceinline__ bool new_token_in_bounds(const Params &p, int b, int g, int L) {
+    return in_bounds(p, b >= 0 && b < p.B && g >= 0 && g < p.Hkv && L >= 1 &&
+                            (L - 1) / kPageSize < p.max_blocks);
+}
+
+// The new-token query rows of (sequence b, KV head g), on the 128 consumer
+// threads: warp w norms and rotates query row 4g + w in fp32.  Lane l holds
+// dims 2l, 2l+1, 64+2l, 65+2l: both members of two rotate-half pairs.  With
+// need_k, warp 0 then also produces and appends the key/value row.
 //
 // Q_OUT = 0: scaled bf16 hi/lo operand rows into shared memory (qb);
 // Q_OUT = 1: fp32 rows to p.q_rot_out (unscaled).
-// kv_new receives bf16(k_rot) and v; the pool slot (b, L-1) receives both.
 template <int Q_OUT>
 __device__ void new_token_rows(const Params &p, int b, int g, int L, bool need_k, uint8_t *sm) {
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
-    // warp 0 fetches the key/value rows and the slot's page up front, so
-    // their latency overlaps the query work
-    if (!in_bounds(p, b >= 0 && b < p.B && g >= 0 && g < p.Hkv && L >= 1 &&
-                          (L - 1) / kPageSize < p.max_blocks))
-        return;  // uniform over the CTA
-    const bool do_k = need_k && w == 0;
-    __nv_bfloat162 ka{}, kc{}, wka{}, wkc{};
-    uint32_t va = 0, vc = 0;
-    int page = -1;
-    if (do_k) {
-        const __nv_bfloat16 *krow = p.k + b * p.k_stride + static_cast<int64_t>(g) * kHeadDim;
-        const __nv_bfloat16 *vrow = p.v + b * p.v_stride + static_cast<int64_t>(g) * kHeadDim;
-        ka = reinterpret_cast<const __nv_bfloat162 *>(krow)[lane];
-        kc = reinterpret_cast<const __nv_bfloat162 *>(krow + 64)[lane];
-        wka = reinterpret_cast<const __nv_bfloat162 *>(p.w_k)[lane];
-        wkc = reinterpret_cast<const __nv_bfloat162 *>(p.w_k + 64)[lane];
-        va = reinterpret_cast<const uint32_t *>(vrow)[lane];
-        vc = reinterpret_cast<const uint32_t *>(vrow + 64)[lane];
-        page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + (L - 1) / kPageSize];
-    }
+    if (!new_token_in_bounds(p, b, g, L)) return;  // uniform over the CTA
     const RopeEntry *rope;
     if (p.rope) {
         rope = p.rope + static_cast<int64_t>(b) * kRotPairs;
     } else {
         RopeEntry *rs = reinterpret_cast<RopeEntry *>(sm + kOffRope);
-        if (t < kRotPairs) rs[t] = rope_entry(p.positions[b], p.inv_freq[t], need_k);
+        if (t < kRotPairs) rs[t] = rope_entry(p.positions[b], p.inv_freq[t], false);
         consumer_sync();
         rope = rs;
     }
@@ -495,31 +540,7 @@ __device__ void new_token_rows(const Params &p, int b, int g, int L, bool need_k
         reinterpret_cast<float2 *>(dst)[lane] = make_float2(y0, y1);
         reinterpret_cast<float2 *>(dst + 64)[lane] = make_float2(y2, y3);
     }
-
-    if (!do_k) return;
-    __nv_bfloat16 kb[4];
-    key_row(p, ka, kc, wka, wkc, e0, e1, kb);
-    const uint32_t k0 = pack_bf16(kb[0], kb[1]), k1 = pack_bf16(kb[2], kb[3]);
-    uint32_t *kv_new = reinterpret_cast<uint32_t *>(sm + kOffKvNew);
-    kv_new[lane] = k0;
-    kv_new[32 + lane] = k1;
-    kv_new[64 + lane] = va;
-    kv_new[96 + lane] = vc;
-    const int slot = L - 1;
-    if (page >= 0 && page < p.num_pages) {
-        const int64_t row =
-            ((static_cast<int64_t>(page) * 2 * p.Hkv + g) * kPageSize + slot % kPageSize) *
-            kHeadDim;
-        uint32_t *kdst = reinterpret_cast<uint32_t *>(p.pool + row);
-        uint32_t *vdst =
-            reinterpret_cast<uint32_t *>(p.pool + row + static_cast<int64_t>(p.Hkv) * kPageSize * kHeadDim);
-        kdst[lane] = k0;
-        kdst[32 + lane] = k1;
-        vdst[lane] = va;
-        vdst[32 + lane] = vc;
-    } else if (lane == 0) {
-        flag_error(p.err, QDEC_FLAG_BAD_PAGE);
-    }
+    if (need_k && w == 0) key_value_row(p, b, g, L, sm);
 }
 
 // ----------------------------------------------------------- tile math --
@@ -702,11 +723,17 @@ __device__ void merge_pieces(const Params &p, int64_t pid0, int b, int g, int np
 // prologue (the group's query rows as MMA operands; with has_last also the
 // new key/value), then the tiles, round-robin over the 4 warps by the CTA's
 // running tile counter i (shared with the producer).
+//
+// The new key/value (piece holding the segment's last page) is computed after
+// the query rows by warp (i + cnt) % 4, which has the fewest tiles of the
+// piece and never the last one; it arrives on the kv-ready barrier (phase =
+// kv_uses, the number of such pieces before in this CTA) and the warp that
+// patches the last page waits for it.
 template <bool kFused>
 __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint32_t full0,
                               uint32_t empty0, volatile int *slot_ok, volatile int *misc, int b,
                               int g, int pg0, int cnt, int L, int n, uint32_t &i,
-                              WarpState &st) {
+                              WarpState &st, int &kv_uses) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tg = lane >> 2, c = lane & 3;
     const int NS = p.stages;
@@ -716,7 +743,7 @@ __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint3
     const bool has_last = pg0 + cnt == n;
 
     if (kFused) {
-        new_token_rows<0>(p, b, g, L, has_last, sm);
+        new_token_rows<0>(p, b, g, L, false, sm);
     } else {
         const float *src =
             p.q_rot_in + (static_cast<int64_t>(b) * p.Hq + g * kGroup + warp) * kHeadDim;
@@ -744,6 +771,16 @@ __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint3
         qf[j][0] = *reinterpret_cast<const uint32_t *>(row);
         qf[j][1] = *reinterpret_cast<const uint32_t *>(row + 8);
     }
+    const uint32_t kv_bar = smem_u32(sm + kOffKvReady);
+    const uint32_t kv_parity = static_cast<uint32_t>(kv_uses) & 1;
+    if (kFused && has_last) {
+        if (warp == static_cast<int>((i + cnt) & 3)) {
+            if (new_token_in_bounds(p, b, g, L)) key_value_row(p, b, g, L, sm);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(kv_bar);
+        }
+        ++kv_uses;
+    }
     for (int k = 0; k < cnt; ++k, ++i) {
         if (static_cast<int>(i & 3) != warp) continue;
         const int slot = i % NS;
@@ -756,7 +793,14 @@ __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint3
         const int ntok = min(kPageSize, L - pg * kPageSize);
         if (ok && slot_ok[slot]) {
             uint8_t *tile = ring + slot * kTileBytes;
-            const bool patch = kFused && pg == n - 1;
+            bool patch = kFused && pg == n - 1;
+            if (patch && !mbar_wait_bounded(kv_bar, kv_parity, misc)) {
+                if (lane == 0) {
+                    misc[0] = 1;
+                    flag_error(p.err, QDEC_FLAG_TIMEOUT);
+                }
+                patch = false;
+            }
             if (patch || ntok < kPageSize) fix_tile(tile, ntok, patch, kv_new, lane);
             const uint32_t ks = smem_u32(tile);
             tile_math(ks, ks + kPlaneBytes, qf, ntok, lane, st, pbuf);
@@ -883,6 +927,9 @@ __device__ void store_partial(const Params &p, volatile int *misc, int64_t pid, 
 __device__ __forceinline__ void cluster_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
 }
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
@@ -931,6 +978,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
+        mbar_init(smem_u32(sm + kOffKvReady), 1);
         misc[0] = 0;
         misc[1] = 0;
         misc[2] = 0;
@@ -963,9 +1011,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         pg_hi = c0 + (crank + 1) * (c1 - c0) / C;
         __syncthreads();  // barrier initialisation
         // first cluster phase: every CTA has started (its shared memory may be
-        // written by peers once this phase completes); waited for before the
-        // push below, by which time it has long completed
-        cluster_arrive_relaxed();
+        // written by peers once this phase completes).  When rank 0 receives
+        // in its ring, the phase also means rank 0 has drained the ring, so
+        // rank 0's threads arrive only once they are done with it.
+        if (crank != 0 || !ring_receives(C)) cluster_arrive_relaxed();
     } else {
         if (warp == kConsumerWarps) build_prefix(p, pre, sl, blockIdx.x == 0);
         __syncthreads();
@@ -1029,6 +1078,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         if (lane == 0) misc[2] = static_cast<int>(i);
         if (kCluster) {  // the producer warp takes part in both cluster phases
+            if (crank == 0 && ring_receives(p.cluster)) cluster_arrive_release();
             cluster_wait();
             cluster_sync_all();
         }
@@ -1038,6 +1088,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         Walk w;
         walk_start(w, pre, p.B, p.Hkv, lo, hi);
         uint32_t i = 0;
+        int kv_uses = 0;
         while (w.f < w.hi) {
             const int cnt = piece_len(w, pre);
             const int b = w.b, g = w.g;
@@ -1045,7 +1096,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             WarpState st;
             reset_state(st);
             process_piece<kFused>(p, sm, ring, full0, empty0, slot_ok, misc, b, g, w.pg, cnt, sl[b],
-                                  n, i, st);
+                                  n, i, st, kv_uses);
             const PieceResult r = combine_warps(st, sm, reinterpret_cast<float *>(sm + kOffOs));
             const long long seg0 = static_cast<long long>(p.Hkv) * pre[b] + static_cast<long long>(g) * n;
             const int j0 = cta_of(seg0, W, G);
@@ -1067,18 +1118,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         WarpState st;
         reset_state(st);
         uint32_t i = 0;
+        int kv_uses = 0;
         if (cnt > 0)
             process_piece<kFused>(p, sm, ring, full0, empty0, slot_ok, misc, cb, cg, pg_lo, cnt, cL,
-                                  cn, i, st);
+                                  cn, i, st, kv_uses);
         // every tile has been consumed (so no copy is landing in the ring)
         // before ring slot 0 becomes the combine scratch
         consumer_sync();
         PieceResult r = combine_warps(st, sm, reinterpret_cast<float *>(ring));
         // a peer pushes its piece into slot crank - 1 of rank 0's receive
         // buffer; rank 0 keeps its own in registers
+        const bool in_ring = ring_receives(C);
+        if (crank == 0 && in_ring) cluster_arrive_release();
         cluster_wait();
         const int h = tid >> 5, d0 = (tid & 31) * 4;
-        float *recv = reinterpret_cast<float *>(sm + kOffOs);
+        float *recv = reinterpret_cast<float *>(in_ring ? ring + kTileBytes : sm + kOffOs);
         if (crank > 0) {
             float *dst = cluster_peer(recv, 0) + ((crank - 1) * kGroup + h) * kPartStride;
             *reinterpret_cast<float4 *>(dst + d0) = r.num;

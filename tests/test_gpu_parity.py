@@ -213,7 +213,7 @@ def make(lens, seed):
     pages = sum((l + 15) // 16 for l in lens) + 9
     return wl.build(wl.custom(len(lens), lens, pool_pages=pages, seed=seed), "cuda")
 
-big = parity.Runner(make([100] * 32, 31))    # 32 sequences: larger shared-memory layout
+big = parity.Runner(make([1056] * 6, 31))    # 6 x 66 pages: clusters of 3-6, 12-slot ring
 big.step(0); big.check_flags()
 first = big.out[0].clone()
 small = parity.Runner(make([20, 21], 32))    # first use of a smaller layout in this process
