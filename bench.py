@@ -90,15 +90,25 @@ def parse_args():
 
 # ------------------------------------------------------------------ infra --
 class Dist:
+    """One process per GPU (torchrun env vars).  The ranks run independent
+    replicas of the workload: the only communication is the barrier around
+    the timed region and the max of the elapsed times.  NCCL on GPUs, gloo
+    where there are none (the CPU tests of this path)."""
+
     def __init__(self):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
+        self.device = "cpu"
         if self.world > 1:
             import torch.distributed as dist
-            torch.cuda.set_device(self.local)
-            dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            if torch.cuda.is_available():
+                torch.cuda.set_device(self.local)
+                self.device = f"cuda:{self.local}"
+                dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            else:
+                dist.init_process_group("gloo")
             self.pg = dist
 
     def barrier(self):
@@ -108,7 +118,7 @@ class Dist:
     def max(self, x: float) -> float:
         if not self.pg:
             return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
 

@@ -40,7 +40,8 @@ qdec_status check_shape(const qdec_shape *s) {
         s->page_size < 1 || s->num_pages < 1 || s->max_blocks_per_seq < 1 ||
         s->max_seq_len < 1 || s->num_ctas < 0)
         return QDEC_ERR_INVALID_ARG;
-    if ((s->launch_flags & ~QDEC_LAUNCH_OVERLAP_PREVIOUS) != 0) return QDEC_ERR_INVALID_ARG;
+    if ((s->launch_flags & ~(QDEC_LAUNCH_OVERLAP_PREVIOUS | QDEC_LAUNCH_TEST_WITHHOLD_TILE)) != 0)
+        return QDEC_ERR_INVALID_ARG;
     if (!(s->rope_theta > 0.f) || !(s->eps >= 0.f) || !(s->sm_scale >= 0.f) ||
         !isfinite(s->rope_theta) || !isfinite(s->eps) || !isfinite(s->sm_scale))
         return QDEC_ERR_INVALID_ARG;
@@ -258,6 +259,8 @@ void fill_common(Params &p, const qdec_shape *s, bool allow_cluster) {
     p.cluster = pl.cluster;
     p.chunks = pl.chunks;
     p.pdl = (s->launch_flags & QDEC_LAUNCH_OVERLAP_PREVIOUS) != 0;
+    p.withhold_first = (s->launch_flags & QDEC_LAUNCH_TEST_WITHHOLD_TILE) != 0;
+    p.wait_cycles = p.withhold_first ? qdec::kTestWaitCycles : qdec::kWaitTimeoutCycles;
     fill_inv_freq(p.inv_freq, s->rope_theta);
 }
 

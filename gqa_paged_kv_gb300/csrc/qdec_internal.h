@@ -26,6 +26,11 @@ constexpr int kTileBytes = 2 * kPlaneBytes;                // K + V = 8 KiB
 constexpr int kCtasPerSm = 2;
 constexpr int kMaxCluster = 8;                             // portable cluster size
 
+// Budget of a bounded wait (SM cycles): ~2 s at the 2.07 GHz maximum clock;
+// ~10 ms under the withheld-tile test hook.
+constexpr long long kWaitTimeoutCycles = 4000000000ll;
+constexpr long long kTestWaitCycles = 20000000ll;
+
 // One RoPE angle of one sequence: cos and sin as unevaluated float pairs
 // (hi + lo), i.e. about 48 significant bits.
 struct RopeEntry {
@@ -57,6 +62,8 @@ struct Params {
     int cluster;             // 0: flat tile partition; C > 0: segment chunks on C-CTA clusters
     int chunks;              // cluster mode: chunks (clusters) per segment
     long long ws_pieces;     // partial slots the workspace holds (device bounds checks)
+    long long wait_cycles;   // budget of every bounded wait, in SM cycles
+    int withhold_first;      // test hook: CTA-local tile 0 is never copied (see qdec.h)
     double inv_freq[kRotPairs];  // rope_theta^(-2i/D), i < D/2
 };
 

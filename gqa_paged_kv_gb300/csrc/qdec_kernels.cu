@@ -49,7 +49,6 @@ namespace {
 
 constexpr float kNegInf = -INFINITY;
 constexpr float kRescaleThreshold = 8.0f;          // log2 units: p <= 2^8 between rescales
-constexpr long long kWaitTimeoutCycles = 4000000000ll;  // ~2 s at the 2.07 GHz max clock
 constexpr unsigned kFull = 0xffffffffu;
 
 // Cody-Waite split of 2*pi for the double-precision angle reduction.
@@ -138,13 +137,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // spins without bound.  The budget is counted with clock64(), which is
 // monotonic on the SM the thread runs on (the global nanosecond timer is
 // not: it can step backwards, which would end a wait at once).
-__device__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+__device__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                  long long budget = kWaitTimeoutCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitTimeoutCycles) return false;
+        if (clock64() - t0 > budget) return false;
     }
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -784,7 +784,7 @@ __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint3
     for (int k = 0; k < cnt; ++k, ++i) {
         if (static_cast<int>(i & 3) != warp) continue;
         const int slot = i % NS;
-        const bool ok = mbar_wait_bounded(full0 + 8 * slot, (i / NS) & 1, misc);
+        const bool ok = mbar_wait_bounded(full0 + 8 * slot, (i / NS) & 1, misc, p.wait_cycles);
         if (!ok && lane == 0) {
             misc[0] = 1;
             flag_error(p.err, QDEC_FLAG_TIMEOUT);
@@ -794,7 +794,7 @@ __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint3
         if (ok && slot_ok[slot]) {
             uint8_t *tile = ring + slot * kTileBytes;
             bool patch = kFused && pg == n - 1;
-            if (patch && !mbar_wait_bounded(kv_bar, kv_parity, misc)) {
+            if (patch && !mbar_wait_bounded(kv_bar, kv_parity, misc, p.wait_cycles)) {
                 if (lane == 0) {
                     misc[0] = 1;
                     flag_error(p.err, QDEC_FLAG_TIMEOUT);
@@ -1057,10 +1057,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     if (misc[0]) {
                         stop = true;  // another thread gave up: issue nothing more
                     } else if (i >= static_cast<uint32_t>(NS) &&
-                        !mbar_wait_bounded(empty0 + 8 * slot, ((i / NS) - 1) & 1, misc)) {
+                        !mbar_wait_bounded(empty0 + 8 * slot, ((i / NS) - 1) & 1, misc,
+                                           p.wait_cycles)) {
                         misc[0] = 1;
                         flag_error(p.err, QDEC_FLAG_TIMEOUT);
                         stop = true;
+                    } else if (p.withhold_first && i == 0) {
+                        // test hook: this tile's barrier phase never completes
                     } else if (pj >= 0 && pj < p.num_pages && gj >= 0 && gj < p.Hkv) {
                         slot_ok[slot] = 1;
                         mbar_arrive_expect_tx(full, kTileBytes);
@@ -1184,7 +1187,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const uint32_t first = issued > static_cast<uint32_t>(NS) ? issued - NS : 0;
         volatile int never = 0;
         for (uint32_t t = first; t < issued; ++t)
-            mbar_wait_bounded(full0 + 8 * (t % NS), (t / NS) & 1, &never);
+            mbar_wait_bounded(full0 + 8 * (t % NS), (t / NS) & 1, &never, p.wait_cycles);
     }
 }
 

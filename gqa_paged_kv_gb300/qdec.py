@@ -30,6 +30,7 @@ QDEC_FLAG_BAD_PAGE = 1
 QDEC_FLAG_BAD_SEQLEN = 2
 QDEC_FLAG_TIMEOUT = 4
 QDEC_FLAG_BAD_INDEX = 8
+QDEC_LAUNCH_TEST_WITHHOLD_TILE = 1 << 30
 
 # Every symbol include/qdec.h declares.
 EXPORTS = ("qdec_workspace_bytes", "qdec_workspace_init", "qdec_rope_table_bytes",
