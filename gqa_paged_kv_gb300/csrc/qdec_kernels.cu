@@ -196,6 +196,12 @@ __device__ __forceinline__ void launch_dependents() {
 __device__ __forceinline__ void fence_acq_rel_gpu() {
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
+// Atomic add with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t *addr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
 
 __device__ __forceinline__ void flag_error(int32_t *err, int bits) {
     if (err) atomicOr(err, bits);
@@ -674,6 +680,40 @@ __device__ void merge_pieces(const Params &p, int64_t pid0, int b, int g, int np
     if (!in_bounds(p, pid0 >= 0 && np >= 1 && pid0 + np <= p.ws_pieces && b >= 0 && b < p.B &&
                           g >= 0 && g < p.Hkv))
         return;
+    if (np <= 8) {
+        float4 o[8];
+        float lse[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            o[u] = u < np ? __ldcg(reinterpret_cast<const float4 *>(
+                                p.ws_o + ((pid0 + u) * kGroup + h) * kHeadDim + d0))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            lse[u] = u < np ? __ldcg(p.ws_lse + (pid0 + u) * kGroup + h) : kNegInf;
+        }
+        float Ms = kNegInf;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) Ms = fmaxf(Ms, lse[u]);
+        float dn = 0.f;
+        float4 nm = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (Ms != kNegInf) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float e = lse[u] == kNegInf ? 0.f : exp2f(lse[u] - Ms);
+                dn += e;
+                nm.x += e * o[u].x;
+                nm.y += e * o[u].y;
+                nm.z += e * o[u].z;
+                nm.w += e * o[u].w;
+            }
+        }
+        const float iv = dn > 0.f ? 1.f / dn : 0.f;
+        __nv_bfloat16 *dst8 =
+            p.out + (static_cast<int64_t>(b) * p.Hq + g * kGroup + h) * kHeadDim + d0;
+        reinterpret_cast<uint2 *>(dst8)[0] =
+            make_uint2(pack_bf16(__float2bfloat16_rn(nm.x * iv), __float2bfloat16_rn(nm.y * iv)),
+                       pack_bf16(__float2bfloat16_rn(nm.z * iv), __float2bfloat16_rn(nm.w * iv)));
+        return;
+    }
     float M = kNegInf;
     for (int j = lane; j < np; j += 32) M = fmaxf(M, __ldcg(p.ws_lse + (pid0 + j) * kGroup + h));
 #pragma unroll
@@ -910,9 +950,7 @@ __device__ void store_partial(const Params &p, volatile int *misc, int64_t pid, 
     // count it; the last piece in acquires all of them
     consumer_sync();
     if (tid == 0) {
-        fence_acq_rel_gpu();
-        const int prev = atomicAdd(p.ws_cnt + sigma, 1);
-        fence_acq_rel_gpu();
+        const int prev = atomic_add_acq_rel_gpu(p.ws_cnt + sigma, 1);
         misc[1] = prev == np - 1;
     }
     consumer_sync();
