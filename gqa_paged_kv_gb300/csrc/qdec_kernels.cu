@@ -193,9 +193,6 @@ __device__ __forceinline__ void launch_dependents() {
 
 // Release/acquire fence at GPU scope (lighter than the sequentially
 // consistent one __threadfence issues).
-__device__ __forceinline__ void fence_acq_rel_gpu() {
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
-}
 // Atomic add with acquire-release semantics at GPU scope; returns the old value.
 __device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t *addr, int v) {
     int old;
@@ -1230,9 +1227,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 }
 
 // ------------------------------------------------------------ rope table --
+constexpr int kRopeThreads = 32;
 // cos/sin of every (sequence, frequency) of the step, computed once and
-// shared by all layers (the angles depend on the positions only).
-__global__ void __launch_bounds__(256) rope_table_kernel(const __grid_constant__ Params p) {
+// shared by all layers (the angles depend on the positions only).  One
+// double-precision sincos per thread, spread over many small CTAs (fp64 is
+// slow per SM).  A following attention launch may start early: it reads the
+// table only after its dependency wait.
+__global__ void __launch_bounds__(kRopeThreads) rope_table_kernel(const __grid_constant__ Params p) {
+    launch_dependents();
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= p.B * kRotPairs) return;
     const int b = idx / kRotPairs, i = idx % kRotPairs;
@@ -1366,7 +1368,7 @@ cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, bool fu
 
 cudaError_t launch_rope_table(const Params &p, cudaStream_t s) {
     const int n = p.B * kRotPairs;
-    rope_table_kernel<<<(n + 255) / 256, 256, 0, s>>>(p);
+    rope_table_kernel<<<(n + kRopeThreads - 1) / kRopeThreads, kRopeThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
