@@ -330,32 +330,37 @@ def run_ours(args, dist: Dist):
                       device="cuda")
     torch.cuda.synchronize()
 
-    def rope_step():
-        qdec.qdec_rope_table(shape, w.positions, rope, stream=stream)
+    Hq, Hkv = spec.num_q_heads, spec.num_kv_heads
 
-    def layers():
-        for l in range(L):
-            qdec.qdec_step(shape, w.q(l), w.k(l), w.v(l), w.w_q[l], w.w_k[l], w.positions,
-                           w.seq_lens, w.block_table, w.pool(l), ws, out[l], err, stream=stream,
-                           rope_table=rope)
+    def step_fn(qkv, seq_lens, positions, block_table, out_t):
+        """One decode step (the rope table, then the L layers) on these buffers."""
+        def fn():
+            qdec.qdec_rope_table(shape, positions, rope, stream=stream)
+            for l in range(L):
+                qdec.qdec_step(shape, qkv[l, :, :Hq], qkv[l, :, Hq:Hq + Hkv],
+                               qkv[l, :, Hq + Hkv:], w.w_q[l], w.w_k[l], positions, seq_lens,
+                               block_table, w.pool(l), ws, out_t[l], err, stream=stream,
+                               rope_table=rope)
+        return fn
 
-    with torch.cuda.stream(stream):
-        rope_step()
-        layers()  # first launch configures the kernels outside capture
-    stream.synchronize()
-    if args.no_graph:
-        def run():
-            rope_step()
-            layers()
-    else:
-        # one graph per step: the rope table, then the layers (the first
-        # layer is a programmatic dependent of the table kernel)
-        g_step = torch.cuda.CUDAGraph()
+    def graph_of(fn):
+        if args.no_graph:
+            return fn
+        # one graph per step (the first layer is a programmatic dependent of
+        # the table kernel)
+        g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
-            with torch.cuda.graph(g_step, stream=stream):
-                rope_step()
-                layers()
-        run = g_step.replay
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+        graphs.append(g)
+        return g.replay
+
+    graphs = []
+    step0 = step_fn(w.qkv, w.seq_lens, w.positions, w.block_table, out)
+    with torch.cuda.stream(stream):
+        step0()  # the first launch configures the kernels outside capture
+    stream.synchronize()
+    run = graph_of(step0)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -408,37 +413,57 @@ def run_ours(args, dist: Dist):
     achieved = bytes_layer / (launch_us * 1e-6) / 1e9
     peak, peak_kind = measured_peaks()
 
-    # ---- end to end: pinned host inputs in, outputs out, every step
-    qkv_h = w.qkv.cpu().pin_memory()
+    # ---- end to end: pinned host inputs in, outputs out, every step.  Two
+    # sets of device buffers: a step's input copies and its output copy run on
+    # their own streams, overlapping the neighbouring steps' kernels.
     meta = [w.seq_lens, w.positions, w.block_table]
+    qkv_h = w.qkv.cpu().pin_memory()
     meta_h = [m.cpu().pin_memory() for m in meta]
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-
-    def e2e_step():
-        w.qkv.copy_(qkv_h, non_blocking=True)
-        for d, h in zip(meta, meta_h):
-            d.copy_(h, non_blocking=True)
-        run()
-        out_h.copy_(out, non_blocking=True)
-
+    h2d = qkv_h.numel() * qkv_h.element_size() + sum(m.numel() * m.element_size() for m in meta_h)
+    d2h = out.numel() * out.element_size()
     k_e2e = 0 if args.no_e2e else max(1, args.steps // 4)
     if k_e2e:
-        with torch.cuda.stream(stream):
-            for _ in range(max(3, args.warmup // 4)):
-                e2e_step()
-        stream.synchronize()
+        sets = []
+        for j in range(2):
+            qkv_d = torch.empty_like(w.qkv)
+            meta_d = [torch.empty_like(m) for m in meta]
+            out_d = torch.empty_like(out)
+            for d, h in zip([qkv_d] + meta_d, [qkv_h] + meta_h):
+                d.copy_(h)
+            fn = graph_of(step_fn(qkv_d, meta_d[0], meta_d[1], meta_d[2], out_d))
+            sets.append(dict(qkv=qkv_d, meta=meta_d, out=out_d, run=fn,
+                             out_h=torch.empty(out.shape, dtype=out.dtype).pin_memory(),
+                             loaded=torch.cuda.Event(), done=torch.cuda.Event()))
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+        def e2e_step(k):
+            b = sets[k & 1]
+            with torch.cuda.stream(s_in):   # inputs of step k (set free once step k-2 ran)
+                s_in.wait_event(b["done"])
+                b["qkv"].copy_(qkv_h, non_blocking=True)
+                for d, h in zip(b["meta"], meta_h):
+                    d.copy_(h, non_blocking=True)
+                b["loaded"].record(s_in)
+            with torch.cuda.stream(stream):
+                stream.wait_event(b["loaded"])
+                b["run"]()
+                b["done"].record(stream)
+            with torch.cuda.stream(s_out):  # outputs of step k
+                s_out.wait_event(b["done"])
+                b["out_h"].copy_(b["out"], non_blocking=True)
+
+        for k in range(max(3, args.warmup // 4)):
+            e2e_step(k)
+        torch.cuda.synchronize()
         dist.barrier()
         torch.cuda.synchronize()
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(k_e2e):
-                e2e_step()
-            e1.record(stream)
+        e0.record(s_in)
+        for k in range(k_e2e):
+            e2e_step(k)
+        e1.record(s_out)
         torch.cuda.synchronize()
         dist.barrier()
         t_e2e = dist.max(e0.elapsed_time(e1))
-    h2d = qkv_h.numel() * qkv_h.element_size() + sum(m.numel() * m.element_size() for m in meta_h)
-    d2h = out_h.numel() * out_h.element_size()
     e2e_value = dist.world * bytes_step * k_e2e / (t_e2e * 1e-3) / 1e9 if k_e2e else None
     st, flags = qdec.qdec_check_error(err, stream)
     assert st == 0, f"device error flags {flags:#x}"
