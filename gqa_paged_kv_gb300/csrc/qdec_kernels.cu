@@ -432,47 +432,60 @@ __device__ void key_row(const Params &p, __nv_bfloat162 ka, __nv_bfloat162 kc, _
 // dims 2l, 2l+1, 64+2l, 65+2l.  bf16(k_rot) (float-float norm and rotation,
 // one rounding) and v go to kv_new in shared memory and to the pool slot of
 // token L-1.
-__device__ void key_value_row(const Params &p, int b, int g, int L, uint8_t *sm) {
+struct KvIn {
+    __nv_bfloat162 ka, kc, wka, wkc;
+    uint32_t va, vc;
+    int page;
+    RopeEntry e0, e1;
+};
+
+// Loads of key_value_row, issued early so that their latency overlaps other work.
+__device__ __forceinline__ KvIn load_kv_inputs(const Params &p, int b, int g, int L) {
     const int lane = threadIdx.x & 31;
     const __nv_bfloat16 *krow = p.k + b * p.k_stride + static_cast<int64_t>(g) * kHeadDim;
     const __nv_bfloat16 *vrow = p.v + b * p.v_stride + static_cast<int64_t>(g) * kHeadDim;
-    const __nv_bfloat162 ka = reinterpret_cast<const __nv_bfloat162 *>(krow)[lane];
-    const __nv_bfloat162 kc = reinterpret_cast<const __nv_bfloat162 *>(krow + 64)[lane];
-    const __nv_bfloat162 wka = reinterpret_cast<const __nv_bfloat162 *>(p.w_k)[lane];
-    const __nv_bfloat162 wkc = reinterpret_cast<const __nv_bfloat162 *>(p.w_k + 64)[lane];
-    const uint32_t va = reinterpret_cast<const uint32_t *>(vrow)[lane];
-    const uint32_t vc = reinterpret_cast<const uint32_t *>(vrow + 64)[lane];
-    const int page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + (L - 1) / kPageSize];
-    RopeEntry e0, e1;
+    KvIn in;
+    in.ka = reinterpret_cast<const __nv_bfloat162 *>(krow)[lane];
+    in.kc = reinterpret_cast<const __nv_bfloat162 *>(krow + 64)[lane];
+    in.wka = reinterpret_cast<const __nv_bfloat162 *>(p.w_k)[lane];
+    in.wkc = reinterpret_cast<const __nv_bfloat162 *>(p.w_k + 64)[lane];
+    in.va = reinterpret_cast<const uint32_t *>(vrow)[lane];
+    in.vc = reinterpret_cast<const uint32_t *>(vrow + 64)[lane];
+    in.page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + (L - 1) / kPageSize];
     if (p.rope) {
         const RopeEntry *rope = p.rope + static_cast<int64_t>(b) * kRotPairs;
-        e0 = rope[2 * lane];
-        e1 = rope[2 * lane + 1];
+        in.e0 = rope[2 * lane];
+        in.e1 = rope[2 * lane + 1];
     } else {
         const int pos = p.positions[b];
-        e0 = rope_entry(pos, p.inv_freq[2 * lane], true);
-        e1 = rope_entry(pos, p.inv_freq[2 * lane + 1], true);
+        in.e0 = rope_entry(pos, p.inv_freq[2 * lane], true);
+        in.e1 = rope_entry(pos, p.inv_freq[2 * lane + 1], true);
     }
+    return in;
+}
+
+__device__ void key_value_row(const Params &p, int b, int g, int L, uint8_t *sm, const KvIn &in) {
+    const int lane = threadIdx.x & 31;
     __nv_bfloat16 kb[4];
-    key_row(p, ka, kc, wka, wkc, e0, e1, kb);
+    key_row(p, in.ka, in.kc, in.wka, in.wkc, in.e0, in.e1, kb);
     const uint32_t k0 = pack_bf16(kb[0], kb[1]), k1 = pack_bf16(kb[2], kb[3]);
     uint32_t *kv_new = reinterpret_cast<uint32_t *>(sm + kOffKvNew);
     kv_new[lane] = k0;
     kv_new[32 + lane] = k1;
-    kv_new[64 + lane] = va;
-    kv_new[96 + lane] = vc;
+    kv_new[64 + lane] = in.va;
+    kv_new[96 + lane] = in.vc;
     const int slot = L - 1;
-    if (page >= 0 && page < p.num_pages) {
+    if (in.page >= 0 && in.page < p.num_pages) {
         const int64_t row =
-            ((static_cast<int64_t>(page) * 2 * p.Hkv + g) * kPageSize + slot % kPageSize) *
+            ((static_cast<int64_t>(in.page) * 2 * p.Hkv + g) * kPageSize + slot % kPageSize) *
             kHeadDim;
         uint32_t *kdst = reinterpret_cast<uint32_t *>(p.pool + row);
         uint32_t *vdst =
             reinterpret_cast<uint32_t *>(p.pool + row + static_cast<int64_t>(p.Hkv) * kPageSize * kHeadDim);
         kdst[lane] = k0;
         kdst[32 + lane] = k1;
-        vdst[lane] = va;
-        vdst[32 + lane] = vc;
+        vdst[lane] = in.va;
+        vdst[32 + lane] = in.vc;
     } else if (lane == 0) {
         flag_error(p.err, QDEC_FLAG_BAD_PAGE);
     }
@@ -543,7 +556,7 @@ __device__ void new_token_rows(const Params &p, int b, int g, int L, bool need_k
         reinterpret_cast<float2 *>(dst)[lane] = make_float2(y0, y1);
         reinterpret_cast<float2 *>(dst + 64)[lane] = make_float2(y2, y3);
     }
-    if (need_k && w == 0) key_value_row(p, b, g, L, sm);
+    if (need_k && w == 0) key_value_row(p, b, g, L, sm, load_kv_inputs(p, b, g, L));
 }
 
 // ----------------------------------------------------------- tile math --
@@ -770,7 +783,7 @@ template <bool kFused>
 __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint32_t full0,
                               uint32_t empty0, volatile int *slot_ok, volatile int *misc, int b,
                               int g, int pg0, int cnt, int L, int n, uint32_t &i,
-                              WarpState &st, int &kv_uses) {
+                              WarpState &st, int &kv_uses, bool early_kv) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tg = lane >> 2, c = lane & 3;
     const int NS = p.stages;
@@ -778,6 +791,13 @@ __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint3
     const __nv_bfloat16 *kv_new = reinterpret_cast<const __nv_bfloat16 *>(sm + kOffKvNew);
     __nv_bfloat16 *pbuf = reinterpret_cast<__nv_bfloat16 *>(sm + kOffPbuf) + warp * 8 * 16;
     const bool has_last = pg0 + cnt == n;
+    // the warp that will produce the new key: with early_kv (one piece per
+    // CTA, latency-bound) it issues its loads first, so their latency overlaps
+    // the query rows
+    const bool key_warp = kFused && has_last && warp == static_cast<int>((i + cnt) & 3) &&
+                          new_token_in_bounds(p, b, g, L);
+    KvIn kv_in;
+    if (key_warp && early_kv) kv_in = load_kv_inputs(p, b, g, L);
 
     if (kFused) {
         new_token_rows<0>(p, b, g, L, false, sm);
@@ -812,7 +832,7 @@ __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint3
     const uint32_t kv_parity = static_cast<uint32_t>(kv_uses) & 1;
     if (kFused && has_last) {
         if (warp == static_cast<int>((i + cnt) & 3)) {
-            if (new_token_in_bounds(p, b, g, L)) key_value_row(p, b, g, L, sm);
+            if (key_warp) key_value_row(p, b, g, L, sm, early_kv ? kv_in : load_kv_inputs(p, b, g, L));
             __syncwarp();
             if (lane == 0) mbar_arrive(kv_bar);
         }
@@ -1134,7 +1154,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             WarpState st;
             reset_state(st);
             process_piece<kFused>(p, sm, ring, full0, empty0, slot_ok, misc, b, g, w.pg, cnt, sl[b],
-                                  n, i, st, kv_uses);
+                                  n, i, st, kv_uses, false);
             const PieceResult r = combine_warps(st, sm, reinterpret_cast<float *>(sm + kOffOs));
             const long long seg0 = static_cast<long long>(p.Hkv) * pre[b] + static_cast<long long>(g) * n;
             const int j0 = cta_of(seg0, W, G);
@@ -1159,7 +1179,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         int kv_uses = 0;
         if (cnt > 0)
             process_piece<kFused>(p, sm, ring, full0, empty0, slot_ok, misc, cb, cg, pg_lo, cnt, cL,
-                                  cn, i, st, kv_uses);
+                                  cn, i, st, kv_uses, true);
         // every tile has been consumed (so no copy is landing in the ring)
         // before ring slot 0 becomes the combine scratch
         consumer_sync();
