@@ -8,21 +8,23 @@
  *
  *   1. QK RMSNorm -- every new-token head row x (Hq query rows, Hkv key rows)
  *      becomes x * rsqrt(mean(x^2) + eps) * w, with one weight vector w_q for
- *      the query rows and one w_k for the key rows.  ("Qwen3 GPU optimisation"
- *      blog by yuzheng310, part 6, fused RMSNorm after the Q/K projection.)
+ *      the query rows and one w_k for the key rows.  (Blog "GPU 算子与执行优化：从 26 到 100 token/s 的推理引擎破茧之路" (yuzheng310.github.io),
+ *      part 6 (第六部分): fused RMSNorm after the Q/K projection.)
  *   2. NeoX RoPE -- rotate-half at position positions[b]: for i < D/2 the pair
  *      (i, i + D/2) turns by pos * rope_theta^(-2i/D).  (Same blog, part 6,
  *      fused NeoX RoPE with interleave=False.)
  *   3. Paged append -- slot t = L_b - 1 lives in page block_table[b][t / P],
  *      row t % P; it receives bf16(k_rot) (round-to-nearest-even) and v (bits
- *      copied).  ("What happens inside an inference engine", PagedAttention
- *      section: 16-token blocks reached through a per-request block table.)
+ *      copied).  (Essay "推理引擎里面发生了什么" (locsic.com),
+ *      section "PagedAttention：vLLM 的解法": 16-token blocks reached through
+ *      a per-request block table.)
  *   4. Split-KV GQA decode attention -- query head h reads KV head h / G;
  *      out = softmax(q_rot K^T * sm_scale) V over the L_b tokens, the new one
  *      included.  The KV sequence of each (b, KV head) is cut into pieces
  *      processed by different CTAs, each piece yields a local softmax, and
  *      the pieces are reduced with the exact log-sum-exp merge.  (Blog part 8,
- *      split-KV; Qwen3-8B engine article, section 4.4.2, grouped decode.)
+ *      split-KV; article "扔掉 vLLM！从零构建 Qwen3-8B 推理引擎" (news.rkmt.cn),
+ *      section 4.4.2, grouped decode.)
  *
  * Pool layout (one pool per layer; the blog's part-4 shape with K and V in
  * one tensor):   kv_pool[num_pages][2][Hkv][P][D] bf16, plane 0 = K, 1 = V.

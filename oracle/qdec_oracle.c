@@ -9,19 +9,20 @@
  *
  * Every step is written from its definition, single-threaded, in double:
  *
- *   RMSNorm   -- "Qwen3 GPU optimisation" blog (yuzheng310), part 6 (fusing
+ *   RMSNorm   -- blog "GPU 算子与执行优化：从 26 到 100 token/s 的推理引擎破茧之路" (yuzheng310.github.io), part 6 (fusing
  *               Norm and RoPE): y = x * rsqrt(mean(x^2) + eps) * w, computed
  *               per head row after the Q/K projection.
  *   NeoX RoPE -- same blog, part 6, fused NeoX RoPE (interleave=False, i.e.
  *               rotate-half): pairs (i, i + D/2) are rotated by
  *               theta_i = pos * rope_theta^(-2i/D).
- *   append    -- "What happens inside an inference engine" (locsic.com),
+ *   append    -- essay "推理引擎里面发生了什么" (locsic.com),
  *               PagedAttention section: a request maps logical blocks of 16
  *               tokens to physical blocks through its block table.
  *   attention -- same essay, "standard attention" (S = QK^T, P = softmax(S),
  *               O = PV) restricted to one query row, with the 1/sqrt(d_head)
  *               scale and the GQA head mapping g = h / heads_per_group of the
- *               Qwen3-8B engine article (news.rkmt.cn), section 4.4.2.
+ *               article "扔掉 vLLM！从零构建 Qwen3-8B 推理引擎" (news.rkmt.cn),
+ *               section 4.4.2.
  *   split/merge -- blog part 8: one head's KV sequence is cut into parts,
  *               each part gets a local softmax, the parts are then reduced.
  *               The reduction is the exact log-sum-exp merge.
