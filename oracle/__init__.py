@@ -93,6 +93,16 @@ class Oracle:
         lib.oracle_decode_layer.argtypes = ([ci] * 7 + [u16p] * 5 + [i32p] * 3 + [u16p]
                                             + [_D] * 3 + [dp] * 4)
         lib.oracle_decode_layer.restype = ci
+        u8p, f32p = ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(ctypes.c_float)
+        lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_to_double.restype = _D
+        lib.oracle_float_to_e4m3_satfinite.argtypes = [ctypes.c_float]
+        lib.oracle_float_to_e4m3_satfinite.restype = ctypes.c_uint8
+        lib.oracle_attention_fp8.argtypes = [ci] * 7 + [u8p, f32p, i32p, i32p, dp, _D, dp, dp]
+        lib.oracle_attention_fp8.restype = ci
+        lib.oracle_decode_layer_fp8.argtypes = ([ci] * 7 + [u16p] * 5 + [i32p] * 3
+                                                + [u8p, f32p] + [_D] * 3 + [dp] * 4)
+        lib.oracle_decode_layer_fp8.restype = ci
         self.lib = lib
         self.path = path
 
@@ -182,6 +192,68 @@ class Oracle:
         return res
 
 
+    # ------------------------------------------------------------- fp8 KV
+    def e4m3_to_double(self, code: int) -> float:
+        return self.lib.oracle_e4m3_to_double(int(code))
+
+    def float_to_e4m3(self, x: float) -> int:
+        """E4M3 code of a binary32 value (nearest-even, saturating)."""
+        return int(self.lib.oracle_float_to_e4m3_satfinite(float(x)))
+
+    def e4m3_codes(self, a) -> np.ndarray:
+        """float_to_e4m3 of every element (taken as binary32)."""
+        flat = np.asarray(a, dtype=np.float32).ravel()
+        f = self.lib.oracle_float_to_e4m3_satfinite
+        out = np.fromiter((f(float(x)) for x in flat), dtype=np.uint8, count=flat.size)
+        return out.reshape(np.shape(a))
+
+    @staticmethod
+    def _fp8_args(pool8, kv_scale):
+        pool8 = np.ascontiguousarray(pool8)
+        assert pool8.dtype == np.uint8, f"expected e4m3 codes (uint8), got {pool8.dtype}"
+        sc = np.ascontiguousarray(kv_scale, dtype=np.float32)
+        num_pages, two, Hkv = pool8.shape[:3]
+        assert sc.shape == (num_pages, two, Hkv), (sc.shape, pool8.shape)
+        return pool8, sc
+
+    def attention_fp8(self, pool8, kv_scale, block_table, seq_lens, q_rot, scale: float):
+        """:meth:`attention` over an FP8 pool (uint8 [pages][2][Hkv][P][D])
+        with scales kv_scale (float32 [pages][2][Hkv])."""
+        pool8, sc = self._fp8_args(pool8, kv_scale)
+        bt, sl, q = _i32(block_table), _i32(seq_lens), _f64(q_rot)
+        out = np.empty(q.shape, np.float64)
+        lse = np.empty(q.shape[:2], np.float64)
+        _check(self.lib.oracle_attention_fp8(
+            *self._dims(pool8, bt, q), _ptr(pool8, ctypes.c_uint8), _ptr(sc, ctypes.c_float),
+            _ptr(bt, _I32), _ptr(sl, _I32), _ptr(q, _D), float(scale), _ptr(out, _D),
+            _ptr(lse, _D)))
+        return out, lse
+
+    def decode_layer_fp8(self, q, k, v, w_q, w_k, positions, seq_lens, block_table, pool8,
+                         kv_scale, rope_theta: float, eps: float, scale: float = 0.0):
+        """:meth:`decode_layer` with an FP8 pool; ``pool8`` (uint8, contiguous)
+        is updated in place by the append, ``kv_scale`` is read only."""
+        q, k, v = _u16(q), _u16(k), _u16(v)
+        w_q, w_k = _u16(w_q), _u16(w_k)
+        pos, sl, bt = _i32(positions), _i32(seq_lens), _i32(block_table)
+        assert pool8.dtype == np.uint8 and pool8.flags["C_CONTIGUOUS"], \
+            "pool8 must be a contiguous uint8 array"
+        _, sc = self._fp8_args(pool8, kv_scale)
+        B, Hq, D = q.shape
+        num_pages, _, Hkv, P, D2 = pool8.shape
+        assert D2 == D and k.shape == (B, Hkv, D) and v.shape == (B, Hkv, D)
+        res = {"q_rot": np.empty((B, Hq, D)), "k_rot": np.empty((B, Hkv, D)),
+               "out": np.empty((B, Hq, D)), "lse": np.empty((B, Hq))}
+        _check(self.lib.oracle_decode_layer_fp8(
+            B, Hq, Hkv, D, P, num_pages, bt.shape[1],
+            _ptr(q, _U16), _ptr(k, _U16), _ptr(v, _U16), _ptr(w_q, _U16), _ptr(w_k, _U16),
+            _ptr(pos, _I32), _ptr(sl, _I32), _ptr(bt, _I32), _ptr(pool8, ctypes.c_uint8),
+            _ptr(sc, ctypes.c_float), float(rope_theta), float(eps), float(scale),
+            _ptr(res["q_rot"], _D), _ptr(res["k_rot"], _D), _ptr(res["out"], _D),
+            _ptr(res["lse"], _D)))
+        return res
+
+
 _default = None
 
 
@@ -221,3 +293,11 @@ def attention_split(pool, block_table, seq_lens, q_rot, scale, chunk_pages):
 
 def decode_layer(*args, **kwargs):
     return default().decode_layer(*args, **kwargs)
+
+
+def attention_fp8(pool8, kv_scale, block_table, seq_lens, q_rot, scale):
+    return default().attention_fp8(pool8, kv_scale, block_table, seq_lens, q_rot, scale)
+
+
+def decode_layer_fp8(*args, **kwargs):
+    return default().decode_layer_fp8(*args, **kwargs)

@@ -26,6 +26,12 @@
  *   split/merge -- blog part 8: one head's KV sequence is cut into parts,
  *               each part gets a local softmax, the parts are then reduced.
  *               The reduction is the exact log-sum-exp merge.
+ *   FP8 KV    -- essay, section on quantization: the KV cache held in FP8
+ *               (half the bytes).  Codes are OCP E4M3; every (page, plane,
+ *               KV head) carries one fp32 scale, value = e4m3(code) * scale.
+ *               The append quantizes the bf16 row it would otherwise store:
+ *               code = RNE_e4m3_satfinite(fp32(row) / scale), the division
+ *               rounded once to fp32.
  *
  * Pool layout (the reading adopted for the shape the blog prints in part 4,
  * [num_blocks, num_heads, block_size, head_dim], with K and V in one tensor):
@@ -334,6 +340,209 @@ int oracle_decode_layer(int B, int Hq, int Hkv, int D, int P, int num_pages,
     if (rc == 0)
         rc = oracle_attention(B, Hq, Hkv, D, P, num_pages, max_blocks, pool, block_table,
                               seq_lens, q_rot, scale, out, lse);
+    free(x);
+    free(xn);
+    free(wq);
+    free(wk);
+    return rc;
+}
+
+/* ------------------------------------------------------------ fp8 e4m3 -- */
+
+/* E4M3 as the OCP 8-bit floating point format defines it: a sign bit, four
+ * exponent bits with bias 7 and three mantissa bits.  Exponent field 0 holds
+ * the subnormals m/8 * 2^-6; exponent and mantissa fields all ones is NaN;
+ * there is no infinity, so the largest finite value is 1.75 * 2^8 = 448. */
+double oracle_e4m3_to_double(uint8_t c)
+{
+    int neg = c >> 7, e = (c >> 3) & 0xF, m = c & 7;
+    double mag;
+    if (e == 0xF && m == 7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)m, -9);
+    else
+        mag = ldexp(8.0 + m, e - 10);
+    return neg ? -mag : mag;
+}
+
+/* Round a binary32 value to E4M3, nearest-even, saturating: a magnitude at or
+ * beyond the largest finite 448 (infinity included) gives +-448, NaN gives
+ * the NaN pattern 0x7F, the sign of zero is kept.  Spacing: 2^(e-4) in
+ * [2^(e-1), 2^e), never below the subnormal step 2^-9. */
+uint8_t oracle_float_to_e4m3_satfinite(float xf)
+{
+    double x = (double)xf;
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs(x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    if (a == 0.0)
+        return sign;
+    int e;
+    (void)frexp(a, &e);                    /* a in [2^(e-1), 2^e) */
+    if (e < -5)
+        e = -5;
+    double ulp = ldexp(1.0, e - 4);
+    double r = nearbyint(a / ulp) * ulp;   /* default mode: nearest-even */
+    if (r < ldexp(1.0, -6))                /* subnormal (or zero) */
+        return (uint8_t)(sign | (int)(r / ldexp(1.0, -9)));
+    int er;
+    (void)frexp(r, &er);                   /* r in [2^(er-1), 2^er) */
+    int field = er - 1 + 7;
+    int m = (int)((r / ldexp(1.0, er - 1) - 1.0) * 8.0);
+    return (uint8_t)(sign | (field << 3) | m);
+}
+
+/* Offset of the scale of (page of token t of sequence b, plane kv, head h):
+ * kv_scale[num_pages][2][Hkv].  -1 if the block-table entry is outside the
+ * pool. */
+static long scale_index(const oracle_dims *d, const int32_t *block_table, int b, int t,
+                        int kv, int h)
+{
+    int32_t page = block_table[(long)b * d->max_blocks + t / d->P];
+    if (page < 0 || page >= d->num_pages)
+        return -1;
+    return ((long)page * 2 + kv) * d->Hkv + h;
+}
+
+/* attend_range over an FP8 pool: row elements are e4m3(code) * scale (exact
+ * in double), then the same scores, softmax and weighted sum. */
+static int attend_range_fp8(const oracle_dims *d, const uint8_t *pool8, const float *kv_scale,
+                            const int32_t *block_table, int b, int g, const double *q,
+                            double scale, int t0, int t1, double *out, double *lse)
+{
+    int D = d->D;
+    int n = t1 - t0;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    double m = -INFINITY;
+    for (int t = t0; t < t1; ++t) {
+        long row = pool_row(d, block_table, b, t, 0, g);
+        long si = scale_index(d, block_table, b, t, 0, g);
+        if (row < 0 || si < 0) {
+            free(s);
+            return -1;
+        }
+        double sk = (double)kv_scale[si];
+        double dot = 0.0;
+        for (int i = 0; i < D; ++i)
+            dot += q[i] * (oracle_e4m3_to_double(pool8[row + i]) * sk);
+        s[t - t0] = scale * dot;
+        if (s[t - t0] > m)
+            m = s[t - t0];
+    }
+    double l = 0.0;
+    for (int i = 0; i < D; ++i)
+        out[i] = 0.0;
+    for (int t = t0; t < t1; ++t) {
+        double w = exp(s[t - t0] - m);
+        l += w;
+        long row = pool_row(d, block_table, b, t, 1, g);
+        double sv = (double)kv_scale[scale_index(d, block_table, b, t, 1, g)];
+        for (int i = 0; i < D; ++i)
+            out[i] += w * (oracle_e4m3_to_double(pool8[row + i]) * sv);
+    }
+    for (int i = 0; i < D; ++i)
+        out[i] /= l;
+    *lse = m + log(l);
+    free(s);
+    return 0;
+}
+
+/* oracle_attention over an FP8 pool (pool8 laid out like the bf16 pool, one
+ * byte per element) with its scales kv_scale[num_pages][2][Hkv]. */
+int oracle_attention_fp8(int B, int Hq, int Hkv, int D, int P, int num_pages,
+                         int max_blocks, const uint8_t *pool8, const float *kv_scale,
+                         const int32_t *block_table, const int32_t *seq_lens,
+                         const double *q_rot, double scale, double *out, double *lse)
+{
+    oracle_dims d = {B, Hq, Hkv, D, P, num_pages, max_blocks};
+    int G = Hq / Hkv;
+    for (int b = 0; b < B; ++b) {
+        int L = seq_lens[b];
+        if (L < 1 || L > max_blocks * P)
+            return -2;
+        for (int h = 0; h < Hq; ++h) {
+            int g = h / G;
+            long o = ((long)b * Hq + h) * D;
+            if (attend_range_fp8(&d, pool8, kv_scale, block_table, b, g, q_rot + o, scale, 0,
+                                 L, out + o, lse + (long)b * Hq + h))
+                return -1;
+        }
+    }
+    return 0;
+}
+
+/* oracle_decode_layer with an FP8 pool: the same norm and rotation, then the
+ * append stores, for every element of the new row,
+ *   K: RNE_e4m3_satfinite(fp32(bf16(k_rot)) / scale_K)
+ *   V: RNE_e4m3_satfinite(fp32(v) / scale_V)
+ * with the scales of the (page, plane, head) the slot lies in (the scales
+ * are inputs and are not changed), then the attention over the FP8 pool. */
+int oracle_decode_layer_fp8(int B, int Hq, int Hkv, int D, int P, int num_pages,
+                            int max_blocks, const uint16_t *q, const uint16_t *k,
+                            const uint16_t *v, const uint16_t *w_q, const uint16_t *w_k,
+                            const int32_t *positions, const int32_t *seq_lens,
+                            const int32_t *block_table, uint8_t *pool8,
+                            const float *kv_scale, double rope_theta, double eps,
+                            double scale, double *q_rot, double *k_rot, double *out,
+                            double *lse)
+{
+    if (Hkv < 1 || Hq % Hkv != 0 || D % 2 != 0)
+        return -4;
+    oracle_dims d = {B, Hq, Hkv, D, P, num_pages, max_blocks};
+    if (scale <= 0.0)
+        scale = 1.0 / sqrt((double)D);
+    double *x = (double *)malloc(sizeof(double) * (size_t)D);
+    double *xn = (double *)malloc(sizeof(double) * (size_t)D);
+    double *wq = (double *)malloc(sizeof(double) * (size_t)D);
+    double *wk = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int i = 0; i < D; ++i) {
+        wq[i] = oracle_bf16_to_double(w_q[i]);
+        wk[i] = oracle_bf16_to_double(w_k[i]);
+    }
+    int rc = 0;
+    for (int b = 0; b < B && rc == 0; ++b) {
+        int L = seq_lens[b];
+        if (L < 1 || L > max_blocks * P) {
+            rc = -2;
+            break;
+        }
+        double pos = (double)positions[b];
+        for (int h = 0; h < Hq; ++h) {
+            long o = ((long)b * Hq + h) * D;
+            for (int i = 0; i < D; ++i)
+                x[i] = oracle_bf16_to_double(q[o + i]);
+            oracle_rmsnorm(x, wq, D, eps, xn);
+            oracle_rope_neox(xn, D, pos, rope_theta, q_rot + o);
+        }
+        for (int h = 0; h < Hkv; ++h) {
+            long o = ((long)b * Hkv + h) * D;
+            for (int i = 0; i < D; ++i)
+                x[i] = oracle_bf16_to_double(k[o + i]);
+            oracle_rmsnorm(x, wk, D, eps, xn);
+            oracle_rope_neox(xn, D, pos, rope_theta, k_rot + o);
+            long rk = pool_row(&d, block_table, b, L - 1, 0, h);
+            long rv = pool_row(&d, block_table, b, L - 1, 1, h);
+            long sk = scale_index(&d, block_table, b, L - 1, 0, h);
+            long sv = scale_index(&d, block_table, b, L - 1, 1, h);
+            if (rk < 0 || rv < 0 || sk < 0 || sv < 0) {
+                rc = -1;
+                break;
+            }
+            for (int i = 0; i < D; ++i) {
+                float kf = (float)oracle_bf16_to_double(oracle_double_to_bf16(k_rot[o + i]));
+                float vf = (float)oracle_bf16_to_double(v[o + i]);
+                pool8[rk + i] = oracle_float_to_e4m3_satfinite(kf / kv_scale[sk]);
+                pool8[rv + i] = oracle_float_to_e4m3_satfinite(vf / kv_scale[sv]);
+            }
+        }
+    }
+    if (rc == 0)
+        rc = oracle_attention_fp8(B, Hq, Hkv, D, P, num_pages, max_blocks, pool8, kv_scale,
+                                  block_table, seq_lens, q_rot, scale, out, lse);
     free(x);
     free(xn);
     free(wq);

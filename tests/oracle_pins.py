@@ -406,4 +406,180 @@ def pin_layer_new_token_attends_itself(orc):
             _close(res["out"][b, h], f64(v[b, h // 4]), 0.0, "out = v")
 
 
+# -------------------------------------------------------------- fp8 (E4M3) --
+# The format is the OCP 8-bit floating point E4M3 (bias 7, three mantissa
+# bits, subnormals, NaN = S.1111.111, no infinity, largest finite 448).
+
+def _torch_e4m3_values() -> np.ndarray:
+    """Values of all 256 codes by PyTorch's float8_e4m3fn widening (a library
+    implementation of the same format)."""
+    return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+
+
+def _e4m3_nearest(x: float, table: np.ndarray) -> int:
+    """Brute force: the finite non-negative code nearest to |x| (ties to the
+    code with even mantissa), magnitudes >= 448 saturate, sign copied."""
+    if math.isnan(x):
+        return 0x7F
+    sign = 0x80 if math.copysign(1.0, x) < 0 else 0
+    a = abs(x)
+    if a >= 448.0:
+        return sign | 0x7E
+    best_d, best_c = None, None
+    for c in range(0x7F):
+        d = abs(table[c] - a)
+        if best_d is None or d < best_d or (d == best_d and c % 2 == 0):
+            best_d, best_c = d, c
+    return sign | best_c
+
+
+def _fp8_codes(rng, shape, sigma=4.0) -> np.ndarray:
+    """Random finite codes: normal draws cast by PyTorch (magnitudes < 448)."""
+    x = np.clip(rng.standard_normal(shape) * sigma, -440, 440).astype(np.float32)
+    return torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def pin_e4m3_decode_table(orc):
+    """All 256 codes against the format's closed description and against
+    PyTorch's widening."""
+    vals = np.array([orc.e4m3_to_double(c) for c in range(256)])
+    lib = _torch_e4m3_values()
+    nan = np.isnan(vals)
+    assert list(np.nonzero(nan)[0]) == [0x7F, 0xFF], "NaN patterns"
+    assert np.array_equal(np.isnan(lib), nan) and np.array_equal(vals[~nan], lib[~nan]), \
+        "differs from float8_e4m3fn"
+    assert vals[0x7E] == 448 and vals[0x01] == 2.0 ** -9 and vals[0x08] == 2.0 ** -6
+    assert vals[0x38] == 1.0 and vals[0x39] == 1.125 and vals[0x30] == 0.5
+    assert vals[0x80] == 0 and math.copysign(1.0, vals[0x80]) < 0, "negative zero"
+    pos = vals[:0x7F]
+    assert np.all(np.diff(pos) > 0), "codes 0x00..0x7E increase"
+    assert np.array_equal(vals[0x80:0xFF], -pos), "sign bit negates"
+    for k in range(-6, 8):   # eight equally spaced values per binade
+        inb = pos[(pos >= 2.0 ** k) & (pos < 2.0 ** (k + 1))]
+        assert np.array_equal(inb, 2.0 ** k * (1 + np.arange(8) / 8)), f"binade 2^{k}"
+    assert np.array_equal(pos[pos >= 256], 256 * (1 + np.arange(7) / 8)), "top binade"
+    assert np.array_equal(pos[(pos > 0) & (pos < 2.0 ** -6)], np.arange(1, 8) * 2.0 ** -9)
+
+
+def pin_e4m3_encode_brute_force(orc):
+    """Encoding equals the nearest code by exhaustive search (ties to even,
+    saturation at 448) on every midpoint, every code and random values; and
+    PyTorch's float8_e4m3fn cast where that cast does not overflow."""
+    table = np.array([orc.e4m3_to_double(c) for c in range(0x7F)])
+    mids = ((table[1:] + table[:-1]) / 2).astype(np.float32)
+    rng = np.random.default_rng(19)
+    xs = np.concatenate([
+        table.astype(np.float32), mids, np.nextafter(mids, np.float32(0)),
+        np.nextafter(mids, np.float32(1e3)),
+        np.exp(rng.uniform(math.log(2.0 ** -12), math.log(600.0), 1500)).astype(np.float32),
+        np.array([0.0, 448.0, 449.0, 463.99, 464.0, 465.0, 1e30, np.inf, 1e-40, 2.0 ** -10,
+                  3 * 2.0 ** -10], np.float32)])
+    xs = np.concatenate([xs, -xs, np.array([np.nan], np.float32)])
+    got = orc.e4m3_codes(xs)
+    for x, c in zip(xs, got):
+        want = _e4m3_nearest(float(x), table)
+        assert c == want, f"e4m3({float(x)!r}) = {c:#x}, nearest is {want:#x}"
+    ok = np.abs(xs) < 464
+    lib = torch.from_numpy(xs[ok]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got[ok], lib), "differs from PyTorch's float8_e4m3fn cast"
+
+
+def _fp8_pool(rng, pb, pow2: bool):
+    pages, _, Hkv = pb.pool.shape[:3]
+    codes = _fp8_codes(rng, pb.pool.shape)
+    if pow2:
+        sc = (2.0 ** rng.integers(-4, 3, size=(pages, 2, Hkv))).astype(np.float32)
+    else:
+        sc = rng.uniform(0.01, 0.5, size=(pages, 2, Hkv)).astype(np.float32)
+    return codes, sc
+
+
+def pin_fp8_attention_pow2_scales_equal_bf16(orc):
+    """With power-of-two scales every element e4m3(code) * scale is exact in
+    bf16, so FP8 attention must equal the (pinned) bf16 attention over the
+    dequantized pool bit for bit."""
+    rng = np.random.default_rng(20)
+    pb = Paged(rng, [1, 3, 4, 5, 8, 15, 17, 40], Hq=8, Hkv=2, D=16, P=4)
+    codes, sc = _fp8_pool(rng, pb, pow2=True)
+    deq = _torch_e4m3_values()[codes] * sc[:, :, :, None, None]
+    out0, lse0 = orc.attention(bits_of(deq.astype(np.float32)), pb.bt, pb.seq_lens, pb.q, 0.25)
+    out1, lse1 = orc.attention_fp8(codes, sc, pb.bt, pb.seq_lens, pb.q, 0.25)
+    assert np.array_equal(out0, out1) and np.array_equal(lse0, lse1), "fp8 vs bf16 attention"
+
+
+def pin_fp8_attention_dense(orc):
+    """General scales: against dense attention over rows dequantized with
+    PyTorch's widening, one scale per (page, plane, head)."""
+    rng = np.random.default_rng(21)
+    pb = Paged(rng, [2, 7, 16, 33], Hq=8, Hkv=2, D=16, P=4)
+    codes, sc = _fp8_pool(rng, pb, pow2=False)
+    table = _torch_e4m3_values()
+    out, lse = orc.attention_fp8(codes, sc, pb.bt, pb.seq_lens, pb.q, 0.25)
+    for b, L in enumerate(pb.seq_lens):
+        t = np.arange(L)
+        pages, off = pb.bt[b, t // 4], t % 4
+        for h in range(8):
+            g = h // 4
+            K = table[codes[pages, 0, g, off]] * sc[pages, 0, g][:, None].astype(np.float64)
+            V = table[codes[pages, 1, g, off]] * sc[pages, 1, g][:, None].astype(np.float64)
+            s = 0.25 * (K @ pb.q[b, h])
+            _close(out[b, h], scipy.special.softmax(s) @ V, 1e-13, f"fp8 dense b={b} h={h}")
+            _close(lse[b, h], scipy.special.logsumexp(s), 1e-12, "fp8 dense lse")
+
+
+def pin_fp8_layer_append(orc):
+    """The FP8 layer-step: the same q_rot/k_rot as the bf16 layer-step; the
+    append changes exactly slot L-1 of every (sequence, plane, head), with
+    K = nearest code of fp32(bf16(k_rot)) / scale and V = nearest code of
+    fp32(v) / scale (fp32 division, brute-force rounding, saturation when
+    the scale is too small); out and lse are the FP8 attention over the
+    updated pool."""
+    rng = np.random.default_rng(22)
+    seq_lens = [1, 4, 5, 16, 22, 9, 31, 2]
+    pb, q, k, v, wq, wk, pos = _layer_problem(rng, seq_lens, Hq=16, Hkv=4, D=32)
+    codes, sc = _fp8_pool(rng, pb, pow2=False)
+    sc[pb.bt[3, (16 - 1) // 4]] = 1e-4          # this page saturates
+    before = codes.copy()
+    res = orc.decode_layer_fp8(q, k, v, wq, wk, pos, pb.seq_lens, pb.bt, codes, sc, 1e6, 1e-6)
+    ref = orc.decode_layer(q, k, v, wq, wk, pos, pb.seq_lens, pb.bt, pb.pool.copy(), 1e6, 1e-6)
+    _close(res["q_rot"], ref["q_rot"], 0.0, "fp8 layer q_rot")
+    _close(res["k_rot"], ref["k_rot"], 0.0, "fp8 layer k_rot")
+    table = np.array([orc.e4m3_to_double(c) for c in range(0x7F)])
+    changed = np.zeros(codes.shape, bool)
+    saturated = 0
+    for b, L in enumerate(pb.seq_lens):
+        page, off = pb.bt[b, (L - 1) // 4], (L - 1) % 4
+        for g in range(4):
+            kf = f64(orc.f64_to_bf16_bits(ref["k_rot"][b, g])).astype(np.float32)
+            vf = f64(v[b, g]).astype(np.float32)
+            want_k = [_e4m3_nearest(float(x / sc[page, 0, g]), table) for x in kf]
+            want_v = [_e4m3_nearest(float(x / sc[page, 1, g]), table) for x in vf]
+            assert np.array_equal(codes[page, 0, g, off], want_k), f"K codes b={b} g={g}"
+            assert np.array_equal(codes[page, 1, g, off], want_v), f"V codes b={b} g={g}"
+            saturated += int(np.sum((codes[page, :, g, off] & 0x7F) == 0x7E))
+        changed[page, :, :, off] = True
+    assert saturated > 0, "the saturating page did not saturate"
+    assert np.array_equal(codes[~changed], before[~changed]), "append touched another slot"
+    out, lse = orc.attention_fp8(codes, sc, pb.bt, pb.seq_lens, res["q_rot"], 1 / math.sqrt(32))
+    _close(res["out"], out, 0.0, "fp8 out after append")
+    _close(res["lse"], lse, 0.0, "fp8 lse after append")
+
+
+def pin_fp8_nan_codes_outside_context(orc):
+    """NaN codes in slots past the end and in unreferenced pages never reach out."""
+    rng = np.random.default_rng(23)
+    pb = Paged(rng, [6, 13], Hq=4, Hkv=1, D=16, P=4, extra_pages=2)
+    codes, sc = _fp8_pool(rng, pb, pow2=False)
+    out0, _ = orc.attention_fp8(codes, sc, pb.bt, pb.seq_lens, pb.q, 0.25)
+    c2 = codes.copy()
+    used = set(int(p) for p in pb.bt.ravel() if p >= 0)
+    for p in range(c2.shape[0]):
+        if p not in used:
+            c2[p] = 0x7F
+    for b, L in enumerate(pb.seq_lens):
+        c2[pb.bt[b, (L - 1) // 4], :, :, (L - 1) % 4 + 1:] = 0xFF
+    out1, _ = orc.attention_fp8(c2, sc, pb.bt, pb.seq_lens, pb.q, 0.25)
+    assert np.array_equal(out0, out1), "NaN codes"
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -44,6 +44,25 @@ MUTANTS = [
      "oracle_rmsnorm(x, wk, D, eps, xn);"),
     ("rope at position + 1", "double pos = (double)positions[b];",
      "double pos = (double)positions[b] + 1.0;"),
+    ("e4m3 exponent bias", "mag = ldexp(8.0 + m, e - 10);", "mag = ldexp(8.0 + m, e - 11);"),
+    ("e4m3 subnormal step", "mag = ldexp((double)m, -9);", "mag = ldexp((double)m, -10);"),
+    ("e4m3 no saturation", "if (a >= 448.0)", "if (a >= 480.0)"),
+    ("e4m3 truncation", "nearbyint(a / ulp)", "trunc(a / ulp)"),
+    ("e4m3 spacing", "double ulp = ldexp(1.0, e - 4);", "double ulp = ldexp(1.0, e - 5);"),
+    ("e4m3 sign of zero", "        return sign;\n", "        return 0;\n"),
+    ("fp8 K scale dropped", "dot += q[i] * (oracle_e4m3_to_double(pool8[row + i]) * sk);",
+     "dot += q[i] * oracle_e4m3_to_double(pool8[row + i]);"),
+    ("fp8 V scale from the K plane", "scale_index(d, block_table, b, t, 1, g)",
+     "scale_index(d, block_table, b, t, 0, g)"),
+    ("fp8 scale layout head/plane", "return ((long)page * 2 + kv) * d->Hkv + h;",
+     "return ((long)page * d->Hkv + h) * 2 + kv;"),
+    ("fp8 append skips the bf16 rounding",
+     "float kf = (float)oracle_bf16_to_double(oracle_double_to_bf16(k_rot[o + i]));",
+     "float kf = (float)k_rot[o + i];"),
+    ("fp8 append multiplies by the scale", "oracle_float_to_e4m3_satfinite(kf / kv_scale[sk])",
+     "oracle_float_to_e4m3_satfinite(kf * kv_scale[sk])"),
+    ("fp8 append V with the K scale", "oracle_float_to_e4m3_satfinite(vf / kv_scale[sv])",
+     "oracle_float_to_e4m3_satfinite(vf / kv_scale[sk])"),
 ]
 
 
