@@ -17,6 +17,9 @@ e2e     = the same metric with, every step, the host->device copy of the
           device->host copy of the outputs inside the timed region.
 roofline = the fused kernel against the measured HBM copy bandwidth.
 cpu_baseline / --impl reference = the fp64 CPU oracle on a bounded sample.
+--kv fp8 runs the same workload over an FP8 (E4M3) pool with per-(page,
+plane, head) scales (qdec_step_fp8); its bytes count one byte per KV element
+plus the scales read.
 
 Multi-GPU: the path shards without any exchange, so N ranks run N
 independent replicas (weak scaling); value sums their work over the slowest
@@ -77,6 +80,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", type=int, default=2, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--kv", choices=("bf16", "fp8"), default="bf16",
+                    help="KV pool element type (fp8: E4M3 codes + per-page scales)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the 36 calls eagerly")
@@ -209,11 +214,15 @@ def l2_bytes(dev=None) -> int:
     return L2_BYTES_NOMINAL
 
 
-def workload_config(spec, seq_lens_host, args, world: int, l2: int = L2_BYTES_NOMINAL) -> dict:
+def workload_name(spec, kv: str) -> str:
+    return spec.name + ("-fp8kv" if kv == "fp8" else "")
+
+
+def workload_config(w: wl.Workload, args, world: int, l2: int = L2_BYTES_NOMINAL) -> dict:
     """The `config` object of the JSON line (the same for both arms)."""
+    spec, seq_lens_host = w.spec, w.seq_lens_host
     L = spec.layers
-    bytes_layer = (int(seq_lens_host.sum()) * spec.kv_bytes_per_token()
-                   + spec.batch * spec.io_bytes_per_seq())
+    bytes_layer = w.algorithmic_bytes_per_layer()
     bytes_step = bytes_layer * L
     if bytes_step < 2 * l2:
         l2_note = (f"L2 flushed: a {2 * l2 / 2**20:.0f} MiB buffer is rewritten before each "
@@ -224,15 +233,18 @@ def workload_config(spec, seq_lens_host, args, world: int, l2: int = L2_BYTES_NO
     else:
         l2_note = (f"inputs larger than L2: each step reads {bytes_step / 1e9:.3f} GB of KV "
                    f"across {L} per-layer pools")
-    return {"workload": spec.name, "batch": spec.batch,
+    return {"workload": workload_name(spec, w.kv), "batch": spec.batch,
             "ctx": f"{int(seq_lens_host.min())}-{int(seq_lens_host.max())}",
             "heads": f"{spec.num_q_heads}q/{spec.num_kv_heads}kv",
             "head_dim": spec.head_dim, "page_size": spec.page_size, "layers": L,
             "pool_pages_per_layer": spec.pool_pages,
+            "kv_cache": ("E4M3 codes + fp32 scale per (page, plane, KV head)" if w.kv == "fp8"
+                         else "bf16"),
             "kv_bytes_per_step": bytes_step,
             "l2": l2_note,
             "launch": ("eager" if args.no_graph else f"CUDA graphs: rope table + "
-                       f"{L} qdec_step") + ("" if args.no_overlap else
+                       f"{L} {'qdec_step_fp8' if w.kv == 'fp8' else 'qdec_step'}")
+                      + ("" if args.no_overlap else
                                             ", programmatic dependent launch"),
             "parallelism": f"replicas x{world}"}
 
@@ -251,18 +263,36 @@ def oracle_sample(w: wl.Workload, seconds: float, per_seq: bool):
     while t_total < seconds or n == 0:
         layer, seqs = units[i % len(units)]
         inp = wl.oracle_inputs(w, layer, seqs)
-        pool = inp["pool"].copy()
         t0 = time.perf_counter()
-        oracle.decode_layer(inp["q"], inp["k"], inp["v"], inp["w_q"], inp["w_k"],
-                            inp["positions"], inp["seq_lens"], inp["block_table"], pool,
-                            inp["rope_theta"], inp["eps"])
+        oracle_layer(inp)
         t_total += time.perf_counter() - t0
-        sl = inp["seq_lens"].astype(np.int64)
-        bytes_done += int(sl.sum()) * w.spec.kv_bytes_per_token() + len(sl) * w.spec.io_bytes_per_seq()
+        bytes_done += sample_bytes(w, inp["seq_lens"])
         n += 1
         i += 1
     what = "one sequence of one layer" if per_seq else "one layer (all sequences)"
     return bytes_done / t_total / 1e9, what, n, t_total
+
+
+def oracle_layer(inp: dict):
+    """One oracle layer-step on oracle_inputs (on a copy of the pool)."""
+    import oracle
+    args = (inp["q"], inp["k"], inp["v"], inp["w_q"], inp["w_k"], inp["positions"],
+            inp["seq_lens"], inp["block_table"], inp["pool"].copy())
+    if "kv_scale" in inp:
+        oracle.decode_layer_fp8(*args, inp["kv_scale"], inp["rope_theta"], inp["eps"])
+    else:
+        oracle.decode_layer(*args, inp["rope_theta"], inp["eps"])
+
+
+def sample_bytes(w: wl.Workload, seq_lens) -> int:
+    """Algorithmic bytes of the given sequences of one layer-step."""
+    s = w.spec
+    sl = np.asarray(seq_lens, dtype=np.int64)
+    io = len(sl) * s.io_bytes_per_seq()
+    if w.kv == "fp8":
+        pages = int(((sl + s.page_size - 1) // s.page_size).sum())
+        return int(sl.sum()) * s.kv_bytes_per_token() // 2 + pages * 2 * s.num_kv_heads * 4 + io
+    return int(sl.sum()) * s.kv_bytes_per_token() + io
 
 
 def run_reference(args, dist: Dist):
@@ -270,7 +300,7 @@ def run_reference(args, dist: Dist):
     if dist.rank != 0:
         return
     spec = wl.WORKLOADS[args.workload]
-    w = wl.build(spec, "cpu", layers=min(spec.layers, CPU_SAMPLE_LAYERS))
+    w = wl.build(spec, "cpu", layers=min(spec.layers, CPU_SAMPLE_LAYERS), kv=args.kv)
     # warm-up steps, then exactly K timed steps; a step is one sequence of one layer
     oracle_steps(w, args.warmup)
     t0 = time.perf_counter()
@@ -282,7 +312,7 @@ def run_reference(args, dist: Dist):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": workload_config(spec, w.seq_lens_host, args, 1),
+        "config": workload_config(w, args, 1),
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} steps of one sequence x one layer, "
                                    f"{dt:.1f} s"},
@@ -294,17 +324,13 @@ def run_reference(args, dist: Dist):
 
 
 def oracle_steps(w: wl.Workload, k: int) -> int:
-    import oracle
     B = w.spec.batch
     done = 0
     for i in range(k):
         layer, b = (i // B) % w.spec.layers, i % B
         inp = wl.oracle_inputs(w, layer, [b])
-        pool = inp["pool"].copy()
-        oracle.decode_layer(inp["q"], inp["k"], inp["v"], inp["w_q"], inp["w_k"],
-                            inp["positions"], inp["seq_lens"], inp["block_table"], pool,
-                            inp["rope_theta"], inp["eps"])
-        done += int(inp["seq_lens"][0]) * w.spec.kv_bytes_per_token() + w.spec.io_bytes_per_seq()
+        oracle_layer(inp)
+        done += sample_bytes(w, inp["seq_lens"])
     return done
 
 
@@ -317,7 +343,7 @@ def run_ours(args, dist: Dist):
     dev = dist.local
     torch.cuda.set_device(dev)
     spec = wl.WORKLOADS[args.workload]
-    w = wl.build(spec, f"cuda:{dev}", layers=args.layers or None)
+    w = wl.build(spec, f"cuda:{dev}", layers=args.layers or None, kv=args.kv)
     spec = w.spec
     L = spec.layers
     shape = qdec.shape_for(w, launch_flags=0 if args.no_overlap
@@ -337,10 +363,16 @@ def run_ours(args, dist: Dist):
         def fn():
             qdec.qdec_rope_table(shape, positions, rope, stream=stream)
             for l in range(L):
-                qdec.qdec_step(shape, qkv[l, :, :Hq], qkv[l, :, Hq:Hq + Hkv],
-                               qkv[l, :, Hq + Hkv:], w.w_q[l], w.w_k[l], positions, seq_lens,
-                               block_table, w.pool(l), ws, out_t[l], err, stream=stream,
-                               rope_table=rope)
+                if w.kv == "fp8":
+                    qdec.qdec_step_fp8(shape, qkv[l, :, :Hq], qkv[l, :, Hq:Hq + Hkv],
+                                       qkv[l, :, Hq + Hkv:], w.w_q[l], w.w_k[l], positions,
+                                       seq_lens, block_table, w.pool8(l), w.scale(l), ws,
+                                       out_t[l], err, stream=stream, rope_table=rope)
+                else:
+                    qdec.qdec_step(shape, qkv[l, :, :Hq], qkv[l, :, Hq:Hq + Hkv],
+                                   qkv[l, :, Hq + Hkv:], w.w_q[l], w.w_k[l], positions, seq_lens,
+                                   block_table, w.pool(l), ws, out_t[l], err, stream=stream,
+                                   rope_table=rope)
         return fn
 
     def graph_of(fn):
@@ -469,32 +501,37 @@ def run_ours(args, dist: Dist):
     assert st == 0, f"device error flags {flags:#x}"
 
     traffic = None
-    tr = TRAFFIC.get(spec.name)
+    tr = TRAFFIC.get(workload_name(spec, w.kv))
     if tr and tr["kernel_sha"] == kernel_sha():
         traffic = tr["bytes_per_launch"]
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        w_cpu = wl.build(spec, "cpu", layers=min(spec.layers, CPU_SAMPLE_LAYERS))
+        w_cpu = wl.build(spec, "cpu", layers=min(spec.layers, CPU_SAMPLE_LAYERS), kv=w.kv)
         gbs, what, n, secs = oracle_sample(w_cpu, args.cpu_seconds, per_seq=False)
         cpu = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n} x {what} of {spec.name} (layers 0-{w_cpu.spec.layers - 1}), "
+               "sample": f"{n} x {what} of {workload_name(spec, w.kv)} "
+                             f"(layers 0-{w_cpu.spec.layers - 1}), "
                              f"fp64, {secs:.1f} s"}
 
     if dist.rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded N(0,1) bf16 q/k/v and KV pages)",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": ("e4m3 KV (f16 mma, f32 accumulate)" if w.kv == "fp8" else "bf16"),
+            "data": "synthetic (seeded N(0,1) bf16 q/k/v and KV pages"
+                    + (", pages cast to E4M3 with amax/448 scales)" if w.kv == "fp8" else ")"),
             "us_per_layer_step": round(ms_step * 1e3 / L, 4),
             "pct_of_hbm_peak": round(100 * value / dist.world / peak, 2),
-            "config": workload_config(spec, w.seq_lens_host, args, dist.world, l2_bytes(dev)),
+            "config": workload_config(w, args, dist.world, l2_bytes(dev)),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_kind == "measured" else "fallback",
-                         "kernel": "attention_kernel<fused>", "launch_us": round(launch_us, 3),
+                         "kernel": ("attention_kernel<fused, fp8>" if w.kv == "fp8"
+                                    else "attention_kernel<fused>"),
+                         "launch_us": round(launch_us, 3),
                          "launch_us_how": f"CUDA events around each step's graph (rope table + "
                                           f"{L} launches, gaps included) / {L}",
                          "bytes_per_launch": bytes_layer},

@@ -101,13 +101,13 @@ constexpr int64_t kFlatMinTilesPerCta = 32;
 
 // Deepest ring (a multiple of the 4 consumer warps) that still lets two
 // CTAs share an SM.
-int ring_cap(const qdec_shape *s, int cluster) {
+int ring_cap(const qdec_shape *s, int cluster, bool fp8) {
     int per_sm = smem_per_sm_of_current_device();
     if (per_sm <= 0) per_sm = 228 * 1024;
     const int w = qdec::kConsumerWarps;
     int cap = qdec::kMaxStages / w * w;
     while (cap > w && static_cast<int64_t>(qdec::kCtasPerSm) *
-                              (qdec::attention_smem_bytes(s->batch, cap, cluster) + 1024) >
+                              (qdec::attention_smem_bytes(s->batch, cap, cluster, fp8) + 1024) >
                           static_cast<int64_t>(per_sm))
         cap -= w;
     return cap;
@@ -123,24 +123,26 @@ int clamp_stages(int64_t want, int cap) {
     return static_cast<int>(st < cap ? st : cap);
 }
 
-// CTAs of cluster size c that fit on the device at once (cached per device).
-int64_t cluster_capacity(const qdec_shape *s, int c, int cap) {
+// CTAs of cluster size c that fit on the device at once (cached per device
+// and pool type).
+int64_t cluster_capacity(const qdec_shape *s, int c, int cap, bool fp8) {
     static std::mutex mu;
-    static int cache[64][qdec::kMaxCluster + 1];
-    static size_t cache_smem[64][qdec::kMaxCluster + 1];
-    const size_t smem = qdec::attention_smem_bytes(s->batch, cap, c);
+    static int cache[64][2][qdec::kMaxCluster + 1];
+    static size_t cache_smem[64][2][qdec::kMaxCluster + 1];
+    const size_t smem = qdec::attention_smem_bytes(s->batch, cap, c, fp8);
+    const int t = fp8 ? 1 : 0;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = -1;
     int n = 0;
     if (dev >= 0) {
         std::lock_guard<std::mutex> lock(mu);
-        n = cache_smem[dev][c] == smem ? cache[dev][c] : 0;
+        n = cache_smem[dev][t][c] == smem ? cache[dev][t][c] : 0;
         if (n == 0) {
-            n = qdec::max_active_clusters(c, smem);
+            n = qdec::max_active_clusters(c, smem, fp8);
             cudaGetLastError();  // a failed query leaves no sticky state behind
             if (n <= 0) n = -1;
-            cache[dev][c] = n;
-            cache_smem[dev][c] = smem;
+            cache[dev][t][c] = n;
+            cache_smem[dev][t][c] = smem;
         }
     }
     if (n > 0) return static_cast<int64_t>(n) * c;
@@ -162,7 +164,7 @@ int64_t cluster_capacity(const qdec_shape *s, int c, int cap) {
 constexpr double kBytesPerCta = 96.0 * 1024;
 constexpr double kGridShare = 0.6;
 
-Plan plan_for(const qdec_shape *s, bool allow_cluster) {
+Plan plan_for(const qdec_shape *s, bool allow_cluster, bool fp8) {
     int sms = sm_count_of_current_device();
     if (sms <= 0) sms = 1;
     const int64_t target = static_cast<int64_t>(sms) * qdec::kCtasPerSm;
@@ -172,7 +174,8 @@ Plan plan_for(const qdec_shape *s, bool allow_cluster) {
     const int64_t segs = static_cast<int64_t>(s->batch) * s->num_kv_heads;
     const int64_t nmax = (s->max_seq_len + qdec::kPageSize - 1) / qdec::kPageSize;
     if (s->num_ctas == 0 && allow_cluster && per_cta < kFlatMinTilesPerCta) {
-        const double bytes = static_cast<double>(wmax) * qdec::kTileBytes;
+        const double bytes =
+            static_cast<double>(wmax) * (fp8 ? qdec::kFp8TileBytes : qdec::kTileBytes);
         const double want = std::min(kGridShare * static_cast<double>(target), bytes / kBytesPerCta);
         Plan widest{};
         for (int64_t k = 1; k <= nmax && pl.grid == 0; ++k) {
@@ -181,13 +184,14 @@ Plan plan_for(const qdec_shape *s, bool allow_cluster) {
                 if (c * k > nmax && c > 1) continue;  // every CTA gets a page
                 const int64_t t = (nmax + c * k - 1) / (c * k);
                 const int64_t grid = c * segs * k;
-                const int cap = ring_cap(s, c);
-                if (grid > cluster_capacity(s, c, cap)) continue;
+                const int cap = ring_cap(s, c, fp8);
+                const int need = qdec::min_stages(c, fp8);
+                if (cap < need || grid > cluster_capacity(s, c, cap, fp8)) continue;
                 Plan cand{};
                 cand.cluster = c;
                 cand.chunks = static_cast<int>(k);
                 cand.grid = static_cast<int>(grid);
-                cand.stages = clamp_stages(t + 1, cap);
+                cand.stages = std::max(clamp_stages(t + 1, cap), need);
                 if (grid > widest.grid) widest = cand;
                 if (static_cast<double>(grid) >= want) pl = cand;
                 break;  // the largest cluster that fits, for this k
@@ -198,14 +202,20 @@ Plan plan_for(const qdec_shape *s, bool allow_cluster) {
     }
     const int64_t g = s->num_ctas > 0 ? s->num_ctas : (target < wmax ? target : wmax);
     pl.grid = static_cast<int>(g);
-    pl.stages = clamp_stages((wmax + g - 1) / g, ring_cap(s, 0));
+    pl.stages = clamp_stages((wmax + g - 1) / g, ring_cap(s, 0, fp8));
     return pl;
 }
 
-// Grid bound covering both layouts (sizes the workspace).
+// The FP8 pool's scale windows need an even number of KV heads.
+bool fp8_supported(const qdec_shape *s) { return s->num_kv_heads % 2 == 0; }
+
+// Grid bound covering both layouts and both pool types (sizes the
+// workspace, so one workspace serves every entry point).
 int attention_grid(const qdec_shape *s) {
-    const Plan a = plan_for(s, true), b = plan_for(s, false);
-    return a.grid > b.grid ? a.grid : b.grid;
+    int g = std::max(plan_for(s, true, false).grid, plan_for(s, false, false).grid);
+    if (fp8_supported(s))
+        g = std::max(g, std::max(plan_for(s, true, true).grid, plan_for(s, false, true).grid));
+    return g;
 }
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -243,7 +253,7 @@ void fill_inv_freq(double *dst, float theta) {
     for (int i = 0; i < qdec::kRotPairs; ++i) dst[i] = table[i];
 }
 
-void fill_common(Params &p, const qdec_shape *s, bool allow_cluster) {
+void fill_common(Params &p, const qdec_shape *s, bool allow_cluster, bool fp8 = false) {
     p.B = s->batch;
     p.Hq = s->num_q_heads;
     p.Hkv = s->num_kv_heads;
@@ -253,7 +263,7 @@ void fill_common(Params &p, const qdec_shape *s, bool allow_cluster) {
     const double scale =
         s->sm_scale > 0.f ? s->sm_scale : 1.0 / sqrt(static_cast<double>(s->head_dim));
     p.qscale = static_cast<float>(scale * 1.4426950408889634074);  // * log2(e)
-    const Plan pl = plan_for(s, allow_cluster);
+    const Plan pl = plan_for(s, allow_cluster, fp8);
     p.grid = pl.grid;
     p.stages = pl.stages;
     p.cluster = pl.cluster;
@@ -318,23 +328,43 @@ qdec_status encode_pool_map(CUtensorMap *map, const qdec_shape *s, const void *p
     return r == CUDA_SUCCESS ? QDEC_OK : QDEC_ERR_CUDA;
 }
 
+// The FP8 pool as a 4-D tensor whose box is one page tile: dims (128 bytes
+// of D, token [16], plane K/V [2], page*2*Hkv + head), strides (128,
+// Hkv*2048, 2048) bytes; 128-byte rows swizzled as in the bf16 map.
+qdec_status encode_pool_map_fp8(CUtensorMap *map, const qdec_shape *s, const void *pool8) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return QDEC_ERR_CUDA;
+    const cuuint64_t plane = static_cast<cuuint64_t>(qdec::kFp8PlaneBytes);
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(qdec::kHeadDim),
+                                static_cast<cuuint64_t>(qdec::kPageSize), 2,
+                                static_cast<cuuint64_t>(s->num_pages) * 2 * s->num_kv_heads};
+    const cuuint64_t strides[3] = {qdec::kHeadDim,
+                                   static_cast<cuuint64_t>(s->num_kv_heads) * plane, plane};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(qdec::kHeadDim),
+                               static_cast<cuuint32_t>(qdec::kPageSize), 2, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(pool8), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? QDEC_OK : QDEC_ERR_CUDA;
+}
+
 qdec_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QDEC_OK : QDEC_ERR_CUDA; }
 
 qdec_status check_new_token_args(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_stride,
                                  const qdec_bf16 *k, int64_t k_stride, const qdec_bf16 *v,
                                  int64_t v_stride, const qdec_bf16 *q_norm_w,
                                  const qdec_bf16 *k_norm_w, const int32_t *positions,
-                                 const int32_t *seq_lens, const int32_t *block_table,
-                                 const qdec_bf16 *kv_pool) {
+                                 const int32_t *seq_lens, const int32_t *block_table) {
     qdec_status st = check_shape(shape);
     if (st != QDEC_OK) return st;
     if ((st = check_row_input(q, q_stride, shape->num_q_heads)) != QDEC_OK) return st;
     if ((st = check_row_input(k, k_stride, shape->num_kv_heads)) != QDEC_OK) return st;
     if ((st = check_row_input(v, v_stride, shape->num_kv_heads)) != QDEC_OK) return st;
-    if (!q_norm_w || !k_norm_w || !positions || !seq_lens || !block_table || !kv_pool)
+    if (!q_norm_w || !k_norm_w || !positions || !seq_lens || !block_table)
         return QDEC_ERR_INVALID_ARG;
-    if (!aligned16(q_norm_w) || !aligned16(k_norm_w) || !aligned16(kv_pool))
-        return QDEC_ERR_INVALID_ARG;
+    if (!aligned16(q_norm_w) || !aligned16(k_norm_w)) return QDEC_ERR_INVALID_ARG;
     return QDEC_OK;
 }
 
@@ -342,6 +372,131 @@ qdec_status check_workspace(const qdec_shape *shape, const void *ws, size_t byte
     if (!ws || !aligned16(ws)) return QDEC_ERR_WORKSPACE;
     if (bytes < workspace_layout(shape).total) return QDEC_ERR_WORKSPACE;
     return QDEC_OK;
+}
+
+// The pool an entry point works on: bf16, or E4M3 codes with their scales.
+struct PoolArg {
+    const void *data;
+    const float *scale;  // FP8 only
+    bool fp8;
+};
+
+qdec_status check_pool(const qdec_shape *shape, const PoolArg &pool) {
+    if (!pool.data || !aligned16(pool.data)) return QDEC_ERR_INVALID_ARG;
+    if (!pool.fp8) return QDEC_OK;
+    if (!fp8_supported(shape)) return QDEC_ERR_UNSUPPORTED;
+    if (!pool.scale || !aligned16(pool.scale)) return QDEC_ERR_INVALID_ARG;
+    return QDEC_OK;
+}
+
+void bind_pool(Params &p, const PoolArg &pool) {
+    if (pool.fp8) {
+        p.pool8 = static_cast<uint8_t *>(const_cast<void *>(pool.data));
+        p.kv_scale = pool.scale;
+    } else {
+        p.pool = static_cast<__nv_bfloat16 *>(const_cast<void *>(pool.data));
+    }
+}
+
+qdec_status encode_map(CUtensorMap *map, const qdec_shape *shape, const PoolArg &pool) {
+    return pool.fp8 ? encode_pool_map_fp8(map, shape, pool.data)
+                    : encode_pool_map(map, shape, pool.data);
+}
+
+void bind_new_token(Params &p, const qdec_bf16 *q, int64_t q_stride, const qdec_bf16 *k,
+                    int64_t k_stride, const qdec_bf16 *v, int64_t v_stride,
+                    const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                    const int32_t *positions, const int32_t *seq_lens,
+                    const int32_t *block_table, const void *rope_table) {
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    p.k = reinterpret_cast<const __nv_bfloat16 *>(k);
+    p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
+    p.q_stride = q_stride;
+    p.k_stride = k_stride;
+    p.v_stride = v_stride;
+    p.w_q = reinterpret_cast<const __nv_bfloat16 *>(q_norm_w);
+    p.w_k = reinterpret_cast<const __nv_bfloat16 *>(k_norm_w);
+    p.positions = positions;
+    p.seq_lens = seq_lens;
+    p.block_table = block_table;
+    p.rope = static_cast<const qdec::RopeEntry *>(rope_table);
+}
+
+qdec_status append_rope_impl(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_stride,
+                             const qdec_bf16 *k, int64_t k_stride, const qdec_bf16 *v,
+                             int64_t v_stride, const qdec_bf16 *q_norm_w,
+                             const qdec_bf16 *k_norm_w, const int32_t *positions,
+                             const int32_t *seq_lens, const int32_t *block_table,
+                             const void *rope_table, const PoolArg &pool, float *q_rot,
+                             int32_t *err_flag, void *stream) {
+    qdec_status st = check_new_token_args(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w,
+                                          k_norm_w, positions, seq_lens, block_table);
+    if (st != QDEC_OK) return st;
+    if ((st = check_pool(shape, pool)) != QDEC_OK) return st;
+    if (rope_table && !aligned16(rope_table)) return QDEC_ERR_INVALID_ARG;
+    if (!q_rot || !aligned16(q_rot)) return QDEC_ERR_INVALID_ARG;
+    Params p{};
+    fill_common(p, shape, false, pool.fp8);
+    bind_new_token(p, q, q_stride, k, k_stride, v, v_stride, q_norm_w, k_norm_w, positions,
+                   seq_lens, block_table, rope_table);
+    bind_pool(p, pool);
+    p.q_rot_out = q_rot;
+    p.err = err_flag;
+    return cuda_status(qdec::launch_append_rope(p, pool.fp8, static_cast<cudaStream_t>(stream)));
+}
+
+qdec_status attn_split_impl(const qdec_shape *shape, const float *q_rot, const PoolArg &pool,
+                            const int32_t *block_table, const int32_t *seq_lens, void *workspace,
+                            size_t workspace_bytes, qdec_bf16 *out, int32_t *err_flag,
+                            void *stream) {
+    qdec_status st = check_shape(shape);
+    if (st != QDEC_OK) return st;
+    if ((st = check_pool(shape, pool)) != QDEC_OK) return st;
+    if (!q_rot || !block_table || !seq_lens || !out) return QDEC_ERR_INVALID_ARG;
+    if (!aligned16(q_rot) || !aligned16(out)) return QDEC_ERR_INVALID_ARG;
+    if ((st = check_workspace(shape, workspace, workspace_bytes)) != QDEC_OK) return st;
+    Params p{};
+    fill_common(p, shape, false, pool.fp8);
+    p.q_rot_in = q_rot;
+    p.seq_lens = seq_lens;
+    p.block_table = block_table;
+    bind_pool(p, pool);
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.err = err_flag;
+    p.pdl = 0;  // reads what the append just wrote: no overlap
+    bind_workspace(p, shape, workspace);
+    CUtensorMap map;
+    if ((st = encode_map(&map, shape, pool)) != QDEC_OK) return st;
+    return cuda_status(
+        qdec::launch_attention(p, map, false, pool.fp8, static_cast<cudaStream_t>(stream)));
+}
+
+qdec_status step_impl(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_stride,
+                      const qdec_bf16 *k, int64_t k_stride, const qdec_bf16 *v, int64_t v_stride,
+                      const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                      const int32_t *positions, const int32_t *seq_lens,
+                      const int32_t *block_table, const void *rope_table, const PoolArg &pool,
+                      void *workspace, size_t workspace_bytes, qdec_bf16 *out,
+                      int32_t *err_flag, void *stream) {
+    qdec_status st = check_new_token_args(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w,
+                                          k_norm_w, positions, seq_lens, block_table);
+    if (st != QDEC_OK) return st;
+    if ((st = check_pool(shape, pool)) != QDEC_OK) return st;
+    if (rope_table && !aligned16(rope_table)) return QDEC_ERR_INVALID_ARG;
+    if (!out || !aligned16(out)) return QDEC_ERR_INVALID_ARG;
+    if ((st = check_workspace(shape, workspace, workspace_bytes)) != QDEC_OK) return st;
+    Params p{};
+    fill_common(p, shape, true, pool.fp8);
+    bind_new_token(p, q, q_stride, k, k_stride, v, v_stride, q_norm_w, k_norm_w, positions,
+                   seq_lens, block_table, rope_table);
+    bind_pool(p, pool);
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.err = err_flag;
+    bind_workspace(p, shape, workspace);
+    CUtensorMap map;
+    if ((st = encode_map(&map, shape, pool)) != QDEC_OK) return st;
+    return cuda_status(
+        qdec::launch_attention(p, map, true, pool.fp8, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -386,53 +541,39 @@ qdec_status qdec_append_rope(const qdec_shape *shape, const qdec_bf16 *q, int64_
                              const int32_t *seq_lens, const int32_t *block_table,
                              const void *rope_table, qdec_bf16 *kv_pool, float *q_rot,
                              int32_t *err_flag, void *stream) {
-    qdec_status st = check_new_token_args(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w,
-                                          k_norm_w, positions, seq_lens, block_table, kv_pool);
-    if (st != QDEC_OK) return st;
-    if (rope_table && !aligned16(rope_table)) return QDEC_ERR_INVALID_ARG;
-    if (!q_rot || !aligned16(q_rot)) return QDEC_ERR_INVALID_ARG;
-    Params p{};
-    fill_common(p, shape, false);
-    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
-    p.k = reinterpret_cast<const __nv_bfloat16 *>(k);
-    p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
-    p.q_stride = q_stride;
-    p.k_stride = k_stride;
-    p.v_stride = v_stride;
-    p.w_q = reinterpret_cast<const __nv_bfloat16 *>(q_norm_w);
-    p.w_k = reinterpret_cast<const __nv_bfloat16 *>(k_norm_w);
-    p.positions = positions;
-    p.seq_lens = seq_lens;
-    p.block_table = block_table;
-    p.pool = reinterpret_cast<__nv_bfloat16 *>(kv_pool);
-    p.q_rot_out = q_rot;
-    p.rope = static_cast<const qdec::RopeEntry *>(rope_table);
-    p.err = err_flag;
-    return cuda_status(qdec::launch_append_rope(p, static_cast<cudaStream_t>(stream)));
+    return append_rope_impl(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w, k_norm_w,
+                            positions, seq_lens, block_table, rope_table,
+                            PoolArg{kv_pool, nullptr, false}, q_rot, err_flag, stream);
+}
+
+qdec_status qdec_append_rope_fp8(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_stride,
+                                 const qdec_bf16 *k, int64_t k_stride, const qdec_bf16 *v,
+                                 int64_t v_stride, const qdec_bf16 *q_norm_w,
+                                 const qdec_bf16 *k_norm_w, const int32_t *positions,
+                                 const int32_t *seq_lens, const int32_t *block_table,
+                                 const void *rope_table, uint8_t *kv_pool_fp8,
+                                 const float *kv_scale, float *q_rot, int32_t *err_flag,
+                                 void *stream) {
+    return append_rope_impl(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w, k_norm_w,
+                            positions, seq_lens, block_table, rope_table,
+                            PoolArg{kv_pool_fp8, kv_scale, true}, q_rot, err_flag, stream);
 }
 
 qdec_status qdec_attn_split(const qdec_shape *shape, const float *q_rot, const qdec_bf16 *kv_pool,
                             const int32_t *block_table, const int32_t *seq_lens, void *workspace,
                             size_t workspace_bytes, qdec_bf16 *out, int32_t *err_flag,
                             void *stream) {
-    qdec_status st = check_shape(shape);
-    if (st != QDEC_OK) return st;
-    if (!q_rot || !kv_pool || !block_table || !seq_lens || !out) return QDEC_ERR_INVALID_ARG;
-    if (!aligned16(q_rot) || !aligned16(kv_pool) || !aligned16(out)) return QDEC_ERR_INVALID_ARG;
-    if ((st = check_workspace(shape, workspace, workspace_bytes)) != QDEC_OK) return st;
-    Params p{};
-    fill_common(p, shape, false);
-    p.q_rot_in = q_rot;
-    p.seq_lens = seq_lens;
-    p.block_table = block_table;
-    p.pool = reinterpret_cast<__nv_bfloat16 *>(const_cast<qdec_bf16 *>(kv_pool));
-    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
-    p.err = err_flag;
-    p.pdl = 0;  // reads what qdec_append_rope just wrote: no overlap
-    bind_workspace(p, shape, workspace);
-    CUtensorMap map;
-    if ((st = encode_pool_map(&map, shape, kv_pool)) != QDEC_OK) return st;
-    return cuda_status(qdec::launch_attention(p, map, false, static_cast<cudaStream_t>(stream)));
+    return attn_split_impl(shape, q_rot, PoolArg{kv_pool, nullptr, false}, block_table, seq_lens,
+                           workspace, workspace_bytes, out, err_flag, stream);
+}
+
+qdec_status qdec_attn_split_fp8(const qdec_shape *shape, const float *q_rot,
+                                const uint8_t *kv_pool_fp8, const float *kv_scale,
+                                const int32_t *block_table, const int32_t *seq_lens,
+                                void *workspace, size_t workspace_bytes, qdec_bf16 *out,
+                                int32_t *err_flag, void *stream) {
+    return attn_split_impl(shape, q_rot, PoolArg{kv_pool_fp8, kv_scale, true}, block_table,
+                           seq_lens, workspace, workspace_bytes, out, err_flag, stream);
 }
 
 qdec_status qdec_attn_merge(const qdec_shape *shape, const int32_t *seq_lens,
@@ -458,33 +599,22 @@ qdec_status qdec_step(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_str
                       const int32_t *block_table, const void *rope_table, qdec_bf16 *kv_pool,
                       void *workspace, size_t workspace_bytes, qdec_bf16 *out,
                       int32_t *err_flag, void *stream) {
-    qdec_status st = check_new_token_args(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w,
-                                          k_norm_w, positions, seq_lens, block_table, kv_pool);
-    if (st != QDEC_OK) return st;
-    if (rope_table && !aligned16(rope_table)) return QDEC_ERR_INVALID_ARG;
-    if (!out || !aligned16(out)) return QDEC_ERR_INVALID_ARG;
-    if ((st = check_workspace(shape, workspace, workspace_bytes)) != QDEC_OK) return st;
-    Params p{};
-    fill_common(p, shape, true);
-    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
-    p.k = reinterpret_cast<const __nv_bfloat16 *>(k);
-    p.v = reinterpret_cast<const __nv_bfloat16 *>(v);
-    p.q_stride = q_stride;
-    p.k_stride = k_stride;
-    p.v_stride = v_stride;
-    p.w_q = reinterpret_cast<const __nv_bfloat16 *>(q_norm_w);
-    p.w_k = reinterpret_cast<const __nv_bfloat16 *>(k_norm_w);
-    p.positions = positions;
-    p.seq_lens = seq_lens;
-    p.block_table = block_table;
-    p.pool = reinterpret_cast<__nv_bfloat16 *>(kv_pool);
-    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
-    p.rope = static_cast<const qdec::RopeEntry *>(rope_table);
-    p.err = err_flag;
-    bind_workspace(p, shape, workspace);
-    CUtensorMap map;
-    if ((st = encode_pool_map(&map, shape, kv_pool)) != QDEC_OK) return st;
-    return cuda_status(qdec::launch_attention(p, map, true, static_cast<cudaStream_t>(stream)));
+    return step_impl(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w, k_norm_w, positions,
+                     seq_lens, block_table, rope_table, PoolArg{kv_pool, nullptr, false},
+                     workspace, workspace_bytes, out, err_flag, stream);
+}
+
+qdec_status qdec_step_fp8(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_stride,
+                          const qdec_bf16 *k, int64_t k_stride, const qdec_bf16 *v,
+                          int64_t v_stride, const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                          const int32_t *positions, const int32_t *seq_lens,
+                          const int32_t *block_table, const void *rope_table,
+                          uint8_t *kv_pool_fp8, const float *kv_scale, void *workspace,
+                          size_t workspace_bytes, qdec_bf16 *out, int32_t *err_flag,
+                          void *stream) {
+    return step_impl(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w, k_norm_w, positions,
+                     seq_lens, block_table, rope_table, PoolArg{kv_pool_fp8, kv_scale, true},
+                     workspace, workspace_bytes, out, err_flag, stream);
 }
 
 qdec_status qdec_check_error(int32_t *err_flag, void *stream, int32_t *flags_out) {

@@ -23,6 +23,17 @@ constexpr int kMaxStages = 24;                             // ring of page tiles
 constexpr int kTileHalfBytes = kPageSize * 64 * 2;         // 16 rows x 64 dims bf16 = 2 KiB
 constexpr int kPlaneBytes = 2 * kTileHalfBytes;            // one (page, plane, head) = 4 KiB
 constexpr int kTileBytes = 2 * kPlaneBytes;                // K + V = 8 KiB
+// FP8 (E4M3) pool: one byte per element, so a (page, plane, head) is 16
+// rows of 128 bytes and a page tile K + V is 4 KiB.  Each tile also brings
+// two 16-byte windows of kv_scale (the aligned 4-float groups holding its K
+// and its V scale).
+constexpr int kFp8PlaneBytes = kPageSize * kHeadDim;       // 2 KiB
+constexpr int kFp8TileBytes = 2 * kFp8PlaneBytes;          // 4 KiB
+constexpr int kScaleWindowBytes = 16;
+constexpr int kFp8SlotExtra = 2 * kScaleWindowBytes;       // per ring slot
+// Cluster layout: the largest cluster whose peers' pieces get their own
+// receive buffer; larger clusters receive in rank 0's drained ring.
+constexpr int kMaxDirectRecv = 6;
 constexpr int kCtasPerSm = 2;
 constexpr int kMaxCluster = 8;                             // portable cluster size
 
@@ -49,6 +60,8 @@ struct Params {
     const RopeEntry *rope;   // [B][D/2] per-step table, or null: angles computed in-kernel
     RopeEntry *rope_out;     // rope-table kernel output
     __nv_bfloat16 *pool;
+    uint8_t *pool8;          // E4M3 pool (FP8 entry points), same layout as pool
+    const float *kv_scale;   // FP8: [num_pages][2][Hkv] scale of each (page, plane, head)
     const float *q_rot_in;   // split kernel (unfused): normed + rotated q rows
     float *q_rot_out;        // append kernel: normed + rotated q rows
     float *ws_o;             // [pieces][G][D] partial outputs (normalised)
@@ -68,16 +81,21 @@ struct Params {
 };
 
 // Dynamic shared memory of the attention kernel for batch B, `stages` ring
-// slots and the given layout (cluster = 0: flat; C > 0: C-CTA clusters).
-size_t attention_smem_bytes(int B, int stages, int cluster);
+// slots, the given layout (cluster = 0: flat; C > 0: C-CTA clusters) and
+// pool element type (fp8: E4M3, else bf16).
+size_t attention_smem_bytes(int B, int stages, int cluster, bool fp8);
+
+// Smallest ring depth the cluster layout of C CTAs needs: with C above
+// kMaxDirectRecv rank 0 receives its peers' pieces in its drained ring.
+int min_stages(int cluster, bool fp8);
 
 // Clusters of `cluster` CTAs (each with `smem` bytes of dynamic shared
 // memory) that can be resident at once on the current device (0 if unknown).
-int max_active_clusters(int cluster, size_t smem);
+int max_active_clusters(int cluster, size_t smem, bool fp8);
 
 cudaError_t launch_rope_table(const Params &p, cudaStream_t s);
-cudaError_t launch_append_rope(const Params &p, cudaStream_t s);
-cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, bool fused,
+cudaError_t launch_append_rope(const Params &p, bool fp8, cudaStream_t s);
+cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, bool fused, bool fp8,
                              cudaStream_t s);
 cudaError_t launch_merge(const Params &p, cudaStream_t s);
 

@@ -32,6 +32,13 @@
 // bf16 hi + lo pairs, so the products carry ~16 mantissa bits while K and V
 // enter exactly; the softmax statistics stay in fp32.
 //
+// With an FP8 (E4M3) pool the tiles are 4 KiB; each also brings its two
+// scales (16-byte windows of kv_scale) on the same barrier.  The warp turns
+// codes into f16 pairs (exact) and runs the same two products with f16
+// mma.sync; the K scale multiplies the scores, the V scale each tile's
+// contribution to O^T.  The new token's k and v are quantized with the
+// scales of their page: fp32 division, then E4M3 nearest-even, saturating.
+//
 // The producer reads only data that no kernel of the step writes (seq_lens,
 // the block table, cached pool pages), so when the launch is a programmatic
 // dependent of the previous layer it streams pages while that layer is still
@@ -40,6 +47,8 @@
 #include "qdec_internal.h"
 #include "qdec.h"
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include <mutex>
@@ -79,8 +88,13 @@ static_assert(kOffKvNew % 16 == 0 && kOffRope % 16 == 0 && kOffBar % 8 == 0 &&
               kOffOs % 16 == 0 && kOffPbuf % 4 == 0 && kRecvSlotBytes % 16 == 0,
               "smem alignment");
 static_assert(kOsBytes <= kTileBytes, "the warp-combine scratch fits in one ring slot");
-static_assert(kTileBytes + (kMaxCluster - 1) * kRecvSlotBytes <= 4 * kTileBytes,
-              "the receive buffer fits in ring slots 1..3");
+static_assert(kOsBytes + (kMaxCluster - 1) * kRecvSlotBytes <= 4 * kTileBytes,
+              "scratch and receive buffer fit in a 4-slot bf16 ring");
+// bytes of one ring slot (the FP8 scale windows live after the ring)
+template <bool kFp8>
+__host__ __device__ constexpr int slot_bytes() {
+    return kFp8 ? kFp8TileBytes : kTileBytes;
+}
 
 // From kOffOs on, the layouts differ:
 //   flat (C = 0):   os[warps][G][D] (the warp combine of each piece), then
@@ -91,9 +105,10 @@ static_assert(kTileBytes + (kMaxCluster - 1) * kRecvSlotBytes <= 4 * kTileBytes,
 //                   ring from slot 1 on (peers push only after rank 0 has
 //                   arrived on the cluster barrier with its tiles consumed).
 // In both cluster layouts one piece per CTA, so once the ring has drained
-// slot 0 is the warp-combine scratch.  kMaxDirectRecv is the largest C whose
-// receive buffer still leaves room for a 12-slot ring at 2 CTAs per SM.
-constexpr int kMaxDirectRecv = 6;
+// its first kOsBytes are the warp-combine scratch (and a receiving ring
+// takes the peers' pieces right after).  kMaxDirectRecv is the largest C
+// whose receive buffer still leaves room for a 12-slot bf16 ring at 2 CTAs
+// per SM.
 __host__ __device__ constexpr bool ring_receives(int C) { return C > kMaxDirectRecv; }
 __host__ __device__ constexpr int pre_offset(int C) {
     return kOffOs + (C == 0 ? kOsBytes : ring_receives(C) ? 0 : (C - 1) * kRecvSlotBytes);
@@ -162,6 +177,34 @@ __device__ __forceinline__ void tma_load_tile(uint32_t dst, const CUtensorMap *m
         "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(plane_row), "r"(bar)
         : "memory");
 }
+// One FP8 page tile: [plane][token][128 bytes of D], 4 KiB, 128-byte
+// swizzled rows.  The tensor map is 4-D (bytes of D, token, plane,
+// page*2*Hkv + head).
+__device__ __forceinline__ void tma_load_tile_fp8(uint32_t dst, const CUtensorMap *map,
+                                                  int plane_row, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %2, %2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(plane_row), "r"(bar)
+        : "memory");
+}
+// Plain bulk copy global -> shared (16-byte aligned addresses and size),
+// counted on the same transaction barrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -180,6 +223,36 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
         "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// D += A (16x32 E4M3, row) * B (32x8 E4M3, col), fp32 accumulate.
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// D += A (16x16 f16, row) * B (16x8 f16, col), fp32 accumulate.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Two E4M3 codes (low byte -> low half) as an f16 pair; exact, since every
+// E4M3 value is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    const __half2_raw h =
+        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+// E4M3 codes of a / s and b / s (fp32 division, one rounding each, then
+// nearest-even with saturation to +-448), a in the low byte.
+__device__ __forceinline__ uint32_t quantize2_e4m3(float a, float b, float s) {
+    return static_cast<uint32_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s)), __NV_SATFINITE,
+                                 __NV_E4M3));
 }
 __device__ __forceinline__ void consumer_sync() {  // the 128 consumer threads only
     asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -431,7 +504,9 @@ __device__ void key_row(const Params &p, __nv_bfloat162 ka, __nv_bfloat162 kc, _
 // The new key/value row of (sequence b, KV head g), on one warp: lane l holds
 // dims 2l, 2l+1, 64+2l, 65+2l.  bf16(k_rot) (float-float norm and rotation,
 // one rounding) and v go to kv_new in shared memory and to the pool slot of
-// token L-1.
+// token L-1.  With an FP8 pool both rows are first quantized with the K and
+// V scales of that slot's (page, head): kv_new then holds 128 K codes and
+// 128 V codes.
 struct KvIn {
     __nv_bfloat162 ka, kc, wka, wkc;
     uint32_t va, vc;
@@ -464,10 +539,47 @@ __device__ __forceinline__ KvIn load_kv_inputs(const Params &p, int b, int g, in
     return in;
 }
 
+template <bool kFp8>
 __device__ void key_value_row(const Params &p, int b, int g, int L, uint8_t *sm, const KvIn &in) {
     const int lane = threadIdx.x & 31;
     __nv_bfloat16 kb[4];
     key_row(p, in.ka, in.kc, in.wka, in.wkc, in.e0, in.e1, kb);
+    if constexpr (kFp8) {
+        const int slot = L - 1;
+        const bool page_ok = in.page >= 0 && in.page < p.num_pages;
+        float sk = 1.f, sv = 1.f;
+        if (page_ok) {
+            const int64_t si = static_cast<int64_t>(in.page) * 2 * p.Hkv + g;
+            sk = p.kv_scale[si];
+            sv = p.kv_scale[si + p.Hkv];
+        }
+        const __nv_bfloat162 va = *reinterpret_cast<const __nv_bfloat162 *>(&in.va);
+        const __nv_bfloat162 vc = *reinterpret_cast<const __nv_bfloat162 *>(&in.vc);
+        const uint32_t k0 = quantize2_e4m3(__bfloat162float(kb[0]), __bfloat162float(kb[1]), sk);
+        const uint32_t k1 = quantize2_e4m3(__bfloat162float(kb[2]), __bfloat162float(kb[3]), sk);
+        const uint32_t v0 = quantize2_e4m3(__low2float(va), __high2float(va), sv);
+        const uint32_t v1 = quantize2_e4m3(__low2float(vc), __high2float(vc), sv);
+        uint16_t *kv_new = reinterpret_cast<uint16_t *>(sm + kOffKvNew);  // [K 128 B][V 128 B]
+        kv_new[lane] = static_cast<uint16_t>(k0);
+        kv_new[32 + lane] = static_cast<uint16_t>(k1);
+        kv_new[64 + lane] = static_cast<uint16_t>(v0);
+        kv_new[96 + lane] = static_cast<uint16_t>(v1);
+        if (page_ok) {
+            const int64_t row =
+                ((static_cast<int64_t>(in.page) * 2 * p.Hkv + g) * kPageSize + slot % kPageSize) *
+                kHeadDim;
+            uint16_t *kdst = reinterpret_cast<uint16_t *>(p.pool8 + row);
+            uint16_t *vdst = reinterpret_cast<uint16_t *>(
+                p.pool8 + row + static_cast<int64_t>(p.Hkv) * kPageSize * kHeadDim);
+            kdst[lane] = static_cast<uint16_t>(k0);
+            kdst[32 + lane] = static_cast<uint16_t>(k1);
+            vdst[lane] = static_cast<uint16_t>(v0);
+            vdst[32 + lane] = static_cast<uint16_t>(v1);
+        } else if (lane == 0) {
+            flag_error(p.err, QDEC_FLAG_BAD_PAGE);
+        }
+        return;
+    }
     const uint32_t k0 = pack_bf16(kb[0], kb[1]), k1 = pack_bf16(kb[2], kb[3]);
     uint32_t *kv_new = reinterpret_cast<uint32_t *>(sm + kOffKvNew);
     kv_new[lane] = k0;
@@ -491,6 +603,53 @@ __device__ void key_value_row(const Params &p, int b, int g, int L, uint8_t *sm,
     }
 }
 
+// FP8 pools multiply K codes as they are (E4M3 mma.sync, m16n8k32), so the
+// query row goes in as E4M3 too, split into four terms: with 2^e putting the
+// row's largest magnitude in [128, 256),
+//   q * 2^e = T0 + T1 / 16 + T2 / 256 + T3 / 4096 + (error below 2^-16 of it),
+// each T_i the E4M3 value nearest to what the previous terms left (times 16).
+// Row w of the group (lane l: dims 2l, 2l+1, 64+2l, 65+2l, scaled) writes
+// term i to operand column 4i + w of q8 ([16][kQ8Stride] bytes: columns 0-7
+// feed n-tile 0, 8-15 n-tile 1) and 2^-e to the head's unscale slot.
+constexpr int kQ8Stride = 136;                                  // bytes per operand column
+constexpr int kOffQScale = kOffKvNew + 2 * kHeadDim;             // float [G], after the FP8 kv_new
+static_assert(16 * kQ8Stride <= kOffKvNew - kOffQb, "FP8 q operand fits the q buffer");
+static_assert(kOffQScale + kGroup * 4 <= kOffRope, "unscale slots fit the kv_new buffer");
+
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
+    const __half2_raw h =
+        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
+    return make_float2(__half2float(__ushort_as_half(h.x)), __half2float(__ushort_as_half(h.y)));
+}
+
+__device__ void store_q_e4m3(uint8_t *sm, int w, int lane, const float (&ys)[4]) {
+    float amax = fmaxf(fmaxf(fabsf(ys[0]), fabsf(ys[1])), fmaxf(fabsf(ys[2]), fabsf(ys[3])));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+    int e = 0;
+    if (amax > 0.f && amax <= 3.0e38f) e = 134 - static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF);
+    float x[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) x[k] = ldexpf(ys[k], e);
+    uint8_t *q8 = sm + kOffQb;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t c01 = static_cast<uint32_t>(
+            __nv_cvt_float2_to_fp8x2(make_float2(x[0], x[1]), __NV_SATFINITE, __NV_E4M3));
+        const uint32_t c23 = static_cast<uint32_t>(
+            __nv_cvt_float2_to_fp8x2(make_float2(x[2], x[3]), __NV_SATFINITE, __NV_E4M3));
+        uint16_t *col = reinterpret_cast<uint16_t *>(q8 + (4 * i + w) * kQ8Stride);
+        col[lane] = static_cast<uint16_t>(c01);
+        col[32 + lane] = static_cast<uint16_t>(c23);
+        const float2 d01 = e4m3x2_to_float2(c01), d23 = e4m3x2_to_float2(c23);
+        x[0] = (x[0] - d01.x) * 16.f;
+        x[1] = (x[1] - d01.y) * 16.f;
+        x[2] = (x[2] - d23.x) * 16.f;
+        x[3] = (x[3] - d23.y) * 16.f;
+    }
+    if (lane == 0) reinterpret_cast<float *>(sm + kOffQScale)[w] = ldexpf(1.f, -e);
+}
+
 // Bounds of the new-token work of (sequence b, KV head g) with L tokens.
 __device__ __forceinline__ bool new_token_in_bounds(const Params &p, int b, int g, int L) {
     return in_bounds(p, b >= 0 && b < p.B && g >= 0 && g < p.Hkv && L >= 1 &&
@@ -502,9 +661,10 @@ __device__ __forceinline__ bool new_token_in_bounds(const Params &p, int b, int 
 // dims 2l, 2l+1, 64+2l, 65+2l: both members of two rotate-half pairs.  With
 // need_k, warp 0 then also produces and appends the key/value row.
 //
-// Q_OUT = 0: scaled bf16 hi/lo operand rows into shared memory (qb);
+// Q_OUT = 0: scaled hi/lo operand rows into shared memory (qb), bf16 (or
+// f16 for an FP8 pool, whose tiles are multiplied in f16);
 // Q_OUT = 1: fp32 rows to p.q_rot_out (unscaled).
-template <int Q_OUT>
+template <int Q_OUT, bool kFp8>
 __device__ void new_token_rows(const Params &p, int b, int g, int L, bool need_k, uint8_t *sm) {
     const int t = threadIdx.x, w = t >> 5, lane = t & 31;
     if (!new_token_in_bounds(p, b, g, L)) return;  // uniform over the CTA
@@ -536,7 +696,10 @@ __device__ void new_token_rows(const Params &p, int b, int g, int L, bool need_k
     const float y2 = x[2] * e0.c_hi + x[0] * e0.s_hi;
     const float y1 = x[1] * e1.c_hi - x[3] * e1.s_hi;
     const float y3 = x[3] * e1.c_hi + x[1] * e1.s_hi;
-    if (Q_OUT == 0) {
+    if (Q_OUT == 0 && kFp8) {
+        const float ys[4] = {y0 * p.qscale, y1 * p.qscale, y2 * p.qscale, y3 * p.qscale};
+        store_q_e4m3(sm, w, lane, ys);
+    } else if (Q_OUT == 0) {
         __nv_bfloat16 *qb = reinterpret_cast<__nv_bfloat16 *>(sm + kOffQb);
         const float ys[4] = {y0 * p.qscale, y1 * p.qscale, y2 * p.qscale, y3 * p.qscale};
         __nv_bfloat16 hi[4], lo[4];
@@ -556,7 +719,7 @@ __device__ void new_token_rows(const Params &p, int b, int g, int L, bool need_k
         reinterpret_cast<float2 *>(dst)[lane] = make_float2(y0, y1);
         reinterpret_cast<float2 *>(dst + 64)[lane] = make_float2(y2, y3);
     }
-    if (need_k && w == 0) key_value_row(p, b, g, L, sm, load_kv_inputs(p, b, g, L));
+    if (need_k && w == 0) key_value_row<kFp8>(p, b, g, L, sm, load_kv_inputs(p, b, g, L));
 }
 
 // ----------------------------------------------------------- tile math --
@@ -681,6 +844,155 @@ __device__ void fix_tile(uint8_t *tile, int ntok, bool patch, const __nv_bfloat1
     __syncwarp();
 }
 
+// The same tile on an FP8 pool.  The order of the reduction dimension is
+// free in both products, so each lane reads whole 16-byte runs of a row:
+//   S^T = K q^T on E4M3 codes as they are (m16n8k32): lane (tg, c) reads
+//     dims 32c .. 32c+31 of tokens tg and tg + 8; in k-step j the bytes
+//     32c+8j .. 32c+8j+7 stand for MMA columns 4c .. 4c+3 and 16+4c ..
+//     16+4c+3, and q's four E4M3 terms are read the same way (n-tile 0:
+//     terms 0, 1; n-tile 1: terms 2, 3; column 4i + h within the pair);
+//   O^T += V^T P^T in f16 (m16n8k16): the MMA rows of m-tile mt are dims
+//     16r + mt (r < 8) and 16(r-8) + 8 + mt, so lane (tg, c) reads dims
+//     16tg .. 16tg+15 of tokens 2c, 2c+1, 2c+8, 2c+9, pairs the tokens'
+//     bytes with byte permutes and turns them into f16 (exact).
+// Accumulator element o[mt][e] then holds dim 16tg + 8(e >> 1) + mt.  The K
+// scale and the query terms' 2^-e multiply the scores, the V scale each
+// m-tile's product.
+__device__ __forceinline__ void tile_math_fp8(uint32_t ks, uint32_t vs, const uint32_t (&qf)[8][2],
+                                              int ntok, int lane, WarpState &st, __half *pbuf,
+                                              float uA, float uB, float sv) {
+    const int tg = lane >> 2, c = lane & 3;
+    const uint4 k0 = lds128(ks + tg * 128 + (((2 * c) ^ tg) << 4));
+    const uint4 k1 = lds128(ks + tg * 128 + (((2 * c + 1) ^ tg) << 4));
+    const uint4 k2 = lds128(ks + (tg + 8) * 128 + (((2 * c) ^ tg) << 4));
+    const uint4 k3 = lds128(ks + (tg + 8) * 128 + (((2 * c + 1) ^ tg) << 4));
+    const uint32_t kr[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+    const uint32_t kr8[8] = {k2.x, k2.y, k2.z, k2.w, k3.x, k3.y, k3.z, k3.w};
+    // two accumulators per n-tile (even and odd k-steps): shorter chains
+    float t0e[4] = {0.f, 0.f, 0.f, 0.f}, t0o[4] = {0.f, 0.f, 0.f, 0.f};
+    float t1e[4] = {0.f, 0.f, 0.f, 0.f}, t1o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t a[4] = {kr[2 * j], kr8[2 * j], kr[2 * j + 1], kr8[2 * j + 1]};
+        mma_e4m3(j & 1 ? t0o : t0e, a, qf[j][0], qf[j][1]);
+        mma_e4m3(j & 1 ? t1o : t1e, a, qf[4 + j][0], qf[4 + j][1]);
+    }
+    // columns 2c, 2c+1: terms 0 (c < 2) or 1 (c >= 2) in n-tile 0, terms 2
+    // or 3 in n-tile 1; the partner lane c ^ 2 holds the other term of each
+    float s[4];
+    const bool lead = c < 2;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float x = (t0e[e] + t0o[e]) + (t1e[e] + t1o[e]) * (1.f / 256.f);
+        const float y = __shfl_xor_sync(kFull, x, 2);
+        s[e] = lead ? x + y * (1.f / 16.f) : y + x * (1.f / 16.f);
+        s[e] *= (e & 1) ? uB : uA;
+    }
+    const bool v0 = tg < ntok, v1 = tg + 8 < ntok;
+    const float sA0 = v0 ? s[0] : kNegInf, sB0 = v0 ? s[1] : kNegInf;
+    const float sA1 = v1 ? s[2] : kNegInf, sB1 = v1 ? s[3] : kNegInf;
+    const bool grow = fmaxf(sA0, sA1) > st.mA + kRescaleThreshold ||
+                      fmaxf(sB0, sB1) > st.mB + kRescaleThreshold;
+    if (__any_sync(kFull, grow)) {
+        float tA = fmaxf(sA0, sA1), tB = fmaxf(sB0, sB1);
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            tA = fmaxf(tA, __shfl_xor_sync(kFull, tA, o));
+            tB = fmaxf(tB, __shfl_xor_sync(kFull, tB, o));
+        }
+        const float nA = fmaxf(st.mA, tA), nB = fmaxf(st.mB, tB);
+        const float aA = st.mA == kNegInf ? 0.f : exp2f(st.mA - nA);
+        const float aB = st.mB == kNegInf ? 0.f : exp2f(st.mB - nB);
+        st.mA = nA;
+        st.mB = nB;
+        st.lA *= aA;
+        st.lB *= aB;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            st.o[mt][0] *= aA;
+            st.o[mt][2] *= aA;
+            st.o[mt][1] *= aB;
+            st.o[mt][3] *= aB;
+        }
+    }
+    const float bA = st.mA == kNegInf ? 0.f : st.mA;
+    const float bB = st.mB == kNegInf ? 0.f : st.mB;
+    const float pA0 = exp2f(sA0 - bA), pA1 = exp2f(sA1 - bA);
+    const float pB0 = exp2f(sB0 - bB), pB1 = exp2f(sB1 - bB);
+    st.lA += pA0 + pA1;
+    st.lB += pB0 + pB1;
+
+    // P^T operand in f16 (p <= 2^8 between rescales): column n < 4 holds
+    // f16(p) of head n, column 4 + n the f16 remainder; row = token.
+    const bool hi = c < 2;
+    const int colA = (hi ? 0 : kGroup) + 2 * (c & 1);
+    auto part = [hi](float v) {
+        const __half h = __float2half_rn(v);
+        return hi ? h : __float2half_rn(v - __half2float(h));
+    };
+    pbuf[colA * 16 + tg] = part(pA0);
+    pbuf[colA * 16 + tg + 8] = part(pA1);
+    pbuf[(colA + 1) * 16 + tg] = part(pB0);
+    pbuf[(colA + 1) * 16 + tg + 8] = part(pB1);
+    __syncwarp();
+    const uint32_t b0 = *reinterpret_cast<const uint32_t *>(pbuf + tg * 16 + 2 * c);
+    const uint32_t b1 = *reinterpret_cast<const uint32_t *>(pbuf + tg * 16 + 2 * c + 8);
+    // rows 2c, 2c+1, 2c+8, 2c+9 (swizzle row index & 7: 2c, 2c+1, 2c, 2c+1)
+    const uint4 va = lds128(vs + (2 * c) * 128 + ((tg ^ (2 * c)) << 4));
+    const uint4 vb = lds128(vs + (2 * c + 1) * 128 + ((tg ^ (2 * c + 1)) << 4));
+    const uint4 vc = lds128(vs + (2 * c + 8) * 128 + ((tg ^ (2 * c)) << 4));
+    const uint4 vd = lds128(vs + (2 * c + 9) * 128 + ((tg ^ (2 * c + 1)) << 4));
+    const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+    const uint32_t wc[4] = {vc.x, vc.y, vc.z, vc.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
+    // token pairs of byte 4w + i: i = 0, 1 in the halves of perm 0x5140, i = 2, 3 of 0x7362
+    uint32_t lo01[4], lo23[4], hi01[4], hi23[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        lo01[w] = __byte_perm(wa[w], wb[w], 0x5140);
+        lo23[w] = __byte_perm(wa[w], wb[w], 0x7362);
+        hi01[w] = __byte_perm(wc[w], wd[w], 0x5140);
+        hi23[w] = __byte_perm(wc[w], wd[w], 0x7362);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const int w = mt >> 2, i = mt & 3;
+        const int sh = (i & 1) * 16;
+        const uint32_t t01 = (i < 2 ? lo01[w] : lo23[w]) >> sh;       // dim 16tg + mt, tokens 2c, 2c+1
+        const uint32_t t89 = (i < 2 ? hi01[w] : hi23[w]) >> sh;       // tokens 2c+8, 2c+9
+        const uint32_t u01 = (i < 2 ? lo01[w + 2] : lo23[w + 2]) >> sh;  // dim 16tg + 8 + mt
+        const uint32_t u89 = (i < 2 ? hi01[w + 2] : hi23[w + 2]) >> sh;
+        uint32_t a[4];
+        a[0] = e4m3x2_to_f16x2(t01);
+        a[1] = e4m3x2_to_f16x2(u01);
+        a[2] = e4m3x2_to_f16x2(t89);
+        a[3] = e4m3x2_to_f16x2(u89);
+        float t[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16(t, a, b0, b1);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st.o[mt][e] = fmaf(sv, t[e], st.o[mt][e]);
+    }
+    __syncwarp();
+}
+
+// fix_tile for an FP8 tile ([plane][token][128 B]): V rows >= ntok become
+// zero; with patch, row ntok-1 of both planes takes the new codes.
+__device__ void fix_tile_fp8(uint8_t *tile, int ntok, bool patch, const uint8_t *kv_new8, int lane) {
+    if (patch && lane < 16) {
+        const int plane = lane >> 3, cc = lane & 7;
+        const int r = ntok - 1;
+        const uint4 val = reinterpret_cast<const uint4 *>(kv_new8 + plane * kHeadDim)[cc];
+        *reinterpret_cast<uint4 *>(tile + plane * kFp8PlaneBytes + r * 128 + ((cc ^ (r & 7)) << 4)) =
+            val;
+    }
+    const int rows = kPageSize - ntok;
+    for (int e = lane; e < rows * 8; e += 32) {
+        const int r = ntok + (e >> 3), cc = e & 7;
+        *reinterpret_cast<uint4 *>(tile + kFp8PlaneBytes + r * 128 + cc * 16) = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();  // ordered before the ring slot is refilled by TMA
+    __syncwarp();
+}
+
 // Log-sum-exp merge of the np partials with workspace ids pid0 .. pid0+np-1
 // into out[b][4g..4g+3].  128 threads: warp h merges head h, lane l owns
 // dims 4l..4l+3.  The lse values are fetched one per lane and the partial
@@ -779,7 +1091,7 @@ __device__ void merge_pieces(const Params &p, int64_t pid0, int b, int g, int np
 // piece and never the last one; it arrives on the kv-ready barrier (phase =
 // kv_uses, the number of such pieces before in this CTA) and the warp that
 // patches the last page waits for it.
-template <bool kFused>
+template <bool kFused, bool kFp8>
 __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint32_t full0,
                               uint32_t empty0, volatile int *slot_ok, volatile int *misc, int b,
                               int g, int pg0, int cnt, int L, int n, uint32_t &i,
@@ -800,39 +1112,58 @@ __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint3
     if (key_warp && early_kv) kv_in = load_kv_inputs(p, b, g, L);
 
     if (kFused) {
-        new_token_rows<0>(p, b, g, L, false, sm);
+        new_token_rows<0, kFp8>(p, b, g, L, false, sm);
     } else {
         const float *src =
             p.q_rot_in + (static_cast<int64_t>(b) * p.Hq + g * kGroup + warp) * kHeadDim;
         const float2 ya = reinterpret_cast<const float2 *>(src)[lane];
         const float2 yb = reinterpret_cast<const float2 *>(src + 64)[lane];
         const float ys[4] = {ya.x * p.qscale, ya.y * p.qscale, yb.x * p.qscale, yb.y * p.qscale};
-        __nv_bfloat16 h4[4], l4[4];
+        if constexpr (kFp8) {
+            store_q_e4m3(sm, warp, lane, ys);
+        } else {
+            __nv_bfloat16 h4[4], l4[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            h4[e] = __float2bfloat16_rn(ys[e]);
-            l4[e] = __float2bfloat16_rn(ys[e] - __bfloat162float(h4[e]));
+            for (int e = 0; e < 4; ++e) {
+                h4[e] = __float2bfloat16_rn(ys[e]);
+                l4[e] = __float2bfloat16_rn(ys[e] - __bfloat162float(h4[e]));
+            }
+            uint32_t *hrow = reinterpret_cast<uint32_t *>(qb + warp * kQbStride);
+            uint32_t *lrow = reinterpret_cast<uint32_t *>(qb + (kGroup + warp) * kQbStride);
+            hrow[lane] = pack_bf16(h4[0], h4[1]);
+            hrow[32 + lane] = pack_bf16(h4[2], h4[3]);
+            lrow[lane] = pack_bf16(l4[0], l4[1]);
+            lrow[32 + lane] = pack_bf16(l4[2], l4[3]);
         }
-        uint32_t *hrow = reinterpret_cast<uint32_t *>(qb + warp * kQbStride);
-        uint32_t *lrow = reinterpret_cast<uint32_t *>(qb + (kGroup + warp) * kQbStride);
-        hrow[lane] = pack_bf16(h4[0], h4[1]);
-        hrow[32 + lane] = pack_bf16(h4[2], h4[3]);
-        lrow[lane] = pack_bf16(l4[0], l4[1]);
-        lrow[32 + lane] = pack_bf16(l4[2], l4[3]);
     }
     consumer_sync();
     uint32_t qf[8][2];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const __nv_bfloat16 *row = qb + tg * kQbStride + 16 * j + 2 * c;
-        qf[j][0] = *reinterpret_cast<const uint32_t *>(row);
-        qf[j][1] = *reinterpret_cast<const uint32_t *>(row + 8);
+        if constexpr (kFp8) {  // n-tile j / 4, k-step j % 4 (see tile_math_fp8)
+            const uint2 q2 = *reinterpret_cast<const uint2 *>(
+                sm + kOffQb + ((j >> 2) * 8 + tg) * kQ8Stride + 32 * c + 8 * (j & 3));
+            qf[j][0] = q2.x;
+            qf[j][1] = q2.y;
+        } else {
+            const __nv_bfloat16 *row = qb + tg * kQbStride + 16 * j + 2 * c;
+            qf[j][0] = *reinterpret_cast<const uint32_t *>(row);
+            qf[j][1] = *reinterpret_cast<const uint32_t *>(row + 8);
+        }
+    }
+    // FP8: 2^-e of the query terms of this lane's heads 2(c&1), 2(c&1)+1
+    float qunA = 1.f, qunB = 1.f;
+    if constexpr (kFp8) {
+        const float *qs = reinterpret_cast<const float *>(sm + kOffQScale);
+        qunA = qs[2 * (c & 1)];
+        qunB = qs[2 * (c & 1) + 1];
     }
     const uint32_t kv_bar = smem_u32(sm + kOffKvReady);
     const uint32_t kv_parity = static_cast<uint32_t>(kv_uses) & 1;
     if (kFused && has_last) {
         if (warp == static_cast<int>((i + cnt) & 3)) {
-            if (key_warp) key_value_row(p, b, g, L, sm, early_kv ? kv_in : load_kv_inputs(p, b, g, L));
+            if (key_warp)
+                key_value_row<kFp8>(p, b, g, L, sm, early_kv ? kv_in : load_kv_inputs(p, b, g, L));
             __syncwarp();
             if (lane == 0) mbar_arrive(kv_bar);
         }
@@ -849,7 +1180,7 @@ __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint3
         const int pg = pg0 + k;
         const int ntok = min(kPageSize, L - pg * kPageSize);
         if (ok && slot_ok[slot]) {
-            uint8_t *tile = ring + slot * kTileBytes;
+            uint8_t *tile = ring + slot * slot_bytes<kFp8>();
             bool patch = kFused && pg == n - 1;
             if (patch && !mbar_wait_bounded(kv_bar, kv_parity, misc, p.wait_cycles)) {
                 if (lane == 0) {
@@ -858,9 +1189,23 @@ __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint3
                 }
                 patch = false;
             }
-            if (patch || ntok < kPageSize) fix_tile(tile, ntok, patch, kv_new, lane);
             const uint32_t ks = smem_u32(tile);
-            tile_math(ks, ks + kPlaneBytes, qf, ntok, lane, st, pbuf);
+            if constexpr (kFp8) {
+                if (patch || ntok < kPageSize)
+                    fix_tile_fp8(tile, ntok, patch, reinterpret_cast<const uint8_t *>(kv_new), lane);
+                // this slot's scale windows: the K scale of head g sits at
+                // float g % 4 of its window (2 Hkv scales per page, Hkv even),
+                // the V scale at (Hkv + g) % 4 of the next
+                const float *win = reinterpret_cast<const float *>(
+                    ring + NS * kFp8TileBytes + slot * kFp8SlotExtra);
+                const float sk = win[g & 3];
+                tile_math_fp8(ks, ks + kFp8PlaneBytes, qf, ntok, lane, st,
+                              reinterpret_cast<__half *>(pbuf), qunA * sk, qunB * sk,
+                              win[4 + ((p.Hkv + g) & 3)]);
+            } else {
+                if (patch || ntok < kPageSize) fix_tile(tile, ntok, patch, kv_new, lane);
+                tile_math(ks, ks + kPlaneBytes, qf, ntok, lane, st, pbuf);
+            }
         }
         __syncwarp();
         // a slot whose copy may still be landing is never handed back
@@ -881,7 +1226,10 @@ struct PieceResult {
     float M, den;
     float4 num;
 };
-// `os` is the scratch for the warps' accumulators (kOsBytes).
+// `os` is the scratch for the warps' accumulators (kOsBytes).  The
+// accumulator element o[mt][e] of lane (tg, c) holds dim 16mt + tg + 8(e>>1)
+// (bf16 tiles) or 16tg + mt + 8(e>>1) (FP8 tiles).
+template <bool kFp8>
 __device__ PieceResult combine_warps(WarpState &st, uint8_t *sm, float *os) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tg = lane >> 2, c = lane & 3;
@@ -902,10 +1250,11 @@ __device__ PieceResult combine_warps(WarpState &st, uint8_t *sm, float *os) {
         float *oB = os + (warp * kGroup + hB) * kHeadDim;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-            oA[16 * mt + tg] = st.o[mt][0];
-            oB[16 * mt + tg] = st.o[mt][1];
-            oA[16 * mt + tg + 8] = st.o[mt][2];
-            oB[16 * mt + tg + 8] = st.o[mt][3];
+            const int d = kFp8 ? 16 * tg + mt : 16 * mt + tg;
+            oA[d] = st.o[mt][0];
+            oB[d] = st.o[mt][1];
+            oA[d + 8] = st.o[mt][2];
+            oB[d + 8] = st.o[mt][3];
         }
         if (tg == 0) {
             ms[warp * kGroup + hA] = st.mA;
@@ -1002,7 +1351,7 @@ __device__ __forceinline__ float *cluster_peer(float *ptr, int rank) {
 }
 
 // ------------------------------------------------------ attention kernel --
-template <bool kFused, bool kCluster>
+template <bool kFused, bool kCluster, bool kFp8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     attention_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -1023,7 +1372,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // of the consumer warp count; then each warp waits on its slots' phases in
     // order.  Otherwise two warps could wait on consecutive phases of one slot
     // and the parity wait of the later one would pass on the earlier phase.
-    if (NS < kConsumerWarps || NS % kConsumerWarps != 0 || NS > kMaxStages) {
+    // A receiving ring must hold the combine scratch and C - 1 pieces; the
+    // FP8 scale windows need an even number of KV heads.
+    const bool ring_short = kCluster && ring_receives(p.cluster) &&
+                            NS * slot_bytes<kFp8>() < kOsBytes + (p.cluster - 1) * kRecvSlotBytes;
+    if (NS < kConsumerWarps || NS % kConsumerWarps != 0 || NS > kMaxStages || ring_short ||
+        (kFp8 && (p.Hkv & 1))) {
         if (tid == 0) flag_error(p.err, QDEC_FLAG_BAD_INDEX);
         return;  // uniform: no barrier has been touched yet
     }
@@ -1121,9 +1475,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         // test hook: this tile's barrier phase never completes
                     } else if (pj >= 0 && pj < p.num_pages && gj >= 0 && gj < p.Hkv) {
                         slot_ok[slot] = 1;
-                        mbar_arrive_expect_tx(full, kTileBytes);
-                        tma_load_tile(smem_u32(ring + slot * kTileBytes), &kv_map,
-                                      pj * 2 * p.Hkv + gj, full);
+                        if constexpr (kFp8) {
+                            // the tile and the two 4-float windows of kv_scale
+                            // holding its K and V scales (2 Hkv scales per
+                            // page with Hkv even: windows never straddle pages)
+                            const int64_t si = static_cast<int64_t>(pj) * 2 * p.Hkv + gj;
+                            const uint32_t win = smem_u32(ring + NS * kFp8TileBytes +
+                                                          slot * kFp8SlotExtra);
+                            mbar_arrive_expect_tx(full, kFp8TileBytes + kFp8SlotExtra);
+                            tma_load_tile_fp8(smem_u32(ring + slot * kFp8TileBytes), &kv_map,
+                                              pj * 2 * p.Hkv + gj, full);
+                            bulk_load(win, p.kv_scale + (si & ~3ll), kScaleWindowBytes, full);
+                            bulk_load(win + kScaleWindowBytes, p.kv_scale + ((si + p.Hkv) & ~3ll),
+                                      kScaleWindowBytes, full);
+                        } else {
+                            mbar_arrive_expect_tx(full, kTileBytes);
+                            tma_load_tile(smem_u32(ring + slot * kTileBytes), &kv_map,
+                                          pj * 2 * p.Hkv + gj, full);
+                        }
                     } else {
                         slot_ok[slot] = 0;
                         flag_error(p.err, QDEC_FLAG_BAD_PAGE);
@@ -1153,9 +1522,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const int n = pre[b + 1] - pre[b];
             WarpState st;
             reset_state(st);
-            process_piece<kFused>(p, sm, ring, full0, empty0, slot_ok, misc, b, g, w.pg, cnt, sl[b],
-                                  n, i, st, kv_uses, false);
-            const PieceResult r = combine_warps(st, sm, reinterpret_cast<float *>(sm + kOffOs));
+            process_piece<kFused, kFp8>(p, sm, ring, full0, empty0, slot_ok, misc, b, g, w.pg, cnt,
+                                        sl[b], n, i, st, kv_uses, false);
+            const PieceResult r =
+                combine_warps<kFp8>(st, sm, reinterpret_cast<float *>(sm + kOffOs));
             const long long seg0 = static_cast<long long>(p.Hkv) * pre[b] + static_cast<long long>(g) * n;
             const int j0 = cta_of(seg0, W, G);
             const int np = cta_of(seg0 + n - 1, W, G) - j0 + 1;
@@ -1178,19 +1548,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         uint32_t i = 0;
         int kv_uses = 0;
         if (cnt > 0)
-            process_piece<kFused>(p, sm, ring, full0, empty0, slot_ok, misc, cb, cg, pg_lo, cnt, cL,
-                                  cn, i, st, kv_uses, true);
+            process_piece<kFused, kFp8>(p, sm, ring, full0, empty0, slot_ok, misc, cb, cg, pg_lo,
+                                        cnt, cL, cn, i, st, kv_uses, true);
         // every tile has been consumed (so no copy is landing in the ring)
-        // before ring slot 0 becomes the combine scratch
+        // before the ring's first kOsBytes become the combine scratch
         consumer_sync();
-        PieceResult r = combine_warps(st, sm, reinterpret_cast<float *>(ring));
+        PieceResult r = combine_warps<kFp8>(st, sm, reinterpret_cast<float *>(ring));
         // a peer pushes its piece into slot crank - 1 of rank 0's receive
         // buffer; rank 0 keeps its own in registers
         const bool in_ring = ring_receives(C);
         if (crank == 0 && in_ring) cluster_arrive_release();
         cluster_wait();
         const int h = tid >> 5, d0 = (tid & 31) * 4;
-        float *recv = reinterpret_cast<float *>(in_ring ? ring + kTileBytes : sm + kOffOs);
+        float *recv = reinterpret_cast<float *>(in_ring ? ring + kOsBytes : sm + kOffOs);
         if (crank > 0) {
             float *dst = cluster_peer(recv, 0) + ((crank - 1) * kGroup + h) * kPartStride;
             *reinterpret_cast<float4 *>(dst + d0) = r.num;
@@ -1264,6 +1634,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_table_kernel(const __grid_c
 // ---------------------------------------------------------- append kernel --
 // Steps 1-3 for (KV head blockIdx.x, sequence blockIdx.y): q rows to
 // q_rot_out, k and v into the pool.
+template <bool kFp8>
 __global__ void __launch_bounds__(128) append_rope_kernel(const __grid_constant__ Params p) {
     __shared__ __align__(16) uint8_t sm[kPrologueBytes];
     const int g = blockIdx.x, b = blockIdx.y;
@@ -1272,7 +1643,7 @@ __global__ void __launch_bounds__(128) append_rope_kernel(const __grid_constant_
         if (threadIdx.x == 0 && g == 0) flag_error(p.err, QDEC_FLAG_BAD_SEQLEN);
         return;
     }
-    new_token_rows<1>(p, b, g, L, true, sm);
+    new_token_rows<1, kFp8>(p, b, g, L, true, sm);
 }
 
 // ----------------------------------------------------------- merge kernel --
@@ -1299,25 +1670,25 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Para
 // occupancy query) that needs less leaves it as it is, so a later launch
 // that needs more than a smaller request in between still finds it set.
 std::mutex g_smem_mu;
-size_t g_smem_attr[4][64];
+size_t g_smem_attr[8][64];
 
-template <bool kFused, bool kCluster>
+template <bool kFused, bool kCluster, bool kFp8>
 cudaError_t allow_smem(int dev, size_t smem) {
     std::lock_guard<std::mutex> lock(g_smem_mu);
-    size_t &attr = g_smem_attr[(kFused ? 2 : 0) + (kCluster ? 1 : 0)][dev];
+    size_t &attr = g_smem_attr[(kFp8 ? 4 : 0) + (kFused ? 2 : 0) + (kCluster ? 1 : 0)][dev];
     if (attr >= smem) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(attention_kernel<kFused, kCluster>,
+    const cudaError_t e = cudaFuncSetAttribute(attention_kernel<kFused, kCluster, kFp8>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
     if (e == cudaSuccess) attr = smem;
     return e;
 }
 
-template <bool kFused, bool kCluster>
+template <bool kFused, bool kCluster, bool kFp8>
 cudaError_t launch_one(const Params &p, const CUtensorMap &kv_map, size_t smem, int dev,
                        cudaStream_t s) {
-    auto kern = attention_kernel<kFused, kCluster>;
-    const cudaError_t e = allow_smem<kFused, kCluster>(dev, smem);
+    auto kern = attention_kernel<kFused, kCluster, kFp8>;
+    const cudaError_t e = allow_smem<kFused, kCluster, kFp8>(dev, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid);
@@ -1345,9 +1716,20 @@ cudaError_t launch_one(const Params &p, const CUtensorMap &kv_map, size_t smem, 
 
 }  // namespace
 
-size_t attention_smem_bytes(int B, int stages, int cluster) {
-    return static_cast<size_t>(ring_offset(B, cluster)) + static_cast<size_t>(stages) * kTileBytes +
-           1024;
+size_t attention_smem_bytes(int B, int stages, int cluster, bool fp8) {
+    const size_t slot = fp8 ? kFp8TileBytes + kFp8SlotExtra : kTileBytes;
+    return static_cast<size_t>(ring_offset(B, cluster)) + static_cast<size_t>(stages) * slot + 1024;
+}
+
+int min_stages(int cluster, bool fp8) {
+    int need = kConsumerWarps;
+    if (cluster > 0 && ring_receives(cluster)) {
+        const int bytes = kOsBytes + (cluster - 1) * kRecvSlotBytes;
+        const int slot = fp8 ? kFp8TileBytes : kTileBytes;
+        need = (bytes + slot - 1) / slot;
+        need = (need + kConsumerWarps - 1) / kConsumerWarps * kConsumerWarps;
+    }
+    return need;
 }
 
 static int current_device() {
@@ -1356,9 +1738,10 @@ static int current_device() {
     return d < 64 ? d : 63;
 }
 
-int max_active_clusters(int cluster, size_t smem) {
-    auto kern = attention_kernel<true, true>;
-    if (allow_smem<true, true>(current_device(), smem) != cudaSuccess) return 0;
+template <bool kFp8>
+static int max_active_clusters_of(int cluster, size_t smem) {
+    auto kern = attention_kernel<true, true, kFp8>;
+    if (allow_smem<true, true, kFp8>(current_device(), smem) != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cluster * 64);
     cfg.blockDim = dim3(kThreads);
@@ -1375,15 +1758,26 @@ int max_active_clusters(int cluster, size_t smem) {
     return n;
 }
 
-cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, bool fused,
+int max_active_clusters(int cluster, size_t smem, bool fp8) {
+    return fp8 ? max_active_clusters_of<true>(cluster, smem)
+               : max_active_clusters_of<false>(cluster, smem);
+}
+
+// The split kernel of the three-call path always runs the flat layout (its
+// merge kernel reads that layout), so it has no cluster variant.
+cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, bool fused, bool fp8,
                              cudaStream_t s) {
-    const size_t smem = attention_smem_bytes(p.B, p.stages, p.cluster);
+    const size_t smem = attention_smem_bytes(p.B, p.stages, p.cluster, fp8);
     const int dev = current_device();
-    if (fused)
-        return p.cluster ? launch_one<true, true>(p, kv_map, smem, dev, s)
-                         : launch_one<true, false>(p, kv_map, smem, dev, s);
-    return p.cluster ? launch_one<false, true>(p, kv_map, smem, dev, s)
-                     : launch_one<false, false>(p, kv_map, smem, dev, s);
+    if (!fused && p.cluster) return cudaErrorInvalidValue;
+    if (fp8) {
+        if (!fused) return launch_one<false, false, true>(p, kv_map, smem, dev, s);
+        return p.cluster ? launch_one<true, true, true>(p, kv_map, smem, dev, s)
+                         : launch_one<true, false, true>(p, kv_map, smem, dev, s);
+    }
+    if (!fused) return launch_one<false, false, false>(p, kv_map, smem, dev, s);
+    return p.cluster ? launch_one<true, true, false>(p, kv_map, smem, dev, s)
+                     : launch_one<true, false, false>(p, kv_map, smem, dev, s);
 }
 
 cudaError_t launch_rope_table(const Params &p, cudaStream_t s) {
@@ -1392,8 +1786,11 @@ cudaError_t launch_rope_table(const Params &p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_append_rope(const Params &p, cudaStream_t s) {
-    append_rope_kernel<<<dim3(p.Hkv, p.B), 128, 0, s>>>(p);
+cudaError_t launch_append_rope(const Params &p, bool fp8, cudaStream_t s) {
+    if (fp8)
+        append_rope_kernel<true><<<dim3(p.Hkv, p.B), 128, 0, s>>>(p);
+    else
+        append_rope_kernel<false><<<dim3(p.Hkv, p.B), 128, 0, s>>>(p);
     return cudaGetLastError();
 }
 

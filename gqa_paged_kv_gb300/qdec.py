@@ -35,8 +35,8 @@ QDEC_LAUNCH_TEST_WITHHOLD_TILE = 1 << 30
 # Every symbol include/qdec.h declares.
 EXPORTS = ("qdec_workspace_bytes", "qdec_workspace_init", "qdec_rope_table_bytes",
            "qdec_rope_table", "qdec_append_rope", "qdec_attn_split", "qdec_attn_merge",
-           "qdec_step", "qdec_step_static_scratch", "qdec_check_error", "qdec_status_string",
-           "qdec_version")
+           "qdec_step", "qdec_append_rope_fp8", "qdec_attn_split_fp8", "qdec_step_fp8",
+           "qdec_step_static_scratch", "qdec_check_error", "qdec_status_string", "qdec_version")
 
 QDEC_STATIC_SCRATCH_BYTES = 4 << 20
 
@@ -105,6 +105,14 @@ def _load():
     lib.qdec_step.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                               vp, vp, vp]
     lib.qdec_step.restype = st
+    lib.qdec_append_rope_fp8.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp,
+                                         vp, vp, vp, vp, vp]
+    lib.qdec_append_rope_fp8.restype = st
+    lib.qdec_attn_split_fp8.argtypes = [sp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+    lib.qdec_attn_split_fp8.restype = st
+    lib.qdec_step_fp8.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp,
+                                  vp, sz, vp, vp, vp]
+    lib.qdec_step_fp8.restype = st
     lib.qdec_step_static_scratch.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp,
                                              vp, vp, vp, vp, vp]
     lib.qdec_step_static_scratch.restype = st
@@ -205,6 +213,44 @@ def qdec_step(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, seq_lens, bl
         _ptr(block_table), _ptr(rope_table), _ptr(kv_pool), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), _ptr(err_flag),
         _stream(stream)), "qdec_step")
+
+
+def _fp8_pool(pool, scale):
+    if pool.dtype != torch.uint8 or scale.dtype != torch.float32:
+        raise ValueError("FP8 pool: expected uint8 E4M3 codes and float32 scales")
+    return _ptr(pool), _ptr(scale)
+
+
+def qdec_append_rope_fp8(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, seq_lens,
+                         block_table, kv_pool_fp8, kv_scale, q_rot, err_flag=None, stream=None,
+                         rope_table=None):
+    pool, scale = _fp8_pool(kv_pool_fp8, kv_scale)
+    _raise(_lib.qdec_append_rope_fp8(
+        ctypes.byref(shape.c()), _ptr(q), _rows(q, "q"), _ptr(k), _rows(k, "k"), _ptr(v),
+        _rows(v, "v"), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions), _ptr(seq_lens),
+        _ptr(block_table), _ptr(rope_table), pool, scale, _ptr(q_rot), _ptr(err_flag),
+        _stream(stream)), "qdec_append_rope_fp8")
+
+
+def qdec_attn_split_fp8(shape: Shape, q_rot, kv_pool_fp8, kv_scale, block_table, seq_lens,
+                        workspace, out, err_flag=None, stream=None):
+    pool, scale = _fp8_pool(kv_pool_fp8, kv_scale)
+    _raise(_lib.qdec_attn_split_fp8(
+        ctypes.byref(shape.c()), _ptr(q_rot), pool, scale, _ptr(block_table), _ptr(seq_lens),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
+        _ptr(err_flag), _stream(stream)), "qdec_attn_split_fp8")
+
+
+def qdec_step_fp8(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, seq_lens, block_table,
+                  kv_pool_fp8, kv_scale, workspace, out, err_flag=None, stream=None,
+                  rope_table=None):
+    pool, scale = _fp8_pool(kv_pool_fp8, kv_scale)
+    _raise(_lib.qdec_step_fp8(
+        ctypes.byref(shape.c()), _ptr(q), _rows(q, "q"), _ptr(k), _rows(k, "k"), _ptr(v),
+        _rows(v, "v"), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions), _ptr(seq_lens),
+        _ptr(block_table), _ptr(rope_table), pool, scale, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), _ptr(err_flag),
+        _stream(stream)), "qdec_step_fp8")
 
 
 def qdec_step_static_scratch(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, seq_lens,

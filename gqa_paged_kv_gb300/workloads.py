@@ -10,7 +10,12 @@ generators:
   generator on the target device, so multi-GiB pools are filled in HBM.
 
 Cached pool contents are drawn directly (they stand for keys that were
-normed and rotated when they were appended).  Five named workloads mirror
+normed and rotated when they were appended).  An FP8 (E4M3) variant of a
+workload holds the same draws stored as codes: every (page, plane, KV head)
+gets the scale amax/448 of its 16 x 128 values, and PyTorch's float8_e4m3fn
+cast turns value/scale into codes.  That is input synthesis (a cache filled
+by some earlier engine), not the path under test: the path's own
+quantization is the append of the new token.  Five named workloads mirror
 the decode workloads of the blog "GPU 算子与执行优化：从 26 到 100 token/s 的推理引擎破茧之路" (yuzheng310.github.io) (single stream,
 concurrency 8 and 16, an 8K context) plus a ragged continuous-batching mix.
 """
@@ -100,6 +105,9 @@ class Workload:
     pools: List[torch.Tensor] = field(default_factory=list)  # bf16 [pages][2][Hkv][P][D]
     seq_lens_host: np.ndarray = None
     block_table_host: np.ndarray = None
+    kv: str = "bf16"              # "bf16" or "fp8"
+    pools8: List[torch.Tensor] = field(default_factory=list)   # uint8 E4M3 [pages][2][Hkv][P][D]
+    scales: List[torch.Tensor] = field(default_factory=list)   # float32 [pages][2][Hkv]
 
     # strided views of the fused qkv buffer, per layer
     def q(self, layer: int) -> torch.Tensor:
@@ -116,14 +124,27 @@ class Workload:
     def pool(self, layer: int) -> torch.Tensor:
         return self.pools[0] if self.spec.shared_pool else self.pools[layer]
 
+    def pool8(self, layer: int) -> torch.Tensor:
+        return self.pools8[0] if self.spec.shared_pool else self.pools8[layer]
+
+    def scale(self, layer: int) -> torch.Tensor:
+        return self.scales[0] if self.spec.shared_pool else self.scales[layer]
+
     @property
     def max_blocks(self) -> int:
         return self.block_table.shape[1]
 
     def algorithmic_bytes_per_layer(self) -> int:
-        """KV read at token granularity plus q/k/v in and out (bf16)."""
+        """KV read at token granularity plus q/k/v in and out (bf16); for an
+        FP8 pool one byte per KV element plus the K and V scale of every
+        (page, head) a sequence reads."""
         s = self.spec
-        return int(self.seq_lens_host.sum()) * s.kv_bytes_per_token() + s.batch * s.io_bytes_per_seq()
+        io = s.batch * s.io_bytes_per_seq()
+        if self.kv == "fp8":
+            pages = int(((self.seq_lens_host + s.page_size - 1) // s.page_size).sum())
+            return (int(self.seq_lens_host.sum()) * s.kv_bytes_per_token() // 2
+                    + pages * 2 * s.num_kv_heads * 4 + io)
+        return int(self.seq_lens_host.sum()) * s.kv_bytes_per_token() + io
 
 
 def draw_seq_lens(spec: WorkloadSpec, gen: torch.Generator) -> np.ndarray:
@@ -153,13 +174,16 @@ def _fill_normal_bf16(t: torch.Tensor, gen: torch.Generator, chunk_elems: int = 
 
 
 def build(spec: WorkloadSpec, device="cpu", poison: bool = False,
-          layers: Optional[int] = None) -> Workload:
+          layers: Optional[int] = None, kv: str = "bf16") -> Workload:
     """Materialise a workload.
 
     poison=True (tests): every pool element the attention must not read is
     NaN -- pages no sequence references, the slots past each sequence's end,
     and the append slot itself (it must be overwritten before it is read).
+    kv="fp8": the pools are held as E4M3 codes plus per-(page, plane, head)
+    scales (NaN poison becomes the NaN code 0x7F); `pools` is then empty.
     """
+    assert kv in ("bf16", "fp8"), kv
     device = torch.device(device)
     nl = spec.layers if layers is None else layers
     spec = replace(spec, layers=nl)
@@ -186,7 +210,7 @@ def build(spec: WorkloadSpec, device="cpu", poison: bool = False,
     w = (torch.rand((2, nl, D), generator=gdev, device=device) + 0.5).to(torch.bfloat16)
 
     npools = 1 if spec.shared_pool else nl
-    pools = []
+    pools, pools8, scales = [], [], []
     referenced = torch.zeros(spec.pool_pages, dtype=torch.bool)
     referenced[torch.from_numpy(perm[:total].astype(np.int64))] = True
     for _ in range(npools):
@@ -194,16 +218,24 @@ def build(spec: WorkloadSpec, device="cpu", poison: bool = False,
         _fill_normal_bf16(pool, gdev)
         if spec.chan_scale:
             sc = torch.rand((2, Hkv, D), generator=gdev, device=device) * 3.9 + 0.1
-            for kv in range(2):
+            for plane in range(2):
                 for s in range(0, spec.pool_pages, 4096):
-                    blk = pool[s:s + 4096, kv].float() * sc[kv][None, :, None, :]
-                    pool[s:s + 4096, kv] = blk.to(torch.bfloat16)
+                    blk = pool[s:s + 4096, plane].float() * sc[plane][None, :, None, :]
+                    pool[s:s + 4096, plane] = blk.to(torch.bfloat16)
         if spec.spike_frac > 0:
             for s in range(0, spec.pool_pages, 4096):
                 e = min(s + 4096, spec.pool_pages)
                 m = torch.rand((e - s, Hkv, P), generator=gdev, device=device) < spec.spike_frac
                 kp = pool[s:e, 0]
                 kp[m] = kp[m] * 8  # a power of two: exact in bf16
+        if kv == "fp8":
+            codes, sc = _to_fp8(pool)
+            del pool
+            if poison:
+                _poison(codes, referenced.to(device), bt, seq_lens, P, value=0x7F)
+            pools8.append(codes)
+            scales.append(sc)
+            continue
         if poison:
             _poison(pool, referenced.to(device), bt, seq_lens, P)
         pools.append(pool)
@@ -220,16 +252,31 @@ def build(spec: WorkloadSpec, device="cpu", poison: bool = False,
         positions=torch.from_numpy((seq_lens - 1).astype(np.int32)).to(device),
         block_table=torch.from_numpy(bt).to(device),
         qkv=qkv, w_q=w[0].contiguous(), w_k=w[1].contiguous(), pools=pools,
-        seq_lens_host=seq_lens.astype(np.int64), block_table_host=bt)
+        seq_lens_host=seq_lens.astype(np.int64), block_table_host=bt, kv=kv, pools8=pools8,
+        scales=scales)
 
 
-def _poison(pool, referenced, bt, seq_lens, P):
-    nan = float("nan")
-    pool[~referenced] = nan
+def _to_fp8(pool: torch.Tensor, chunk: int = 4096):
+    """E4M3 codes and per-(page, plane, head) scales amax/448 of a bf16 pool
+    (PyTorch's float8_e4m3fn cast; magnitudes are at most 448 by construction)."""
+    codes = torch.empty(pool.shape, dtype=torch.uint8, device=pool.device)
+    sc = torch.empty(pool.shape[:3], dtype=torch.float32, device=pool.device)
+    for s in range(0, pool.shape[0], chunk):
+        x = pool[s:s + chunk].float()
+        amax = x.abs().amax(dim=(3, 4))
+        scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+        y = (x / scale[..., None, None]).clamp(-448.0, 448.0)
+        codes[s:s + chunk] = y.to(torch.float8_e4m3fn).view(torch.uint8)
+        sc[s:s + chunk] = scale
+    return codes, sc
+
+
+def _poison(pool, referenced, bt, seq_lens, P, value=float("nan")):
+    pool[~referenced] = value
     for b, L in enumerate(seq_lens):
         L = int(L)
         last = int(bt[b, (L - 1) // P])
-        pool[last, :, :, (L - 1) % P:, :] = nan   # the append slot and everything after it
+        pool[last, :, :, (L - 1) % P:, :] = value   # the append slot and everything after it
 
 
 def custom(batch: int, seq_lens, pool_pages: int, layers: int = 1, seed: int = 1234,
@@ -270,11 +317,19 @@ def oracle_inputs(w: Workload, layer: int, seqs=None):
     for i in range(len(seqs)):
         bt[i, :n[i]] = np.arange(off, off + n[i], dtype=np.int32)
         off += int(n[i])
-    pool = w.pool(layer)
-    idx = torch.from_numpy(pages.astype(np.int64)).to(pool.device)
-    sub = bf16_bits(pool.index_select(0, idx))
     sel = torch.as_tensor(seqs, dtype=torch.long, device=w.qkv.device)
-    return dict(
+    extra = {}
+    if w.kv == "fp8":
+        pool = w.pool8(layer)
+        idx = torch.from_numpy(pages.astype(np.int64)).to(pool.device)
+        sub = np.ascontiguousarray(pool.index_select(0, idx).cpu().numpy())
+        extra["kv_scale"] = np.ascontiguousarray(
+            w.scale(layer).index_select(0, idx).cpu().numpy())
+    else:
+        pool = w.pool(layer)
+        idx = torch.from_numpy(pages.astype(np.int64)).to(pool.device)
+        sub = bf16_bits(pool.index_select(0, idx))
+    return dict(extra,
         q=bf16_bits(w.q(layer).index_select(0, sel)),
         k=bf16_bits(w.k(layer).index_select(0, sel)),
         v=bf16_bits(w.v(layer).index_select(0, sel)),

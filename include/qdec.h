@@ -1,6 +1,7 @@
 /*
  * qdec.h -- C ABI of libqdec: the attention block of one GQA decode
- * layer-step over a paged bf16 KV cache, on one NVIDIA GB300 (sm_103a).
+ * layer-step over a paged bf16 (or FP8 E4M3) KV cache, on one NVIDIA GB300
+ * (sm_103a).
  *
  * What the block computes (for every sequence b of the batch, with
  * L_b = seq_lens[b] tokens including the new one, G = 4 query heads per KV
@@ -196,6 +197,62 @@ qdec_status qdec_step(const qdec_shape *shape,
                       const int32_t *block_table, const void *rope_table,
                       qdec_bf16 *kv_pool, void *workspace, size_t workspace_bytes,
                       qdec_bf16 *out, int32_t *err_flag, void *stream);
+
+/* ------------------------------------------------------------ FP8 KV pool --
+ * The same block over a KV cache held in FP8 (essay "推理引擎里面发生了什么"
+ * (locsic.com), section on quantization: an FP8 KV cache halves its memory
+ * and traffic at a negligible quality cost; the format and the scale
+ * granularity are not given there, the choices below are this library's):
+ *   kv_pool_fp8[num_pages][2][Hkv][P][D] uint8 -- OCP E4M3 codes (sign, 4
+ *     exponent bits with bias 7, 3 mantissa bits, subnormals, NaN =
+ *     S.1111.111, no infinity, largest finite 448), the bf16 pool's layout
+ *     with one byte per element (a (page, plane, head) tile is 2 KiB);
+ *   kv_scale[num_pages][2][Hkv] float -- one scale per (page, plane, KV
+ *     head): an element's value is e4m3(code) * scale.  The caller sets a
+ *     page's scales (positive, finite) before the page is first written and
+ *     owns them like the block table; the library only reads them.
+ * The append quantizes the row the bf16 entry points would store:
+ *   K code = E4M3_RNE_satfinite(fp32(bf16(k_rot)) / scale_K),
+ *   V code = E4M3_RNE_satfinite(fp32(v) / scale_V),
+ * each division rounded once to fp32, then round-to-nearest-even to E4M3 with
+ * magnitudes beyond 448 saturating to +-448.  The attention computes with the
+ * dequantized values (scores and the output in fp32, as in the bf16 path);
+ * out stays bf16 [B][Hq][D].  Requires num_kv_heads even (UNSUPPORTED
+ * otherwise); kv_pool_fp8 and kv_scale must be 16-byte aligned.  The
+ * workspace (qdec_workspace_bytes) and qdec_attn_merge serve both pool types. */
+
+/* qdec_append_rope with an FP8 pool: writes the codes of slot seq_lens[b]-1
+ * of every (sequence, KV head); kv_scale is read only. */
+qdec_status qdec_append_rope_fp8(const qdec_shape *shape,
+                                 const qdec_bf16 *q, int64_t q_stride,
+                                 const qdec_bf16 *k, int64_t k_stride,
+                                 const qdec_bf16 *v, int64_t v_stride,
+                                 const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                                 const int32_t *positions, const int32_t *seq_lens,
+                                 const int32_t *block_table, const void *rope_table,
+                                 uint8_t *kv_pool_fp8, const float *kv_scale, float *q_rot,
+                                 int32_t *err_flag, void *stream);
+
+/* qdec_attn_split over an FP8 pool; finish with qdec_attn_merge. */
+qdec_status qdec_attn_split_fp8(const qdec_shape *shape, const float *q_rot,
+                                const uint8_t *kv_pool_fp8, const float *kv_scale,
+                                const int32_t *block_table, const int32_t *seq_lens,
+                                void *workspace, size_t workspace_bytes, qdec_bf16 *out,
+                                int32_t *err_flag, void *stream);
+
+/* qdec_step over an FP8 pool: one launch for steps 1-4, the new key and
+ * value quantized into their slot as above.  Same launch flags, workspace
+ * and error reporting as qdec_step. */
+qdec_status qdec_step_fp8(const qdec_shape *shape,
+                          const qdec_bf16 *q, int64_t q_stride,
+                          const qdec_bf16 *k, int64_t k_stride,
+                          const qdec_bf16 *v, int64_t v_stride,
+                          const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                          const int32_t *positions, const int32_t *seq_lens,
+                          const int32_t *block_table, const void *rope_table,
+                          uint8_t *kv_pool_fp8, const float *kv_scale, void *workspace,
+                          size_t workspace_bytes, qdec_bf16 *out, int32_t *err_flag,
+                          void *stream);
 
 /* qdec_step without a caller-provided workspace, for callers that cannot
  * allocate device memory (e.g. a serving loop that must not call

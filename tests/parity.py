@@ -6,6 +6,10 @@ Tolerances (stated for bf16 outputs of an fp32 pipeline against fp64):
   k slot  |gpu - ref| <= 1 bf16 ulp of ref         (ref: unrounded k_rot)
   v slot  bit-equal to the input v
   q_rot   |gpu - ref| <= 2e-5 (1 + |ref|)          (fp32 output, unrounded)
+FP8 (E4M3) pools: the same out tolerance (the oracle attends over the exact
+dequantized values, so only the kernel's arithmetic is measured); the K and V
+codes of every appended slot bit-equal to the oracle's (both sides divide in
+fp32 and round to E4M3 nearest-even with saturation).
 """
 from __future__ import annotations
 
@@ -60,17 +64,31 @@ class Runner:
 
     def step(self, layer: int):
         q, w = qdec(), self.w
+        if w.kv == "fp8":
+            q.qdec_step_fp8(self.shape, w.q(layer), w.k(layer), w.v(layer), w.w_q[layer],
+                            w.w_k[layer], w.positions, w.seq_lens, w.block_table, w.pool8(layer),
+                            w.scale(layer), self.ws, self.out[layer], self.err,
+                            rope_table=self.rope)
+            return
         q.qdec_step(self.shape, w.q(layer), w.k(layer), w.v(layer), w.w_q[layer], w.w_k[layer],
                     w.positions, w.seq_lens, w.block_table, w.pool(layer), self.ws,
                     self.out[layer], self.err, rope_table=self.rope)
 
     def unfused(self, layer: int):
         q, w = qdec(), self.w
-        q.qdec_append_rope(self.shape, w.q(layer), w.k(layer), w.v(layer), w.w_q[layer],
-                           w.w_k[layer], w.positions, w.seq_lens, w.block_table, w.pool(layer),
-                           self.q_rot, self.err, rope_table=self.rope)
-        q.qdec_attn_split(self.shape, self.q_rot, w.pool(layer), w.block_table, w.seq_lens,
-                          self.ws, self.out[layer], self.err)
+        if w.kv == "fp8":
+            q.qdec_append_rope_fp8(self.shape, w.q(layer), w.k(layer), w.v(layer), w.w_q[layer],
+                                   w.w_k[layer], w.positions, w.seq_lens, w.block_table,
+                                   w.pool8(layer), w.scale(layer), self.q_rot, self.err,
+                                   rope_table=self.rope)
+            q.qdec_attn_split_fp8(self.shape, self.q_rot, w.pool8(layer), w.scale(layer),
+                                  w.block_table, w.seq_lens, self.ws, self.out[layer], self.err)
+        else:
+            q.qdec_append_rope(self.shape, w.q(layer), w.k(layer), w.v(layer), w.w_q[layer],
+                               w.w_k[layer], w.positions, w.seq_lens, w.block_table,
+                               w.pool(layer), self.q_rot, self.err, rope_table=self.rope)
+            q.qdec_attn_split(self.shape, self.q_rot, w.pool(layer), w.block_table, w.seq_lens,
+                              self.ws, self.out[layer], self.err)
         q.qdec_attn_merge(self.shape, w.seq_lens, self.ws, self.out[layer], self.err)
 
     def check_flags(self):
@@ -81,11 +99,15 @@ class Runner:
 def run_oracle(inputs: dict) -> dict:
     """One layer on the oracle; `inputs` from workloads.oracle_inputs (pool copied)."""
     pool = inputs["pool"].copy()
-    res = oracle.decode_layer(inputs["q"], inputs["k"], inputs["v"], inputs["w_q"],
-                              inputs["w_k"], inputs["positions"], inputs["seq_lens"],
-                              inputs["block_table"], pool, inputs["rope_theta"],
-                              float(np.float32(inputs["eps"])))
+    args = (inputs["q"], inputs["k"], inputs["v"], inputs["w_q"], inputs["w_k"],
+            inputs["positions"], inputs["seq_lens"], inputs["block_table"], pool)
+    if "kv_scale" in inputs:
+        res = oracle.decode_layer_fp8(*args, inputs["kv_scale"], inputs["rope_theta"],
+                                      float(np.float32(inputs["eps"])))
+    else:
+        res = oracle.decode_layer(*args, inputs["rope_theta"], float(np.float32(inputs["eps"])))
     res["pool_after"] = pool
+    res["block_table"] = inputs["block_table"]
     return res
 
 
@@ -121,3 +143,19 @@ def assert_slots(w: wl.Workload, layer: int, seqs, res: dict):
         assert np.array_equal(row[1], v_in[b]), f"v slot seq {b}"
     assert not_exact == 0, f"{not_exact} k elements differ from the oracle's rounding"
     return not_exact
+
+
+def assert_slots_fp8(w: wl.Workload, layer: int, seqs, res: dict):
+    """The appended K and V codes of every (sequence, KV head) equal the
+    oracle's (both quantize fp32(row) / scale with E4M3 nearest-even)."""
+    P = w.spec.page_size
+    pool = w.pool8(layer)
+    for i, b in enumerate(seqs):
+        L = int(w.seq_lens_host[b])
+        page = int(w.block_table_host[b, (L - 1) // P])
+        gpu = pool[page, :, :, (L - 1) % P, :].cpu().numpy()            # [2][Hkv][D] codes
+        ref = res["pool_after"][res["block_table"][i, (L - 1) // P], :, :, (L - 1) % P, :]
+        bad = np.argwhere(gpu != ref)
+        assert bad.size == 0, (f"seq {b}: {len(bad)} slot codes differ, first "
+                               f"(plane, head, dim) {tuple(bad[0])}: gpu {gpu[tuple(bad[0])]:#x} "
+                               f"oracle {ref[tuple(bad[0])]:#x}")

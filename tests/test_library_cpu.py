@@ -21,7 +21,7 @@ def q():
 def declared_symbols():
     with open(os.path.join(ROOT, "include", "qdec.h")) as f:
         text = f.read()
-    return sorted(set(re.findall(r"\b(qdec_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(qdec_[a-z0-9_]+)\(", text)))
 
 
 def test_exports_every_declared_symbol(q):
@@ -91,6 +91,36 @@ def test_entry_points_reject_null_and_misaligned_arguments(q):
     assert step(shape=sh2) == q.QDEC_ERR_UNSUPPORTED
     sh3 = ctypes.byref(_shape(q, launch_flags=2).c())
     assert step(shape=sh3) == q.QDEC_ERR_INVALID_ARG
+
+
+def test_fp8_entry_points_reject_bad_arguments(q):
+    """FP8 pool: null or misaligned scales, an odd number of KV heads."""
+    lib = q._lib
+    sh = ctypes.byref(_shape(q).c())
+    ok = ctypes.c_void_p(1 << 20)
+    bad = ctypes.c_void_p((1 << 20) + 4)
+    z = ctypes.c_void_p(0)
+    S = 48 * 128
+
+    def step(shape=sh, pool=ok, scale=ok):
+        # shape, q, q_stride, k, k_stride, v, v_stride, w_q, w_k, positions, seq_lens,
+        # block_table, rope_table, pool, kv_scale, workspace, bytes, out, err, stream
+        return lib.qdec_step_fp8(shape, ok, S, ok, S, ok, S, ok, ok, ok, ok, ok, z, pool, scale,
+                                 ok, 16, ok, z, z)
+
+    assert step(pool=z) == q.QDEC_ERR_INVALID_ARG
+    assert step(pool=bad) == q.QDEC_ERR_INVALID_ARG
+    assert step(scale=z) == q.QDEC_ERR_INVALID_ARG
+    assert step(scale=bad) == q.QDEC_ERR_INVALID_ARG
+    assert step() == q.QDEC_ERR_WORKSPACE                   # checks passed up to the workspace
+    odd = ctypes.byref(_shape(q, num_q_heads=12, num_kv_heads=3).c())
+    assert step(shape=odd) == q.QDEC_ERR_UNSUPPORTED
+    assert lib.qdec_attn_split_fp8(odd, ok, ok, ok, ok, ok, ok, 1 << 30, ok, z,
+                                   z) == q.QDEC_ERR_UNSUPPORTED
+    assert lib.qdec_append_rope_fp8(sh, ok, S, ok, S, ok, S, ok, ok, ok, ok, ok, z, ok, z, ok, z,
+                                    z) == q.QDEC_ERR_INVALID_ARG
+    # one workspace size serves both pool types
+    assert q.qdec_workspace_bytes(_shape(q, num_q_heads=12, num_kv_heads=3)) > 0
 
 
 def test_rope_table_bytes(q):
