@@ -99,14 +99,14 @@ struct Plan {
 // global merge, so the cluster layout is used.
 constexpr int64_t kFlatMinTilesPerCta = 32;
 
-// Deepest ring (a multiple of the 4 consumer warps) that still lets two
-// CTAs share an SM.
+// Deepest ring (a multiple of the 4 consumer warps) that still lets the
+// layout's CTAs per SM share it.
 int ring_cap(const qdec_shape *s, int cluster, bool fp8) {
     int per_sm = smem_per_sm_of_current_device();
     if (per_sm <= 0) per_sm = 228 * 1024;
     const int w = qdec::kConsumerWarps;
     int cap = qdec::kMaxStages / w * w;
-    while (cap > w && static_cast<int64_t>(qdec::kCtasPerSm) *
+    while (cap > w && static_cast<int64_t>(qdec::ctas_per_sm(cluster > 0, fp8)) *
                               (qdec::attention_smem_bytes(s->batch, cap, cluster, fp8) + 1024) >
                           static_cast<int64_t>(per_sm))
         cap -= w;
@@ -200,7 +200,13 @@ Plan plan_for(const qdec_shape *s, bool allow_cluster, bool fp8) {
         if (pl.grid == 0 && widest.grid > 0 && per_cta < kFlatMinTilesPerCta / 2) pl = widest;
         if (pl.grid > 0) return pl;
     }
-    const int64_t g = s->num_ctas > 0 ? s->num_ctas : (target < wmax ? target : wmax);
+    // flat layout: a whole number of CTAs per SM for the pool type in the
+    // fused kernel; the three-call path keeps two per SM for both types, as
+    // its merge kernel (which knows no pool type) rebuilds the piece layout
+    // from the grid
+    const int64_t flat_target =
+        static_cast<int64_t>(sms) * (allow_cluster ? qdec::ctas_per_sm(false, fp8) : qdec::kCtasPerSm);
+    const int64_t g = s->num_ctas > 0 ? s->num_ctas : std::min(flat_target, wmax);
     pl.grid = static_cast<int>(g);
     pl.stages = clamp_stages((wmax + g - 1) / g, ring_cap(s, 0, fp8));
     return pl;

@@ -35,6 +35,12 @@ constexpr int kFp8SlotExtra = 2 * kScaleWindowBytes;       // per ring slot
 // receive buffer; larger clusters receive in rank 0's drained ring.
 constexpr int kMaxDirectRecv = 6;
 constexpr int kCtasPerSm = 2;
+// The FP8 flat layout (long tile ranges, half-size tiles) runs three CTAs per
+// SM: more tiles in flight per SM at 128 registers a thread.
+constexpr int kCtasPerSmFp8Flat = 3;
+constexpr int ctas_per_sm(bool cluster, bool fp8) {
+    return (!cluster && fp8) ? kCtasPerSmFp8Flat : kCtasPerSm;
+}
 constexpr int kMaxCluster = 8;                             // portable cluster size
 
 // Budget of a bounded wait (SM cycles): ~2 s at the 2.07 GHz maximum clock;

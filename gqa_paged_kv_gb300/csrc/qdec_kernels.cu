@@ -1352,7 +1352,7 @@ __device__ __forceinline__ float *cluster_peer(float *ptr, int rank) {
 
 // ------------------------------------------------------ attention kernel --
 template <bool kFused, bool kCluster, bool kFp8>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+__global__ void __launch_bounds__(kThreads, ctas_per_sm(kCluster, kFp8))
     attention_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
