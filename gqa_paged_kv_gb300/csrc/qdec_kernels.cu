@@ -542,17 +542,19 @@ __device__ __forceinline__ KvIn load_kv_inputs(const Params &p, int b, int g, in
 template <bool kFp8>
 __device__ void key_value_row(const Params &p, int b, int g, int L, uint8_t *sm, const KvIn &in) {
     const int lane = threadIdx.x & 31;
+    // FP8: the slot's scales are loaded before the key arithmetic, which
+    // hides their latency
+    const bool page_ok = in.page >= 0 && in.page < p.num_pages;
+    float sk = 1.f, sv = 1.f;
+    if (kFp8 && page_ok) {
+        const int64_t si = static_cast<int64_t>(in.page) * 2 * p.Hkv + g;
+        sk = __ldg(p.kv_scale + si);
+        sv = __ldg(p.kv_scale + si + p.Hkv);
+    }
     __nv_bfloat16 kb[4];
     key_row(p, in.ka, in.kc, in.wka, in.wkc, in.e0, in.e1, kb);
     if constexpr (kFp8) {
         const int slot = L - 1;
-        const bool page_ok = in.page >= 0 && in.page < p.num_pages;
-        float sk = 1.f, sv = 1.f;
-        if (page_ok) {
-            const int64_t si = static_cast<int64_t>(in.page) * 2 * p.Hkv + g;
-            sk = p.kv_scale[si];
-            sv = p.kv_scale[si + p.Hkv];
-        }
         const __nv_bfloat162 va = *reinterpret_cast<const __nv_bfloat162 *>(&in.va);
         const __nv_bfloat162 vc = *reinterpret_cast<const __nv_bfloat162 *>(&in.vc);
         const uint32_t k0 = quantize2_e4m3(__bfloat162float(kb[0]), __bfloat162float(kb[1]), sk);
