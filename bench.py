@@ -53,10 +53,12 @@ KERNEL_SOURCES = ("gqa_paged_kv_gb300/csrc/qdec_kernels.cu", "gqa_paged_kv_gb300
 # profiles/), keyed by workload; used only while the kernel source hash
 # still matches the one the counters were taken on.
 TRAFFIC = {
-    "b8-ctx256to384-36layer": {"kernel_sha": "c2f50e83cef72e2f", "bytes_per_launch": 10903040},
-    "b1-ctx8192-spikes-36layer": {"kernel_sha": "c2f50e83cef72e2f", "bytes_per_launch": 33632768},
-    "b64-ragged128to16384-sharedpool-36layer": {"kernel_sha": "c2f50e83cef72e2f",
-                                                "bytes_per_launch": 1036986000},
+    "b8-ctx256to384-36layer": {"kernel_sha": "2680acf25bb157ff", "bytes_per_launch": 10900480},
+    "b1-ctx8192-spikes-36layer": {"kernel_sha": "2680acf25bb157ff", "bytes_per_launch": 33634432},
+    "b64-ragged128to16384-sharedpool-36layer": {"kernel_sha": "2680acf25bb157ff",
+                                                "bytes_per_launch": 1038058240},
+    "b64-ragged128to16384-sharedpool-36layer-fp8kv": {"kernel_sha": "2680acf25bb157ff",
+                                                      "bytes_per_launch": 524734848},
 }
 
 # The CPU timings sample the first few layers of a workload (same shapes and
