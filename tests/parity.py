@@ -159,3 +159,23 @@ def assert_slots_fp8(w: wl.Workload, layer: int, seqs, res: dict):
         assert bad.size == 0, (f"seq {b}: {len(bad)} slot codes differ, first "
                                f"(plane, head, dim) {tuple(bad[0])}: gpu {gpu[tuple(bad[0])]:#x} "
                                f"oracle {ref[tuple(bad[0])]:#x}")
+
+
+def assert_slots_for(w: wl.Workload, layer: int, seqs, res: dict):
+    """The appended slots, checked the way the workload's pool type defines them."""
+    if w.kv == "fp8":
+        return assert_slots_fp8(w, layer, seqs, res)
+    return assert_slots(w, layer, seqs, res)
+
+
+def step_call(shape, w: wl.Workload, layer: int, ws, out, err, rope=None):
+    """One qdec_step / qdec_step_fp8 launch of `layer` with the given shape and buffers."""
+    q = qdec()
+    if w.kv == "fp8":
+        q.qdec_step_fp8(shape, w.q(layer), w.k(layer), w.v(layer), w.w_q[layer], w.w_k[layer],
+                        w.positions, w.seq_lens, w.block_table, w.pool8(layer), w.scale(layer),
+                        ws, out, err, rope_table=rope)
+    else:
+        q.qdec_step(shape, w.q(layer), w.k(layer), w.v(layer), w.w_q[layer], w.w_k[layer],
+                    w.positions, w.seq_lens, w.block_table, w.pool(layer), ws, out, err,
+                    rope_table=rope)
