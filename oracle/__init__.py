@@ -103,6 +103,9 @@ class Oracle:
         lib.oracle_decode_layer_fp8.argtypes = ([ci] * 7 + [u16p] * 5 + [i32p] * 3
                                                 + [u8p, f32p] + [_D] * 3 + [dp] * 4)
         lib.oracle_decode_layer_fp8.restype = ci
+        lib.oracle_qkv_append.argtypes = ([ci] * 8 + [u16p] * 4 + [i32p] * 3 + [u16p]
+                                          + [_D] * 2 + [dp] * 3)
+        lib.oracle_qkv_append.restype = ci
         self.lib = lib
         self.path = path
 
@@ -254,6 +257,31 @@ class Oracle:
         return res
 
 
+    # ------------------------------------------------------ QKV projection
+    def qkv_append(self, x, w_qkv, w_q, w_k, positions, seq_lens, block_table, pool,
+                   rope_theta: float, eps: float, num_q_heads: int, num_kv_heads: int):
+        """The merged QKV projection fused with norm, rotation and append.
+        x [B][hidden], w_qkv [(Hq+2Hkv)*D][hidden] (bf16 as uint16); ``pool``
+        (uint16 [pages][2][Hkv][P][D]) is updated in place.  Returns double
+        arrays q_rot [B][Hq][D], k_rot and v [B][Hkv][D] (unrounded)."""
+        x, w, w_q, w_k = _u16(x), _u16(w_qkv), _u16(w_q), _u16(w_k)
+        pos, sl, bt = _i32(positions), _i32(seq_lens), _i32(block_table)
+        assert pool.dtype == np.uint16 and pool.flags["C_CONTIGUOUS"]
+        B, hidden = x.shape
+        num_pages, _, Hkv, P, D = pool.shape
+        Hq = num_q_heads
+        assert Hkv == num_kv_heads and w.shape == ((Hq + 2 * Hkv) * D, hidden)
+        res = {"q_rot": np.empty((B, Hq, D)), "k_rot": np.empty((B, Hkv, D)),
+               "v": np.empty((B, Hkv, D))}
+        _check(self.lib.oracle_qkv_append(
+            B, Hq, Hkv, D, P, num_pages, bt.shape[1], hidden,
+            _ptr(x, _U16), _ptr(w, _U16), _ptr(w_q, _U16), _ptr(w_k, _U16),
+            _ptr(pos, _I32), _ptr(sl, _I32), _ptr(bt, _I32), _ptr(pool, _U16),
+            float(rope_theta), float(eps),
+            _ptr(res["q_rot"], _D), _ptr(res["k_rot"], _D), _ptr(res["v"], _D)))
+        return res
+
+
 _default = None
 
 
@@ -301,3 +329,7 @@ def attention_fp8(pool8, kv_scale, block_table, seq_lens, q_rot, scale):
 
 def decode_layer_fp8(*args, **kwargs):
     return default().decode_layer_fp8(*args, **kwargs)
+
+
+def qkv_append(*args, **kwargs):
+    return default().qkv_append(*args, **kwargs)

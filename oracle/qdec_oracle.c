@@ -26,6 +26,11 @@
  *   split/merge -- blog part 8: one head's KV sequence is cut into parts,
  *               each part gets a local softmax, the parts are then reduced.
  *               The reduction is the exact log-sum-exp merge.
+ *   QKV projection -- engine article, section 4.4.3 (fused QKV): one merged
+ *               matrix W [(Hq + 2 Hkv) D][hidden] (rows: the q heads, then the
+ *               k heads, then the v heads) gives qkv = W x for each sequence;
+ *               fused with steps 1-3 the projection stays unrounded (double
+ *               here) into the norm, the rotation and the append.
  *   FP8 KV    -- essay, section on quantization: the KV cache held in FP8
  *               (half the bytes).  Codes are OCP E4M3; every (page, plane,
  *               KV head) carries one fp32 scale, value = e4m3(code) * scale.
@@ -544,6 +549,84 @@ int oracle_decode_layer_fp8(int B, int Hq, int Hkv, int D, int P, int num_pages,
         rc = oracle_attention_fp8(B, Hq, Hkv, D, P, num_pages, max_blocks, pool8, kv_scale,
                                   block_table, seq_lens, q_rot, scale, out, lse);
     free(x);
+    free(xn);
+    free(wq);
+    free(wk);
+    return rc;
+}
+
+/* ------------------------------------------------------ QKV projection -- */
+
+/* The merged QKV projection fused with steps 1-3, for every sequence b:
+ *   qkv[j] = sum_i W[j][i] * x[b][i]          (double, no rounding)
+ * rows j of query head h: h*D .. h*D+D-1; key head g: (Hq+g)*D ..; value
+ * head g: (Hq+Hkv+g)*D ..; then RMSNorm + NeoX RoPE of the q and k rows at
+ * positions[b], and the append of bf16(k_rot) and bf16(v) (each rounded once,
+ * nearest-even) into slot seq_lens[b]-1.
+ *   x [B][hidden], W [(Hq+2Hkv)*D][hidden], w_q, w_k [D] (bf16 as uint16).
+ * Outputs (double): q_rot [B][Hq][D], k_rot and v [B][Hkv][D] (unrounded).
+ * Returns 0, -1 (block-table entry outside the pool), -2 (bad seq_len),
+ * -4 (Hq not a multiple of Hkv, or odd D). */
+int oracle_qkv_append(int B, int Hq, int Hkv, int D, int P, int num_pages, int max_blocks,
+                      int hidden, const uint16_t *x, const uint16_t *w_qkv,
+                      const uint16_t *w_q, const uint16_t *w_k, const int32_t *positions,
+                      const int32_t *seq_lens, const int32_t *block_table, uint16_t *pool,
+                      double rope_theta, double eps, double *q_rot, double *k_rot,
+                      double *v_out)
+{
+    if (Hkv < 1 || Hq % Hkv != 0 || D % 2 != 0)
+        return -4;
+    oracle_dims d = {B, Hq, Hkv, D, P, num_pages, max_blocks};
+    int rows = (Hq + 2 * Hkv) * D;
+    double *qkv = (double *)malloc(sizeof(double) * (size_t)rows);
+    double *xd = (double *)malloc(sizeof(double) * (size_t)hidden);
+    double *xn = (double *)malloc(sizeof(double) * (size_t)D);
+    double *wq = (double *)malloc(sizeof(double) * (size_t)D);
+    double *wk = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int i = 0; i < D; ++i) {
+        wq[i] = oracle_bf16_to_double(w_q[i]);
+        wk[i] = oracle_bf16_to_double(w_k[i]);
+    }
+    int rc = 0;
+    for (int b = 0; b < B && rc == 0; ++b) {
+        int L = seq_lens[b];
+        if (L < 1 || L > max_blocks * P) {
+            rc = -2;
+            break;
+        }
+        double pos = (double)positions[b];
+        for (int i = 0; i < hidden; ++i)
+            xd[i] = oracle_bf16_to_double(x[(long)b * hidden + i]);
+        for (int j = 0; j < rows; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < hidden; ++i)
+                acc += oracle_bf16_to_double(w_qkv[(long)j * hidden + i]) * xd[i];
+            qkv[j] = acc;
+        }
+        for (int h = 0; h < Hq; ++h) {
+            oracle_rmsnorm(qkv + (long)h * D, wq, D, eps, xn);
+            oracle_rope_neox(xn, D, pos, rope_theta, q_rot + ((long)b * Hq + h) * D);
+        }
+        for (int g = 0; g < Hkv; ++g) {
+            long o = ((long)b * Hkv + g) * D;
+            oracle_rmsnorm(qkv + (long)(Hq + g) * D, wk, D, eps, xn);
+            oracle_rope_neox(xn, D, pos, rope_theta, k_rot + o);
+            for (int i = 0; i < D; ++i)
+                v_out[o + i] = qkv[(long)(Hq + Hkv + g) * D + i];
+            long rk = pool_row(&d, block_table, b, L - 1, 0, g);
+            long rv = pool_row(&d, block_table, b, L - 1, 1, g);
+            if (rk < 0 || rv < 0) {
+                rc = -1;
+                break;
+            }
+            for (int i = 0; i < D; ++i) {
+                pool[rk + i] = oracle_double_to_bf16(k_rot[o + i]);
+                pool[rv + i] = oracle_double_to_bf16(v_out[o + i]);
+            }
+        }
+    }
+    free(qkv);
+    free(xd);
     free(xn);
     free(wq);
     free(wk);

@@ -582,4 +582,73 @@ def pin_fp8_nan_codes_outside_context(orc):
     assert np.array_equal(out0, out1), "NaN codes"
 
 
+# --------------------------------------------------------- QKV projection --
+
+def _qkv_problem(rng, seq_lens, Hq=8, Hkv=2, D=16, hidden=24):
+    pb, q, k, v, wq, wk, pos = _layer_problem(rng, seq_lens, Hq=Hq, Hkv=Hkv, D=D)
+    B = len(seq_lens)
+    x = random_bits(rng, (B, hidden))
+    w = random_bits(rng, ((Hq + 2 * Hkv) * D, hidden), scale=0.2)
+    return pb, x, w, wq, wk, pos
+
+
+def pin_qkv_projection_is_the_matrix_product(orc):
+    """q_rot and k_rot are norm + rotation (both pinned) of the rows of
+    numpy's W @ x; v is the value rows of the same product."""
+    rng = np.random.default_rng(24)
+    Hq, Hkv, D = 8, 2, 16
+    pb, x, w, wq, wk, pos = _qkv_problem(rng, [3, 17, 31])
+    res = orc.qkv_append(x, w, wq, wk, pos, pb.seq_lens, pb.bt, pb.pool, 1e6, 1e-6, Hq, Hkv)
+    for b in range(3):
+        qkv = f64(w) @ f64(x[b])
+        for h in range(Hq):
+            want = orc.rope_neox(orc.rmsnorm(qkv[h * D:(h + 1) * D], f64(wq), 1e-6), pos[b], 1e6)
+            _close(res["q_rot"][b, h], want, 1e-12, "qkv q_rot")
+        for g in range(Hkv):
+            row = qkv[(Hq + g) * D:(Hq + g + 1) * D]
+            want = orc.rope_neox(orc.rmsnorm(row, f64(wk), 1e-6), pos[b], 1e6)
+            _close(res["k_rot"][b, g], want, 1e-12, "qkv k_rot")
+            _close(res["v"][b, g], qkv[(Hq + Hkv + g) * D:(Hq + Hkv + g + 1) * D], 1e-12, "qkv v")
+
+
+def pin_qkv_one_hot_input_equals_the_layer_step(orc):
+    """With x one-hot the projection picks one bf16 column of W exactly, so
+    the fused projection must equal the (pinned) layer-step's steps 1-3 on
+    those columns as q, k and v: the same q_rot, k_rot and pool bits."""
+    rng = np.random.default_rng(25)
+    Hq, Hkv, D, hidden = 8, 2, 16, 24
+    pb, x, w, wq, wk, pos = _qkv_problem(rng, [1, 5, 16, 22], hidden=hidden)
+    cols = rng.integers(0, hidden, size=4)
+    x = np.zeros_like(x)
+    x[np.arange(4), cols] = 0x3F80                      # 1.0 in bf16
+    pool_a, pool_b = pb.pool.copy(), pb.pool.copy()
+    res = orc.qkv_append(x, w, wq, wk, pos, pb.seq_lens, pb.bt, pool_a, 1e6, 1e-6, Hq, Hkv)
+    picked = np.stack([w[:, c] for c in cols])           # [B][(Hq+2Hkv)*D] bf16 bits
+    q = np.ascontiguousarray(picked[:, :Hq * D].reshape(4, Hq, D))
+    k = np.ascontiguousarray(picked[:, Hq * D:(Hq + Hkv) * D].reshape(4, Hkv, D))
+    v = np.ascontiguousarray(picked[:, (Hq + Hkv) * D:].reshape(4, Hkv, D))
+    ref = orc.decode_layer(q, k, v, wq, wk, pos, pb.seq_lens, pb.bt, pool_b, 1e6, 1e-6)
+    assert np.array_equal(res["q_rot"], ref["q_rot"]), "one-hot q_rot"
+    assert np.array_equal(res["k_rot"], ref["k_rot"]), "one-hot k_rot"
+    assert np.array_equal(pool_a, pool_b), "one-hot pool"
+
+
+def pin_qkv_append_one_slot(orc):
+    """Exactly slot L-1 of every (sequence, KV head, plane) changes: K gets
+    bf16(k_rot), V gets bf16(v), both rounded once to nearest even."""
+    rng = np.random.default_rng(26)
+    Hq, Hkv = 8, 2
+    pb, x, w, wq, wk, pos = _qkv_problem(rng, [1, 4, 5, 16, 22])
+    before = pb.pool.copy()
+    res = orc.qkv_append(x, w, wq, wk, pos, pb.seq_lens, pb.bt, pb.pool, 1e6, 1e-6, Hq, Hkv)
+    changed = np.zeros(before.shape, bool)
+    for b, L in enumerate(pb.seq_lens):
+        page, off = pb.bt[b, (L - 1) // 4], (L - 1) % 4
+        for g in range(Hkv):
+            assert np.array_equal(pb.pool[page, 0, g, off], orc.f64_to_bf16_bits(res["k_rot"][b, g]))
+            assert np.array_equal(pb.pool[page, 1, g, off], orc.f64_to_bf16_bits(res["v"][b, g]))
+        changed[page, :, :, off] = True
+    assert np.array_equal(pb.pool[~changed], before[~changed]), "append touched another slot"
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

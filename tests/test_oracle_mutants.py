@@ -63,6 +63,16 @@ MUTANTS = [
      "oracle_float_to_e4m3_satfinite(kf * kv_scale[sk])"),
     ("fp8 append V with the K scale", "oracle_float_to_e4m3_satfinite(vf / kv_scale[sv])",
      "oracle_float_to_e4m3_satfinite(vf / kv_scale[sk])"),
+    ("qkv weight transposed", "oracle_bf16_to_double(w_qkv[(long)j * hidden + i])",
+     "oracle_bf16_to_double(w_qkv[(long)i * rows + j])"),
+    ("qkv keys from the value rows", "oracle_rmsnorm(qkv + (long)(Hq + g) * D, wk, D, eps, xn);",
+     "oracle_rmsnorm(qkv + (long)(Hq + Hkv + g) * D, wk, D, eps, xn);"),
+    ("qkv values from the key rows", "v_out[o + i] = qkv[(long)(Hq + Hkv + g) * D + i];",
+     "v_out[o + i] = qkv[(long)(Hq + g) * D + i];"),
+    ("qkv queries normed with the key weight", "oracle_rmsnorm(qkv + (long)h * D, wq, D, eps, xn);",
+     "oracle_rmsnorm(qkv + (long)h * D, wk, D, eps, xn);"),
+    ("qkv value slot perturbed", "pool[rv + i] = oracle_double_to_bf16(v_out[o + i]);",
+     "pool[rv + i] = oracle_double_to_bf16(v_out[o + i] * 1.001);"),
 ]
 
 
