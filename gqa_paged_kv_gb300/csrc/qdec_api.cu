@@ -356,6 +356,23 @@ qdec_status encode_pool_map_fp8(CUtensorMap *map, const qdec_shape *s, const voi
     return r == CUDA_SUCCESS ? QDEC_OK : QDEC_ERR_CUDA;
 }
 
+// A row-major bf16 matrix [rows][cols] (row stride `stride` elements) as a
+// 2-D tensor with box_rows x 64 boxes, 128-byte swizzled.
+qdec_status encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols,
+                            int64_t stride, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return QDEC_ERR_CUDA;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? QDEC_OK : QDEC_ERR_CUDA;
+}
+
 qdec_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QDEC_OK : QDEC_ERR_CUDA; }
 
 qdec_status check_new_token_args(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_stride,
@@ -621,6 +638,43 @@ qdec_status qdec_step_fp8(const qdec_shape *shape, const qdec_bf16 *q, int64_t q
     return step_impl(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w, k_norm_w, positions,
                      seq_lens, block_table, rope_table, PoolArg{kv_pool_fp8, kv_scale, true},
                      workspace, workspace_bytes, out, err_flag, stream);
+}
+
+qdec_status qdec_qkv_append_rope(const qdec_shape *shape, int32_t hidden, const qdec_bf16 *x,
+                                 int64_t x_stride, const qdec_bf16 *w_qkv,
+                                 const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                                 const int32_t *positions, const int32_t *seq_lens,
+                                 const int32_t *block_table, const void *rope_table,
+                                 qdec_bf16 *kv_pool, float *q_rot, int32_t *err_flag,
+                                 void *stream) {
+    qdec_status st = check_shape(shape);
+    if (st != QDEC_OK) return st;
+    if (hidden < 64 || hidden % 64 != 0) return QDEC_ERR_UNSUPPORTED;
+    if (!x || !w_qkv || !q_norm_w || !k_norm_w || !positions || !seq_lens || !block_table ||
+        !rope_table || !kv_pool || !q_rot)
+        return QDEC_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(q_norm_w) || !aligned16(k_norm_w) ||
+        !aligned16(rope_table) || !aligned16(kv_pool) || !aligned16(q_rot))
+        return QDEC_ERR_INVALID_ARG;
+    if (x_stride < hidden || x_stride % 8 != 0) return QDEC_ERR_INVALID_ARG;
+    Params p{};
+    fill_common(p, shape, false);
+    p.hidden = hidden;
+    p.w_q = reinterpret_cast<const __nv_bfloat16 *>(q_norm_w);
+    p.w_k = reinterpret_cast<const __nv_bfloat16 *>(k_norm_w);
+    p.positions = positions;
+    p.seq_lens = seq_lens;
+    p.block_table = block_table;
+    p.rope = static_cast<const qdec::RopeEntry *>(rope_table);
+    p.pool = reinterpret_cast<__nv_bfloat16 *>(kv_pool);
+    p.q_rot_out = q_rot;
+    p.err = err_flag;
+    const int64_t rows = static_cast<int64_t>(shape->num_q_heads + 2 * shape->num_kv_heads) *
+                         qdec::kHeadDim;
+    CUtensorMap w_map, x_map;
+    if ((st = encode_rows_map(&w_map, w_qkv, rows, hidden, hidden, 16)) != QDEC_OK) return st;
+    if ((st = encode_rows_map(&x_map, x, shape->batch, hidden, x_stride, 64)) != QDEC_OK) return st;
+    return cuda_status(qdec::launch_qkv_append(p, w_map, x_map, static_cast<cudaStream_t>(stream)));
 }
 
 qdec_status qdec_check_error(int32_t *err_flag, void *stream, int32_t *flags_out) {

@@ -83,6 +83,7 @@ struct Params {
     long long ws_pieces;     // partial slots the workspace holds (device bounds checks)
     long long wait_cycles;   // budget of every bounded wait, in SM cycles
     int withhold_first;      // test hook: CTA-local tile 0 is never copied (see qdec.h)
+    int hidden;              // QKV projection: hidden size (a multiple of 64)
     double inv_freq[kRotPairs];  // rope_theta^(-2i/D), i < D/2
 };
 
@@ -104,5 +105,11 @@ cudaError_t launch_append_rope(const Params &p, bool fp8, cudaStream_t s);
 cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, bool fused, bool fp8,
                              cudaStream_t s);
 cudaError_t launch_merge(const Params &p, cudaStream_t s);
+
+// The merged QKV projection fused with steps 1-3 (qdec_qkv.cu): w_map views
+// W [(Hq+2Hkv)*D][hidden] with 64 x 16 boxes, x_map views x [B][hidden] with
+// 64 x 64 boxes, both bf16, 128-byte swizzled.
+cudaError_t launch_qkv_append(const Params &p, const CUtensorMap &w_map, const CUtensorMap &x_map,
+                              cudaStream_t s);
 
 }  // namespace qdec

@@ -45,6 +45,7 @@
 // finishing; the consumers wait for the previous kernel before they touch q,
 // k, v, the pool slot they append to, the workspace or `out`.
 #include "qdec_internal.h"
+#include "qdec_ptx.cuh"
 #include "qdec.h"
 
 #include <cuda_fp16.h>
@@ -120,51 +121,6 @@ __host__ __device__ constexpr int ring_offset(int B, int C) {
 }
 
 // ------------------------------------------------------------ PTX helpers --
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Wait for a barrier phase; give up after kWaitTimeoutCycles SM cycles (about
-// two seconds) or when another thread of the CTA has already given up.  Never
-// spins without bound.  The budget is counted with clock64(), which is
-// monotonic on the SM the thread runs on (the global nanosecond timer is
-// not: it can step backwards, which would end a wait at once).
-__device__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                  long long budget = kWaitTimeoutCycles) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (clock64() - t0 > budget) return false;
-    }
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 // One whole page tile: the K and V planes of one (page, KV head), 8 KiB,
 // landing as [plane][half of D][token][64 dims] in 128-byte swizzled rows.
 // The pool's tensor map is 5-D (dims, token, half, plane, page*2*Hkv + head);
@@ -205,25 +161,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                  : "r"(addr));
     return v;
 }
-__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-// D += A (16x16 bf16, row) * B (16x8 bf16, col), fp32 accumulate.
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
-        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 // D += A (16x32 E4M3, row) * B (32x8 E4M3, col), fp32 accumulate.
 __device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
@@ -256,12 +193,6 @@ __device__ __forceinline__ uint32_t quantize2_e4m3(float a, float b, float s) {
 }
 __device__ __forceinline__ void consumer_sync() {  // the 128 consumer threads only
     asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-__device__ __forceinline__ void grid_dependency_wait() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Release/acquire fence at GPU scope (lighter than the sequentially
@@ -1328,29 +1259,6 @@ __device__ void store_partial(const Params &p, volatile int *misc, int64_t pid, 
     }
 }
 
-// Split cluster barrier: every thread of every CTA of the cluster arrives,
-// then waits for all arrivals.
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-    asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_arrive_release() {
-    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-// Generic address of the same shared-memory location in CTA `rank` of this
-// cluster (distributed shared memory).
-__device__ __forceinline__ float *cluster_peer(float *ptr, int rank) {
-    uint64_t r;
-    asm volatile("mapa.u64 %0, %1, %2;"
-                 : "=l"(r)
-                 : "l"(reinterpret_cast<uint64_t>(ptr)), "r"(rank));
-    return reinterpret_cast<float *>(r);
-}
 
 // ------------------------------------------------------ attention kernel --
 template <bool kFused, bool kCluster, bool kFp8>

@@ -198,6 +198,30 @@ qdec_status qdec_step(const qdec_shape *shape,
                       qdec_bf16 *kv_pool, void *workspace, size_t workspace_bytes,
                       qdec_bf16 *out, int32_t *err_flag, void *stream);
 
+/* The merged QKV projection fused with steps 1-3 (article "扔掉 vLLM！从零
+ * 构建 Qwen3-8B 推理引擎" (news.rkmt.cn), section 4.4.3: the q, k and v
+ * projections as one matrix), in place of qdec_append_rope when the layer's
+ * input is the hidden state:
+ *   qkv = W x[b]  for every sequence b, with
+ *   x [B][hidden] bf16 (row stride x_stride elements, a multiple of 8),
+ *   w_qkv [(Hq + 2 Hkv) * 128][hidden] bf16, row-major: rows h*128 .. +127
+ *     are query head h, then the key heads, then the value heads (no bias);
+ *   hidden a multiple of 64.
+ * The projection is kept unrounded (fp32 accumulate) into RMSNorm + NeoX RoPE
+ * of the q and k heads and the append: q_rot [B][Hq][128] fp32 (as
+ * qdec_append_rope writes it, for qdec_attn_split / qdec_attn_merge), bf16 of
+ * the rotated k and of v into slot seq_lens[b]-1 of kv_pool (bf16 pool).
+ * rope_table (from qdec_rope_table) is required.  Errors as qdec_append_rope;
+ * hidden not a multiple of 64 gives QDEC_ERR_UNSUPPORTED. */
+qdec_status qdec_qkv_append_rope(const qdec_shape *shape, int32_t hidden,
+                                 const qdec_bf16 *x, int64_t x_stride,
+                                 const qdec_bf16 *w_qkv,
+                                 const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                                 const int32_t *positions, const int32_t *seq_lens,
+                                 const int32_t *block_table, const void *rope_table,
+                                 qdec_bf16 *kv_pool, float *q_rot, int32_t *err_flag,
+                                 void *stream);
+
 /* ------------------------------------------------------------ FP8 KV pool --
  * The same block over a KV cache held in FP8 (essay "推理引擎里面发生了什么"
  * (locsic.com), section on quantization: an FP8 KV cache halves its memory

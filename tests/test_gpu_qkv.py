@@ -1,0 +1,155 @@
+"""The merged QKV projection fused with norm, rotation and append, through the
+C ABI (marked gpu), against the oracle.  The GPU sums the projection in fp32,
+so each element carries the fp32 dot-product error bound
+    E_j = 2 * hidden * 2^-24 * sum_i |x_i w_ji|
+(twice the first-order bound of a sum of `hidden` products), which the norm
+and the rotation carry into q_rot and k_rot as r * max|w| * (E_i + E_(i+64)).
+Checked: q_rot within the fp32 q_rot tolerance plus that bound; the appended
+k and v within one bf16 ulp of the oracle's unrounded values plus that bound;
+the rest of the pool untouched; the whole block (projection, split attention,
+merge) within the out tolerance.  Batches of 1 to 70 rows (two 64-row blocks), hidden sizes 64 to
+2560, NaN-poisoned pools.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_paged_kv_gb300 import workloads as wl
+import parity
+
+pytestmark = pytest.mark.gpu
+
+
+def _problem(lens, hidden, seed, hkv=8):
+    pages = sum((l + 15) // 16 for l in lens) + 9
+    spec = wl.custom(len(lens), lens, pool_pages=pages, seed=seed, num_q_heads=4 * hkv,
+                     num_kv_heads=hkv)
+    w = wl.build(spec, "cuda", poison=True)
+    gen = torch.Generator(device="cuda").manual_seed(seed + 7)
+    rows = (spec.num_q_heads + 2 * hkv) * spec.head_dim
+    x = torch.randn((len(lens), hidden), generator=gen, device="cuda").to(torch.bfloat16)
+    wqkv = (torch.randn((rows, hidden), generator=gen, device="cuda") /
+            math.sqrt(hidden)).to(torch.bfloat16)
+    return w, x, wqkv
+
+
+def _run(w, x, wqkv):
+    q = parity.qdec()
+    s = w.spec
+    shape = q.shape_for(w)
+    rope = q.alloc_rope_table(shape)
+    q.qdec_rope_table(shape, w.positions, rope)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q_rot = torch.empty((s.batch, s.num_q_heads, s.head_dim), dtype=torch.float32, device="cuda")
+    q.qdec_qkv_append_rope(shape, x, wqkv, w.w_q[0], w.w_k[0], w.positions, w.seq_lens,
+                           w.block_table, w.pool(0), q_rot, rope, err)
+    ws = q.alloc_workspace(shape)
+    out = torch.empty((s.batch, s.num_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
+    q.qdec_attn_split(shape, q_rot, w.pool(0), w.block_table, w.seq_lens, ws, out, err)
+    q.qdec_attn_merge(shape, w.seq_lens, ws, out, err)
+    return q_rot, out, err
+
+
+def _projection_bounds(w, x, wqkv, res):
+    """Per-element error bounds of the fp32 projection: E for v, and E
+    carried through norm + rotation for q_rot and k_rot."""
+    s = w.spec
+    D, Hq, Hkv = s.head_dim, s.num_q_heads, s.num_kv_heads
+    xf = np.abs(oracle.bf16_bits_to_f64(wl.bf16_bits(x)))
+    wf = np.abs(oracle.bf16_bits_to_f64(wl.bf16_bits(wqkv)))
+    E = 2 * x.shape[1] * 2.0 ** -24 * (xf @ wf.T)          # [B][(Hq+2Hkv)*D]
+    E = E.reshape(s.batch, Hq + 2 * Hkv, D)
+    def rotated(Eh, rows, wmax):
+        # r = 1/rms of the projected row, from the oracle's own values
+        pair = Eh + np.concatenate([Eh[..., D // 2:], Eh[..., :D // 2]], axis=-1)
+        return rows * wmax * pair
+    inp = wl.oracle_inputs(w, 0)
+    wq = np.abs(oracle.bf16_bits_to_f64(inp["w_q"])).max()
+    wk = np.abs(oracle.bf16_bits_to_f64(inp["w_k"])).max()
+    xq = oracle.bf16_bits_to_f64(wl.bf16_bits(x)) @ oracle.bf16_bits_to_f64(wl.bf16_bits(wqkv)).T
+    xq = xq.reshape(s.batch, Hq + 2 * Hkv, D)
+    r = 1 / np.sqrt((xq * xq).mean(axis=-1, keepdims=True) + float(np.float32(inp["eps"])))
+    return {"q_rot": rotated(E[:, :Hq], r[:, :Hq], wq),
+            "k_rot": rotated(E[:, Hq:Hq + Hkv], r[:, Hq:Hq + Hkv], wk),
+            "v": E[:, Hq + Hkv:]}
+
+
+def _oracle(w, x, wqkv):
+    inp = wl.oracle_inputs(w, 0)
+    pool = inp["pool"].copy()
+    s = w.spec
+    res = oracle.qkv_append(wl.bf16_bits(x), wl.bf16_bits(wqkv), inp["w_q"], inp["w_k"],
+                            inp["positions"], inp["seq_lens"], inp["block_table"], pool,
+                            inp["rope_theta"], float(np.float32(inp["eps"])), s.num_q_heads,
+                            s.num_kv_heads)
+    out, _ = oracle.attention(pool, inp["block_table"], inp["seq_lens"], res["q_rot"],
+                              1 / math.sqrt(s.head_dim))
+    res["out"] = out
+    res["bound"] = _projection_bounds(w, x, wqkv, res)
+    return res
+
+
+def _check_slots(w, res):
+    P = w.spec.page_size
+    for b in range(w.spec.batch):
+        L = int(w.seq_lens_host[b])
+        page = int(w.block_table_host[b, (L - 1) // P])
+        row = wl.bf16_bits(w.pool(0)[page, :, :, (L - 1) % P, :])
+        for plane, key in ((0, "k_rot"), (1, "v")):
+            ref = res[key][b]
+            got = oracle.bf16_bits_to_f64(row[plane])
+            excess = np.abs(got - ref) - parity.bf16_ulp(ref) - res["bound"][key][b]
+            i = np.unravel_index(np.argmax(excess), excess.shape)
+            assert excess[i] <= 0, (f"seq {b} plane {plane} at {i}: got {got[i]!r} ref {ref[i]!r} "
+                                    f"ulp {parity.bf16_ulp(ref)[i]!r}; "
+                                    f"{int((excess > 0).sum())} elements beyond 1 ulp")
+
+
+@pytest.mark.parametrize("lens,hidden", [
+    ([1], 64), ([17, 1, 300], 256), ([40] * 8, 2560), ([300, 17, 1000, 64], 2560),
+    ([int(x) for x in np.random.default_rng(5).integers(1, 200, size=70)], 512),
+], ids=["b1-h64", "b3-h256", "b8-h2560", "b4-h2560", "b70-h512"])
+def test_qkv_projection_matches_oracle(lens, hidden):
+    w, x, wqkv = _problem(lens, hidden, seed=61)
+    res = _oracle(w, x, wqkv)
+    before = wl.bf16_bits(w.pool(0)).copy()
+    q_rot, out, err = _run(w, x, wqkv)
+    st, flags = parity.qdec().qdec_check_error(err)
+    assert st == 0 and flags == 0, (st, flags)
+    g = q_rot.double().cpu().numpy()
+    tol = parity.QROT_TOL * (1 + np.abs(res["q_rot"])) + res["bound"]["q_rot"]
+    assert np.all(np.abs(g - res["q_rot"]) <= tol), np.abs(g - res["q_rot"]).max()
+    _check_slots(w, res)
+    parity.assert_out_close(out, res["out"])
+    # only the append slots changed
+    after = wl.bf16_bits(w.pool(0))
+    P = w.spec.page_size
+    mask = np.zeros(after.shape, bool)
+    for b in range(w.spec.batch):
+        L = int(w.seq_lens_host[b])
+        mask[int(w.block_table_host[b, (L - 1) // P]), :, :, (L - 1) % P] = True
+    same = (after == before) | (np.isnan(oracle.bf16_bits_to_f64(after)) &
+                                np.isnan(oracle.bf16_bits_to_f64(before)))
+    assert same[~mask].all(), "the projection wrote outside the append slots"
+
+
+def test_qkv_group_of_two_kv_heads():
+    w, x, wqkv = _problem([33, 5, 16], 128, seed=62, hkv=2)
+    res = _oracle(w, x, wqkv)
+    q_rot, out, err = _run(w, x, wqkv)
+    st, flags = parity.qdec().qdec_check_error(err)
+    assert st == 0 and flags == 0
+    _check_slots(w, res)
+    parity.assert_out_close(out, res["out"])
+
+
+def test_qkv_bad_page_is_flagged():
+    q = parity.qdec()
+    w, x, wqkv = _problem([40, 17], 256, seed=63)
+    w.block_table[1, 1] = w.spec.pool_pages + 3   # the append page of sequence 1
+    _, _, err = _run(w, x, wqkv)
+    st, flags = q.qdec_check_error(err)
+    assert st == q.QDEC_ERR_DEVICE_BOUNDS and flags & q.QDEC_FLAG_BAD_PAGE, (st, flags)
