@@ -20,6 +20,11 @@ cpu_baseline / --impl reference = the fp64 CPU oracle on a bounded sample.
 --kv fp8 runs the same workload over an FP8 (E4M3) pool with per-(page,
 plane, head) scales (qdec_step_fp8); its bytes count one byte per KV element
 plus the scales read.
+--qkv runs the block from hidden states instead: per layer the merged QKV
+projection fused with norm, rotation and append (qdec_qkv_append_rope, a
+random [(Hq+2Hkv)*128][hidden] weight per layer), then qdec_attn_split and
+qdec_attn_merge; its bytes add the weight and the hidden states and drop
+q/k/v, and the roofline object describes the projection kernel.
 
 Multi-GPU: the path shards without any exchange, so N ranks run N
 independent replicas (weak scaling); value sums their work over the slowest
@@ -84,6 +89,9 @@ def parse_args():
     ap.add_argument("--workload", type=int, default=2, choices=sorted(wl.WORKLOADS))
     ap.add_argument("--kv", choices=("bf16", "fp8"), default="bf16",
                     help="KV pool element type (fp8: E4M3 codes + per-page scales)")
+    ap.add_argument("--qkv", action="store_true",
+                    help="start each layer from hidden states: fused QKV projection + attention")
+    ap.add_argument("--hidden", type=int, default=2560, help="hidden size for --qkv")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the 36 calls eagerly")
@@ -216,15 +224,31 @@ def l2_bytes(dev=None) -> int:
     return L2_BYTES_NOMINAL
 
 
-def workload_name(spec, kv: str) -> str:
-    return spec.name + ("-fp8kv" if kv == "fp8" else "")
+def workload_name(spec, kv: str, qkv_hidden: int = 0) -> str:
+    return (spec.name + ("-fp8kv" if kv == "fp8" else "")
+            + (f"-qkv{qkv_hidden}" if qkv_hidden else ""))
+
+
+def qkv_weight_bytes(spec, hidden: int) -> int:
+    return (spec.num_q_heads + 2 * spec.num_kv_heads) * spec.head_dim * hidden * 2
+
+
+def block_bytes_per_layer(w: wl.Workload, hidden: int) -> int:
+    """--qkv: the weight, the hidden states, the KV read at token granularity
+    and the output."""
+    s = w.spec
+    kv = w.algorithmic_bytes_per_layer() - s.batch * s.io_bytes_per_seq()
+    return (qkv_weight_bytes(s, hidden) + s.batch * hidden * 2 + kv
+            + s.batch * s.num_q_heads * s.head_dim * 2)
 
 
 def workload_config(w: wl.Workload, args, world: int, l2: int = L2_BYTES_NOMINAL) -> dict:
     """The `config` object of the JSON line (the same for both arms)."""
     spec, seq_lens_host = w.spec, w.seq_lens_host
     L = spec.layers
-    bytes_layer = w.algorithmic_bytes_per_layer()
+    qkv_hidden = args.hidden if getattr(args, "qkv", False) else 0
+    bytes_layer = (block_bytes_per_layer(w, qkv_hidden) if qkv_hidden
+                   else w.algorithmic_bytes_per_layer())
     bytes_step = bytes_layer * L
     if bytes_step < 2 * l2:
         l2_note = (f"L2 flushed: a {2 * l2 / 2**20:.0f} MiB buffer is rewritten before each "
@@ -235,7 +259,7 @@ def workload_config(w: wl.Workload, args, world: int, l2: int = L2_BYTES_NOMINAL
     else:
         l2_note = (f"inputs larger than L2: each step reads {bytes_step / 1e9:.3f} GB of KV "
                    f"across {L} per-layer pools")
-    return {"workload": workload_name(spec, w.kv), "batch": spec.batch,
+    cfg = {"workload": workload_name(spec, w.kv, qkv_hidden), "batch": spec.batch,
             "ctx": f"{int(seq_lens_host.min())}-{int(seq_lens_host.max())}",
             "heads": f"{spec.num_q_heads}q/{spec.num_kv_heads}kv",
             "head_dim": spec.head_dim, "page_size": spec.page_size, "layers": L,
@@ -249,6 +273,11 @@ def workload_config(w: wl.Workload, args, world: int, l2: int = L2_BYTES_NOMINAL
                       + ("" if args.no_overlap else
                                             ", programmatic dependent launch"),
             "parallelism": f"replicas x{world}"}
+    if qkv_hidden:
+        cfg["hidden"] = qkv_hidden
+        cfg["launch"] = (f"CUDA graphs: rope table + {L} x (qdec_qkv_append_rope, "
+                         f"qdec_attn_split, qdec_attn_merge)")
+    return cfg
 
 
 # ------------------------------------------------------------ CPU oracle --
@@ -359,13 +388,36 @@ def run_ours(args, dist: Dist):
     torch.cuda.synchronize()
 
     Hq, Hkv = spec.num_q_heads, spec.num_kv_heads
+    if args.qkv:
+        assert w.kv == "bf16", "--qkv runs on a bf16 pool"
+        # hidden states and one merged projection weight per layer (seeded)
+        gen = torch.Generator(device="cuda").manual_seed(spec.seed + 11)
+        step_in = torch.randn((L, spec.batch, args.hidden), generator=gen,
+                              device="cuda").to(torch.bfloat16)
+        w_qkv = torch.empty((L, (Hq + 2 * Hkv) * spec.head_dim, args.hidden),
+                            dtype=torch.bfloat16, device="cuda")
+        for l in range(L):
+            w_qkv[l] = (torch.randn(w_qkv.shape[1:], generator=gen, device="cuda")
+                        / args.hidden ** 0.5).to(torch.bfloat16)
+        q_rot = torch.empty((spec.batch, Hq, spec.head_dim), dtype=torch.float32, device="cuda")
+    else:
+        step_in = w.qkv
+
+    def qkv_layer(l, x, seq_lens, positions, block_table, out_l):
+        qdec.qdec_qkv_append_rope(shape, x, w_qkv[l], w.w_q[l], w.w_k[l], positions, seq_lens,
+                                  block_table, w.pool(l), q_rot, rope, err, stream=stream)
+        qdec.qdec_attn_split(shape, q_rot, w.pool(l), block_table, seq_lens, ws, out_l, err,
+                             stream=stream)
+        qdec.qdec_attn_merge(shape, seq_lens, ws, out_l, err, stream=stream)
 
     def step_fn(qkv, seq_lens, positions, block_table, out_t):
         """One decode step (the rope table, then the L layers) on these buffers."""
         def fn():
             qdec.qdec_rope_table(shape, positions, rope, stream=stream)
             for l in range(L):
-                if w.kv == "fp8":
+                if args.qkv:
+                    qkv_layer(l, qkv[l], seq_lens, positions, block_table, out_t[l])
+                elif w.kv == "fp8":
                     qdec.qdec_step_fp8(shape, qkv[l, :, :Hq], qkv[l, :, Hq:Hq + Hkv],
                                        qkv[l, :, Hq + Hkv:], w.w_q[l], w.w_k[l], positions,
                                        seq_lens, block_table, w.pool8(l), w.scale(l), ws,
@@ -390,7 +442,7 @@ def run_ours(args, dist: Dist):
         return g.replay
 
     graphs = []
-    step0 = step_fn(w.qkv, w.seq_lens, w.positions, w.block_table, out)
+    step0 = step_fn(step_in, w.seq_lens, w.positions, w.block_table, out)
     with torch.cuda.stream(stream):
         step0()  # the first launch configures the kernels outside capture
     stream.synchronize()
@@ -406,8 +458,10 @@ def run_ours(args, dist: Dist):
     # Steps whose inputs fit in L2 twice over are timed L2-cold: a buffer
     # larger than L2 is rewritten before each one, outside the timed steps.
     l2 = l2_bytes(dev)
+    bytes_layer = (block_bytes_per_layer(w, args.hidden) if args.qkv
+                   else w.algorithmic_bytes_per_layer())
     flush = (torch.empty(2 * l2 // 4, dtype=torch.int32, device="cuda")
-             if w.algorithmic_bytes_per_layer() * L < 2 * l2 else None)
+             if bytes_layer * L < 2 * l2 else None)
 
     # ---- device-timed region
     clocks = Clocks(dev)
@@ -437,7 +491,6 @@ def run_ours(args, dist: Dist):
     st, flags = qdec.qdec_check_error(err, stream)
     assert st == 0, f"device error flags {flags:#x}"
 
-    bytes_layer = w.algorithmic_bytes_per_layer()
     bytes_step = bytes_layer * L
     ms_step = t_ms_max / args.steps
     value = dist.world * bytes_step * args.steps / (t_ms_max * 1e-3) / 1e9
@@ -445,13 +498,39 @@ def run_ours(args, dist: Dist):
     # over its L launches, so an upper bound of the launch's duration
     launch_us = t_steps_ms / args.steps / L * 1e3
     achieved = bytes_layer / (launch_us * 1e-6) / 1e9
+    roof_bytes, roof_kernel = bytes_layer, ("attention_kernel<fused, fp8>" if w.kv == "fp8"
+                                            else "attention_kernel<fused>")
+    roof_how = (f"CUDA events around each step's graph (rope table + {L} launches, gaps "
+                f"included) / {L}")
+    if args.qkv:
+        # the projection kernel alone: a graph of its L launches, timed the same way
+        gq = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(gq, stream=stream):
+                for l in range(L):
+                    qdec.qdec_qkv_append_rope(shape, step_in[l], w_qkv[l], w.w_q[l], w.w_k[l],
+                                              w.positions, w.seq_lens, w.block_table, w.pool(l),
+                                              q_rot, rope, err, stream=stream)
+            for _ in range(3):
+                gq.replay()
+            e0.record(stream)
+            reps = max(10, args.steps // 4)
+            for _ in range(reps):
+                gq.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        launch_us = e0.elapsed_time(e1) / reps / L * 1e3
+        roof_bytes = qkv_weight_bytes(spec, args.hidden) + spec.batch * args.hidden * 2
+        achieved = roof_bytes / (launch_us * 1e-6) / 1e9
+        roof_kernel = "qkv_append_kernel"
+        roof_how = f"CUDA events around a graph of {L} projection launches, {reps} replays"
     peak, peak_kind = measured_peaks()
 
     # ---- end to end: pinned host inputs in, outputs out, every step.  Two
     # sets of device buffers: a step's input copies and its output copy run on
     # their own streams, overlapping the neighbouring steps' kernels.
     meta = [w.seq_lens, w.positions, w.block_table]
-    qkv_h = w.qkv.cpu().pin_memory()
+    qkv_h = step_in.cpu().pin_memory()
     meta_h = [m.cpu().pin_memory() for m in meta]
     h2d = qkv_h.numel() * qkv_h.element_size() + sum(m.numel() * m.element_size() for m in meta_h)
     d2h = out.numel() * out.element_size()
@@ -459,7 +538,7 @@ def run_ours(args, dist: Dist):
     if k_e2e:
         sets = []
         for j in range(2):
-            qkv_d = torch.empty_like(w.qkv)
+            qkv_d = torch.empty_like(step_in)
             meta_d = [torch.empty_like(m) for m in meta]
             out_d = torch.empty_like(out)
             for d, h in zip([qkv_d] + meta_d, [qkv_h] + meta_h):
@@ -503,12 +582,12 @@ def run_ours(args, dist: Dist):
     assert st == 0, f"device error flags {flags:#x}"
 
     traffic = None
-    tr = TRAFFIC.get(workload_name(spec, w.kv))
+    tr = TRAFFIC.get(workload_name(spec, w.kv, args.hidden if args.qkv else 0))
     if tr and tr["kernel_sha"] == kernel_sha():
         traffic = tr["bytes_per_launch"]
 
     cpu = None
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and not args.qkv:
         w_cpu = wl.build(spec, "cpu", layers=min(spec.layers, CPU_SAMPLE_LAYERS), kv=w.kv)
         gbs, what, n, secs = oracle_sample(w_cpu, args.cpu_seconds, per_seq=False)
         cpu = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -522,8 +601,10 @@ def run_ours(args, dist: Dist):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": ("e4m3 KV (f16 mma, f32 accumulate)" if w.kv == "fp8" else "bf16"),
-            "data": "synthetic (seeded N(0,1) bf16 q/k/v and KV pages"
-                    + (", pages cast to E4M3 with amax/448 scales)" if w.kv == "fp8" else ")"),
+            "data": ("synthetic (seeded N(0,1) bf16 hidden states, N(0,1/hidden) bf16 merged "
+                     "QKV weights and KV pages)" if args.qkv else
+                     "synthetic (seeded N(0,1) bf16 q/k/v and KV pages"
+                     + (", pages cast to E4M3 with amax/448 scales)" if w.kv == "fp8" else ")")),
             "us_per_layer_step": round(ms_step * 1e3 / L, 4),
             "pct_of_hbm_peak": round(100 * value / dist.world / peak, 2),
             "config": workload_config(w, args, dist.world, l2_bytes(dev)),
@@ -531,16 +612,14 @@ def run_ours(args, dist: Dist):
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_kind == "measured" else "fallback",
-                         "kernel": ("attention_kernel<fused, fp8>" if w.kv == "fp8"
-                                    else "attention_kernel<fused>"),
+                         "kernel": roof_kernel,
                          "launch_us": round(launch_us, 3),
-                         "launch_us_how": f"CUDA events around each step's graph (rope table + "
-                                          f"{L} launches, gaps included) / {L}",
-                         "bytes_per_launch": bytes_layer},
+                         "launch_us_how": roof_how,
+                         "bytes_per_launch": roof_bytes},
             "e2e": {"value": e2e_value and round(e2e_value, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": k_e2e},
-            "gpu_launches": (L + 1) * args.steps,
+            "gpu_launches": ((3 * L if args.qkv else L) + 1) * args.steps,
             "clocks": ck,
             "cpu_baseline": cpu,
         }

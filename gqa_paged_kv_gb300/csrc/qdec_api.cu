@@ -660,6 +660,7 @@ qdec_status qdec_qkv_append_rope(const qdec_shape *shape, int32_t hidden, const 
     Params p{};
     fill_common(p, shape, false);
     p.hidden = hidden;
+    qdec::qkv_geometry(shape->batch, hidden, p.qkv_rows, p.qkv_boxes, p.qkv_stages);
     p.w_q = reinterpret_cast<const __nv_bfloat16 *>(q_norm_w);
     p.w_k = reinterpret_cast<const __nv_bfloat16 *>(k_norm_w);
     p.positions = positions;
@@ -673,7 +674,8 @@ qdec_status qdec_qkv_append_rope(const qdec_shape *shape, int32_t hidden, const 
                          qdec::kHeadDim;
     CUtensorMap w_map, x_map;
     if ((st = encode_rows_map(&w_map, w_qkv, rows, hidden, hidden, 16)) != QDEC_OK) return st;
-    if ((st = encode_rows_map(&x_map, x, shape->batch, hidden, x_stride, 64)) != QDEC_OK) return st;
+    if ((st = encode_rows_map(&x_map, x, shape->batch, hidden, x_stride, p.qkv_rows)) != QDEC_OK)
+        return st;
     return cuda_status(qdec::launch_qkv_append(p, w_map, x_map, static_cast<cudaStream_t>(stream)));
 }
 

@@ -84,6 +84,9 @@ struct Params {
     long long wait_cycles;   // budget of every bounded wait, in SM cycles
     int withhold_first;      // test hook: CTA-local tile 0 is never copied (see qdec.h)
     int hidden;              // QKV projection: hidden size (a multiple of 64)
+    int qkv_rows;            // QKV projection: hidden-state rows per stage (16, 32, 48 or 64)
+    int qkv_stages;          // QKV projection: ring depth
+    int qkv_boxes;           // QKV projection: 64-element boxes along hidden per stage
     double inv_freq[kRotPairs];  // rope_theta^(-2i/D), i < D/2
 };
 
@@ -111,5 +114,11 @@ cudaError_t launch_merge(const Params &p, cudaStream_t s);
 // 64 x 64 boxes, both bf16, 128-byte swizzled.
 cudaError_t launch_qkv_append(const Params &p, const CUtensorMap &w_map, const CUtensorMap &x_map,
                               cudaStream_t s);
+// Stage geometry of the projection for batch B and hidden size: the hidden-
+// state rows (B rounded up to 16, at most 64), 64-element boxes along hidden
+// per stage (4 for up to 16 rows, 2 up to 32, else 1, so that each weight
+// row is read in runs of up to 512 bytes), and as many stages as about
+// 96 KiB hold.
+void qkv_geometry(int B, int hidden, int &rows, int &boxes, int &stages);
 
 }  // namespace qdec

@@ -13,12 +13,15 @@
 // Layout: a cluster of 4 CTAs per output head; CTA r of the cluster computes
 // head dims 16r .. 16r+15 and 64+16r .. 64+16r+15 (so every rotate-half pair
 // stays inside one CTA) for 64 batch rows, over the whole hidden dimension.
-// One producer warp streams 64-element chunks of W (two 16-row boxes) and of
-// x (one 64-row box, rows past B read as zero) with TMA into a ring; four
-// consumer warps each own 16 batch rows and run bf16 mma.sync (fp32
-// accumulate).  The RMSNorm needs the sum of squares over all 128 dims: each
-// CTA leaves its share per row in shared memory and reads the peers' shares
-// over distributed shared memory between two cluster-barrier phases.
+// One producer warp streams chunks of 64, 128 or 256 hidden elements (1, 2 or
+// 4 boxes of 64 along hidden, the more the smaller the batch, so that each
+// weight row is read in runs of up to 512 bytes) of W (two 16-row blocks) and
+// of x (the batch rounded up to 16 rows, at most 64; rows past B read as
+// zero) with TMA into a ring of about 96 KiB; four consumer warps each own 16
+// batch rows and run bf16 mma.sync (fp32 accumulate).  The
+// RMSNorm needs the sum of squares over all 128 dims: each CTA leaves its
+// share per row in shared memory and reads the peers' shares over
+// distributed shared memory between two cluster-barrier phases.
 #include "qdec_internal.h"
 #include "qdec_ptx.cuh"
 #include "qdec.h"
@@ -34,12 +37,16 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr int kQkvCluster = 4;                              // CTAs per output head
 constexpr int kQkvRows = 4 * 16;                            // batch rows per CTA (4 warps x m16)
 constexpr int kQkvChunk = 64;                               // hidden elements per stage
-constexpr int kQkvStages = 8;
+constexpr int kQkvMaxStages = 16;
 constexpr int kQkvWBox = 16 * kQkvChunk * 2;                // one 16-row W box, 2 KiB
-constexpr int kQkvXBytes = kQkvRows * kQkvChunk * 2;        // 8 KiB
-constexpr int kQkvStageBytes = 2 * kQkvWBox + kQkvXBytes;   // 12 KiB
-constexpr int kQkvTail = kQkvStages * kQkvStageBytes;       // barriers, flags, row sums
-constexpr int kQkvSmem = kQkvTail + 2 * kQkvStages * 8 + 16 + kQkvRows * 4 + 1024;
+constexpr int kQkvRingBytes = 96 * 1024;
+// after the ring: barriers full[16], empty[16], the abort flag, row sums
+constexpr int kQkvTailBytes = 2 * kQkvMaxStages * 8 + 16 + kQkvRows * 4;
+// a stage: [W rows 16r.. boxes][W rows 64+16r.. boxes][x boxes], each box
+// starting on a 1024-byte boundary (rows is a multiple of 16)
+__host__ __device__ constexpr int qkv_stage_bytes(int rows, int boxes) {
+    return boxes * (2 * kQkvWBox + rows * kQkvChunk * 2);
+}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
                                             uint32_t bar) {
@@ -73,14 +80,23 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int head = blockIdx.x / kQkvCluster, rank = blockIdx.x % kQkvCluster;
     const int row0 = blockIdx.y * kQkvRows;
-    const int nchunks = p.hidden / kQkvChunk;
-    const uint32_t full0 = smem_u32(sm + kQkvTail);
-    const uint32_t empty0 = full0 + kQkvStages * 8;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + kQkvTail + 2 * kQkvStages * 8);
-    float *ss = reinterpret_cast<float *>(sm + kQkvTail + 2 * kQkvStages * 8 + 16);
+    const int NB = p.qkv_boxes;
+    const int nchunks = p.hidden / (kQkvChunk * NB);
+    const int NS = p.qkv_stages;
+    const int stage_bytes = qkv_stage_bytes(p.qkv_rows, NB);
+    uint8_t *tail = sm + NS * stage_bytes;
+    const uint32_t full0 = smem_u32(tail);
+    const uint32_t empty0 = full0 + kQkvMaxStages * 8;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tail + 2 * kQkvMaxStages * 8);
+    float *ss = reinterpret_cast<float *>(tail + 2 * kQkvMaxStages * 8 + 16);
+    if (NS < 1 || NS > kQkvMaxStages || p.qkv_rows < 16 || p.qkv_rows > kQkvRows ||
+        p.qkv_rows % 16 != 0 || NB < 1 || NB > 4 || p.hidden % (kQkvChunk * NB) != 0) {
+        if (tid == 0) flag_error(p.err, QDEC_FLAG_BAD_INDEX);
+        return;  // uniform over the cluster: every CTA sees the same parameters
+    }
 
     if (tid == 0) {
-        for (int s = 0; s < kQkvStages; ++s) {
+        for (int s = 0; s < NS; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, kConsumerWarps);  // every warp takes every chunk
         }
@@ -94,20 +110,24 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) {
             const int wrow = head * kHeadDim + 16 * rank;
             for (int c = 0; c < nchunks; ++c) {
-                const int s = c % kQkvStages;
-                if (c >= kQkvStages &&
-                    !mbar_wait_bounded(empty0 + 8 * s, ((c / kQkvStages) - 1) & 1, abort_flag,
+                const int s = c % NS;
+                if (c >= NS &&
+                    !mbar_wait_bounded(empty0 + 8 * s, ((c / NS) - 1) & 1, abort_flag,
                                        p.wait_cycles)) {
                     *abort_flag = 1;
                     flag_error(p.err, QDEC_FLAG_TIMEOUT);
                     break;
                 }
                 const uint32_t full = full0 + 8 * s;
-                const uint32_t dst = smem_u32(sm + s * kQkvStageBytes);
-                mbar_arrive_expect_tx(full, kQkvStageBytes);
-                tma_load_2d(dst, &w_map, c * kQkvChunk, wrow, full);
-                tma_load_2d(dst + kQkvWBox, &w_map, c * kQkvChunk, wrow + 64, full);
-                tma_load_2d(dst + 2 * kQkvWBox, &x_map, c * kQkvChunk, row0, full);
+                const uint32_t dst = smem_u32(sm + s * stage_bytes);
+                mbar_arrive_expect_tx(full, stage_bytes);
+                for (int j = 0; j < NB; ++j) {
+                    const int k = (c * NB + j) * kQkvChunk;
+                    tma_load_2d(dst + j * kQkvWBox, &w_map, k, wrow, full);
+                    tma_load_2d(dst + (NB + j) * kQkvWBox, &w_map, k, wrow + 64, full);
+                    tma_load_2d(dst + 2 * NB * kQkvWBox + j * p.qkv_rows * kQkvChunk * 2, &x_map,
+                                k, row0, full);
+                }
             }
         }
         __syncwarp();
@@ -126,8 +146,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int arow = 16 * warp + (mi & 1) * 8 + r8;  // x row this lane addresses
         const int brow = (mi >> 1) * 8 + r8;             // W row within a 16-row box
         for (int c = 0; c < nchunks; ++c) {
-            const int s = c % kQkvStages;
-            const bool ok = mbar_wait_bounded(full0 + 8 * s, (c / kQkvStages) & 1, abort_flag,
+            const int s = c % NS;
+            const bool ok = mbar_wait_bounded(full0 + 8 * s, (c / NS) & 1, abort_flag,
                                               p.wait_cycles);
             if (!ok) {
                 if (lane == 0) {
@@ -136,15 +156,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 break;
             }
-            if (live) {
-                const uint32_t wb = smem_u32(sm + s * kQkvStageBytes);
-                const uint32_t xb = wb + 2 * kQkvWBox;
+            for (int j = 0; j < NB && live; ++j) {
+                const uint32_t sb = smem_u32(sm + s * stage_bytes);
+                const uint32_t wa = sb + j * kQkvWBox, wbb = sb + (NB + j) * kQkvWBox;
+                const uint32_t xb = sb + 2 * NB * kQkvWBox + j * p.qkv_rows * kQkvChunk * 2;
 #pragma unroll
                 for (int kk = 0; kk < kQkvChunk / 16; ++kk) {
                     uint32_t a[4], b01[4], b23[4];
                     ldmatrix_x4(a, swz(xb, arow, 2 * kk + (mi >> 1)));
-                    ldmatrix_x4(b01, swz(wb, brow, 2 * kk + (mi & 1)));
-                    ldmatrix_x4(b23, swz(wb + kQkvWBox, brow, 2 * kk + (mi & 1)));
+                    ldmatrix_x4(b01, swz(wa, brow, 2 * kk + (mi & 1)));
+                    ldmatrix_x4(b23, swz(wbb, brow, 2 * kk + (mi & 1)));
                     mma_bf16(acc[0], a, b01[0], b01[1]);
                     mma_bf16(acc[1], a, b01[2], b01[3]);
                     mma_bf16(acc[2], a, b23[0], b23[1]);
@@ -243,19 +264,25 @@ __global__ void __launch_bounds__(kThreads, 2)
     // a wait that gave up may leave copies in flight: let them land (bounded)
     if (tid == 0 && *abort_flag) {
         volatile int never = 0;
-        const int first = nchunks > kQkvStages ? nchunks - kQkvStages : 0;
+        const int first = nchunks > NS ? nchunks - NS : 0;
         for (int c = first; c < nchunks; ++c)
-            mbar_wait_bounded(full0 + 8 * (c % kQkvStages), (c / kQkvStages) & 1, &never,
-                              p.wait_cycles);
+            mbar_wait_bounded(full0 + 8 * (c % NS), (c / NS) & 1, &never, p.wait_cycles);
     }
 }
 
 std::mutex g_qkv_mu;
 bool g_qkv_smem_set[64];
+constexpr int kQkvSmemMax = kQkvRingBytes + kQkvTailBytes + 1024;
 
 }  // namespace
 
-size_t qkv_smem_bytes() { return kQkvSmem; }
+void qkv_geometry(int B, int hidden, int &rows, int &boxes, int &stages) {
+    rows = B >= kQkvRows ? kQkvRows : (B + 15) / 16 * 16;
+    boxes = rows <= 16 ? 4 : (rows <= 32 ? 2 : 1);
+    while (boxes > 1 && hidden % (kQkvChunk * boxes) != 0) boxes /= 2;
+    stages = kQkvRingBytes / qkv_stage_bytes(rows, boxes);
+    if (stages > kQkvMaxStages) stages = kQkvMaxStages;
+}
 
 cudaError_t launch_qkv_append(const Params &p, const CUtensorMap &w_map, const CUtensorMap &x_map,
                               cudaStream_t s) {
@@ -266,7 +293,7 @@ cudaError_t launch_qkv_append(const Params &p, const CUtensorMap &w_map, const C
         std::lock_guard<std::mutex> lock(g_qkv_mu);
         if (!g_qkv_smem_set[dev]) {
             const cudaError_t e = cudaFuncSetAttribute(
-                qkv_append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkvSmem);
+                qkv_append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkvSmemMax);
             if (e != cudaSuccess) return e;
             g_qkv_smem_set[dev] = true;
         }
@@ -274,7 +301,8 @@ cudaError_t launch_qkv_append(const Params &p, const CUtensorMap &w_map, const C
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((p.Hq + 2 * p.Hkv) * kQkvCluster, (p.B + kQkvRows - 1) / kQkvRows);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kQkvSmem;
+    cfg.dynamicSmemBytes =
+        p.qkv_stages * qkv_stage_bytes(p.qkv_rows, p.qkv_boxes) + kQkvTailBytes + 1024;
     cfg.stream = s;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
