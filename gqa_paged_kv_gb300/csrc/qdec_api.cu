@@ -640,8 +640,21 @@ qdec_status qdec_step_fp8(const qdec_shape *shape, const qdec_bf16 *q, int64_t q
                      workspace, workspace_bytes, out, err_flag, stream);
 }
 
+qdec_status qdec_qkv_pack_weights(const qdec_shape *shape, int32_t hidden, const qdec_bf16 *w_qkv,
+                                  qdec_bf16 *w_packed, void *stream) {
+    qdec_status st = check_shape(shape);
+    if (st != QDEC_OK) return st;
+    if (hidden < 64 || hidden % 64 != 0) return QDEC_ERR_UNSUPPORTED;
+    if (!w_qkv || !w_packed || !aligned16(w_qkv) || !aligned16(w_packed) || w_qkv == w_packed)
+        return QDEC_ERR_INVALID_ARG;
+    const int rows = (shape->num_q_heads + 2 * shape->num_kv_heads) * qdec::kHeadDim;
+    return cuda_status(qdec::launch_qkv_pack(reinterpret_cast<const __nv_bfloat16 *>(w_qkv),
+                                             reinterpret_cast<__nv_bfloat16 *>(w_packed), rows,
+                                             hidden, static_cast<cudaStream_t>(stream)));
+}
+
 qdec_status qdec_qkv_append_rope(const qdec_shape *shape, int32_t hidden, const qdec_bf16 *x,
-                                 int64_t x_stride, const qdec_bf16 *w_qkv,
+                                 int64_t x_stride, const qdec_bf16 *w_packed,
                                  const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
                                  const int32_t *positions, const int32_t *seq_lens,
                                  const int32_t *block_table, const void *rope_table,
@@ -650,10 +663,10 @@ qdec_status qdec_qkv_append_rope(const qdec_shape *shape, int32_t hidden, const 
     qdec_status st = check_shape(shape);
     if (st != QDEC_OK) return st;
     if (hidden < 64 || hidden % 64 != 0) return QDEC_ERR_UNSUPPORTED;
-    if (!x || !w_qkv || !q_norm_w || !k_norm_w || !positions || !seq_lens || !block_table ||
+    if (!x || !w_packed || !q_norm_w || !k_norm_w || !positions || !seq_lens || !block_table ||
         !rope_table || !kv_pool || !q_rot)
         return QDEC_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(q_norm_w) || !aligned16(k_norm_w) ||
+    if (!aligned16(x) || !aligned16(w_packed) || !aligned16(q_norm_w) || !aligned16(k_norm_w) ||
         !aligned16(rope_table) || !aligned16(kv_pool) || !aligned16(q_rot))
         return QDEC_ERR_INVALID_ARG;
     if (x_stride < hidden || x_stride % 8 != 0) return QDEC_ERR_INVALID_ARG;
@@ -670,13 +683,11 @@ qdec_status qdec_qkv_append_rope(const qdec_shape *shape, int32_t hidden, const 
     p.pool = reinterpret_cast<__nv_bfloat16 *>(kv_pool);
     p.q_rot_out = q_rot;
     p.err = err_flag;
-    const int64_t rows = static_cast<int64_t>(shape->num_q_heads + 2 * shape->num_kv_heads) *
-                         qdec::kHeadDim;
-    CUtensorMap w_map, x_map;
-    if ((st = encode_rows_map(&w_map, w_qkv, rows, hidden, hidden, 16)) != QDEC_OK) return st;
+    p.w_packed = reinterpret_cast<const __nv_bfloat16 *>(w_packed);
+    CUtensorMap x_map;
     if ((st = encode_rows_map(&x_map, x, shape->batch, hidden, x_stride, p.qkv_rows)) != QDEC_OK)
         return st;
-    return cuda_status(qdec::launch_qkv_append(p, w_map, x_map, static_cast<cudaStream_t>(stream)));
+    return cuda_status(qdec::launch_qkv_append(p, x_map, static_cast<cudaStream_t>(stream)));
 }
 
 qdec_status qdec_check_error(int32_t *err_flag, void *stream, int32_t *flags_out) {

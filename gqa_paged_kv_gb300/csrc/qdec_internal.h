@@ -86,7 +86,8 @@ struct Params {
     int hidden;              // QKV projection: hidden size (a multiple of 64)
     int qkv_rows;            // QKV projection: hidden-state rows per stage (16, 32, 48 or 64)
     int qkv_stages;          // QKV projection: ring depth
-    int qkv_boxes;           // QKV projection: 64-element boxes along hidden per stage
+    int qkv_boxes;           // QKV projection: 64-element blocks along hidden per stage
+    const __nv_bfloat16 *w_packed;  // QKV projection: the weight in the packed order
     double inv_freq[kRotPairs];  // rope_theta^(-2i/D), i < D/2
 };
 
@@ -109,11 +110,14 @@ cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, bool fu
                              cudaStream_t s);
 cudaError_t launch_merge(const Params &p, cudaStream_t s);
 
-// The merged QKV projection fused with steps 1-3 (qdec_qkv.cu): w_map views
-// W [(Hq+2Hkv)*D][hidden] with 64 x 16 boxes, x_map views x [B][hidden] with
-// 64 x 64 boxes, both bf16, 128-byte swizzled.
-cudaError_t launch_qkv_append(const Params &p, const CUtensorMap &w_map, const CUtensorMap &x_map,
-                              cudaStream_t s);
+// The merged QKV projection fused with steps 1-3 (qdec_qkv.cu): the weight
+// comes packed (qdec_qkv_pack_weights), x_map views x [B][hidden] with boxes
+// of 64 elements x p.qkv_rows rows, 128-byte swizzled.
+cudaError_t launch_qkv_append(const Params &p, const CUtensorMap &x_map, cudaStream_t s);
+// Packs W [rows][hidden] (rows = (Hq + 2 Hkv) * 128) into the order the
+// projection streams it.
+cudaError_t launch_qkv_pack(const __nv_bfloat16 *w, __nv_bfloat16 *w_packed, int rows,
+                            int hidden, cudaStream_t s);
 // Stage geometry of the projection for batch B and hidden size: the hidden-
 // state rows (B rounded up to 16, at most 64), 64-element boxes along hidden
 // per stage (4 for up to 16 rows, 2 up to 32, else 1, so that each weight

@@ -52,6 +52,16 @@ static __device__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile
 static __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Plain bulk copy global -> shared (16-byte aligned addresses and size),
+// counted on the transaction barrier `bar`.
+static __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                                 uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
 static __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])

@@ -13,12 +13,15 @@
 // Layout: a cluster of 4 CTAs per output head; CTA r of the cluster computes
 // head dims 16r .. 16r+15 and 64+16r .. 64+16r+15 (so every rotate-half pair
 // stays inside one CTA) for 64 batch rows, over the whole hidden dimension.
-// One producer warp streams chunks of 64, 128 or 256 hidden elements (1, 2 or
-// 4 boxes of 64 along hidden, the more the smaller the batch, so that each
-// weight row is read in runs of up to 512 bytes) of W (two 16-row blocks) and
-// of x (the batch rounded up to 16 rows, at most 64; rows past B read as
-// zero) with TMA into a ring of about 96 KiB; four consumer warps each own 16
-// batch rows and run bf16 mma.sync (fp32 accumulate).  The
+// The weight is packed once (qdec_qkv_pack_weights) into the order the
+// projection reads it: for every (head, cluster rank) the 32 rows it owns, in
+// blocks of 64 hidden elements, each block 4 KiB contiguous with its
+// 128-byte rows already swizzled for conflict-free matrix loads; a CTA's
+// whole share is one contiguous run.  One producer warp streams stages of
+// 1, 2 or 4 such blocks (one bulk copy; more for smaller batches) and the
+// matching boxes of x (the batch rounded up to 16 rows, at most 64; rows past
+// B read as zero, TMA) into a ring of about 96 KiB; four consumer warps each
+// own 16 batch rows and run bf16 mma.sync (fp32 accumulate).  The
 // RMSNorm needs the sum of squares over all 128 dims: each CTA leaves its
 // share per row in shared memory and reads the peers' shares over
 // distributed shared memory between two cluster-barrier phases.
@@ -28,6 +31,7 @@
 
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 namespace qdec {
@@ -42,8 +46,8 @@ constexpr int kQkvWBox = 16 * kQkvChunk * 2;                // one 16-row W box,
 constexpr int kQkvRingBytes = 96 * 1024;
 // after the ring: barriers full[16], empty[16], the abort flag, row sums
 constexpr int kQkvTailBytes = 2 * kQkvMaxStages * 8 + 16 + kQkvRows * 4;
-// a stage: [W rows 16r.. boxes][W rows 64+16r.. boxes][x boxes], each box
-// starting on a 1024-byte boundary (rows is a multiple of 16)
+// a stage: [packed W blocks, 4 KiB each: rows 16r.. then rows 64+16r..][x
+// boxes], each piece starting on a 1024-byte boundary (rows % 16 == 0)
 __host__ __device__ constexpr int qkv_stage_bytes(int rows, int boxes) {
     return boxes * (2 * kQkvWBox + rows * kQkvChunk * 2);
 }
@@ -72,8 +76,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c) {
 }
 
 __global__ void __launch_bounds__(kThreads, 2)
-    qkv_append_kernel(const __grid_constant__ CUtensorMap w_map,
-                      const __grid_constant__ CUtensorMap x_map, const __grid_constant__ Params p) {
+    qkv_append_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -108,7 +111,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == kConsumerWarps) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
-            const int wrow = head * kHeadDim + 16 * rank;
+            // this CTA's packed blocks: (head * 4 + rank) * (hidden / 64) onwards
+            const __nv_bfloat16 *wsrc =
+                p.w_packed + static_cast<int64_t>(head * kQkvCluster + rank) * p.hidden * 32;
             for (int c = 0; c < nchunks; ++c) {
                 const int s = c % NS;
                 if (c >= NS &&
@@ -121,13 +126,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const uint32_t full = full0 + 8 * s;
                 const uint32_t dst = smem_u32(sm + s * stage_bytes);
                 mbar_arrive_expect_tx(full, stage_bytes);
-                for (int j = 0; j < NB; ++j) {
-                    const int k = (c * NB + j) * kQkvChunk;
-                    tma_load_2d(dst + j * kQkvWBox, &w_map, k, wrow, full);
-                    tma_load_2d(dst + (NB + j) * kQkvWBox, &w_map, k, wrow + 64, full);
+                bulk_load(dst, wsrc + static_cast<int64_t>(c) * NB * 32 * kQkvChunk,
+                          NB * 2 * kQkvWBox, full);
+                for (int j = 0; j < NB; ++j)
                     tma_load_2d(dst + 2 * NB * kQkvWBox + j * p.qkv_rows * kQkvChunk * 2, &x_map,
-                                k, row0, full);
-                }
+                                (c * NB + j) * kQkvChunk, row0, full);
             }
         }
         __syncwarp();
@@ -158,7 +161,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             for (int j = 0; j < NB && live; ++j) {
                 const uint32_t sb = smem_u32(sm + s * stage_bytes);
-                const uint32_t wa = sb + j * kQkvWBox, wbb = sb + (NB + j) * kQkvWBox;
+                // packed block j: rows 0..15 dims 16r.., rows 16..31 dims 64 + 16r..
+                const uint32_t wa = sb + j * 2 * kQkvWBox, wbb = wa + kQkvWBox;
                 const uint32_t xb = sb + 2 * NB * kQkvWBox + j * p.qkv_rows * kQkvChunk * 2;
 #pragma unroll
                 for (int kk = 0; kk < kQkvChunk / 16; ++kk) {
@@ -270,6 +274,29 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
+// Packing: destination 16-byte unit u lies in block u / 256 (4 KiB), row
+// (u / 8) % 32 of the block, position u % 8, which holds source chunk
+// (u % 8) ^ (row % 8) of that row (the 128-byte swizzle).  Block index =
+// (head * 4 + rank) * (hidden / 64) + k-block; block rows 0-15 are weight rows
+// head * 128 + 16 rank + i, rows 16-31 are head * 128 + 64 + 16 rank + i.
+__global__ void qkv_pack_kernel(const __nv_bfloat16 *w, __nv_bfloat16 *wp, int rows, int hidden) {
+    const int64_t total = static_cast<int64_t>(rows) * hidden / 8;
+    const int nk = hidden / kQkvChunk;
+    for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < total;
+         u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t block = u / 256;
+        const int rho = static_cast<int>((u / 8) % 32), pos = static_cast<int>(u % 8);
+        const int q = pos ^ (rho & 7);
+        const int kb = static_cast<int>(block % nk);
+        const int64_t hr = block / nk;  // head * 4 + rank
+        const int head = static_cast<int>(hr / kQkvCluster), rank = static_cast<int>(hr % kQkvCluster);
+        const int row = head * kHeadDim + (rho < 16 ? 16 * rank + rho : 64 + 16 * rank + rho - 16);
+        const uint4 v = *reinterpret_cast<const uint4 *>(
+            w + static_cast<int64_t>(row) * hidden + kb * kQkvChunk + q * 8);
+        *reinterpret_cast<uint4 *>(wp + u * 8) = v;
+    }
+}
+
 std::mutex g_qkv_mu;
 bool g_qkv_smem_set[64];
 constexpr int kQkvSmemMax = kQkvRingBytes + kQkvTailBytes + 1024;
@@ -284,8 +311,16 @@ void qkv_geometry(int B, int hidden, int &rows, int &boxes, int &stages) {
     if (stages > kQkvMaxStages) stages = kQkvMaxStages;
 }
 
-cudaError_t launch_qkv_append(const Params &p, const CUtensorMap &w_map, const CUtensorMap &x_map,
-                              cudaStream_t s) {
+cudaError_t launch_qkv_pack(const __nv_bfloat16 *w, __nv_bfloat16 *w_packed, int rows,
+                            int hidden, cudaStream_t s) {
+    const int64_t units = static_cast<int64_t>(rows) * hidden / 8;
+    const int threads = 256;
+    const int blocks = static_cast<int>(std::min<int64_t>((units + threads - 1) / threads, 4096));
+    qkv_pack_kernel<<<blocks, threads, 0, s>>>(w, w_packed, rows, hidden);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qkv_append(const Params &p, const CUtensorMap &x_map, cudaStream_t s) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 63;
@@ -311,7 +346,7 @@ cudaError_t launch_qkv_append(const Params &p, const CUtensorMap &w_map, const C
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, qkv_append_kernel, w_map, x_map, p);
+    return cudaLaunchKernelEx(&cfg, qkv_append_kernel, x_map, p);
 }
 
 }  // namespace qdec

@@ -35,7 +35,8 @@ QDEC_LAUNCH_TEST_WITHHOLD_TILE = 1 << 30
 # Every symbol include/qdec.h declares.
 EXPORTS = ("qdec_workspace_bytes", "qdec_workspace_init", "qdec_rope_table_bytes",
            "qdec_rope_table", "qdec_append_rope", "qdec_attn_split", "qdec_attn_merge",
-           "qdec_step", "qdec_qkv_append_rope", "qdec_append_rope_fp8", "qdec_attn_split_fp8",
+           "qdec_step", "qdec_qkv_append_rope", "qdec_qkv_pack_weights", "qdec_append_rope_fp8",
+           "qdec_attn_split_fp8",
            "qdec_step_fp8",
            "qdec_step_static_scratch", "qdec_check_error", "qdec_status_string", "qdec_version")
 
@@ -109,6 +110,8 @@ def _load():
     lib.qdec_qkv_append_rope.argtypes = [sp, ctypes.c_int32, vp, i64, vp, vp, vp, vp, vp, vp, vp,
                                          vp, vp, vp, vp]
     lib.qdec_qkv_append_rope.restype = st
+    lib.qdec_qkv_pack_weights.argtypes = [sp, ctypes.c_int32, vp, vp, vp]
+    lib.qdec_qkv_pack_weights.restype = st
     lib.qdec_append_rope_fp8.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp,
                                          vp, vp, vp, vp, vp]
     lib.qdec_append_rope_fp8.restype = st
@@ -219,14 +222,20 @@ def qdec_step(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, seq_lens, bl
         _stream(stream)), "qdec_step")
 
 
-def qdec_qkv_append_rope(shape: Shape, x, w_qkv, q_norm_w, k_norm_w, positions, seq_lens,
+def qdec_qkv_pack_weights(shape: Shape, w_qkv, w_packed, stream=None):
+    """Pack the row-major merged weight [(Hq+2Hkv)*D][hidden] for the projection."""
+    _raise(_lib.qdec_qkv_pack_weights(ctypes.byref(shape.c()), int(w_qkv.shape[1]), _ptr(w_qkv),
+                                      _ptr(w_packed), _stream(stream)), "qdec_qkv_pack_weights")
+
+
+def qdec_qkv_append_rope(shape: Shape, x, w_packed, q_norm_w, k_norm_w, positions, seq_lens,
                          block_table, kv_pool, q_rot, rope_table, err_flag=None, stream=None):
-    """The merged QKV projection of hidden states x [B][hidden] (row-major
-    w_qkv [(Hq+2Hkv)*D][hidden]) fused with norm, rotation and append."""
+    """The merged QKV projection of hidden states x [B][hidden] (weight packed
+    by qdec_qkv_pack_weights) fused with norm, rotation and append."""
     if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
         raise ValueError("x: expected a bf16 [B][hidden] view with contiguous rows")
     _raise(_lib.qdec_qkv_append_rope(
-        ctypes.byref(shape.c()), int(x.shape[1]), _ptr(x), x.stride(0), _ptr(w_qkv),
+        ctypes.byref(shape.c()), int(x.shape[1]), _ptr(x), x.stride(0), _ptr(w_packed),
         _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions), _ptr(seq_lens), _ptr(block_table),
         _ptr(rope_table), _ptr(kv_pool), _ptr(q_rot), _ptr(err_flag), _stream(stream)),
         "qdec_qkv_append_rope")

@@ -204,8 +204,10 @@ qdec_status qdec_step(const qdec_shape *shape,
  * input is the hidden state:
  *   qkv = W x[b]  for every sequence b, with
  *   x [B][hidden] bf16 (row stride x_stride elements, a multiple of 8),
- *   w_qkv [(Hq + 2 Hkv) * 128][hidden] bf16, row-major: rows h*128 .. +127
- *     are query head h, then the key heads, then the value heads (no bias);
+ *   W = w_qkv [(Hq + 2 Hkv) * 128][hidden] bf16, row-major: rows h*128 .. +127
+ *     are query head h, then the key heads, then the value heads (no bias),
+ *     passed in the packed order qdec_qkv_pack_weights writes (once per
+ *     model load);
  *   hidden a multiple of 64.
  * The projection is kept unrounded (fp32 accumulate) into RMSNorm + NeoX RoPE
  * of the q and k heads and the append: q_rot [B][Hq][128] fp32 (as
@@ -215,12 +217,20 @@ qdec_status qdec_step(const qdec_shape *shape,
  * hidden not a multiple of 64 gives QDEC_ERR_UNSUPPORTED. */
 qdec_status qdec_qkv_append_rope(const qdec_shape *shape, int32_t hidden,
                                  const qdec_bf16 *x, int64_t x_stride,
-                                 const qdec_bf16 *w_qkv,
+                                 const qdec_bf16 *w_packed,
                                  const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
                                  const int32_t *positions, const int32_t *seq_lens,
                                  const int32_t *block_table, const void *rope_table,
                                  qdec_bf16 *kv_pool, float *q_rot, int32_t *err_flag,
                                  void *stream);
+
+/* Rearranges w_qkv (row-major, as above) into w_packed (a separate buffer of
+ * the same size, 16-byte aligned): for every (output head, quarter of its
+ * dims) the rows that quarter needs, in 4 KiB blocks of 64 hidden elements,
+ * so the projection streams one contiguous run per CTA.  A device-side copy
+ * on `stream`; run it once per weight. */
+qdec_status qdec_qkv_pack_weights(const qdec_shape *shape, int32_t hidden,
+                                  const qdec_bf16 *w_qkv, qdec_bf16 *w_packed, void *stream);
 
 /* ------------------------------------------------------------ FP8 KV pool --
  * The same block over a KV cache held in FP8 (essay "推理引擎里面发生了什么"

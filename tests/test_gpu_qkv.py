@@ -44,7 +44,9 @@ def _run(w, x, wqkv):
     q.qdec_rope_table(shape, w.positions, rope)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     q_rot = torch.empty((s.batch, s.num_q_heads, s.head_dim), dtype=torch.float32, device="cuda")
-    q.qdec_qkv_append_rope(shape, x, wqkv, w.w_q[0], w.w_k[0], w.positions, w.seq_lens,
+    packed = torch.empty_like(wqkv)
+    q.qdec_qkv_pack_weights(shape, wqkv, packed)
+    q.qdec_qkv_append_rope(shape, x, packed, w.w_q[0], w.w_k[0], w.positions, w.seq_lens,
                            w.block_table, w.pool(0), q_rot, rope, err)
     ws = q.alloc_workspace(shape)
     out = torch.empty((s.batch, s.num_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
