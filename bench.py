@@ -22,9 +22,10 @@ plane, head) scales (qdec_step_fp8); its bytes count one byte per KV element
 plus the scales read.
 --qkv runs the block from hidden states instead: per layer the merged QKV
 projection fused with norm, rotation and append (qdec_qkv_append_rope, a
-random [(Hq+2Hkv)*128][hidden] weight per layer), then qdec_attn_split and
-qdec_attn_merge; its bytes add the weight and the hidden states and drop
-q/k/v, and the roofline object describes the projection kernel.
+random [(Hq+2Hkv)*128][hidden] weight per layer), then qdec_attn_decode
+(split-KV attention and merge in one launch); its bytes add the weight and
+the hidden states and drop q/k/v, and the roofline object describes the
+projection kernel.
 
 Multi-GPU: the path shards without any exchange, so N ranks run N
 independent replicas (weak scaling); value sums their work over the slowest
@@ -284,7 +285,7 @@ def workload_config(w: wl.Workload, args, world: int, l2: int = L2_BYTES_NOMINAL
     if qkv_hidden:
         cfg["hidden"] = qkv_hidden
         cfg["launch"] = (f"CUDA graphs: rope table + {L} x (qdec_qkv_append_rope, "
-                         f"qdec_attn_split, qdec_attn_merge)")
+                         f"qdec_attn_decode)")
     return cfg
 
 
@@ -416,9 +417,8 @@ def run_ours(args, dist: Dist):
     def qkv_layer(l, x, seq_lens, positions, block_table, out_l):
         qdec.qdec_qkv_append_rope(shape, x, w_qkv[l], w.w_q[l], w.w_k[l], positions, seq_lens,
                                   block_table, w.pool(l), q_rot, rope, err, stream=stream)
-        qdec.qdec_attn_split(shape, q_rot, w.pool(l), block_table, seq_lens, ws, out_l, err,
-                             stream=stream)
-        qdec.qdec_attn_merge(shape, seq_lens, ws, out_l, err, stream=stream)
+        qdec.qdec_attn_decode(shape, q_rot, w.pool(l), block_table, seq_lens, ws, out_l, err,
+                              stream=stream)
 
     def step_fn(qkv, seq_lens, positions, block_table, out_t):
         """One decode step (the rope table, then the L layers) on these buffers."""
@@ -630,7 +630,7 @@ def run_ours(args, dist: Dist):
             "e2e": {"value": e2e_value and round(e2e_value, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": k_e2e},
-            "gpu_launches": ((3 * L if args.qkv else L) + 1) * args.steps,
+            "gpu_launches": ((2 * L if args.qkv else L) + 1) * args.steps,
             "clocks": ck,
             "cpu_baseline": cpu,
         }

@@ -491,7 +491,8 @@ qdec_status attn_split_impl(const qdec_shape *shape, const float *q_rot, const P
     CUtensorMap map;
     if ((st = encode_map(&map, shape, pool)) != QDEC_OK) return st;
     return cuda_status(
-        qdec::launch_attention(p, map, false, pool.fp8, static_cast<cudaStream_t>(stream)));
+        qdec::launch_attention(p, map, qdec::kAttnSplit, pool.fp8,
+                               static_cast<cudaStream_t>(stream)));
 }
 
 qdec_status step_impl(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_stride,
@@ -519,7 +520,33 @@ qdec_status step_impl(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_str
     CUtensorMap map;
     if ((st = encode_map(&map, shape, pool)) != QDEC_OK) return st;
     return cuda_status(
-        qdec::launch_attention(p, map, true, pool.fp8, static_cast<cudaStream_t>(stream)));
+        qdec::launch_attention(p, map, qdec::kAttnFused, pool.fp8,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+qdec_status attn_decode_impl(const qdec_shape *shape, const float *q_rot, const PoolArg &pool,
+                             const int32_t *block_table, const int32_t *seq_lens, void *workspace,
+                             size_t workspace_bytes, qdec_bf16 *out, int32_t *err_flag,
+                             void *stream) {
+    qdec_status st = check_shape(shape);
+    if (st != QDEC_OK) return st;
+    if ((st = check_pool(shape, pool)) != QDEC_OK) return st;
+    if (!q_rot || !block_table || !seq_lens || !out) return QDEC_ERR_INVALID_ARG;
+    if (!aligned16(q_rot) || !aligned16(out)) return QDEC_ERR_INVALID_ARG;
+    if ((st = check_workspace(shape, workspace, workspace_bytes)) != QDEC_OK) return st;
+    Params p{};
+    fill_common(p, shape, true, pool.fp8);
+    p.q_rot_in = q_rot;
+    p.seq_lens = seq_lens;
+    p.block_table = block_table;
+    bind_pool(p, pool);
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.err = err_flag;
+    bind_workspace(p, shape, workspace);
+    CUtensorMap map;
+    if ((st = encode_map(&map, shape, pool)) != QDEC_OK) return st;
+    return cuda_status(qdec::launch_attention(p, map, qdec::kAttnDecode, pool.fp8,
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -597,6 +624,23 @@ qdec_status qdec_attn_split_fp8(const qdec_shape *shape, const float *q_rot,
                                 int32_t *err_flag, void *stream) {
     return attn_split_impl(shape, q_rot, PoolArg{kv_pool_fp8, kv_scale, true}, block_table,
                            seq_lens, workspace, workspace_bytes, out, err_flag, stream);
+}
+
+qdec_status qdec_attn_decode(const qdec_shape *shape, const float *q_rot,
+                             const qdec_bf16 *kv_pool, const int32_t *block_table,
+                             const int32_t *seq_lens, void *workspace, size_t workspace_bytes,
+                             qdec_bf16 *out, int32_t *err_flag, void *stream) {
+    return attn_decode_impl(shape, q_rot, PoolArg{kv_pool, nullptr, false}, block_table,
+                            seq_lens, workspace, workspace_bytes, out, err_flag, stream);
+}
+
+qdec_status qdec_attn_decode_fp8(const qdec_shape *shape, const float *q_rot,
+                                 const uint8_t *kv_pool_fp8, const float *kv_scale,
+                                 const int32_t *block_table, const int32_t *seq_lens,
+                                 void *workspace, size_t workspace_bytes, qdec_bf16 *out,
+                                 int32_t *err_flag, void *stream) {
+    return attn_decode_impl(shape, q_rot, PoolArg{kv_pool_fp8, kv_scale, true}, block_table,
+                            seq_lens, workspace, workspace_bytes, out, err_flag, stream);
 }
 
 qdec_status qdec_attn_merge(const qdec_shape *shape, const int32_t *seq_lens,

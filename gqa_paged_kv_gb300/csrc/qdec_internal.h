@@ -106,7 +106,15 @@ int max_active_clusters(int cluster, size_t smem, bool fp8);
 
 cudaError_t launch_rope_table(const Params &p, cudaStream_t s);
 cudaError_t launch_append_rope(const Params &p, bool fp8, cudaStream_t s);
-cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, bool fused, bool fp8,
+// What one attention launch does around step 4:
+//   kAttnSplit  q_rot in; pieces of split segments left in the workspace for
+//               the merge kernel (flat layout only)
+//   kAttnFused  steps 1-4: new-token rows normed, rotated and appended in the
+//               kernel; the last piece of a split segment merges it
+//   kAttnDecode q_rot in (the slot already appended); the last piece merges
+enum AttnMode : int { kAttnSplit = 0, kAttnFused = 1, kAttnDecode = 2 };
+
+cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, AttnMode mode, bool fp8,
                              cudaStream_t s);
 cudaError_t launch_merge(const Params &p, cudaStream_t s);
 

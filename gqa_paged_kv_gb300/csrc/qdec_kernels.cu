@@ -1221,10 +1221,10 @@ __device__ __forceinline__ void store_out(const Params &p, int b, int g, const P
         pack_bf16(__float2bfloat16_rn(r.num.z * inv), __float2bfloat16_rn(r.num.w * inv)));
 }
 
-// Write this piece's (o, lse) as workspace partial `pid`; in the fused
-// kernel count it against segment sigma's np partials, and if it is the
-// last to arrive merge all of them (ids pid0 .. pid0+np-1) into out.
-template <bool kFused>
+// Write this piece's (o, lse) as workspace partial `pid`; with kMerge count
+// it against segment sigma's np partials, and if it is the last to arrive
+// merge all of them (ids pid0 .. pid0+np-1) into out.
+template <bool kMerge>
 __device__ void store_partial(const Params &p, volatile int *misc, int64_t pid, int sigma,
                               int64_t pid0, int np, int b, int g, const PieceResult &r) {
     const int tid = threadIdx.x, h = tid >> 5, d0 = (tid & 31) * 4;
@@ -1234,7 +1234,7 @@ __device__ void store_partial(const Params &p, volatile int *misc, int64_t pid, 
     *reinterpret_cast<float4 *>(p.ws_o + (pid * kGroup + h) * kHeadDim + d0) =
         make_float4(r.num.x * inv, r.num.y * inv, r.num.z * inv, r.num.w * inv);
     if ((tid & 31) == 0) p.ws_lse[pid * kGroup + h] = r.den > 0.f ? r.M + log2f(r.den) : kNegInf;
-    if (!kFused) return;
+    if (!kMerge) return;
     // release the partial (all 128 threads' stores, ordered by the barrier),
     // count it; the last piece in acquires all of them
     consumer_sync();
@@ -1251,9 +1251,11 @@ __device__ void store_partial(const Params &p, volatile int *misc, int64_t pid, 
 
 
 // ------------------------------------------------------ attention kernel --
-template <bool kFused, bool kCluster, bool kFp8>
+template <int kMode, bool kCluster, bool kFp8>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm(kCluster, kFp8))
     attention_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ Params p) {
+    constexpr bool kFused = kMode == kAttnFused;      // steps 1-3 in the kernel
+    constexpr bool kMerge = kMode != kAttnSplit;      // the last piece merges
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1338,7 +1340,9 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kCluster, kFp8))
     if (warp == kConsumerWarps) {
         // ------------------------------------------------ TMA producer --
         // 32 tiles at a time: every lane looks up one tile's page, lane 0
-        // issues the copies in order as ring slots come free.
+        // issues the copies in order as ring slots come free.  In decode
+        // mode the previous kernel may have written the pages' new slots.
+        if (kMode == kAttnDecode && p.pdl) grid_dependency_wait();
         const long long ntiles = kCluster ? pg_hi - pg_lo : hi - lo;
         uint32_t i = 0;
         bool stop = false;
@@ -1433,7 +1437,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kCluster, kFp8))
             if (np == 1)
                 store_out(p, b, g, r);
             else
-                store_partial<kFused>(p, misc, sigma + static_cast<int64_t>(blockIdx.x), sigma,
+                store_partial<kMerge>(p, misc, sigma + static_cast<int64_t>(blockIdx.x), sigma,
                                       sigma + static_cast<int64_t>(j0), np, b, g, r);
             consumer_sync();  // the shared scratch is reused by the next piece
             walk_next(w, pre, p.Hkv, cnt);
@@ -1499,7 +1503,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kCluster, kFp8))
                 store_out(p, cb, cg, m);
             } else {
                 const int sigma = cb * p.Hkv + cg;
-                store_partial<kFused>(p, misc, cid, sigma, static_cast<int64_t>(sigma) * K, K, cb,
+                store_partial<kMerge>(p, misc, cid, sigma, static_cast<int64_t>(sigma) * K, K, cb,
                                       cg, m);
             }
         }
@@ -1570,25 +1574,25 @@ __global__ void __launch_bounds__(128) merge_kernel(const __grid_constant__ Para
 // occupancy query) that needs less leaves it as it is, so a later launch
 // that needs more than a smaller request in between still finds it set.
 std::mutex g_smem_mu;
-size_t g_smem_attr[8][64];
+size_t g_smem_attr[12][64];
 
-template <bool kFused, bool kCluster, bool kFp8>
+template <int kMode, bool kCluster, bool kFp8>
 cudaError_t allow_smem(int dev, size_t smem) {
     std::lock_guard<std::mutex> lock(g_smem_mu);
-    size_t &attr = g_smem_attr[(kFp8 ? 4 : 0) + (kFused ? 2 : 0) + (kCluster ? 1 : 0)][dev];
+    size_t &attr = g_smem_attr[(kFp8 ? 6 : 0) + 2 * kMode + (kCluster ? 1 : 0)][dev];
     if (attr >= smem) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(attention_kernel<kFused, kCluster, kFp8>,
+    const cudaError_t e = cudaFuncSetAttribute(attention_kernel<kMode, kCluster, kFp8>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
     if (e == cudaSuccess) attr = smem;
     return e;
 }
 
-template <bool kFused, bool kCluster, bool kFp8>
+template <int kMode, bool kCluster, bool kFp8>
 cudaError_t launch_one(const Params &p, const CUtensorMap &kv_map, size_t smem, int dev,
                        cudaStream_t s) {
-    auto kern = attention_kernel<kFused, kCluster, kFp8>;
-    const cudaError_t e = allow_smem<kFused, kCluster, kFp8>(dev, smem);
+    auto kern = attention_kernel<kMode, kCluster, kFp8>;
+    const cudaError_t e = allow_smem<kMode, kCluster, kFp8>(dev, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid);
@@ -1640,8 +1644,8 @@ static int current_device() {
 
 template <bool kFp8>
 static int max_active_clusters_of(int cluster, size_t smem) {
-    auto kern = attention_kernel<true, true, kFp8>;
-    if (allow_smem<true, true, kFp8>(current_device(), smem) != cudaSuccess) return 0;
+    auto kern = attention_kernel<kAttnFused, true, kFp8>;
+    if (allow_smem<kAttnFused, true, kFp8>(current_device(), smem) != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cluster * 64);
     cfg.blockDim = dim3(kThreads);
@@ -1665,19 +1669,29 @@ int max_active_clusters(int cluster, size_t smem, bool fp8) {
 
 // The split kernel of the three-call path always runs the flat layout (its
 // merge kernel reads that layout), so it has no cluster variant.
-cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, bool fused, bool fp8,
+template <bool kFp8>
+cudaError_t launch_mode(const Params &p, const CUtensorMap &kv_map, AttnMode mode, size_t smem,
+                        int dev, cudaStream_t s) {
+    switch (mode) {
+    case kAttnSplit:
+        if (p.cluster) return cudaErrorInvalidValue;
+        return launch_one<kAttnSplit, false, kFp8>(p, kv_map, smem, dev, s);
+    case kAttnFused:
+        return p.cluster ? launch_one<kAttnFused, true, kFp8>(p, kv_map, smem, dev, s)
+                         : launch_one<kAttnFused, false, kFp8>(p, kv_map, smem, dev, s);
+    case kAttnDecode:
+        return p.cluster ? launch_one<kAttnDecode, true, kFp8>(p, kv_map, smem, dev, s)
+                         : launch_one<kAttnDecode, false, kFp8>(p, kv_map, smem, dev, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, AttnMode mode, bool fp8,
                              cudaStream_t s) {
     const size_t smem = attention_smem_bytes(p.B, p.stages, p.cluster, fp8);
     const int dev = current_device();
-    if (!fused && p.cluster) return cudaErrorInvalidValue;
-    if (fp8) {
-        if (!fused) return launch_one<false, false, true>(p, kv_map, smem, dev, s);
-        return p.cluster ? launch_one<true, true, true>(p, kv_map, smem, dev, s)
-                         : launch_one<true, false, true>(p, kv_map, smem, dev, s);
-    }
-    if (!fused) return launch_one<false, false, false>(p, kv_map, smem, dev, s);
-    return p.cluster ? launch_one<true, true, false>(p, kv_map, smem, dev, s)
-                     : launch_one<true, false, false>(p, kv_map, smem, dev, s);
+    return fp8 ? launch_mode<true>(p, kv_map, mode, smem, dev, s)
+               : launch_mode<false>(p, kv_map, mode, smem, dev, s);
 }
 
 cudaError_t launch_rope_table(const Params &p, cudaStream_t s) {

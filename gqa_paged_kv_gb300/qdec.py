@@ -35,8 +35,8 @@ QDEC_LAUNCH_TEST_WITHHOLD_TILE = 1 << 30
 # Every symbol include/qdec.h declares.
 EXPORTS = ("qdec_workspace_bytes", "qdec_workspace_init", "qdec_rope_table_bytes",
            "qdec_rope_table", "qdec_append_rope", "qdec_attn_split", "qdec_attn_merge",
-           "qdec_step", "qdec_qkv_append_rope", "qdec_qkv_pack_weights", "qdec_append_rope_fp8",
-           "qdec_attn_split_fp8",
+           "qdec_attn_decode", "qdec_step", "qdec_qkv_append_rope", "qdec_qkv_pack_weights",
+           "qdec_append_rope_fp8", "qdec_attn_split_fp8", "qdec_attn_decode_fp8",
            "qdec_step_fp8",
            "qdec_step_static_scratch", "qdec_check_error", "qdec_status_string", "qdec_version")
 
@@ -104,6 +104,8 @@ def _load():
     lib.qdec_attn_split.restype = st
     lib.qdec_attn_merge.argtypes = [sp, vp, vp, sz, vp, vp, vp]
     lib.qdec_attn_merge.restype = st
+    lib.qdec_attn_decode.argtypes = [sp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+    lib.qdec_attn_decode.restype = st
     lib.qdec_step.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                               vp, vp, vp]
     lib.qdec_step.restype = st
@@ -117,6 +119,8 @@ def _load():
     lib.qdec_append_rope_fp8.restype = st
     lib.qdec_attn_split_fp8.argtypes = [sp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     lib.qdec_attn_split_fp8.restype = st
+    lib.qdec_attn_decode_fp8.argtypes = [sp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+    lib.qdec_attn_decode_fp8.restype = st
     lib.qdec_step_fp8.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp,
                                   vp, sz, vp, vp, vp]
     lib.qdec_step_fp8.restype = st
@@ -205,6 +209,14 @@ def qdec_attn_split(shape: Shape, q_rot, kv_pool, block_table, seq_lens, workspa
         _ptr(err_flag), _stream(stream)), "qdec_attn_split")
 
 
+def qdec_attn_decode(shape: Shape, q_rot, kv_pool, block_table, seq_lens, workspace, out,
+                     err_flag=None, stream=None):
+    _raise(_lib.qdec_attn_decode(
+        ctypes.byref(shape.c()), _ptr(q_rot), _ptr(kv_pool), _ptr(block_table), _ptr(seq_lens),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
+        _ptr(err_flag), _stream(stream)), "qdec_attn_decode")
+
+
 def qdec_attn_merge(shape: Shape, seq_lens, workspace, out, err_flag=None, stream=None):
     _raise(_lib.qdec_attn_merge(
         ctypes.byref(shape.c()), _ptr(seq_lens), _ptr(workspace),
@@ -265,6 +277,15 @@ def qdec_attn_split_fp8(shape: Shape, q_rot, kv_pool_fp8, kv_scale, block_table,
         ctypes.byref(shape.c()), _ptr(q_rot), pool, scale, _ptr(block_table), _ptr(seq_lens),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
         _ptr(err_flag), _stream(stream)), "qdec_attn_split_fp8")
+
+
+def qdec_attn_decode_fp8(shape: Shape, q_rot, kv_pool_fp8, kv_scale, block_table, seq_lens,
+                         workspace, out, err_flag=None, stream=None):
+    pool, scale = _fp8_pool(kv_pool_fp8, kv_scale)
+    _raise(_lib.qdec_attn_decode_fp8(
+        ctypes.byref(shape.c()), _ptr(q_rot), pool, scale, _ptr(block_table), _ptr(seq_lens),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
+        _ptr(err_flag), _stream(stream)), "qdec_attn_decode_fp8")
 
 
 def qdec_step_fp8(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, seq_lens, block_table,

@@ -180,6 +180,22 @@ qdec_status qdec_attn_merge(const qdec_shape *shape, const int32_t *seq_lens,
                             const void *workspace, size_t workspace_bytes,
                             qdec_bf16 *out, int32_t *err_flag, void *stream);
 
+/* Step 4 whole in ONE launch: split-KV attention of q_rot (from
+ * qdec_append_rope or qdec_qkv_append_rope, whose append this launch must
+ * follow on the stream) over the pool, and the log-sum-exp merge of every
+ * split (sequence, KV head) by the last of its pieces to finish, bf16 result
+ * into out [B][Hq][D].  The work plan (cluster or flat layout) is
+ * qdec_step's; the workspace counters must be zero on entry
+ * (qdec_workspace_init once; every launch leaves them zero).  With
+ * QDEC_LAUNCH_OVERLAP_PREVIOUS the launch may start while the previous kernel
+ * on the stream finishes; it reads q_rot, the pool and writes out only after
+ * that kernel has completed.  Errors as qdec_attn_split. */
+qdec_status qdec_attn_decode(const qdec_shape *shape, const float *q_rot,
+                             const qdec_bf16 *kv_pool, const int32_t *block_table,
+                             const int32_t *seq_lens, void *workspace,
+                             size_t workspace_bytes, qdec_bf16 *out,
+                             int32_t *err_flag, void *stream);
+
 /* The whole layer-step (steps 1-4) in ONE kernel launch: every CTA norms and
  * rotates the four query rows of the (sequence, KV head) it works on, the CTA
  * that holds the last page of a (sequence, KV head) also norms, rotates and
@@ -273,6 +289,13 @@ qdec_status qdec_attn_split_fp8(const qdec_shape *shape, const float *q_rot,
                                 const int32_t *block_table, const int32_t *seq_lens,
                                 void *workspace, size_t workspace_bytes, qdec_bf16 *out,
                                 int32_t *err_flag, void *stream);
+
+/* qdec_attn_decode over an FP8 pool. */
+qdec_status qdec_attn_decode_fp8(const qdec_shape *shape, const float *q_rot,
+                                 const uint8_t *kv_pool_fp8, const float *kv_scale,
+                                 const int32_t *block_table, const int32_t *seq_lens,
+                                 void *workspace, size_t workspace_bytes, qdec_bf16 *out,
+                                 int32_t *err_flag, void *stream);
 
 /* qdec_step over an FP8 pool: one launch for steps 1-4, the new key and
  * value quantized into their slot as above.  Same launch flags, workspace

@@ -91,6 +91,24 @@ class Runner:
                               self.ws, self.out[layer], self.err)
         q.qdec_attn_merge(self.shape, w.seq_lens, self.ws, self.out[layer], self.err)
 
+    def two_calls(self, layer: int):
+        """Steps 1-3 (qdec_append_rope) and then step 4 in one launch
+        (qdec_attn_decode)."""
+        q, w = qdec(), self.w
+        if w.kv == "fp8":
+            q.qdec_append_rope_fp8(self.shape, w.q(layer), w.k(layer), w.v(layer), w.w_q[layer],
+                                   w.w_k[layer], w.positions, w.seq_lens, w.block_table,
+                                   w.pool8(layer), w.scale(layer), self.q_rot, self.err,
+                                   rope_table=self.rope)
+            q.qdec_attn_decode_fp8(self.shape, self.q_rot, w.pool8(layer), w.scale(layer),
+                                   w.block_table, w.seq_lens, self.ws, self.out[layer], self.err)
+        else:
+            q.qdec_append_rope(self.shape, w.q(layer), w.k(layer), w.v(layer), w.w_q[layer],
+                               w.w_k[layer], w.positions, w.seq_lens, w.block_table,
+                               w.pool(layer), self.q_rot, self.err, rope_table=self.rope)
+            q.qdec_attn_decode(self.shape, self.q_rot, w.pool(layer), w.block_table, w.seq_lens,
+                               self.ws, self.out[layer], self.err)
+
     def check_flags(self):
         st, flags = qdec().qdec_check_error(self.err)
         assert st == 0 and flags == 0, f"device error flags {flags:#x} (status {st})"

@@ -60,6 +60,34 @@ def test_unfused_three_calls_fp8(lens, num_ctas):
     parity.assert_slots_fp8(w, 0, range(len(lens)), ref)
 
 
+@pytest.mark.parametrize("lens,num_ctas", SMALL, ids=lambda x: str(x))
+def test_append_then_decode_fp8(lens, num_ctas):
+    """qdec_append_rope_fp8 followed by the one-launch qdec_attn_decode_fp8."""
+    w = _small(lens, seed=44)
+    ref = parity.run_oracle(wl.oracle_inputs(w, 0))
+    r = parity.Runner(w, num_ctas=num_ctas)
+    r.two_calls(0)
+    r.check_flags()
+    parity.assert_out_close(r.out[0], ref["out"])
+    parity.assert_slots_fp8(w, 0, range(len(lens)), ref)
+    torch.cuda.synchronize()
+    n = w.spec.batch * w.spec.num_kv_heads
+    assert torch.count_nonzero(r.ws[:4 * n].view(torch.int32)).item() == 0
+
+
+def test_decode_overlapped_layers_match_serial_fp8():
+    spec = wl.custom(5, [17, 1, 300, 64, 1000], pool_pages=120, layers=4, seed=45)
+    w = wl.build(spec, "cuda", poison=True, kv="fp8")
+    outs = []
+    for overlap in (False, True):
+        r = parity.Runner(w, overlap=overlap)
+        for layer in range(4):
+            r.two_calls(layer)
+        r.check_flags()
+        outs.append(r.out.clone())
+    assert torch.equal(outs[0], outs[1])
+
+
 def test_saturating_page_fp8():
     """Scales far too small for the new rows: the appended codes saturate at
     +-448 (0x7E / 0xFE) exactly where the oracle's do."""

@@ -60,6 +60,50 @@ def test_unfused_three_calls(lens, num_ctas, rope):
     parity.assert_slots(w, 0, range(len(lens)), ref)
 
 
+@pytest.mark.parametrize("lens,num_ctas", SMALL, ids=lambda x: str(x))
+def test_append_then_decode(lens, num_ctas):
+    """qdec_append_rope followed by the one-launch qdec_attn_decode (the
+    fused step's work plan and in-kernel merge, q_rot read from memory)."""
+    w = _small(lens, seed=14)
+    ref = parity.run_oracle(wl.oracle_inputs(w, 0))
+    r = parity.Runner(w, num_ctas=num_ctas)
+    r.two_calls(0)
+    r.check_flags()
+    parity.assert_out_close(r.out[0], ref["out"])
+    parity.assert_slots(w, 0, range(len(lens)), ref)
+    torch.cuda.synchronize()
+    n = w.spec.batch * w.spec.num_kv_heads
+    assert torch.count_nonzero(r.ws[:4 * n].view(torch.int32)).item() == 0
+
+
+def test_decode_equals_split_and_merge_closely():
+    w = _small([17, 1, 300, 64, 16, 2, 999, 4096], seed=15)
+    r = parity.Runner(w)
+    r.unfused(0)
+    a = r.out[0].float().clone()
+    r.two_calls(0)
+    r.check_flags()
+    # the same q_rot and tile math; the pieces and merge order may differ
+    assert torch.allclose(a, r.out[0].float(), rtol=2 ** -7, atol=1e-3)
+
+
+@pytest.mark.parametrize("num_ctas", [0, 5])
+def test_decode_overlapped_layers_match_serial(num_ctas):
+    """qdec_attn_decode with the overlap flag after each append: no bit changes."""
+    for shared in (False, True):
+        spec = wl.custom(5, [17, 1, 300, 64, 1000], pool_pages=120, layers=4, seed=21,
+                         shared_pool=shared)
+        w = wl.build(spec, "cuda", poison=True)
+        outs = []
+        for overlap in (False, True):
+            r = parity.Runner(w, num_ctas=num_ctas, overlap=overlap)
+            for layer in range(4):
+                r.two_calls(layer)
+            r.check_flags()
+            outs.append(r.out.clone())
+        assert torch.equal(outs[0], outs[1])
+
+
 def test_fused_equals_unfused_closely():
     w = _small([17, 1, 300, 64, 16, 2, 999], seed=13)
     r1 = parity.Runner(w)

@@ -6,8 +6,8 @@ so each element carries the fp32 dot-product error bound
 and the rotation carry into q_rot and k_rot as r * max|w| * (E_i + E_(i+64)).
 Checked: q_rot within the fp32 q_rot tolerance plus that bound; the appended
 k and v within one bf16 ulp of the oracle's unrounded values plus that bound;
-the rest of the pool untouched; the whole block (projection, split attention,
-merge) within the out tolerance.  Batches of 1 to 70 rows (two 64-row blocks), hidden sizes 64 to
+the rest of the pool untouched; the whole block (projection, then
+qdec_attn_decode, or split attention and merge) within the out tolerance.  Batches of 1 to 70 rows (two 64-row blocks), hidden sizes 64 to
 2560, NaN-poisoned pools.
 """
 import math
@@ -36,7 +36,7 @@ def _problem(lens, hidden, seed, hkv=8):
     return w, x, wqkv
 
 
-def _run(w, x, wqkv):
+def _run(w, x, wqkv, attn="decode"):
     q = parity.qdec()
     s = w.spec
     shape = q.shape_for(w)
@@ -50,8 +50,11 @@ def _run(w, x, wqkv):
                            w.block_table, w.pool(0), q_rot, rope, err)
     ws = q.alloc_workspace(shape)
     out = torch.empty((s.batch, s.num_q_heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
-    q.qdec_attn_split(shape, q_rot, w.pool(0), w.block_table, w.seq_lens, ws, out, err)
-    q.qdec_attn_merge(shape, w.seq_lens, ws, out, err)
+    if attn == "decode":
+        q.qdec_attn_decode(shape, q_rot, w.pool(0), w.block_table, w.seq_lens, ws, out, err)
+    else:
+        q.qdec_attn_split(shape, q_rot, w.pool(0), w.block_table, w.seq_lens, ws, out, err)
+        q.qdec_attn_merge(shape, w.seq_lens, ws, out, err)
     return q_rot, out, err
 
 
@@ -136,6 +139,15 @@ def test_qkv_projection_matches_oracle(lens, hidden):
     same = (after == before) | (np.isnan(oracle.bf16_bits_to_f64(after)) &
                                 np.isnan(oracle.bf16_bits_to_f64(before)))
     assert same[~mask].all(), "the projection wrote outside the append slots"
+
+
+def test_qkv_then_split_and_merge():
+    w, x, wqkv = _problem([300, 17, 1000, 64], 512, seed=64)
+    res = _oracle(w, x, wqkv)
+    _, out, err = _run(w, x, wqkv, attn="split")
+    st, flags = parity.qdec().qdec_check_error(err)
+    assert st == 0 and flags == 0, (st, flags)
+    parity.assert_out_close(out, res["out"])
 
 
 def test_qkv_group_of_two_kv_heads():

@@ -80,6 +80,14 @@ def test_entry_points_reject_null_and_misaligned_arguments(q):
     assert step(ws=z) == q.QDEC_ERR_WORKSPACE
     assert lib.qdec_attn_split(sh, ok, ok, ok, ok, z, 1 << 30, ok, z, z) == q.QDEC_ERR_WORKSPACE
     assert lib.qdec_attn_merge(sh, z, ok, 1 << 30, ok, z, z) == q.QDEC_ERR_INVALID_ARG
+    # decode: workspace missing, q_rot missing or misaligned, out missing
+    assert lib.qdec_attn_decode(sh, ok, ok, ok, ok, z, 1 << 30, ok, z, z) == q.QDEC_ERR_WORKSPACE
+    assert lib.qdec_attn_decode(sh, z, ok, ok, ok, ok, 1 << 30, ok, z, z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_attn_decode(sh, bad, ok, ok, ok, ok, 1 << 30, ok, z,
+                                z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_attn_decode(sh, ok, ok, ok, ok, ok, 1 << 30, z, z, z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_attn_decode(None, ok, ok, ok, ok, ok, 1 << 30, ok, z,
+                                z) == q.QDEC_ERR_INVALID_ARG
     # append without a q_rot output
     assert lib.qdec_append_rope(sh, ok, S, ok, S, ok, S, ok, ok, ok, ok, ok, z, ok, z, z,
                                 z) == q.QDEC_ERR_INVALID_ARG
@@ -118,6 +126,10 @@ def test_fp8_entry_points_reject_bad_arguments(q):
     assert lib.qdec_attn_split_fp8(odd, ok, ok, ok, ok, ok, ok, 1 << 30, ok, z,
                                    z) == q.QDEC_ERR_UNSUPPORTED
     assert lib.qdec_append_rope_fp8(sh, ok, S, ok, S, ok, S, ok, ok, ok, ok, ok, z, ok, z, ok, z,
+                                    z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_attn_decode_fp8(odd, ok, ok, ok, ok, ok, ok, 1 << 30, ok, z,
+                                    z) == q.QDEC_ERR_UNSUPPORTED
+    assert lib.qdec_attn_decode_fp8(sh, ok, ok, z, ok, ok, ok, 1 << 30, ok, z,
                                     z) == q.QDEC_ERR_INVALID_ARG
     # one workspace size serves both pool types
     assert q.qdec_workspace_bytes(_shape(q, num_q_heads=12, num_kv_heads=3)) > 0
