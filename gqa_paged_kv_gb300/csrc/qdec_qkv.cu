@@ -65,6 +65,10 @@ __device__ __forceinline__ void flag_error(int32_t *err, int bits) {
     if (err) atomicOr(err, bits);
 }
 
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {  // exact: bf16 -> fp32
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
     return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
            (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
@@ -98,6 +102,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         return;  // uniform over the cluster: every CTA sees the same parameters
     }
 
+    if (p.pdl && tid == 0) launch_dependents();  // the next kernel waits for our completion
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(full0 + 8 * s, 1);
@@ -114,20 +119,34 @@ __global__ void __launch_bounds__(kThreads, 2)
             // this CTA's packed blocks: (head * 4 + rank) * (hidden / 64) onwards
             const __nv_bfloat16 *wsrc =
                 p.w_packed + static_cast<int64_t>(head * kQkvCluster + rank) * p.hidden * 32;
+            // With an overlapped launch the weight (which no kernel writes) of
+            // the first stages goes out before the dependency wait; the hidden
+            // states only after it.
+            const int pre = p.pdl ? min(NS, nchunks) : 0;
+            for (int c = 0; c < pre; ++c) {
+                const uint32_t full = full0 + 8 * c;
+                mbar_arrive_expect_tx(full, stage_bytes);
+                bulk_load(smem_u32(sm + c * stage_bytes),
+                          wsrc + static_cast<int64_t>(c) * NB * 32 * kQkvChunk, NB * 2 * kQkvWBox,
+                          full);
+            }
+            if (p.pdl) grid_dependency_wait();
             for (int c = 0; c < nchunks; ++c) {
                 const int s = c % NS;
-                if (c >= NS &&
-                    !mbar_wait_bounded(empty0 + 8 * s, ((c / NS) - 1) & 1, abort_flag,
-                                       p.wait_cycles)) {
-                    *abort_flag = 1;
-                    flag_error(p.err, QDEC_FLAG_TIMEOUT);
-                    break;
-                }
                 const uint32_t full = full0 + 8 * s;
                 const uint32_t dst = smem_u32(sm + s * stage_bytes);
-                mbar_arrive_expect_tx(full, stage_bytes);
-                bulk_load(dst, wsrc + static_cast<int64_t>(c) * NB * 32 * kQkvChunk,
-                          NB * 2 * kQkvWBox, full);
+                if (c >= pre) {
+                    if (c >= NS &&
+                        !mbar_wait_bounded(empty0 + 8 * s, ((c / NS) - 1) & 1, abort_flag,
+                                           p.wait_cycles)) {
+                        *abort_flag = 1;
+                        flag_error(p.err, QDEC_FLAG_TIMEOUT);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full, stage_bytes);
+                    bulk_load(dst, wsrc + static_cast<int64_t>(c) * NB * 32 * kQkvChunk,
+                              NB * 2 * kQkvWBox, full);
+                }
                 for (int j = 0; j < NB; ++j)
                     tma_load_2d(dst + 2 * NB * kQkvWBox + j * p.qkv_rows * kQkvChunk * 2, &x_map,
                                 (c * NB + j) * kQkvChunk, row0, full);
@@ -148,6 +167,48 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int mi = lane >> 3, r8 = lane & 7;
         const int arow = 16 * warp + (mi & 1) * 8 + r8;  // x row this lane addresses
         const int brow = (mi >> 1) * 8 + r8;             // W row within a 16-row box
+        if (p.pdl) grid_dependency_wait();  // the tables, q_rot and the pool of earlier kernels
+
+        // the epilogue's lookups for rows g and g + 8, made while the weight
+        // streams: the append slot (-1: skip the row) and the norm weights
+        const int Hq = p.Hq, Hkv = p.Hkv;
+        const int kind = head < Hq ? 0 : (head < Hq + Hkv ? 1 : 2);  // q, k or v head
+        const int kvh = kind == 1 ? head - Hq : head - Hq - Hkv;
+        int64_t slot[2] = {-1, -1};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int b = row0 + 16 * warp + g + 8 * half;
+            if (!live || b >= p.B) continue;
+            const int L = p.seq_lens[b];
+            if (L < 1 || L > p.max_blocks * kPageSize) {
+                if (t == 0 && head == 0 && rank == 0) flag_error(p.err, QDEC_FLAG_BAD_SEQLEN);
+                continue;
+            }
+            if (kind == 0) {
+                slot[half] = 0;
+                continue;
+            }
+            const int page =
+                p.block_table[static_cast<int64_t>(b) * p.max_blocks + (L - 1) / kPageSize];
+            if (page < 0 || page >= p.num_pages) {
+                if (t == 0 && rank == 0 && kind == 1 && kvh == 0)
+                    flag_error(p.err, QDEC_FLAG_BAD_PAGE);
+                continue;
+            }
+            slot[half] =
+                ((static_cast<int64_t>(page) * 2 * Hkv + kvh) * kPageSize + (L - 1) % kPageSize) *
+                kHeadDim;
+        }
+        uint32_t wn2[2][2];  // norm weight pairs (d, d+1), (d+64, d+65) of n-tiles 0, 1
+        {
+            const __nv_bfloat16 *wn = kind == 0 ? p.w_q : p.w_k;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int d = 16 * rank + 8 * nt + 2 * t;
+                wn2[nt][0] = kind == 2 ? 0u : *reinterpret_cast<const uint32_t *>(wn + d);
+                wn2[nt][1] = kind == 2 ? 0u : *reinterpret_cast<const uint32_t *>(wn + d + 64);
+            }
+        }
         for (int c = 0; c < nchunks; ++c) {
             const int s = c % NS;
             const bool ok = mbar_wait_bounded(full0 + 8 * s, (c / NS) & 1, abort_flag,
@@ -205,33 +266,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         cluster_sync_all();  // nobody leaves while a peer may still read
 
-        const int Hq = p.Hq, Hkv = p.Hkv;
-        const int kind = head < Hq ? 0 : (head < Hq + Hkv ? 1 : 2);  // q, k or v head
-        const int kvh = kind == 1 ? head - Hq : head - Hq - Hkv;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const int b = row0 + 16 * warp + g + 8 * half;
-            if (!live || *abort_flag || b >= p.B) continue;
+            if (*abort_flag || slot[half] < 0) continue;
             const float tot = half ? totB : totA;
-            const int L = p.seq_lens[b];
-            if (L < 1 || L > p.max_blocks * kPageSize) {
-                if (t == 0 && head == 0 && rank == 0) flag_error(p.err, QDEC_FLAG_BAD_SEQLEN);
-                continue;
-            }
-            int64_t kslot = -1;
-            if (kind != 0) {
-                const int page = p.block_table[static_cast<int64_t>(b) * p.max_blocks +
-                                               (L - 1) / kPageSize];
-                if (page < 0 || page >= p.num_pages) {
-                    if (t == 0 && rank == 0 && kind == 1 && kvh == 0)
-                        flag_error(p.err, QDEC_FLAG_BAD_PAGE);
-                    continue;
-                }
-                kslot = ((static_cast<int64_t>(page) * 2 * Hkv + kvh) * kPageSize +
-                         (L - 1) % kPageSize) * kHeadDim;
-            }
+            const int64_t kslot = slot[half];
             const float rn = rsqrtf(tot * (1.0f / kHeadDim) + p.eps);
-            const __nv_bfloat16 *wn = kind == 0 ? p.w_q : p.w_k;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int d = 16 * rank + 8 * nt + 2 * t;  // dims d, d+1 and d+64, d+65
@@ -244,10 +285,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                     *reinterpret_cast<uint32_t *>(vdst + d + 64) = pack2_bf16(x2a, x2b);
                     continue;
                 }
-                const float n1a = x1a * rn * __bfloat162float(wn[d]);
-                const float n1b = x1b * rn * __bfloat162float(wn[d + 1]);
-                const float n2a = x2a * rn * __bfloat162float(wn[d + 64]);
-                const float n2b = x2b * rn * __bfloat162float(wn[d + 65]);
+                const float2 w1 = bf16x2_to_float2(wn2[nt][0]), w2 = bf16x2_to_float2(wn2[nt][1]);
+                const float n1a = x1a * rn * w1.x, n1b = x1b * rn * w1.y;
+                const float n2a = x2a * rn * w2.x, n2b = x2b * rn * w2.y;
                 const RopeEntry ea = p.rope[static_cast<int64_t>(b) * kRotPairs + d];
                 const RopeEntry eb = p.rope[static_cast<int64_t>(b) * kRotPairs + d + 1];
                 const float y1a = n1a * ea.c_hi - n2a * ea.s_hi, y2a = n2a * ea.c_hi + n1a * ea.s_hi;
@@ -339,13 +379,19 @@ cudaError_t launch_qkv_append(const Params &p, const CUtensorMap &x_map, cudaStr
     cfg.dynamicSmemBytes =
         p.qkv_stages * qkv_stage_bytes(p.qkv_rows, p.qkv_boxes) + kQkvTailBytes + 1024;
     cfg.stream = s;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = kQkvCluster;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = kQkvCluster;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    int na = 1;
+    if (p.pdl) {
+        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, qkv_append_kernel, x_map, p);
 }
 

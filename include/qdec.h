@@ -92,7 +92,12 @@ typedef enum {
  * for it before reading q, k, v, positions, the norm weights, the rope table
  * or writing anything.  Set it only when the immediately preceding kernel
  * does not write seq_lens, block_table or kv_pool pages other than the
- * append slots of this step (e.g. the previous layer's qdec_step). */
+ * append slots of this step (e.g. the previous layer's qdec_step).
+ * qdec_attn_decode with the flag waits for the previous kernel before it
+ * reads anything but its launch parameters.  qdec_qkv_append_rope with the
+ * flag streams the first stages of its (packed) weight before that wait and
+ * waits before it reads x, the tables or the norm weights or writes anything,
+ * so the weight must not be written by the kernel before it. */
 
 /* Bits a kernel ORs into *err_flag. */
 #define QDEC_FLAG_BAD_PAGE   1   /* block-table entry outside [0, num_pages)   */

@@ -167,3 +167,43 @@ def test_qkv_bad_page_is_flagged():
     _, _, err = _run(w, x, wqkv)
     st, flags = q.qdec_check_error(err)
     assert st == q.QDEC_ERR_DEVICE_BOUNDS and flags & q.QDEC_FLAG_BAD_PAGE, (st, flags)
+
+
+@pytest.mark.parametrize("shared", [False, True], ids=["per_layer_pools", "shared_pool"])
+def test_qkv_block_overlapped_layers_match_serial(shared):
+    """Layers of (qdec_qkv_append_rope, qdec_attn_decode) launched as
+    programmatic dependents of each other change no bit of out or q_rot."""
+    q = parity.qdec()
+    lens, hidden, layers = [17, 1, 300, 64, 1000], 512, 4
+    spec = wl.custom(len(lens), lens, pool_pages=120, layers=layers, seed=65, shared_pool=shared)
+    w = wl.build(spec, "cuda", poison=True)
+    s = w.spec
+    gen = torch.Generator(device="cuda").manual_seed(66)
+    rows = (s.num_q_heads + 2 * s.num_kv_heads) * s.head_dim
+    xs = torch.randn((layers, s.batch, hidden), generator=gen, device="cuda").to(torch.bfloat16)
+    packed = torch.empty((layers, rows, hidden), dtype=torch.bfloat16, device="cuda")
+    for l in range(layers):
+        wl_ = (torch.randn((rows, hidden), generator=gen, device="cuda") /
+               math.sqrt(hidden)).to(torch.bfloat16)
+        q.qdec_qkv_pack_weights(q.shape_for(w), wl_, packed[l])
+    results = []
+    for overlap in (False, True):
+        shape = q.shape_for(w, launch_flags=q.QDEC_LAUNCH_OVERLAP_PREVIOUS if overlap else 0)
+        rope = q.alloc_rope_table(shape)
+        q.qdec_rope_table(shape, w.positions, rope)
+        ws = q.alloc_workspace(shape)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        q_rot = torch.empty((s.batch, s.num_q_heads, s.head_dim), dtype=torch.float32,
+                            device="cuda")
+        out = torch.empty((layers, s.batch, s.num_q_heads, s.head_dim), dtype=torch.bfloat16,
+                          device="cuda")
+        for l in range(layers):
+            q.qdec_qkv_append_rope(shape, xs[l], packed[l], w.w_q[l], w.w_k[l], w.positions,
+                                   w.seq_lens, w.block_table, w.pool(l), q_rot, rope, err)
+            q.qdec_attn_decode(shape, q_rot, w.pool(l), w.block_table, w.seq_lens, ws, out[l],
+                               err)
+        st, flags = q.qdec_check_error(err)
+        assert st == 0 and flags == 0, (st, flags)
+        results.append((out.clone(), q_rot.clone()))
+    assert torch.equal(results[0][0], results[1][0])
+    assert torch.equal(results[0][1], results[1][1])
