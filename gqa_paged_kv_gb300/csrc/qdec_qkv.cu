@@ -7,24 +7,31 @@
 // then the value heads), applied to every sequence's hidden state x [B][hidden].
 // Its epilogue keeps each head's 128 outputs unrounded (fp32) into the norm,
 // the rotation and the append: query heads go to q_rot (fp32, unscaled, the
-// input of qdec_attn_split), key heads are rounded once to bf16 after the
-// rotation and value heads once as they are, into slot seq_lens[b] - 1.
+// input of qdec_attn_decode / qdec_attn_split), key heads are rounded once to
+// bf16 after the rotation and value heads once as they are, into slot
+// seq_lens[b] - 1.
 //
-// Layout: a cluster of 4 CTAs per output head; CTA r of the cluster computes
-// head dims 16r .. 16r+15 and 64+16r .. 64+16r+15 (so every rotate-half pair
-// stays inside one CTA) for 64 batch rows, over the whole hidden dimension.
-// The weight is packed once (qdec_qkv_pack_weights) into the order the
-// projection reads it: for every (head, cluster rank) the 32 rows it owns, in
-// blocks of 64 hidden elements, each block 4 KiB contiguous with its
-// 128-byte rows already swizzled for conflict-free matrix loads; a CTA's
-// whole share is one contiguous run.  One producer warp streams stages of
-// 1, 2 or 4 such blocks (one bulk copy; more for smaller batches) and the
-// matching boxes of x (the batch rounded up to 16 rows, at most 64; rows past
-// B read as zero, TMA) into a ring of about 96 KiB; four consumer warps each
-// own 16 batch rows and run bf16 mma.sync (fp32 accumulate).  The
-// RMSNorm needs the sum of squares over all 128 dims: each CTA leaves its
-// share per row in shared memory and reads the peers' shares over
-// distributed shared memory between two cluster-barrier phases.
+// Layout: a cluster of 4 CTAs per output head splits the hidden dimension:
+// CTA r computes all 128 dims of the head for up to 64 batch rows over its
+// quarter of the 64-element blocks of hidden, so it streams a quarter of the
+// head's weight and of x.  The weight is packed once (qdec_qkv_pack_weights)
+// into the order the projection reads it: per (head, block of 64 hidden
+// elements) 16 KiB, four 4 KiB sub-blocks of 32 rows (sub-block i: dims
+// 16i .. 16i+15, then 64+16i .. 64+16i+15), each 128-byte row already
+// swizzled for conflict-free matrix loads; a CTA's share is one contiguous
+// run.  One producer warp streams stages of one 16 KiB block (one bulk copy)
+// and the matching box of x (the batch rounded up to 16 rows, at most 64; rows
+// past B read as zero, TMA) into a ring of about 96 KiB; the four consumer
+// warps split the stage's rows x 128 columns into 16-row tiles and column
+// groups (one tile and all 16 n-tiles at 64 rows, four column groups of one
+// tile at 16 rows) and run bf16 mma.sync with fp32 accumulators.  At the end
+// every CTA leaves its partial sums in shared memory and, after one cluster
+// barrier, pushes to CTA q (one bulk shared-to-shared copy each, counted on
+// q's transaction barrier) the rows q owns: rows q R/4 .. (q+1) R/4 - 1 of
+// the R.  The owner adds the four partials in rank order, so each row's 128
+// dims are complete in one CTA: the RMSNorm sum of squares, the rotation and
+// the writes need nothing from the peers.  The epilogue's lookups (append
+// slot, norm weights, rotation table) are made before the main loop.
 #include "qdec_internal.h"
 #include "qdec_ptx.cuh"
 #include "qdec.h"
@@ -39,17 +46,23 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kQkvCluster = 4;                              // CTAs per output head
-constexpr int kQkvRows = 4 * 16;                            // batch rows per CTA (4 warps x m16)
-constexpr int kQkvChunk = 64;                               // hidden elements per stage
+constexpr int kQkvRows = 4 * 16;                            // batch rows per CTA
+constexpr int kQkvChunk = 64;                               // hidden elements per block
 constexpr int kQkvMaxStages = 16;
-constexpr int kQkvWBox = 16 * kQkvChunk * 2;                // one 16-row W box, 2 KiB
+constexpr int kQkvSub = 32 * kQkvChunk * 2;                 // one 32-row sub-block, 4 KiB
+constexpr int kQkvBlock = kQkvCluster * kQkvSub;            // one head's block, 16 KiB
 constexpr int kQkvRingBytes = 96 * 1024;
-// after the ring: barriers full[16], empty[16], the abort flag, row sums
-constexpr int kQkvTailBytes = 2 * kQkvMaxStages * 8 + 16 + kQkvRows * 4;
-// a stage: [packed W blocks, 4 KiB each: rows 16r.. then rows 64+16r..][x
-// boxes], each piece starting on a 1024-byte boundary (rows % 16 == 0)
+constexpr int kQkvPartStride = kHeadDim + 8;                // floats per row of the partials
+constexpr int kQkvSliceMax = kQkvRows / kQkvCluster * kQkvPartStride * 4;  // rows one CTA owns
+constexpr int kQkvRecvOff = 36 * 1024;                      // receive area in the ring
+constexpr int kQkvRingUse = kQkvRecvOff + kQkvCluster * kQkvSliceMax;
+// after the ring: barriers full[16], empty[16], recv, the abort flag
+constexpr int kQkvTailBytes = 2 * kQkvMaxStages * 8 + 8 + 8;
+static_assert(kQkvRows * kQkvPartStride * 4 <= kQkvRecvOff, "partials end before the receive area");
+// a stage: [boxes packed blocks of 16 KiB][boxes x boxes of rows x 64], each
+// piece starting on a 1024-byte boundary (rows % 16 == 0)
 __host__ __device__ constexpr int qkv_stage_bytes(int rows, int boxes) {
-    return boxes * (2 * kQkvWBox + rows * kQkvChunk * 2);
+    return boxes * (kQkvBlock + rows * kQkvChunk * 2);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
@@ -59,6 +72,22 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// Bulk copy of `bytes` from this CTA's shared memory to the same-offset-mapped
+// address `dst` of a peer (shared::cluster), counted on the peer's barrier.
+__device__ __forceinline__ void bulk_push(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];" ::"r"(dst),
+        "r"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, int rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
 }
 
 __device__ __forceinline__ void flag_error(int32_t *err, int bits) {
@@ -88,16 +117,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int head = blockIdx.x / kQkvCluster, rank = blockIdx.x % kQkvCluster;
     const int row0 = blockIdx.y * kQkvRows;
     const int NB = p.qkv_boxes;
-    const int nchunks = p.hidden / (kQkvChunk * NB);
+    const int R = p.qkv_rows;
     const int NS = p.qkv_stages;
-    const int stage_bytes = qkv_stage_bytes(p.qkv_rows, NB);
+    const int stage_bytes = qkv_stage_bytes(R, NB);
+    // this CTA's 64-element blocks of hidden: [kb0, kb1), in stages of NB
+    const int nk = p.hidden / kQkvChunk;
+    const int kb0 = rank * nk / kQkvCluster, kb1 = (rank + 1) * nk / kQkvCluster;
+    const int nchunks = (kb1 - kb0) / max(NB, 1);
     uint8_t *tail = sm + NS * stage_bytes;
     const uint32_t full0 = smem_u32(tail);
     const uint32_t empty0 = full0 + kQkvMaxStages * 8;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tail + 2 * kQkvMaxStages * 8);
-    float *ss = reinterpret_cast<float *>(tail + 2 * kQkvMaxStages * 8 + 16);
-    if (NS < 1 || NS > kQkvMaxStages || p.qkv_rows < 16 || p.qkv_rows > kQkvRows ||
-        p.qkv_rows % 16 != 0 || NB < 1 || NB > 4 || p.hidden % (kQkvChunk * NB) != 0) {
+    const uint32_t recv_bar = empty0 + kQkvMaxStages * 8;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tail + 2 * kQkvMaxStages * 8 + 8);
+    if (NS < 1 || NS > kQkvMaxStages || R < 16 || R > kQkvRows || R % 16 != 0 || NB < 1 ||
+        NB > 2 || p.hidden % kQkvChunk != 0 || (kb1 - kb0) % NB != 0 ||
+        NS * stage_bytes < kQkvRingUse) {
         if (tid == 0) flag_error(p.err, QDEC_FLAG_BAD_INDEX);
         return;  // uniform over the cluster: every CTA sees the same parameters
     }
@@ -106,19 +140,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, kConsumerWarps);  // every warp takes every chunk
+            mbar_init(empty0 + 8 * s, kConsumerWarps);  // every warp takes every stage
         }
+        mbar_init(recv_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
 
+    // The partial sums [64 rows][128 + 8] fp32 overwrite the ring once every
+    // stage is consumed; CTA q owns rows q R/4 .. (q+1) R/4 - 1 (a contiguous
+    // slice of part) and receives the peers' slices of them at
+    // recv + sender * kQkvSliceMax.
+    float *part = reinterpret_cast<float *>(sm);
+    const int R4 = R / kQkvCluster;
+    const uint32_t slice_bytes = R4 * kQkvPartStride * 4;
+    const uint32_t recv = smem_u32(sm + kQkvRecvOff);
     if (warp == kConsumerWarps) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
-            // this CTA's packed blocks: (head * 4 + rank) * (hidden / 64) onwards
             const __nv_bfloat16 *wsrc =
-                p.w_packed + static_cast<int64_t>(head * kQkvCluster + rank) * p.hidden * 32;
+                p.w_packed + (static_cast<int64_t>(head) * nk + kb0) * (kQkvBlock / 2);
             // With an overlapped launch the weight (which no kernel writes) of
             // the first stages goes out before the dependency wait; the hidden
             // states only after it.
@@ -127,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const uint32_t full = full0 + 8 * c;
                 mbar_arrive_expect_tx(full, stage_bytes);
                 bulk_load(smem_u32(sm + c * stage_bytes),
-                          wsrc + static_cast<int64_t>(c) * NB * 32 * kQkvChunk, NB * 2 * kQkvWBox,
+                          wsrc + static_cast<int64_t>(c) * NB * (kQkvBlock / 2), NB * kQkvBlock,
                           full);
             }
             if (p.pdl) grid_dependency_wait();
@@ -144,71 +186,82 @@ __global__ void __launch_bounds__(kThreads, 2)
                         break;
                     }
                     mbar_arrive_expect_tx(full, stage_bytes);
-                    bulk_load(dst, wsrc + static_cast<int64_t>(c) * NB * 32 * kQkvChunk,
-                              NB * 2 * kQkvWBox, full);
+                    bulk_load(dst, wsrc + static_cast<int64_t>(c) * NB * (kQkvBlock / 2),
+                              NB * kQkvBlock, full);
                 }
                 for (int j = 0; j < NB; ++j)
-                    tma_load_2d(dst + 2 * NB * kQkvWBox + j * p.qkv_rows * kQkvChunk * 2, &x_map,
-                                (c * NB + j) * kQkvChunk, row0, full);
+                    tma_load_2d(dst + NB * kQkvBlock + j * R * kQkvChunk * 2, &x_map,
+                                (kb0 + c * NB + j) * kQkvChunk, row0, full);
             }
         }
         __syncwarp();
-        cluster_sync_all();  // row sums published
-        cluster_sync_all();  // peers done reading them
+        cluster_sync_all();  // partials in place, every ring free
     } else {
         // ------------------------------------------- consumer warps --
-        // warp w: batch rows row0 + 16w .. +15; n-tiles 0, 1: dims 16r + 0..15,
-        // n-tiles 2, 3: dims 64 + 16r + 0..15
+        // RT 16-row tiles x CG column groups (RT * CG <= 4): warp w takes
+        // tile w / CG and sub-blocks [(w % CG) * 4 / CG, +4 / CG) of every
+        // block, i.e. NT = 16 / CG n-tiles of 8 columns
         const int g = lane >> 2, t = lane & 3;
-        const bool live = row0 + 16 * warp < p.B;
-        float acc[4][4];
+        const int RT = R / 16;
+        const int CG = RT == 1 ? 4 : (RT == 2 ? 2 : 1);
+        const int NT = 16 / CG;
+        const int rt = warp / CG, sb0 = (warp % CG) * (4 / CG);
+        const bool live = rt < RT && row0 + 16 * rt < p.B;
+        float acc[16][4];
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+        for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
         const int mi = lane >> 3, r8 = lane & 7;
-        const int arow = 16 * warp + (mi & 1) * 8 + r8;  // x row this lane addresses
-        const int brow = (mi >> 1) * 8 + r8;             // W row within a 16-row box
+        const int arow = 16 * rt + (mi & 1) * 8 + r8;  // x row this lane addresses
+        const int brow = (mi >> 1) * 8 + r8;            // W row within a 16-row half sub-block
         if (p.pdl) grid_dependency_wait();  // the tables, q_rot and the pool of earlier kernels
 
-        // the epilogue's lookups for rows g and g + 8, made while the weight
-        // streams: the append slot (-1: skip the row) and the norm weights
+        // ---- the epilogue's inputs, fetched while the weight streams.  Thread
+        // tid takes rows rs and rs + 8 (rs = tid / 16) of this CTA's R/4 and
+        // the rotate-half pairs 4 (tid % 16) .. +3: dims d0 .. d0+3 and
+        // d0+64 .. d0+67.  slot: the append slot (-1: skip the row).
+        const int rs = tid >> 4, d0 = 4 * (tid & 15);
         const int Hq = p.Hq, Hkv = p.Hkv;
         const int kind = head < Hq ? 0 : (head < Hq + Hkv ? 1 : 2);  // q, k or v head
         const int kvh = kind == 1 ? head - Hq : head - Hq - Hkv;
         int64_t slot[2] = {-1, -1};
+        float4 cs[2][2];  // (c_hi, s_hi) of pairs d0 .. d0+3 per row: {c0 s0 c1 s1}, {c2 s2 c3 s3}
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int b = row0 + 16 * warp + g + 8 * half;
-            if (!live || b >= p.B) continue;
+        for (int h = 0; h < 2; ++h) {
+            cs[h][0] = cs[h][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            const int i = rs + 8 * h, b = row0 + rank * R4 + i;
+            if (i >= R4 || b >= p.B) continue;
             const int L = p.seq_lens[b];
             if (L < 1 || L > p.max_blocks * kPageSize) {
-                if (t == 0 && head == 0 && rank == 0) flag_error(p.err, QDEC_FLAG_BAD_SEQLEN);
+                if ((tid & 15) == 0 && head == 0) flag_error(p.err, QDEC_FLAG_BAD_SEQLEN);
                 continue;
             }
+            if (kind != 2) {
+                const RopeEntry *e = p.rope + static_cast<int64_t>(b) * kRotPairs + d0;
+                cs[h][0] = make_float4(e[0].c_hi, e[0].s_hi, e[1].c_hi, e[1].s_hi);
+                cs[h][1] = make_float4(e[2].c_hi, e[2].s_hi, e[3].c_hi, e[3].s_hi);
+            }
             if (kind == 0) {
-                slot[half] = 0;
+                slot[h] = 0;
                 continue;
             }
             const int page =
                 p.block_table[static_cast<int64_t>(b) * p.max_blocks + (L - 1) / kPageSize];
             if (page < 0 || page >= p.num_pages) {
-                if (t == 0 && rank == 0 && kind == 1 && kvh == 0)
-                    flag_error(p.err, QDEC_FLAG_BAD_PAGE);
+                if ((tid & 15) == 0 && kvh == 0 && kind == 1) flag_error(p.err, QDEC_FLAG_BAD_PAGE);
                 continue;
             }
-            slot[half] =
+            slot[h] =
                 ((static_cast<int64_t>(page) * 2 * Hkv + kvh) * kPageSize + (L - 1) % kPageSize) *
                 kHeadDim;
         }
-        uint32_t wn2[2][2];  // norm weight pairs (d, d+1), (d+64, d+65) of n-tiles 0, 1
-        {
+        uint2 wn1 = make_uint2(0u, 0u), wn2 = make_uint2(0u, 0u);  // norm weights, bf16 pairs
+        if (kind != 2) {
             const __nv_bfloat16 *wn = kind == 0 ? p.w_q : p.w_k;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int d = 16 * rank + 8 * nt + 2 * t;
-                wn2[nt][0] = kind == 2 ? 0u : *reinterpret_cast<const uint32_t *>(wn + d);
-                wn2[nt][1] = kind == 2 ? 0u : *reinterpret_cast<const uint32_t *>(wn + d + 64);
-            }
+            wn1 = *reinterpret_cast<const uint2 *>(wn + d0);
+            wn2 = *reinterpret_cast<const uint2 *>(wn + d0 + 64);
         }
+
+        bool aborted = false;
         for (int c = 0; c < nchunks; ++c) {
             const int s = c % NS;
             const bool ok = mbar_wait_bounded(full0 + 8 * s, (c / NS) & 1, abort_flag,
@@ -218,91 +271,137 @@ __global__ void __launch_bounds__(kThreads, 2)
                     *abort_flag = 1;
                     flag_error(p.err, QDEC_FLAG_TIMEOUT);
                 }
+                aborted = true;
                 break;
             }
             for (int j = 0; j < NB && live; ++j) {
                 const uint32_t sb = smem_u32(sm + s * stage_bytes);
-                // packed block j: rows 0..15 dims 16r.., rows 16..31 dims 64 + 16r..
-                const uint32_t wa = sb + j * 2 * kQkvWBox, wbb = wa + kQkvWBox;
-                const uint32_t xb = sb + 2 * NB * kQkvWBox + j * p.qkv_rows * kQkvChunk * 2;
+                const uint32_t wb = sb + j * kQkvBlock + sb0 * kQkvSub;
+                const uint32_t xb = sb + NB * kQkvBlock + j * R * kQkvChunk * 2;
 #pragma unroll
                 for (int kk = 0; kk < kQkvChunk / 16; ++kk) {
-                    uint32_t a[4], b01[4], b23[4];
+                    uint32_t a[4];
                     ldmatrix_x4(a, swz(xb, arow, 2 * kk + (mi >> 1)));
-                    ldmatrix_x4(b01, swz(wa, brow, 2 * kk + (mi & 1)));
-                    ldmatrix_x4(b23, swz(wbb, brow, 2 * kk + (mi & 1)));
-                    mma_bf16(acc[0], a, b01[0], b01[1]);
-                    mma_bf16(acc[1], a, b01[2], b01[3]);
-                    mma_bf16(acc[2], a, b23[0], b23[1]);
-                    mma_bf16(acc[3], a, b23[2], b23[3]);
+#pragma unroll
+                    for (int pr = 0; pr < 8; ++pr) {  // n-tile pairs: 16 W rows each
+                        if (2 * pr >= NT) break;
+                        uint32_t b[4];
+                        // pair pr: sub-block pr / 2, rows 16 (pr % 2) ..
+                        ldmatrix_x4(b, swz(wb + (pr >> 1) * kQkvSub, 16 * (pr & 1) + brow,
+                                           2 * kk + (mi & 1)));
+                        mma_bf16(acc[2 * pr], a, b[0], b[1]);
+                        mma_bf16(acc[2 * pr + 1], a, b[2], b[3]);
+                    }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8 * s);
         }
-        // this CTA's share of each row's sum of squares (rows g and g + 8)
-        float sA = 0.f, sB = 0.f;
+        // every stage is consumed (no copy is landing in the ring): the
+        // partials go to part[row][column], column = 32 * sub-block + row of it
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+        if (live && !aborted) {
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            sA += acc[nt][0] * acc[nt][0] + acc[nt][1] * acc[nt][1];
-            sB += acc[nt][2] * acc[nt][2] + acc[nt][3] * acc[nt][3];
-        }
-#pragma unroll
-        for (int o = 1; o < 4; o <<= 1) {
-            sA += __shfl_xor_sync(kFull, sA, o);
-            sB += __shfl_xor_sync(kFull, sB, o);
-        }
-        if (t == 0) {
-            ss[16 * warp + g] = sA;
-            ss[16 * warp + g + 8] = sB;
-        }
-        cluster_sync_all();  // every CTA's shares are in place
-        float totA = 0.f, totB = 0.f;
-#pragma unroll
-        for (int q = 0; q < kQkvCluster; ++q) {
-            const float *peer = cluster_peer(ss, q);
-            totA += peer[16 * warp + g];
-            totB += peer[16 * warp + g + 8];
-        }
-        cluster_sync_all();  // nobody leaves while a peer may still read
-
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int b = row0 + 16 * warp + g + 8 * half;
-            if (*abort_flag || slot[half] < 0) continue;
-            const float tot = half ? totB : totA;
-            const int64_t kslot = slot[half];
-            const float rn = rsqrtf(tot * (1.0f / kHeadDim) + p.eps);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int d = 16 * rank + 8 * nt + 2 * t;  // dims d, d+1 and d+64, d+65
-                const float x1a = acc[nt][2 * half], x1b = acc[nt][2 * half + 1];
-                const float x2a = acc[nt + 2][2 * half], x2b = acc[nt + 2][2 * half + 1];
-                if (kind == 2) {
-                    __nv_bfloat16 *vdst = p.pool + kslot + static_cast<int64_t>(Hkv) * kPageSize *
-                                                               kHeadDim;
-                    *reinterpret_cast<uint32_t *>(vdst + d) = pack2_bf16(x1a, x1b);
-                    *reinterpret_cast<uint32_t *>(vdst + d + 64) = pack2_bf16(x2a, x2b);
-                    continue;
-                }
-                const float2 w1 = bf16x2_to_float2(wn2[nt][0]), w2 = bf16x2_to_float2(wn2[nt][1]);
-                const float n1a = x1a * rn * w1.x, n1b = x1b * rn * w1.y;
-                const float n2a = x2a * rn * w2.x, n2b = x2b * rn * w2.y;
-                const RopeEntry ea = p.rope[static_cast<int64_t>(b) * kRotPairs + d];
-                const RopeEntry eb = p.rope[static_cast<int64_t>(b) * kRotPairs + d + 1];
-                const float y1a = n1a * ea.c_hi - n2a * ea.s_hi, y2a = n2a * ea.c_hi + n1a * ea.s_hi;
-                const float y1b = n1b * eb.c_hi - n2b * eb.s_hi, y2b = n2b * eb.c_hi + n1b * eb.s_hi;
-                if (kind == 0) {
-                    float *dst = p.q_rot_out + (static_cast<int64_t>(b) * Hq + head) * kHeadDim;
-                    *reinterpret_cast<float2 *>(dst + d) = make_float2(y1a, y1b);
-                    *reinterpret_cast<float2 *>(dst + d + 64) = make_float2(y2a, y2b);
-                } else {
-                    __nv_bfloat16 *kdst = p.pool + kslot;
-                    *reinterpret_cast<uint32_t *>(kdst + d) = pack2_bf16(y1a, y1b);
-                    *reinterpret_cast<uint32_t *>(kdst + d + 64) = pack2_bf16(y2a, y2b);
-                }
+            for (int nt = 0; nt < 16; ++nt) {
+                if (nt >= NT) break;
+                const int col = 32 * sb0 + 8 * nt + 2 * t;
+                float *r0 = part + (16 * rt + g) * kQkvPartStride + col;
+                *reinterpret_cast<float2 *>(r0) = make_float2(acc[nt][0], acc[nt][1]);
+                *reinterpret_cast<float2 *>(r0 + 8 * kQkvPartStride) =
+                    make_float2(acc[nt][2], acc[nt][3]);
             }
         }
+        fence_proxy_async_smem();  // the partials are read next by bulk copies
+        cluster_sync_all();        // every CTA's partials are in place, every ring is free
+
+        // push slice q of the partials to CTA q (one bulk copy each)
+        if (tid == 0) {
+            mbar_arrive_expect_tx(recv_bar, (kQkvCluster - 1) * slice_bytes);
+#pragma unroll
+            for (int q = 0; q < kQkvCluster; ++q) {
+                if (q == rank) continue;
+                bulk_push(cluster_addr(recv + rank * kQkvSliceMax, q),
+                          smem_u32(part + q * R4 * kQkvPartStride), slice_bytes,
+                          cluster_addr(recv_bar, q));
+            }
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        // every peer pushes after the barrier whatever happened before it, so
+        // wait for the bytes even after an abort: this CTA's memory must
+        // outlive the copies into it (bounded all the same)
+        volatile int never = 0;
+        const bool got = mbar_wait_bounded(recv_bar, 0, &never, p.wait_cycles);
+        if (!got && tid == 0) {
+            *abort_flag = 1;
+            flag_error(p.err, QDEC_FLAG_TIMEOUT);
+        }
+
+        // the owned rows: the four CTAs' partials added in rank order, then
+        // RMSNorm over the 128 dims (16 threads per row), RoPE, write
+        const float2 w01 = bf16x2_to_float2(wn1.x), w23 = bf16x2_to_float2(wn1.y);
+        const float2 w45 = bf16x2_to_float2(wn2.x), w67 = bf16x2_to_float2(wn2.y);
+        const float wv[8] = {w01.x, w01.y, w23.x, w23.y, w45.x, w45.y, w67.x, w67.y};
+        // part column of dim d < 64: 32 (d / 16) + d % 16; of dim 64 + d: that + 16
+        const int clo = 32 * (d0 >> 4) + (d0 & 15);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = rs + 8 * h;
+            if (i >= R4) break;  // uniform over each half-warp (16 threads per row)
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = 0.f;
+#pragma unroll
+            for (int q = 0; q < kQkvCluster; ++q) {
+                const float *src = q == rank ? part + (rank * R4 + i) * kQkvPartStride
+                                             : reinterpret_cast<const float *>(
+                                                   sm + kQkvRecvOff + q * kQkvSliceMax) +
+                                                   i * kQkvPartStride;
+                const float4 lo = *reinterpret_cast<const float4 *>(src + clo);
+                const float4 hi = *reinterpret_cast<const float4 *>(src + clo + 16);
+                y[0] += lo.x; y[1] += lo.y; y[2] += lo.z; y[3] += lo.w;
+                y[4] += hi.x; y[5] += hi.y; y[6] += hi.z; y[7] += hi.w;
+            }
+            float sq = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sq += y[e] * y[e];
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) sq += __shfl_xor_sync(kFull, sq, o);
+            const int b = row0 + rank * R4 + i;
+            if (aborted || *abort_flag || slot[h] < 0) continue;
+            const int64_t kslot = slot[h];
+            if (kind == 2) {
+                __nv_bfloat16 *vdst =
+                    p.pool + kslot + static_cast<int64_t>(Hkv) * kPageSize * kHeadDim;
+                *reinterpret_cast<uint2 *>(vdst + d0) =
+                    make_uint2(pack2_bf16(y[0], y[1]), pack2_bf16(y[2], y[3]));
+                *reinterpret_cast<uint2 *>(vdst + d0 + 64) =
+                    make_uint2(pack2_bf16(y[4], y[5]), pack2_bf16(y[6], y[7]));
+                continue;
+            }
+            const float rn = rsqrtf(sq * (1.0f / kHeadDim) + p.eps);
+            const float c[4] = {cs[h][0].x, cs[h][0].z, cs[h][1].x, cs[h][1].z};
+            const float sn[4] = {cs[h][0].y, cs[h][0].w, cs[h][1].y, cs[h][1].w};
+            float o1[4], o2[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float n1 = y[e] * rn * wv[e], n2 = y[4 + e] * rn * wv[4 + e];
+                o1[e] = n1 * c[e] - n2 * sn[e];
+                o2[e] = n2 * c[e] + n1 * sn[e];
+            }
+            if (kind == 0) {
+                float *dst = p.q_rot_out + (static_cast<int64_t>(b) * Hq + head) * kHeadDim;
+                *reinterpret_cast<float4 *>(dst + d0) = make_float4(o1[0], o1[1], o1[2], o1[3]);
+                *reinterpret_cast<float4 *>(dst + d0 + 64) = make_float4(o2[0], o2[1], o2[2], o2[3]);
+            } else {
+                __nv_bfloat16 *kdst = p.pool + kslot;
+                *reinterpret_cast<uint2 *>(kdst + d0) =
+                    make_uint2(pack2_bf16(o1[0], o1[1]), pack2_bf16(o1[2], o1[3]));
+                *reinterpret_cast<uint2 *>(kdst + d0 + 64) =
+                    make_uint2(pack2_bf16(o2[0], o2[1]), pack2_bf16(o2[2], o2[3]));
+            }
+        }
+        // the pushed slices must be read out before this CTA's memory is released
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
     }
     __syncthreads();
     // a wait that gave up may leave copies in flight: let them land (bounded)
@@ -314,23 +413,24 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-// Packing: destination 16-byte unit u lies in block u / 256 (4 KiB), row
-// (u / 8) % 32 of the block, position u % 8, which holds source chunk
-// (u % 8) ^ (row % 8) of that row (the 128-byte swizzle).  Block index =
-// (head * 4 + rank) * (hidden / 64) + k-block; block rows 0-15 are weight rows
-// head * 128 + 16 rank + i, rows 16-31 are head * 128 + 64 + 16 rank + i.
+// Packing: destination 16-byte unit u lies in block u / 1024 (16 KiB, block
+// index = head * (hidden / 64) + k-block), sub-block (u / 256) % 4, row
+// (u / 8) % 32 of the sub-block, position u % 8, which holds source chunk
+// (u % 8) ^ (row % 8) of that row (the 128-byte swizzle).  Sub-block i rows
+// 0-15 are weight rows head * 128 + 16 i + row, rows 16-31 are
+// head * 128 + 64 + 16 i + row - 16.
 __global__ void qkv_pack_kernel(const __nv_bfloat16 *w, __nv_bfloat16 *wp, int rows, int hidden) {
     const int64_t total = static_cast<int64_t>(rows) * hidden / 8;
     const int nk = hidden / kQkvChunk;
     for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < total;
          u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t block = u / 256;
+        const int64_t block = u / 1024;
+        const int sub = static_cast<int>((u / 256) % 4);
         const int rho = static_cast<int>((u / 8) % 32), pos = static_cast<int>(u % 8);
         const int q = pos ^ (rho & 7);
         const int kb = static_cast<int>(block % nk);
-        const int64_t hr = block / nk;  // head * 4 + rank
-        const int head = static_cast<int>(hr / kQkvCluster), rank = static_cast<int>(hr % kQkvCluster);
-        const int row = head * kHeadDim + (rho < 16 ? 16 * rank + rho : 64 + 16 * rank + rho - 16);
+        const int head = static_cast<int>(block / nk);
+        const int row = head * kHeadDim + (rho < 16 ? 16 * sub + rho : 64 + 16 * sub + rho - 16);
         const uint4 v = *reinterpret_cast<const uint4 *>(
             w + static_cast<int64_t>(row) * hidden + kb * kQkvChunk + q * 8);
         *reinterpret_cast<uint4 *>(wp + u * 8) = v;
@@ -344,9 +444,9 @@ constexpr int kQkvSmemMax = kQkvRingBytes + kQkvTailBytes + 1024;
 }  // namespace
 
 void qkv_geometry(int B, int hidden, int &rows, int &boxes, int &stages) {
+    (void)hidden;
     rows = B >= kQkvRows ? kQkvRows : (B + 15) / 16 * 16;
-    boxes = rows <= 16 ? 4 : (rows <= 32 ? 2 : 1);
-    while (boxes > 1 && hidden % (kQkvChunk * boxes) != 0) boxes /= 2;
+    boxes = 1;
     stages = kQkvRingBytes / qkv_stage_bytes(rows, boxes);
     if (stages > kQkvMaxStages) stages = kQkvMaxStages;
 }

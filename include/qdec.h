@@ -246,10 +246,11 @@ qdec_status qdec_qkv_append_rope(const qdec_shape *shape, int32_t hidden,
                                  void *stream);
 
 /* Rearranges w_qkv (row-major, as above) into w_packed (a separate buffer of
- * the same size, 16-byte aligned): for every (output head, quarter of its
- * dims) the rows that quarter needs, in 4 KiB blocks of 64 hidden elements,
- * so the projection streams one contiguous run per CTA.  A device-side copy
- * on `stream`; run it once per weight. */
+ * the same size, 16-byte aligned): per (output head, block of 64 hidden
+ * elements) 16 KiB, the head's 128 rows in four 4 KiB sub-blocks (sub-block i:
+ * dims 16i .. 16i+15, then 64+16i .. 64+16i+15), each 128-byte row swizzled,
+ * so each CTA of the projection streams one contiguous run.  A device-side
+ * copy on `stream`; run it once per weight. */
 qdec_status qdec_qkv_pack_weights(const qdec_shape *shape, int32_t hidden,
                                   const qdec_bf16 *w_qkv, qdec_bf16 *w_packed, void *stream);
 

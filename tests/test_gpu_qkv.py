@@ -7,8 +7,10 @@ and the rotation carry into q_rot and k_rot as r * max|w| * (E_i + E_(i+64)).
 Checked: q_rot within the fp32 q_rot tolerance plus that bound; the appended
 k and v within one bf16 ulp of the oracle's unrounded values plus that bound;
 the rest of the pool untouched; the whole block (projection, then
-qdec_attn_decode, or split attention and merge) within the out tolerance.  Batches of 1 to 70 rows (two 64-row blocks), hidden sizes 64 to
-2560, NaN-poisoned pools.
+qdec_attn_decode, or split attention and merge) within the out tolerance.
+Batches of 1 to 70 rows (16-, 32-, 48- and 64-row tiles; two 64-row blocks),
+hidden sizes 64 to 2560 (blocks of 64 split unevenly, some CTAs of a cluster
+with none), NaN-poisoned pools.
 """
 import math
 
@@ -116,7 +118,11 @@ def _check_slots(w, res):
 @pytest.mark.parametrize("lens,hidden", [
     ([1], 64), ([17, 1, 300], 256), ([40] * 8, 2560), ([300, 17, 1000, 64], 2560),
     ([int(x) for x in np.random.default_rng(5).integers(1, 200, size=70)], 512),
-], ids=["b1-h64", "b3-h256", "b8-h2560", "b4-h2560", "b70-h512"])
+    ([int(x) for x in np.random.default_rng(6).integers(1, 400, size=20)], 192),
+    ([int(x) for x in np.random.default_rng(7).integers(1, 400, size=40)], 1280),
+    ([int(x) for x in np.random.default_rng(8).integers(1, 100, size=64)], 320),
+], ids=["b1-h64", "b3-h256", "b8-h2560", "b4-h2560", "b70-h512", "b20-h192", "b40-h1280",
+        "b64-h320"])
 def test_qkv_projection_matches_oracle(lens, hidden):
     w, x, wqkv = _problem(lens, hidden, seed=61)
     res = _oracle(w, x, wqkv)
