@@ -21,14 +21,17 @@
 // swizzled for conflict-free matrix loads; a CTA's share is one contiguous
 // run.  One producer warp streams stages of one 16 KiB block (one bulk copy)
 // and the matching box of x (the batch rounded up to 16 rows, at most 64; rows
-// past B read as zero, TMA) into a ring of about 96 KiB; the four consumer
-// warps split the stage's rows x 128 columns into 16-row tiles and column
-// groups (one tile and all 16 n-tiles at 64 rows, four column groups of one
-// tile at 16 rows) and run bf16 mma.sync with fp32 accumulators.  At the end
-// every CTA leaves its partial sums in shared memory and, after one cluster
-// barrier, pushes to CTA q (one bulk shared-to-shared copy each, counted on
-// q's transaction barrier) the rows q owns: rows q R/4 .. (q+1) R/4 - 1 of
-// the R.  The owner adds the four partials in rank order, so each row's 128
+// past B read as zero, TMA) into a ring of about 96 KiB.  Both land in the
+// K-major 128-byte-swizzled layout the 5th-generation tensor core reads from
+// shared memory: one thread issues, per stage, four tcgen05.mma of kind f16
+// (bf16 operands, M = 128 head dims, N = the R batch rows, K = 16) that
+// accumulate D [128][R] in fp32 in tensor memory, and commits them to the
+// stage's empty barrier, so the stage is refilled as soon as they have read it.
+// Once the MMAs have completed, the four consumer warps read D out of tensor
+// memory (warp w: lanes 32w .. 32w+31) into a partial-sum tile in shared
+// memory, and after one cluster barrier every CTA pushes to CTA q (one bulk
+// shared-to-shared copy each, counted on q's transaction barrier) the rows q
+// owns: rows q R/4 .. (q+1) R/4 - 1 of the R.  The owner adds the four partials in rank order, so each row's 128
 // dims are complete in one CTA: the RMSNorm sum of squares, the rotation and
 // the writes need nothing from the peers.  The epilogue's lookups (append
 // slot, norm weights, rotation table) are made before the main loop.
@@ -56,8 +59,10 @@ constexpr int kQkvPartStride = kHeadDim + 8;                // floats per row of
 constexpr int kQkvSliceMax = kQkvRows / kQkvCluster * kQkvPartStride * 4;  // rows one CTA owns
 constexpr int kQkvRecvOff = 36 * 1024;                      // receive area in the ring
 constexpr int kQkvRingUse = kQkvRecvOff + kQkvCluster * kQkvSliceMax;
-// after the ring: barriers full[16], empty[16], recv, the abort flag
-constexpr int kQkvTailBytes = 2 * kQkvMaxStages * 8 + 8 + 8;
+constexpr int kQkvTmemCols = 64;                           // fp32 accumulator columns (N <= 64)
+// after the ring: barriers full[16], empty[16], recv, mma-done, the abort
+// flag, the tensor-memory address
+constexpr int kQkvTailBytes = 2 * kQkvMaxStages * 8 + 8 + 8 + 8 + 8;
 static_assert(kQkvRows * kQkvPartStride * 4 <= kQkvRecvOff, "partials end before the receive area");
 // a stage: [boxes packed blocks of 16 KiB][boxes x boxes of rows x 64], each
 // piece starting on a 1024-byte boundary (rows % 16 == 0)
@@ -90,6 +95,79 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t local, int rank) {
     return r;
 }
 
+// Address of row r, 16-byte chunk c of a 128-byte-swizzled box at `base`.
+__device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c) {
+    return base + r * 128 + ((c ^ (r & 7)) << 4);
+}
+
+// ---- 5th-generation tensor core (tcgen05) wrappers.  The accumulator D
+// lives in tensor memory (lane = row of D, one 32-bit column per fp32
+// element); A and B are read from shared memory through matrix descriptors.
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols) {  // whole warp
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                 "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {  // whole warp
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzled layout (8-row x 128-byte atoms, 1024 bytes apart; the atoms must
+// start on 1024-byte boundaries): start address >> 4 in bits 0-13, leading
+// byte offset (unused for this layout; 16 bytes) >> 4 in bits 16-29, stride
+// byte offset 1024 >> 4 in bits 32-45, descriptor version 1 in bits 46-47,
+// layout 2 (128-byte swizzle) in bits 61-63.  Stepping K by 16 elements adds
+// 32 bytes to the start address.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3fffu) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+// Instruction descriptor of kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t f16_idesc(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+// D (+)= A B^T for one K = 16 step, issued by one thread
+__device__ __forceinline__ void tc_mma(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1 : 0)
+        : "memory");
+}
+// arrive (once) on `bar` when every tcgen05 operation this thread issued so
+// far has completed
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+// 16 consecutive columns of this warp's 32 lanes (lane l: row 32 (warp % 4) + l)
+__device__ __forceinline__ void tmem_ld16(uint32_t (&v)[16], uint32_t taddr) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void flag_error(int32_t *err, int bits) {
     if (err) atomicOr(err, bits);
 }
@@ -103,11 +181,12 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
            (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
 }
 
-// Address of row r, 16-byte chunk c of a 128-byte-swizzled box at `base`.
-__device__ __forceinline__ uint32_t swz(uint32_t base, int r, int c) {
-    return base + r * 128 + ((c ^ (r & 7)) << 4);
-}
-
+// kTc: the contraction on the 5th-generation tensor core (tcgen05, operands
+// read from shared memory, the accumulator in tensor memory); otherwise on
+// mma.sync with the accumulators in registers, which has the shorter fixed
+// cost per launch and is used when the batch fits one 16-row tile (where the
+// weight stream, not the arithmetic, sets the time).
+template <bool kTc>
 __global__ void __launch_bounds__(kThreads, 2)
     qkv_append_kernel(const __grid_constant__ CUtensorMap x_map, const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -128,7 +207,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t full0 = smem_u32(tail);
     const uint32_t empty0 = full0 + kQkvMaxStages * 8;
     const uint32_t recv_bar = empty0 + kQkvMaxStages * 8;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tail + 2 * kQkvMaxStages * 8 + 8);
+    const uint32_t done_bar = recv_bar + 8;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tail + 2 * kQkvMaxStages * 8 + 16);
+    volatile uint32_t *tmem_slot =
+        reinterpret_cast<volatile uint32_t *>(tail + 2 * kQkvMaxStages * 8 + 24);
     if (NS < 1 || NS > kQkvMaxStages || R < 16 || R > kQkvRows || R % 16 != 0 || NB < 1 ||
         NB > 2 || p.hidden % kQkvChunk != 0 || (kb1 - kb0) % NB != 0 ||
         NS * stage_bytes < kQkvRingUse) {
@@ -137,16 +219,38 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     if (p.pdl && tid == 0) launch_dependents();  // the next kernel waits for our completion
-    if (tid == 0) {
+    // The producer thread sets up the barriers and at once sends the weight
+    // (which no kernel writes) of the first stages, before any dependency
+    // wait, with their boxes of x unless the launch overlaps the previous
+    // kernel; warp 0 meanwhile allocates the tensor memory.
+    const __nv_bfloat16 *wsrc =
+        p.w_packed + (static_cast<int64_t>(head) * nk + kb0) * (kQkvBlock / 2);
+    const int pre = min(NS, nchunks);
+    if (warp == kConsumerWarps && lane == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, kConsumerWarps);  // every warp takes every stage
+            // tcgen05: the commit of the stage's MMAs; mma.sync: every consumer warp
+            mbar_init(empty0 + 8 * s, kTc ? 1 : kConsumerWarps);
         }
         mbar_init(recv_bar, 1);
+        mbar_init(done_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
+        for (int c = 0; c < pre; ++c) {
+            const uint32_t full = full0 + 8 * c;
+            mbar_arrive_expect_tx(full, stage_bytes);
+            bulk_load(smem_u32(sm + c * stage_bytes),
+                      wsrc + static_cast<int64_t>(c) * NB * (kQkvBlock / 2), NB * kQkvBlock, full);
+            for (int j = 0; j < NB && !p.pdl; ++j)
+                tma_load_2d(smem_u32(sm + c * stage_bytes) + NB * kQkvBlock + j * R * kQkvChunk * 2,
+                            &x_map, (kb0 + c * NB + j) * kQkvChunk, row0, full);
+        }
     }
+    if (kTc && warp == 0) tmem_alloc(smem_u32(const_cast<uint32_t *>(tmem_slot)), kQkvTmemCols);
+    if (kTc) tc_fence_before();
     __syncthreads();
+    if (kTc) tc_fence_after();
+    const uint32_t tmem = kTc ? *tmem_slot : 0u;  // lane 0, the first allocated column
 
     // The partial sums [64 rows][128 + 8] fp32 overwrite the ring once every
     // stage is consumed; CTA q owns rows q R/4 .. (q+1) R/4 - 1 (a contiguous
@@ -159,19 +263,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == kConsumerWarps) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
-            const __nv_bfloat16 *wsrc =
-                p.w_packed + (static_cast<int64_t>(head) * nk + kb0) * (kQkvBlock / 2);
-            // With an overlapped launch the weight (which no kernel writes) of
-            // the first stages goes out before the dependency wait; the hidden
-            // states only after it.
-            const int pre = p.pdl ? min(NS, nchunks) : 0;
-            for (int c = 0; c < pre; ++c) {
-                const uint32_t full = full0 + 8 * c;
-                mbar_arrive_expect_tx(full, stage_bytes);
-                bulk_load(smem_u32(sm + c * stage_bytes),
-                          wsrc + static_cast<int64_t>(c) * NB * (kQkvBlock / 2), NB * kQkvBlock,
-                          full);
-            }
+            // the remaining hidden states only after the dependency wait
             if (p.pdl) grid_dependency_wait();
             for (int c = 0; c < nchunks; ++c) {
                 const int s = c % NS;
@@ -189,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     bulk_load(dst, wsrc + static_cast<int64_t>(c) * NB * (kQkvBlock / 2),
                               NB * kQkvBlock, full);
                 }
-                for (int j = 0; j < NB; ++j)
+                for (int j = 0; j < NB && (c >= pre || p.pdl); ++j)
                     tma_load_2d(dst + NB * kQkvBlock + j * R * kQkvChunk * 2, &x_map,
                                 (kb0 + c * NB + j) * kQkvChunk, row0, full);
             }
@@ -198,21 +290,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         cluster_sync_all();  // partials in place, every ring free
     } else {
         // ------------------------------------------- consumer warps --
-        // RT 16-row tiles x CG column groups (RT * CG <= 4): warp w takes
-        // tile w / CG and sub-blocks [(w % CG) * 4 / CG, +4 / CG) of every
-        // block, i.e. NT = 16 / CG n-tiles of 8 columns
-        const int g = lane >> 2, t = lane & 3;
-        const int RT = R / 16;
-        const int CG = RT == 1 ? 4 : (RT == 2 ? 2 : 1);
-        const int NT = 16 / CG;
-        const int rt = warp / CG, sb0 = (warp % CG) * (4 / CG);
-        const bool live = rt < RT && row0 + 16 * rt < p.B;
-        float acc[16][4];
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-        const int mi = lane >> 3, r8 = lane & 7;
-        const int arow = 16 * rt + (mi & 1) * 8 + r8;  // x row this lane addresses
-        const int brow = (mi >> 1) * 8 + r8;            // W row within a 16-row half sub-block
+        // kTc: thread 0 issues the tensor-core MMAs: per stage, D [128 dims]
+        // [R rows] += W_block [128][64] x_box [R][64]^T in four K = 16 steps,
+        // committed to the stage's empty barrier; all four warps then read D.
+        // Otherwise every warp takes every stage with mma.sync (see below).
         if (p.pdl) grid_dependency_wait();  // the tables, q_rot and the pool of earlier kernels
 
         // ---- the epilogue's inputs, fetched while the weight streams.  Thread
@@ -262,53 +343,124 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
 
         bool aborted = false;
-        for (int c = 0; c < nchunks; ++c) {
-            const int s = c % NS;
-            const bool ok = mbar_wait_bounded(full0 + 8 * s, (c / NS) & 1, abort_flag,
-                                              p.wait_cycles);
-            if (!ok) {
-                if (lane == 0) {
-                    *abort_flag = 1;
-                    flag_error(p.err, QDEC_FLAG_TIMEOUT);
+        if constexpr (kTc) {
+            if (tid == 0) {
+                const uint32_t idesc = f16_idesc(kHeadDim, R);
+                for (int c = 0; c < nchunks; ++c) {
+                    const int s = c % NS;
+                    if (!mbar_wait_bounded(full0 + 8 * s, (c / NS) & 1, abort_flag, p.wait_cycles)) {
+                        *abort_flag = 1;
+                        flag_error(p.err, QDEC_FLAG_TIMEOUT);
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sb = smem_u32(sm + s * stage_bytes);
+                    for (int j = 0; j < NB; ++j) {
+                        const uint32_t wb = sb + j * kQkvBlock;
+                        const uint32_t xb = sb + NB * kQkvBlock + j * R * kQkvChunk * 2;
+#pragma unroll
+                        for (int kk = 0; kk < kQkvChunk / 16; ++kk)
+                            tc_mma(tmem, sw128_desc(wb + 32 * kk), sw128_desc(xb + 32 * kk), idesc,
+                                   c > 0 || j > 0 || kk > 0);
+                    }
+                    tc_commit(empty0 + 8 * s);  // the stage may be refilled once these are done
                 }
-                aborted = true;
-                break;
+                tc_commit(done_bar);  // every MMA issued above has completed
             }
-            for (int j = 0; j < NB && live; ++j) {
-                const uint32_t sb = smem_u32(sm + s * stage_bytes);
-                const uint32_t wb = sb + j * kQkvBlock + sb0 * kQkvSub;
-                const uint32_t xb = sb + NB * kQkvBlock + j * R * kQkvChunk * 2;
-#pragma unroll
-                for (int kk = 0; kk < kQkvChunk / 16; ++kk) {
-                    uint32_t a[4];
-                    ldmatrix_x4(a, swz(xb, arow, 2 * kk + (mi >> 1)));
-#pragma unroll
-                    for (int pr = 0; pr < 8; ++pr) {  // n-tile pairs: 16 W rows each
-                        if (2 * pr >= NT) break;
-                        uint32_t b[4];
-                        // pair pr: sub-block pr / 2, rows 16 (pr % 2) ..
-                        ldmatrix_x4(b, swz(wb + (pr >> 1) * kQkvSub, 16 * (pr & 1) + brow,
-                                           2 * kk + (mi & 1)));
-                        mma_bf16(acc[2 * pr], a, b[0], b[1]);
-                        mma_bf16(acc[2 * pr + 1], a, b[2], b[3]);
+            __syncwarp();
+            // wait for the MMAs whatever happened: tensor memory is released below
+            {
+                volatile int never = 0;
+                if (!mbar_wait_bounded(done_bar, 0, &never, p.wait_cycles)) {
+                    aborted = true;
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        flag_error(p.err, QDEC_FLAG_TIMEOUT);
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * s);
-        }
-        // every stage is consumed (no copy is landing in the ring): the
-        // partials go to part[row][column], column = 32 * sub-block + row of it
-        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-        if (live && !aborted) {
+            aborted = aborted || *abort_flag;
+            tc_fence_after();
+            // D row 32 warp + lane (part column) for batch rows 0 .. R-1 -> part
+            // [row][column]; the ring is free (every stage's MMAs completed)
+            for (int c0 = 0; c0 < R; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(v, tmem + (static_cast<uint32_t>(32 * warp) << 16) + c0);
 #pragma unroll
-            for (int nt = 0; nt < 16; ++nt) {
-                if (nt >= NT) break;
-                const int col = 32 * sb0 + 8 * nt + 2 * t;
-                float *r0 = part + (16 * rt + g) * kQkvPartStride + col;
-                *reinterpret_cast<float2 *>(r0) = make_float2(acc[nt][0], acc[nt][1]);
-                *reinterpret_cast<float2 *>(r0 + 8 * kQkvPartStride) =
-                    make_float2(acc[nt][2], acc[nt][3]);
+                for (int e = 0; e < 16; ++e)
+                    part[(c0 + e) * kQkvPartStride + 32 * warp + lane] =
+                        nchunks > 0 && !aborted ? __uint_as_float(v[e]) : 0.f;
+            }
+            tc_fence_before();
+            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+            if (warp == 0) {
+                tc_fence_after();
+                tmem_dealloc(tmem, kQkvTmemCols);
+            }
+        } else {
+            // RT 16-row tiles x CG column groups (RT * CG <= 4): warp w takes
+            // tile w / CG and sub-blocks [(w % CG) * 4 / CG, +4 / CG) of every
+            // block, i.e. NT = 16 / CG n-tiles of 8 columns
+            const int g = lane >> 2, t = lane & 3;
+            const int RT = R / 16;
+            const int CG = RT == 1 ? 4 : (RT == 2 ? 2 : 1);
+            const int NT = 16 / CG;
+            const int rt = warp / CG, sb0 = (warp % CG) * (4 / CG);
+            const bool live = rt < RT && row0 + 16 * rt < p.B;
+            float acc[16][4];
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+            const int mi = lane >> 3, r8 = lane & 7;
+            const int arow = 16 * rt + (mi & 1) * 8 + r8;  // x row this lane addresses
+            const int brow = (mi >> 1) * 8 + r8;            // W row within a 16-row half sub-block
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c % NS;
+                const bool ok = mbar_wait_bounded(full0 + 8 * s, (c / NS) & 1, abort_flag,
+                                                  p.wait_cycles);
+                if (!ok) {
+                    if (lane == 0) {
+                        *abort_flag = 1;
+                        flag_error(p.err, QDEC_FLAG_TIMEOUT);
+                    }
+                    aborted = true;
+                    break;
+                }
+                for (int j = 0; j < NB && live; ++j) {
+                    const uint32_t sb = smem_u32(sm + s * stage_bytes);
+                    const uint32_t wb = sb + j * kQkvBlock + sb0 * kQkvSub;
+                    const uint32_t xb = sb + NB * kQkvBlock + j * R * kQkvChunk * 2;
+#pragma unroll
+                    for (int kk = 0; kk < kQkvChunk / 16; ++kk) {
+                        uint32_t a[4];
+                        ldmatrix_x4(a, swz(xb, arow, 2 * kk + (mi >> 1)));
+#pragma unroll
+                        for (int pr = 0; pr < 8; ++pr) {  // n-tile pairs: 16 W rows each
+                            if (2 * pr >= NT) break;
+                            uint32_t b[4];
+                            // pair pr: sub-block pr / 2, rows 16 (pr % 2) ..
+                            ldmatrix_x4(b, swz(wb + (pr >> 1) * kQkvSub, 16 * (pr & 1) + brow,
+                                               2 * kk + (mi & 1)));
+                            mma_bf16(acc[2 * pr], a, b[0], b[1]);
+                            mma_bf16(acc[2 * pr + 1], a, b[2], b[3]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8 * s);
+            }
+            // every stage is consumed (no copy is landing in the ring): the
+            // partials go to part[row][column], column = 32 * sub-block + row of it
+            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+            if (live && !aborted) {
+#pragma unroll
+                for (int nt = 0; nt < 16; ++nt) {
+                    if (nt >= NT) break;
+                    const int col = 32 * sb0 + 8 * nt + 2 * t;
+                    float *r0 = part + (16 * rt + g) * kQkvPartStride + col;
+                    *reinterpret_cast<float2 *>(r0) = make_float2(acc[nt][0], acc[nt][1]);
+                    *reinterpret_cast<float2 *>(r0 + 8 * kQkvPartStride) =
+                        make_float2(acc[nt][2], acc[nt][3]);
+                }
             }
         }
         fence_proxy_async_smem();  // the partials are read next by bulk copies
@@ -467,8 +619,11 @@ cudaError_t launch_qkv_append(const Params &p, const CUtensorMap &x_map, cudaStr
     {
         std::lock_guard<std::mutex> lock(g_qkv_mu);
         if (!g_qkv_smem_set[dev]) {
-            const cudaError_t e = cudaFuncSetAttribute(
-                qkv_append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkvSmemMax);
+            cudaError_t e = cudaFuncSetAttribute(
+                qkv_append_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQkvSmemMax);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(qkv_append_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kQkvSmemMax);
             if (e != cudaSuccess) return e;
             g_qkv_smem_set[dev] = true;
         }
@@ -492,7 +647,9 @@ cudaError_t launch_qkv_append(const Params &p, const CUtensorMap &x_map, cudaStr
     }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, qkv_append_kernel, x_map, p);
+    // one 16-row tile: mma.sync; larger batches: tcgen05
+    return p.qkv_rows <= 16 ? cudaLaunchKernelEx(&cfg, qkv_append_kernel<false>, x_map, p)
+                            : cudaLaunchKernelEx(&cfg, qkv_append_kernel<true>, x_map, p);
 }
 
 }  // namespace qdec
