@@ -67,12 +67,16 @@ KERNEL_SOURCES = {
 # profiles/), keyed by workload; used only while the kernel source hash
 # still matches the one the counters were taken on.
 TRAFFIC = {
-    "b8-ctx256to384-36layer": {"kernel_sha": "2680acf25bb157ff", "bytes_per_launch": 10900480},
-    "b1-ctx8192-spikes-36layer": {"kernel_sha": "2680acf25bb157ff", "bytes_per_launch": 33634432},
-    "b64-ragged128to16384-sharedpool-36layer": {"kernel_sha": "2680acf25bb157ff",
-                                                "bytes_per_launch": 1038058240},
-    "b64-ragged128to16384-sharedpool-36layer-fp8kv": {"kernel_sha": "2680acf25bb157ff",
-                                                      "bytes_per_launch": 524734848},
+    "b8-ctx256to384-36layer": {"kernel_sha": "92059be5fa501bc5", "bytes_per_launch": 10899505},
+    "b1-ctx8192-spikes-36layer": {"kernel_sha": "92059be5fa501bc5", "bytes_per_launch": 33633920},
+    "b64-ragged128to16384-sharedpool-36layer": {"kernel_sha": "92059be5fa501bc5",
+                                                "bytes_per_launch": 1038078449},
+    "b64-ragged128to16384-sharedpool-36layer-fp8kv": {"kernel_sha": "92059be5fa501bc5",
+                                                      "bytes_per_launch": 524764114},
+    # --qkv: the projection kernel
+    "b8-ctx256to384-36layer-qkv2560": {"kernel_sha": "3a96e0c7a7742cc6", "bytes_per_launch": 31541187},
+    "b64-ragged128to16384-sharedpool-36layer-qkv2560": {"kernel_sha": "3a96e0c7a7742cc6",
+                                                        "bytes_per_launch": 31897324},
 }
 
 # The CPU timings sample the first few layers of a workload (same shapes and
