@@ -106,6 +106,12 @@ class Oracle:
         lib.oracle_qkv_append.argtypes = ([ci] * 8 + [u16p] * 4 + [i32p] * 3 + [u16p]
                                           + [_D] * 2 + [dp] * 3)
         lib.oracle_qkv_append.restype = ci
+        lib.oracle_prefill_append.argtypes = ([ci] * 7 + [u16p] * 5 + [i32p] * 4 + [u16p]
+                                              + [_D] * 2 + [dp] * 2)
+        lib.oracle_prefill_append.restype = ci
+        lib.oracle_prefill_attention.argtypes = ([ci] * 7 + [u16p] + [i32p] * 3 + [dp, _D]
+                                                 + [dp] * 2)
+        lib.oracle_prefill_attention.restype = ci
         self.lib = lib
         self.path = path
 
@@ -282,6 +288,46 @@ class Oracle:
         return res
 
 
+    # ------------------------------------------------------------- prefill
+    def prefill_append(self, q, k, v, w_q, w_k, positions, qo_indptr, seq_lens, block_table,
+                       pool, rope_theta: float, eps: float):
+        """Norm, rotation and append of a chunk of tokens per sequence.
+        q [T][Hq][D], k/v [T][Hkv][D] (bf16 as uint16), positions [T],
+        qo_indptr [B+1], seq_lens [B] (after the chunk); ``pool`` updated in
+        place.  Returns double arrays q_rot [T][Hq][D], k_rot [T][Hkv][D]."""
+        q, k, v, w_q, w_k = _u16(q), _u16(k), _u16(v), _u16(w_q), _u16(w_k)
+        pos, qo, sl, bt = _i32(positions), _i32(qo_indptr), _i32(seq_lens), _i32(block_table)
+        assert pool.dtype == np.uint16 and pool.flags["C_CONTIGUOUS"]
+        T, Hq, D = q.shape
+        num_pages, _, Hkv, P, D2 = pool.shape
+        B = sl.shape[0]
+        assert D2 == D and k.shape == (T, Hkv, D) and v.shape == (T, Hkv, D)
+        assert qo.shape == (B + 1,) and pos.shape == (T,) and qo[-1] == T
+        res = {"q_rot": np.empty((T, Hq, D)), "k_rot": np.empty((T, Hkv, D))}
+        _check(self.lib.oracle_prefill_append(
+            B, Hq, Hkv, D, P, num_pages, bt.shape[1],
+            _ptr(q, _U16), _ptr(k, _U16), _ptr(v, _U16), _ptr(w_q, _U16), _ptr(w_k, _U16),
+            _ptr(pos, _I32), _ptr(qo, _I32), _ptr(sl, _I32), _ptr(bt, _I32), _ptr(pool, _U16),
+            float(rope_theta), float(eps), _ptr(res["q_rot"], _D), _ptr(res["k_rot"], _D)))
+        return res
+
+    def prefill_attention(self, pool, block_table, qo_indptr, seq_lens, q_rot, scale: float):
+        """Causal paged attention of the chunk rows q_rot (double [T][Hq][D]).
+        Returns (out [T][Hq][D], lse [T][Hq]), both double."""
+        pool, bt, qo, sl, q = (_u16(pool), _i32(block_table), _i32(qo_indptr), _i32(seq_lens),
+                               _f64(q_rot))
+        B = sl.shape[0]
+        assert qo.shape == (B + 1,) and qo[-1] == q.shape[0]
+        num_pages, _, Hkv, P, D = pool.shape
+        out = np.empty(q.shape, np.float64)
+        lse = np.empty(q.shape[:2], np.float64)
+        _check(self.lib.oracle_prefill_attention(
+            B, q.shape[1], Hkv, D, P, num_pages, bt.shape[1], _ptr(pool, _U16), _ptr(bt, _I32),
+            _ptr(qo, _I32), _ptr(sl, _I32), _ptr(q, _D), float(scale), _ptr(out, _D),
+            _ptr(lse, _D)))
+        return out, lse
+
+
 _default = None
 
 
@@ -333,3 +379,11 @@ def decode_layer_fp8(*args, **kwargs):
 
 def qkv_append(*args, **kwargs):
     return default().qkv_append(*args, **kwargs)
+
+
+def prefill_append(*args, **kwargs):
+    return default().prefill_append(*args, **kwargs)
+
+
+def prefill_attention(pool, block_table, qo_indptr, seq_lens, q_rot, scale):
+    return default().prefill_attention(pool, block_table, qo_indptr, seq_lens, q_rot, scale)

@@ -26,6 +26,14 @@
  *   split/merge -- blog part 8: one head's KV sequence is cut into parts,
  *               each part gets a local softmax, the parts are then reduced.
  *               The reduction is the exact log-sum-exp merge.
+ *   prefill   -- engine article, section 4.4.1 (FlashAttention-2 prefill):
+ *               a chunk of new tokens per sequence is normed, rotated and
+ *               appended like the decode token, then every chunk query row
+ *               attends causally (keys at or before its own index); the
+ *               blockwise computation there is exact, so the oracle is plain
+ *               causal softmax attention.  Its printed loop takes a softmax
+ *               per key block and adds the blocks, which is not attention;
+ *               the plain reading is taken.
  *   QKV projection -- engine article, section 4.4.3 (fused QKV): one merged
  *               matrix W [(Hq + 2 Hkv) D][hidden] (rows: the q heads, then the
  *               k heads, then the v heads) gives qkv = W x for each sequence;
@@ -631,4 +639,124 @@ int oracle_qkv_append(int B, int Hq, int Hkv, int D, int P, int num_pages, int m
     free(wq);
     free(wk);
     return rc;
+}
+
+/* ------------------------------------------------------------- prefill -- */
+
+/* A chunk of new tokens per sequence (chunked prefill): sequence b brings
+ * n_b = qo_indptr[b+1] - qo_indptr[b] tokens, packed as rows
+ * qo_indptr[b] .. qo_indptr[b+1]-1 of q, k, v; they become tokens
+ * L_b - n_b .. L_b - 1 of the sequence (L_b = seq_lens[b], counted after the
+ * chunk).  Validates the chunk layout: -2 if qo_indptr[0] != 0, a chunk is
+ * negative or longer than its sequence, or L_b is outside [1, max_blocks*P]. */
+static int prefill_check(int B, int P, int max_blocks, const int32_t *qo_indptr,
+                         const int32_t *seq_lens)
+{
+    if (qo_indptr[0] != 0)
+        return -2;
+    for (int b = 0; b < B; ++b) {
+        int n = qo_indptr[b + 1] - qo_indptr[b], L = seq_lens[b];
+        if (n < 0 || L < 1 || L > max_blocks * P || n > L)
+            return -2;
+    }
+    return 0;
+}
+
+/* Steps 1-2 for every chunk token (row r of sequence b, index
+ * t = L_b - n_b + (r - qo_indptr[b])): RMSNorm and NeoX RoPE at positions[r]
+ * of its q rows and k rows, then slot t of sequence b receives bf16(k_rot)
+ * (one round-to-nearest-even) and v (bits copied).
+ *   q [T][Hq][D], k,v [T][Hkv][D], positions [T] (T = qo_indptr[B]);
+ *   outputs q_rot [T][Hq][D], k_rot [T][Hkv][D] (double, unrounded). */
+int oracle_prefill_append(int B, int Hq, int Hkv, int D, int P, int num_pages, int max_blocks,
+                          const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                          const uint16_t *w_q, const uint16_t *w_k, const int32_t *positions,
+                          const int32_t *qo_indptr, const int32_t *seq_lens,
+                          const int32_t *block_table, uint16_t *pool, double rope_theta,
+                          double eps, double *q_rot, double *k_rot)
+{
+    if (Hkv < 1 || Hq % Hkv != 0 || D % 2 != 0)
+        return -4;
+    int rc = prefill_check(B, P, max_blocks, qo_indptr, seq_lens);
+    if (rc)
+        return rc;
+    oracle_dims d = {B, Hq, Hkv, D, P, num_pages, max_blocks};
+    double *x = (double *)malloc(sizeof(double) * (size_t)D);
+    double *xn = (double *)malloc(sizeof(double) * (size_t)D);
+    double *wq = (double *)malloc(sizeof(double) * (size_t)D);
+    double *wk = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int i = 0; i < D; ++i) {
+        wq[i] = oracle_bf16_to_double(w_q[i]);
+        wk[i] = oracle_bf16_to_double(w_k[i]);
+    }
+    for (int b = 0; b < B && rc == 0; ++b) {
+        int n = qo_indptr[b + 1] - qo_indptr[b], L = seq_lens[b];
+        for (int j = 0; j < n && rc == 0; ++j) {
+            int r = qo_indptr[b] + j, t = L - n + j;
+            double pos = (double)positions[r];
+            for (int h = 0; h < Hq; ++h) {
+                long o = ((long)r * Hq + h) * D;
+                for (int i = 0; i < D; ++i)
+                    x[i] = oracle_bf16_to_double(q[o + i]);
+                oracle_rmsnorm(x, wq, D, eps, xn);
+                oracle_rope_neox(xn, D, pos, rope_theta, q_rot + o);
+            }
+            for (int h = 0; h < Hkv; ++h) {
+                long o = ((long)r * Hkv + h) * D;
+                for (int i = 0; i < D; ++i)
+                    x[i] = oracle_bf16_to_double(k[o + i]);
+                oracle_rmsnorm(x, wk, D, eps, xn);
+                oracle_rope_neox(xn, D, pos, rope_theta, k_rot + o);
+                long rk = pool_row(&d, block_table, b, t, 0, h);
+                long rv = pool_row(&d, block_table, b, t, 1, h);
+                if (rk < 0 || rv < 0) {
+                    rc = -1;
+                    break;
+                }
+                for (int i = 0; i < D; ++i) {
+                    pool[rk + i] = oracle_double_to_bf16(k_rot[o + i]);
+                    pool[rv + i] = v[o + i];
+                }
+            }
+        }
+    }
+    free(x);
+    free(xn);
+    free(wq);
+    free(wk);
+    return rc;
+}
+
+/* Step 4 for the chunk: causal attention.  Query row r of sequence b (chunk
+ * token at index t = L_b - n_b + (r - qo_indptr[b])) attends over tokens
+ * 0..t of its sequence, i.e. attend_range(.., 0, t + 1) with its KV head
+ * g = h / (Hq / Hkv) -- engine article, 4.4.1 (blockwise causal prefill
+ * attention: a query block sees only keys at or before it; computed by
+ * blocks it is exactly this softmax attention).
+ *   q_rot [T][Hq][D] double; out [T][Hq][D]; lse [T][Hq]. */
+int oracle_prefill_attention(int B, int Hq, int Hkv, int D, int P, int num_pages,
+                             int max_blocks, const uint16_t *pool, const int32_t *block_table,
+                             const int32_t *qo_indptr, const int32_t *seq_lens,
+                             const double *q_rot, double scale, double *out, double *lse)
+{
+    if (Hkv < 1 || Hq % Hkv != 0)
+        return -4;
+    int rc = prefill_check(B, P, max_blocks, qo_indptr, seq_lens);
+    if (rc)
+        return rc;
+    oracle_dims d = {B, Hq, Hkv, D, P, num_pages, max_blocks};
+    int G = Hq / Hkv;
+    for (int b = 0; b < B; ++b) {
+        int n = qo_indptr[b + 1] - qo_indptr[b], L = seq_lens[b];
+        for (int j = 0; j < n; ++j) {
+            int r = qo_indptr[b] + j, t = L - n + j;
+            for (int h = 0; h < Hq; ++h) {
+                long o = ((long)r * Hq + h) * D;
+                if (attend_range(&d, pool, block_table, b, h / G, q_rot + o, scale, 0, t + 1,
+                                 out + o, lse + (long)r * Hq + h))
+                    return -1;
+            }
+        }
+    }
+    return 0;
 }

@@ -651,4 +651,125 @@ def pin_qkv_append_one_slot(orc):
     assert np.array_equal(pb.pool[~changed], before[~changed]), "append touched another slot"
 
 
+# --------------------------------------------------------------- prefill --
+# A chunk of n_b new tokens per sequence, packed by qo_indptr; chunk token j
+# of sequence b is token t = L_b - n_b + j (L_b counted after the chunk).
+
+def _prefill_problem(rng, seq_lens, chunks, Hq=8, Hkv=2, D=16, P=4, pos_offset=0):
+    pb = Paged(rng, seq_lens, Hq=Hq, Hkv=Hkv, D=D, P=P, extra_pages=4)
+    qo = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    T = int(qo[-1])
+    q = random_bits(rng, (T, Hq, D))
+    k = random_bits(rng, (T, Hkv, D))
+    v = random_bits(rng, (T, Hkv, D))
+    wq = bits_of((rng.integers(2, 6, D) / 4).astype(np.float32))
+    wk = bits_of((rng.integers(2, 6, D) / 4).astype(np.float32))
+    idx = np.concatenate([np.arange(L - n, L) for L, n in zip(seq_lens, chunks)]).astype(np.int32)
+    return pb, qo, q, k, v, wq, wk, idx + pos_offset, idx
+
+
+def pin_prefill_attention_dense_causal(orc):
+    """Brute force on tiny inputs: gather each sequence's K and V densely and
+    take softmax(q K^T / sqrt(D) + causal mask) V with numpy/scipy; chunk row
+    j of sequence b sees keys 0 .. L_b - n_b + j."""
+    rng = np.random.default_rng(31)
+    seq_lens, chunks = [5, 9, 13, 4], [5, 3, 6, 1]
+    pb, qo, *_ = _prefill_problem(rng, seq_lens, chunks)
+    T = int(qo[-1])
+    q_rot = rng.standard_normal((T, 8, 16))
+    out, lse = orc.prefill_attention(pb.pool, pb.bt, qo, pb.seq_lens, q_rot, 0.25)
+    for b, (L, n) in enumerate(zip(seq_lens, chunks)):
+        for h in range(8):
+            K, V = pb.gather(b, 0, h // 4), pb.gather(b, 1, h // 4)
+            Q = q_rot[qo[b]:qo[b + 1], h]
+            S = 0.25 * Q @ K.T
+            mask = np.arange(L)[None, :] > (L - n + np.arange(n))[:, None]
+            S[mask] = -np.inf
+            _close(out[qo[b]:qo[b + 1], h], scipy.special.softmax(S, axis=1) @ V, 1e-12,
+                   "causal out")
+            _close(lse[qo[b]:qo[b + 1], h], scipy.special.logsumexp(S, axis=1), 1e-12,
+                   "causal lse")
+
+
+def pin_prefill_last_token_equals_decode(orc):
+    """The chunk's last row attends to the whole sequence: the (pinned)
+    decode attention of that row, bit for bit."""
+    rng = np.random.default_rng(32)
+    seq_lens, chunks = [7, 12, 3], [2, 5, 3]
+    pb, qo, *_ = _prefill_problem(rng, seq_lens, chunks)
+    q_rot = rng.standard_normal((int(qo[-1]), 8, 16))
+    out, lse = orc.prefill_attention(pb.pool, pb.bt, qo, pb.seq_lens, q_rot, 0.3)
+    last = qo[1:] - 1
+    ref_out, ref_lse = orc.attention(pb.pool, pb.bt, pb.seq_lens,
+                                     np.ascontiguousarray(q_rot[last]), 0.3)
+    assert np.array_equal(out[last], ref_out) and np.array_equal(lse[last], ref_lse)
+
+
+def pin_prefill_fresh_sequence_first_token_is_v(orc):
+    """A sequence with no cached prefix (n_b = L_b): its first row attends
+    only to token 0, so out = V_0 exactly and lse = the single score."""
+    rng = np.random.default_rng(33)
+    pb, qo, *_ = _prefill_problem(rng, [6, 8], [6, 3])
+    q_rot = rng.standard_normal((int(qo[-1]), 8, 16))
+    out, lse = orc.prefill_attention(pb.pool, pb.bt, qo, pb.seq_lens, q_rot, 0.25)
+    for h in range(8):
+        V0, K0 = pb.gather(0, 1, h // 4)[0], pb.gather(0, 0, h // 4)[0]
+        _close(out[0, h], V0, 0.0, "first token out = v0")
+        _close([lse[0, h]], [0.25 * q_rot[0, h] @ K0], 1e-12, "first token lse")
+
+
+def pin_prefill_append_slots_and_rows(orc):
+    """Norm and rotation of every chunk row at its own position (both
+    pinned per row; positions differ from the token index here), and exactly
+    the chunk's slots L-n .. L-1 change: K = bf16(k_rot), V = v's bits."""
+    rng = np.random.default_rng(34)
+    seq_lens, chunks = [5, 9, 13, 4], [5, 3, 6, 1]
+    pb, qo, q, k, v, wq, wk, pos, idx = _prefill_problem(rng, seq_lens, chunks, pos_offset=7)
+    before = pb.pool.copy()
+    res = orc.prefill_append(q, k, v, wq, wk, pos, qo, pb.seq_lens, pb.bt, pb.pool, 1e6, 1e-6)
+    changed = np.zeros(before.shape, bool)
+    for b in range(len(seq_lens)):
+        for r in range(qo[b], qo[b + 1]):
+            for h in range(8):
+                want = orc.rope_neox(orc.rmsnorm(f64(q[r, h]), f64(wq), 1e-6), pos[r], 1e6)
+                _close(res["q_rot"][r, h], want, 0.0, "prefill q_rot")
+            page, off = pb.bt[b, idx[r] // 4], idx[r] % 4
+            for g in range(2):
+                want = orc.rope_neox(orc.rmsnorm(f64(k[r, g]), f64(wk), 1e-6), pos[r], 1e6)
+                _close(res["k_rot"][r, g], want, 0.0, "prefill k_rot")
+                assert np.array_equal(pb.pool[page, 0, g, off], orc.f64_to_bf16_bits(want))
+                assert np.array_equal(pb.pool[page, 1, g, off], v[r, g])
+            changed[page, :, :, off] = True
+    assert np.array_equal(pb.pool[~changed], before[~changed]), "append touched another slot"
+
+
+def pin_prefill_chunk_of_one_is_the_decode_step(orc):
+    """One new token per sequence: prefill append + attention is the
+    (pinned) decode layer-step, bit for bit."""
+    rng = np.random.default_rng(35)
+    seq_lens = [3, 17, 31]
+    pb, qo, q, k, v, wq, wk, pos, _ = _prefill_problem(rng, seq_lens, [1, 1, 1])
+    pool_a, pool_b = pb.pool.copy(), pb.pool.copy()
+    res = orc.prefill_append(q, k, v, wq, wk, pos, qo, pb.seq_lens, pb.bt, pool_a, 1e6, 1e-6)
+    out, lse = orc.prefill_attention(pool_a, pb.bt, qo, pb.seq_lens, res["q_rot"], 0.25)
+    ref = orc.decode_layer(q, k, v, wq, wk, pos, pb.seq_lens, pb.bt, pool_b, 1e6, 1e-6)
+    assert np.array_equal(pool_a, pool_b) and np.array_equal(out, ref["out"])
+    assert np.array_equal(lse, ref["lse"]) and np.array_equal(res["q_rot"], ref["q_rot"])
+
+
+def pin_prefill_rejects_bad_chunks(orc):
+    """A chunk longer than its sequence, a negative chunk or qo_indptr not
+    starting at 0 is an error, not a silent read outside the sequence."""
+    rng = np.random.default_rng(36)
+    pb, qo, *_ = _prefill_problem(rng, [5, 9], [2, 3])
+    for bad in ([0, 6, 9], [0, 2, 1], [1, 3, 5]):     # too long, negative, offset start
+        q_rot = rng.standard_normal((bad[-1], 8, 16))
+        try:
+            orc.prefill_attention(pb.pool, pb.bt, np.array(bad, np.int32), pb.seq_lens, q_rot,
+                                  0.25)
+        except OracleError:
+            continue
+        raise AssertionError(f"qo_indptr {bad} accepted")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

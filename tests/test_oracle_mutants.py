@@ -73,6 +73,20 @@ MUTANTS = [
      "oracle_rmsnorm(qkv + (long)h * D, wk, D, eps, xn);"),
     ("qkv value slot perturbed", "pool[rv + i] = oracle_double_to_bf16(v_out[o + i]);",
      "pool[rv + i] = oracle_double_to_bf16(v_out[o + i] * 1.001);"),
+    ("prefill query excludes itself", "scale, 0, t + 1,", "scale, 0, t > 0 ? t : 1,"),
+    ("prefill not causal", "scale, 0, t + 1,", "scale, 0, L,"),
+    ("prefill causal window from the chunk start", "scale, 0, t + 1,",
+     "scale, L - n, t + 1,"),
+    ("prefill chunk index ignores the cached prefix", "int r = qo_indptr[b] + j, t = L - n + j;",
+     "int r = qo_indptr[b] + j, t = j;"),
+    ("prefill rope at the token index", "double pos = (double)positions[r];",
+     "double pos = (double)(L - n + j);"),
+    ("prefill gqa head mapping", "b, h / G, q_rot + o, scale, 0, t + 1,",
+     "b, h % Hkv, q_rot + o, scale, 0, t + 1,"),
+    ("prefill chunk longer than its sequence accepted", "if (n < 0 || L < 1 || L > max_blocks * P || n > L)",
+     "if (n < 0 || L < 1 || L > max_blocks * P)"),
+    ("prefill v row of the previous token", "pool[rv + i] = v[o + i];\n                }\n            }\n        }\n    }",
+     "pool[rv + i] = v[o > D ? o - D : o + i];\n                }\n            }\n        }\n    }"),
 ]
 
 
