@@ -29,7 +29,8 @@ def _sources():
 
 
 def _inputs():
-    return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.h"))) + [
+    return _sources() + sorted(glob.glob(os.path.join(CSRC, "*.h"))) + sorted(
+        glob.glob(os.path.join(CSRC, "*.cuh"))) + [
         os.path.join(INCLUDE, "qdec.h"), os.path.abspath(__file__)]
 
 

@@ -88,6 +88,8 @@ struct Params {
     int qkv_stages;          // QKV projection: ring depth
     int qkv_boxes;           // QKV projection: 64-element blocks along hidden per stage
     const __nv_bfloat16 *w_packed;  // QKV projection: the weight in the packed order
+    const int32_t *qo_indptr;  // prefill: [B+1] packed chunk rows of each sequence
+    int T;                     // prefill: rows the caller's buffers hold (qo_indptr[B] <= T)
     double inv_freq[kRotPairs];  // rope_theta^(-2i/D), i < D/2
 };
 
@@ -117,6 +119,11 @@ enum AttnMode : int { kAttnSplit = 0, kAttnFused = 1, kAttnDecode = 2 };
 cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, AttnMode mode, bool fp8,
                              cudaStream_t s);
 cudaError_t launch_merge(const Params &p, cudaStream_t s);
+
+// Chunked prefill (qdec_prefill.cu): steps 1-3 for every chunk row, and the
+// causal paged attention of the chunk (kv_map: the bf16 pool's page-tile map).
+cudaError_t launch_prefill_append(const Params &p, cudaStream_t s);
+cudaError_t launch_prefill_attention(const Params &p, const CUtensorMap &kv_map, cudaStream_t s);
 
 // The merged QKV projection fused with steps 1-3 (qdec_qkv.cu): the weight
 // comes packed (qdec_qkv_pack_weights), x_map views x [B][hidden] with boxes

@@ -1,0 +1,482 @@
+// qdec_prefill.cu -- chunked prefill over the paged pool, on sm_103a.
+//
+// A chunk of n_b new tokens per sequence (packed rows qo_indptr[b] ..
+// qo_indptr[b+1]-1; they become tokens L_b - n_b .. L_b - 1 of the sequence,
+// L_b = seq_lens[b] counted after the chunk):
+//
+// prefill_append_kernel -- steps 1-3 for every chunk token: RMSNorm and NeoX
+//   RoPE (at positions[row]) of its query rows into q_rot (fp32) and of its
+//   key rows, then bf16(k_rot) and v into slot L_b - n_b + j of the pool.
+//   One CTA per (token, KV head): warp w norms and rotates query head
+//   4 g + w; warp 0 the key row, warp 1 copies the value row.
+//
+// prefill_attention_kernel -- causal paged attention of the chunk (article
+//   "扔掉 vLLM！从零构建 Qwen3-8B 推理引擎" (news.rkmt.cn), section 4.4.1:
+//   FlashAttention-2 prefill, the queries in blocks that each see only the
+//   keys at or before them, never forming the whole score matrix).  One CTA
+//   per (sequence, KV head, block of 16 chunk tokens), the blocks with the
+//   most keys first.  A producer warp streams the sequence's page tiles (K
+//   and V of one page and KV head, 8 KiB, one TMA box) up to the block's last
+//   query into a ring; each of the four consumer warps owns one query head
+//   of the group for the block's 16 tokens and, per tile, forms S = Q K^T
+//   with mma.sync (q as bf16 hi + lo, ~16-bit mantissa), masks keys after
+//   each query, keeps the online softmax in fp32 (log2 units) and adds
+//   P V with P taken straight from the score accumulators as bf16.
+#include "qdec_internal.h"
+#include "qdec_ptx.cuh"
+#include "qdec.h"
+
+#include <math.h>
+
+#include <mutex>
+
+namespace qdec {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kPfRows = 16;                 // chunk tokens per work unit (one m16 tile)
+constexpr int kPfStages = 8;                // page tiles in flight per CTA
+constexpr int kPfRingBytes = kPfStages * kTileBytes;
+// after the ring: full[8], empty[8], slot_ok[8], the abort flag, the unit
+constexpr int kPfSmemBytes = kPfRingBytes + 2 * kPfStages * 8 + kPfStages * 4 + 16 + 1024;
+
+__device__ __forceinline__ void flag_error(int32_t *err, int bits) {
+    if (err) atomicOr(err, bits);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
+// The sequence b with qo[b] <= r < qo[b+1] when qo is a valid layout (binary
+// search; always in [0, B)).
+__device__ int seq_of_row(const int32_t *qo, int B, int r) {
+    int lo = 0, hi = B;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (qo[mid] <= r)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+// Whether sequence b's chunk is well formed: 0 <= n <= L <= max_blocks * P,
+// L >= 1, rows inside [0, T).
+__device__ __forceinline__ bool chunk_ok(const Params &p, int b, int &n, int &L) {
+    const int q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
+    n = q1 - q0;
+    L = p.seq_lens[b];
+    return q0 >= 0 && q1 <= p.T && n >= 0 && L >= 1 && L <= p.max_blocks * kPageSize && n <= L;
+}
+
+// ------------------------------------------------------------------ append --
+__global__ void __launch_bounds__(128) prefill_append_kernel(const __grid_constant__ Params p) {
+    const int r = blockIdx.x, g = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = seq_of_row(p.qo_indptr, p.B, r);
+    int n, L;
+    if (!chunk_ok(p, b, n, L) || r < p.qo_indptr[b] || r >= p.qo_indptr[b + 1]) {
+        if (threadIdx.x == 0 && g == 0) flag_error(p.err, QDEC_FLAG_BAD_SEQLEN);
+        return;  // uniform over the CTA
+    }
+    const int t = L - n + (r - p.qo_indptr[b]);  // token index in the sequence
+    const int pos = p.positions[r];
+    // this lane's rotate-half pairs i = 2 lane, 2 lane + 1: dims i and i + 64;
+    // the angle pos * theta^(-2i/D), its cos and sin in double
+    double cs[2], sn[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+        sincos(static_cast<double>(pos) * p.inv_freq[2 * lane + e], &sn[e], &cs[e]);
+    // RMSNorm (eps inside the root) and rotation of one 128-dim row: y holds
+    // dims 2 lane, 2 lane + 1, 64 + 2 lane, 64 + 2 lane + 1.  x w is exact in
+    // fp32 (a product of two bf16); the rotation's difference is formed in
+    // double, so a result near zero keeps its relative accuracy (the only
+    // error left is the fp32 root, relative to the whole row), which keeps the
+    // key within one bf16 step of the exact value.
+    auto norm_rotate = [&](const __nv_bfloat16 *x, const __nv_bfloat16 *w, float (&y)[4]) {
+        const float2 a = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(x)[lane]);
+        const float2 c = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(x + 64)[lane]);
+        const float ss = warp_sum(a.x * a.x + a.y * a.y + c.x * c.x + c.y * c.y);
+        const double rn = static_cast<double>(rsqrtf(ss * (1.0f / kHeadDim) + p.eps));
+        const float2 wa = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(w)[lane]);
+        const float2 wc = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(w + 64)[lane]);
+        const double n1a = a.x * wa.x, n1b = a.y * wa.y;  // exact products
+        const double n2a = c.x * wc.x, n2b = c.y * wc.y;
+        y[0] = static_cast<float>(rn * (n1a * cs[0] - n2a * sn[0]));
+        y[1] = static_cast<float>(rn * (n1b * cs[1] - n2b * sn[1]));
+        y[2] = static_cast<float>(rn * (n2a * cs[0] + n1a * sn[0]));
+        y[3] = static_cast<float>(rn * (n2b * cs[1] + n1b * sn[1]));
+    };
+    {
+        const int h = g * kGroup + warp;
+        float y[4];
+        norm_rotate(p.q + static_cast<int64_t>(r) * p.q_stride + h * kHeadDim, p.w_q, y);
+        float *dst = p.q_rot_out + (static_cast<int64_t>(r) * p.Hq + h) * kHeadDim;
+        reinterpret_cast<float2 *>(dst)[lane] = make_float2(y[0], y[1]);
+        reinterpret_cast<float2 *>(dst + 64)[lane] = make_float2(y[2], y[3]);
+    }
+    if (warp >= 2) return;
+    const int page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + t / kPageSize];
+    if (page < 0 || page >= p.num_pages) {
+        if (lane == 0 && warp == 0) flag_error(p.err, QDEC_FLAG_BAD_PAGE);
+        return;
+    }
+    const int64_t slot =
+        ((static_cast<int64_t>(page) * 2 * p.Hkv + g) * kPageSize + t % kPageSize) * kHeadDim;
+    if (warp == 0) {
+        float y[4];
+        norm_rotate(p.k + static_cast<int64_t>(r) * p.k_stride + g * kHeadDim, p.w_k, y);
+        uint32_t *kd = reinterpret_cast<uint32_t *>(p.pool + slot);
+        kd[lane] = pack_bf16x2(y[0], y[1]);
+        kd[32 + lane] = pack_bf16x2(y[2], y[3]);
+    } else {
+        const uint32_t *vs = reinterpret_cast<const uint32_t *>(
+            p.v + static_cast<int64_t>(r) * p.v_stride + g * kHeadDim);
+        uint32_t *vd = reinterpret_cast<uint32_t *>(
+            p.pool + slot + static_cast<int64_t>(p.Hkv) * kPageSize * kHeadDim);
+        vd[lane] = vs[lane];
+        vd[32 + lane] = vs[32 + lane];
+    }
+}
+
+// --------------------------------------------------------------- attention --
+// One page tile (K and V of one page and KV head, 8 KiB): the pool's 5-D
+// tensor map (64 dims, 16 tokens, 2 halves of D, K/V plane, page*2*Hkv +
+// head) lands it as [plane][half][token][64 dims], 128-byte rows swizzled by
+// (token % 8).
+__device__ __forceinline__ void tma_load_page_tile(uint32_t dst, const CUtensorMap *map,
+                                                   int plane_row, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %2, %2, %2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(plane_row), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory address of token `tok`, 16-byte chunk `c` (dims 8c .. 8c+7,
+// c < 16) of plane `plane` of the tile at `tile`.
+__device__ __forceinline__ uint32_t tile_addr(uint32_t tile, int plane, int tok, int c) {
+    return tile + plane * kPlaneBytes + (c >> 3) * kTileHalfBytes + tok * 128 +
+           (((c & 7) ^ (tok & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    prefill_attention_kernel(const __grid_constant__ CUtensorMap kv_map,
+                             const __grid_constant__ Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint8_t *tail = sm + kPfRingBytes;
+    const uint32_t full0 = smem_u32(tail);
+    const uint32_t empty0 = full0 + kPfStages * 8;
+    volatile int *slot_ok = reinterpret_cast<volatile int *>(tail + 2 * kPfStages * 8);
+    volatile int *misc = reinterpret_cast<volatile int *>(tail + 2 * kPfStages * 8 + kPfStages * 4);
+    // misc: [0] abort, [1] sequence, [2] query block, [3] pages issued
+    const int g = blockIdx.x % p.Hkv;
+    const int unit = blockIdx.x / p.Hkv;
+
+    // ---- which (sequence, block) this CTA takes: units enumerate every
+    // sequence's blocks from its last (most keys) to its first
+    if (warp == 0) {
+        const int per = (p.B + 31) / 32;
+        int cnt = 0;
+        for (int i = 0; i < per; ++i) {
+            const int b = lane * per + i;
+            int n, L;
+            if (b < p.B && chunk_ok(p, b, n, L)) cnt += (n + kPfRows - 1) / kPfRows;
+        }
+        int incl = cnt;  // inclusive prefix over the lanes
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const int excl = incl - cnt;
+        if (lane == 0) misc[1] = -1;
+        __syncwarp();
+        if (unit >= excl && unit < incl) {
+            int k = unit - excl;
+            for (int i = 0; i < per; ++i) {
+                const int b = lane * per + i;
+                int n, L;
+                if (b >= p.B || !chunk_ok(p, b, n, L)) continue;
+                const int nb = (n + kPfRows - 1) / kPfRows;
+                if (k < nb) {
+                    misc[1] = b;
+                    misc[2] = nb - 1 - k;
+                    break;
+                }
+                k -= nb;
+            }
+        }
+        if (blockIdx.x == 0) {  // report malformed chunks once
+            for (int b = lane; b < p.B; b += 32) {
+                int n, L;
+                if (!chunk_ok(p, b, n, L)) flag_error(p.err, QDEC_FLAG_BAD_SEQLEN);
+            }
+        }
+        if (tid == 0) {
+            for (int s = 0; s < kPfStages; ++s) {
+                mbar_init(full0 + 8 * s, 1);
+                mbar_init(empty0 + 8 * s, kConsumerWarps);  // every warp reads every tile
+            }
+            misc[0] = 0;
+            misc[3] = 0;
+            fence_mbar_init();
+        }
+    }
+    __syncthreads();
+    const int b = misc[1];
+    if (b < 0) return;  // no unit for this CTA (the grid is an upper bound)
+    const int qb = misc[2];
+    int n, L;
+    chunk_ok(p, b, n, L);
+    const int row0 = p.qo_indptr[b] + qb * kPfRows;             // first packed row
+    const int nrows = min(kPfRows, n - qb * kPfRows);           // rows of this block
+    const int t0 = L - n + qb * kPfRows;                        // token index of row 0
+    const int npages = (t0 + nrows - 1) / kPageSize + 1;        // pages up to the last query
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------ TMA producer --
+        uint32_t i = 0;
+        bool stop = false;
+        for (int base = 0; base < npages && !stop; base += 32) {
+            int page = -1;
+            if (base + lane < npages)
+                page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + base + lane];
+            const int cnt = min(32, npages - base);
+            for (int j = 0; j < cnt; ++j, ++i) {
+                const int pj = __shfl_sync(kFull, page, j);
+                if (lane == 0) {
+                    const int slot = i % kPfStages;
+                    const uint32_t full = full0 + 8 * slot;
+                    if (misc[0]) {
+                        stop = true;
+                    } else if (i >= static_cast<uint32_t>(kPfStages) &&
+                               !mbar_wait_bounded(empty0 + 8 * slot, ((i / kPfStages) - 1) & 1,
+                                                  misc, p.wait_cycles)) {
+                        misc[0] = 1;
+                        flag_error(p.err, QDEC_FLAG_TIMEOUT);
+                        stop = true;
+                    } else if (pj >= 0 && pj < p.num_pages) {
+                        slot_ok[slot] = 1;
+                        mbar_arrive_expect_tx(full, kTileBytes);
+                        tma_load_page_tile(smem_u32(sm + slot * kTileBytes), &kv_map,
+                                           pj * 2 * p.Hkv + g, full);
+                    } else {
+                        slot_ok[slot] = 0;
+                        flag_error(p.err, QDEC_FLAG_BAD_PAGE);
+                        mbar_arrive(full);
+                    }
+                }
+                stop = __shfl_sync(kFull, stop, 0);
+                if (stop) break;
+            }
+        }
+        if (lane == 0) misc[3] = static_cast<int>(i);
+    } else {
+        // ------------------------------------------- consumer warps --
+        const int h = g * kGroup + warp;
+        const int gq = lane >> 2, tq = lane & 3;  // fragment row group, column pair
+        // Q fragments (A of m16n8k16, 16 tokens x 128 dims in 8 k-steps),
+        // scaled to log2 units, as bf16 hi + lo
+        uint32_t qh[8][4], ql[8][4];
+        {
+            const float *q0 = p.q_rot_in + (static_cast<int64_t>(row0 + gq) * p.Hq + h) * kHeadDim;
+            const float *q1 = q0 + 8 * static_cast<int64_t>(p.Hq) * kHeadDim;
+            const bool v0 = gq < nrows, v1 = gq + 8 < nrows;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float *src = (e & 1) ? q1 : q0;
+                    const bool valid = (e & 1) ? v1 : v0;
+                    const int col = 16 * kk + 2 * tq + ((e >> 1) << 3);
+                    float2 x = valid ? *reinterpret_cast<const float2 *>(src + col)
+                                     : make_float2(0.f, 0.f);
+                    x.x *= p.qscale;
+                    x.y *= p.qscale;
+                    const __nv_bfloat16 hx = __float2bfloat16_rn(x.x), hy = __float2bfloat16_rn(x.y);
+                    qh[kk][e] = static_cast<uint32_t>(__bfloat16_as_ushort(hx)) |
+                                (static_cast<uint32_t>(__bfloat16_as_ushort(hy)) << 16);
+                    ql[kk][e] = pack_bf16x2(x.x - __bfloat162float(hx), x.y - __bfloat162float(hy));
+                }
+            }
+        }
+        // the last key each of this thread's two rows may see (causal, and
+        // never past the sequence)
+        const int lim0 = min(t0 + gq, L - 1), lim1 = min(t0 + gq + 8, L - 1);
+        float o[16][4];
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        const int mi = lane >> 3, r8 = lane & 7;
+        bool aborted = false;
+        for (int pg = 0; pg < npages; ++pg) {
+            const int slot = pg % kPfStages;
+            if (!mbar_wait_bounded(full0 + 8 * slot, (pg / kPfStages) & 1, misc, p.wait_cycles)) {
+                if (lane == 0) {
+                    misc[0] = 1;
+                    flag_error(p.err, QDEC_FLAG_TIMEOUT);
+                }
+                aborted = true;
+                break;
+            }
+            if (slot_ok[slot]) {
+                const uint32_t tile = smem_u32(sm + slot * kTileBytes);
+                // ---- S = Q K^T: 16 tokens x 16 keys (two n-tiles of 8 keys)
+                float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    uint32_t kb[4];
+                    // matrices: keys 0-7 / 8-15 (mi >> 1) x dims 16kk.. / 16kk+8.. (mi & 1)
+                    ldmatrix_x4(kb, tile_addr(tile, 0, (mi >> 1) * 8 + r8, 2 * kk + (mi & 1)));
+                    mma_bf16(s[0], qh[kk], kb[0], kb[1]);
+                    mma_bf16(s[0], ql[kk], kb[0], kb[1]);
+                    mma_bf16(s[1], qh[kk], kb[2], kb[3]);
+                    mma_bf16(s[1], ql[kk], kb[2], kb[3]);
+                }
+                // ---- causal mask: key 16 pg + 8 j + 2 tq + e against each row's limit
+                const int kbase = pg * kPageSize + 2 * tq;
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int key = kbase + 8 * j + e;
+                        if (key > lim0) s[j][e] = -INFINITY;
+                        if (key > lim1) s[j][2 + e] = -INFINITY;
+                    }
+                }
+                // ---- online softmax (log2 units), rows gq and gq + 8
+                float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+                float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+#pragma unroll
+                for (int off = 1; off < 4; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
+                }
+                const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+                // a row that has seen no key yet keeps m = -inf, weights 0
+                const float a0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
+                const float a1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+                float pw[2][4];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        pw[j][e] = n0 == -INFINITY ? 0.f : exp2f(s[j][e] - n0);
+                        pw[j][2 + e] = n1 == -INFINITY ? 0.f : exp2f(s[j][2 + e] - n1);
+                    }
+                }
+                l0 = l0 * a0 + pw[0][0] + pw[0][1] + pw[1][0] + pw[1][1];
+                l1 = l1 * a1 + pw[0][2] + pw[0][3] + pw[1][2] + pw[1][3];
+                m0 = n0;
+                m1 = n1;
+#pragma unroll
+                for (int nt = 0; nt < 16; ++nt) {
+                    o[nt][0] *= a0;
+                    o[nt][1] *= a0;
+                    o[nt][2] *= a1;
+                    o[nt][3] *= a1;
+                }
+                // ---- O += P V: P (16 tokens x 16 keys) from the score
+                // accumulators as the A operand; V rows past the sequence
+                // (possibly not finite) are zeroed in the B fragments
+                uint32_t pa[4];
+                pa[0] = pack_bf16x2(pw[0][0], pw[0][1]);
+                pa[1] = pack_bf16x2(pw[0][2], pw[0][3]);
+                pa[2] = pack_bf16x2(pw[1][0], pw[1][1]);
+                pa[3] = pack_bf16x2(pw[1][2], pw[1][3]);
+                const int ntok = min(kPageSize, L - pg * kPageSize);  // keys of this page in the sequence
+                // this thread's B elements hold keys 2 tq, 2 tq + 1 (b0) and +8 (b1)
+                const uint32_t keep0 = (2 * tq < ntok ? 0x0000ffffu : 0u) |
+                                       (2 * tq + 1 < ntok ? 0xffff0000u : 0u);
+                const uint32_t keep1 = (2 * tq + 8 < ntok ? 0x0000ffffu : 0u) |
+                                       (2 * tq + 9 < ntok ? 0xffff0000u : 0u);
+#pragma unroll
+                for (int pr = 0; pr < 8; ++pr) {
+                    uint32_t vb[4];
+                    // matrices: keys 0-7 / 8-15 (mi & 1) x dims 16pr.. / 16pr+8.. (mi >> 1)
+                    ldmatrix_x4_trans(vb, tile_addr(tile, 1, (mi & 1) * 8 + r8, 2 * pr + (mi >> 1)));
+                    mma_bf16(o[2 * pr], pa, vb[0] & keep0, vb[1] & keep1);
+                    mma_bf16(o[2 * pr + 1], pa, vb[2] & keep0, vb[3] & keep1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+        }
+        // ---- normalise and write the block's rows of head h
+#pragma unroll
+        for (int off = 1; off < 4; off <<= 1) {
+            l0 += __shfl_xor_sync(kFull, l0, off);
+            l1 += __shfl_xor_sync(kFull, l1, off);
+        }
+        if (!aborted && !misc[0]) {
+            const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+            __nv_bfloat16 *d0 = p.out + (static_cast<int64_t>(row0 + gq) * p.Hq + h) * kHeadDim;
+            __nv_bfloat16 *d1 = d0 + 8 * static_cast<int64_t>(p.Hq) * kHeadDim;
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt) {
+                const int col = 8 * nt + 2 * tq;
+                if (gq < nrows)
+                    *reinterpret_cast<uint32_t *>(d0 + col) = pack_bf16x2(o[nt][0] * i0, o[nt][1] * i0);
+                if (gq + 8 < nrows)
+                    *reinterpret_cast<uint32_t *>(d1 + col) = pack_bf16x2(o[nt][2] * i1, o[nt][3] * i1);
+            }
+        }
+    }
+    __syncthreads();
+    // a wait that gave up may leave copies in flight: let them land (bounded)
+    if (tid == 0 && misc[0]) {
+        const uint32_t issued = static_cast<uint32_t>(misc[3]);
+        const uint32_t first = issued > static_cast<uint32_t>(kPfStages) ? issued - kPfStages : 0;
+        volatile int never = 0;
+        for (uint32_t t = first; t < issued; ++t)
+            mbar_wait_bounded(full0 + 8 * (t % kPfStages), (t / kPfStages) & 1, &never,
+                              p.wait_cycles);
+    }
+}
+
+std::mutex g_pf_mu;
+bool g_pf_smem_set[64];
+
+}  // namespace
+
+cudaError_t launch_prefill_append(const Params &p, cudaStream_t s) {
+    if (p.T <= 0) return cudaSuccess;
+    prefill_append_kernel<<<dim3(p.T, p.Hkv), 128, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_attention(const Params &p, const CUtensorMap &kv_map, cudaStream_t s) {
+    if (p.T <= 0) return cudaSuccess;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 63;
+    {
+        std::lock_guard<std::mutex> lock(g_pf_mu);
+        if (!g_pf_smem_set[dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(
+                prefill_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmemBytes);
+            if (e != cudaSuccess) return e;
+            g_pf_smem_set[dev] = true;
+        }
+    }
+    // units: at most T / 16 + B blocks of 16 chunk rows, times the KV heads
+    const int64_t units = (static_cast<int64_t>(p.T) + kPfRows - 1) / kPfRows + p.B;
+    prefill_attention_kernel<<<static_cast<unsigned>(units * p.Hkv), kThreads, kPfSmemBytes, s>>>(
+        kv_map, p);
+    return cudaGetLastError();
+}
+
+}  // namespace qdec

@@ -37,6 +37,7 @@ EXPORTS = ("qdec_workspace_bytes", "qdec_workspace_init", "qdec_rope_table_bytes
            "qdec_rope_table", "qdec_append_rope", "qdec_attn_split", "qdec_attn_merge",
            "qdec_attn_decode", "qdec_step", "qdec_qkv_append_rope", "qdec_qkv_pack_weights",
            "qdec_append_rope_fp8", "qdec_attn_split_fp8", "qdec_attn_decode_fp8",
+           "qdec_prefill_append_rope", "qdec_prefill_attn",
            "qdec_step_fp8",
            "qdec_step_static_scratch", "qdec_check_error", "qdec_status_string", "qdec_version")
 
@@ -106,6 +107,11 @@ def _load():
     lib.qdec_attn_merge.restype = st
     lib.qdec_attn_decode.argtypes = [sp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     lib.qdec_attn_decode.restype = st
+    lib.qdec_prefill_append_rope.argtypes = [sp, ctypes.c_int32, vp, i64, vp, i64, vp, i64, vp,
+                                             vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.qdec_prefill_append_rope.restype = st
+    lib.qdec_prefill_attn.argtypes = [sp, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.qdec_prefill_attn.restype = st
     lib.qdec_step.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                               vp, vp, vp]
     lib.qdec_step.restype = st
@@ -215,6 +221,25 @@ def qdec_attn_decode(shape: Shape, q_rot, kv_pool, block_table, seq_lens, worksp
         ctypes.byref(shape.c()), _ptr(q_rot), _ptr(kv_pool), _ptr(block_table), _ptr(seq_lens),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
         _ptr(err_flag), _stream(stream)), "qdec_attn_decode")
+
+
+def qdec_prefill_append_rope(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, qo_indptr,
+                             seq_lens, block_table, kv_pool, q_rot, err_flag=None, stream=None):
+    """Chunk rows q [T][Hq][D], k/v [T][Hkv][D] (row-strided views allowed),
+    positions [T], qo_indptr [B+1]; q_rot [T][Hq][D] float32 out."""
+    _raise(_lib.qdec_prefill_append_rope(
+        ctypes.byref(shape.c()), q.shape[0], _ptr(q), _rows(q, "q"), _ptr(k), _rows(k, "k"),
+        _ptr(v), _rows(v, "v"), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions), _ptr(qo_indptr),
+        _ptr(seq_lens), _ptr(block_table), _ptr(kv_pool), _ptr(q_rot), _ptr(err_flag),
+        _stream(stream)), "qdec_prefill_append_rope")
+
+
+def qdec_prefill_attn(shape: Shape, q_rot, qo_indptr, seq_lens, block_table, kv_pool, out,
+                      err_flag=None, stream=None):
+    _raise(_lib.qdec_prefill_attn(
+        ctypes.byref(shape.c()), q_rot.shape[0], _ptr(q_rot), _ptr(qo_indptr), _ptr(seq_lens),
+        _ptr(block_table), _ptr(kv_pool), _ptr(out), _ptr(err_flag), _stream(stream)),
+        "qdec_prefill_attn")
 
 
 def qdec_attn_merge(shape: Shape, seq_lens, workspace, out, err_flag=None, stream=None):

@@ -338,3 +338,69 @@ def oracle_inputs(w: Workload, layer: int, seqs=None):
         seq_lens=sl.astype(np.int32),
         block_table=bt, pool=np.ascontiguousarray(sub),
         rope_theta=ROPE_THETA, eps=EPS)
+
+
+# ------------------------------------------------------------ chunked prefill --
+
+@dataclass
+class PrefillCase:
+    """A chunked-prefill input: B sequences of seq_lens[b] tokens (after the
+    chunk), the last chunks[b] of them new, packed by qo_indptr."""
+    seq_lens: torch.Tensor      # [B] int32
+    qo_indptr: torch.Tensor     # [B+1] int32
+    positions: torch.Tensor     # [T] int32 (RoPE positions of the chunk rows)
+    block_table: torch.Tensor   # [B][max_blocks] int32
+    pool: torch.Tensor          # [pages][2][Hkv][P][D] bf16
+    q: torch.Tensor             # [T][Hq][D] bf16
+    k: torch.Tensor             # [T][Hkv][D] bf16
+    v: torch.Tensor             # [T][Hkv][D] bf16
+    w_q: torch.Tensor           # [D] bf16
+    w_k: torch.Tensor           # [D] bf16
+    max_blocks: int
+    num_pages: int
+
+
+def prefill_case(seq_lens, chunks, seed: int = 7, device="cuda", poison: bool = True,
+                 pos_offset: int = 0, num_q_heads: int = NUM_Q_HEADS,
+                 num_kv_heads: int = NUM_KV_HEADS, extra_pages: int = 5) -> PrefillCase:
+    """Seeded chunked-prefill input.  Every sequence's pages are a random
+    permutation of one pool (plus unreferenced pages); tokens 0..L-n-1 hold
+    N(0,1) cached K/V, the chunk's slots hold N(0,1) too (the append
+    overwrites them); with poison every element past a sequence's last token
+    and every unreferenced page is NaN.  Chunk q/k/v are N(0,1), the norm
+    weights U(0.5, 1.5); positions = token index + pos_offset."""
+    assert len(seq_lens) == len(chunks)
+    gen = torch.Generator().manual_seed(seed)
+    P, D = PAGE_SIZE, HEAD_DIM
+    Hq, Hkv = num_q_heads, num_kv_heads
+    L = np.asarray(seq_lens, np.int64)
+    n = np.asarray(chunks, np.int64)
+    npg = (L + P - 1) // P
+    mb = int(max(1, npg.max()))
+    total = int(npg.sum()) + extra_pages
+    perm = torch.randperm(total, generator=gen).numpy()
+    bt = np.full((len(L), mb), -1, np.int32)
+    off = 0
+    for b in range(len(L)):
+        bt[b, :npg[b]] = perm[off:off + npg[b]]
+        off += int(npg[b])
+    pool = torch.randn((total, 2, Hkv, P, D), generator=gen).to(torch.bfloat16)
+    if poison:
+        used = np.zeros((total, P), bool)
+        for b in range(len(L)):
+            t = np.arange(L[b])
+            used[bt[b, t // P], t % P] = True
+        mask = torch.from_numpy(~used)[:, None, None, :, None].expand_as(pool)
+        pool = pool.masked_fill(mask, float("nan"))
+    qo = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    T = int(qo[-1])
+    idx = np.concatenate([np.arange(Lb - nb, Lb) for Lb, nb in zip(L, n)] + [np.zeros(0)])
+    mk = lambda *shape: torch.randn(shape, generator=gen).to(torch.bfloat16)
+    w = lambda: (0.5 + torch.rand(D, generator=gen)).to(torch.bfloat16)
+    return PrefillCase(
+        seq_lens=torch.tensor(L, dtype=torch.int32, device=device),
+        qo_indptr=torch.tensor(qo, dtype=torch.int32, device=device),
+        positions=torch.tensor(idx.astype(np.int64) + pos_offset, dtype=torch.int32, device=device),
+        block_table=torch.from_numpy(bt).to(device), pool=pool.to(device),
+        q=mk(T, Hq, D).to(device), k=mk(T, Hkv, D).to(device), v=mk(T, Hkv, D).to(device),
+        w_q=w().to(device), w_k=w().to(device), max_blocks=mb, num_pages=total)

@@ -254,6 +254,43 @@ qdec_status qdec_qkv_append_rope(const qdec_shape *shape, int32_t hidden,
 qdec_status qdec_qkv_pack_weights(const qdec_shape *shape, int32_t hidden,
                                   const qdec_bf16 *w_qkv, qdec_bf16 *w_packed, void *stream);
 
+/* ------------------------------------------------------- chunked prefill --
+ * The step that fills the pool (article "扔掉 vLLM！从零构建 Qwen3-8B 推理引擎"
+ * (news.rkmt.cn), section 4.4.1: FlashAttention-2 prefill, queries in blocks
+ * that see only keys at or before them).  A chunk of n_b new tokens per
+ * sequence (n_b may be 0), packed as rows qo_indptr[b] .. qo_indptr[b+1]-1
+ * (qo_indptr [B+1] int32, qo_indptr[0] = 0, non-decreasing, qo_indptr[B] <=
+ * num_tokens); chunk row j of sequence b becomes token t = seq_lens[b] - n_b
+ * + j of it (seq_lens counted after the chunk, n_b <= seq_lens[b]).  The
+ * block table must map every page up to token seq_lens[b] - 1.  Sequences
+ * whose chunk is malformed are skipped and flagged QDEC_FLAG_BAD_SEQLEN.
+ * bf16 pool only; shape->batch = B sequences. */
+
+/* Steps 1-3 for every chunk row r: RMSNorm + NeoX RoPE at positions[r] of
+ * its query rows (q [num_tokens][Hq][D], row stride q_stride) into q_rot
+ * [num_tokens][Hq][D] fp32 (unscaled), and of its key rows; bf16(k_rot) and v
+ * (k, v [num_tokens][Hkv][D], row strides k_stride, v_stride) into slot t of
+ * its sequence.  positions [num_tokens] int32.  Errors as qdec_append_rope. */
+qdec_status qdec_prefill_append_rope(const qdec_shape *shape, int32_t num_tokens,
+                                     const qdec_bf16 *q, int64_t q_stride,
+                                     const qdec_bf16 *k, int64_t k_stride,
+                                     const qdec_bf16 *v, int64_t v_stride,
+                                     const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                                     const int32_t *positions, const int32_t *qo_indptr,
+                                     const int32_t *seq_lens, const int32_t *block_table,
+                                     qdec_bf16 *kv_pool, float *q_rot, int32_t *err_flag,
+                                     void *stream);
+
+/* Causal paged attention of the chunk: q_rot row r (query head h) of
+ * sequence b attends to tokens 0 .. t of b through KV head h / (Hq / Hkv),
+ * softmax scale shape->sm_scale (0: 1/sqrt(D)); bf16 out [num_tokens][Hq][D]
+ * (rows past qo_indptr[B] untouched).  Run after qdec_prefill_append_rope on
+ * the same stream.  One launch; no workspace. */
+qdec_status qdec_prefill_attn(const qdec_shape *shape, int32_t num_tokens, const float *q_rot,
+                              const int32_t *qo_indptr, const int32_t *seq_lens,
+                              const int32_t *block_table, const qdec_bf16 *kv_pool,
+                              qdec_bf16 *out, int32_t *err_flag, void *stream);
+
 /* ------------------------------------------------------------ FP8 KV pool --
  * The same block over a KV cache held in FP8 (essay "推理引擎里面发生了什么"
  * (locsic.com), section on quantization: an FP8 KV cache halves its memory

@@ -1,0 +1,156 @@
+"""Chunked prefill through the C ABI (marked gpu), against the oracle.
+
+Each case appends a chunk of new tokens per sequence (qdec_prefill_append_rope)
+and runs the causal paged attention of the chunk (qdec_prefill_attn); the
+oracle runs the same two steps in fp64 on a host copy of the pool taken before
+the append.  Checked: q_rot within the fp32 tolerance 2e-5 (1 + |ref|); every
+appended key within 1 bf16 ulp of the oracle's unrounded k_rot and every
+appended value bit-equal to v; out within 2e-2 + 1e-2 |ref|; nothing outside
+the chunk's slots written.  Pools are NaN-poisoned past every sequence's last
+token.  Cases: fresh prompts (no cached prefix), chunks after a cached prefix,
+chunks that start and end inside a page and across many pages, chunks of one
+token (equal to the decode step), empty chunks, ragged batches, positions
+that differ from the token index, and malformed chunks (flagged, skipped).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_paged_kv_gb300 import workloads as wl
+import parity
+
+pytestmark = pytest.mark.gpu
+
+
+def _shape(c, B):
+    q = parity.qdec()
+    return q.Shape(batch=B, num_pages=c.num_pages, max_blocks_per_seq=c.max_blocks,
+                   max_seq_len=c.max_blocks * 16)
+
+
+def _run(c, B):
+    q = parity.qdec()
+    shape = _shape(c, B)
+    T = c.q.shape[0]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q_rot = torch.empty((T, 32, 128), dtype=torch.float32, device="cuda")
+    out = torch.full((T, 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    q.qdec_prefill_append_rope(shape, c.q, c.k, c.v, c.w_q, c.w_k, c.positions, c.qo_indptr,
+                               c.seq_lens, c.block_table, c.pool, q_rot, err)
+    q.qdec_prefill_attn(shape, q_rot, c.qo_indptr, c.seq_lens, c.block_table, c.pool, out, err)
+    return q_rot, out, err
+
+
+def _oracle(c):
+    pool = wl.bf16_bits(c.pool).copy()
+    res = oracle.prefill_append(wl.bf16_bits(c.q), wl.bf16_bits(c.k), wl.bf16_bits(c.v),
+                                wl.bf16_bits(c.w_q), wl.bf16_bits(c.w_k),
+                                c.positions.cpu().numpy(), c.qo_indptr.cpu().numpy(),
+                                c.seq_lens.cpu().numpy(), c.block_table.cpu().numpy(), pool,
+                                1e6, float(np.float32(1e-6)))
+    out, _ = oracle.prefill_attention(pool, c.block_table.cpu().numpy(),
+                                      c.qo_indptr.cpu().numpy(), c.seq_lens.cpu().numpy(),
+                                      res["q_rot"], 1 / math.sqrt(128))
+    res["out"], res["pool_after"] = out, pool
+    return res
+
+
+def _check(c, res, q_rot, out, pool_before):
+    g = q_rot.double().cpu().numpy()
+    qerr = np.abs(g - res["q_rot"])
+    assert np.all(qerr <= parity.QROT_TOL * (1 + np.abs(res["q_rot"]))), qerr.max()
+    parity.assert_out_close(out, res["out"])
+    got = wl.bf16_bits(c.pool)
+    qo, L = c.qo_indptr.cpu().numpy(), c.seq_lens.cpu().numpy()
+    bt = c.block_table.cpu().numpy()
+    changed = np.zeros(got.shape, bool)
+    v_in = wl.bf16_bits(c.v)
+    for b in range(len(L)):
+        n = qo[b + 1] - qo[b]
+        for j in range(n):
+            r, t = qo[b] + j, L[b] - n + j
+            page, off = bt[b, t // 16], t % 16
+            k_ref = res["k_rot"][r]
+            k_gpu = oracle.bf16_bits_to_f64(got[page, 0, :, off])
+            assert np.all(np.abs(k_gpu - k_ref) <= parity.bf16_ulp(k_ref)), f"k slot row {r}"
+            assert np.array_equal(got[page, 1, :, off], v_in[r]), f"v slot row {r}"
+            changed[page, :, :, off] = True
+    same = (got == pool_before) | (np.isnan(oracle.bf16_bits_to_f64(got)) &
+                                   np.isnan(oracle.bf16_bits_to_f64(pool_before)))
+    assert same[~changed].all(), "the append wrote outside the chunk's slots"
+
+
+CASES = [
+    ([37], [37]),                                  # a fresh prompt, ragged last page
+    ([16], [16]),                                  # exactly one page
+    ([300, 17, 1000], [20, 17, 1]),                # after a cached prefix; fresh; one token
+    ([64, 65, 31], [48, 1, 15]),                   # chunks ending on / after / before a page edge
+    ([500, 40, 77, 250], [0, 40, 33, 0]),          # empty chunks
+    ([2048], [256]),                               # a long prefix and a multi-block chunk
+    ([int(x) for x in np.random.default_rng(9).integers(1, 400, size=12)],
+     [int(x) for x in np.random.default_rng(10).integers(0, 40, size=12)]),
+]
+
+
+@pytest.mark.parametrize("seq_lens,chunks", CASES, ids=lambda x: str(x)[:40])
+def test_prefill_matches_oracle(seq_lens, chunks):
+    chunks = [min(n, L) for L, n in zip(seq_lens, chunks)]
+    c = wl.prefill_case(seq_lens, chunks, seed=sum(seq_lens) % 97)
+    before = wl.bf16_bits(c.pool).copy()
+    res = _oracle(c)
+    q_rot, out, err = _run(c, len(seq_lens))
+    st, flags = parity.qdec().qdec_check_error(err)
+    assert st == 0 and flags == 0, (st, flags)
+    _check(c, res, q_rot, out, before)
+
+
+def test_prefill_positions_differ_from_token_index():
+    c = wl.prefill_case([90, 33], [30, 33], seed=5, pos_offset=1000)
+    before = wl.bf16_bits(c.pool).copy()
+    res = _oracle(c)
+    q_rot, out, err = _run(c, 2)
+    st, flags = parity.qdec().qdec_check_error(err)
+    assert st == 0 and flags == 0
+    _check(c, res, q_rot, out, before)
+
+
+def test_prefill_chunk_of_one_equals_decode():
+    """One token per sequence: the prefill pair gives the decode path's
+    output (same q_rot).  The prefill kernel carries the softmax weights as
+    bf16 (decode: bf16 hi + lo), so the two differ by at most about
+    2^-9 max|v| (<= 8e-3 here) besides the final bf16 rounding."""
+    q = parity.qdec()
+    c = wl.prefill_case([300, 17, 1000, 64], [1, 1, 1, 1], seed=11)
+    shape = _shape(c, 4)
+    q_rot, out, err = _run(c, 4)
+    ws = q.alloc_workspace(shape)
+    out_d = torch.empty_like(out)
+    q.qdec_attn_decode(shape, q_rot, c.pool, c.block_table, c.seq_lens, ws, out_d, err)
+    st, flags = q.qdec_check_error(err)
+    assert st == 0 and flags == 0
+    assert torch.allclose(out.float(), out_d.float(), rtol=2 ** -7, atol=8e-3)
+
+
+def test_prefill_malformed_chunk_is_flagged():
+    """A chunk longer than its sequence is skipped and flagged; the others
+    are exact."""
+    q = parity.qdec()
+    c = wl.prefill_case([40, 50, 60], [10, 20, 30], seed=12)
+    good = wl.prefill_case([40, 50, 60], [10, 20, 30], seed=12)
+    res = _oracle(good)
+    c.seq_lens[1] = 15                                  # chunk of 20 in 15 tokens (device copy)
+    q_rot, out, err = _run(c, 3)
+    st, flags = q.qdec_check_error(err)
+    assert st == q.QDEC_ERR_DEVICE_BOUNDS and flags & q.QDEC_FLAG_BAD_SEQLEN, (st, flags)
+    rows = np.r_[0:10, 30:60]
+    parity.assert_out_close(out[rows], res["out"][rows])
+
+
+def test_prefill_deterministic():
+    c = wl.prefill_case([700, 129], [300, 129], seed=13)
+    _, out1, _ = _run(c, 2)
+    _, out2, _ = _run(c, 2)
+    assert torch.equal(out1, out2)

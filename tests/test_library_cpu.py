@@ -88,6 +88,19 @@ def test_entry_points_reject_null_and_misaligned_arguments(q):
     assert lib.qdec_attn_decode(sh, ok, ok, ok, ok, ok, 1 << 30, z, z, z) == q.QDEC_ERR_INVALID_ARG
     assert lib.qdec_attn_decode(None, ok, ok, ok, ok, ok, 1 << 30, ok, z,
                                 z) == q.QDEC_ERR_INVALID_ARG
+    # prefill: missing qo_indptr / q_rot / out, misaligned q_rot, negative row count
+    def pre_append(n=4, qo=ok, qr=ok):
+        return lib.qdec_prefill_append_rope(sh, n, ok, S, ok, S, ok, S, ok, ok, ok, qo, ok, ok, ok,
+                                            qr, z, z)
+    assert pre_append(qo=z) == q.QDEC_ERR_INVALID_ARG
+    assert pre_append(qr=z) == q.QDEC_ERR_INVALID_ARG
+    assert pre_append(qr=bad) == q.QDEC_ERR_INVALID_ARG
+    assert pre_append(n=-1) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_prefill_attn(sh, 4, z, ok, ok, ok, ok, ok, z, z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_prefill_attn(sh, 4, ok, z, ok, ok, ok, ok, z, z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_prefill_attn(sh, 4, ok, ok, ok, ok, ok, z, z, z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_prefill_attn(sh, -2, ok, ok, ok, ok, ok, ok, z, z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_prefill_attn(None, 4, ok, ok, ok, ok, ok, ok, z, z) == q.QDEC_ERR_INVALID_ARG
     # append without a q_rot output
     assert lib.qdec_append_rope(sh, ok, S, ok, S, ok, S, ok, ok, ok, ok, ok, z, ok, z, z,
                                 z) == q.QDEC_ERR_INVALID_ARG
