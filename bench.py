@@ -53,6 +53,8 @@ from gqa_paged_kv_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "decode-attn µs/layer-step and KV GB/s (% of GB300 HBM peak) per batch×ctx"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+PREFILL_METRIC = "prefill-attn TFLOP/s (causal, algorithmic) and µs/layer per prompt"
 # the sources each roofline kernel is built from (its traffic entry below
 # stays valid only while their hash matches)
 _CSRC = "gqa_paged_kv_gb300/csrc/"
@@ -61,6 +63,8 @@ KERNEL_SOURCES = {
                                                   "qdec_ptx.cuh")),
     "qkv_append_kernel": tuple(_CSRC + f for f in ("qdec_qkv.cu", "qdec_internal.h",
                                                    "qdec_ptx.cuh")),
+    "prefill_attention_kernel": tuple(_CSRC + f for f in ("qdec_prefill.cu", "qdec_internal.h",
+                                                          "qdec_ptx.cuh")),
 }
 
 # DRAM bytes per launch of the fused kernel measured with ncu (see
@@ -105,6 +109,9 @@ def parse_args():
     ap.add_argument("--qkv", action="store_true",
                     help="start each layer from hidden states: fused QKV projection + attention")
     ap.add_argument("--hidden", type=int, default=2560, help="hidden size for --qkv")
+    ap.add_argument("--prefill", type=int, default=0, metavar="PROMPT",
+                    help="chunked prefill instead of decode: one fresh prompt of PROMPT tokens "
+                         "per layer (append + causal attention), metric TFLOP/s")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the 36 calls eagerly")
@@ -163,6 +170,14 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 class Clocks:
@@ -641,12 +656,199 @@ def run_ours(args, dist: Dist):
         print(json.dumps(line), flush=True)
 
 
+def prefill_flops(seq_lens, chunks, Hq=32, D=128) -> int:
+    """Algorithmic FLOPs of the causal attention of the chunks: per head,
+    query row at token index t and each of its t+1 keys, 2 D for q.k and 2 D
+    for p v."""
+    tot = 0
+    for L, n in zip(seq_lens, chunks):
+        t = np.arange(L - n, L, dtype=np.int64)
+        tot += int((t + 1).sum())
+    return 4 * D * Hq * tot
+
+
+def run_prefill(args, dist: Dist):
+    """Chunked prefill: per layer one fresh prompt of args.prefill tokens
+    (qdec_prefill_append_rope, then qdec_prefill_attn) over that layer's pool;
+    a step = all layers, one CUDA graph."""
+    from gqa_paged_kv_gb300 import build as qbuild
+    qbuild.build()
+    from gqa_paged_kv_gb300 import qdec
+
+    dev = dist.local
+    torch.cuda.set_device(dev)
+    P = args.prefill
+    L = args.layers or 36
+    name = f"prefill-b1-prompt{P}-{L}layer"
+    cases = [wl.prefill_case([P], [P], seed=1000 + l, device="cuda", poison=False) for l in range(L)]
+    c0 = cases[0]
+    shape = qdec.Shape(batch=1, num_pages=c0.num_pages, max_blocks_per_seq=c0.max_blocks,
+                       max_seq_len=c0.max_blocks * 16)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q_rot = torch.empty((P, 32, 128), dtype=torch.float32, device="cuda")
+    out = torch.empty((L, P, 32, 128), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.Stream()
+    flops_layer = prefill_flops([P], [P])
+
+    def step_fn(ins, outs):
+        def fn():
+            for l, c in enumerate(cases):
+                q, k, v = ins[l]
+                qdec.qdec_prefill_append_rope(shape, q, k, v, c.w_q, c.w_k, c.positions,
+                                              c.qo_indptr, c.seq_lens, c.block_table, c.pool,
+                                              q_rot, err, stream=stream)
+                qdec.qdec_prefill_attn(shape, q_rot, c.qo_indptr, c.seq_lens, c.block_table,
+                                       c.pool, outs[l], err, stream=stream)
+        return fn
+
+    def graph_of(fn):
+        with torch.cuda.stream(stream):
+            fn()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+        return g
+
+    ins = [(c.q, c.k, c.v) for c in cases]
+    g = graph_of(step_fn(ins, out))
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+    stream.synchronize()
+    st, flags = qdec.qdec_check_error(err, stream)
+    assert st == 0, f"device error flags {flags:#x}"
+
+    clocks = Clocks(dev)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    ck = clocks.stop()
+    t_ms = dist.max(e0.elapsed_time(e1))
+    ms_step = t_ms / args.steps
+    value = dist.world * flops_layer * L * args.steps / (t_ms * 1e-3) / 1e12
+
+    # the attention kernel alone: a graph of its L launches
+    ga = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(ga, stream=stream):
+            for l, c in enumerate(cases):
+                qdec.qdec_prefill_attn(shape, q_rot, c.qo_indptr, c.seq_lens, c.block_table,
+                                       c.pool, out[l], err, stream=stream)
+        for _ in range(3):
+            ga.replay()
+        reps = max(5, args.steps // 4)
+        e0.record(stream)
+        for _ in range(reps):
+            ga.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    launch_us = e0.elapsed_time(e1) / reps / L * 1e3
+    achieved = flops_layer / (launch_us * 1e-6) / 1e12
+    peak, peak_kind = measured_bf16_tflops()
+
+    # end to end: each step's chunk q/k/v from pinned host memory, out back
+    k_e2e = 0 if args.no_e2e else max(1, args.steps // 4)
+    h2d = sum(t.numel() * t.element_size() for trip in ins for t in trip)
+    d2h = out.numel() * out.element_size()
+    e2e_value = None
+    if k_e2e:
+        host = [tuple(t.cpu().pin_memory() for t in trip) for trip in ins]
+        dev_in = [tuple(torch.empty_like(t) for t in trip) for trip in ins]
+        out_d = torch.empty_like(out)
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        ge = graph_of(step_fn(dev_in, out_d))
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for hs, ds in zip(host, dev_in):
+                    for h_, d_ in zip(hs, ds):
+                        d_.copy_(h_, non_blocking=True)
+                ge.replay()
+                out_h.copy_(out_d, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        dist.barrier()
+        e0.record(stream)
+        for _ in range(k_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        e2e_value = dist.world * flops_layer * L * k_e2e / (dist.max(e0.elapsed_time(e1)) * 1e-3) / 1e12
+    st, flags = qdec.qdec_check_error(err, stream)
+    assert st == 0, f"device error flags {flags:#x}"
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        import math
+
+        import oracle
+        Pc = min(P, 256)   # bounded sample: one layer, a fresh prompt of Pc tokens
+        c = wl.prefill_case([Pc], [Pc], seed=1000, device="cpu", poison=False)
+        pool = wl.bf16_bits(c.pool).copy()
+        t0 = time.perf_counter()
+        res = oracle.prefill_append(wl.bf16_bits(c.q), wl.bf16_bits(c.k), wl.bf16_bits(c.v),
+                                    wl.bf16_bits(c.w_q), wl.bf16_bits(c.w_k),
+                                    c.positions.numpy(), c.qo_indptr.numpy(), c.seq_lens.numpy(),
+                                    c.block_table.numpy(), pool, 1e6, float(np.float32(1e-6)))
+        oracle.prefill_attention(pool, c.block_table.numpy(), c.qo_indptr.numpy(),
+                                 c.seq_lens.numpy(), res["q_rot"], 1 / math.sqrt(128))
+        secs = time.perf_counter() - t0
+        cpu = {"value": round(prefill_flops([Pc], [Pc]) / secs / 1e12, 9), "unit": "TFLOP/s",
+               "cores": 1, "kind": "oracle",
+               "sample": f"one layer of a fresh {Pc}-token prompt (append + causal attention), "
+                         f"fp64, {secs:.1f} s"}
+
+    if dist.rank == 0:
+        line = {
+            "metric": PREFILL_METRIC, "value": round(value, 3), "unit": "TFLOP/s",
+            "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 (mma.sync bf16, q as hi+lo, f32 accumulate)",
+            "data": "synthetic (seeded N(0,1) bf16 q/k/v, U(0.5,1.5) norm weights)",
+            "us_per_layer_step": round(ms_step * 1e3 / L, 3),
+            "config": {"workload": name, "batch": 1, "prompt": P, "layers": L,
+                       "heads": "32 q / 8 kv, head_dim 128, page 16",
+                       "launch": f"CUDA graph: {L} x (qdec_prefill_append_rope, qdec_prefill_attn)",
+                       "l2": "not flushed (compute-bound: each layer's K/V is re-read from L2 "
+                             "by its query blocks by design)"},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                         "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, cuBLAS "
+                                      f"burst)" if peak_kind == "measured" else "fallback",
+                         "kernel": "prefill_attention_kernel", "launch_us": round(launch_us, 3),
+                         "launch_us_how": f"CUDA events around a graph of {L} attention "
+                                          f"launches, {reps} replays",
+                         "flops_per_launch": flops_layer},
+            "e2e": {"value": e2e_value and round(e2e_value, 3), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k_e2e},
+            "gpu_launches": 2 * L * args.steps,
+            "clocks": ck,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     dist = Dist()
     try:
         if args.impl == "reference":
             run_reference(args, dist)
+        elif args.prefill:
+            run_prefill(args, dist)
         else:
             run_ours(args, dist)
     finally:

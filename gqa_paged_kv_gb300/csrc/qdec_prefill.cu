@@ -7,8 +7,7 @@
 // prefill_append_kernel -- steps 1-3 for every chunk token: RMSNorm and NeoX
 //   RoPE (at positions[row]) of its query rows into q_rot (fp32) and of its
 //   key rows, then bf16(k_rot) and v into slot L_b - n_b + j of the pool.
-//   One CTA per (token, KV head): warp w norms and rotates query head
-//   4 g + w; warp 0 the key row, warp 1 copies the value row.
+//   One CTA per token (the angles taken once), one warp per KV head.
 //
 // prefill_attention_kernel -- causal paged attention of the chunk (article
 //   "扔掉 vLLM！从零构建 Qwen3-8B 推理引擎" (news.rkmt.cn), section 4.4.1:
@@ -79,66 +78,78 @@ __device__ __forceinline__ bool chunk_ok(const Params &p, int b, int &n, int &L)
 }
 
 // ------------------------------------------------------------------ append --
-__global__ void __launch_bounds__(128) prefill_append_kernel(const __grid_constant__ Params p) {
-    const int r = blockIdx.x, g = blockIdx.y;
+// One CTA per chunk row, 256 threads: the 64 angles of the row's position are
+// taken once (double sincos) into shared memory; warp w then handles KV head
+// w (and w + 8, ...): its four query rows in fp32 (q_rot's tolerance is
+// absolute), its key row with the rotation's difference in double (a key near
+// zero keeps its relative accuracy, so it stays within one bf16 step of the
+// exact value), and the copy of its value row.
+constexpr int kPfAppendThreads = 256;
+
+__global__ void __launch_bounds__(kPfAppendThreads) prefill_append_kernel(
+    const __grid_constant__ Params p) {
+    __shared__ double cs_d[kRotPairs], sn_d[kRotPairs];
+    const int r = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = seq_of_row(p.qo_indptr, p.B, r);
     int n, L;
     if (!chunk_ok(p, b, n, L) || r < p.qo_indptr[b] || r >= p.qo_indptr[b + 1]) {
-        if (threadIdx.x == 0 && g == 0) flag_error(p.err, QDEC_FLAG_BAD_SEQLEN);
+        if (threadIdx.x == 0) flag_error(p.err, QDEC_FLAG_BAD_SEQLEN);
         return;  // uniform over the CTA
     }
     const int t = L - n + (r - p.qo_indptr[b]);  // token index in the sequence
-    const int pos = p.positions[r];
-    // this lane's rotate-half pairs i = 2 lane, 2 lane + 1: dims i and i + 64;
-    // the angle pos * theta^(-2i/D), its cos and sin in double
-    double cs[2], sn[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e)
-        sincos(static_cast<double>(pos) * p.inv_freq[2 * lane + e], &sn[e], &cs[e]);
-    // RMSNorm (eps inside the root) and rotation of one 128-dim row: y holds
-    // dims 2 lane, 2 lane + 1, 64 + 2 lane, 64 + 2 lane + 1.  x w is exact in
-    // fp32 (a product of two bf16); the rotation's difference is formed in
-    // double, so a result near zero keeps its relative accuracy (the only
-    // error left is the fp32 root, relative to the whole row), which keeps the
-    // key within one bf16 step of the exact value.
-    auto norm_rotate = [&](const __nv_bfloat16 *x, const __nv_bfloat16 *w, float (&y)[4]) {
+    if (threadIdx.x < kRotPairs)  // angle i: positions[r] * theta^(-2i/D)
+        sincos(static_cast<double>(p.positions[r]) * p.inv_freq[threadIdx.x], &sn_d[threadIdx.x],
+               &cs_d[threadIdx.x]);
+    __syncthreads();
+    // this lane's rotate-half pairs i = 2 lane, 2 lane + 1: dims i and i + 64
+    const double c0 = cs_d[2 * lane], c1 = cs_d[2 * lane + 1];
+    const double s0 = sn_d[2 * lane], s1 = sn_d[2 * lane + 1];
+    const float fc0 = static_cast<float>(c0), fc1 = static_cast<float>(c1);
+    const float fs0 = static_cast<float>(s0), fs1 = static_cast<float>(s1);
+    // RMSNorm (eps inside the root) of one 128-dim row; x w is exact in fp32
+    // (a product of two bf16).  Returns the root; n holds x w for dims
+    // 2 lane, 2 lane + 1, 64 + 2 lane, 64 + 2 lane + 1.
+    auto norm = [&](const __nv_bfloat16 *x, const __nv_bfloat16 *w, float (&nv)[4]) {
         const float2 a = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(x)[lane]);
         const float2 c = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(x + 64)[lane]);
         const float ss = warp_sum(a.x * a.x + a.y * a.y + c.x * c.x + c.y * c.y);
-        const double rn = static_cast<double>(rsqrtf(ss * (1.0f / kHeadDim) + p.eps));
         const float2 wa = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(w)[lane]);
         const float2 wc = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(w + 64)[lane]);
-        const double n1a = a.x * wa.x, n1b = a.y * wa.y;  // exact products
-        const double n2a = c.x * wc.x, n2b = c.y * wc.y;
-        y[0] = static_cast<float>(rn * (n1a * cs[0] - n2a * sn[0]));
-        y[1] = static_cast<float>(rn * (n1b * cs[1] - n2b * sn[1]));
-        y[2] = static_cast<float>(rn * (n2a * cs[0] + n1a * sn[0]));
-        y[3] = static_cast<float>(rn * (n2b * cs[1] + n1b * sn[1]));
+        nv[0] = a.x * wa.x;
+        nv[1] = a.y * wa.y;
+        nv[2] = c.x * wc.x;
+        nv[3] = c.y * wc.y;
+        return rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
     };
-    {
-        const int h = g * kGroup + warp;
-        float y[4];
-        norm_rotate(p.q + static_cast<int64_t>(r) * p.q_stride + h * kHeadDim, p.w_q, y);
-        float *dst = p.q_rot_out + (static_cast<int64_t>(r) * p.Hq + h) * kHeadDim;
-        reinterpret_cast<float2 *>(dst)[lane] = make_float2(y[0], y[1]);
-        reinterpret_cast<float2 *>(dst + 64)[lane] = make_float2(y[2], y[3]);
-    }
-    if (warp >= 2) return;
-    const int page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + t / kPageSize];
-    if (page < 0 || page >= p.num_pages) {
-        if (lane == 0 && warp == 0) flag_error(p.err, QDEC_FLAG_BAD_PAGE);
-        return;
-    }
-    const int64_t slot =
-        ((static_cast<int64_t>(page) * 2 * p.Hkv + g) * kPageSize + t % kPageSize) * kHeadDim;
-    if (warp == 0) {
-        float y[4];
-        norm_rotate(p.k + static_cast<int64_t>(r) * p.k_stride + g * kHeadDim, p.w_k, y);
+    for (int g = warp; g < p.Hkv; g += kPfAppendThreads / 32) {
+#pragma unroll 1
+        for (int j = 0; j < kGroup; ++j) {
+            const int h = g * kGroup + j;
+            float nv[4];
+            const float rn = norm(p.q + static_cast<int64_t>(r) * p.q_stride + h * kHeadDim,
+                                  p.w_q, nv);
+            const float n1a = nv[0] * rn, n1b = nv[1] * rn, n2a = nv[2] * rn, n2b = nv[3] * rn;
+            float *dst = p.q_rot_out + (static_cast<int64_t>(r) * p.Hq + h) * kHeadDim;
+            reinterpret_cast<float2 *>(dst)[lane] =
+                make_float2(n1a * fc0 - n2a * fs0, n1b * fc1 - n2b * fs1);
+            reinterpret_cast<float2 *>(dst + 64)[lane] =
+                make_float2(n2a * fc0 + n1a * fs0, n2b * fc1 + n1b * fs1);
+        }
+        const int page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + t / kPageSize];
+        if (page < 0 || page >= p.num_pages) {
+            if (lane == 0) flag_error(p.err, QDEC_FLAG_BAD_PAGE);
+            continue;
+        }
+        const int64_t slot =
+            ((static_cast<int64_t>(page) * 2 * p.Hkv + g) * kPageSize + t % kPageSize) * kHeadDim;
+        float nv[4];
+        const double rn = norm(p.k + static_cast<int64_t>(r) * p.k_stride + g * kHeadDim, p.w_k, nv);
         uint32_t *kd = reinterpret_cast<uint32_t *>(p.pool + slot);
-        kd[lane] = pack_bf16x2(y[0], y[1]);
-        kd[32 + lane] = pack_bf16x2(y[2], y[3]);
-    } else {
+        kd[lane] = pack_bf16x2(static_cast<float>(rn * (nv[0] * c0 - nv[2] * s0)),
+                               static_cast<float>(rn * (nv[1] * c1 - nv[3] * s1)));
+        kd[32 + lane] = pack_bf16x2(static_cast<float>(rn * (nv[2] * c0 + nv[0] * s0)),
+                                    static_cast<float>(rn * (nv[3] * c1 + nv[1] * s1)));
         const uint32_t *vs = reinterpret_cast<const uint32_t *>(
             p.v + static_cast<int64_t>(r) * p.v_stride + g * kHeadDim);
         uint32_t *vd = reinterpret_cast<uint32_t *>(
@@ -335,17 +346,24 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (slot_ok[slot]) {
                 const uint32_t tile = smem_u32(sm + slot * kTileBytes);
                 // ---- S = Q K^T: 16 tokens x 16 keys (two n-tiles of 8 keys)
+                // (the hi and lo products in separate accumulators: four
+                // independent chains of 8 MMAs instead of two of 16)
                 float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                float sl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     uint32_t kb[4];
                     // matrices: keys 0-7 / 8-15 (mi >> 1) x dims 16kk.. / 16kk+8.. (mi & 1)
                     ldmatrix_x4(kb, tile_addr(tile, 0, (mi >> 1) * 8 + r8, 2 * kk + (mi & 1)));
                     mma_bf16(s[0], qh[kk], kb[0], kb[1]);
-                    mma_bf16(s[0], ql[kk], kb[0], kb[1]);
                     mma_bf16(s[1], qh[kk], kb[2], kb[3]);
-                    mma_bf16(s[1], ql[kk], kb[2], kb[3]);
+                    mma_bf16(sl[0], ql[kk], kb[0], kb[1]);
+                    mma_bf16(sl[1], ql[kk], kb[2], kb[3]);
                 }
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s[j][e] += sl[j][e];
                 // ---- causal mask: key 16 pg + 8 j + 2 tq + e against each row's limit
                 const int kbase = pg * kPageSize + 2 * tq;
 #pragma unroll
@@ -454,7 +472,7 @@ bool g_pf_smem_set[64];
 
 cudaError_t launch_prefill_append(const Params &p, cudaStream_t s) {
     if (p.T <= 0) return cudaSuccess;
-    prefill_append_kernel<<<dim3(p.T, p.Hkv), 128, 0, s>>>(p);
+    prefill_append_kernel<<<p.T, kPfAppendThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
