@@ -77,6 +77,8 @@ TRAFFIC = {
                                                 "bytes_per_launch": 1038078449},
     "b64-ragged128to16384-sharedpool-36layer-fp8kv": {"kernel_sha": "92059be5fa501bc5",
                                                       "bytes_per_launch": 524764114},
+    # --prefill 2048: the causal prefill attention kernel
+    "prefill-b1-prompt2048-36layer": {"kernel_sha": "5ab06e7214f5ffde", "bytes_per_launch": 41995136},
     # --qkv: the projection kernel
     "b8-ctx256to384-36layer-qkv2560": {"kernel_sha": "3a96e0c7a7742cc6", "bytes_per_launch": 31541187},
     "b64-ragged128to16384-sharedpool-36layer-qkv2560": {"kernel_sha": "3a96e0c7a7742cc6",
@@ -790,6 +792,10 @@ def run_prefill(args, dist: Dist):
     st, flags = qdec.qdec_check_error(err, stream)
     assert st == 0, f"device error flags {flags:#x}"
 
+    tr = TRAFFIC.get(name)
+    traffic = (tr["bytes_per_launch"]
+               if tr and tr["kernel_sha"] == kernel_sha("prefill_attention_kernel") else None)
+
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         import math
@@ -825,7 +831,7 @@ def run_prefill(args, dist: Dist):
                        "l2": "not flushed (compute-bound: each layer's K/V is re-read from L2 "
                              "by its query blocks by design)"},
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
-                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, cuBLAS "
                                       f"burst)" if peak_kind == "measured" else "fallback",
                          "kernel": "prefill_attention_kernel", "launch_us": round(launch_us, 3),
