@@ -364,18 +364,24 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int j = 0; j < 2; ++j)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) s[j][e] += sl[j][e];
-                // ---- causal mask: key 16 pg + 8 j + 2 tq + e against each row's limit
+                // ---- causal mask: key 16 pg + 8 j + 2 tq + e against each
+                // row's limit (only tiles that reach past a limit need it)
                 const int kbase = pg * kPageSize + 2 * tq;
+                if (pg * kPageSize + kPageSize - 1 > lim0) {
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
+                    for (int j = 0; j < 2; ++j) {
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int key = kbase + 8 * j + e;
-                        if (key > lim0) s[j][e] = -INFINITY;
-                        if (key > lim1) s[j][2 + e] = -INFINITY;
+                        for (int e = 0; e < 2; ++e) {
+                            const int key = kbase + 8 * j + e;
+                            if (key > lim0) s[j][e] = -INFINITY;
+                            if (key > lim1) s[j][2 + e] = -INFINITY;
+                        }
                     }
                 }
-                // ---- online softmax (log2 units), rows gq and gq + 8
+                // ---- online softmax (log2 units), rows gq and gq + 8.  The
+                // running maximum is kept until a tile's maximum exceeds it
+                // by more than 2^8 (weights then stay below 256, exact enough
+                // in bf16 and fp32), so most tiles rescale nothing.
                 float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
                 float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
 #pragma unroll
@@ -383,30 +389,34 @@ __global__ void __launch_bounds__(kThreads, 2)
                     mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
                     mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
                 }
-                const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
                 // a row that has seen no key yet keeps m = -inf, weights 0
-                const float a0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
-                const float a1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+                if (mx0 > m0 + 8.f || mx1 > m1 + 8.f) {
+                    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+                    const float a0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
+                    const float a1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+                    l0 *= a0;
+                    l1 *= a1;
+                    m0 = n0;
+                    m1 = n1;
+#pragma unroll
+                    for (int nt = 0; nt < 16; ++nt) {
+                        o[nt][0] *= a0;
+                        o[nt][1] *= a0;
+                        o[nt][2] *= a1;
+                        o[nt][3] *= a1;
+                    }
+                }
                 float pw[2][4];
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        pw[j][e] = n0 == -INFINITY ? 0.f : exp2f(s[j][e] - n0);
-                        pw[j][2 + e] = n1 == -INFINITY ? 0.f : exp2f(s[j][2 + e] - n1);
+                        pw[j][e] = m0 == -INFINITY ? 0.f : exp2f(s[j][e] - m0);
+                        pw[j][2 + e] = m1 == -INFINITY ? 0.f : exp2f(s[j][2 + e] - m1);
                     }
                 }
-                l0 = l0 * a0 + pw[0][0] + pw[0][1] + pw[1][0] + pw[1][1];
-                l1 = l1 * a1 + pw[0][2] + pw[0][3] + pw[1][2] + pw[1][3];
-                m0 = n0;
-                m1 = n1;
-#pragma unroll
-                for (int nt = 0; nt < 16; ++nt) {
-                    o[nt][0] *= a0;
-                    o[nt][1] *= a0;
-                    o[nt][2] *= a1;
-                    o[nt][3] *= a1;
-                }
+                l0 += pw[0][0] + pw[0][1] + pw[1][0] + pw[1][1];
+                l1 += pw[0][2] + pw[0][3] + pw[1][2] + pw[1][3];
                 // ---- O += P V: P (16 tokens x 16 keys) from the score
                 // accumulators as the A operand; V rows past the sequence
                 // (possibly not finite) are zeroed in the B fragments
