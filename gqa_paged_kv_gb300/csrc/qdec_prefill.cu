@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(kPfAppendThreads) prefill_append_kernel(
         return rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
     };
     for (int g = warp; g < p.Hkv; g += kPfAppendThreads / 32) {
-#pragma unroll 1
-        for (int j = 0; j < kGroup; ++j) {
+#pragma unroll
+        for (int j = 0; j < kGroup; ++j) {  // unrolled: the four rows' loads overlap
             const int h = g * kGroup + j;
             float nv[4];
             const float rn = norm(p.q + static_cast<int64_t>(r) * p.q_stride + h * kHeadDim,
