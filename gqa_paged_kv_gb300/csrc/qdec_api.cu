@@ -106,9 +106,11 @@ int ring_cap(const qdec_shape *s, int cluster, bool fp8) {
     if (per_sm <= 0) per_sm = 228 * 1024;
     const int w = qdec::kConsumerWarps;
     int cap = qdec::kMaxStages / w * w;
-    while (cap > w && static_cast<int64_t>(qdec::ctas_per_sm(cluster > 0, fp8)) *
-                              (qdec::attention_smem_bytes(s->batch, cap, cluster, fp8) + 1024) >
-                          static_cast<int64_t>(per_sm))
+    while (cap > w &&
+           static_cast<int64_t>(qdec::ctas_per_sm(cluster > 0, fp8)) *
+                   static_cast<int64_t>(qdec::attention_smem_bytes(s->batch, cap, cluster, fp8) +
+                                        1024) >
+               static_cast<int64_t>(per_sm))
         cap -= w;
     return cap;
 }

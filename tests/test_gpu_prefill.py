@@ -154,3 +154,19 @@ def test_prefill_deterministic():
     _, out1, _ = _run(c, 2)
     _, out2, _ = _run(c, 2)
     assert torch.equal(out1, out2)
+
+
+@pytest.mark.parametrize("bad_entry", [-1, 10 ** 6], ids=["negative", "beyond_pool"])
+def test_prefill_bad_page_is_flagged(bad_entry):
+    """A block-table entry outside the pool in one sequence's chunk pages is
+    flagged; the other sequences are exact."""
+    q = parity.qdec()
+    c = wl.prefill_case([60, 70, 80], [20, 30, 40], seed=14)
+    good = wl.prefill_case([60, 70, 80], [20, 30, 40], seed=14)
+    res = _oracle(good)
+    c.block_table[1, 3] = bad_entry                     # a chunk page of sequence 1
+    q_rot, out, err = _run(c, 3)
+    st, flags = q.qdec_check_error(err)
+    assert st == q.QDEC_ERR_DEVICE_BOUNDS and flags & q.QDEC_FLAG_BAD_PAGE, (st, flags)
+    rows = np.r_[0:20, 50:90]
+    parity.assert_out_close(out[rows], res["out"][rows])
