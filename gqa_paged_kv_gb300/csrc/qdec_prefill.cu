@@ -173,13 +173,6 @@ __device__ __forceinline__ void tma_load_page_tile(uint32_t dst, const CUtensorM
         : "memory");
 }
 
-// Shared-memory address of token `tok`, 16-byte chunk `c` (dims 8c .. 8c+7,
-// c < 16) of plane `plane` of the tile at `tile`.
-__device__ __forceinline__ uint32_t tile_addr(uint32_t tile, int plane, int tok, int c) {
-    return tile + plane * kPlaneBytes + (c >> 3) * kTileHalfBytes + tok * 128 +
-           (((c & 7) ^ (tok & 7)) << 4);
-}
-
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_attention_kernel(const __grid_constant__ CUtensorMap kv_map,
                              const __grid_constant__ Params p) {
@@ -332,6 +325,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
         const int mi = lane >> 3, r8 = lane & 7;
+        // this lane's matrix-load offsets within a tile: K (keys (mi >> 1) * 8
+        // + r8, dim chunk 2 kk + (mi & 1)) and V (keys (mi & 1) * 8 + r8, dim
+        // chunk 2 pr + (mi >> 1)), for chunk pairs j = kk, pr mod 4 (the
+        // halves of D add 2 KiB)
+        uint32_t koff[4], voff[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int kt = (mi >> 1) * 8 + r8, vt = (mi & 1) * 8 + r8;
+            koff[j] = kt * 128 + (((2 * j + (mi & 1)) ^ (kt & 7)) << 4);
+            voff[j] = kPlaneBytes + vt * 128 + (((2 * j + (mi >> 1)) ^ (vt & 7)) << 4);
+        }
         bool aborted = false;
         for (int pg = 0; pg < npages; ++pg) {
             const int slot = pg % kPfStages;
@@ -354,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int kk = 0; kk < 8; ++kk) {
                     uint32_t kb[4];
                     // matrices: keys 0-7 / 8-15 (mi >> 1) x dims 16kk.. / 16kk+8.. (mi & 1)
-                    ldmatrix_x4(kb, tile_addr(tile, 0, (mi >> 1) * 8 + r8, 2 * kk + (mi & 1)));
+                    ldmatrix_x4(kb, tile + (kk >> 2) * kTileHalfBytes + koff[kk & 3]);
                     mma_bf16(s[0], qh[kk], kb[0], kb[1]);
                     mma_bf16(s[1], qh[kk], kb[2], kb[3]);
                     mma_bf16(sl[0], ql[kk], kb[0], kb[1]);
@@ -435,9 +439,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int pr = 0; pr < 8; ++pr) {
                     uint32_t vb[4];
                     // matrices: keys 0-7 / 8-15 (mi & 1) x dims 16pr.. / 16pr+8.. (mi >> 1)
-                    ldmatrix_x4_trans(vb, tile_addr(tile, 1, (mi & 1) * 8 + r8, 2 * pr + (mi >> 1)));
-                    mma_bf16(o[2 * pr], pa, vb[0] & keep0, vb[1] & keep1);
-                    mma_bf16(o[2 * pr + 1], pa, vb[2] & keep0, vb[3] & keep1);
+                    ldmatrix_x4_trans(vb, tile + (pr >> 2) * kTileHalfBytes + voff[pr & 3]);
+                    if (ntok < kPageSize) {  // the sequence's last page
+                        vb[0] &= keep0;
+                        vb[1] &= keep1;
+                        vb[2] &= keep0;
+                        vb[3] &= keep1;
+                    }
+                    mma_bf16(o[2 * pr], pa, vb[0], vb[1]);
+                    mma_bf16(o[2 * pr + 1], pa, vb[2], vb[3]);
                 }
             }
             __syncwarp();
