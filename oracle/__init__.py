@@ -112,6 +112,12 @@ class Oracle:
         lib.oracle_prefill_attention.argtypes = ([ci] * 7 + [u16p] + [i32p] * 3 + [dp, _D]
                                                  + [dp] * 2)
         lib.oracle_prefill_attention.restype = ci
+        lib.oracle_prefill_append_fp8.argtypes = ([ci] * 7 + [u16p] * 5 + [i32p] * 4
+                                                  + [u8p, f32p] + [_D] * 2 + [dp] * 2)
+        lib.oracle_prefill_append_fp8.restype = ci
+        lib.oracle_prefill_attention_fp8.argtypes = ([ci] * 7 + [u8p, f32p] + [i32p] * 3
+                                                     + [dp, _D] + [dp] * 2)
+        lib.oracle_prefill_attention_fp8.restype = ci
         self.lib = lib
         self.path = path
 
@@ -328,6 +334,44 @@ class Oracle:
         return out, lse
 
 
+    def prefill_append_fp8(self, q, k, v, w_q, w_k, positions, qo_indptr, seq_lens,
+                           block_table, pool8, kv_scale, rope_theta: float, eps: float):
+        """:meth:`prefill_append` with an FP8 pool (uint8, updated in place)
+        and its scales kv_scale (float32 [pages][2][Hkv], read only)."""
+        q, k, v, w_q, w_k = _u16(q), _u16(k), _u16(v), _u16(w_q), _u16(w_k)
+        pos, qo, sl, bt = _i32(positions), _i32(qo_indptr), _i32(seq_lens), _i32(block_table)
+        assert pool8.dtype == np.uint8 and pool8.flags["C_CONTIGUOUS"]
+        _, sc = self._fp8_args(pool8, kv_scale)
+        T, Hq, D = q.shape
+        num_pages, _, Hkv, P, D2 = pool8.shape
+        B = sl.shape[0]
+        assert D2 == D and k.shape == (T, Hkv, D) and qo.shape == (B + 1,) and qo[-1] == T
+        res = {"q_rot": np.empty((T, Hq, D)), "k_rot": np.empty((T, Hkv, D))}
+        _check(self.lib.oracle_prefill_append_fp8(
+            B, Hq, Hkv, D, P, num_pages, bt.shape[1],
+            _ptr(q, _U16), _ptr(k, _U16), _ptr(v, _U16), _ptr(w_q, _U16), _ptr(w_k, _U16),
+            _ptr(pos, _I32), _ptr(qo, _I32), _ptr(sl, _I32), _ptr(bt, _I32),
+            _ptr(pool8, ctypes.c_uint8), _ptr(sc, ctypes.c_float), float(rope_theta),
+            float(eps), _ptr(res["q_rot"], _D), _ptr(res["k_rot"], _D)))
+        return res
+
+    def prefill_attention_fp8(self, pool8, kv_scale, block_table, qo_indptr, seq_lens, q_rot,
+                              scale: float):
+        """:meth:`prefill_attention` over an FP8 pool."""
+        pool8, sc = self._fp8_args(pool8, kv_scale)
+        bt, qo, sl, q = _i32(block_table), _i32(qo_indptr), _i32(seq_lens), _f64(q_rot)
+        B = sl.shape[0]
+        assert qo.shape == (B + 1,) and qo[-1] == q.shape[0]
+        num_pages, _, Hkv, P, D = pool8.shape
+        out = np.empty(q.shape, np.float64)
+        lse = np.empty(q.shape[:2], np.float64)
+        _check(self.lib.oracle_prefill_attention_fp8(
+            B, q.shape[1], Hkv, D, P, num_pages, bt.shape[1], _ptr(pool8, ctypes.c_uint8),
+            _ptr(sc, ctypes.c_float), _ptr(bt, _I32), _ptr(qo, _I32), _ptr(sl, _I32),
+            _ptr(q, _D), float(scale), _ptr(out, _D), _ptr(lse, _D)))
+        return out, lse
+
+
 _default = None
 
 
@@ -387,3 +431,11 @@ def prefill_append(*args, **kwargs):
 
 def prefill_attention(pool, block_table, qo_indptr, seq_lens, q_rot, scale):
     return default().prefill_attention(pool, block_table, qo_indptr, seq_lens, q_rot, scale)
+
+
+def prefill_append_fp8(*args, **kwargs):
+    return default().prefill_append_fp8(*args, **kwargs)
+
+
+def prefill_attention_fp8(*args, **kwargs):
+    return default().prefill_attention_fp8(*args, **kwargs)

@@ -760,3 +760,103 @@ int oracle_prefill_attention(int B, int Hq, int Hkv, int D, int P, int num_pages
     }
     return 0;
 }
+
+/* oracle_prefill_append with an FP8 pool: the same norm and rotation of every
+ * chunk row; slot t of its sequence receives, for every element,
+ *   K: RNE_e4m3_satfinite(fp32(bf16(k_rot)) / scale_K)
+ *   V: RNE_e4m3_satfinite(fp32(v) / scale_V)
+ * with the scales of the (page, plane, head) the slot lies in (inputs, read
+ * only) -- the decode step's FP8 append applied to each chunk row. */
+int oracle_prefill_append_fp8(int B, int Hq, int Hkv, int D, int P, int num_pages,
+                              int max_blocks, const uint16_t *q, const uint16_t *k,
+                              const uint16_t *v, const uint16_t *w_q, const uint16_t *w_k,
+                              const int32_t *positions, const int32_t *qo_indptr,
+                              const int32_t *seq_lens, const int32_t *block_table,
+                              uint8_t *pool8, const float *kv_scale, double rope_theta,
+                              double eps, double *q_rot, double *k_rot)
+{
+    if (Hkv < 1 || Hq % Hkv != 0 || D % 2 != 0)
+        return -4;
+    int rc = prefill_check(B, P, max_blocks, qo_indptr, seq_lens);
+    if (rc)
+        return rc;
+    oracle_dims d = {B, Hq, Hkv, D, P, num_pages, max_blocks};
+    double *x = (double *)malloc(sizeof(double) * (size_t)D);
+    double *xn = (double *)malloc(sizeof(double) * (size_t)D);
+    double *wq = (double *)malloc(sizeof(double) * (size_t)D);
+    double *wk = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int i = 0; i < D; ++i) {
+        wq[i] = oracle_bf16_to_double(w_q[i]);
+        wk[i] = oracle_bf16_to_double(w_k[i]);
+    }
+    for (int b = 0; b < B && rc == 0; ++b) {
+        int n = qo_indptr[b + 1] - qo_indptr[b], L = seq_lens[b];
+        for (int j = 0; j < n && rc == 0; ++j) {
+            int r = qo_indptr[b] + j, t = L - n + j;
+            double pos = (double)positions[r];
+            for (int h = 0; h < Hq; ++h) {
+                long o = ((long)r * Hq + h) * D;
+                for (int i = 0; i < D; ++i)
+                    x[i] = oracle_bf16_to_double(q[o + i]);
+                oracle_rmsnorm(x, wq, D, eps, xn);
+                oracle_rope_neox(xn, D, pos, rope_theta, q_rot + o);
+            }
+            for (int h = 0; h < Hkv; ++h) {
+                long o = ((long)r * Hkv + h) * D;
+                for (int i = 0; i < D; ++i)
+                    x[i] = oracle_bf16_to_double(k[o + i]);
+                oracle_rmsnorm(x, wk, D, eps, xn);
+                oracle_rope_neox(xn, D, pos, rope_theta, k_rot + o);
+                long rk = pool_row(&d, block_table, b, t, 0, h);
+                long rv = pool_row(&d, block_table, b, t, 1, h);
+                long sk = scale_index(&d, block_table, b, t, 0, h);
+                long sv = scale_index(&d, block_table, b, t, 1, h);
+                if (rk < 0 || rv < 0 || sk < 0 || sv < 0) {
+                    rc = -1;
+                    break;
+                }
+                for (int i = 0; i < D; ++i) {
+                    float kf = (float)oracle_bf16_to_double(oracle_double_to_bf16(k_rot[o + i]));
+                    float vf = (float)oracle_bf16_to_double(v[o + i]);
+                    pool8[rk + i] = oracle_float_to_e4m3_satfinite(kf / kv_scale[sk]);
+                    pool8[rv + i] = oracle_float_to_e4m3_satfinite(vf / kv_scale[sv]);
+                }
+            }
+        }
+    }
+    free(x);
+    free(xn);
+    free(wq);
+    free(wk);
+    return rc;
+}
+
+/* oracle_prefill_attention over an FP8 pool: query row r attends over tokens
+ * 0..t of its sequence, the keys and values dequantized exactly. */
+int oracle_prefill_attention_fp8(int B, int Hq, int Hkv, int D, int P, int num_pages,
+                                 int max_blocks, const uint8_t *pool8, const float *kv_scale,
+                                 const int32_t *block_table, const int32_t *qo_indptr,
+                                 const int32_t *seq_lens, const double *q_rot, double scale,
+                                 double *out, double *lse)
+{
+    if (Hkv < 1 || Hq % Hkv != 0)
+        return -4;
+    int rc = prefill_check(B, P, max_blocks, qo_indptr, seq_lens);
+    if (rc)
+        return rc;
+    oracle_dims d = {B, Hq, Hkv, D, P, num_pages, max_blocks};
+    int G = Hq / Hkv;
+    for (int b = 0; b < B; ++b) {
+        int n = qo_indptr[b + 1] - qo_indptr[b], L = seq_lens[b];
+        for (int j = 0; j < n; ++j) {
+            int r = qo_indptr[b] + j, t = L - n + j;
+            for (int h = 0; h < Hq; ++h) {
+                long o = ((long)r * Hq + h) * D;
+                if (attend_range_fp8(&d, pool8, kv_scale, block_table, b, h / G, q_rot + o,
+                                     scale, 0, t + 1, out + o, lse + (long)r * Hq + h))
+                    return -1;
+            }
+        }
+    }
+    return 0;
+}

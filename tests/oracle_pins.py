@@ -772,4 +772,65 @@ def pin_prefill_rejects_bad_chunks(orc):
         raise AssertionError(f"qo_indptr {bad} accepted")
 
 
+def pin_fp8_prefill_pow2_scales_equal_bf16(orc):
+    """With power-of-two scales the dequantized pool is exact in bf16, so the
+    FP8 causal prefill attention equals the (pinned) bf16 one bit for bit."""
+    rng = np.random.default_rng(37)
+    seq_lens, chunks = [5, 9, 13, 4], [5, 3, 6, 1]
+    pb, qo, *_ = _prefill_problem(rng, seq_lens, chunks)
+    codes, sc = _fp8_pool(rng, pb, pow2=True)
+    deq = _torch_e4m3_values()[codes] * sc[:, :, :, None, None]
+    q_rot = rng.standard_normal((int(qo[-1]), 8, 16))
+    out0, lse0 = orc.prefill_attention(bits_of(deq.astype(np.float32)), pb.bt, qo,
+                                       pb.seq_lens, q_rot, 0.25)
+    out1, lse1 = orc.prefill_attention_fp8(codes, sc, pb.bt, qo, pb.seq_lens, q_rot, 0.25)
+    assert np.array_equal(out0, out1) and np.array_equal(lse0, lse1), "fp8 vs bf16 prefill"
+
+
+def pin_fp8_prefill_chunk_of_one_is_the_decode_step(orc):
+    """One new token per sequence: the FP8 prefill append + attention is the
+    (pinned) FP8 decode layer-step, codes and outputs bit for bit."""
+    rng = np.random.default_rng(38)
+    seq_lens = [3, 17, 31, 8]
+    pb, qo, q, k, v, wq, wk, pos, _ = _prefill_problem(rng, seq_lens, [1, 1, 1, 1])
+    codes, sc = _fp8_pool(rng, pb, pow2=False)
+    sc[pb.bt[1, (17 - 1) // 4]] = 1e-4            # this page saturates
+    a, b_ = codes.copy(), codes.copy()
+    res = orc.prefill_append_fp8(q, k, v, wq, wk, pos, qo, pb.seq_lens, pb.bt, a, sc, 1e6, 1e-6)
+    out, lse = orc.prefill_attention_fp8(a, sc, pb.bt, qo, pb.seq_lens, res["q_rot"], 0.25)
+    ref = orc.decode_layer_fp8(q, k, v, wq, wk, pos, pb.seq_lens, pb.bt, b_, sc, 1e6, 1e-6)
+    assert np.array_equal(a, b_), "fp8 prefill codes vs decode codes"
+    assert np.array_equal(out, ref["out"]) and np.array_equal(lse, ref["lse"])
+
+
+def pin_fp8_prefill_append_codes(orc):
+    """Every chunk row's slot gets the nearest codes (brute force) of
+    fp32(bf16(k_rot)) / scale_K and fp32(v) / scale_V, k_rot being the
+    (pinned) bf16 prefill append's; no other slot changes."""
+    rng = np.random.default_rng(39)
+    seq_lens, chunks = [6, 9, 4], [4, 3, 4]
+    pb, qo, q, k, v, wq, wk, pos, idx = _prefill_problem(rng, seq_lens, chunks, pos_offset=3)
+    codes, sc = _fp8_pool(rng, pb, pow2=False)
+    before = codes.copy()
+    res = orc.prefill_append_fp8(q, k, v, wq, wk, pos, qo, pb.seq_lens, pb.bt, codes, sc, 1e6,
+                                 1e-6)
+    ref = orc.prefill_append(q, k, v, wq, wk, pos, qo, pb.seq_lens, pb.bt, pb.pool.copy(), 1e6,
+                             1e-6)
+    _close(res["k_rot"], ref["k_rot"], 0.0, "fp8 prefill k_rot")
+    table = np.array([orc.e4m3_to_double(c) for c in range(0x7F)])
+    changed = np.zeros(codes.shape, bool)
+    for b in range(len(seq_lens)):
+        for r in range(qo[b], qo[b + 1]):
+            page, off = pb.bt[b, idx[r] // 4], idx[r] % 4
+            for g in range(2):
+                kf = f64(orc.f64_to_bf16_bits(ref["k_rot"][r, g])).astype(np.float32)
+                vf = f64(v[r, g]).astype(np.float32)
+                want_k = [_e4m3_nearest(float(x / sc[page, 0, g]), table) for x in kf]
+                want_v = [_e4m3_nearest(float(x / sc[page, 1, g]), table) for x in vf]
+                assert np.array_equal(codes[page, 0, g, off], want_k), f"K codes row {r}"
+                assert np.array_equal(codes[page, 1, g, off], want_v), f"V codes row {r}"
+            changed[page, :, :, off] = True
+    assert np.array_equal(codes[~changed], before[~changed]), "append touched another slot"
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -85,6 +85,10 @@ MUTANTS = [
      "b, h % Hkv, q_rot + o, scale, 0, t + 1,"),
     ("prefill chunk longer than its sequence accepted", "if (n < 0 || L < 1 || L > max_blocks * P || n > L)",
      "if (n < 0 || L < 1 || L > max_blocks * P)"),
+    ("fp8 prefill causal window", "scale, 0, t + 1, out + o, lse + (long)r * Hq + h))\n                    return -1;\n            }\n        }\n    }\n    return 0;\n}\n",
+     "scale, 0, L, out + o, lse + (long)r * Hq + h))\n                    return -1;\n            }\n        }\n    }\n    return 0;\n}\n"),
+    ("fp8 prefill append slot at the chunk index", "long sk = scale_index(&d, block_table, b, t, 0, h);",
+     "long sk = scale_index(&d, block_table, b, t > 0 ? t - 1 : 0, 0, h);"),
     ("prefill v row of the previous token", "pool[rv + i] = v[o + i];\n                }\n            }\n        }\n    }",
      "pool[rv + i] = v[o > D ? o - D : o + i];\n                }\n            }\n        }\n    }"),
 ]
