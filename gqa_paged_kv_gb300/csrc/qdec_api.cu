@@ -551,6 +551,57 @@ qdec_status attn_decode_impl(const qdec_shape *shape, const float *q_rot, const 
                                               static_cast<cudaStream_t>(stream)));
 }
 
+qdec_status prefill_append_impl(const qdec_shape *shape, int32_t num_tokens, const qdec_bf16 *q,
+                                int64_t q_stride, const qdec_bf16 *k, int64_t k_stride,
+                                const qdec_bf16 *v, int64_t v_stride, const qdec_bf16 *q_norm_w,
+                                const qdec_bf16 *k_norm_w, const int32_t *positions,
+                                const int32_t *qo_indptr, const int32_t *seq_lens,
+                                const int32_t *block_table, const PoolArg &pool, float *q_rot,
+                                int32_t *err_flag, void *stream) {
+    qdec_status st = check_new_token_args(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w,
+                                          k_norm_w, positions, seq_lens, block_table);
+    if (st != QDEC_OK) return st;
+    if ((st = check_pool(shape, pool)) != QDEC_OK) return st;
+    if (num_tokens < 0 || !qo_indptr || !q_rot || !aligned16(q_rot)) return QDEC_ERR_INVALID_ARG;
+    Params p{};
+    fill_common(p, shape, false, pool.fp8);
+    bind_new_token(p, q, q_stride, k, k_stride, v, v_stride, q_norm_w, k_norm_w, positions,
+                   seq_lens, block_table, nullptr);
+    bind_pool(p, pool);
+    p.qo_indptr = qo_indptr;
+    p.T = num_tokens;
+    p.q_rot_out = q_rot;
+    p.err = err_flag;
+    return cuda_status(
+        qdec::launch_prefill_append(p, pool.fp8, static_cast<cudaStream_t>(stream)));
+}
+
+qdec_status prefill_attn_impl(const qdec_shape *shape, int32_t num_tokens, const float *q_rot,
+                              const int32_t *qo_indptr, const int32_t *seq_lens,
+                              const int32_t *block_table, const PoolArg &pool, qdec_bf16 *out,
+                              int32_t *err_flag, void *stream) {
+    qdec_status st = check_shape(shape);
+    if (st != QDEC_OK) return st;
+    if ((st = check_pool(shape, pool)) != QDEC_OK) return st;
+    if (num_tokens < 0 || !q_rot || !qo_indptr || !seq_lens || !block_table || !out)
+        return QDEC_ERR_INVALID_ARG;
+    if (!aligned16(q_rot) || !aligned16(out)) return QDEC_ERR_INVALID_ARG;
+    Params p{};
+    fill_common(p, shape, false, pool.fp8);
+    p.q_rot_in = q_rot;
+    p.qo_indptr = qo_indptr;
+    p.T = num_tokens;
+    p.seq_lens = seq_lens;
+    p.block_table = block_table;
+    bind_pool(p, pool);
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.err = err_flag;
+    CUtensorMap map;
+    if ((st = encode_map(&map, shape, pool)) != QDEC_OK) return st;
+    return cuda_status(
+        qdec::launch_prefill_attention(p, map, pool.fp8, static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -653,48 +704,40 @@ qdec_status qdec_prefill_append_rope(const qdec_shape *shape, int32_t num_tokens
                                      const int32_t *seq_lens, const int32_t *block_table,
                                      qdec_bf16 *kv_pool, float *q_rot, int32_t *err_flag,
                                      void *stream) {
-    qdec_status st = check_new_token_args(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w,
-                                          k_norm_w, positions, seq_lens, block_table);
-    if (st != QDEC_OK) return st;
-    const PoolArg pool{kv_pool, nullptr, false};
-    if ((st = check_pool(shape, pool)) != QDEC_OK) return st;
-    if (num_tokens < 0 || !qo_indptr || !q_rot || !aligned16(q_rot)) return QDEC_ERR_INVALID_ARG;
-    Params p{};
-    fill_common(p, shape, false);
-    bind_new_token(p, q, q_stride, k, k_stride, v, v_stride, q_norm_w, k_norm_w, positions,
-                   seq_lens, block_table, nullptr);
-    bind_pool(p, pool);
-    p.qo_indptr = qo_indptr;
-    p.T = num_tokens;
-    p.q_rot_out = q_rot;
-    p.err = err_flag;
-    return cuda_status(qdec::launch_prefill_append(p, static_cast<cudaStream_t>(stream)));
+    return prefill_append_impl(shape, num_tokens, q, q_stride, k, k_stride, v, v_stride, q_norm_w,
+                               k_norm_w, positions, qo_indptr, seq_lens, block_table,
+                               PoolArg{kv_pool, nullptr, false}, q_rot, err_flag, stream);
+}
+
+qdec_status qdec_prefill_append_rope_fp8(const qdec_shape *shape, int32_t num_tokens,
+                                         const qdec_bf16 *q, int64_t q_stride,
+                                         const qdec_bf16 *k, int64_t k_stride,
+                                         const qdec_bf16 *v, int64_t v_stride,
+                                         const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                                         const int32_t *positions, const int32_t *qo_indptr,
+                                         const int32_t *seq_lens, const int32_t *block_table,
+                                         uint8_t *kv_pool_fp8, const float *kv_scale,
+                                         float *q_rot, int32_t *err_flag, void *stream) {
+    return prefill_append_impl(shape, num_tokens, q, q_stride, k, k_stride, v, v_stride, q_norm_w,
+                               k_norm_w, positions, qo_indptr, seq_lens, block_table,
+                               PoolArg{kv_pool_fp8, kv_scale, true}, q_rot, err_flag, stream);
 }
 
 qdec_status qdec_prefill_attn(const qdec_shape *shape, int32_t num_tokens, const float *q_rot,
                               const int32_t *qo_indptr, const int32_t *seq_lens,
                               const int32_t *block_table, const qdec_bf16 *kv_pool,
                               qdec_bf16 *out, int32_t *err_flag, void *stream) {
-    qdec_status st = check_shape(shape);
-    if (st != QDEC_OK) return st;
-    const PoolArg pool{kv_pool, nullptr, false};
-    if ((st = check_pool(shape, pool)) != QDEC_OK) return st;
-    if (num_tokens < 0 || !q_rot || !qo_indptr || !seq_lens || !block_table || !out)
-        return QDEC_ERR_INVALID_ARG;
-    if (!aligned16(q_rot) || !aligned16(out)) return QDEC_ERR_INVALID_ARG;
-    Params p{};
-    fill_common(p, shape, false);
-    p.q_rot_in = q_rot;
-    p.qo_indptr = qo_indptr;
-    p.T = num_tokens;
-    p.seq_lens = seq_lens;
-    p.block_table = block_table;
-    bind_pool(p, pool);
-    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
-    p.err = err_flag;
-    CUtensorMap map;
-    if ((st = encode_map(&map, shape, pool)) != QDEC_OK) return st;
-    return cuda_status(qdec::launch_prefill_attention(p, map, static_cast<cudaStream_t>(stream)));
+    return prefill_attn_impl(shape, num_tokens, q_rot, qo_indptr, seq_lens, block_table,
+                             PoolArg{kv_pool, nullptr, false}, out, err_flag, stream);
+}
+
+qdec_status qdec_prefill_attn_fp8(const qdec_shape *shape, int32_t num_tokens,
+                                  const float *q_rot, const int32_t *qo_indptr,
+                                  const int32_t *seq_lens, const int32_t *block_table,
+                                  const uint8_t *kv_pool_fp8, const float *kv_scale,
+                                  qdec_bf16 *out, int32_t *err_flag, void *stream) {
+    return prefill_attn_impl(shape, num_tokens, q_rot, qo_indptr, seq_lens, block_table,
+                             PoolArg{kv_pool_fp8, kv_scale, true}, out, err_flag, stream);
 }
 
 qdec_status qdec_attn_merge(const qdec_shape *shape, const int32_t *seq_lens,

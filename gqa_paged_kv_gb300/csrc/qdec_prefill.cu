@@ -21,10 +21,19 @@
 //   with mma.sync (q as bf16 hi + lo, ~16-bit mantissa), masks keys after
 //   each query, keeps the online softmax in fp32 (log2 units) and adds
 //   P V with P taken straight from the score accumulators as bf16.
+//
+// Over an FP8 (E4M3) pool the append stores codes, each row element divided
+// by its (page, plane, head) scale in fp32 and rounded to nearest-even with
+// saturation (the decode step's rule), and the attention brings each page
+// tile as codes plus its two scales, converts the codes to bf16 in shared
+// memory (exact: every E4M3 value is a bf16 value), multiplies the scores by
+// the K scale and folds the V scale into the weights of the value product.
 #include "qdec_internal.h"
 #include "qdec_ptx.cuh"
 #include "qdec.h"
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include <mutex>
@@ -35,9 +44,25 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kPfRows = 16;                 // chunk tokens per work unit (one m16 tile)
 constexpr int kPfStages = 8;                // page tiles in flight per CTA
-constexpr int kPfRingBytes = kPfStages * kTileBytes;
-// after the ring: full[8], empty[8], slot_ok[8], the abort flag, the unit
-constexpr int kPfSmemBytes = kPfRingBytes + 2 * kPfStages * 8 + kPfStages * 4 + 16 + 1024;
+// shared memory: [ring of page tiles][FP8: scale windows of every slot, two
+// converted bf16 tiles][full[8], empty[8], slot_ok[8], the abort flag, the unit]
+template <bool kFp8>
+__host__ __device__ constexpr int pf_ring_bytes() {
+    return kPfStages * (kFp8 ? kFp8TileBytes : kTileBytes);
+}
+template <bool kFp8>
+__host__ __device__ constexpr int pf_extra_bytes() {
+    return kFp8 ? kPfStages * kFp8SlotExtra + 2 * kTileBytes : 0;
+}
+// the tail: full and empty barriers (128 B), slot_ok (32 B), misc (16 B, then
+// 16 B unused), the FP8 conversion barriers (32 B), the slot scale indices
+// (32 B); plus up to 1 KiB lost aligning the base
+constexpr int kPfTailBytes = 2 * kPfStages * 8 + kPfStages * 4 + 32 + 32 + kPfStages * 4;
+static_assert(kPfTailBytes == 256, "tail layout");
+template <bool kFp8>
+__host__ __device__ constexpr int pf_smem_bytes() {
+    return pf_ring_bytes<kFp8>() + pf_extra_bytes<kFp8>() + kPfTailBytes + 1024;
+}
 
 __device__ __forceinline__ void flag_error(int32_t *err, int bits) {
     if (err) atomicOr(err, bits);
@@ -46,6 +71,10 @@ __device__ __forceinline__ void flag_error(int32_t *err, int bits) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
            (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t v) {  // exact: bf16 -> fp32
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -86,6 +115,14 @@ __device__ __forceinline__ bool chunk_ok(const Params &p, int b, int &n, int &L)
 // exact value), and the copy of its value row.
 constexpr int kPfAppendThreads = 256;
 
+// E4M3 codes of a / s and b / s (fp32 division, one rounding each, then
+// nearest-even with saturation to +-448), a in the low byte.
+__device__ __forceinline__ uint16_t quantize_pair_e4m3(float a, float b, float s) {
+    return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(
+        make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s)), __NV_SATFINITE, __NV_E4M3));
+}
+
+template <bool kFp8>
 __global__ void __launch_bounds__(kPfAppendThreads) prefill_append_kernel(
     const __grid_constant__ Params p) {
     __shared__ double cs_d[kRotPairs], sn_d[kRotPairs];
@@ -145,17 +182,34 @@ __global__ void __launch_bounds__(kPfAppendThreads) prefill_append_kernel(
             ((static_cast<int64_t>(page) * 2 * p.Hkv + g) * kPageSize + t % kPageSize) * kHeadDim;
         float nv[4];
         const double rn = norm(p.k + static_cast<int64_t>(r) * p.k_stride + g * kHeadDim, p.w_k, nv);
-        uint32_t *kd = reinterpret_cast<uint32_t *>(p.pool + slot);
-        kd[lane] = pack_bf16x2(static_cast<float>(rn * (nv[0] * c0 - nv[2] * s0)),
-                               static_cast<float>(rn * (nv[1] * c1 - nv[3] * s1)));
-        kd[32 + lane] = pack_bf16x2(static_cast<float>(rn * (nv[2] * c0 + nv[0] * s0)),
-                                    static_cast<float>(rn * (nv[3] * c1 + nv[1] * s1)));
+        const uint32_t k01 = pack_bf16x2(static_cast<float>(rn * (nv[0] * c0 - nv[2] * s0)),
+                                         static_cast<float>(rn * (nv[1] * c1 - nv[3] * s1)));
+        const uint32_t k23 = pack_bf16x2(static_cast<float>(rn * (nv[2] * c0 + nv[0] * s0)),
+                                         static_cast<float>(rn * (nv[3] * c1 + nv[1] * s1)));
         const uint32_t *vs = reinterpret_cast<const uint32_t *>(
             p.v + static_cast<int64_t>(r) * p.v_stride + g * kHeadDim);
-        uint32_t *vd = reinterpret_cast<uint32_t *>(
-            p.pool + slot + static_cast<int64_t>(p.Hkv) * kPageSize * kHeadDim);
-        vd[lane] = vs[lane];
-        vd[32 + lane] = vs[32 + lane];
+        const uint32_t v01 = vs[lane], v23 = vs[32 + lane];
+        const int64_t vslot = slot + static_cast<int64_t>(p.Hkv) * kPageSize * kHeadDim;
+        if constexpr (kFp8) {
+            // the bf16 rows the bf16 pool would hold, divided by the scales
+            const int64_t si = static_cast<int64_t>(page) * 2 * p.Hkv + g;
+            const float sk = p.kv_scale[si], sv = p.kv_scale[si + p.Hkv];
+            const float2 ka = bf16x2_to_float2(k01), kc = bf16x2_to_float2(k23);
+            const float2 va = bf16x2_to_float2(v01), vc = bf16x2_to_float2(v23);
+            uint16_t *kd = reinterpret_cast<uint16_t *>(p.pool8 + slot);
+            uint16_t *vd = reinterpret_cast<uint16_t *>(p.pool8 + vslot);
+            kd[lane] = quantize_pair_e4m3(ka.x, ka.y, sk);
+            kd[32 + lane] = quantize_pair_e4m3(kc.x, kc.y, sk);
+            vd[lane] = quantize_pair_e4m3(va.x, va.y, sv);
+            vd[32 + lane] = quantize_pair_e4m3(vc.x, vc.y, sv);
+        } else {
+            uint32_t *kd = reinterpret_cast<uint32_t *>(p.pool + slot);
+            uint32_t *vd = reinterpret_cast<uint32_t *>(p.pool + vslot);
+            kd[lane] = k01;
+            kd[32 + lane] = k23;
+            vd[lane] = v01;
+            vd[32 + lane] = v23;
+        }
     }
 }
 
@@ -173,6 +227,29 @@ __device__ __forceinline__ void tma_load_page_tile(uint32_t dst, const CUtensorM
         : "memory");
 }
 
+// One FP8 page tile: [plane][token][128 bytes of D], 4 KiB, 128-byte
+// swizzled rows (the pool's 4-D tensor map: bytes of D, token, plane,
+// page*2*Hkv + head).
+__device__ __forceinline__ void tma_load_page_tile_fp8(uint32_t dst, const CUtensorMap *map,
+                                                       int plane_row, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %2, %2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(plane_row), "r"(bar)
+        : "memory");
+}
+
+// Two E4M3 codes (low byte first) as a bf16 pair: exact (every E4M3 value
+// is a bf16 value; NaN stays NaN).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+        static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
+    const float lo = __half2float(__half(__half_raw{h.x}));
+    const float hi = __half2float(__half(__half_raw{h.y}));
+    return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xffff0000u);
+}
+
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_attention_kernel(const __grid_constant__ CUtensorMap kv_map,
                              const __grid_constant__ Params p) {
@@ -180,12 +257,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    uint8_t *tail = sm + kPfRingBytes;
+    constexpr int kSlot = kFp8 ? kFp8TileBytes : kTileBytes;  // ring slot
+    // FP8: after the ring, the scale windows of every slot, then two bf16
+    // tiles the codes are converted into
+    uint8_t *extra = sm + pf_ring_bytes<kFp8>();
+    uint8_t *conv = extra + kPfStages * kFp8SlotExtra;
+    uint8_t *tail = extra + pf_extra_bytes<kFp8>();
     const uint32_t full0 = smem_u32(tail);
     const uint32_t empty0 = full0 + kPfStages * 8;
     volatile int *slot_ok = reinterpret_cast<volatile int *>(tail + 2 * kPfStages * 8);
     volatile int *misc = reinterpret_cast<volatile int *>(tail + 2 * kPfStages * 8 + kPfStages * 4);
-    // misc: [0] abort, [1] sequence, [2] query block, [3] pages issued
+    // misc: [0] abort, [1] sequence, [2] query block, [3] pages issued;
+    // FP8: [4] conv_full[2], conv_empty[2] barriers (8-byte aligned), then
+    // the scale index of every slot
+    const uint32_t convb0 = smem_u32(tail + 2 * kPfStages * 8 + kPfStages * 4 + 32);
+    volatile int *slot_si =
+        reinterpret_cast<volatile int *>(tail + 2 * kPfStages * 8 + kPfStages * 4 + 64);
     const int g = blockIdx.x % p.Hkv;
     const int unit = blockIdx.x / p.Hkv;
 
@@ -234,6 +321,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 mbar_init(full0 + 8 * s, 1);
                 mbar_init(empty0 + 8 * s, kConsumerWarps);  // every warp reads every tile
             }
+            if (kFp8)
+                for (int i = 0; i < 4; ++i) mbar_init(convb0 + 8 * i, kConsumerWarps);
             misc[0] = 0;
             misc[3] = 0;
             fence_mbar_init();
@@ -274,9 +363,24 @@ __global__ void __launch_bounds__(kThreads, 2)
                         stop = true;
                     } else if (pj >= 0 && pj < p.num_pages) {
                         slot_ok[slot] = 1;
-                        mbar_arrive_expect_tx(full, kTileBytes);
-                        tma_load_page_tile(smem_u32(sm + slot * kTileBytes), &kv_map,
-                                           pj * 2 * p.Hkv + g, full);
+                        if constexpr (kFp8) {
+                            // the tile and the two 16-byte windows of kv_scale
+                            // holding its K and V scales (Hkv even: a window
+                            // never straddles pages)
+                            const int64_t si = static_cast<int64_t>(pj) * 2 * p.Hkv + g;
+                            slot_si[slot] = static_cast<int>(((si & 3) | (((si + p.Hkv) & 3) << 2)));
+                            const uint32_t win = smem_u32(extra + slot * kFp8SlotExtra);
+                            mbar_arrive_expect_tx(full, kFp8TileBytes + kFp8SlotExtra);
+                            tma_load_page_tile_fp8(smem_u32(sm + slot * kSlot), &kv_map,
+                                                   pj * 2 * p.Hkv + g, full);
+                            bulk_load(win, p.kv_scale + (si & ~3ll), kScaleWindowBytes, full);
+                            bulk_load(win + kScaleWindowBytes, p.kv_scale + ((si + p.Hkv) & ~3ll),
+                                      kScaleWindowBytes, full);
+                        } else {
+                            mbar_arrive_expect_tx(full, kTileBytes);
+                            tma_load_page_tile(smem_u32(sm + slot * kSlot), &kv_map,
+                                               pj * 2 * p.Hkv + g, full);
+                        }
                     } else {
                         slot_ok[slot] = 0;
                         flag_error(p.err, QDEC_FLAG_BAD_PAGE);
@@ -347,8 +451,68 @@ __global__ void __launch_bounds__(kThreads, 2)
                 aborted = true;
                 break;
             }
-            if (slot_ok[slot]) {
-                const uint32_t tile = smem_u32(sm + slot * kTileBytes);
+            const bool ok = slot_ok[slot];
+            uint32_t tile = smem_u32(sm + slot * kSlot);
+            float sk = 1.f, sv = 1.f;  // FP8: the tile's K and V scales
+            if constexpr (kFp8) {
+                // convert this warp's quarter of the codes into buffer pg & 1
+                // (once its previous tile has been read by every warp), hand
+                // the ring slot back, wait for the other quarters
+                const int cb = pg & 1;
+                if (pg >= 2 && !mbar_wait_bounded(convb0 + 8 * (2 + cb), ((pg >> 1) - 1) & 1,
+                                                  misc, p.wait_cycles)) {
+                    if (lane == 0) {
+                        misc[0] = 1;
+                        flag_error(p.err, QDEC_FLAG_TIMEOUT);
+                    }
+                    aborted = true;
+                    break;
+                }
+                uint8_t *cvt = conv + cb * kTileBytes;
+                if (ok) {
+                    const int si = slot_si[slot];
+                    const float *win = reinterpret_cast<const float *>(extra + slot * kFp8SlotExtra);
+                    sk = win[si & 3];
+                    sv = win[4 + (si >> 2)];
+#pragma unroll
+                    for (int it = 0; it < 2; ++it) {
+                        // item: plane, token, 16 codes of dims 16 c .. 16 c + 15
+                        const int item = (warp * 32 + lane) + 128 * it;
+                        const int plane = item >> 7, tok = (item >> 3) & 15, c = item & 7;
+                        const uint4 codes = *reinterpret_cast<const uint4 *>(
+                            sm + slot * kSlot + plane * kFp8PlaneBytes + tok * 128 +
+                            ((c ^ (tok & 7)) << 4));
+                        const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+                        uint32_t bf[8];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            bf[2 * q] = e4m3x2_to_bf16x2(w[q]);
+                            bf[2 * q + 1] = e4m3x2_to_bf16x2(w[q] >> 16);
+                        }
+                        // bf16 chunks 2c, 2c + 1 of the token: half c / 4
+                        uint8_t *dst = cvt + plane * kPlaneBytes + (c >> 2) * kTileHalfBytes + tok * 128;
+                        *reinterpret_cast<uint4 *>(dst + ((((2 * c) & 7) ^ (tok & 7)) << 4)) =
+                            make_uint4(bf[0], bf[1], bf[2], bf[3]);
+                        *reinterpret_cast<uint4 *>(dst + ((((2 * c + 1) & 7) ^ (tok & 7)) << 4)) =
+                            make_uint4(bf[4], bf[5], bf[6], bf[7]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(empty0 + 8 * slot);     // the codes are no longer needed
+                    mbar_arrive(convb0 + 8 * cb);       // this warp's quarter is in place
+                }
+                if (!mbar_wait_bounded(convb0 + 8 * cb, (pg >> 1) & 1, misc, p.wait_cycles)) {
+                    if (lane == 0) {
+                        misc[0] = 1;
+                        flag_error(p.err, QDEC_FLAG_TIMEOUT);
+                    }
+                    aborted = true;
+                    break;
+                }
+                tile = smem_u32(cvt);
+            }
+            if (ok) {
                 // ---- S = Q K^T: 16 tokens x 16 keys (two n-tiles of 8 keys)
                 // (the hi and lo products in separate accumulators: four
                 // independent chains of 8 MMAs instead of two of 16)
@@ -367,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) s[j][e] += sl[j][e];
+                    for (int e = 0; e < 4; ++e) s[j][e] = (s[j][e] + sl[j][e]) * sk;
                 // ---- causal mask: key 16 pg + 8 j + 2 tq + e against each
                 // row's limit (only tiles that reach past a limit need it)
                 const int kbase = pg * kPageSize + 2 * tq;
@@ -424,11 +588,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 // ---- O += P V: P (16 tokens x 16 keys) from the score
                 // accumulators as the A operand; V rows past the sequence
                 // (possibly not finite) are zeroed in the B fragments
+                // (FP8: the V scale folded into the weights)
                 uint32_t pa[4];
-                pa[0] = pack_bf16x2(pw[0][0], pw[0][1]);
-                pa[1] = pack_bf16x2(pw[0][2], pw[0][3]);
-                pa[2] = pack_bf16x2(pw[1][0], pw[1][1]);
-                pa[3] = pack_bf16x2(pw[1][2], pw[1][3]);
+                pa[0] = pack_bf16x2(pw[0][0] * sv, pw[0][1] * sv);
+                pa[1] = pack_bf16x2(pw[0][2] * sv, pw[0][3] * sv);
+                pa[2] = pack_bf16x2(pw[1][0] * sv, pw[1][1] * sv);
+                pa[3] = pack_bf16x2(pw[1][2] * sv, pw[1][3] * sv);
                 const int ntok = min(kPageSize, L - pg * kPageSize);  // keys of this page in the sequence
                 // this thread's B elements hold keys 2 tq, 2 tq + 1 (b0) and +8 (b1)
                 const uint32_t keep0 = (2 * tq < ntok ? 0x0000ffffu : 0u) |
@@ -451,7 +616,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+            if (lane == 0) {
+                if (kFp8)
+                    mbar_arrive(convb0 + 8 * (2 + (pg & 1)));  // buffer pg & 1 read
+                else
+                    mbar_arrive(empty0 + 8 * slot);
+            }
         }
         // ---- normalise and write the block's rows of head h
 #pragma unroll
@@ -486,35 +656,45 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 std::mutex g_pf_mu;
-bool g_pf_smem_set[64];
+bool g_pf_smem_set[2][64];
 
 }  // namespace
 
-cudaError_t launch_prefill_append(const Params &p, cudaStream_t s) {
+cudaError_t launch_prefill_append(const Params &p, bool fp8, cudaStream_t s) {
     if (p.T <= 0) return cudaSuccess;
-    prefill_append_kernel<<<p.T, kPfAppendThreads, 0, s>>>(p);
+    if (fp8)
+        prefill_append_kernel<true><<<p.T, kPfAppendThreads, 0, s>>>(p);
+    else
+        prefill_append_kernel<false><<<p.T, kPfAppendThreads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_attention(const Params &p, const CUtensorMap &kv_map, cudaStream_t s) {
-    if (p.T <= 0) return cudaSuccess;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 63;
+template <bool kFp8>
+cudaError_t launch_attn(const Params &p, const CUtensorMap &kv_map, int dev, cudaStream_t s) {
     {
         std::lock_guard<std::mutex> lock(g_pf_mu);
-        if (!g_pf_smem_set[dev]) {
-            const cudaError_t e = cudaFuncSetAttribute(
-                prefill_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmemBytes);
+        if (!g_pf_smem_set[kFp8 ? 1 : 0][dev]) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(prefill_attention_kernel<kFp8>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, pf_smem_bytes<kFp8>());
             if (e != cudaSuccess) return e;
-            g_pf_smem_set[dev] = true;
+            g_pf_smem_set[kFp8 ? 1 : 0][dev] = true;
         }
     }
     // units: at most T / 16 + B blocks of 16 chunk rows, times the KV heads
     const int64_t units = (static_cast<int64_t>(p.T) + kPfRows - 1) / kPfRows + p.B;
-    prefill_attention_kernel<<<static_cast<unsigned>(units * p.Hkv), kThreads, kPfSmemBytes, s>>>(
-        kv_map, p);
+    prefill_attention_kernel<kFp8>
+        <<<static_cast<unsigned>(units * p.Hkv), kThreads, pf_smem_bytes<kFp8>(), s>>>(kv_map, p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_attention(const Params &p, const CUtensorMap &kv_map, bool fp8,
+                                     cudaStream_t s) {
+    if (p.T <= 0) return cudaSuccess;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 63;
+    return fp8 ? launch_attn<true>(p, kv_map, dev, s) : launch_attn<false>(p, kv_map, dev, s);
 }
 
 }  // namespace qdec

@@ -37,7 +37,8 @@ EXPORTS = ("qdec_workspace_bytes", "qdec_workspace_init", "qdec_rope_table_bytes
            "qdec_rope_table", "qdec_append_rope", "qdec_attn_split", "qdec_attn_merge",
            "qdec_attn_decode", "qdec_step", "qdec_qkv_append_rope", "qdec_qkv_pack_weights",
            "qdec_append_rope_fp8", "qdec_attn_split_fp8", "qdec_attn_decode_fp8",
-           "qdec_prefill_append_rope", "qdec_prefill_attn",
+           "qdec_prefill_append_rope", "qdec_prefill_attn", "qdec_prefill_append_rope_fp8",
+           "qdec_prefill_attn_fp8",
            "qdec_step_fp8",
            "qdec_step_static_scratch", "qdec_check_error", "qdec_status_string", "qdec_version")
 
@@ -112,6 +113,11 @@ def _load():
     lib.qdec_prefill_append_rope.restype = st
     lib.qdec_prefill_attn.argtypes = [sp, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.qdec_prefill_attn.restype = st
+    lib.qdec_prefill_append_rope_fp8.argtypes = [sp, ctypes.c_int32, vp, i64, vp, i64, vp, i64,
+                                                 vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.qdec_prefill_append_rope_fp8.restype = st
+    lib.qdec_prefill_attn_fp8.argtypes = [sp, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.qdec_prefill_attn_fp8.restype = st
     lib.qdec_step.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                               vp, vp, vp]
     lib.qdec_step.restype = st
@@ -240,6 +246,26 @@ def qdec_prefill_attn(shape: Shape, q_rot, qo_indptr, seq_lens, block_table, kv_
         ctypes.byref(shape.c()), q_rot.shape[0], _ptr(q_rot), _ptr(qo_indptr), _ptr(seq_lens),
         _ptr(block_table), _ptr(kv_pool), _ptr(out), _ptr(err_flag), _stream(stream)),
         "qdec_prefill_attn")
+
+
+def qdec_prefill_append_rope_fp8(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, qo_indptr,
+                                 seq_lens, block_table, kv_pool_fp8, kv_scale, q_rot,
+                                 err_flag=None, stream=None):
+    pool, scale = _fp8_pool(kv_pool_fp8, kv_scale)
+    _raise(_lib.qdec_prefill_append_rope_fp8(
+        ctypes.byref(shape.c()), q.shape[0], _ptr(q), _rows(q, "q"), _ptr(k), _rows(k, "k"),
+        _ptr(v), _rows(v, "v"), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions), _ptr(qo_indptr),
+        _ptr(seq_lens), _ptr(block_table), pool, scale, _ptr(q_rot), _ptr(err_flag),
+        _stream(stream)), "qdec_prefill_append_rope_fp8")
+
+
+def qdec_prefill_attn_fp8(shape: Shape, q_rot, qo_indptr, seq_lens, block_table, kv_pool_fp8,
+                          kv_scale, out, err_flag=None, stream=None):
+    pool, scale = _fp8_pool(kv_pool_fp8, kv_scale)
+    _raise(_lib.qdec_prefill_attn_fp8(
+        ctypes.byref(shape.c()), q_rot.shape[0], _ptr(q_rot), _ptr(qo_indptr), _ptr(seq_lens),
+        _ptr(block_table), pool, scale, _ptr(out), _ptr(err_flag), _stream(stream)),
+        "qdec_prefill_attn_fp8")
 
 
 def qdec_attn_merge(shape: Shape, seq_lens, workspace, out, err_flag=None, stream=None):

@@ -404,3 +404,22 @@ def prefill_case(seq_lens, chunks, seed: int = 7, device="cuda", poison: bool = 
         block_table=torch.from_numpy(bt).to(device), pool=pool.to(device),
         q=mk(T, Hq, D).to(device), k=mk(T, Hkv, D).to(device), v=mk(T, Hkv, D).to(device),
         w_q=w().to(device), w_k=w().to(device), max_blocks=mb, num_pages=total)
+
+
+def prefill_case_fp8(seq_lens, chunks, seed: int = 7, device="cuda", pos_offset: int = 0):
+    """prefill_case held in an FP8 pool: the same draws as E4M3 codes with
+    per-(page, plane, head) scales amax/448 (PyTorch's float8_e4m3fn cast);
+    every element past a sequence's last token and every unreferenced page is
+    the NaN code 0x7F.  Returns (case, codes, scales)."""
+    c = prefill_case(seq_lens, chunks, seed=seed, device=device, poison=False,
+                     pos_offset=pos_offset)
+    codes, sc = _to_fp8(c.pool)
+    P = PAGE_SIZE
+    used = torch.zeros(codes.shape[0], P, dtype=torch.bool, device=codes.device)
+    bt = c.block_table.cpu().numpy()
+    for b, L in enumerate(seq_lens):
+        t = torch.arange(int(L))
+        used[torch.as_tensor(bt[b, (t // P).numpy()], device=codes.device),
+             (t % P).to(codes.device)] = True
+    codes.masked_fill_(~used[:, None, None, :, None].expand_as(codes), 0x7F)
+    return c, codes, sc

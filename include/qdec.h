@@ -264,7 +264,7 @@ qdec_status qdec_qkv_pack_weights(const qdec_shape *shape, int32_t hidden,
  * + j of it (seq_lens counted after the chunk, n_b <= seq_lens[b]).  The
  * block table must map every page up to token seq_lens[b] - 1.  Sequences
  * whose chunk is malformed are skipped and flagged QDEC_FLAG_BAD_SEQLEN.
- * bf16 pool only; shape->batch = B sequences. */
+ * shape->batch = B sequences.  FP8-pool forms follow the FP8 section below. */
 
 /* Steps 1-3 for every chunk row r: RMSNorm + NeoX RoPE at positions[r] of
  * its query rows (q [num_tokens][Hq][D], row stride q_stride) into q_rot
@@ -339,6 +339,25 @@ qdec_status qdec_attn_decode_fp8(const qdec_shape *shape, const float *q_rot,
                                  const int32_t *block_table, const int32_t *seq_lens,
                                  void *workspace, size_t workspace_bytes, qdec_bf16 *out,
                                  int32_t *err_flag, void *stream);
+
+/* Chunked prefill over an FP8 pool: qdec_prefill_append_rope storing the
+ * chunk rows' codes (the append rule above, each row with the scales of its
+ * slot's (page, plane, head)), and qdec_prefill_attn over the dequantized
+ * pool.  kv_scale is read only. */
+qdec_status qdec_prefill_append_rope_fp8(const qdec_shape *shape, int32_t num_tokens,
+                                         const qdec_bf16 *q, int64_t q_stride,
+                                         const qdec_bf16 *k, int64_t k_stride,
+                                         const qdec_bf16 *v, int64_t v_stride,
+                                         const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                                         const int32_t *positions, const int32_t *qo_indptr,
+                                         const int32_t *seq_lens, const int32_t *block_table,
+                                         uint8_t *kv_pool_fp8, const float *kv_scale,
+                                         float *q_rot, int32_t *err_flag, void *stream);
+qdec_status qdec_prefill_attn_fp8(const qdec_shape *shape, int32_t num_tokens,
+                                  const float *q_rot, const int32_t *qo_indptr,
+                                  const int32_t *seq_lens, const int32_t *block_table,
+                                  const uint8_t *kv_pool_fp8, const float *kv_scale,
+                                  qdec_bf16 *out, int32_t *err_flag, void *stream);
 
 /* qdec_step over an FP8 pool: one launch for steps 1-4, the new key and
  * value quantized into their slot as above.  Same launch flags, workspace

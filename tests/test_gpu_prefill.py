@@ -170,3 +170,83 @@ def test_prefill_bad_page_is_flagged(bad_entry):
     assert st == q.QDEC_ERR_DEVICE_BOUNDS and flags & q.QDEC_FLAG_BAD_PAGE, (st, flags)
     rows = np.r_[0:20, 50:90]
     parity.assert_out_close(out[rows], res["out"][rows])
+
+
+# ------------------------------------------------------------------- FP8 pool --
+
+def _run_fp8(c, codes, sc, B):
+    q = parity.qdec()
+    shape = _shape(c, B)
+    T = c.q.shape[0]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q_rot = torch.empty((T, 32, 128), dtype=torch.float32, device="cuda")
+    out = torch.full((T, 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    q.qdec_prefill_append_rope_fp8(shape, c.q, c.k, c.v, c.w_q, c.w_k, c.positions, c.qo_indptr,
+                                   c.seq_lens, c.block_table, codes, sc, q_rot, err)
+    q.qdec_prefill_attn_fp8(shape, q_rot, c.qo_indptr, c.seq_lens, c.block_table, codes, sc, out,
+                            err)
+    return q_rot, out, err
+
+
+FP8_CASES = [([37], [37]), ([300, 17, 1000], [20, 17, 1]), ([64, 65, 31], [48, 1, 15]),
+             ([500, 40, 77, 250], [0, 40, 33, 0]), ([2048], [200])]
+
+
+@pytest.mark.parametrize("seq_lens,chunks", FP8_CASES, ids=lambda x: str(x)[:40])
+def test_prefill_fp8_matches_oracle(seq_lens, chunks):
+    """FP8 pool: q_rot and out as for bf16; the appended V codes equal the
+    oracle's bit for bit (both divide fp32(v) by the scale and round once);
+    the K codes too, or at most one E4M3 step apart where the kernel's bf16
+    key (within one bf16 step of the exact value) sits across a rounding
+    boundary from the oracle's; nothing outside the chunk's slots changes."""
+    c, codes, sc = wl.prefill_case_fp8(seq_lens, chunks, seed=sum(seq_lens) % 89)
+    before = codes.cpu().numpy().copy()
+    pool = before.copy()
+    sc_h = sc.cpu().numpy()
+    qo, L, bt = c.qo_indptr.cpu().numpy(), c.seq_lens.cpu().numpy(), c.block_table.cpu().numpy()
+    res = oracle.prefill_append_fp8(wl.bf16_bits(c.q), wl.bf16_bits(c.k), wl.bf16_bits(c.v),
+                                    wl.bf16_bits(c.w_q), wl.bf16_bits(c.w_k),
+                                    c.positions.cpu().numpy(), qo, L, bt, pool, sc_h, 1e6,
+                                    float(np.float32(1e-6)))
+    ref_out, _ = oracle.prefill_attention_fp8(pool, sc_h, bt, qo, L, res["q_rot"],
+                                              1 / math.sqrt(128))
+    q_rot, out, err = _run_fp8(c, codes, sc, len(seq_lens))
+    st, flags = parity.qdec().qdec_check_error(err)
+    assert st == 0 and flags == 0, (st, flags)
+    g = q_rot.double().cpu().numpy()
+    assert np.all(np.abs(g - res["q_rot"]) <= parity.QROT_TOL * (1 + np.abs(res["q_rot"])))
+    parity.assert_out_close(out, ref_out)
+    got = codes.cpu().numpy()
+    changed = np.zeros(got.shape, bool)
+    k_off = 0
+    for b in range(len(L)):
+        n = qo[b + 1] - qo[b]
+        for j in range(n):
+            t = L[b] - n + j
+            page, off = bt[b, t // 16], t % 16
+            assert np.array_equal(got[page, 1, :, off], pool[page, 1, :, off]), f"V codes t={t}"
+            kg = got[page, 0, :, off].astype(np.int32)
+            kr = pool[page, 0, :, off].astype(np.int32)
+            diff = kg != kr
+            # adjacent codes of the same sign differ by one in their low 7 bits
+            assert np.all(((kg & 0x80) == (kr & 0x80)) | ~diff), f"K code sign t={t}"
+            assert np.all(np.abs((kg & 0x7F) - (kr & 0x7F)) <= 1), f"K codes t={t}"
+            k_off += int(diff.sum())
+            changed[page, :, :, off] = True
+    assert k_off <= max(2, got.size // 100000), f"{k_off} K codes one step off"
+    assert np.array_equal(got[~changed], before[~changed]), "append touched another slot"
+
+
+def test_prefill_fp8_chunk_of_one_equals_fp8_decode():
+    """One token per sequence over an FP8 pool: the prefill pair and the FP8
+    decode attention on the same appended pool agree closely."""
+    q = parity.qdec()
+    c, codes, sc = wl.prefill_case_fp8([300, 17, 1000, 64], [1, 1, 1, 1], seed=15)
+    shape = _shape(c, 4)
+    q_rot, out, err = _run_fp8(c, codes, sc, 4)
+    ws = q.alloc_workspace(shape)
+    out_d = torch.empty_like(out)
+    q.qdec_attn_decode_fp8(shape, q_rot, codes, sc, c.block_table, c.seq_lens, ws, out_d, err)
+    st, flags = q.qdec_check_error(err)
+    assert st == 0 and flags == 0
+    assert torch.allclose(out.float(), out_d.float(), rtol=2 ** -7, atol=8e-3)
