@@ -681,8 +681,15 @@ def run_prefill(args, dist: Dist):
     torch.cuda.set_device(dev)
     P = args.prefill
     L = args.layers or 36
-    name = f"prefill-b1-prompt{P}-{L}layer"
-    cases = [wl.prefill_case([P], [P], seed=1000 + l, device="cuda", poison=False) for l in range(L)]
+    fp8 = args.kv == "fp8"
+    name = f"prefill-b1-prompt{P}-{L}layer" + ("-fp8kv" if fp8 else "")
+    if fp8:   # E4M3 codes and per-(page, plane, head) scales of the same draws
+        made = [wl.prefill_case_fp8([P], [P], seed=1000 + l, device="cuda") for l in range(L)]
+        cases = [m[0] for m in made]
+        pools8 = [(m[1], m[2]) for m in made]
+    else:
+        cases = [wl.prefill_case([P], [P], seed=1000 + l, device="cuda", poison=False)
+                 for l in range(L)]
     c0 = cases[0]
     shape = qdec.Shape(batch=1, num_pages=c0.num_pages, max_blocks_per_seq=c0.max_blocks,
                        max_seq_len=c0.max_blocks * 16)
@@ -696,6 +703,15 @@ def run_prefill(args, dist: Dist):
         def fn():
             for l, c in enumerate(cases):
                 q, k, v = ins[l]
+                if fp8:
+                    codes, sc = pools8[l]
+                    qdec.qdec_prefill_append_rope_fp8(shape, q, k, v, c.w_q, c.w_k, c.positions,
+                                                      c.qo_indptr, c.seq_lens, c.block_table,
+                                                      codes, sc, q_rot, err, stream=stream)
+                    qdec.qdec_prefill_attn_fp8(shape, q_rot, c.qo_indptr, c.seq_lens,
+                                               c.block_table, codes, sc, outs[l], err,
+                                               stream=stream)
+                    continue
                 qdec.qdec_prefill_append_rope(shape, q, k, v, c.w_q, c.w_k, c.positions,
                                               c.qo_indptr, c.seq_lens, c.block_table, c.pool,
                                               q_rot, err, stream=stream)
@@ -744,8 +760,13 @@ def run_prefill(args, dist: Dist):
     with torch.cuda.stream(stream):
         with torch.cuda.graph(ga, stream=stream):
             for l, c in enumerate(cases):
-                qdec.qdec_prefill_attn(shape, q_rot, c.qo_indptr, c.seq_lens, c.block_table,
-                                       c.pool, out[l], err, stream=stream)
+                if fp8:
+                    qdec.qdec_prefill_attn_fp8(shape, q_rot, c.qo_indptr, c.seq_lens,
+                                               c.block_table, *pools8[l], out[l], err,
+                                               stream=stream)
+                else:
+                    qdec.qdec_prefill_attn(shape, q_rot, c.qo_indptr, c.seq_lens, c.block_table,
+                                           c.pool, out[l], err, stream=stream)
         for _ in range(3):
             ga.replay()
         reps = max(5, args.steps // 4)
@@ -802,15 +823,26 @@ def run_prefill(args, dist: Dist):
 
         import oracle
         Pc = min(P, 256)   # bounded sample: one layer, a fresh prompt of Pc tokens
-        c = wl.prefill_case([Pc], [Pc], seed=1000, device="cpu", poison=False)
-        pool = wl.bf16_bits(c.pool).copy()
+        ins_h = None
+        if fp8:
+            c, codes_h, sc_h = wl.prefill_case_fp8([Pc], [Pc], seed=1000, device="cpu")
+            pool = codes_h.numpy().copy()
+            sc_h = sc_h.numpy()
+        else:
+            c = wl.prefill_case([Pc], [Pc], seed=1000, device="cpu", poison=False)
+            pool = wl.bf16_bits(c.pool).copy()
+        ins_h = (wl.bf16_bits(c.q), wl.bf16_bits(c.k), wl.bf16_bits(c.v), wl.bf16_bits(c.w_q),
+                 wl.bf16_bits(c.w_k), c.positions.numpy(), c.qo_indptr.numpy(),
+                 c.seq_lens.numpy(), c.block_table.numpy())
         t0 = time.perf_counter()
-        res = oracle.prefill_append(wl.bf16_bits(c.q), wl.bf16_bits(c.k), wl.bf16_bits(c.v),
-                                    wl.bf16_bits(c.w_q), wl.bf16_bits(c.w_k),
-                                    c.positions.numpy(), c.qo_indptr.numpy(), c.seq_lens.numpy(),
-                                    c.block_table.numpy(), pool, 1e6, float(np.float32(1e-6)))
-        oracle.prefill_attention(pool, c.block_table.numpy(), c.qo_indptr.numpy(),
-                                 c.seq_lens.numpy(), res["q_rot"], 1 / math.sqrt(128))
+        if fp8:
+            res = oracle.prefill_append_fp8(*ins_h, pool, sc_h, 1e6, float(np.float32(1e-6)))
+            oracle.prefill_attention_fp8(pool, sc_h, c.block_table.numpy(), c.qo_indptr.numpy(),
+                                         c.seq_lens.numpy(), res["q_rot"], 1 / math.sqrt(128))
+        else:
+            res = oracle.prefill_append(*ins_h, pool, 1e6, float(np.float32(1e-6)))
+            oracle.prefill_attention(pool, c.block_table.numpy(), c.qo_indptr.numpy(),
+                                     c.seq_lens.numpy(), res["q_rot"], 1 / math.sqrt(128))
         secs = time.perf_counter() - t0
         cpu = {"value": round(prefill_flops([Pc], [Pc]) / secs / 1e12, 9), "unit": "TFLOP/s",
                "cores": 1, "kind": "oracle",
@@ -822,7 +854,9 @@ def run_prefill(args, dist: Dist):
             "metric": PREFILL_METRIC, "value": round(value, 3), "unit": "TFLOP/s",
             "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16 (mma.sync bf16, q as hi+lo, f32 accumulate)",
+            "vs_baseline": None,
+            "dtype": ("e4m3 KV converted to bf16 in shared memory" if fp8 else "bf16")
+                     + " (mma.sync bf16, q as hi+lo, f32 accumulate)",
             "data": "synthetic (seeded N(0,1) bf16 q/k/v, U(0.5,1.5) norm weights)",
             "us_per_layer_step": round(ms_step * 1e3 / L, 3),
             "config": {"workload": name, "batch": 1, "prompt": P, "layers": L,
