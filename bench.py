@@ -71,18 +71,19 @@ KERNEL_SOURCES = {
 # profiles/), keyed by workload; used only while the kernel source hash
 # still matches the one the counters were taken on.
 TRAFFIC = {
-    "b8-ctx256to384-36layer": {"kernel_sha": "5478e33b7b4d6ead", "bytes_per_launch": 10900038},
-    "b1-ctx8192-spikes-36layer": {"kernel_sha": "5478e33b7b4d6ead", "bytes_per_launch": 33634048},
-    "b64-ragged128to16384-sharedpool-36layer": {"kernel_sha": "5478e33b7b4d6ead",
-                                                "bytes_per_launch": 1038092457},
-    "b64-ragged128to16384-sharedpool-36layer-fp8kv": {"kernel_sha": "5478e33b7b4d6ead",
-                                                      "bytes_per_launch": 524768297},
+    "b8-ctx256to384-36layer": {"kernel_sha": "860bc4989aee25ef", "bytes_per_launch": 10899397},
+    "b1-ctx8192-spikes-36layer": {"kernel_sha": "860bc4989aee25ef", "bytes_per_launch": 33647616},
+    "b64-ragged128to16384-sharedpool-36layer": {"kernel_sha": "860bc4989aee25ef",
+                                                "bytes_per_launch": 1038090004},
+    "b64-ragged128to16384-sharedpool-36layer-fp8kv": {"kernel_sha": "860bc4989aee25ef",
+                                                      "bytes_per_launch": 524760185},
     # --prefill 2048: the causal prefill attention kernel
-    "prefill-b1-prompt2048-36layer": {"kernel_sha": "a745e98784a430d3", "bytes_per_launch": 41993045},
+    "prefill-b1-prompt2048-36layer": {"kernel_sha": "485da7eb1438d8dd", "bytes_per_launch": 41996779},
+    "prefill-b1-prompt2048-36layer-fp8kv": {"kernel_sha": "485da7eb1438d8dd", "bytes_per_launch": 37814763},
     # --qkv: the projection kernel
-    "b8-ctx256to384-36layer-qkv2560": {"kernel_sha": "0f336e8e14cd48d0", "bytes_per_launch": 31541252},
-    "b64-ragged128to16384-sharedpool-36layer-qkv2560": {"kernel_sha": "0f336e8e14cd48d0",
-                                                        "bytes_per_launch": 31896777},
+    "b8-ctx256to384-36layer-qkv2560": {"kernel_sha": "f601289afdbb7741", "bytes_per_launch": 31541255},
+    "b64-ragged128to16384-sharedpool-36layer-qkv2560": {"kernel_sha": "f601289afdbb7741",
+                                                        "bytes_per_launch": 31896932},
 }
 
 # The CPU timings sample the first few layers of a workload (same shapes and
