@@ -112,6 +112,9 @@ class Oracle:
         lib.oracle_prefill_attention.argtypes = ([ci] * 7 + [u16p] + [i32p] * 3 + [dp, _D]
                                                  + [dp] * 2)
         lib.oracle_prefill_attention.restype = ci
+        lib.oracle_qkv_append_fp8.argtypes = ([ci] * 8 + [u16p] * 4 + [i32p] * 3 + [u8p, f32p]
+                                              + [_D] * 2 + [dp] * 3)
+        lib.oracle_qkv_append_fp8.restype = ci
         lib.oracle_prefill_append_fp8.argtypes = ([ci] * 7 + [u16p] * 5 + [i32p] * 4
                                                   + [u8p, f32p] + [_D] * 2 + [dp] * 2)
         lib.oracle_prefill_append_fp8.restype = ci
@@ -294,6 +297,29 @@ class Oracle:
         return res
 
 
+    def qkv_append_fp8(self, x, w_qkv, w_q, w_k, positions, seq_lens, block_table, pool8,
+                       kv_scale, rope_theta: float, eps: float, num_q_heads: int,
+                       num_kv_heads: int):
+        """:meth:`qkv_append` with an FP8 pool (uint8, updated in place) and its
+        scales (float32 [pages][2][Hkv], read only)."""
+        x, w, w_q, w_k = _u16(x), _u16(w_qkv), _u16(w_q), _u16(w_k)
+        pos, sl, bt = _i32(positions), _i32(seq_lens), _i32(block_table)
+        assert pool8.dtype == np.uint8 and pool8.flags["C_CONTIGUOUS"]
+        _, sc = self._fp8_args(pool8, kv_scale)
+        B, hidden = x.shape
+        num_pages, _, Hkv, P, D = pool8.shape
+        Hq = num_q_heads
+        assert Hkv == num_kv_heads and w.shape == ((Hq + 2 * Hkv) * D, hidden)
+        res = {"q_rot": np.empty((B, Hq, D)), "k_rot": np.empty((B, Hkv, D)),
+               "v": np.empty((B, Hkv, D))}
+        _check(self.lib.oracle_qkv_append_fp8(
+            B, Hq, Hkv, D, P, num_pages, bt.shape[1], hidden,
+            _ptr(x, _U16), _ptr(w, _U16), _ptr(w_q, _U16), _ptr(w_k, _U16),
+            _ptr(pos, _I32), _ptr(sl, _I32), _ptr(bt, _I32), _ptr(pool8, ctypes.c_uint8),
+            _ptr(sc, ctypes.c_float), float(rope_theta), float(eps),
+            _ptr(res["q_rot"], _D), _ptr(res["k_rot"], _D), _ptr(res["v"], _D)))
+        return res
+
     # ------------------------------------------------------------- prefill
     def prefill_append(self, q, k, v, w_q, w_k, positions, qo_indptr, seq_lens, block_table,
                        pool, rope_theta: float, eps: float):
@@ -439,3 +465,7 @@ def prefill_append_fp8(*args, **kwargs):
 
 def prefill_attention_fp8(*args, **kwargs):
     return default().prefill_attention_fp8(*args, **kwargs)
+
+
+def qkv_append_fp8(*args, **kwargs):
+    return default().qkv_append_fp8(*args, **kwargs)

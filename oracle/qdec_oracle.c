@@ -860,3 +860,42 @@ int oracle_prefill_attention_fp8(int B, int Hq, int Hkv, int D, int P, int num_p
     }
     return 0;
 }
+
+/* oracle_qkv_append with an FP8 pool: the projection, norm and rotation as
+ * above into the bf16 rows the bf16 pool would receive (bf16(k_rot),
+ * bf16(v)), then for every element of slot seq_lens[b]-1
+ *   code = RNE_e4m3_satfinite(fp32(bf16 row) / scale)
+ * with the scales of the slot's (page, plane, head) -- the FP8 append rule
+ * of the decode step.  kv_scale is read only. */
+int oracle_qkv_append_fp8(int B, int Hq, int Hkv, int D, int P, int num_pages, int max_blocks,
+                          int hidden, const uint16_t *x, const uint16_t *w_qkv,
+                          const uint16_t *w_q, const uint16_t *w_k, const int32_t *positions,
+                          const int32_t *seq_lens, const int32_t *block_table, uint8_t *pool8,
+                          const float *kv_scale, double rope_theta, double eps, double *q_rot,
+                          double *k_rot, double *v_out)
+{
+    oracle_dims d = {B, Hq, Hkv, D, P, num_pages, max_blocks};
+    size_t n = (size_t)num_pages * 2 * (size_t)Hkv * (size_t)P * (size_t)D;
+    uint16_t *rows = (uint16_t *)calloc(n, sizeof(uint16_t));
+    int rc = oracle_qkv_append(B, Hq, Hkv, D, P, num_pages, max_blocks, hidden, x, w_qkv, w_q,
+                               w_k, positions, seq_lens, block_table, rows, rope_theta, eps,
+                               q_rot, k_rot, v_out);
+    for (int b = 0; b < B && rc == 0; ++b) {
+        int L = seq_lens[b];
+        for (int g = 0; g < Hkv; ++g) {
+            for (int kv = 0; kv < 2; ++kv) {
+                long r = pool_row(&d, block_table, b, L - 1, kv, g);
+                long si = scale_index(&d, block_table, b, L - 1, kv, g);
+                if (r < 0 || si < 0) {
+                    rc = -1;
+                    break;
+                }
+                for (int i = 0; i < D; ++i)
+                    pool8[r + i] = oracle_float_to_e4m3_satfinite(
+                        (float)oracle_bf16_to_double(rows[r + i]) / kv_scale[si]);
+            }
+        }
+    }
+    free(rows);
+    return rc;
+}

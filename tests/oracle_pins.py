@@ -833,4 +833,36 @@ def pin_fp8_prefill_append_codes(orc):
     assert np.array_equal(codes[~changed], before[~changed]), "append touched another slot"
 
 
+def pin_qkv_fp8_append_codes(orc):
+    """The projection into an FP8 pool: the same q_rot, k_rot and v as the
+    (pinned) bf16 projection; slot L-1 of every (sequence, plane, head) gets
+    the nearest codes (brute force) of the bf16 row the bf16 pool receives
+    divided by the slot's scale in fp32, saturating where the scale is too
+    small; no other slot changes."""
+    rng = np.random.default_rng(40)
+    Hq, Hkv = 8, 2
+    pb, x, w, wq, wk, pos = _qkv_problem(rng, [1, 4, 5, 16, 22])
+    codes, sc = _fp8_pool(rng, pb, pow2=False)
+    sc[pb.bt[3, (16 - 1) // 4]] = 1e-4            # this page saturates
+    before = codes.copy()
+    res = orc.qkv_append_fp8(x, w, wq, wk, pos, pb.seq_lens, pb.bt, codes, sc, 1e6, 1e-6, Hq, Hkv)
+    ref = orc.qkv_append(x, w, wq, wk, pos, pb.seq_lens, pb.bt, pb.pool.copy(), 1e6, 1e-6, Hq, Hkv)
+    for key in ("q_rot", "k_rot", "v"):
+        _close(res[key], ref[key], 0.0, f"qkv fp8 {key}")
+    table = np.array([orc.e4m3_to_double(c) for c in range(0x7F)])
+    changed = np.zeros(codes.shape, bool)
+    saturated = 0
+    for b, L in enumerate(pb.seq_lens):
+        page, off = pb.bt[b, (L - 1) // 4], (L - 1) % 4
+        for g in range(Hkv):
+            for plane, key in ((0, "k_rot"), (1, "v")):
+                row = f64(orc.f64_to_bf16_bits(ref[key][b, g])).astype(np.float32)
+                want = [_e4m3_nearest(float(v_ / sc[page, plane, g]), table) for v_ in row]
+                assert np.array_equal(codes[page, plane, g, off], want), f"codes b={b} {key}"
+                saturated += int(np.sum((codes[page, plane, g, off] & 0x7F) == 0x7E))
+        changed[page, :, :, off] = True
+    assert saturated > 0, "the saturating page did not saturate"
+    assert np.array_equal(codes[~changed], before[~changed]), "append touched another slot"
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -89,6 +89,10 @@ MUTANTS = [
      "scale, 0, L, out + o, lse + (long)r * Hq + h))\n                    return -1;\n            }\n        }\n    }\n    return 0;\n}\n"),
     ("fp8 prefill append slot at the chunk index", "long sk = scale_index(&d, block_table, b, t, 0, h);",
      "long sk = scale_index(&d, block_table, b, t > 0 ? t - 1 : 0, 0, h);"),
+    ("qkv fp8 codes from the unrounded row", "(float)oracle_bf16_to_double(rows[r + i]) / kv_scale[si]);",
+     "(float)oracle_bf16_to_double(rows[r + i]) * 1.01f / kv_scale[si]);"),
+    ("qkv fp8 both planes with the K scale", "long si = scale_index(&d, block_table, b, L - 1, kv, g);",
+     "long si = scale_index(&d, block_table, b, L - 1, 0, g);"),
     ("prefill v row of the previous token", "pool[rv + i] = v[o + i];\n                }\n            }\n        }\n    }",
      "pool[rv + i] = v[o > D ? o - D : o + i];\n                }\n            }\n        }\n    }"),
 ]
