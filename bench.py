@@ -81,9 +81,9 @@ TRAFFIC = {
     "prefill-b1-prompt2048-36layer": {"kernel_sha": "485da7eb1438d8dd", "bytes_per_launch": 41996779},
     "prefill-b1-prompt2048-36layer-fp8kv": {"kernel_sha": "485da7eb1438d8dd", "bytes_per_launch": 37814763},
     # --qkv: the projection kernel
-    "b8-ctx256to384-36layer-qkv2560": {"kernel_sha": "f601289afdbb7741", "bytes_per_launch": 31541255},
-    "b64-ragged128to16384-sharedpool-36layer-qkv2560": {"kernel_sha": "f601289afdbb7741",
-                                                        "bytes_per_launch": 31896932},
+    "b8-ctx256to384-36layer-qkv2560": {"kernel_sha": "6989601104e612d5", "bytes_per_launch": 31552802},
+    "b64-ragged128to16384-sharedpool-36layer-qkv2560": {"kernel_sha": "6989601104e612d5",
+                                                        "bytes_per_launch": 31908550},
 }
 
 # The CPU timings sample the first few layers of a workload (same shapes and

@@ -602,6 +602,42 @@ qdec_status prefill_attn_impl(const qdec_shape *shape, int32_t num_tokens, const
         qdec::launch_prefill_attention(p, map, pool.fp8, static_cast<cudaStream_t>(stream)));
 }
 
+qdec_status qkv_impl(const qdec_shape *shape, int32_t hidden, const qdec_bf16 *x,
+                     int64_t x_stride, const qdec_bf16 *w_packed, const qdec_bf16 *q_norm_w,
+                     const qdec_bf16 *k_norm_w, const int32_t *positions, const int32_t *seq_lens,
+                     const int32_t *block_table, const void *rope_table, const PoolArg &pool,
+                     float *q_rot, int32_t *err_flag, void *stream) {
+    qdec_status st = check_shape(shape);
+    if (st != QDEC_OK) return st;
+    if ((st = check_pool(shape, pool)) != QDEC_OK) return st;
+    if (hidden < 64 || hidden % 64 != 0) return QDEC_ERR_UNSUPPORTED;
+    if (!x || !w_packed || !q_norm_w || !k_norm_w || !positions || !seq_lens || !block_table ||
+        !rope_table || !q_rot)
+        return QDEC_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w_packed) || !aligned16(q_norm_w) || !aligned16(k_norm_w) ||
+        !aligned16(rope_table) || !aligned16(q_rot))
+        return QDEC_ERR_INVALID_ARG;
+    if (x_stride < hidden || x_stride % 8 != 0) return QDEC_ERR_INVALID_ARG;
+    Params p{};
+    fill_common(p, shape, false);
+    p.hidden = hidden;
+    qdec::qkv_geometry(shape->batch, hidden, p.qkv_rows, p.qkv_boxes, p.qkv_stages);
+    p.w_q = reinterpret_cast<const __nv_bfloat16 *>(q_norm_w);
+    p.w_k = reinterpret_cast<const __nv_bfloat16 *>(k_norm_w);
+    p.positions = positions;
+    p.seq_lens = seq_lens;
+    p.block_table = block_table;
+    p.rope = static_cast<const qdec::RopeEntry *>(rope_table);
+    bind_pool(p, pool);
+    p.q_rot_out = q_rot;
+    p.err = err_flag;
+    p.w_packed = reinterpret_cast<const __nv_bfloat16 *>(w_packed);
+    CUtensorMap x_map;
+    if ((st = encode_rows_map(&x_map, x, shape->batch, hidden, x_stride, p.qkv_rows)) != QDEC_OK)
+        return st;
+    return cuda_status(qdec::launch_qkv_append(p, x_map, static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -801,34 +837,21 @@ qdec_status qdec_qkv_append_rope(const qdec_shape *shape, int32_t hidden, const 
                                  const int32_t *block_table, const void *rope_table,
                                  qdec_bf16 *kv_pool, float *q_rot, int32_t *err_flag,
                                  void *stream) {
-    qdec_status st = check_shape(shape);
-    if (st != QDEC_OK) return st;
-    if (hidden < 64 || hidden % 64 != 0) return QDEC_ERR_UNSUPPORTED;
-    if (!x || !w_packed || !q_norm_w || !k_norm_w || !positions || !seq_lens || !block_table ||
-        !rope_table || !kv_pool || !q_rot)
-        return QDEC_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(w_packed) || !aligned16(q_norm_w) || !aligned16(k_norm_w) ||
-        !aligned16(rope_table) || !aligned16(kv_pool) || !aligned16(q_rot))
-        return QDEC_ERR_INVALID_ARG;
-    if (x_stride < hidden || x_stride % 8 != 0) return QDEC_ERR_INVALID_ARG;
-    Params p{};
-    fill_common(p, shape, false);
-    p.hidden = hidden;
-    qdec::qkv_geometry(shape->batch, hidden, p.qkv_rows, p.qkv_boxes, p.qkv_stages);
-    p.w_q = reinterpret_cast<const __nv_bfloat16 *>(q_norm_w);
-    p.w_k = reinterpret_cast<const __nv_bfloat16 *>(k_norm_w);
-    p.positions = positions;
-    p.seq_lens = seq_lens;
-    p.block_table = block_table;
-    p.rope = static_cast<const qdec::RopeEntry *>(rope_table);
-    p.pool = reinterpret_cast<__nv_bfloat16 *>(kv_pool);
-    p.q_rot_out = q_rot;
-    p.err = err_flag;
-    p.w_packed = reinterpret_cast<const __nv_bfloat16 *>(w_packed);
-    CUtensorMap x_map;
-    if ((st = encode_rows_map(&x_map, x, shape->batch, hidden, x_stride, p.qkv_rows)) != QDEC_OK)
-        return st;
-    return cuda_status(qdec::launch_qkv_append(p, x_map, static_cast<cudaStream_t>(stream)));
+    return qkv_impl(shape, hidden, x, x_stride, w_packed, q_norm_w, k_norm_w, positions, seq_lens,
+                    block_table, rope_table, PoolArg{kv_pool, nullptr, false}, q_rot, err_flag,
+                    stream);
+}
+
+qdec_status qdec_qkv_append_rope_fp8(const qdec_shape *shape, int32_t hidden, const qdec_bf16 *x,
+                                     int64_t x_stride, const qdec_bf16 *w_packed,
+                                     const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                                     const int32_t *positions, const int32_t *seq_lens,
+                                     const int32_t *block_table, const void *rope_table,
+                                     uint8_t *kv_pool_fp8, const float *kv_scale, float *q_rot,
+                                     int32_t *err_flag, void *stream) {
+    return qkv_impl(shape, hidden, x, x_stride, w_packed, q_norm_w, k_norm_w, positions, seq_lens,
+                    block_table, rope_table, PoolArg{kv_pool_fp8, kv_scale, true}, q_rot,
+                    err_flag, stream);
 }
 
 qdec_status qdec_check_error(int32_t *err_flag, void *stream, int32_t *flags_out) {

@@ -9,7 +9,8 @@
 // the rotation and the append: query heads go to q_rot (fp32, unscaled, the
 // input of qdec_attn_decode / qdec_attn_split), key heads are rounded once to
 // bf16 after the rotation and value heads once as they are, into slot
-// seq_lens[b] - 1.
+// seq_lens[b] - 1 (into an FP8 pool: those bf16 rows divided by the slot's
+// scales and rounded to E4M3).
 //
 // Layout: a cluster of 4 CTAs per output head splits the hidden dimension:
 // CTA r computes all 128 dims of the head for up to 64 batch rows over its
@@ -39,6 +40,7 @@
 #include "qdec_ptx.cuh"
 #include "qdec.h"
 
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include <algorithm>
@@ -180,6 +182,35 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
     return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
            (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
 }
+
+// Four dims d0 .. d0+3 (a) and d0+64 .. d0+67 (c) of a key or value row into
+// its slot at element offset `slot`: bf16 (nearest-even) into the bf16 pool,
+// or, with an FP8 pool, the E4M3 codes of those bf16 values divided by the
+// slot's scale kv_scale[si] (fp32 division, nearest-even, saturating) --
+// slot / (16 * 128) is page * 2 Hkv + head, the K scale's index.
+__device__ __forceinline__ void store_row4(const Params &p, int64_t slot, int d0,
+                                           const float *a, const float *c, int64_t si) {
+    const uint2 lo = make_uint2(pack2_bf16(a[0], a[1]), pack2_bf16(a[2], a[3]));
+    const uint2 hi = make_uint2(pack2_bf16(c[0], c[1]), pack2_bf16(c[2], c[3]));
+    if (p.pool8 == nullptr) {
+        *reinterpret_cast<uint2 *>(p.pool + slot + d0) = lo;
+        *reinterpret_cast<uint2 *>(p.pool + slot + d0 + 64) = hi;
+        return;
+    }
+    const float s = p.kv_scale[si];
+    auto codes = [s](uint2 v) {  // four bf16 -> four E4M3 codes, low dim first
+        const float2 f0 = make_float2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
+        const float2 f1 = make_float2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+        const uint32_t c0 = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f0.x, s), __fdiv_rn(f0.y, s)),
+                                                     __NV_SATFINITE, __NV_E4M3);
+        const uint32_t c1 = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f1.x, s), __fdiv_rn(f1.y, s)),
+                                                     __NV_SATFINITE, __NV_E4M3);
+        return (c0 & 0xffffu) | (c1 << 16);
+    };
+    *reinterpret_cast<uint32_t *>(p.pool8 + slot + d0) = codes(lo);
+    *reinterpret_cast<uint32_t *>(p.pool8 + slot + d0 + 64) = codes(hi);
+}
+
 
 // kTc: the contraction on the 5th-generation tensor core (tcgen05, operands
 // read from shared memory, the accumulator in tensor memory); otherwise on
@@ -522,12 +553,8 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (aborted || *abort_flag || slot[h] < 0) continue;
             const int64_t kslot = slot[h];
             if (kind == 2) {
-                __nv_bfloat16 *vdst =
-                    p.pool + kslot + static_cast<int64_t>(Hkv) * kPageSize * kHeadDim;
-                *reinterpret_cast<uint2 *>(vdst + d0) =
-                    make_uint2(pack2_bf16(y[0], y[1]), pack2_bf16(y[2], y[3]));
-                *reinterpret_cast<uint2 *>(vdst + d0 + 64) =
-                    make_uint2(pack2_bf16(y[4], y[5]), pack2_bf16(y[6], y[7]));
+                const int64_t vslot = kslot + static_cast<int64_t>(Hkv) * kPageSize * kHeadDim;
+                store_row4(p, vslot, d0, y, y + 4, (kslot >> 11) + Hkv);
                 continue;
             }
             const float rn = rsqrtf(sq * (1.0f / kHeadDim) + p.eps);
@@ -545,11 +572,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 *reinterpret_cast<float4 *>(dst + d0) = make_float4(o1[0], o1[1], o1[2], o1[3]);
                 *reinterpret_cast<float4 *>(dst + d0 + 64) = make_float4(o2[0], o2[1], o2[2], o2[3]);
             } else {
-                __nv_bfloat16 *kdst = p.pool + kslot;
-                *reinterpret_cast<uint2 *>(kdst + d0) =
-                    make_uint2(pack2_bf16(o1[0], o1[1]), pack2_bf16(o1[2], o1[3]));
-                *reinterpret_cast<uint2 *>(kdst + d0 + 64) =
-                    make_uint2(pack2_bf16(o2[0], o2[1]), pack2_bf16(o2[2], o2[3]));
+                store_row4(p, kslot, d0, o1, o2, kslot >> 11);
             }
         }
         // the pushed slices must be read out before this CTA's memory is released

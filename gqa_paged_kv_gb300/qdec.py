@@ -38,7 +38,7 @@ EXPORTS = ("qdec_workspace_bytes", "qdec_workspace_init", "qdec_rope_table_bytes
            "qdec_attn_decode", "qdec_step", "qdec_qkv_append_rope", "qdec_qkv_pack_weights",
            "qdec_append_rope_fp8", "qdec_attn_split_fp8", "qdec_attn_decode_fp8",
            "qdec_prefill_append_rope", "qdec_prefill_attn", "qdec_prefill_append_rope_fp8",
-           "qdec_prefill_attn_fp8",
+           "qdec_prefill_attn_fp8", "qdec_qkv_append_rope_fp8",
            "qdec_step_fp8",
            "qdec_step_static_scratch", "qdec_check_error", "qdec_status_string", "qdec_version")
 
@@ -124,6 +124,9 @@ def _load():
     lib.qdec_qkv_append_rope.argtypes = [sp, ctypes.c_int32, vp, i64, vp, vp, vp, vp, vp, vp, vp,
                                          vp, vp, vp, vp]
     lib.qdec_qkv_append_rope.restype = st
+    lib.qdec_qkv_append_rope_fp8.argtypes = [sp, ctypes.c_int32, vp, i64, vp, vp, vp, vp, vp,
+                                             vp, vp, vp, vp, vp, vp, vp]
+    lib.qdec_qkv_append_rope_fp8.restype = st
     lib.qdec_qkv_pack_weights.argtypes = [sp, ctypes.c_int32, vp, vp, vp]
     lib.qdec_qkv_pack_weights.restype = st
     lib.qdec_append_rope_fp8.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp,
@@ -302,6 +305,21 @@ def qdec_qkv_append_rope(shape: Shape, x, w_packed, q_norm_w, k_norm_w, position
         _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions), _ptr(seq_lens), _ptr(block_table),
         _ptr(rope_table), _ptr(kv_pool), _ptr(q_rot), _ptr(err_flag), _stream(stream)),
         "qdec_qkv_append_rope")
+
+
+def qdec_qkv_append_rope_fp8(shape: Shape, x, w_packed, q_norm_w, k_norm_w, positions, seq_lens,
+                             block_table, kv_pool_fp8, kv_scale, q_rot, rope_table,
+                             err_flag=None, stream=None):
+    """qdec_qkv_append_rope into an FP8 pool (E4M3 codes, per-(page, plane,
+    head) scales)."""
+    if x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x: expected a bf16 [B][hidden] view with contiguous rows")
+    pool, scale = _fp8_pool(kv_pool_fp8, kv_scale)
+    _raise(_lib.qdec_qkv_append_rope_fp8(
+        ctypes.byref(shape.c()), int(x.shape[1]), _ptr(x), x.stride(0), _ptr(w_packed),
+        _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions), _ptr(seq_lens), _ptr(block_table),
+        _ptr(rope_table), pool, scale, _ptr(q_rot), _ptr(err_flag), _stream(stream)),
+        "qdec_qkv_append_rope_fp8")
 
 
 def _fp8_pool(pool, scale):

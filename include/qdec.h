@@ -359,6 +359,18 @@ qdec_status qdec_prefill_attn_fp8(const qdec_shape *shape, int32_t num_tokens,
                                   const uint8_t *kv_pool_fp8, const float *kv_scale,
                                   qdec_bf16 *out, int32_t *err_flag, void *stream);
 
+/* qdec_qkv_append_rope with an FP8 pool: the projected key and value rows,
+ * rounded to bf16 as the bf16 pool would hold them, are divided by their
+ * slot's scales and rounded to E4M3 (the append rule above). */
+qdec_status qdec_qkv_append_rope_fp8(const qdec_shape *shape, int32_t hidden,
+                                     const qdec_bf16 *x, int64_t x_stride,
+                                     const qdec_bf16 *w_packed,
+                                     const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
+                                     const int32_t *positions, const int32_t *seq_lens,
+                                     const int32_t *block_table, const void *rope_table,
+                                     uint8_t *kv_pool_fp8, const float *kv_scale, float *q_rot,
+                                     int32_t *err_flag, void *stream);
+
 /* qdec_step over an FP8 pool: one launch for steps 1-4, the new key and
  * value quantized into their slot as above.  Same launch flags, workspace
  * and error reporting as qdec_step. */
