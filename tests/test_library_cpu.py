@@ -144,6 +144,18 @@ def test_fp8_entry_points_reject_bad_arguments(q):
                                     z) == q.QDEC_ERR_UNSUPPORTED
     assert lib.qdec_attn_decode_fp8(sh, ok, ok, z, ok, ok, ok, 1 << 30, ok, z,
                                     z) == q.QDEC_ERR_INVALID_ARG
+    # prefill and the fused projection over an FP8 pool: scales required,
+    # an odd number of KV heads unsupported
+    assert lib.qdec_prefill_append_rope_fp8(sh, 4, ok, S, ok, S, ok, S, ok, ok, ok, ok, ok, ok,
+                                            ok, z, ok, z, z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_prefill_attn_fp8(odd, 4, ok, ok, ok, ok, ok, ok, ok, z,
+                                     z) == q.QDEC_ERR_UNSUPPORTED
+    assert lib.qdec_prefill_attn_fp8(sh, 4, ok, ok, ok, ok, ok, bad, ok, z,
+                                     z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_qkv_append_rope_fp8(sh, 256, ok, 256, ok, ok, ok, ok, ok, ok, ok, ok, z, ok,
+                                        z, z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_qkv_append_rope_fp8(odd, 256, ok, 256, ok, ok, ok, ok, ok, ok, ok, ok, ok, ok,
+                                        z, z) == q.QDEC_ERR_UNSUPPORTED
     # one workspace size serves both pool types
     assert q.qdec_workspace_bytes(_shape(q, num_q_heads=12, num_kv_heads=3)) > 0
 
