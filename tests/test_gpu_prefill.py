@@ -250,3 +250,46 @@ def test_prefill_fp8_chunk_of_one_equals_fp8_decode():
     st, flags = q.qdec_check_error(err)
     assert st == 0 and flags == 0
     assert torch.allclose(out.float(), out_d.float(), rtol=2 ** -7, atol=8e-3)
+
+
+# ------------------------------------------------------------ full size --
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_prefill_full_prompt_sampled(kv):
+    """The benchmark's size: one fresh 2048-token prompt in one chunk, run as
+    the benchmark runs it.  The oracle appends on its own copy of the pool
+    (taken before the GPU runs) and gives q_rot for every row; the attention
+    is compared on sampled rows: row r's causal attention is the (pinned)
+    decode attention of the oracle's q_rot[r] over the first r + 1 tokens of
+    the oracle-appended pool."""
+    P = 2048
+    rows = np.array([0, 1, 15, 16, 17, 255, 1000, 1023, 1024, 2046, 2047])
+    if kv == "fp8":
+        c, codes, sc = wl.prefill_case_fp8([P], [P], seed=1000)
+        pool = codes.cpu().numpy().copy()
+        sc_h = sc.cpu().numpy()
+    else:
+        c = wl.prefill_case([P], [P], seed=1000, poison=True)
+        pool = wl.bf16_bits(c.pool).copy()
+    bt = c.block_table.cpu().numpy()
+    qo, L = c.qo_indptr.cpu().numpy(), c.seq_lens.cpu().numpy()
+    ins = (wl.bf16_bits(c.q), wl.bf16_bits(c.k), wl.bf16_bits(c.v), wl.bf16_bits(c.w_q),
+           wl.bf16_bits(c.w_k), c.positions.cpu().numpy(), qo, L, bt)
+    if kv == "fp8":
+        ref = oracle.prefill_append_fp8(*ins, pool, sc_h, 1e6, float(np.float32(1e-6)))
+        q_rot, out, err = _run_fp8(c, codes, sc, 1)
+    else:
+        ref = oracle.prefill_append(*ins, pool, 1e6, float(np.float32(1e-6)))
+        q_rot, out, err = _run(c, 1)
+    st, flags = parity.qdec().qdec_check_error(err)
+    assert st == 0 and flags == 0, (st, flags)
+    g = q_rot.double().cpu().numpy()
+    assert np.all(np.abs(g - ref["q_rot"]) <= parity.QROT_TOL * (1 + np.abs(ref["q_rot"])))
+    bt_r = np.repeat(bt, len(rows), axis=0)
+    lens = (rows + 1).astype(np.int32)
+    qr = np.ascontiguousarray(ref["q_rot"][rows])
+    if kv == "fp8":
+        ref_out, _ = oracle.attention_fp8(pool, sc_h, bt_r, lens, qr, 1 / math.sqrt(128))
+    else:
+        ref_out, _ = oracle.attention(pool, bt_r, lens, qr, 1 / math.sqrt(128))
+    parity.assert_out_close(out[torch.as_tensor(rows, device="cuda")], ref_out)
