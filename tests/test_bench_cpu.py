@@ -1,0 +1,39 @@
+"""Host-side arithmetic of bench.py (no GPU): the algorithmic FLOP count of
+the causal prefill attention against a brute-force count of (query, key)
+pairs, and the per-kernel source hashes the traffic table is keyed by."""
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_prefill_flops_counts_causal_pairs():
+    rng = np.random.default_rng(3)
+    for _ in range(20):
+        B = int(rng.integers(1, 5))
+        L = [int(x) for x in rng.integers(1, 300, size=B)]
+        n = [int(rng.integers(0, l + 1)) for l in L]
+        pairs = 0
+        for Lb, nb in zip(L, n):
+            for j in range(nb):             # chunk row j is token Lb - nb + j
+                t = Lb - nb + j
+                pairs += sum(1 for key in range(Lb) if key <= t)
+        # q.k and p.v: 2 D FLOP each per pair and head
+        assert bench.prefill_flops(L, n, Hq=32, D=128) == pairs * 32 * 128 * 4
+
+
+def test_prefill_flops_fresh_prompt_closed_form():
+    P = 2048
+    assert bench.prefill_flops([P], [P]) == 4 * 128 * 32 * P * (P + 1) // 2
+
+
+def test_traffic_entries_name_a_kernel_with_sources():
+    for name, tr in bench.TRAFFIC.items():
+        assert len(tr["kernel_sha"]) == 16 and tr["bytes_per_launch"] > 0, name
+    for k, files in bench.KERNEL_SOURCES.items():
+        for f in files:
+            assert os.path.exists(os.path.join(ROOT, f)), (k, f)
