@@ -264,7 +264,9 @@ qdec_status qdec_qkv_pack_weights(const qdec_shape *shape, int32_t hidden,
  * + j of it (seq_lens counted after the chunk, n_b <= seq_lens[b]).  The
  * block table must map every page up to token seq_lens[b] - 1.  Sequences
  * whose chunk is malformed are skipped and flagged QDEC_FLAG_BAD_SEQLEN.
- * shape->batch = B sequences.  FP8-pool forms follow the FP8 section below. */
+ * shape->batch = B sequences; shape->num_ctas and QDEC_LAUNCH_OVERLAP_PREVIOUS
+ * are ignored (each call starts after the previous kernel on the stream).
+ * FP8-pool forms follow the FP8 section below. */
 
 /* Steps 1-3 for every chunk row r: RMSNorm + NeoX RoPE at positions[r] of
  * its query rows (q [num_tokens][Hq][D], row stride q_stride) into q_rot
