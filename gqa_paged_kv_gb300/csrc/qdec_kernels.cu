@@ -33,17 +33,29 @@
 // enter exactly; the softmax statistics stay in fp32.
 //
 // With an FP8 (E4M3) pool the tiles are 4 KiB; each also brings its two
-// scales (16-byte windows of kv_scale) on the same barrier.  The warp turns
-// codes into f16 pairs (exact) and runs the same two products with f16
-// mma.sync; the K scale multiplies the scores, the V scale each tile's
-// contribution to O^T.  The new token's k and v are quantized with the
-// scales of their page: fp32 division, then E4M3 nearest-even, saturating.
+// scales (16-byte windows of kv_scale) on the same barrier.  The scores come
+// from E4M3 mma.sync (m16n8k32) on the K codes as they are, the query rows
+// entering as four E4M3 terms (q 2^e = T0 + T1/16 + T2/256 + T3/4096); the V
+// codes are turned into f16 pairs (exact) for an f16 mma.sync with P as f16
+// hi + lo.  The K scale and 2^-e multiply the scores, the V scale each
+// tile's contribution to O^T.  The new token's k and v are quantized with
+// the scales of their page: fp32 division, then E4M3 nearest-even,
+// saturating.
+//
+// The kernel's mode (template argument): split -- q_rot read from memory,
+// the pieces of split segments left in the workspace for merge_kernel (flat
+// layout only); fused -- steps 1-4, the new-token rows normed, rotated and
+// appended in the kernel, the last piece of a split segment merging it;
+// decode -- q_rot read from memory (the slot already appended) with the
+// fused mode's layouts and in-kernel merge.
 //
 // The producer reads only data that no kernel of the step writes (seq_lens,
 // the block table, cached pool pages), so when the launch is a programmatic
 // dependent of the previous layer it streams pages while that layer is still
 // finishing; the consumers wait for the previous kernel before they touch q,
-// k, v, the pool slot they append to, the workspace or `out`.
+// k, v, the pool slot they append to, the workspace or `out`.  In decode
+// mode the previous kernel wrote the appended slots, so there the producer
+// waits too before its first copy.
 #include "qdec_internal.h"
 #include "qdec_ptx.cuh"
 #include "qdec.h"
