@@ -78,12 +78,12 @@ TRAFFIC = {
     "b64-ragged128to16384-sharedpool-36layer-fp8kv": {"kernel_sha": "db22c2a1a1b797eb",
                                                       "bytes_per_launch": 524764583},
     # --prefill 2048: the causal prefill attention kernel
-    "prefill-b1-prompt2048-36layer": {"kernel_sha": "485da7eb1438d8dd", "bytes_per_launch": 41996779},
-    "prefill-b1-prompt2048-36layer-fp8kv": {"kernel_sha": "485da7eb1438d8dd", "bytes_per_launch": 37814763},
+    "prefill-b1-prompt2048-36layer": {"kernel_sha": "fb9a77aa27ecf581", "bytes_per_launch": 41995115},
+    "prefill-b1-prompt2048-36layer-fp8kv": {"kernel_sha": "fb9a77aa27ecf581", "bytes_per_launch": 37815019},
     # --qkv: the projection kernel
-    "b8-ctx256to384-36layer-qkv2560": {"kernel_sha": "6989601104e612d5", "bytes_per_launch": 31552802},
-    "b64-ragged128to16384-sharedpool-36layer-qkv2560": {"kernel_sha": "6989601104e612d5",
-                                                        "bytes_per_launch": 31908550},
+    "b8-ctx256to384-36layer-qkv2560": {"kernel_sha": "ba9a59823eb8e517", "bytes_per_launch": 31553185},
+    "b64-ragged128to16384-sharedpool-36layer-qkv2560": {"kernel_sha": "ba9a59823eb8e517",
+                                                        "bytes_per_launch": 31908342},
 }
 
 # The CPU timings sample the first few layers of a workload (same shapes and

@@ -361,6 +361,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                         misc[0] = 1;
                         flag_error(p.err, QDEC_FLAG_TIMEOUT);
                         stop = true;
+                    } else if (p.withhold_first && i == 0) {
+                        // test hook: this tile's barrier phase never completes
                     } else if (pj >= 0 && pj < p.num_pages) {
                         slot_ok[slot] = 1;
                         if constexpr (kFp8) {

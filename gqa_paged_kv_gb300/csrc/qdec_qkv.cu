@@ -268,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         *abort_flag = 0;
         fence_mbar_init();
         for (int c = 0; c < pre; ++c) {
+            if (p.withhold_first && c == 0) continue;  // test hook: stage 0 never lands
             const uint32_t full = full0 + 8 * c;
             mbar_arrive_expect_tx(full, stage_bytes);
             bulk_load(smem_u32(sm + c * stage_bytes),
@@ -312,7 +313,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     bulk_load(dst, wsrc + static_cast<int64_t>(c) * NB * (kQkvBlock / 2),
                               NB * kQkvBlock, full);
                 }
-                for (int j = 0; j < NB && (c >= pre || p.pdl); ++j)
+                const bool send_x = (c >= pre || p.pdl) && !(p.withhold_first && c == 0);
+                for (int j = 0; j < NB && send_x; ++j)
                     tma_load_2d(dst + NB * kQkvBlock + j * R * kQkvChunk * 2, &x_map,
                                 (kb0 + c * NB + j) * kQkvChunk, row0, full);
             }

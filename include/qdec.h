@@ -80,11 +80,15 @@ typedef enum {
 /* qdec_shape.launch_flags */
 #define QDEC_LAUNCH_OVERLAP_PREVIOUS 1
 /* Test hook for the failure path, not for production use: in every CTA of
- * the attention kernel the first page tile is never copied, so the wait for
- * it runs out (after ~10 ms instead of ~2 s), the kernel stops its copies,
- * lets those in flight land and returns; qdec_check_error then reports
- * QDEC_ERR_TIMEOUT.  Outputs of such a call are undefined; the device stays
- * usable.  No counterpart in the pages. */
+ * the paged attention kernels (qdec_step, qdec_attn_split, qdec_attn_decode,
+ * qdec_prefill_attn and their FP8 forms) the first page tile is never
+ * copied, and in every CTA of the QKV projection the first stage of weight
+ * and hidden states, so the wait for it runs out (after ~10 ms instead of
+ * ~2 s), the kernel stops its copies, lets those in flight land and returns;
+ * qdec_check_error then reports QDEC_ERR_TIMEOUT.  Outputs of such a call
+ * are undefined; the device stays usable.  The calls whose kernels wait on
+ * nothing (rope table, append, merge, weight packing) ignore it.  No
+ * counterpart in the pages. */
 #define QDEC_LAUNCH_TEST_WITHHOLD_TILE (1 << 30)
 /* qdec_step may be launched as a programmatic dependent of the kernel before
  * it on the stream: it starts streaming cached KV pages (reading seq_lens,

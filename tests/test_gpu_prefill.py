@@ -25,10 +25,10 @@ import parity
 pytestmark = pytest.mark.gpu
 
 
-def _shape(c, B):
+def _shape(c, B, launch_flags=0):
     q = parity.qdec()
     return q.Shape(batch=B, num_pages=c.num_pages, max_blocks_per_seq=c.max_blocks,
-                   max_seq_len=c.max_blocks * 16)
+                   max_seq_len=c.max_blocks * 16, launch_flags=launch_flags)
 
 
 def _run(c, B):
@@ -172,6 +172,30 @@ def test_prefill_bad_page_is_flagged(bad_entry):
     parity.assert_out_close(out[rows], res["out"][rows])
 
 
+def test_prefill_wait_that_runs_out_returns_timeout_and_device_stays_usable():
+    """The test hook withholds every CTA's first page tile: the wait for it
+    gives up, the call reports a timeout, and the next normal call on the
+    same device and pool gives the verified result bit for bit."""
+    q = parity.qdec()
+    c = wl.prefill_case([300, 17, 1000], [20, 17, 200], seed=16)
+    res = _oracle(c)
+    q_rot, out, err = _run(c, 3)
+    parity.assert_out_close(out, res["out"])
+    st, flags = q.qdec_check_error(err)
+    assert st == 0 and flags == 0, (st, flags)
+    withheld = torch.empty_like(out)
+    q.qdec_prefill_attn(_shape(c, 3, q.QDEC_LAUNCH_TEST_WITHHOLD_TILE), q_rot, c.qo_indptr,
+                        c.seq_lens, c.block_table, c.pool, withheld, err)
+    st, flags = q.qdec_check_error(err)
+    assert st == q.QDEC_ERR_TIMEOUT and flags & q.QDEC_FLAG_TIMEOUT, (st, flags)
+    again = torch.empty_like(out)
+    q.qdec_prefill_attn(_shape(c, 3), q_rot, c.qo_indptr, c.seq_lens, c.block_table, c.pool,
+                        again, err)
+    st, flags = q.qdec_check_error(err)
+    assert st == 0 and flags == 0, (st, flags)
+    assert torch.equal(again, out)
+
+
 # ------------------------------------------------------------------- FP8 pool --
 
 def _run_fp8(c, codes, sc, B):
@@ -235,6 +259,28 @@ def test_prefill_fp8_matches_oracle(seq_lens, chunks):
             changed[page, :, :, off] = True
     assert k_off <= max(2, got.size // 100000), f"{k_off} K codes one step off"
     assert np.array_equal(got[~changed], before[~changed]), "append touched another slot"
+
+
+def test_prefill_fp8_wait_that_runs_out_returns_timeout_and_device_stays_usable():
+    """FP8 pool: as for bf16, the withheld tile's wait gives up with a timeout
+    (the conversion barriers are never reached) and the next normal call
+    gives the verified result bit for bit."""
+    q = parity.qdec()
+    c, codes, sc = wl.prefill_case_fp8([300, 17, 1000], [20, 17, 200], seed=17)
+    q_rot, out, err = _run_fp8(c, codes, sc, 3)
+    st, flags = q.qdec_check_error(err)
+    assert st == 0 and flags == 0, (st, flags)
+    withheld = torch.empty_like(out)
+    q.qdec_prefill_attn_fp8(_shape(c, 3, q.QDEC_LAUNCH_TEST_WITHHOLD_TILE), q_rot, c.qo_indptr,
+                            c.seq_lens, c.block_table, codes, sc, withheld, err)
+    st, flags = q.qdec_check_error(err)
+    assert st == q.QDEC_ERR_TIMEOUT and flags & q.QDEC_FLAG_TIMEOUT, (st, flags)
+    again = torch.empty_like(out)
+    q.qdec_prefill_attn_fp8(_shape(c, 3), q_rot, c.qo_indptr, c.seq_lens, c.block_table, codes,
+                            sc, again, err)
+    st, flags = q.qdec_check_error(err)
+    assert st == 0 and flags == 0, (st, flags)
+    assert torch.equal(again, out)
 
 
 def test_prefill_fp8_chunk_of_one_equals_fp8_decode():

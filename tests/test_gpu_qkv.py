@@ -281,3 +281,32 @@ def test_qkv_fp8_pool_matches_oracle(lens, hidden):
         assert np.all(np.abs((gc & 0x7F) - (oc & 0x7F)) <= 1), f"codes seq {b}"
         off_step += int(diff.sum())
     assert off_step <= max(2, s.batch * 2 * s.num_kv_heads * s.head_dim // 100), off_step
+
+
+@pytest.mark.parametrize("batch", [4, 20], ids=["mma_sync_rows16", "tcgen05_rows32"])
+def test_qkv_wait_that_runs_out_returns_timeout_and_device_stays_usable(batch):
+    """The test hook withholds every CTA's first stage of weight and hidden
+    states: the wait for it gives up (the tensor-core variant still frees its
+    tensor memory and every cluster still exchanges its partial sums), the
+    call reports a timeout, and the next normal block on the same device
+    gives the earlier result bit for bit."""
+    q = parity.qdec()
+    lens = [200 + 37 * i for i in range(batch)]
+    w, x, wqkv = _problem(lens, 2560, seed=90 + batch)
+    q_rot, out, err = _run(w, x, wqkv)
+    st, flags = q.qdec_check_error(err)
+    assert st == 0 and flags == 0, (st, flags)
+    shape = q.shape_for(w, launch_flags=q.QDEC_LAUNCH_TEST_WITHHOLD_TILE)
+    rope = q.alloc_rope_table(shape)
+    q.qdec_rope_table(shape, w.positions, rope)
+    packed = torch.empty_like(wqkv)
+    q.qdec_qkv_pack_weights(shape, wqkv, packed)
+    withheld = torch.empty_like(q_rot)
+    q.qdec_qkv_append_rope(shape, x, packed, w.w_q[0], w.w_k[0], w.positions, w.seq_lens,
+                           w.block_table, w.pool(0), withheld, rope, err)
+    st, flags = q.qdec_check_error(err)
+    assert st == q.QDEC_ERR_TIMEOUT and flags & q.QDEC_FLAG_TIMEOUT, (st, flags)
+    q_rot2, out2, err = _run(w, x, wqkv)
+    st, flags = q.qdec_check_error(err)
+    assert st == 0 and flags == 0, (st, flags)
+    assert torch.equal(q_rot2, q_rot) and torch.equal(out2, out)
