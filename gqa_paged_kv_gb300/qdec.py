@@ -167,7 +167,19 @@ def qdec_version() -> int:
 
 
 def _ptr(t) -> int:
-    return None if t is None else t.data_ptr()
+    """Device address of a tensor argument (None passes NULL where the C ABI
+    allows it).  Every pointer the library takes is a device pointer on the
+    current device, so a host tensor, or one on another GPU, is refused here
+    rather than handed to a kernel as an address it cannot use."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got {type(t).__name__}"
+                         + (f" on {t.device}" if isinstance(t, torch.Tensor) else ""))
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"tensor on {t.device}, but the current device is "
+                         f"cuda:{torch.cuda.current_device()}")
+    return t.data_ptr()
 
 
 def _stream(stream):

@@ -163,3 +163,21 @@ def test_fp8_entry_points_reject_bad_arguments(q):
 def test_rope_table_bytes(q):
     assert q.qdec_rope_table_bytes(_shape(q, batch=3)) == 3 * 64 * 16
     assert q.qdec_rope_table_bytes(_shape(q, head_dim=64)) == 0
+
+
+def test_binding_refuses_host_tensors(q):
+    """Every pointer the library takes is a device pointer: the Python
+    binding refuses a host tensor (or anything that is not a tensor) before
+    the library is entered."""
+    import torch
+    sh = _shape(q, batch=2)
+    host = torch.zeros(64, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        q.qdec_rope_table(sh, host, host)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        q.qdec_check_error(host)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        q.qdec_attn_merge(sh, [1, 2], host, host)
+    x = torch.zeros((2, 256), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        q.qdec_qkv_append_rope(sh, x, x, x, x, host, host, host, host, host, host)
