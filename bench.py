@@ -273,10 +273,13 @@ def block_bytes_per_layer(w: wl.Workload, hidden: int) -> int:
             + s.batch * s.num_q_heads * s.head_dim * 2)
 
 
-def workload_config(w: wl.Workload, args, world: int, l2: int = L2_BYTES_NOMINAL) -> dict:
-    """The `config` object of the JSON line (the same for both arms)."""
+def workload_config(w: wl.Workload, args, world: int, l2: int = L2_BYTES_NOMINAL,
+                    layers: int = 0) -> dict:
+    """The `config` object of the JSON line (the same for both arms; the
+    reference arm times a few layers of the workload and passes the full
+    layer count as `layers`)."""
     spec, seq_lens_host = w.spec, w.seq_lens_host
-    L = spec.layers
+    L = layers or spec.layers
     qkv_hidden = args.hidden if getattr(args, "qkv", False) else 0
     bytes_layer = (block_bytes_per_layer(w, qkv_hidden) if qkv_hidden
                    else w.algorithmic_bytes_per_layer())
@@ -374,9 +377,10 @@ def run_reference(args, dist: Dist):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-        "config": workload_config(w, args, 1),
+        "config": workload_config(w, args, 1, layers=spec.layers),
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{args.steps} steps of one sequence x one layer, "
+                         "sample": f"{args.steps} steps of one sequence x one layer "
+                                   f"(layers 0-{w.spec.layers - 1} of the workload), "
                                    f"{dt:.1f} s"},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

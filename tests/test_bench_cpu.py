@@ -1,6 +1,7 @@
 """Host-side arithmetic of bench.py (no GPU): the algorithmic FLOP count of
 the causal prefill attention against a brute-force count of (query, key)
-pairs, and the per-kernel source hashes the traffic table is keyed by."""
+pairs, the per-kernel source hashes the traffic table is keyed by, and the
+reference arm's config."""
 import os
 import sys
 
@@ -37,3 +38,20 @@ def test_traffic_entries_name_a_kernel_with_sources():
     for k, files in bench.KERNEL_SOURCES.items():
         for f in files:
             assert os.path.exists(os.path.join(ROOT, f)), (k, f)
+
+
+def test_reference_arm_reports_the_full_workload_config():
+    """The reference arm times a few layers of a workload on the host but its
+    line carries the workload's own config (the full layer count and the
+    bytes of a whole step), the same object the GPU arm prints."""
+    import argparse
+    from gqa_paged_kv_gb300 import workloads as wl
+    spec = wl.custom(3, [40, 17, 300], pool_pages=64, layers=2, shared_pool=False)
+    w = wl.build(spec, "cpu")
+    args = argparse.Namespace(no_graph=False, no_overlap=False, qkv=False, hidden=0)
+    few = bench.workload_config(w, args, 1)
+    full = bench.workload_config(w, args, 1, layers=36)
+    assert few["layers"] == 2 and full["layers"] == 36
+    assert full["kv_bytes_per_step"] == 18 * few["kv_bytes_per_step"]
+    assert "36 qdec_step" in full["launch"]
+    assert {k for k in few} == {k for k in full}
