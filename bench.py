@@ -360,6 +360,57 @@ def sample_bytes(w: wl.Workload, seq_lens) -> int:
     return int(sl.sum()) * s.kv_bytes_per_token() + io
 
 
+def qkv_sample_bytes(w: wl.Workload, hidden: int, seq_lens) -> int:
+    """--qkv: algorithmic bytes of the given sequences of one layer's block
+    (the whole weight, their hidden states, KV and output)."""
+    s = w.spec
+    n = len(seq_lens)
+    kv = sample_bytes(w, seq_lens) - n * s.io_bytes_per_seq()
+    return qkv_weight_bytes(s, hidden) + n * hidden * 2 + kv + n * s.num_q_heads * s.head_dim * 2
+
+
+def oracle_qkv_operands(w: wl.Workload, hidden: int):
+    """Seeded hidden states [B][hidden] and one merged weight for the oracle
+    (bf16 bits; the GPU arm's distributions, drawn on the host)."""
+    s = w.spec
+    gen = torch.Generator().manual_seed(s.seed + 11)
+    x = torch.randn((s.batch, hidden), generator=gen).to(torch.bfloat16)
+    rows = (s.num_q_heads + 2 * s.num_kv_heads) * s.head_dim
+    wq = (torch.randn((rows, hidden), generator=gen) / hidden ** 0.5).to(torch.bfloat16)
+    return wl.bf16_bits(x), wl.bf16_bits(wq)
+
+
+def oracle_qkv_block(inp: dict, x, wqkv, seqs=None):
+    """One oracle step of the --qkv block on oracle_inputs (a copy of the
+    pool): projection fused with norm, rotation and append, then attention."""
+    import math
+
+    import oracle
+    s_x = x if seqs is None else np.ascontiguousarray(x[seqs])
+    pool = inp["pool"].copy()
+    Hq = inp["q"].shape[1]
+    res = oracle.qkv_append(s_x, wqkv, inp["w_q"], inp["w_k"], inp["positions"],
+                            inp["seq_lens"], inp["block_table"], pool, inp["rope_theta"],
+                            inp["eps"], Hq, pool.shape[2])
+    oracle.attention(pool, inp["block_table"], inp["seq_lens"], res["q_rot"],
+                     1 / math.sqrt(pool.shape[4]))
+
+
+def oracle_qkv_sample(w: wl.Workload, hidden: int, seconds: float):
+    """Time the oracle's --qkv block (one thread) on whole layers in order
+    until `seconds` have passed.  Returns (GB/s, layers done, elapsed)."""
+    x, wqkv = oracle_qkv_operands(w, hidden)
+    bytes_done, n, t_total = 0, 0, 0.0
+    while t_total < seconds or n == 0:
+        inp = wl.oracle_inputs(w, n % w.spec.layers)
+        t0 = time.perf_counter()
+        oracle_qkv_block(inp, x, wqkv)
+        t_total += time.perf_counter() - t0
+        bytes_done += qkv_sample_bytes(w, hidden, inp["seq_lens"])
+        n += 1
+    return bytes_done / t_total / 1e9, n, t_total
+
+
 def run_reference(args, dist: Dist):
     """The reference arm: the CPU oracle, timed as it stands on the host."""
     if dist.rank != 0:
@@ -367,9 +418,10 @@ def run_reference(args, dist: Dist):
     spec = wl.WORKLOADS[args.workload]
     w = wl.build(spec, "cpu", layers=min(spec.layers, CPU_SAMPLE_LAYERS), kv=args.kv)
     # warm-up steps, then exactly K timed steps; a step is one sequence of one layer
-    oracle_steps(w, args.warmup)
+    ops = oracle_qkv_operands(w, args.hidden) if args.qkv else None
+    oracle_steps(w, args.warmup, ops, args.hidden)
     t0 = time.perf_counter()
-    gbs_bytes = oracle_steps(w, args.steps)
+    gbs_bytes = oracle_steps(w, args.steps, ops, args.hidden)
     dt = time.perf_counter() - t0
     value = gbs_bytes / dt / 1e9
     line = {
@@ -379,7 +431,8 @@ def run_reference(args, dist: Dist):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
         "config": workload_config(w, args, 1, layers=spec.layers),
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{args.steps} steps of one sequence x one layer "
+                         "sample": f"{args.steps} steps of one sequence x one layer"
+                                   f"{' of the QKV block' if args.qkv else ''} "
                                    f"(layers 0-{w.spec.layers - 1} of the workload), "
                                    f"{dt:.1f} s"},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -389,14 +442,20 @@ def run_reference(args, dist: Dist):
     print(json.dumps(line), flush=True)
 
 
-def oracle_steps(w: wl.Workload, k: int) -> int:
+def oracle_steps(w: wl.Workload, k: int, qkv_ops=None, hidden: int = 0) -> int:
+    """k oracle steps of one sequence of one layer (of the --qkv block when
+    qkv_ops holds its hidden states and weight); returns their bytes."""
     B = w.spec.batch
     done = 0
     for i in range(k):
         layer, b = (i // B) % w.spec.layers, i % B
         inp = wl.oracle_inputs(w, layer, [b])
-        oracle_layer(inp)
-        done += sample_bytes(w, inp["seq_lens"])
+        if qkv_ops is not None:
+            oracle_qkv_block(inp, qkv_ops[0], qkv_ops[1], [b])
+            done += qkv_sample_bytes(w, hidden, inp["seq_lens"])
+        else:
+            oracle_layer(inp)
+            done += sample_bytes(w, inp["seq_lens"])
     return done
 
 
@@ -624,7 +683,14 @@ def run_ours(args, dist: Dist):
         traffic = tr["bytes_per_launch"]
 
     cpu = None
-    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and not args.qkv:
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline and args.qkv:
+        w_cpu = wl.build(spec, "cpu", layers=min(spec.layers, CPU_SAMPLE_LAYERS), kv=w.kv)
+        gbs, n, secs = oracle_qkv_sample(w_cpu, args.hidden, args.cpu_seconds)
+        cpu = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} x one layer (all sequences) of the QKV block of "
+                         f"{workload_name(spec, w.kv, args.hidden)} "
+                         f"(layers 0-{w_cpu.spec.layers - 1}), fp64, {secs:.1f} s"}
+    elif dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         w_cpu = wl.build(spec, "cpu", layers=min(spec.layers, CPU_SAMPLE_LAYERS), kv=w.kv)
         gbs, what, n, secs = oracle_sample(w_cpu, args.cpu_seconds, per_seq=False)
         cpu = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -674,6 +740,75 @@ def prefill_flops(seq_lens, chunks, Hq=32, D=128) -> int:
     return 4 * D * Hq * tot
 
 
+def prefill_config(P: int, L: int, fp8: bool) -> dict:
+    """The `config` object of a --prefill line (the same for both arms)."""
+    return {"workload": f"prefill-b1-prompt{P}-{L}layer" + ("-fp8kv" if fp8 else ""),
+            "batch": 1, "prompt": P, "layers": L, "heads": "32 q / 8 kv, head_dim 128, page 16",
+            "launch": f"CUDA graph: {L} x (qdec_prefill_append_rope, qdec_prefill_attn)",
+            "l2": "not flushed (compute-bound: each layer's K/V is re-read from L2 "
+                  "by its query blocks by design)"}
+
+
+def oracle_prefill_sample(P: int, fp8: bool):
+    """A bounded sample of a --prefill step for the fp64 oracle: one layer of
+    a fresh prompt of min(P, 256) tokens (append, then causal attention).
+    Returns (run, flops, tokens); run() executes it on a fresh copy of the
+    pool, the inputs being made once."""
+    import math
+
+    import oracle
+    Pc = min(P, 256)
+    if fp8:
+        c, codes_h, sc_h = wl.prefill_case_fp8([Pc], [Pc], seed=1000, device="cpu")
+        pool0, sc = codes_h.numpy().copy(), sc_h.numpy()
+    else:
+        c = wl.prefill_case([Pc], [Pc], seed=1000, device="cpu", poison=False)
+        pool0, sc = wl.bf16_bits(c.pool).copy(), None
+    bt, qo, sl = c.block_table.numpy(), c.qo_indptr.numpy(), c.seq_lens.numpy()
+    ins = (wl.bf16_bits(c.q), wl.bf16_bits(c.k), wl.bf16_bits(c.v), wl.bf16_bits(c.w_q),
+           wl.bf16_bits(c.w_k), c.positions.numpy(), qo, sl, bt)
+    eps, scale = float(np.float32(1e-6)), 1 / math.sqrt(128)
+
+    def run():
+        pool = pool0.copy()
+        if fp8:
+            res = oracle.prefill_append_fp8(*ins, pool, sc, 1e6, eps)
+            oracle.prefill_attention_fp8(pool, sc, bt, qo, sl, res["q_rot"], scale)
+        else:
+            res = oracle.prefill_append(*ins, pool, 1e6, eps)
+            oracle.prefill_attention(pool, bt, qo, sl, res["q_rot"], scale)
+    return run, prefill_flops([Pc], [Pc]), Pc
+
+
+def run_reference_prefill(args, dist: Dist):
+    """The reference arm of --prefill: the oracle on the host, each step one
+    bounded sample of the workload (see oracle_prefill_sample)."""
+    if dist.rank != 0:
+        return
+    P, L, fp8 = args.prefill, args.layers or 36, args.kv == "fp8"
+    run, flops, Pc = oracle_prefill_sample(P, fp8)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    value = args.steps * flops / dt / 1e12
+    print(json.dumps({
+        "impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 9),
+        "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": prefill_config(P, L, fp8),
+        "cpu_baseline": {"value": round(value, 9), "unit": "TFLOP/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"{args.steps} steps of one layer of a fresh {Pc}-token "
+                                   f"prompt (append + causal attention), {dt:.1f} s"},
+        "e2e": {"value": round(value, 9), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0}), flush=True)
+
+
 def run_prefill(args, dist: Dist):
     """Chunked prefill: per layer one fresh prompt of args.prefill tokens
     (qdec_prefill_append_rope, then qdec_prefill_attn) over that layer's pool;
@@ -687,7 +822,7 @@ def run_prefill(args, dist: Dist):
     P = args.prefill
     L = args.layers or 36
     fp8 = args.kv == "fp8"
-    name = f"prefill-b1-prompt{P}-{L}layer" + ("-fp8kv" if fp8 else "")
+    name = prefill_config(P, L, fp8)["workload"]
     if fp8:   # E4M3 codes and per-(page, plane, head) scales of the same draws
         made = [wl.prefill_case_fp8([P], [P], seed=1000 + l, device="cuda") for l in range(L)]
         cases = [m[0] for m in made]
@@ -824,35 +959,17 @@ def run_prefill(args, dist: Dist):
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        import math
-
-        import oracle
-        Pc = min(P, 256)   # bounded sample: one layer, a fresh prompt of Pc tokens
-        ins_h = None
-        if fp8:
-            c, codes_h, sc_h = wl.prefill_case_fp8([Pc], [Pc], seed=1000, device="cpu")
-            pool = codes_h.numpy().copy()
-            sc_h = sc_h.numpy()
-        else:
-            c = wl.prefill_case([Pc], [Pc], seed=1000, device="cpu", poison=False)
-            pool = wl.bf16_bits(c.pool).copy()
-        ins_h = (wl.bf16_bits(c.q), wl.bf16_bits(c.k), wl.bf16_bits(c.v), wl.bf16_bits(c.w_q),
-                 wl.bf16_bits(c.w_k), c.positions.numpy(), c.qo_indptr.numpy(),
-                 c.seq_lens.numpy(), c.block_table.numpy())
-        t0 = time.perf_counter()
-        if fp8:
-            res = oracle.prefill_append_fp8(*ins_h, pool, sc_h, 1e6, float(np.float32(1e-6)))
-            oracle.prefill_attention_fp8(pool, sc_h, c.block_table.numpy(), c.qo_indptr.numpy(),
-                                         c.seq_lens.numpy(), res["q_rot"], 1 / math.sqrt(128))
-        else:
-            res = oracle.prefill_append(*ins_h, pool, 1e6, float(np.float32(1e-6)))
-            oracle.prefill_attention(pool, c.block_table.numpy(), c.qo_indptr.numpy(),
-                                     c.seq_lens.numpy(), res["q_rot"], 1 / math.sqrt(128))
-        secs = time.perf_counter() - t0
-        cpu = {"value": round(prefill_flops([Pc], [Pc]) / secs / 1e12, 9), "unit": "TFLOP/s",
-               "cores": 1, "kind": "oracle",
-               "sample": f"one layer of a fresh {Pc}-token prompt (append + causal attention), "
-                         f"fp64, {secs:.1f} s"}
+        run, flops, Pc = oracle_prefill_sample(P, fp8)
+        n, secs = 0, 0.0
+        while secs < args.cpu_seconds or n == 0:
+            t0 = time.perf_counter()
+            run()
+            secs += time.perf_counter() - t0
+            n += 1
+        cpu = {"value": round(n * flops / secs / 1e12, 9), "unit": "TFLOP/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"{n} x one layer of a fresh {Pc}-token prompt (append + causal "
+                         f"attention), fp64, {secs:.1f} s"}
 
     if dist.rank == 0:
         line = {
@@ -864,11 +981,7 @@ def run_prefill(args, dist: Dist):
                      + " (mma.sync bf16, q as hi+lo, f32 accumulate)",
             "data": "synthetic (seeded N(0,1) bf16 q/k/v, U(0.5,1.5) norm weights)",
             "us_per_layer_step": round(ms_step * 1e3 / L, 3),
-            "config": {"workload": name, "batch": 1, "prompt": P, "layers": L,
-                       "heads": "32 q / 8 kv, head_dim 128, page 16",
-                       "launch": f"CUDA graph: {L} x (qdec_prefill_append_rope, qdec_prefill_attn)",
-                       "l2": "not flushed (compute-bound: each layer's K/V is re-read from L2 "
-                             "by its query blocks by design)"},
+            "config": prefill_config(P, L, fp8),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, cuBLAS "
@@ -891,7 +1004,10 @@ def main():
     dist = Dist()
     try:
         if args.impl == "reference":
-            run_reference(args, dist)
+            if args.prefill:
+                run_reference_prefill(args, dist)
+            else:
+                run_reference(args, dist)
         elif args.prefill:
             run_prefill(args, dist)
         else:

@@ -55,3 +55,28 @@ def test_reference_arm_reports_the_full_workload_config():
     assert full["kv_bytes_per_step"] == 18 * few["kv_bytes_per_step"]
     assert "36 qdec_step" in full["launch"]
     assert {k for k in few} == {k for k in full}
+
+
+def test_qkv_sample_bytes_of_every_sequence_is_the_block_bytes():
+    from gqa_paged_kv_gb300 import workloads as wl
+    spec = wl.custom(3, [40, 17, 300], pool_pages=64, layers=1)
+    w = wl.build(spec, "cpu")
+    assert (bench.qkv_sample_bytes(w, 256, w.seq_lens_host)
+            == bench.block_bytes_per_layer(w, 256))
+
+
+def test_oracle_samples_of_the_qkv_block_and_prefill_run():
+    """The host oracle samples behind cpu_baseline and the reference arm of
+    --qkv and --prefill run on small inputs and report positive rates."""
+    from gqa_paged_kv_gb300 import workloads as wl
+    spec = wl.custom(2, [40, 17], pool_pages=16, layers=2)
+    w = wl.build(spec, "cpu")
+    gbs, n, secs = bench.oracle_qkv_sample(w, 128, 0.0)
+    assert gbs > 0 and n == 1 and secs > 0
+    ops = bench.oracle_qkv_operands(w, 128)
+    assert bench.oracle_steps(w, 3, ops, 128) == sum(
+        bench.qkv_sample_bytes(w, 128, [L]) for L in (40, 17, 40))
+    for fp8 in (False, True):
+        run, flops, Pc = bench.oracle_prefill_sample(48, fp8)
+        run()
+        assert Pc == 48 and flops == bench.prefill_flops([48], [48])

@@ -39,7 +39,7 @@ def _rank_main(rank, world, port, out):
 
 def test_dist_max_and_barrier_gloo_two_ranks():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:   # no fork of a threaded process
         out = m.dict()
         mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
         assert dict(out) == {0: 20.0, 1: 20.0}
