@@ -9,6 +9,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 namespace {
@@ -18,17 +19,22 @@ using qdec::Params;
 constexpr int kVersion = 10000;  // 1.0.0
 
 // ----------------------------------------------------------- device info --
-int sm_count_of_current_device() {
-    static int cache[64] = {0};
+// Per-device attribute caches: calls may come from several host threads, so
+// the entries are atomics (every writer stores the same value).
+int cached_attribute(std::atomic<int> (&cache)[64], cudaDeviceAttr attr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cache[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return 0;
-        cache[dev] = n;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, attr, dev) != cudaSuccess) return 0;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
+}
+
+int sm_count_of_current_device() {
+    static std::atomic<int> cache[64];
+    return cached_attribute(cache, cudaDevAttrMultiProcessorCount);
 }
 
 // ------------------------------------------------------------ validation --
@@ -67,17 +73,8 @@ qdec_status check_row_input(const void *p, int64_t stride, int rows) {
 }
 
 int smem_per_sm_of_current_device() {
-    static int cache[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cache[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
-            cudaSuccess)
-            return 0;
-        cache[dev] = n;
-    }
-    return cache[dev];
+    static std::atomic<int> cache[64];
+    return cached_attribute(cache, cudaDevAttrMaxSharedMemoryPerMultiprocessor);
 }
 
 // ----------------------------------------------------------------- plan --
