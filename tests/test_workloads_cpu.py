@@ -101,3 +101,45 @@ def test_poison_marks_exactly_what_attention_must_not_read():
     w8 = wl.build(spec, "cpu", poison=True, kv="fp8")
     codes = w8.pools8[0]
     assert torch.all(codes[~live] == 0x7F) and torch.all(codes[live] != 0x7F)
+
+
+def test_prefill_case_packs_the_last_tokens_of_each_sequence():
+    L, n = [300, 17, 1000, 5], [20, 17, 0, 5]
+    c = wl.prefill_case(L, n, seed=11, device="cpu", pos_offset=3)
+    qo = c.qo_indptr.numpy()
+    assert list(qo) == [0, 20, 37, 37, 42] and c.q.shape[0] == 42
+    pos = c.positions.numpy()
+    for b in range(4):
+        assert list(pos[qo[b]:qo[b + 1]]) == list(range(L[b] - n[b] + 3, L[b] + 3))
+    bt = c.block_table.numpy()
+    used = [p for b in range(4) for p in bt[b, :(L[b] + 15) // 16]]
+    assert len(used) == len(set(used)) and max(used) < c.num_pages
+    assert c.num_pages == len(used) + 5                    # plus unreferenced pages
+    pool = c.pool.float()
+    for b in range(4):                                     # finite up to the last token only
+        last = bt[b, (L[b] - 1) // 16]
+        assert torch.all(torch.isfinite(pool[last, :, :, :(L[b] - 1) % 16 + 1]))
+        assert torch.all(torch.isnan(pool[last, :, :, (L[b] - 1) % 16 + 1:]))
+    free = sorted(set(range(c.num_pages)) - set(used))
+    assert torch.all(torch.isnan(pool[free]))
+
+
+def test_prefill_case_fp8_holds_the_same_draws():
+    """The FP8 case is the bf16 case's draws: scales amax/448 of every
+    (page, plane, head) block, codes within E4M3 rounding of the values up to
+    each sequence's last token, the NaN code 0x7F everywhere else."""
+    c, codes, sc = wl.prefill_case_fp8([40, 100], [40, 3], seed=13, device="cpu")
+    ref = wl.prefill_case([40, 100], [40, 3], seed=13, device="cpu", poison=False)
+    assert torch.equal(c.q, ref.q) and torch.equal(c.block_table, ref.block_table)
+    x = ref.pool.float()
+    amax = x.abs().amax(dim=(3, 4))
+    assert torch.equal(sc, torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)))
+    live = torch.zeros(x.shape, dtype=torch.bool)
+    bt = c.block_table.numpy()
+    for b, Lb in enumerate([40, 100]):
+        for t in range(Lb):
+            live[bt[b, t // 16], :, :, t % 16, :] = True
+    assert torch.all(codes[~live] == 0x7F) and torch.all(codes[live] != 0x7F)
+    dec = codes.view(torch.float8_e4m3fn).float() * sc[..., None, None]
+    bound = torch.maximum(x.abs() * 2.0 ** -4, sc[..., None, None] * 2.0 ** -10) * (1 + 1e-6)
+    assert torch.all((dec - x).abs()[live] <= bound[live])
