@@ -1,7 +1,7 @@
 """The seeded synthetic input recipe (no GPU): context-length recipes of the
 five workloads, block tables, the key-row spikes of the 8K workload, the
-per-channel K/V scales, the FP8 pools' per-(page, plane, head) scales and the
-NaN poison the tests rely on."""
+per-channel K/V scales, the FP8 pools' per-(page, plane, head) scales, the
+NaN poison the tests rely on, and the chunked-prefill inputs."""
 import math
 
 import numpy as np
