@@ -3,8 +3,10 @@
 Every function here has the name of the C entry point it calls, takes torch
 tensors that already live on the current CUDA device, passes their raw
 pointers and the current stream, and raises :class:`QdecError` on a non-OK
-status.  All arithmetic runs in the library's kernels; if the library is
-missing or cannot be loaded, importing this module fails.
+status.  A tensor that is not on the current CUDA device is refused with
+ValueError before the library is entered.  All arithmetic runs in the
+library's kernels; if the library is missing or cannot be loaded, importing
+this module fails.
 """
 from __future__ import annotations
 
