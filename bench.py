@@ -106,7 +106,14 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", type=int, default=2, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--workload", type=int, default=5, choices=sorted(wl.WORKLOADS),
+                    help="the headline workload (default 5, the largest; the others get one "
+                         "record each in the line's `configs`)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="time the headline workload only")
+    ap.add_argument("--plan-bound", type=int, default=0, metavar="TOKENS",
+                    help="plan the step for contexts up to TOKENS (a model-wide bound) "
+                         "instead of the workload's own maximum")
     ap.add_argument("--kv", choices=("bf16", "fp8"), default="bf16",
                     help="KV pool element type (fp8: E4M3 codes + per-page scales)")
     ap.add_argument("--qkv", action="store_true",
@@ -411,17 +418,27 @@ def oracle_qkv_sample(w: wl.Workload, hidden: int, seconds: float):
     return bytes_done / t_total / 1e9, n, t_total
 
 
+def reference_device() -> str:
+    """Where the reference arm synthesises its inputs: the GPU when there is
+    one (drawing an 8 GiB pool there takes a second), else the host.  The
+    oracle itself always runs on the host cores, on host copies."""
+    return "cuda:0" if torch.cuda.is_available() else "cpu"
+
+
 def run_reference(args, dist: Dist):
     """The reference arm: the CPU oracle, timed as it stands on the host."""
     if dist.rank != 0:
         return
     spec = wl.WORKLOADS[args.workload]
-    w = wl.build(spec, "cpu", layers=min(spec.layers, CPU_SAMPLE_LAYERS), kv=args.kv)
-    # warm-up steps, then exactly K timed steps; a step is one sequence of one layer
+    w = wl.build(spec, reference_device(), layers=min(spec.layers, CPU_SAMPLE_LAYERS),
+                 kv=args.kv)
+    # a step is one sequence of one layer; the host copies of the steps'
+    # inputs are made before the clock starts
     ops = oracle_qkv_operands(w, args.hidden) if args.qkv else None
-    oracle_steps(w, args.warmup, ops, args.hidden)
+    prepared = oracle_step_inputs(w, max(args.steps, args.warmup))
+    oracle_run_steps(w, prepared[:args.warmup], ops, args.hidden)
     t0 = time.perf_counter()
-    gbs_bytes = oracle_steps(w, args.steps, ops, args.hidden)
+    gbs_bytes = oracle_run_steps(w, prepared[:args.steps], ops, args.hidden)
     dt = time.perf_counter() - t0
     value = gbs_bytes / dt / 1e9
     line = {
@@ -442,14 +459,22 @@ def run_reference(args, dist: Dist):
     print(json.dumps(line), flush=True)
 
 
-def oracle_steps(w: wl.Workload, k: int, qkv_ops=None, hidden: int = 0) -> int:
-    """k oracle steps of one sequence of one layer (of the --qkv block when
-    qkv_ops holds its hidden states and weight); returns their bytes."""
+def oracle_step_inputs(w: wl.Workload, k: int):
+    """Host inputs of k oracle steps of one sequence of one layer (sequences
+    in order, then layers), as (inputs, sequence) pairs."""
     B = w.spec.batch
-    done = 0
+    out = []
     for i in range(k):
         layer, b = (i // B) % w.spec.layers, i % B
-        inp = wl.oracle_inputs(w, layer, [b])
+        out.append((wl.oracle_inputs(w, layer, [b]), b))
+    return out
+
+
+def oracle_run_steps(w: wl.Workload, prepared, qkv_ops=None, hidden: int = 0) -> int:
+    """Run prepared oracle steps (of the --qkv block when qkv_ops holds its
+    hidden states and weight); returns their bytes."""
+    done = 0
+    for inp, b in prepared:
         if qkv_ops is not None:
             oracle_qkv_block(inp, qkv_ops[0], qkv_ops[1], [b])
             done += qkv_sample_bytes(w, hidden, inp["seq_lens"])
@@ -459,7 +484,225 @@ def oracle_steps(w: wl.Workload, k: int, qkv_ops=None, hidden: int = 0) -> int:
     return done
 
 
+def oracle_steps(w: wl.Workload, k: int, qkv_ops=None, hidden: int = 0) -> int:
+    """k oracle steps of one sequence of one layer; returns their bytes."""
+    return oracle_run_steps(w, oracle_step_inputs(w, k), qkv_ops, hidden)
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def balanced_parts(seq_lens, parts: int):
+    """Sequence indices split into `parts` groups of about equal total length
+    (longest first, each to the least loaded group)."""
+    groups = [[] for _ in range(parts)]
+    load = [0] * parts
+    for b in sorted(range(len(seq_lens)), key=lambda i: -int(seq_lens[i])):
+        j = load.index(min(load))
+        groups[j].append(b)
+        load[j] += int(seq_lens[b])
+    return [sorted(g) for g in groups if g]
+
+
+def oracle_sample_all_cores(w: wl.Workload, seconds: float, threads: int):
+    """The same oracle on every host core: each layer-step's sequences are
+    split into `threads` groups of about equal length and the oracle runs on
+    each group in its own thread (the C oracle holds no shared state and the
+    call releases the interpreter lock), until `seconds` have passed.
+    Returns (GB/s, threads used, layer-steps, elapsed)."""
+    from concurrent.futures import ThreadPoolExecutor
+    groups = balanced_parts(w.seq_lens_host, threads)
+    layers = list(range(min(2, w.spec.layers)))
+    prepared = {l: [wl.oracle_inputs(w, l, g) for g in groups] for l in layers}
+    bytes_done, n, t_total = 0, 0, 0.0
+    with ThreadPoolExecutor(max_workers=len(groups)) as ex:
+        while t_total < seconds or n == 0:
+            parts = prepared[layers[n % len(layers)]]
+            t0 = time.perf_counter()
+            list(ex.map(oracle_layer, parts))
+            t_total += time.perf_counter() - t0
+            bytes_done += sample_bytes(w, w.seq_lens_host)
+            n += 1
+    return bytes_done / t_total / 1e9, len(groups), n, t_total
+
+
 # -------------------------------------------------------------- our path --
+# A model-wide plan bound for the graph-reuse records: the step is captured
+# once for contexts up to this many tokens and replayed on shorter ones.
+MODEL_SEQ_BOUND = 16384
+
+
+class DecodeLayers:
+    """Device buffers, shape and step function of one decode workload on
+    this rank's GPU.  plan_bound > 0 plans (and sizes the block-table rows
+    for) contexts up to plan_bound tokens instead of the workload's own
+    maximum, as an engine that captures one graph for every length would."""
+
+    def __init__(self, qdec, w: wl.Workload, args, stream, plan_bound: int = 0):
+        self.qdec, self.w, self.args, self.stream = qdec, w, args, stream
+        spec = w.spec
+        P = spec.page_size
+        mb = w.max_blocks
+        self.block_table = w.block_table
+        if plan_bound:
+            mb = max(mb, (plan_bound + P - 1) // P)
+            bt = torch.full((spec.batch, mb), -1, dtype=torch.int32, device=w.block_table.device)
+            bt[:, :w.max_blocks] = w.block_table
+            self.block_table = bt
+        flags = 0 if args.no_overlap else qdec.QDEC_LAUNCH_OVERLAP_PREVIOUS
+        self.shape = qdec.Shape(batch=spec.batch, num_pages=spec.pool_pages,
+                                max_blocks_per_seq=mb,
+                                max_seq_len=max(plan_bound, w.max_blocks * P) if plan_bound
+                                else mb * P,
+                                num_q_heads=spec.num_q_heads, num_kv_heads=spec.num_kv_heads,
+                                head_dim=spec.head_dim, page_size=P, launch_flags=flags)
+        self.ws = qdec.alloc_workspace(self.shape)
+        self.rope = qdec.alloc_rope_table(self.shape)
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.out = torch.empty((spec.layers, spec.batch, spec.num_q_heads, spec.head_dim),
+                               dtype=torch.bfloat16, device="cuda")
+
+    def step_fn(self, qkv, seq_lens, positions, block_table, out_t):
+        """One decode step (the rope table, then every layer) on these buffers."""
+        qdec, w, shape, s = self.qdec, self.w, self.shape, self.stream
+        Hq, Hkv = w.spec.num_q_heads, w.spec.num_kv_heads
+
+        def fn():
+            qdec.qdec_rope_table(shape, positions, self.rope, stream=s)
+            for l in range(w.spec.layers):
+                if w.kv == "fp8":
+                    qdec.qdec_step_fp8(shape, qkv[l, :, :Hq], qkv[l, :, Hq:Hq + Hkv],
+                                       qkv[l, :, Hq + Hkv:], w.w_q[l], w.w_k[l], positions,
+                                       seq_lens, block_table, w.pool8(l), w.scale(l), self.ws,
+                                       out_t[l], self.err, stream=s, rope_table=self.rope)
+                else:
+                    qdec.qdec_step(shape, qkv[l, :, :Hq], qkv[l, :, Hq:Hq + Hkv],
+                                   qkv[l, :, Hq + Hkv:], w.w_q[l], w.w_k[l], positions,
+                                   seq_lens, block_table, w.pool(l), self.ws, out_t[l],
+                                   self.err, stream=s, rope_table=self.rope)
+        return fn
+
+    def default_step(self):
+        w = self.w
+        return self.step_fn(w.qkv, w.seq_lens, w.positions, self.block_table, self.out)
+
+    def check(self):
+        st, flags = self.qdec.qdec_check_error(self.err, self.stream)
+        assert st == 0, f"device error flags {flags:#x}"
+
+
+def capture(fn, stream):
+    """fn once eagerly (it configures the kernels outside capture), then
+    captured into a CUDA graph; returns the graph's replay."""
+    with torch.cuda.stream(stream):
+        fn()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    capture.keep.append(g)
+    return g.replay
+
+
+capture.keep = []
+
+
+def timed_steps(run, stream, steps: int, warmup: int, dist: Dist, flush=None, clocks=None):
+    """warmup untimed steps, then exactly `steps` timed ones, bracketed by a
+    barrier and a device synchronisation.  With `flush` (a buffer larger than
+    L2) it is rewritten before every step, outside the per-step events, and
+    the time is the sum of the steps; else the whole region.  Returns
+    (this rank's ms, max over ranks of it, per-step ms)."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            run()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if clocks:
+        clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for k in range(steps):
+            if flush is not None:
+                flush.add_(1)   # evict the previous step's lines from L2 (not timed)
+            starts[k].record(stream)
+            run()
+            ends[k].record(stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    per = [a.elapsed_time(e) for a, e in zip(starts, ends)]
+    t_ms = sum(per) if flush is not None else e0.elapsed_time(e1)
+    return t_ms, dist.max(t_ms), per
+
+
+def l2_flush_buffer(bytes_step: int, l2: int):
+    """A buffer of twice the L2 size when a step's inputs would fit in it."""
+    if bytes_step < 2 * l2:
+        return torch.empty(2 * l2 // 4, dtype=torch.int32, device="cuda")
+    return None
+
+
+def config_record(qdec, workload_id: int, args, dist: Dist, dev: int, peak: float) -> dict:
+    """One bench record per workload (besides the headline line): µs per
+    layer-step and GB/s of the graph-replayed step (the contract's timing),
+    the same step launched from the host without a graph, for workload 1
+    also L2-warm, and for the short-context workloads 2 and 4 also with the
+    step planned for a model-wide bound of MODEL_SEQ_BOUND tokens."""
+    spec = wl.WORKLOADS[workload_id]
+    w = wl.build(spec, f"cuda:{dev}", kv=args.kv)
+    L = w.spec.layers
+    stream = torch.cuda.Stream()
+    bytes_layer = w.algorithmic_bytes_per_layer()
+    l2 = l2_bytes(dev)
+    flush = l2_flush_buffer(bytes_layer * L, l2)
+
+    def measure(layers: DecodeLayers, graph: bool, fl, with_clocks: bool):
+        step = layers.default_step()
+        run = capture(step, stream) if graph else step
+        if not graph:
+            with torch.cuda.stream(stream):
+                step()   # first launch configures the kernels
+        ck = Clocks(dev) if with_clocks else None
+        t_ms, t_max, _ = timed_steps(run, stream, args.steps, max(3, args.warmup), dist, fl, ck)
+        layers.check()
+        us = t_max / args.steps / L * 1e3
+        rec = {"us_per_layer_step": round(us, 4),
+               "gbs": round(dist.world * bytes_layer / (us * 1e-6) / 1e9, 2),
+               "frac_of_hbm": round(bytes_layer / (us * 1e-6) / 1e9 / peak, 4)}
+        if ck:
+            rec["clocks"] = ck.stop()
+        return rec
+
+    base = DecodeLayers(qdec, w, args, stream)
+    rec = {"workload": workload_name(w.spec, w.kv), "layers": L,
+           "bytes_per_layer_step": bytes_layer,
+           "l2": "flushed before each step" if flush is not None else "inputs larger than L2",
+           "plan": "exact bound (max_seq_len = the workload's block-table rows x 16)"}
+    rec.update(measure(base, True, flush, True))
+    rec["eager"] = measure(base, False, flush, False)
+    if flush is not None:
+        rec["l2_warm"] = measure(base, True, None, False)
+    if workload_id in (2, 4) and w.spec.max_seq_len_bound < MODEL_SEQ_BOUND:
+        bound = DecodeLayers(qdec, w, args, stream, plan_bound=MODEL_SEQ_BOUND)
+        rec[f"plan_bound_{MODEL_SEQ_BOUND}"] = measure(bound, True, flush, False)
+        del bound
+    del base, w, flush
+    capture.keep.clear()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_ours(args, dist: Dist):
     from gqa_paged_kv_gb300 import build as qbuild
     qbuild.build()
@@ -471,14 +714,9 @@ def run_ours(args, dist: Dist):
     w = wl.build(spec, f"cuda:{dev}", layers=args.layers or None, kv=args.kv)
     spec = w.spec
     L = spec.layers
-    shape = qdec.shape_for(w, launch_flags=0 if args.no_overlap
-                           else qdec.QDEC_LAUNCH_OVERLAP_PREVIOUS)
     stream = torch.cuda.Stream()
-    ws = qdec.alloc_workspace(shape)
-    rope = qdec.alloc_rope_table(shape)
-    err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = torch.empty((L, spec.batch, spec.num_q_heads, spec.head_dim), dtype=torch.bfloat16,
-                      device="cuda")
+    layers = DecodeLayers(qdec, w, args, stream, plan_bound=args.plan_bound)
+    shape, ws, rope, err, out = layers.shape, layers.ws, layers.rope, layers.err, layers.out
     torch.cuda.synchronize()
 
     Hq, Hkv = spec.num_q_heads, spec.num_kv_heads
@@ -499,92 +737,43 @@ def run_ours(args, dist: Dist):
     else:
         step_in = w.qkv
 
-    def qkv_layer(l, x, seq_lens, positions, block_table, out_l):
-        qdec.qdec_qkv_append_rope(shape, x, w_qkv[l], w.w_q[l], w.w_k[l], positions, seq_lens,
-                                  block_table, w.pool(l), q_rot, rope, err, stream=stream)
-        qdec.qdec_attn_decode(shape, q_rot, w.pool(l), block_table, seq_lens, ws, out_l, err,
-                              stream=stream)
-
     def step_fn(qkv, seq_lens, positions, block_table, out_t):
         """One decode step (the rope table, then the L layers) on these buffers."""
+        if not args.qkv:
+            return layers.step_fn(qkv, seq_lens, positions, block_table, out_t)
+
         def fn():
             qdec.qdec_rope_table(shape, positions, rope, stream=stream)
             for l in range(L):
-                if args.qkv:
-                    qkv_layer(l, qkv[l], seq_lens, positions, block_table, out_t[l])
-                elif w.kv == "fp8":
-                    qdec.qdec_step_fp8(shape, qkv[l, :, :Hq], qkv[l, :, Hq:Hq + Hkv],
-                                       qkv[l, :, Hq + Hkv:], w.w_q[l], w.w_k[l], positions,
-                                       seq_lens, block_table, w.pool8(l), w.scale(l), ws,
-                                       out_t[l], err, stream=stream, rope_table=rope)
-                else:
-                    qdec.qdec_step(shape, qkv[l, :, :Hq], qkv[l, :, Hq:Hq + Hkv],
-                                   qkv[l, :, Hq + Hkv:], w.w_q[l], w.w_k[l], positions, seq_lens,
-                                   block_table, w.pool(l), ws, out_t[l], err, stream=stream,
-                                   rope_table=rope)
+                qdec.qdec_qkv_append_rope(shape, qkv[l], w_qkv[l], w.w_q[l], w.w_k[l], positions,
+                                          seq_lens, block_table, w.pool(l), q_rot, rope, err,
+                                          stream=stream)
+                qdec.qdec_attn_decode(shape, q_rot, w.pool(l), block_table, seq_lens, ws,
+                                      out_t[l], err, stream=stream)
         return fn
 
     def graph_of(fn):
         if args.no_graph:
+            with torch.cuda.stream(stream):
+                fn()   # the first launch configures the kernels
             return fn
-        # one graph per step (the first layer is a programmatic dependent of
-        # the table kernel)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream):
-                fn()
-        graphs.append(g)
-        return g.replay
+        return capture(fn, stream)
 
-    graphs = []
-    step0 = step_fn(step_in, w.seq_lens, w.positions, w.block_table, out)
-    with torch.cuda.stream(stream):
-        step0()  # the first launch configures the kernels outside capture
-    stream.synchronize()
-    run = graph_of(step0)
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            run()
-    stream.synchronize()
-    st, flags = qdec.qdec_check_error(err, stream)
-    assert st == 0, f"device error flags {flags:#x}"
+    run = graph_of(step_fn(step_in, w.seq_lens, w.positions, layers.block_table, out))
 
     # Steps whose inputs fit in L2 twice over are timed L2-cold: a buffer
     # larger than L2 is rewritten before each one, outside the timed steps.
     l2 = l2_bytes(dev)
     bytes_layer = (block_bytes_per_layer(w, args.hidden) if args.qkv
                    else w.algorithmic_bytes_per_layer())
-    flush = (torch.empty(2 * l2 // 4, dtype=torch.int32, device="cuda")
-             if bytes_layer * L < 2 * l2 else None)
+    flush = l2_flush_buffer(bytes_layer * L, l2)
 
-    # ---- device-timed region
+    # ---- device-timed region (clocks sampled during it)
     clocks = Clocks(dev)
-    clocks.start()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    dist.barrier()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for k in range(args.steps):
-            if flush is not None:
-                flush.add_(1)   # evict the previous step's lines from L2 (not timed)
-            starts[k].record(stream)
-            run()
-            ends[k].record(stream)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    dist.barrier()
+    t_ms, t_ms_max, per = timed_steps(run, stream, args.steps, args.warmup, dist, flush, clocks)
     ck = clocks.stop()
-    # the steps themselves: without a flush this is the whole region
-    t_ms = (sum(a.elapsed_time(e) for a, e in zip(starts, ends)) if flush is not None
-            else e0.elapsed_time(e1))
-    t_steps_ms = sum(a.elapsed_time(e) for a, e in zip(starts, ends))
-    t_ms_max = dist.max(t_ms)
-    st, flags = qdec.qdec_check_error(err, stream)
-    assert st == 0, f"device error flags {flags:#x}"
+    layers.check()
+    t_steps_ms = sum(per)
 
     bytes_step = bytes_layer * L
     ms_step = t_ms_max / args.steps
@@ -597,6 +786,7 @@ def run_ours(args, dist: Dist):
                                             else "attention_kernel<fused>")
     roof_how = (f"CUDA events around each step's graph (rope table + {L} launches, gaps "
                 f"included) / {L}")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if args.qkv:
         # the projection kernel alone: a graph of its L launches, timed the same way
         gq = torch.cuda.CUDAGraph()
@@ -604,8 +794,8 @@ def run_ours(args, dist: Dist):
             with torch.cuda.graph(gq, stream=stream):
                 for l in range(L):
                     qdec.qdec_qkv_append_rope(shape, step_in[l], w_qkv[l], w.w_q[l], w.w_k[l],
-                                              w.positions, w.seq_lens, w.block_table, w.pool(l),
-                                              q_rot, rope, err, stream=stream)
+                                              w.positions, w.seq_lens, layers.block_table,
+                                              w.pool(l), q_rot, rope, err, stream=stream)
             for _ in range(3):
                 gq.replay()
             e0.record(stream)
@@ -621,15 +811,17 @@ def run_ours(args, dist: Dist):
         roof_how = f"CUDA events around a graph of {L} projection launches, {reps} replays"
     peak, peak_kind = measured_peaks()
 
-    # ---- end to end: pinned host inputs in, outputs out, every step.  Two
-    # sets of device buffers: a step's input copies and its output copy run on
-    # their own streams, overlapping the neighbouring steps' kernels.
-    meta = [w.seq_lens, w.positions, w.block_table]
+    # ---- end to end, over as many steps as the device-timed region: every
+    # step copies its new-token inputs and metadata in from pinned host
+    # memory and its outputs back.  Two sets of device buffers: a step's
+    # input copies and its output copy run on their own streams, overlapping
+    # the neighbouring steps' kernels.
+    meta = [w.seq_lens, w.positions, layers.block_table]
     qkv_h = step_in.cpu().pin_memory()
     meta_h = [m.cpu().pin_memory() for m in meta]
     h2d = qkv_h.numel() * qkv_h.element_size() + sum(m.numel() * m.element_size() for m in meta_h)
     d2h = out.numel() * out.element_size()
-    k_e2e = 0 if args.no_e2e else max(1, args.steps // 4)
+    k_e2e = 0 if args.no_e2e else args.steps
     if k_e2e:
         sets = []
         for j in range(2):
@@ -660,7 +852,7 @@ def run_ours(args, dist: Dist):
                 s_out.wait_event(b["done"])
                 b["out_h"].copy_(b["out"], non_blocking=True)
 
-        for k in range(max(3, args.warmup // 4)):
+        for k in range(max(3, args.warmup)):
             e2e_step(k)
         torch.cuda.synchronize()
         dist.barrier()
@@ -673,8 +865,7 @@ def run_ours(args, dist: Dist):
         dist.barrier()
         t_e2e = dist.max(e0.elapsed_time(e1))
     e2e_value = dist.world * bytes_step * k_e2e / (t_e2e * 1e-3) / 1e9 if k_e2e else None
-    st, flags = qdec.qdec_check_error(err, stream)
-    assert st == 0, f"device error flags {flags:#x}"
+    layers.check()
 
     traffic = None
     tr = TRAFFIC.get(workload_name(spec, w.kv, args.hidden if args.qkv else 0))
@@ -690,27 +881,54 @@ def run_ours(args, dist: Dist):
                "sample": f"{n} x one layer (all sequences) of the QKV block of "
                          f"{workload_name(spec, w.kv, args.hidden)} "
                          f"(layers 0-{w_cpu.spec.layers - 1}), fp64, {secs:.1f} s"}
+        del w_cpu
     elif dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        w_cpu = wl.build(spec, "cpu", layers=min(spec.layers, CPU_SAMPLE_LAYERS), kv=w.kv)
-        gbs, what, n, secs = oracle_sample(w_cpu, args.cpu_seconds, per_seq=False)
+        # host copies of the sampled layers come from the GPU workload (the
+        # pages each layer references); the oracle runs on the host cores
+        gbs, what, n, secs = oracle_sample(w, args.cpu_seconds, per_seq=False)
         cpu = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n} x {what} of {workload_name(spec, w.kv)} "
-                             f"(layers 0-{w_cpu.spec.layers - 1}), "
-                             f"fp64, {secs:.1f} s"}
+               "sample": f"{n} x {what} of {workload_name(spec, w.kv)}, fp64, {secs:.1f} s"}
+        gbs_all, used, n_all, secs_all = oracle_sample_all_cores(w, args.cpu_seconds,
+                                                                host_cores())
+        cpu["all_cores"] = {
+            "value": round(gbs_all, 6), "unit": "GB/s", "cores": used, "kind": "oracle",
+            "sample": f"{n_all} x one layer, its sequences split into {used} groups of about "
+                      f"equal length, one oracle call per group on its own thread "
+                      f"({host_cores()} host cores), fp64, {secs_all:.1f} s"}
+
+    cfg = workload_config(w, args, dist.world, l2)
+    if args.plan_bound:
+        cfg["plan"] = (f"planned for contexts up to {args.plan_bound} tokens (block-table rows "
+                       f"of {layers.shape.max_blocks_per_seq} pages)")
+    configs = []
+    if not args.qkv and not args.layers and not args.no_configs:
+        # the other workloads of the benchmark plan, each on its own (the
+        # headline's buffers are released first)
+        del layers, run, w, step_in, flush
+        if k_e2e:
+            del sets
+        capture.keep.clear()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        for wid in sorted(wl.WORKLOADS):
+            if wid != args.workload:
+                configs.append(config_record(qdec, wid, args, dist, dev, peak))
 
     if dist.rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": ("e4m3 KV (e4m3 q.k and f16 p.v mma, f32 accumulate)" if w.kv == "fp8" else "bf16"),
+            "dtype": ("e4m3 KV (e4m3 q.k and f16 p.v mma, f32 accumulate)" if args.kv == "fp8"
+                      else "bf16"),
             "data": ("synthetic (seeded N(0,1) bf16 hidden states, N(0,1/hidden) bf16 merged "
                      "QKV weights and KV pages)" if args.qkv else
                      "synthetic (seeded N(0,1) bf16 q/k/v and KV pages"
-                     + (", pages cast to E4M3 with amax/448 scales)" if w.kv == "fp8" else ")")),
+                     + (", pages cast to E4M3 with amax/448 scales)" if args.kv == "fp8"
+                        else ")")),
             "us_per_layer_step": round(ms_step * 1e3 / L, 4),
             "pct_of_hbm_peak": round(100 * value / dist.world / peak, 2),
-            "config": workload_config(w, args, dist.world, l2_bytes(dev)),
+            "config": cfg,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
@@ -726,6 +944,8 @@ def run_ours(args, dist: Dist):
             "clocks": ck,
             "cpu_baseline": cpu,
         }
+        if configs:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
 
 

@@ -137,8 +137,11 @@ int64_t cluster_capacity(const qdec_shape *s, int c, int cap, bool fp8) {
         std::lock_guard<std::mutex> lock(mu);
         n = cache_smem[dev][t][c] == smem ? cache[dev][t][c] : 0;
         if (n == 0) {
+            // a failed query leaves no error behind, but an error the caller
+            // has not read yet stays pending
+            const cudaError_t pending = cudaPeekAtLastError();
             n = qdec::max_active_clusters(c, smem, fp8);
-            cudaGetLastError();  // a failed query leaves no sticky state behind
+            if (pending == cudaSuccess) cudaGetLastError();
             if (n <= 0) n = -1;
             cache[dev][t][c] = n;
             cache_smem[dev][t][c] = smem;

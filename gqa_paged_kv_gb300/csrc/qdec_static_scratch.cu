@@ -36,9 +36,12 @@ qdec_status scratch_address(void **addr) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_scratch_addr[dev] == nullptr) {
         void *ptr = nullptr;
+        // An error the caller has not read yet stays pending; only the one
+        // this lookup raised is cleared.
+        const cudaError_t pending = cudaPeekAtLastError();
         const cudaError_t e = cudaGetSymbolAddress(&ptr, g_static_scratch);
         if (e != cudaSuccess || ptr == nullptr) {
-            cudaGetLastError();
+            if (pending == cudaSuccess) cudaGetLastError();
             return QDEC_ERR_CUDA;
         }
         g_scratch_addr[dev] = ptr;

@@ -408,7 +408,10 @@ qdec_status qdec_step_fp8(const qdec_shape *shape,
  *   - Every call, on any stream, uses the same array, which keeps the
  *     previous call's contents; each call clears the counters it needs on its
  *     stream before the kernel runs.  Calls that can overlap on the GPU (other
- *     streams, other threads) race on the array: serialise them. */
+ *     streams, other threads) race on the array: serialise them.
+ *   - That clearing is a memset on the stream between the previous kernel
+ *     and this call's kernel, so QDEC_LAUNCH_OVERLAP_PREVIOUS does not let the
+ *     kernel start before the previous one ends through this entry point. */
 #define QDEC_STATIC_SCRATCH_BYTES (4u << 20)
 qdec_status qdec_step_static_scratch(const qdec_shape *shape,
                                      const qdec_bf16 *q, int64_t q_stride,

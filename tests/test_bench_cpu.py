@@ -80,3 +80,37 @@ def test_oracle_samples_of_the_qkv_block_and_prefill_run():
         run, flops, Pc = bench.oracle_prefill_sample(48, fp8)
         run()
         assert Pc == 48 and flops == bench.prefill_flops([48], [48])
+
+
+def test_balanced_parts_cover_every_sequence_once():
+    rng = np.random.default_rng(5)
+    for parts in (1, 3, 16):
+        lens = rng.integers(1, 16384, size=64)
+        groups = bench.balanced_parts(lens, parts)
+        flat = sorted(b for g in groups for b in g)
+        assert flat == list(range(64)) and len(groups) == min(parts, 64)
+        loads = [int(lens[g].sum()) for g in groups]
+        # greedy longest-first: no group exceeds the mean by more than the longest sequence
+        assert max(loads) <= sum(loads) / len(loads) + lens.max()
+
+
+def test_all_core_oracle_sample_runs_on_threads():
+    """The all-core CPU baseline: a layer's sequences split over threads,
+    the same oracle call per group; it reports the threads it used."""
+    from gqa_paged_kv_gb300 import workloads as wl
+    spec = wl.custom(5, [40, 17, 300, 2, 90], pool_pages=64, layers=2)
+    w = wl.build(spec, "cpu")
+    gbs, used, n, secs = bench.oracle_sample_all_cores(w, 0.0, 3)
+    assert gbs > 0 and used == 3 and n == 1 and secs > 0
+    gbs1, what, n1, _ = bench.oracle_sample(w, 0.0, per_seq=False)
+    assert gbs1 > 0 and n1 == 1
+
+
+def test_reference_arm_prepares_its_steps_outside_the_clock():
+    from gqa_paged_kv_gb300 import workloads as wl
+    spec = wl.custom(2, [40, 17], pool_pages=16, layers=2)
+    w = wl.build(spec, "cpu")
+    prepared = bench.oracle_step_inputs(w, 5)
+    assert [b for _, b in prepared] == [0, 1, 0, 1, 0]
+    assert bench.oracle_run_steps(w, prepared) == sum(
+        bench.sample_bytes(w, [L]) for L in (40, 17, 40, 17, 40))
