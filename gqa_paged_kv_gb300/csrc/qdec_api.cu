@@ -175,7 +175,11 @@ Plan plan_for(const qdec_shape *s, bool allow_cluster, bool fp8) {
     const int64_t per_cta = (wmax + target - 1) / target;
     const int64_t segs = static_cast<int64_t>(s->batch) * s->num_kv_heads;
     const int64_t nmax = (s->max_seq_len + qdec::kPageSize - 1) / qdec::kPageSize;
-    if (s->num_ctas == 0 && allow_cluster && per_cta < kFlatMinTilesPerCta) {
+    // Few segments: every one can have CTAs of its own within the grid share,
+    // so the cluster layout's per-segment split adapts to the actual lengths
+    // whatever the bound (an engine plans one graph for its longest context).
+    const bool few_segments = static_cast<double>(segs) <= kGridShare * static_cast<double>(target);
+    if (s->num_ctas == 0 && allow_cluster && (per_cta < kFlatMinTilesPerCta || few_segments)) {
         const double bytes =
             static_cast<double>(wmax) * (fp8 ? qdec::kFp8TileBytes : qdec::kTileBytes);
         const double want = std::min(kGridShare * static_cast<double>(target), bytes / kBytesPerCta);
@@ -199,7 +203,8 @@ Plan plan_for(const qdec_shape *s, bool allow_cluster, bool fp8) {
                 break;  // the largest cluster that fits, for this k
             }
         }
-        if (pl.grid == 0 && widest.grid > 0 && per_cta < kFlatMinTilesPerCta / 2) pl = widest;
+        if (pl.grid == 0 && widest.grid > 0 && (per_cta < kFlatMinTilesPerCta / 2 || few_segments))
+            pl = widest;
         if (pl.grid > 0) return pl;
     }
     // flat layout: a whole number of CTAs per SM for the pool type in the

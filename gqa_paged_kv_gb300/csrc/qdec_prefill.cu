@@ -110,10 +110,26 @@ __device__ __forceinline__ bool chunk_ok(const Params &p, int b, int &n, int &L)
 // One CTA per chunk row, 256 threads: the 64 angles of the row's position are
 // taken once (double sincos) into shared memory; warp w then handles KV head
 // w (and w + 8, ...): its four query rows in fp32 (q_rot's tolerance is
-// absolute), its key row with the rotation's difference in double (a key near
-// zero keeps its relative accuracy, so it stays within one bf16 step of the
-// exact value), and the copy of its value row.
+// absolute), its key row in double from the sum of squares on (about 1e-16
+// relative error, so rounding it once to bf16 gives the nearest-even bf16 of
+// the exact value: a key near zero keeps its relative accuracy too), and the
+// copy of its value row.
 constexpr int kPfAppendThreads = 256;
+
+// bf16 nearest-even of a double, rounded once: truncation to binary32 with
+// the inexactness kept in the last bit (round-to-odd, 24 bits), then
+// nearest-even to bf16's 8 bits.  Rounding to odd with at least two more bits
+// than the target never changes the final nearest-even result (Boldo and
+// Melquiond, "When double rounding is odd", 2005).
+__device__ __forceinline__ float round_to_odd_float(double d) {
+    const float f = __double2float_rz(d);
+    return static_cast<double>(f) == d ? f : __uint_as_float(__float_as_uint(f) | 1u);
+}
+__device__ __forceinline__ uint32_t pack_bf16x2_of_doubles(double lo, double hi) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(round_to_odd_float(lo)))) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(round_to_odd_float(hi))))
+            << 16);
+}
 
 // E4M3 codes of a / s and b / s (fp32 division, one rounding each, then
 // nearest-even with saturation to +-448), a in the low byte.
@@ -180,12 +196,23 @@ __global__ void __launch_bounds__(kPfAppendThreads) prefill_append_kernel(
         }
         const int64_t slot =
             ((static_cast<int64_t>(page) * 2 * p.Hkv + g) * kPageSize + t % kPageSize) * kHeadDim;
-        float nv[4];
-        const double rn = norm(p.k + static_cast<int64_t>(r) * p.k_stride + g * kHeadDim, p.w_k, nv);
-        const uint32_t k01 = pack_bf16x2(static_cast<float>(rn * (nv[0] * c0 - nv[2] * s0)),
-                                         static_cast<float>(rn * (nv[1] * c1 - nv[3] * s1)));
-        const uint32_t k23 = pack_bf16x2(static_cast<float>(rn * (nv[2] * c0 + nv[0] * s0)),
-                                         static_cast<float>(rn * (nv[3] * c1 + nv[1] * s1)));
+        // the key: sum of squares, root and rotation in double (x^2 and x w
+        // are exact in fp32), one rounding to bf16
+        const __nv_bfloat16 *krow = p.k + static_cast<int64_t>(r) * p.k_stride + g * kHeadDim;
+        const float2 ka = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(krow)[lane]);
+        const float2 kc =
+            __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(krow + 64)[lane]);
+        const float2 wka = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(p.w_k)[lane]);
+        const float2 wkc =
+            __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(p.w_k + 64)[lane]);
+        double kss = (static_cast<double>(ka.x * ka.x) + static_cast<double>(ka.y * ka.y)) +
+                     (static_cast<double>(kc.x * kc.x) + static_cast<double>(kc.y * kc.y));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) kss += __shfl_xor_sync(kFull, kss, o);
+        const double rn = 1.0 / sqrt(kss / kHeadDim + static_cast<double>(p.eps));
+        const double n0 = ka.x * wka.x, n1 = ka.y * wka.y, n2 = kc.x * wkc.x, n3 = kc.y * wkc.y;
+        const uint32_t k01 = pack_bf16x2_of_doubles(rn * (n0 * c0 - n2 * s0), rn * (n1 * c1 - n3 * s1));
+        const uint32_t k23 = pack_bf16x2_of_doubles(rn * (n2 * c0 + n0 * s0), rn * (n3 * c1 + n1 * s1));
         const uint32_t *vs = reinterpret_cast<const uint32_t *>(
             p.v + static_cast<int64_t>(r) * p.v_stride + g * kHeadDim);
         const uint32_t v01 = vs[lane], v23 = vs[32 + lane];

@@ -9,9 +9,11 @@ layer-steps) is captured ONCE with a plan for contexts up to 16384 tokens;
 then, for one set of lengths after another, the lengths, positions, block
 table, new-token rows and pools are rewritten in place and the same graph is
 replayed; every layer's output and appended slots are compared with the
-oracle.  Lengths run from 1 to the bound, across page boundaries; a batch of
-one is planned on the cluster layout and a batch of four on the flat layout,
-so both layouts take every length.
+oracle.  Lengths run from 1 to the bound, across page boundaries.  Batches of
+one and four sequences (8 and 32 (sequence, KV head) segments) are planned on
+the cluster layout, whose per-segment split follows the actual lengths; a
+batch of 24 (192 segments, more than 60 % of the CTAs resident on a 152-SM
+GPU) on the flat layout, so both layouts take every length.
 """
 import numpy as np
 import pytest
@@ -27,10 +29,15 @@ PAGE = 16
 MAX_BLOCKS = BOUND // PAGE
 LAYERS = 3
 
+_R = np.random.default_rng(77)
 LENGTH_SETS = {
     1: [[1], [2], [16], [17], [300], [1024], [4097], [8192], [12345], [16383], [16384]],
     4: [[1, 2, 15, 16], [17, 300, 64, 1000], [16384, 1, 5000, 33], [8192, 8192, 8192, 8192],
         [513, 4097, 12000, 7], [16384, 16384, 16384, 16384]],
+    24: [[1, 2, 15, 16, 17, 31, 32, 33] * 3,
+         [16384, 1] + [int(x) for x in _R.integers(1, 400, 22)],
+         [int(x) for x in np.exp(_R.uniform(0.0, np.log(16384), 24)).round().clip(1, 16384)],
+         [384] * 24],
 }
 
 
