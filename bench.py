@@ -64,7 +64,7 @@ KERNEL_SOURCES = {
     "qkv_append_kernel": tuple(_CSRC + f for f in ("qdec_qkv.cu", "qdec_internal.h",
                                                    "qdec_ptx.cuh")),
     "prefill_attention_kernel": tuple(_CSRC + f for f in ("qdec_prefill.cu", "qdec_internal.h",
-                                                          "qdec_ptx.cuh")),
+                                                          "qdec_ptx.cuh", "qdec_tc.cuh")),
 }
 
 # DRAM bytes per launch of the fused kernel measured with ncu (see
@@ -1197,8 +1197,9 @@ def run_prefill(args, dist: Dist):
             "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,
-            "dtype": ("e4m3 KV converted to bf16 in shared memory" if fp8 else "bf16")
-                     + " (mma.sync bf16, q as hi+lo, f32 accumulate)",
+            "dtype": ("e4m3 KV converted to bf16 in shared memory (mma.sync bf16, q as hi+lo, "
+                      "f32 accumulate)" if fp8 else
+                      "bf16 (tcgen05 kind::f16, q as hi+lo, f32 accumulators in tensor memory)"),
             "data": "synthetic (seeded N(0,1) bf16 q/k/v, U(0.5,1.5) norm weights)",
             "us_per_layer_step": round(ms_step * 1e3 / L, 3),
             "config": prefill_config(P, L, fp8),
@@ -1206,7 +1207,9 @@ def run_prefill(args, dist: Dist):
                          "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, cuBLAS "
                                       f"burst)" if peak_kind == "measured" else "fallback",
-                         "kernel": "prefill_attention_kernel", "launch_us": round(launch_us, 3),
+                         "kernel": ("prefill_attention_kernel<fp8>" if fp8
+                                    else "prefill_attention_tc_kernel"),
+                         "launch_us": round(launch_us, 3),
                          "launch_us_how": f"CUDA events around a graph of {L} attention "
                                           f"launches, {reps} replays",
                          "flops_per_launch": flops_layer},

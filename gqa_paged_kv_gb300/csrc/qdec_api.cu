@@ -341,6 +341,26 @@ qdec_status encode_pool_map(CUtensorMap *map, const qdec_shape *s, const void *p
     return r == CUDA_SUCCESS ? QDEC_OK : QDEC_ERR_CUDA;
 }
 
+// The same 5-D view of the bf16 pool with a box of one (page, plane, half
+// of D) region: 16 tokens x 64 dims, 2 KiB (the tensor-core prefill brings
+// each region of four pages side by side).
+qdec_status encode_pool_region_map(CUtensorMap *map, const qdec_shape *s, const void *pool) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return QDEC_ERR_CUDA;
+    const cuuint64_t plane = static_cast<cuuint64_t>(qdec::kPageSize) * qdec::kHeadDim * 2;
+    const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(qdec::kPageSize), 2, 2,
+                                static_cast<cuuint64_t>(s->num_pages) * 2 * s->num_kv_heads};
+    const cuuint64_t strides[4] = {qdec::kHeadDim * 2, 128,
+                                   static_cast<cuuint64_t>(s->num_kv_heads) * plane, plane};
+    const cuuint32_t box[5] = {64, static_cast<cuuint32_t>(qdec::kPageSize), 1, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(pool), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? QDEC_OK : QDEC_ERR_CUDA;
+}
+
 // The FP8 pool as a 4-D tensor whose box is one page tile: dims (128 bytes
 // of D, token [16], plane K/V [2], page*2*Hkv + head), strides (128,
 // Hkv*2048, 2048) bytes; 128-byte rows swizzled as in the bf16 map.
@@ -602,6 +622,11 @@ qdec_status prefill_attn_impl(const qdec_shape *shape, int32_t num_tokens, const
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
     p.err = err_flag;
     CUtensorMap map;
+    if (!pool.fp8) {  // bf16 pool: the tensor-core kernel
+        if ((st = encode_pool_region_map(&map, shape, pool.data)) != QDEC_OK) return st;
+        return cuda_status(
+            qdec::launch_prefill_attention_tc(p, map, static_cast<cudaStream_t>(stream)));
+    }
     if ((st = encode_map(&map, shape, pool)) != QDEC_OK) return st;
     return cuda_status(
         qdec::launch_prefill_attention(p, map, pool.fp8, static_cast<cudaStream_t>(stream)));

@@ -126,6 +126,10 @@ cudaError_t launch_merge(const Params &p, cudaStream_t s);
 cudaError_t launch_prefill_append(const Params &p, bool fp8, cudaStream_t s);
 cudaError_t launch_prefill_attention(const Params &p, const CUtensorMap &kv_map, bool fp8,
                                      cudaStream_t s);
+// The same attention over a bf16 pool on the 5th-generation tensor core;
+// region_map views the pool with one (page, plane, half of D) region per box.
+cudaError_t launch_prefill_attention_tc(const Params &p, const CUtensorMap &region_map,
+                                        cudaStream_t s);
 
 // The merged QKV projection fused with steps 1-3 (qdec_qkv.cu): the weight
 // comes packed (qdec_qkv_pack_weights), x_map views x [B][hidden] with boxes

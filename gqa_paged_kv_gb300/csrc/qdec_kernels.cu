@@ -58,6 +58,7 @@
 // waits too before its first copy.
 #include "qdec_internal.h"
 #include "qdec_ptx.cuh"
+#include "qdec_ff.cuh"
 #include "qdec.h"
 
 #include <cuda_fp16.h>
@@ -225,60 +226,6 @@ __device__ __forceinline__ uint32_t pack_bf16(__nv_bfloat16 lo, __nv_bfloat16 hi
            (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
 }
 
-// ----------------------------------------------------- float-float math --
-// Unevaluated sums hi + lo of two floats (Dekker 1971; Knuth's TwoSum):
-// ~48 significant bits from fp32 arithmetic, so the appended key can be
-// rounded to bf16 as if from the exact value without fp64 (which GB300
-// executes at a small fraction of its fp32 rate).
-struct ff {
-    float hi, lo;
-};
-__device__ __forceinline__ ff two_sum(float a, float b) {
-    const float s = a + b;
-    const float bb = s - a;
-    return {s, (a - (s - bb)) + (b - bb)};
-}
-__device__ __forceinline__ ff fast_two_sum(float a, float b) {  // |a| >= |b|
-    const float s = a + b;
-    return {s, b - (s - a)};
-}
-__device__ __forceinline__ ff two_prod(float a, float b) {
-    const float p = a * b;
-    return {p, fmaf(a, b, -p)};
-}
-__device__ __forceinline__ ff ff_add(ff a, ff b) {
-    ff s = two_sum(a.hi, b.hi);
-    const ff t = two_sum(a.lo, b.lo);
-    s.lo += t.hi;
-    s = fast_two_sum(s.hi, s.lo);
-    s.lo += t.lo;
-    return fast_two_sum(s.hi, s.lo);
-}
-__device__ __forceinline__ ff ff_neg(ff a) { return {-a.hi, -a.lo}; }
-__device__ __forceinline__ ff ff_mul(ff a, ff b) {
-    ff p = two_prod(a.hi, b.hi);
-    p.lo += a.hi * b.lo + a.lo * b.hi;
-    return fast_two_sum(p.hi, p.lo);
-}
-__device__ __forceinline__ ff ff_mul_f(ff a, float b) {
-    ff p = two_prod(a.hi, b);
-    p.lo += a.lo * b;
-    return fast_two_sum(p.hi, p.lo);
-}
-// Round hi + lo to bf16, nearest-even: hi is the float nearest to the exact
-// sum, so the two differ in bf16 only when hi sits exactly on a bf16
-// midpoint, where the sign of lo decides.
-__device__ __forceinline__ __nv_bfloat16 ff_to_bf16(ff y) {
-    const uint32_t u = __float_as_uint(y.hi);
-    if ((u & 0xFFFFu) == 0x8000u && y.lo != 0.0f) {
-        const uint32_t toward_zero = u & 0xFFFF0000u;
-        const bool away = (y.lo > 0.0f) == (y.hi > 0.0f);
-        return __ushort_as_bfloat16(
-            static_cast<unsigned short>((away ? toward_zero + 0x10000u : toward_zero) >> 16));
-    }
-    return __float2bfloat16_rn(y.hi);
-}
-
 // ------------------------------------------------------------ RoPE angles --
 // Angle i of position pos is pos * theta^(-2i/D), formed in double (the
 // frequency comes in as a double).  precise: cos/sin from double sincos,
@@ -402,38 +349,6 @@ __device__ void walk_next(Walk &w, const int *pre, int Hkv, int cnt) {
     }
 }
 
-// ------------------------------------------------------------ row math --
-// The new key row (sequence b, KV head g) on one warp, lane l holding dims
-// 2l, 2l+1, 64+2l, 65+2l: RMSNorm and RoPE in float-float arithmetic, then
-// one rounding to bf16.  x*w is exact in fp32 (two bf16 values), so is x^2.
-__device__ void key_row(const Params &p, __nv_bfloat162 ka, __nv_bfloat162 kc, __nv_bfloat162 wa,
-                        __nv_bfloat162 wc, const RopeEntry &e0, const RopeEntry &e1,
-                        __nv_bfloat16 (&kb)[4]) {
-    const float x[4] = {__low2float(ka), __high2float(ka), __low2float(kc), __high2float(kc)};
-    const float wv[4] = {__low2float(wa), __high2float(wa), __low2float(wc), __high2float(wc)};
-    ff ss = {x[0] * x[0], 0.f};
-#pragma unroll
-    for (int e = 1; e < 4; ++e) ss = ff_add(ss, ff{x[e] * x[e], 0.f});
-#pragma unroll
-    for (int o = 16; o; o >>= 1)
-        ss = ff_add(ss, ff{__shfl_xor_sync(kFull, ss.hi, o), __shfl_xor_sync(kFull, ss.lo, o)});
-    const ff v = ff_add(ff{ss.hi * (1.0f / kHeadDim), ss.lo * (1.0f / kHeadDim)}, ff{p.eps, 0.f});
-    // r = 1/sqrt(v): one Newton step from rsqrtf in float-float
-    const float r0 = rsqrtf(v.hi);
-    const ff t = ff_mul(v, two_prod(r0, r0));          // v * r0^2, close to 1
-    const float h = (1.0f - t.hi) - t.lo;              // 1 - t.hi is exact there
-    const ff r = fast_two_sum(r0, 0.5f * r0 * h);
-    ff xh[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) xh[e] = ff_mul_f(r, x[e] * wv[e]);
-    const ff c0 = {e0.c_hi, e0.c_lo}, s0 = {e0.s_hi, e0.s_lo};
-    const ff c1 = {e1.c_hi, e1.c_lo}, s1 = {e1.s_hi, e1.s_lo};
-    kb[0] = ff_to_bf16(ff_add(ff_mul(xh[0], c0), ff_neg(ff_mul(xh[2], s0))));
-    kb[2] = ff_to_bf16(ff_add(ff_mul(xh[2], c0), ff_mul(xh[0], s0)));
-    kb[1] = ff_to_bf16(ff_add(ff_mul(xh[1], c1), ff_neg(ff_mul(xh[3], s1))));
-    kb[3] = ff_to_bf16(ff_add(ff_mul(xh[3], c1), ff_mul(xh[1], s1)));
-}
-
 // The new key/value row of (sequence b, KV head g), on one warp: lane l holds
 // dims 2l, 2l+1, 64+2l, 65+2l.  bf16(k_rot) (float-float norm and rotation,
 // one rounding) and v go to kv_new in shared memory and to the pool slot of
@@ -485,7 +400,7 @@ __device__ void key_value_row(const Params &p, int b, int g, int L, uint8_t *sm,
         sv = __ldg(p.kv_scale + si + p.Hkv);
     }
     __nv_bfloat16 kb[4];
-    key_row(p, in.ka, in.kc, in.wka, in.wkc, in.e0, in.e1, kb);
+    key_row(p.eps, in.ka, in.kc, in.wka, in.wkc, in.e0, in.e1, kb);
     if constexpr (kFp8) {
         const int slot = L - 1;
         const __nv_bfloat162 va = *reinterpret_cast<const __nv_bfloat162 *>(&in.va);

@@ -30,6 +30,8 @@
 // the K scale and folds the V scale into the weights of the value product.
 #include "qdec_internal.h"
 #include "qdec_ptx.cuh"
+#include "qdec_ff.cuh"
+#include "qdec_tc.cuh"
 #include "qdec.h"
 
 #include <cuda_fp16.h>
@@ -110,26 +112,10 @@ __device__ __forceinline__ bool chunk_ok(const Params &p, int b, int &n, int &L)
 // One CTA per chunk row, 256 threads: the 64 angles of the row's position are
 // taken once (double sincos) into shared memory; warp w then handles KV head
 // w (and w + 8, ...): its four query rows in fp32 (q_rot's tolerance is
-// absolute), its key row in double from the sum of squares on (about 1e-16
-// relative error, so rounding it once to bf16 gives the nearest-even bf16 of
-// the exact value: a key near zero keeps its relative accuracy too), and the
+// absolute), its key row in float-float arithmetic rounded once to bf16 (the
+// decode append's rule: the nearest-even bf16 of the exact value), and the
 // copy of its value row.
 constexpr int kPfAppendThreads = 256;
-
-// bf16 nearest-even of a double, rounded once: truncation to binary32 with
-// the inexactness kept in the last bit (round-to-odd, 24 bits), then
-// nearest-even to bf16's 8 bits.  Rounding to odd with at least two more bits
-// than the target never changes the final nearest-even result (Boldo and
-// Melquiond, "When double rounding is odd", 2005).
-__device__ __forceinline__ float round_to_odd_float(double d) {
-    const float f = __double2float_rz(d);
-    return static_cast<double>(f) == d ? f : __uint_as_float(__float_as_uint(f) | 1u);
-}
-__device__ __forceinline__ uint32_t pack_bf16x2_of_doubles(double lo, double hi) {
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(round_to_odd_float(lo)))) |
-           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(round_to_odd_float(hi))))
-            << 16);
-}
 
 // E4M3 codes of a / s and b / s (fp32 division, one rounding each, then
 // nearest-even with saturation to +-448), a in the low byte.
@@ -196,23 +182,21 @@ __global__ void __launch_bounds__(kPfAppendThreads) prefill_append_kernel(
         }
         const int64_t slot =
             ((static_cast<int64_t>(page) * 2 * p.Hkv + g) * kPageSize + t % kPageSize) * kHeadDim;
-        // the key: sum of squares, root and rotation in double (x^2 and x w
-        // are exact in fp32), one rounding to bf16
+        // the key: norm and rotation in float-float, one rounding to bf16
         const __nv_bfloat16 *krow = p.k + static_cast<int64_t>(r) * p.k_stride + g * kHeadDim;
-        const float2 ka = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(krow)[lane]);
-        const float2 kc =
-            __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(krow + 64)[lane]);
-        const float2 wka = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(p.w_k)[lane]);
-        const float2 wkc =
-            __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(p.w_k + 64)[lane]);
-        double kss = (static_cast<double>(ka.x * ka.x) + static_cast<double>(ka.y * ka.y)) +
-                     (static_cast<double>(kc.x * kc.x) + static_cast<double>(kc.y * kc.y));
-#pragma unroll
-        for (int o = 16; o; o >>= 1) kss += __shfl_xor_sync(kFull, kss, o);
-        const double rn = 1.0 / sqrt(kss / kHeadDim + static_cast<double>(p.eps));
-        const double n0 = ka.x * wka.x, n1 = ka.y * wka.y, n2 = kc.x * wkc.x, n3 = kc.y * wkc.y;
-        const uint32_t k01 = pack_bf16x2_of_doubles(rn * (n0 * c0 - n2 * s0), rn * (n1 * c1 - n3 * s1));
-        const uint32_t k23 = pack_bf16x2_of_doubles(rn * (n2 * c0 + n0 * s0), rn * (n3 * c1 + n1 * s1));
+        const RopeEntry e0 = {fc0, static_cast<float>(c0 - static_cast<double>(fc0)), fs0,
+                              static_cast<float>(s0 - static_cast<double>(fs0))};
+        const RopeEntry e1 = {fc1, static_cast<float>(c1 - static_cast<double>(fc1)), fs1,
+                              static_cast<float>(s1 - static_cast<double>(fs1))};
+        __nv_bfloat16 kb[4];
+        key_row(p.eps, reinterpret_cast<const __nv_bfloat162 *>(krow)[lane],
+                reinterpret_cast<const __nv_bfloat162 *>(krow + 64)[lane],
+                reinterpret_cast<const __nv_bfloat162 *>(p.w_k)[lane],
+                reinterpret_cast<const __nv_bfloat162 *>(p.w_k + 64)[lane], e0, e1, kb);
+        const uint32_t k01 = static_cast<uint32_t>(__bfloat16_as_ushort(kb[0])) |
+                             (static_cast<uint32_t>(__bfloat16_as_ushort(kb[1])) << 16);
+        const uint32_t k23 = static_cast<uint32_t>(__bfloat16_as_ushort(kb[2])) |
+                             (static_cast<uint32_t>(__bfloat16_as_ushort(kb[3])) << 16);
         const uint32_t *vs = reinterpret_cast<const uint32_t *>(
             p.v + static_cast<int64_t>(r) * p.v_stride + g * kHeadDim);
         const uint32_t v01 = vs[lane], v23 = vs[32 + lane];
@@ -684,8 +668,489 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
+// ------------------------------------- attention on the 5th-gen tensor core --
+// prefill_attention_tc_kernel: the same causal paged attention (bf16 pool)
+// with both products on the tensor core (tcgen05, accumulators in tensor
+// memory).  One CTA per (sequence, KV head, block of 32 chunk tokens), the
+// blocks with the most keys first.  The M = 128 rows of the tile are the 4
+// query heads of the group x the block's 32 tokens (row 32 j + i: head
+// 4 g + j, token i), so each K/V stage in shared memory serves the group.
+// Per stage the producer warp brings 64 keys (4 pages) as four 8 KiB regions
+// [K dims 0-63][K dims 64-127][V dims 0-63][V dims 64-127], each [64 keys]
+// [128 bytes], 128-byte swizzled (one 2 KiB TMA box per page and region), so
+// that, from one issuing thread (warp 5),
+//   S = Q K^T  (M 128, N 64, K 128 in steps of 16; Q and K both K-major;
+//               q enters as bf16 hi + lo, i.e. 16 MMAs, keeping ~16 bits),
+//   O += P V   (M 128, N 128, K 64: 4 MMAs; P K-major from shared memory, V
+//               read in place as an MN-major operand).
+// S is double-buffered in tensor memory, so the scores of stage j + 1 are
+// formed while the four softmax warps (thread r owns row r, its tensor-
+// memory lane) work on stage j: load the 64 scores, mask keys past each
+// row's token, keep a stale running maximum (O in tensor memory is rescaled
+// only when a stage's maximum exceeds it by more than 2^8, so the weights
+// stay below 256), and write P as bf16 into one of two shared buffers.  V
+// rows of keys past the sequence (or of pages not brought) are zeroed
+// before the value product reads them.  The epilogue reads O out of tensor
+// memory, divides by the row sum and stores the row.  Every wait is
+// bounded; the decisions that lead to warp-collective tensor-memory loads
+// and stores are made warp-uniform.
+constexpr int kTcTok = 32;                                 // chunk tokens per CTA
+constexpr int kTcRows = kTcTok * kGroup;                   // M = 128
+constexpr int kTcKeys = 64;                                // keys per stage
+constexpr int kTcPagesPerStage = kTcKeys / kPageSize;      // 4
+constexpr int kTcStages = 3;
+constexpr int kTcRegion = kTcKeys * 128;                   // [64 keys][64 dims] bf16, 8 KiB
+constexpr int kTcStageBytes = 4 * kTcRegion;               // K lo, K hi, V lo, V hi halves of D
+constexpr int kTcQHalf = kTcRows * 128;                    // [128 rows][64 dims] bf16, 16 KiB
+constexpr int kTcQBytes = 2 * kTcQHalf;
+constexpr int kTcPBytes = kTcRows * 128;                   // [128 rows][64 keys] bf16, 16 KiB
+constexpr int kTcOffQhi = 0;
+constexpr int kTcOffQlo = kTcOffQhi + kTcQBytes;
+constexpr int kTcOffP = kTcOffQlo + kTcQBytes;
+constexpr int kTcOffRing = kTcOffP + 2 * kTcPBytes;
+constexpr int kTcOffTail = kTcOffRing + kTcStages * kTcStageBytes;
+// tail: barriers kv_full[S], kv_empty[S], s_full[2], s_free[2], p_full[2],
+// o_done[2], q_ready, done; then ints: abort, sequence, block, tiles issued,
+// tensor-memory address, and the mask of pages brought into every stage
+constexpr int kTcBars = 2 * kTcStages + 2 + 2 + 2 + 2 + 1 + 1;
+constexpr int kTcTailBytes = kTcBars * 8 + (5 + kTcStages) * 4;
+constexpr int kTcSmemBytes = kTcOffTail + kTcTailBytes + 1024;
+constexpr int kTcWarps = 6;                                // 4 softmax, producer, MMA
+constexpr int kTcThreads = kTcWarps * 32;
+constexpr uint32_t kTcTmemCols = 256;                      // S0 [0,64), S1 [64,128), O [128,256)
+static_assert(kTcSmemBytes <= 227 * 1024, "one CTA per SM");
+static_assert(kTcOffRing % 1024 == 0 && kTcOffP % 1024 == 0 && kTcOffQlo % 1024 == 0,
+              "swizzled operands start on 1024-byte boundaries");
+
+// One (page, plane, half of D) region of a page: 16 tokens x 64 dims, 2 KiB,
+// with the pool's region map (5-D: 64 dims, token, half, plane, page*2*Hkv +
+// head; box 64 x 16 x 1 x 1 x 1).
+__device__ __forceinline__ void tma_load_region(uint32_t dst, const CUtensorMap *map, int half,
+                                                int plane, int row, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(half), "r"(plane), "r"(row), "r"(bar)
+        : "memory");
+}
+
+// Offset of 16-byte chunk c of row r in a [rows][128 bytes] 128-byte
+// swizzled block starting on a 1024-byte boundary.
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
+    return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_attention_tc_kernel(const __grid_constant__ CUtensorMap region_map,
+                                const __grid_constant__ Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint8_t *tail = sm + kTcOffTail;
+    const uint32_t kv_full0 = smem_u32(tail);
+    const uint32_t kv_empty0 = kv_full0 + 8 * kTcStages;
+    const uint32_t s_full0 = kv_empty0 + 8 * kTcStages;
+    const uint32_t s_free0 = s_full0 + 16;
+    const uint32_t p_full0 = s_free0 + 16;
+    const uint32_t o_done0 = p_full0 + 16;
+    const uint32_t q_ready = o_done0 + 16;
+    const uint32_t done_bar = q_ready + 8;
+    // misc: [0] abort, [1] sequence, [2] query block, [3] tiles issued,
+    // [4] tensor-memory address; pmask[s]: pages brought into stage s
+    volatile int *misc = reinterpret_cast<volatile int *>(tail + kTcBars * 8);
+    volatile int *pmask = misc + 5;
+    const int g = blockIdx.x % p.Hkv;
+    const int unit = blockIdx.x / p.Hkv;
+
+    // ---- which (sequence, block) this CTA takes: units enumerate every
+    // sequence's blocks from its last (most keys) to its first
+    if (warp == 0) {
+        const int per = (p.B + 31) / 32;
+        int cnt = 0;
+        for (int i = 0; i < per; ++i) {
+            const int b = lane * per + i;
+            int n, L;
+            if (b < p.B && chunk_ok(p, b, n, L)) cnt += (n + kTcTok - 1) / kTcTok;
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const int excl = incl - cnt;
+        if (lane == 0) misc[1] = -1;
+        __syncwarp();
+        if (unit >= excl && unit < incl) {
+            int k = unit - excl;
+            for (int i = 0; i < per; ++i) {
+                const int b = lane * per + i;
+                int n, L;
+                if (b >= p.B || !chunk_ok(p, b, n, L)) continue;
+                const int nb = (n + kTcTok - 1) / kTcTok;
+                if (k < nb) {
+                    misc[1] = b;
+                    misc[2] = nb - 1 - k;
+                    break;
+                }
+                k -= nb;
+            }
+        }
+        if (blockIdx.x == 0) {  // report malformed chunks once
+            for (int b = lane; b < p.B; b += 32) {
+                int n, L;
+                if (!chunk_ok(p, b, n, L)) flag_error(p.err, QDEC_FLAG_BAD_SEQLEN);
+            }
+        }
+        if (lane == 0) {
+            for (int s = 0; s < kTcStages; ++s) {
+                mbar_init(kv_full0 + 8 * s, 1);   // the producer's arrival + the bytes
+                mbar_init(kv_empty0 + 8 * s, 1);  // the commit of the stage's value product
+            }
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(s_full0 + 8 * i, 1);    // commit of the score product
+                mbar_init(s_free0 + 8 * i, 4);    // every softmax warp has read the scores
+                mbar_init(p_full0 + 8 * i, 4);    // every softmax warp has written its P rows
+                mbar_init(o_done0 + 8 * i, 1);    // commit of the value product
+            }
+            mbar_init(q_ready, 4);
+            mbar_init(done_bar, 1);
+            misc[0] = 0;
+            misc[3] = 0;
+            fence_mbar_init();
+        }
+    }
+    if (warp == 5) tc::alloc(smem_u32(const_cast<int *>(misc + 4)), kTcTmemCols);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = static_cast<uint32_t>(misc[4]);
+    const int b = misc[1];
+    if (b < 0) {  // no unit for this CTA (the grid is an upper bound)
+        if (warp == 5) tc::dealloc(tmem, kTcTmemCols);
+        return;
+    }
+    const int qb = misc[2];
+    int n, L;
+    chunk_ok(p, b, n, L);
+    const int row0 = p.qo_indptr[b] + qb * kTcTok;       // first packed row
+    const int nrows = min(kTcTok, n - qb * kTcTok);      // rows of this block
+    const int t0 = L - n + qb * kTcTok;                  // token index of row 0
+    const int ntiles = (t0 + nrows - 1) / kTcKeys + 1;   // stages up to the last query
+    const int npg = (L + kPageSize - 1) / kPageSize;     // pages of the sequence
+
+    if (warp == 4) {
+        // ------------------------------------------------ TMA producer --
+        // lanes 0-3 each bring one page of the stage (its four regions)
+        int issued = 0;
+        for (int j = 0; j < ntiles; ++j) {
+            const int s = j % kTcStages;
+            bool stop = false;
+            if (lane == 0) {
+                if (misc[0]) {
+                    stop = true;
+                } else if (j >= kTcStages &&
+                           !mbar_wait_bounded(kv_empty0 + 8 * s, ((j / kTcStages) - 1) & 1, misc,
+                                              p.wait_cycles)) {
+                    misc[0] = 1;
+                    flag_error(p.err, QDEC_FLAG_TIMEOUT);
+                    stop = true;
+                }
+            }
+            if (__shfl_sync(kFull, stop, 0)) break;
+            const int pg = j * kTcPagesPerStage + lane;
+            int page = -1;
+            if (lane < kTcPagesPerStage && pg < npg)
+                page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg];
+            const bool ok = lane < kTcPagesPerStage && pg < npg && page >= 0 && page < p.num_pages;
+            if (lane < kTcPagesPerStage && pg < npg && !ok) flag_error(p.err, QDEC_FLAG_BAD_PAGE);
+            const unsigned mask = __ballot_sync(kFull, ok) & 0xFu;
+            const bool withheld = p.withhold_first && j == 0;  // test hook: never lands
+            if (lane == 0) {
+                pmask[s] = static_cast<int>(mask);
+                if (!withheld) {
+                    if (mask == 0)
+                        mbar_arrive(kv_full0 + 8 * s);
+                    else
+                        mbar_arrive_expect_tx(kv_full0 + 8 * s,
+                                              __popc(mask) * 4 * (kPageSize * 128));
+                }
+            }
+            __syncwarp();
+            if (ok && !withheld) {
+                const uint32_t dst = smem_u32(sm + kTcOffRing + s * kTcStageBytes) +
+                                     lane * (kPageSize * 128);
+                const int row = page * 2 * p.Hkv + g;
+#pragma unroll
+                for (int r = 0; r < 4; ++r)  // region r: plane r / 2, half r % 2
+                    tma_load_region(dst + r * kTcRegion, &region_map, r & 1, r >> 1, row,
+                                    kv_full0 + 8 * s);
+            }
+            issued = j + 1;
+        }
+        if (lane == 0) misc[3] = issued;
+    } else if (warp == 5) {
+        // --------------------------------------------- the MMA issuer --
+        if (lane == 0) {
+            const uint32_t qhi = smem_u32(sm + kTcOffQhi), qlo = smem_u32(sm + kTcOffQlo);
+            const uint32_t pbuf = smem_u32(sm + kTcOffP);
+            const uint32_t ring = smem_u32(sm + kTcOffRing);
+            constexpr uint32_t kIdS = tc::idesc_bf16(kTcRows, kTcKeys, false);
+            constexpr uint32_t kIdO = tc::idesc_bf16(kTcRows, kHeadDim, true);
+            const uint32_t tO = tmem + 128;
+            // O += P_t V_t once the softmax warps have written P_t; the
+            // commits free the P buffer (o_done) and the stage (kv_empty)
+            auto value_product = [&](int t) -> bool {
+                if (!mbar_wait_bounded(p_full0 + 8 * (t & 1), (t >> 1) & 1, misc, p.wait_cycles))
+                    return false;
+                tc::fence_after();
+                const uint32_t vst = ring + (t % kTcStages) * kTcStageBytes + 2 * kTcRegion;
+#pragma unroll
+                for (int kk = 0; kk < kTcKeys / 16; ++kk)
+                    tc::mma(tO, tc::desc_sw128(pbuf + (t & 1) * kTcPBytes + 32 * kk, 16, 1024),
+                            tc::desc_sw128(vst + kk * 2048, kTcRegion, 1024), kIdO, t > 0 || kk > 0);
+                tc::commit(o_done0 + 8 * (t & 1));
+                tc::commit(kv_empty0 + 8 * (t % kTcStages));
+                return true;
+            };
+            bool ok = mbar_wait_bounded(q_ready, 0, misc, p.wait_cycles);
+            for (int j = 0; ok && j < ntiles; ++j) {
+                const int s = j % kTcStages;
+                if (!mbar_wait_bounded(kv_full0 + 8 * s, (j / kTcStages) & 1, misc, p.wait_cycles) ||
+                    (j >= 2 && !mbar_wait_bounded(s_free0 + 8 * (j & 1), ((j - 2) >> 1) & 1, misc,
+                                                  p.wait_cycles))) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after();
+                const uint32_t kst = ring + s * kTcStageBytes;
+                const uint32_t tS = tmem + (j & 1) * kTcKeys;
+#pragma unroll
+                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                    const uint32_t ko = (kk >> 2) * kTcRegion + 32 * (kk & 3);
+                    const uint32_t qo = (kk >> 2) * kTcQHalf + 32 * (kk & 3);
+                    const uint64_t kd = tc::desc_sw128(kst + ko, 16, 1024);
+                    tc::mma(tS, tc::desc_sw128(qhi + qo, 16, 1024), kd, kIdS, kk > 0);
+                    tc::mma(tS, tc::desc_sw128(qlo + qo, 16, 1024), kd, kIdS, true);
+                }
+                tc::commit(s_full0 + 8 * (j & 1));
+                if (j >= 1 && !value_product(j - 1)) ok = false;
+            }
+            if (ok && !value_product(ntiles - 1)) ok = false;
+            if (!ok) {
+                misc[0] = 1;
+                flag_error(p.err, QDEC_FLAG_TIMEOUT);
+            }
+            tc::commit(done_bar);  // every MMA issued above has completed
+        }
+        __syncwarp();
+    } else {
+        // --------------------------------------------- softmax warps --
+        const int r = tid;                        // row of the tile, tensor-memory lane
+        const int hj = r >> 5, ti = r & 31;       // head 4 g + hj, token t0 + ti
+        const bool live = ti < nrows;
+        // a wait every lane of the warp passes, or none: the tensor-memory
+        // loads and stores below are warp-collective
+        auto wait_all = [&](uint32_t bar, uint32_t parity) {
+            bool ok = mbar_wait_bounded(bar, parity, misc, p.wait_cycles);
+            ok = __all_sync(kFull, ok);
+            if (!ok && lane == 0) {
+                misc[0] = 1;
+                flag_error(p.err, QDEC_FLAG_TIMEOUT);
+            }
+            return ok;
+        };
+        {
+            // Q, scaled to log2 units, as bf16 hi + lo: warp w converts rows
+            // w, w + 4, ..., lane l taking dims 4 l .. 4 l + 3 of each (one
+            // coalesced 512-byte row per warp load, all of them in flight)
+            uint8_t *qh = sm + kTcOffQhi, *ql = sm + kTcOffQlo;
+            const int half = lane >> 4, cc = (lane & 15) >> 1, sub = (lane & 1) * 8;
+            float4 x[kTcRows / 4];
+#pragma unroll
+            for (int k = 0; k < kTcRows / 4; ++k) {
+                const int rr = warp + 4 * k, tt = rr & 31;
+                x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (tt < nrows)
+                    x[k] = reinterpret_cast<const float4 *>(
+                        p.q_rot_in + (static_cast<int64_t>(row0 + tt) * p.Hq + g * kGroup + (rr >> 5)) *
+                                         kHeadDim)[lane];
+            }
+#pragma unroll
+            for (int k = 0; k < kTcRows / 4; ++k) {
+                const int rr = warp + 4 * k;
+                const float v[4] = {x[k].x * p.qscale, x[k].y * p.qscale, x[k].z * p.qscale,
+                                    x[k].w * p.qscale};
+                __nv_bfloat16 h[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) h[e] = __float2bfloat16_rn(v[e]);
+                const uint2 hi = make_uint2(
+                    static_cast<uint32_t>(__bfloat16_as_ushort(h[0])) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(h[1])) << 16),
+                    static_cast<uint32_t>(__bfloat16_as_ushort(h[2])) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(h[3])) << 16));
+                const uint2 lo = make_uint2(
+                    pack_bf16x2(v[0] - __bfloat162float(h[0]), v[1] - __bfloat162float(h[1])),
+                    pack_bf16x2(v[2] - __bfloat162float(h[2]), v[3] - __bfloat162float(h[3])));
+                const uint32_t off = half * kTcQHalf + sw128_off(rr, cc) + sub;
+                *reinterpret_cast<uint2 *>(qh + off) = hi;
+                *reinterpret_cast<uint2 *>(ql + off) = lo;
+            }
+            fence_proxy_async_smem();  // read next by the tensor core
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_ready);
+        }
+        const int lim = min(t0 + ti, L - 1);      // the last key this row sees
+        const uint32_t trow = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            const int s = j % kTcStages;
+            if (!wait_all(kv_full0 + 8 * s, (j / kTcStages) & 1) ||
+                !wait_all(s_full0 + 8 * (j & 1), (j >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after();
+            float sc[kTcKeys];
+            {
+                uint32_t v[32];
+                tc::ld32(v, trow + (j & 1) * kTcKeys);
+                tc::wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) sc[c] = __uint_as_float(v[c]);
+                tc::ld32(v, trow + (j & 1) * kTcKeys + 32);
+                tc::wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) sc[32 + c] = __uint_as_float(v[c]);
+            }
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free0 + 8 * (j & 1));
+            const int kb = j * kTcKeys;
+            if (kb + kTcKeys - 1 > lim) {
+#pragma unroll
+                for (int c = 0; c < kTcKeys; ++c)
+                    if (kb + c > lim) sc[c] = -INFINITY;
+            }
+            float mx = sc[0];
+#pragma unroll
+            for (int c = 1; c < kTcKeys; ++c) mx = fmaxf(mx, sc[c]);
+            const bool grow = mx > m + 8.f;
+            if (__any_sync(kFull, grow)) {
+                const float mn = grow ? fmaxf(m, mx) : m;
+                const float alpha = !grow ? 1.f : (m == -INFINITY ? 0.f : exp2f(m - mn));
+                l *= alpha;
+                m = mn;
+                if (j > 0) {
+                    // O holds stages 0 .. j-1 once their last product is done
+                    if (!wait_all(o_done0 + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+#pragma unroll 1
+                    for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+                        uint32_t o[32];
+                        tc::ld32(o, trow + 128 + c0);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tc::st32(trow + 128 + c0, o);
+                    }
+                    tc::wait_st();
+                    tc::fence_before();
+                }
+            }
+            // P buffer j & 1 is free once the value product of stage j - 2 is done
+            if (j >= 2 && !wait_all(o_done0 + 8 * (j & 1), ((j - 2) >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            uint8_t *pb = sm + kTcOffP + (j & 1) * kTcPBytes;
+            float psum = 0.f;
+#pragma unroll
+            for (int c = 0; c < kTcKeys / 8; ++c) {   // keys 8 c .. 8 c + 7
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = exp2f(sc[8 * c + 2 * e] - m);
+                    const float p1 = exp2f(sc[8 * c + 2 * e + 1] - m);
+                    psum += p0 + p1;
+                    w[e] = pack_bf16x2(p0, p1);
+                }
+                *reinterpret_cast<uint4 *>(pb + sw128_off(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            l += psum;
+            // V rows of keys past the sequence, or on pages not brought, are
+            // zeroed: the product would turn a non-finite one into NaN
+            const int pm = pmask[s];
+            if (kb + kTcKeys > L || pm != (1 << kTcPagesPerStage) - 1) {
+                uint8_t *vr = sm + kTcOffRing + s * kTcStageBytes + 2 * kTcRegion;
+                for (int e = r; e < kTcKeys * 16; e += kTcRows) {
+                    const int kr = e >> 4, c = e & 15;
+                    if (kb + kr >= L || !((pm >> (kr / kPageSize)) & 1))
+                        *reinterpret_cast<uint4 *>(vr + (c >> 3) * kTcRegion + kr * 128 +
+                                                   ((c & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async_smem();  // P and the zeroed rows are read by the tensor core
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full0 + 8 * (j & 1));
+        }
+        // ---- epilogue: O / l for this row, after every product has completed
+        volatile int never = 0;
+        bool fin = mbar_wait_bounded(done_bar, 0, &never, p.wait_cycles);
+        fin = __all_sync(kFull, fin);
+        ok = __all_sync(kFull, ok && !misc[0]);
+        tc::fence_after();
+        if (fin && ok) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16 *dst =
+                p.out + (static_cast<int64_t>(row0 + ti) * p.Hq + g * kGroup + hj) * kHeadDim;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
+                uint32_t o[32];
+                tc::ld32(o, trow + 128 + c0);
+                tc::wait_ld();
+                if (live) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(o[8 * q]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(dst + c0 + 8 * q) = w;
+                    }
+                }
+            }
+        } else if (!fin && lane == 0) {
+            misc[0] = 1;
+            flag_error(p.err, QDEC_FLAG_TIMEOUT);
+        }
+        tc::fence_before();
+    }
+    __syncthreads();
+    if (warp == 5) {
+        tc::fence_after();
+        tc::dealloc(tmem, kTcTmemCols);
+    }
+    // a wait that gave up may leave copies in flight: let them land (bounded)
+    if (tid == 4 * 32 && misc[0]) {
+        const int issued = misc[3];
+        volatile int never = 0;
+        for (int t = max(0, issued - kTcStages); t < issued; ++t)
+            mbar_wait_bounded(kv_full0 + 8 * (t % kTcStages), (t / kTcStages) & 1, &never,
+                              p.wait_cycles);
+    }
+}
+
 std::mutex g_pf_mu;
 bool g_pf_smem_set[2][64];
+bool g_pf_tc_smem_set[64];
 
 }  // namespace
 
@@ -714,6 +1179,28 @@ cudaError_t launch_attn(const Params &p, const CUtensorMap &kv_map, int dev, cud
     const int64_t units = (static_cast<int64_t>(p.T) + kPfRows - 1) / kPfRows + p.B;
     prefill_attention_kernel<kFp8>
         <<<static_cast<unsigned>(units * p.Hkv), kThreads, pf_smem_bytes<kFp8>(), s>>>(kv_map, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_attention_tc(const Params &p, const CUtensorMap &region_map,
+                                        cudaStream_t s) {
+    if (p.T <= 0) return cudaSuccess;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 63;
+    {
+        std::lock_guard<std::mutex> lock(g_pf_mu);
+        if (!g_pf_tc_smem_set[dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(
+                prefill_attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
+            if (e != cudaSuccess) return e;
+            g_pf_tc_smem_set[dev] = true;
+        }
+    }
+    // units: at most T / 32 + B blocks of 32 chunk rows, times the KV heads
+    const int64_t units = (static_cast<int64_t>(p.T) + kTcTok - 1) / kTcTok + p.B;
+    prefill_attention_tc_kernel<<<static_cast<unsigned>(units * p.Hkv), kTcThreads, kTcSmemBytes,
+                                  s>>>(region_map, p);
     return cudaGetLastError();
 }
 
