@@ -671,56 +671,62 @@ __global__ void __launch_bounds__(kThreads, 2)
 // ------------------------------------- attention on the 5th-gen tensor core --
 // prefill_attention_tc_kernel: the same causal paged attention (bf16 pool)
 // with both products on the tensor core (tcgen05, accumulators in tensor
-// memory).  One CTA per (sequence, KV head, block of 32 chunk tokens), the
-// blocks with the most keys first.  The M = 128 rows of the tile are the 4
-// query heads of the group x the block's 32 tokens (row 32 j + i: head
-// 4 g + j, token i), so each K/V stage in shared memory serves the group.
-// Per stage the producer warp brings 64 keys (4 pages) as four 8 KiB regions
-// [K dims 0-63][K dims 64-127][V dims 0-63][V dims 64-127], each [64 keys]
-// [128 bytes], 128-byte swizzled (one 2 KiB TMA box per page and region), so
-// that, from one issuing thread (warp 5),
-//   S = Q K^T  (M 128, N 64, K 128 in steps of 16; Q and K both K-major;
-//               q enters as bf16 hi + lo, i.e. 16 MMAs, keeping ~16 bits),
+// memory).  One CTA per (sequence, KV head, block of 64 chunk tokens), the
+// blocks with the most keys first.  The block is two tiles of M = 128 rows:
+// tile u holds tokens 32 u .. 32 u + 31 of the block for the 4 query heads
+// of the group (row 32 j + i: head 4 g + j, token 32 u + i), so each K/V
+// stage in shared memory serves 256 query rows.  Per stage the producer warp
+// brings 64 keys (4 pages) as four 8 KiB regions [K dims 0-63][K dims 64-127]
+// [V dims 0-63][V dims 64-127], each [64 keys][128 bytes], 128-byte swizzled
+// (one 2 KiB TMA box per page and region), so that, from one issuing thread
+// (warp 9), for each tile
+//   S = Q K^T  (M 128, N 64, K 128: 8 MMAs of K 16; Q and K both K-major;
+//               q enters as bf16),
 //   O += P V   (M 128, N 128, K 64: 4 MMAs; P K-major from shared memory, V
 //               read in place as an MN-major operand).
-// S is double-buffered in tensor memory, so the scores of stage j + 1 are
-// formed while the four softmax warps (thread r owns row r, its tensor-
-// memory lane) work on stage j: load the 64 scores, mask keys past each
-// row's token, keep a stale running maximum (O in tensor memory is rescaled
-// only when a stage's maximum exceeds it by more than 2^8, so the weights
-// stay below 256), and write P as bf16 into one of two shared buffers.  V
-// rows of keys past the sequence (or of pages not brought) are zeroed
-// before the value product reads them.  The epilogue reads O out of tensor
-// memory, divides by the row sum and stores the row.  Every wait is
-// bounded; the decisions that lead to warp-collective tensor-memory loads
-// and stores are made warp-uniform.
-constexpr int kTcTok = 32;                                 // chunk tokens per CTA
-constexpr int kTcRows = kTcTok * kGroup;                   // M = 128
+// S is double-buffered in tensor memory per tile, so the scores of stage
+// j + 1 are formed while the softmax warps (warps 4 u .. 4 u + 3 for tile u,
+// thread r of the group owning row r, its tensor-memory lane) work on stage
+// j: load the 64 scores, mask keys past each row's token, keep a stale
+// running maximum (O in tensor memory is rescaled only when a stage's
+// maximum exceeds it by more than 2^8, so the weights stay below 256), and
+// write P as bf16 into one of two shared buffers of the tile.  V rows of
+// keys past the sequence (or of pages not brought) are zeroed before a value
+// product reads them.  The epilogue reads O out of tensor memory, divides by
+// the row sum and stores the row.  Every wait is bounded; the decisions that
+// lead to warp-collective tensor-memory loads and stores are warp-uniform.
+constexpr int kTcTiles = 2;                                // query tiles per CTA
+constexpr int kTcTileTok = 32;                             // chunk tokens per tile
+constexpr int kTcTok = kTcTiles * kTcTileTok;              // chunk tokens per CTA
+constexpr int kTcRows = kTcTileTok * kGroup;               // M = 128 rows per tile
 constexpr int kTcKeys = 64;                                // keys per stage
 constexpr int kTcPagesPerStage = kTcKeys / kPageSize;      // 4
 constexpr int kTcStages = 3;
 constexpr int kTcRegion = kTcKeys * 128;                   // [64 keys][64 dims] bf16, 8 KiB
 constexpr int kTcStageBytes = 4 * kTcRegion;               // K lo, K hi, V lo, V hi halves of D
 constexpr int kTcQHalf = kTcRows * 128;                    // [128 rows][64 dims] bf16, 16 KiB
-constexpr int kTcQBytes = 2 * kTcQHalf;
+constexpr int kTcQBytes = 2 * kTcQHalf;                    // one tile's Q
 constexpr int kTcPBytes = kTcRows * 128;                   // [128 rows][64 keys] bf16, 16 KiB
-constexpr int kTcOffQhi = 0;
-constexpr int kTcOffQlo = kTcOffQhi + kTcQBytes;
-constexpr int kTcOffP = kTcOffQlo + kTcQBytes;
-constexpr int kTcOffRing = kTcOffP + 2 * kTcPBytes;
+constexpr int kTcOffQ = 0;                                 // Q of tile u at u * kTcQBytes
+constexpr int kTcOffP = kTcOffQ + kTcTiles * kTcQBytes;    // P of tile u, buffer q: (2u + q)
+constexpr int kTcOffRing = kTcOffP + 2 * kTcTiles * kTcPBytes;
 constexpr int kTcOffTail = kTcOffRing + kTcStages * kTcStageBytes;
-// tail: barriers kv_full[S], kv_empty[S], s_full[2], s_free[2], p_full[2],
-// o_done[2], q_ready, done; then ints: abort, sequence, block, tiles issued,
-// tensor-memory address, and the mask of pages brought into every stage
-constexpr int kTcBars = 2 * kTcStages + 2 + 2 + 2 + 2 + 1 + 1;
+// tail: barriers kv_full[S], kv_empty[S]; per tile s_full[2], s_free[2],
+// p_full[2], o_done[2]; q_ready, done; then ints: abort, sequence, block,
+// stages issued, tensor-memory address, and the mask of pages brought into
+// every stage
+constexpr int kTcBars = 2 * kTcStages + kTcTiles * 8 + 2;
 constexpr int kTcTailBytes = kTcBars * 8 + (5 + kTcStages) * 4;
 constexpr int kTcSmemBytes = kTcOffTail + kTcTailBytes + 1024;
-constexpr int kTcWarps = 6;                                // 4 softmax, producer, MMA
-constexpr int kTcThreads = kTcWarps * 32;
-constexpr uint32_t kTcTmemCols = 256;                      // S0 [0,64), S1 [64,128), O [128,256)
+constexpr int kTcSoftmaxWarps = 4 * kTcTiles;
+constexpr int kTcProducerWarp = kTcSoftmaxWarps;
+constexpr int kTcMmaWarp = kTcSoftmaxWarps + 1;
+constexpr int kTcThreads = (kTcSoftmaxWarps + 2) * 32;
+// tile u: S buffers at columns 256 u + {0, 64}, O at 256 u + 128
+constexpr uint32_t kTcTmemCols = 256 * kTcTiles;
 static_assert(kTcSmemBytes <= 227 * 1024, "one CTA per SM");
-static_assert(kTcOffRing % 1024 == 0 && kTcOffP % 1024 == 0 && kTcOffQlo % 1024 == 0,
-              "swizzled operands start on 1024-byte boundaries");
+static_assert(kTcOffRing % 1024 == 0 && kTcOffP % 1024 == 0, "swizzled operands start on 1024-byte boundaries");
+static_assert(kTcTmemCols <= 512, "tensor memory");
 
 // One (page, plane, half of D) region of a page: 16 tokens x 64 dims, 2 KiB,
 // with the pool's region map (5-D: 64 dims, token, half, plane, page*2*Hkv +
@@ -732,6 +738,15 @@ __device__ __forceinline__ void tma_load_region(uint32_t dst, const CUtensorMap 
         " [%0], [%1, {%2, %2, %3, %4, %5}], [%6];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(half), "r"(plane), "r"(row), "r"(bar)
         : "memory");
+}
+
+// 2^x by the hardware's approximation (one instruction; relative error
+// about 2^-22, far below the bf16 rounding of the weights it feeds;
+// 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // Offset of 16-byte chunk c of row r in a [rows][128 bytes] 128-byte
@@ -750,13 +765,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t *tail = sm + kTcOffTail;
     const uint32_t kv_full0 = smem_u32(tail);
     const uint32_t kv_empty0 = kv_full0 + 8 * kTcStages;
-    const uint32_t s_full0 = kv_empty0 + 8 * kTcStages;
-    const uint32_t s_free0 = s_full0 + 16;
-    const uint32_t p_full0 = s_free0 + 16;
-    const uint32_t o_done0 = p_full0 + 16;
-    const uint32_t q_ready = o_done0 + 16;
+    // per tile u: s_full, s_free, p_full, o_done, two of each (buffer q)
+    const uint32_t tile_bar0 = kv_empty0 + 8 * kTcStages;
+    auto s_full = [&](int u, int q) { return tile_bar0 + 64 * u + 8 * q; };
+    auto s_free = [&](int u, int q) { return tile_bar0 + 64 * u + 16 + 8 * q; };
+    auto p_full = [&](int u, int q) { return tile_bar0 + 64 * u + 32 + 8 * q; };
+    auto o_done = [&](int u, int q) { return tile_bar0 + 64 * u + 48 + 8 * q; };
+    const uint32_t q_ready = tile_bar0 + 64 * kTcTiles;
     const uint32_t done_bar = q_ready + 8;
-    // misc: [0] abort, [1] sequence, [2] query block, [3] tiles issued,
+    // misc: [0] abort, [1] sequence, [2] query block, [3] stages issued,
     // [4] tensor-memory address; pmask[s]: pages brought into stage s
     volatile int *misc = reinterpret_cast<volatile int *>(tail + kTcBars * 8);
     volatile int *pmask = misc + 5;
@@ -806,29 +823,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             for (int s = 0; s < kTcStages; ++s) {
                 mbar_init(kv_full0 + 8 * s, 1);   // the producer's arrival + the bytes
-                mbar_init(kv_empty0 + 8 * s, 1);  // the commit of the stage's value product
+                mbar_init(kv_empty0 + 8 * s, 1);  // the commit of the stage's value products
             }
-            for (int i = 0; i < 2; ++i) {
-                mbar_init(s_full0 + 8 * i, 1);    // commit of the score product
-                mbar_init(s_free0 + 8 * i, 4);    // every softmax warp has read the scores
-                mbar_init(p_full0 + 8 * i, 4);    // every softmax warp has written its P rows
-                mbar_init(o_done0 + 8 * i, 1);    // commit of the value product
+            for (int u = 0; u < kTcTiles; ++u) {
+                for (int q = 0; q < 2; ++q) {
+                    mbar_init(s_full(u, q), 1);   // commit of the score product
+                    mbar_init(s_free(u, q), 4);   // the tile's softmax warps have read the scores
+                    mbar_init(p_full(u, q), 4);   // the tile's softmax warps have written P
+                    mbar_init(o_done(u, q), 1);   // commit of the value product
+                }
             }
-            mbar_init(q_ready, 4);
+            mbar_init(q_ready, kTcSoftmaxWarps);
             mbar_init(done_bar, 1);
             misc[0] = 0;
             misc[3] = 0;
             fence_mbar_init();
         }
     }
-    if (warp == 5) tc::alloc(smem_u32(const_cast<int *>(misc + 4)), kTcTmemCols);
+    if (warp == kTcMmaWarp) tc::alloc(smem_u32(const_cast<int *>(misc + 4)), kTcTmemCols);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = static_cast<uint32_t>(misc[4]);
     const int b = misc[1];
     if (b < 0) {  // no unit for this CTA (the grid is an upper bound)
-        if (warp == 5) tc::dealloc(tmem, kTcTmemCols);
+        if (warp == kTcMmaWarp) tc::dealloc(tmem, kTcTmemCols);
         return;
     }
     const int qb = misc[2];
@@ -840,7 +859,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int ntiles = (t0 + nrows - 1) / kTcKeys + 1;   // stages up to the last query
     const int npg = (L + kPageSize - 1) / kPageSize;     // pages of the sequence
 
-    if (warp == 4) {
+    if (warp == kTcProducerWarp) {
         // ------------------------------------------------ TMA producer --
         // lanes 0-3 each bring one page of the stage (its four regions)
         int issued = 0;
@@ -890,54 +909,63 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             issued = j + 1;
         }
         if (lane == 0) misc[3] = issued;
-    } else if (warp == 5) {
+    } else if (warp == kTcMmaWarp) {
         // --------------------------------------------- the MMA issuer --
         if (lane == 0) {
-            const uint32_t qhi = smem_u32(sm + kTcOffQhi), qlo = smem_u32(sm + kTcOffQlo);
-            const uint32_t pbuf = smem_u32(sm + kTcOffP);
+            const uint32_t qbase = smem_u32(sm + kTcOffQ);
+            const uint32_t pbase = smem_u32(sm + kTcOffP);
             const uint32_t ring = smem_u32(sm + kTcOffRing);
             constexpr uint32_t kIdS = tc::idesc_bf16(kTcRows, kTcKeys, false);
             constexpr uint32_t kIdO = tc::idesc_bf16(kTcRows, kHeadDim, true);
-            const uint32_t tO = tmem + 128;
-            // O += P_t V_t once the softmax warps have written P_t; the
-            // commits free the P buffer (o_done) and the stage (kv_empty)
-            auto value_product = [&](int t) -> bool {
-                if (!mbar_wait_bounded(p_full0 + 8 * (t & 1), (t >> 1) & 1, misc, p.wait_cycles))
-                    return false;
-                tc::fence_after();
+            // O_u += P_u,t V_t for both tiles once their softmax warps have
+            // written P; the commits free the P buffers (o_done) and the
+            // stage (kv_empty)
+            auto value_products = [&](int t) -> bool {
                 const uint32_t vst = ring + (t % kTcStages) * kTcStageBytes + 2 * kTcRegion;
+                for (int u = 0; u < kTcTiles; ++u) {
+                    if (!mbar_wait_bounded(p_full(u, t & 1), (t >> 1) & 1, misc, p.wait_cycles))
+                        return false;
+                    tc::fence_after();
+                    const uint32_t pb = pbase + (2 * u + (t & 1)) * kTcPBytes;
 #pragma unroll
-                for (int kk = 0; kk < kTcKeys / 16; ++kk)
-                    tc::mma(tO, tc::desc_sw128(pbuf + (t & 1) * kTcPBytes + 32 * kk, 16, 1024),
-                            tc::desc_sw128(vst + kk * 2048, kTcRegion, 1024), kIdO, t > 0 || kk > 0);
-                tc::commit(o_done0 + 8 * (t & 1));
+                    for (int kk = 0; kk < kTcKeys / 16; ++kk)
+                        tc::mma(tmem + 256 * u + 128, tc::desc_sw128(pb + 32 * kk, 16, 1024),
+                                tc::desc_sw128(vst + kk * 2048, kTcRegion, 1024), kIdO,
+                                t > 0 || kk > 0);
+                    tc::commit(o_done(u, t & 1));
+                }
                 tc::commit(kv_empty0 + 8 * (t % kTcStages));
                 return true;
             };
             bool ok = mbar_wait_bounded(q_ready, 0, misc, p.wait_cycles);
             for (int j = 0; ok && j < ntiles; ++j) {
                 const int s = j % kTcStages;
-                if (!mbar_wait_bounded(kv_full0 + 8 * s, (j / kTcStages) & 1, misc, p.wait_cycles) ||
-                    (j >= 2 && !mbar_wait_bounded(s_free0 + 8 * (j & 1), ((j - 2) >> 1) & 1, misc,
-                                                  p.wait_cycles))) {
+                if (!mbar_wait_bounded(kv_full0 + 8 * s, (j / kTcStages) & 1, misc, p.wait_cycles)) {
                     ok = false;
                     break;
                 }
-                tc::fence_after();
                 const uint32_t kst = ring + s * kTcStageBytes;
-                const uint32_t tS = tmem + (j & 1) * kTcKeys;
+                for (int u = 0; u < kTcTiles && ok; ++u) {
+                    if (j >= 2 && !mbar_wait_bounded(s_free(u, j & 1), ((j - 2) >> 1) & 1, misc,
+                                                     p.wait_cycles)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const uint32_t qt = qbase + u * kTcQBytes;
+                    const uint32_t tS = tmem + 256 * u + (j & 1) * kTcKeys;
 #pragma unroll
-                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                    const uint32_t ko = (kk >> 2) * kTcRegion + 32 * (kk & 3);
-                    const uint32_t qo = (kk >> 2) * kTcQHalf + 32 * (kk & 3);
-                    const uint64_t kd = tc::desc_sw128(kst + ko, 16, 1024);
-                    tc::mma(tS, tc::desc_sw128(qhi + qo, 16, 1024), kd, kIdS, kk > 0);
-                    tc::mma(tS, tc::desc_sw128(qlo + qo, 16, 1024), kd, kIdS, true);
+                    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                        const uint32_t o = (kk >> 2) * kTcRegion + 32 * (kk & 3);
+                        const uint32_t qo = (kk >> 2) * kTcQHalf + 32 * (kk & 3);
+                        tc::mma(tS, tc::desc_sw128(qt + qo, 16, 1024),
+                                tc::desc_sw128(kst + o, 16, 1024), kIdS, kk > 0);
+                    }
+                    tc::commit(s_full(u, j & 1));
                 }
-                tc::commit(s_full0 + 8 * (j & 1));
-                if (j >= 1 && !value_product(j - 1)) ok = false;
+                if (ok && j >= 1 && !value_products(j - 1)) ok = false;
             }
-            if (ok && !value_product(ntiles - 1)) ok = false;
+            if (ok && !value_products(ntiles - 1)) ok = false;
             if (!ok) {
                 misc[0] = 1;
                 flag_error(p.err, QDEC_FLAG_TIMEOUT);
@@ -947,9 +975,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else {
         // --------------------------------------------- softmax warps --
-        const int r = tid;                        // row of the tile, tensor-memory lane
-        const int hj = r >> 5, ti = r & 31;       // head 4 g + hj, token t0 + ti
-        const bool live = ti < nrows;
+        const int u = warp >> 2;                  // query tile
+        const int r = tid & (kTcRows - 1);        // row of the tile, tensor-memory lane
+        const int hj = r >> 5, ti = r & 31;       // head 4 g + hj, token t0 + 32 u + ti
+        const int tok = kTcTileTok * u + ti;      // token of the block
+        const bool live = tok < nrows;
         // a wait every lane of the warp passes, or none: the tensor-memory
         // loads and stores below are warp-collective
         auto wait_all = [&](uint32_t bar, uint32_t parity) {
@@ -962,15 +992,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             return ok;
         };
         {
-            // Q, scaled to log2 units, as bf16 hi + lo: warp w converts rows
-            // w, w + 4, ..., lane l taking dims 4 l .. 4 l + 3 of each (one
-            // coalesced 512-byte row per warp load, all of them in flight)
-            uint8_t *qh = sm + kTcOffQhi, *ql = sm + kTcOffQlo;
+            // Q of the tile, scaled to log2 units, as bf16: warp w converts
+            // rows w % 4, w % 4 + 4, ..., lane l taking dims 4 l .. 4 l + 3 of
+            // each (one coalesced 512-byte row per warp load, all in flight)
+            uint8_t *qt = sm + kTcOffQ + u * kTcQBytes;
             const int half = lane >> 4, cc = (lane & 15) >> 1, sub = (lane & 1) * 8;
             float4 x[kTcRows / 4];
 #pragma unroll
             for (int k = 0; k < kTcRows / 4; ++k) {
-                const int rr = warp + 4 * k, tt = rr & 31;
+                const int rr = (warp & 3) + 4 * k, tt = kTcTileTok * u + (rr & 31);
                 x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (tt < nrows)
                     x[k] = reinterpret_cast<const float4 *>(
@@ -979,64 +1009,58 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
 #pragma unroll
             for (int k = 0; k < kTcRows / 4; ++k) {
-                const int rr = warp + 4 * k;
-                const float v[4] = {x[k].x * p.qscale, x[k].y * p.qscale, x[k].z * p.qscale,
-                                    x[k].w * p.qscale};
-                __nv_bfloat16 h[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) h[e] = __float2bfloat16_rn(v[e]);
-                const uint2 hi = make_uint2(
-                    static_cast<uint32_t>(__bfloat16_as_ushort(h[0])) |
-                        (static_cast<uint32_t>(__bfloat16_as_ushort(h[1])) << 16),
-                    static_cast<uint32_t>(__bfloat16_as_ushort(h[2])) |
-                        (static_cast<uint32_t>(__bfloat16_as_ushort(h[3])) << 16));
-                const uint2 lo = make_uint2(
-                    pack_bf16x2(v[0] - __bfloat162float(h[0]), v[1] - __bfloat162float(h[1])),
-                    pack_bf16x2(v[2] - __bfloat162float(h[2]), v[3] - __bfloat162float(h[3])));
-                const uint32_t off = half * kTcQHalf + sw128_off(rr, cc) + sub;
-                *reinterpret_cast<uint2 *>(qh + off) = hi;
-                *reinterpret_cast<uint2 *>(ql + off) = lo;
+                const int rr = (warp & 3) + 4 * k;
+                const uint2 w = make_uint2(pack_bf16x2(x[k].x * p.qscale, x[k].y * p.qscale),
+                                           pack_bf16x2(x[k].z * p.qscale, x[k].w * p.qscale));
+                *reinterpret_cast<uint2 *>(qt + half * kTcQHalf + sw128_off(rr, cc) + sub) = w;
             }
             fence_proxy_async_smem();  // read next by the tensor core
             __syncwarp();
             if (lane == 0) mbar_arrive(q_ready);
         }
-        const int lim = min(t0 + ti, L - 1);      // the last key this row sees
-        const uint32_t trow = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+        const int lim = min(t0 + tok, L - 1);     // the last key this row sees
+        const uint32_t trow = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 256 * u;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
             const int s = j % kTcStages;
             if (!wait_all(kv_full0 + 8 * s, (j / kTcStages) & 1) ||
-                !wait_all(s_full0 + 8 * (j & 1), (j >> 1) & 1)) {
+                !wait_all(s_full(u, j & 1), (j >> 1) & 1)) {
                 ok = false;
                 break;
             }
             tc::fence_after();
             float sc[kTcKeys];
             {
-                uint32_t v[32];
-                tc::ld32(v, trow + (j & 1) * kTcKeys);
+                uint32_t v0[32], v1[32];
+                tc::ld32(v0, trow + (j & 1) * kTcKeys);
+                tc::ld32(v1, trow + (j & 1) * kTcKeys + 32);
                 tc::wait_ld();
 #pragma unroll
-                for (int c = 0; c < 32; ++c) sc[c] = __uint_as_float(v[c]);
-                tc::ld32(v, trow + (j & 1) * kTcKeys + 32);
-                tc::wait_ld();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) sc[32 + c] = __uint_as_float(v[c]);
+                for (int c = 0; c < 32; ++c) {
+                    sc[c] = __uint_as_float(v0[c]);
+                    sc[32 + c] = __uint_as_float(v1[c]);
+                }
             }
             tc::fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_free0 + 8 * (j & 1));
+            if (lane == 0) mbar_arrive(s_free(u, j & 1));
             const int kb = j * kTcKeys;
             if (kb + kTcKeys - 1 > lim) {
 #pragma unroll
                 for (int c = 0; c < kTcKeys; ++c)
                     if (kb + c > lim) sc[c] = -INFINITY;
             }
-            float mx = sc[0];
+            // the row maximum as a tree (short dependency chains)
+            float mq[8];
 #pragma unroll
-            for (int c = 1; c < kTcKeys; ++c) mx = fmaxf(mx, sc[c]);
+            for (int q = 0; q < 8; ++q) mq[q] = fmaxf(sc[q], sc[8 + q]);
+#pragma unroll
+            for (int c = 16; c < kTcKeys; c += 8)
+#pragma unroll
+                for (int q = 0; q < 8; ++q) mq[q] = fmaxf(mq[q], sc[c + q]);
+            const float mx = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
+                                   fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
             const bool grow = mx > m + 8.f;
             if (__any_sync(kFull, grow)) {
                 const float mn = grow ? fmaxf(m, mx) : m;
@@ -1045,7 +1069,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 m = mn;
                 if (j > 0) {
                     // O holds stages 0 .. j-1 once their last product is done
-                    if (!wait_all(o_done0 + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1)) {
+                    if (!wait_all(o_done(u, (j - 1) & 1), ((j - 1) >> 1) & 1)) {
                         ok = false;
                         break;
                     }
@@ -1065,27 +1089,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             // P buffer j & 1 is free once the value product of stage j - 2 is done
-            if (j >= 2 && !wait_all(o_done0 + 8 * (j & 1), ((j - 2) >> 1) & 1)) {
+            if (j >= 2 && !wait_all(o_done(u, j & 1), ((j - 2) >> 1) & 1)) {
                 ok = false;
                 break;
             }
-            uint8_t *pb = sm + kTcOffP + (j & 1) * kTcPBytes;
-            float psum = 0.f;
+            uint8_t *pb = sm + kTcOffP + (2 * u + (j & 1)) * kTcPBytes;
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};   // the row sum in four chains
 #pragma unroll
             for (int c = 0; c < kTcKeys / 8; ++c) {   // keys 8 c .. 8 c + 7
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float p0 = exp2f(sc[8 * c + 2 * e] - m);
-                    const float p1 = exp2f(sc[8 * c + 2 * e + 1] - m);
-                    psum += p0 + p1;
+                    const float p0 = fast_exp2(sc[8 * c + 2 * e] - m);
+                    const float p1 = fast_exp2(sc[8 * c + 2 * e + 1] - m);
+                    ps[e] += p0 + p1;
                     w[e] = pack_bf16x2(p0, p1);
                 }
                 *reinterpret_cast<uint4 *>(pb + sw128_off(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            l += psum;
+            l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
             // V rows of keys past the sequence, or on pages not brought, are
-            // zeroed: the product would turn a non-finite one into NaN
+            // zeroed (by each tile's warps: both value products read them)
             const int pm = pmask[s];
             if (kb + kTcKeys > L || pm != (1 << kTcPagesPerStage) - 1) {
                 uint8_t *vr = sm + kTcOffRing + s * kTcStageBytes + 2 * kTcRegion;
@@ -1098,7 +1122,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             fence_proxy_async_smem();  // P and the zeroed rows are read by the tensor core
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full0 + 8 * (j & 1));
+            if (lane == 0) mbar_arrive(p_full(u, j & 1));
         }
         // ---- epilogue: O / l for this row, after every product has completed
         volatile int never = 0;
@@ -1109,7 +1133,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (fin && ok) {
             const float inv = l > 0.f ? 1.f / l : 0.f;
             __nv_bfloat16 *dst =
-                p.out + (static_cast<int64_t>(row0 + ti) * p.Hq + g * kGroup + hj) * kHeadDim;
+                p.out + (static_cast<int64_t>(row0 + tok) * p.Hq + g * kGroup + hj) * kHeadDim;
 #pragma unroll 1
             for (int c0 = 0; c0 < kHeadDim; c0 += 32) {
                 uint32_t o[32];
@@ -1134,12 +1158,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::fence_before();
     }
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kTcMmaWarp) {
         tc::fence_after();
         tc::dealloc(tmem, kTcTmemCols);
     }
     // a wait that gave up may leave copies in flight: let them land (bounded)
-    if (tid == 4 * 32 && misc[0]) {
+    if (tid == kTcProducerWarp * 32 && misc[0]) {
         const int issued = misc[3];
         volatile int never = 0;
         for (int t = max(0, issued - kTcStages); t < issued; ++t)
