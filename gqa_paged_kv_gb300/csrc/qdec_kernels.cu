@@ -37,8 +37,8 @@
 // from E4M3 mma.sync (m16n8k32) on the K codes as they are, the query rows
 // entering as four E4M3 terms (q 2^e = T0 + T1/16 + T2/256 + T3/4096); the V
 // codes are turned into f16 pairs (exact) for an f16 mma.sync with P as f16
-// hi + lo.  The K scale and 2^-e multiply the scores, the V scale each
-// tile's contribution to O^T.  The new token's k and v are quantized with
+// hi + lo.  The K scale and 2^-e multiply the scores; the V scale multiplies
+// the weights in the P operand of each tile's product.  The new token's k and v are quantized with
 // the scales of their page: fp32 division, then E4M3 nearest-even,
 // saturating.
 //
@@ -706,8 +706,8 @@ __device__ void fix_tile(uint8_t *tile, int ntok, bool patch, const __nv_bfloat1
 //     16tg .. 16tg+15 of tokens 2c, 2c+1, 2c+8, 2c+9, pairs the tokens'
 //     bytes with byte permutes and turns them into f16 (exact).
 // Accumulator element o[mt][e] then holds dim 16tg + 8(e >> 1) + mt.  The K
-// scale and the query terms' 2^-e multiply the scores, the V scale each
-// m-tile's product.
+// scale and the query terms' 2^-e multiply the scores; the V scale multiplies
+// the weights in the P operand (the row sums keep the unscaled weights).
 __device__ __forceinline__ void tile_math_fp8(uint32_t ks, uint32_t vs, const uint32_t (&qf)[8][2],
                                               int ntok, int lane, WarpState &st, __half *pbuf,
                                               float uA, float uB, float sv) {
@@ -772,13 +772,16 @@ __device__ __forceinline__ void tile_math_fp8(uint32_t ks, uint32_t vs, const ui
     st.lA += pA0 + pA1;
     st.lB += pB0 + pB1;
 
-    // P^T operand in f16 (p <= 2^8 between rescales): column n < 4 holds
-    // f16(p) of head n, column 4 + n the f16 remainder; row = token.
+    // P^T operand in f16, each weight times the tile's V scale (p <= 2^8
+    // between rescales; the row sums above keep the unscaled weights): column
+    // n < 4 holds f16(p sv) of head n, column 4 + n the f16 remainder; row =
+    // token.
     const bool hi = c < 2;
     const int colA = (hi ? 0 : kGroup) + 2 * (c & 1);
-    auto part = [hi](float v) {
-        const __half h = __float2half_rn(v);
-        return hi ? h : __float2half_rn(v - __half2float(h));
+    auto part = [hi, sv](float v) {
+        const float x = v * sv;
+        const __half h = __float2half_rn(x);
+        return hi ? h : __float2half_rn(x - __half2float(h));
     };
     pbuf[colA * 16 + tg] = part(pA0);
     pbuf[colA * 16 + tg + 8] = part(pA1);
@@ -816,10 +819,7 @@ __device__ __forceinline__ void tile_math_fp8(uint32_t ks, uint32_t vs, const ui
         a[1] = e4m3x2_to_f16x2(u01);
         a[2] = e4m3x2_to_f16x2(t89);
         a[3] = e4m3x2_to_f16x2(u89);
-        float t[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_f16(t, a, b0, b1);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) st.o[mt][e] = fmaf(sv, t[e], st.o[mt][e]);
+        mma_f16(st.o[mt], a, b0, b1);
     }
     __syncwarp();
 }

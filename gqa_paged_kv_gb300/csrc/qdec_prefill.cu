@@ -861,10 +861,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == kTcProducerWarp) {
         // ------------------------------------------------ TMA producer --
-        // lanes 0-3 each bring one page of the stage (its four regions)
+        // lanes 0-3 each bring one page of the stage (its four regions).  The
+        // block-table entries are looked up 32 pages (8 stages) at a time, one
+        // group ahead, so no lookup sits between a freed stage and its refill.
         int issued = 0;
+        auto lookup = [&](int grp) {  // lane l: page index 32 grp + l of the sequence
+            const int pg = 32 * grp + lane;
+            return pg < npg ? p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg] : -1;
+        };
+        int cur = lookup(0), nxt = lookup(1);
         for (int j = 0; j < ntiles; ++j) {
             const int s = j % kTcStages;
+            if (j > 0 && (j * kTcPagesPerStage) % 32 == 0) {
+                cur = nxt;
+                nxt = lookup(j * kTcPagesPerStage / 32 + 1);
+            }
             bool stop = false;
             if (lane == 0) {
                 if (misc[0]) {
@@ -879,9 +890,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (__shfl_sync(kFull, stop, 0)) break;
             const int pg = j * kTcPagesPerStage + lane;
-            int page = -1;
-            if (lane < kTcPagesPerStage && pg < npg)
-                page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg];
+            const int page = __shfl_sync(kFull, cur, (j * kTcPagesPerStage + (lane & 3)) & 31);
             const bool ok = lane < kTcPagesPerStage && pg < npg && page >= 0 && page < p.num_pages;
             if (lane < kTcPagesPerStage && pg < npg && !ok) flag_error(p.err, QDEC_FLAG_BAD_PAGE);
             const unsigned mask = __ballot_sync(kFull, ok) & 0xFu;
