@@ -336,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int i = 0; i < 4; ++i) mbar_init(convb0 + 8 * i, kConsumerWarps);
             misc[0] = 0;
             misc[3] = 0;
+            misc[5] = 0;
             fence_mbar_init();
         }
     }
@@ -675,10 +676,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 // blocks with the most keys first.  The block is two tiles of M = 128 rows:
 // tile u holds tokens 32 u .. 32 u + 31 of the block for the 4 query heads
 // of the group (row 32 j + i: head 4 g + j, token 32 u + i), so each K/V
-// stage in shared memory serves 256 query rows.  Per stage the producer warp
-// brings 64 keys (4 pages) as four 8 KiB regions [K dims 0-63][K dims 64-127]
-// [V dims 0-63][V dims 64-127], each [64 keys][128 bytes], 128-byte swizzled
-// (one 2 KiB TMA box per page and region), so that, from one issuing thread
+// stage in shared memory serves 256 query rows.  Per stage of 64 keys (4
+// pages) one producer warp brings K and another V, each into its own ring,
+// as two 8 KiB regions [dims 0-63][dims 64-127] of [64 keys][128 bytes],
+// 128-byte swizzled (one 2 KiB TMA box per page and region): a K slot is
+// refilled as soon as the stage's score products are done, while V is only
+// needed by the value products, one softmax later.  From one issuing thread
 // (warp 9), for each tile
 //   S = Q K^T  (M 128, N 64, K 128: 8 MMAs of K 16; Q and K both K-major;
 //               q enters as bf16),
@@ -703,29 +706,32 @@ constexpr int kTcKeys = 64;                                // keys per stage
 constexpr int kTcPagesPerStage = kTcKeys / kPageSize;      // 4
 constexpr int kTcStages = 3;
 constexpr int kTcRegion = kTcKeys * 128;                   // [64 keys][64 dims] bf16, 8 KiB
-constexpr int kTcStageBytes = 4 * kTcRegion;               // K lo, K hi, V lo, V hi halves of D
+constexpr int kTcSlotBytes = 2 * kTcRegion;                // K (or V): dims 0-63, dims 64-127
 constexpr int kTcQHalf = kTcRows * 128;                    // [128 rows][64 dims] bf16, 16 KiB
 constexpr int kTcQBytes = 2 * kTcQHalf;                    // one tile's Q
 constexpr int kTcPBytes = kTcRows * 128;                   // [128 rows][64 keys] bf16, 16 KiB
 constexpr int kTcOffQ = 0;                                 // Q of tile u at u * kTcQBytes
 constexpr int kTcOffP = kTcOffQ + kTcTiles * kTcQBytes;    // P of tile u, buffer q: (2u + q)
-constexpr int kTcOffRing = kTcOffP + 2 * kTcTiles * kTcPBytes;
-constexpr int kTcOffTail = kTcOffRing + kTcStages * kTcStageBytes;
-// tail: barriers kv_full[S], kv_empty[S]; per tile s_full[2], s_free[2],
-// p_full[2], o_done[2]; q_ready, done; then ints: abort, sequence, block,
-// stages issued, tensor-memory address, and the mask of pages brought into
-// every stage
-constexpr int kTcBars = 2 * kTcStages + kTcTiles * 8 + 2;
-constexpr int kTcTailBytes = kTcBars * 8 + (5 + kTcStages) * 4;
+constexpr int kTcOffKRing = kTcOffP + 2 * kTcTiles * kTcPBytes;
+constexpr int kTcOffVRing = kTcOffKRing + kTcStages * kTcSlotBytes;
+constexpr int kTcOffTail = kTcOffVRing + kTcStages * kTcSlotBytes;
+// tail: barriers k_full[S], k_empty[S], v_full[S], v_empty[S]; per tile
+// s_full[2], s_free[2], p_full[2], o_done[2]; q_ready, done; then ints:
+// abort, sequence, block, K stages issued, tensor-memory address, V stages
+// issued, and the mask of pages brought into every V slot
+constexpr int kTcBars = 4 * kTcStages + kTcTiles * 8 + 2;
+constexpr int kTcTailBytes = kTcBars * 8 + (6 + kTcStages) * 4;
 constexpr int kTcSmemBytes = kTcOffTail + kTcTailBytes + 1024;
 constexpr int kTcSoftmaxWarps = 4 * kTcTiles;
-constexpr int kTcProducerWarp = kTcSoftmaxWarps;
+constexpr int kTcProducerWarp = kTcSoftmaxWarps;           // K stages
 constexpr int kTcMmaWarp = kTcSoftmaxWarps + 1;
-constexpr int kTcThreads = (kTcSoftmaxWarps + 2) * 32;
+constexpr int kTcVProducerWarp = kTcSoftmaxWarps + 2;      // V stages
+constexpr int kTcThreads = (kTcSoftmaxWarps + 3) * 32;
 // tile u: S buffers at columns 256 u + {0, 64}, O at 256 u + 128
 constexpr uint32_t kTcTmemCols = 256 * kTcTiles;
 static_assert(kTcSmemBytes <= 227 * 1024, "one CTA per SM");
-static_assert(kTcOffRing % 1024 == 0 && kTcOffP % 1024 == 0, "swizzled operands start on 1024-byte boundaries");
+static_assert(kTcOffKRing % 1024 == 0 && kTcOffVRing % 1024 == 0 && kTcOffP % 1024 == 0,
+              "swizzled operands start on 1024-byte boundaries");
 static_assert(kTcTmemCols <= 512, "tensor memory");
 
 // One (page, plane, half of D) region of a page: 16 tokens x 64 dims, 2 KiB,
@@ -763,20 +769,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint8_t *tail = sm + kTcOffTail;
-    const uint32_t kv_full0 = smem_u32(tail);
-    const uint32_t kv_empty0 = kv_full0 + 8 * kTcStages;
+    const uint32_t k_full0 = smem_u32(tail);
+    const uint32_t k_empty0 = k_full0 + 8 * kTcStages;
+    const uint32_t v_full0 = k_empty0 + 8 * kTcStages;
+    const uint32_t v_empty0 = v_full0 + 8 * kTcStages;
     // per tile u: s_full, s_free, p_full, o_done, two of each (buffer q)
-    const uint32_t tile_bar0 = kv_empty0 + 8 * kTcStages;
+    const uint32_t tile_bar0 = v_empty0 + 8 * kTcStages;
     auto s_full = [&](int u, int q) { return tile_bar0 + 64 * u + 8 * q; };
     auto s_free = [&](int u, int q) { return tile_bar0 + 64 * u + 16 + 8 * q; };
     auto p_full = [&](int u, int q) { return tile_bar0 + 64 * u + 32 + 8 * q; };
     auto o_done = [&](int u, int q) { return tile_bar0 + 64 * u + 48 + 8 * q; };
     const uint32_t q_ready = tile_bar0 + 64 * kTcTiles;
     const uint32_t done_bar = q_ready + 8;
-    // misc: [0] abort, [1] sequence, [2] query block, [3] stages issued,
-    // [4] tensor-memory address; pmask[s]: pages brought into stage s
+    // misc: [0] abort, [1] sequence, [2] query block, [3] K stages issued,
+    // [4] tensor-memory address, [5] V stages issued; pmask[s]: pages
+    // brought into V slot s
     volatile int *misc = reinterpret_cast<volatile int *>(tail + kTcBars * 8);
-    volatile int *pmask = misc + 5;
+    volatile int *pmask = misc + 6;
     const int g = blockIdx.x % p.Hkv;
     const int unit = blockIdx.x / p.Hkv;
 
@@ -822,8 +831,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (lane == 0) {
             for (int s = 0; s < kTcStages; ++s) {
-                mbar_init(kv_full0 + 8 * s, 1);   // the producer's arrival + the bytes
-                mbar_init(kv_empty0 + 8 * s, 1);  // the commit of the stage's value products
+                mbar_init(k_full0 + 8 * s, 1);    // the K producer's arrival + the bytes
+                mbar_init(k_empty0 + 8 * s, 1);   // the commit of the stage's score products
+                mbar_init(v_full0 + 8 * s, 1);    // the V producer's arrival + the bytes
+                mbar_init(v_empty0 + 8 * s, 1);   // the commit of the stage's value products
             }
             for (int u = 0; u < kTcTiles; ++u) {
                 for (int q = 0; q < 2; ++q) {
@@ -859,11 +870,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int ntiles = (t0 + nrows - 1) / kTcKeys + 1;   // stages up to the last query
     const int npg = (L + kPageSize - 1) / kPageSize;     // pages of the sequence
 
-    if (warp == kTcProducerWarp) {
-        // ------------------------------------------------ TMA producer --
-        // lanes 0-3 each bring one page of the stage (its four regions).  The
-        // block-table entries are looked up 32 pages (8 stages) at a time, one
-        // group ahead, so no lookup sits between a freed stage and its refill.
+    if (warp == kTcProducerWarp || warp == kTcVProducerWarp) {
+        // ----------------------------------------------- TMA producers --
+        // One warp brings the K halves of every stage, the other the V
+        // halves, each into its own ring: a K slot frees as soon as the
+        // stage's score products are done, a V slot once its value products
+        // are.  Lanes 0-3 each bring one page of the stage (its two regions);
+        // the block-table entries are looked up 32 pages (8 stages) at a time,
+        // one group ahead.
+        const bool isv = warp == kTcVProducerWarp;
+        const uint32_t full0 = isv ? v_full0 : k_full0;
+        const uint32_t empty0 = isv ? v_empty0 : k_empty0;
+        uint8_t *ringp = sm + (isv ? kTcOffVRing : kTcOffKRing);
         int issued = 0;
         auto lookup = [&](int grp) {  // lane l: page index 32 grp + l of the sequence
             const int pg = 32 * grp + lane;
@@ -881,7 +899,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (misc[0]) {
                     stop = true;
                 } else if (j >= kTcStages &&
-                           !mbar_wait_bounded(kv_empty0 + 8 * s, ((j / kTcStages) - 1) & 1, misc,
+                           !mbar_wait_bounded(empty0 + 8 * s, ((j / kTcStages) - 1) & 1, misc,
                                               p.wait_cycles)) {
                     misc[0] = 1;
                     flag_error(p.err, QDEC_FLAG_TIMEOUT);
@@ -892,45 +910,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int pg = j * kTcPagesPerStage + lane;
             const int page = __shfl_sync(kFull, cur, (j * kTcPagesPerStage + (lane & 3)) & 31);
             const bool ok = lane < kTcPagesPerStage && pg < npg && page >= 0 && page < p.num_pages;
-            if (lane < kTcPagesPerStage && pg < npg && !ok) flag_error(p.err, QDEC_FLAG_BAD_PAGE);
+            if (!isv && lane < kTcPagesPerStage && pg < npg && !ok) flag_error(p.err, QDEC_FLAG_BAD_PAGE);
             const unsigned mask = __ballot_sync(kFull, ok) & 0xFu;
-            const bool withheld = p.withhold_first && j == 0;  // test hook: never lands
+            const bool withheld = !isv && p.withhold_first && j == 0;  // test hook: never lands
             if (lane == 0) {
-                pmask[s] = static_cast<int>(mask);
+                if (isv) pmask[s] = static_cast<int>(mask);
                 if (!withheld) {
                     if (mask == 0)
-                        mbar_arrive(kv_full0 + 8 * s);
+                        mbar_arrive(full0 + 8 * s);
                     else
-                        mbar_arrive_expect_tx(kv_full0 + 8 * s,
-                                              __popc(mask) * 4 * (kPageSize * 128));
+                        mbar_arrive_expect_tx(full0 + 8 * s, __popc(mask) * 2 * (kPageSize * 128));
                 }
             }
             __syncwarp();
             if (ok && !withheld) {
-                const uint32_t dst = smem_u32(sm + kTcOffRing + s * kTcStageBytes) +
-                                     lane * (kPageSize * 128);
+                const uint32_t dst = smem_u32(ringp + s * kTcSlotBytes) + lane * (kPageSize * 128);
                 const int row = page * 2 * p.Hkv + g;
 #pragma unroll
-                for (int r = 0; r < 4; ++r)  // region r: plane r / 2, half r % 2
-                    tma_load_region(dst + r * kTcRegion, &region_map, r & 1, r >> 1, row,
-                                    kv_full0 + 8 * s);
+                for (int h = 0; h < 2; ++h)  // region h: dims 64 h .. 64 h + 63 of the plane
+                    tma_load_region(dst + h * kTcRegion, &region_map, h, isv ? 1 : 0, row,
+                                    full0 + 8 * s);
             }
             issued = j + 1;
         }
-        if (lane == 0) misc[3] = issued;
+        if (lane == 0) misc[isv ? 5 : 3] = issued;
     } else if (warp == kTcMmaWarp) {
         // --------------------------------------------- the MMA issuer --
         if (lane == 0) {
             const uint32_t qbase = smem_u32(sm + kTcOffQ);
             const uint32_t pbase = smem_u32(sm + kTcOffP);
-            const uint32_t ring = smem_u32(sm + kTcOffRing);
+            const uint32_t kring = smem_u32(sm + kTcOffKRing), vring = smem_u32(sm + kTcOffVRing);
             constexpr uint32_t kIdS = tc::idesc_bf16(kTcRows, kTcKeys, false);
             constexpr uint32_t kIdO = tc::idesc_bf16(kTcRows, kHeadDim, true);
-            // O_u += P_u,t V_t for both tiles once their softmax warps have
-            // written P; the commits free the P buffers (o_done) and the
-            // stage (kv_empty)
+            // O_u += P_u,t V_t for both tiles once V_t has landed and their
+            // softmax warps have written P; the commits free the P buffers
+            // (o_done) and the V slot (v_empty)
             auto value_products = [&](int t) -> bool {
-                const uint32_t vst = ring + (t % kTcStages) * kTcStageBytes + 2 * kTcRegion;
+                if (!mbar_wait_bounded(v_full0 + 8 * (t % kTcStages), (t / kTcStages) & 1, misc,
+                                       p.wait_cycles))
+                    return false;
+                const uint32_t vst = vring + (t % kTcStages) * kTcSlotBytes;
                 for (int u = 0; u < kTcTiles; ++u) {
                     if (!mbar_wait_bounded(p_full(u, t & 1), (t >> 1) & 1, misc, p.wait_cycles))
                         return false;
@@ -943,17 +962,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 t > 0 || kk > 0);
                     tc::commit(o_done(u, t & 1));
                 }
-                tc::commit(kv_empty0 + 8 * (t % kTcStages));
+                tc::commit(v_empty0 + 8 * (t % kTcStages));
                 return true;
             };
             bool ok = mbar_wait_bounded(q_ready, 0, misc, p.wait_cycles);
             for (int j = 0; ok && j < ntiles; ++j) {
                 const int s = j % kTcStages;
-                if (!mbar_wait_bounded(kv_full0 + 8 * s, (j / kTcStages) & 1, misc, p.wait_cycles)) {
+                if (!mbar_wait_bounded(k_full0 + 8 * s, (j / kTcStages) & 1, misc, p.wait_cycles)) {
                     ok = false;
                     break;
                 }
-                const uint32_t kst = ring + s * kTcStageBytes;
+                const uint32_t kst = kring + s * kTcSlotBytes;
                 for (int u = 0; u < kTcTiles && ok; ++u) {
                     if (j >= 2 && !mbar_wait_bounded(s_free(u, j & 1), ((j - 2) >> 1) & 1, misc,
                                                      p.wait_cycles)) {
@@ -972,6 +991,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     tc::commit(s_full(u, j & 1));
                 }
+                if (ok) tc::commit(k_empty0 + 8 * s);  // the K slot frees once both products are done
                 if (ok && j >= 1 && !value_products(j - 1)) ok = false;
             }
             if (ok && !value_products(ntiles - 1)) ok = false;
@@ -1033,8 +1053,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
             const int s = j % kTcStages;
-            if (!wait_all(kv_full0 + 8 * s, (j / kTcStages) & 1) ||
-                !wait_all(s_full(u, j & 1), (j >> 1) & 1)) {
+            if (!wait_all(s_full(u, j & 1), (j >> 1) & 1)) {
                 ok = false;
                 break;
             }
@@ -1117,11 +1136,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 *reinterpret_cast<uint4 *>(pb + sw128_off(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
             l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-            // V rows of keys past the sequence, or on pages not brought, are
-            // zeroed (by each tile's warps: both value products read them)
-            const int pm = pmask[s];
-            if (kb + kTcKeys > L || pm != (1 << kTcPagesPerStage) - 1) {
-                uint8_t *vr = sm + kTcOffRing + s * kTcStageBytes + 2 * kTcRegion;
+            // V rows of keys past the sequence (and of pages not brought there)
+            // are zeroed once the slot has landed, by each tile's warps: both
+            // value products read them
+            if (kb + kTcKeys > L) {
+                if (!wait_all(v_full0 + 8 * s, (j / kTcStages) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const int pm = pmask[s];
+                uint8_t *vr = sm + kTcOffVRing + s * kTcSlotBytes;
                 for (int e = r; e < kTcKeys * 16; e += kTcRows) {
                     const int kr = e >> 4, c = e & 15;
                     if (kb + kr >= L || !((pm >> (kr / kPageSize)) & 1))
@@ -1172,11 +1196,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc::dealloc(tmem, kTcTmemCols);
     }
     // a wait that gave up may leave copies in flight: let them land (bounded)
-    if (tid == kTcProducerWarp * 32 && misc[0]) {
-        const int issued = misc[3];
+    if ((tid == kTcProducerWarp * 32 || tid == kTcVProducerWarp * 32) && misc[0]) {
+        const bool isv = warp == kTcVProducerWarp;
+        const uint32_t full0 = isv ? v_full0 : k_full0;
+        const int issued = misc[isv ? 5 : 3];
         volatile int never = 0;
         for (int t = max(0, issued - kTcStages); t < issued; ++t)
-            mbar_wait_bounded(kv_full0 + 8 * (t % kTcStages), (t / kTcStages) & 1, &never,
+            mbar_wait_bounded(full0 + 8 * (t % kTcStages), (t / kTcStages) & 1, &never,
                               p.wait_cycles);
     }
 }
