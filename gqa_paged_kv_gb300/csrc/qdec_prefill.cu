@@ -685,15 +685,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 // (warp 9), for each tile
 //   S = Q K^T  (M 128, N 64, K 128: 8 MMAs of K 16; Q and K both K-major;
 //               q enters as bf16),
-//   O += P V   (M 128, N 128, K 64: 4 MMAs; P K-major from shared memory, V
-//               read in place as an MN-major operand).
+//   O += P V   (M 128, N 128, K 64: 4 MMAs; P read from tensor memory, V
+//               read in place from shared memory as an MN-major operand).
 // S is double-buffered in tensor memory per tile, so the scores of stage
 // j + 1 are formed while the softmax warps (warps 4 u .. 4 u + 3 for tile u,
 // thread r of the group owning row r, its tensor-memory lane) work on stage
 // j: load the 64 scores, mask keys past each row's token, keep a stale
 // running maximum (O in tensor memory is rescaled only when a stage's
 // maximum exceeds it by more than 2^8, so the weights stay below 256), and
-// write P as bf16 into one of two shared buffers of the tile.  V rows of
+// write P as bf16 into tensor memory over the scores just read.  V rows of
 // keys past the sequence (or of pages not brought) are zeroed before a value
 // product reads them.  The epilogue reads O out of tensor memory, divides by
 // the row sum and stores the row.  Every wait is bounded; the decisions that
@@ -704,19 +704,17 @@ constexpr int kTcTok = kTcTiles * kTcTileTok;              // chunk tokens per C
 constexpr int kTcRows = kTcTileTok * kGroup;               // M = 128 rows per tile
 constexpr int kTcKeys = 64;                                // keys per stage
 constexpr int kTcPagesPerStage = kTcKeys / kPageSize;      // 4
-constexpr int kTcStages = 3;
+constexpr int kTcStages = 4;
 constexpr int kTcRegion = kTcKeys * 128;                   // [64 keys][64 dims] bf16, 8 KiB
 constexpr int kTcSlotBytes = 2 * kTcRegion;                // K (or V): dims 0-63, dims 64-127
 constexpr int kTcQHalf = kTcRows * 128;                    // [128 rows][64 dims] bf16, 16 KiB
 constexpr int kTcQBytes = 2 * kTcQHalf;                    // one tile's Q
-constexpr int kTcPBytes = kTcRows * 128;                   // [128 rows][64 keys] bf16, 16 KiB
 constexpr int kTcOffQ = 0;                                 // Q of tile u at u * kTcQBytes
-constexpr int kTcOffP = kTcOffQ + kTcTiles * kTcQBytes;    // P of tile u, buffer q: (2u + q)
-constexpr int kTcOffKRing = kTcOffP + 2 * kTcTiles * kTcPBytes;
+constexpr int kTcOffKRing = kTcOffQ + kTcTiles * kTcQBytes;
 constexpr int kTcOffVRing = kTcOffKRing + kTcStages * kTcSlotBytes;
 constexpr int kTcOffTail = kTcOffVRing + kTcStages * kTcSlotBytes;
 // tail: barriers k_full[S], k_empty[S], v_full[S], v_empty[S]; per tile
-// s_full[2], s_free[2], p_full[2], o_done[2]; q_ready, done; then ints:
+// s_full[2], (unused)[2], p_full[2], o_done[2]; q_ready, done; then ints:
 // abort, sequence, block, K stages issued, tensor-memory address, V stages
 // issued, and the mask of pages brought into every V slot
 constexpr int kTcBars = 4 * kTcStages + kTcTiles * 8 + 2;
@@ -730,7 +728,7 @@ constexpr int kTcThreads = (kTcSoftmaxWarps + 3) * 32;
 // tile u: S buffers at columns 256 u + {0, 64}, O at 256 u + 128
 constexpr uint32_t kTcTmemCols = 256 * kTcTiles;
 static_assert(kTcSmemBytes <= 227 * 1024, "one CTA per SM");
-static_assert(kTcOffKRing % 1024 == 0 && kTcOffVRing % 1024 == 0 && kTcOffP % 1024 == 0,
+static_assert(kTcOffKRing % 1024 == 0 && kTcOffVRing % 1024 == 0,
               "swizzled operands start on 1024-byte boundaries");
 static_assert(kTcTmemCols <= 512, "tensor memory");
 
@@ -773,10 +771,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t k_empty0 = k_full0 + 8 * kTcStages;
     const uint32_t v_full0 = k_empty0 + 8 * kTcStages;
     const uint32_t v_empty0 = v_full0 + 8 * kTcStages;
-    // per tile u: s_full, s_free, p_full, o_done, two of each (buffer q)
+    // per tile u: s_full, p_full, o_done, two of each (buffer q)
     const uint32_t tile_bar0 = v_empty0 + 8 * kTcStages;
     auto s_full = [&](int u, int q) { return tile_bar0 + 64 * u + 8 * q; };
-    auto s_free = [&](int u, int q) { return tile_bar0 + 64 * u + 16 + 8 * q; };
     auto p_full = [&](int u, int q) { return tile_bar0 + 64 * u + 32 + 8 * q; };
     auto o_done = [&](int u, int q) { return tile_bar0 + 64 * u + 48 + 8 * q; };
     const uint32_t q_ready = tile_bar0 + 64 * kTcTiles;
@@ -839,7 +836,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int u = 0; u < kTcTiles; ++u) {
                 for (int q = 0; q < 2; ++q) {
                     mbar_init(s_full(u, q), 1);   // commit of the score product
-                    mbar_init(s_free(u, q), 4);   // the tile's softmax warps have read the scores
                     mbar_init(p_full(u, q), 4);   // the tile's softmax warps have written P
                     mbar_init(o_done(u, q), 1);   // commit of the value product
                 }
@@ -938,13 +934,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // --------------------------------------------- the MMA issuer --
         if (lane == 0) {
             const uint32_t qbase = smem_u32(sm + kTcOffQ);
-            const uint32_t pbase = smem_u32(sm + kTcOffP);
             const uint32_t kring = smem_u32(sm + kTcOffKRing), vring = smem_u32(sm + kTcOffVRing);
             constexpr uint32_t kIdS = tc::idesc_bf16(kTcRows, kTcKeys, false);
             constexpr uint32_t kIdO = tc::idesc_bf16(kTcRows, kHeadDim, true);
             // O_u += P_u,t V_t for both tiles once V_t has landed and their
-            // softmax warps have written P; the commits free the P buffers
-            // (o_done) and the V slot (v_empty)
+            // softmax warps have written P (over the scores of stage t, in
+            // tensor memory); the commits free that buffer for the scores of
+            // stage t + 2 (o_done) and the V slot (v_empty)
             auto value_products = [&](int t) -> bool {
                 if (!mbar_wait_bounded(v_full0 + 8 * (t % kTcStages), (t / kTcStages) & 1, misc,
                                        p.wait_cycles))
@@ -954,12 +950,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (!mbar_wait_bounded(p_full(u, t & 1), (t >> 1) & 1, misc, p.wait_cycles))
                         return false;
                     tc::fence_after();
-                    const uint32_t pb = pbase + (2 * u + (t & 1)) * kTcPBytes;
+                    const uint32_t tp = tmem + 256 * u + (t & 1) * kTcKeys;  // P: 32 columns
 #pragma unroll
                     for (int kk = 0; kk < kTcKeys / 16; ++kk)
-                        tc::mma(tmem + 256 * u + 128, tc::desc_sw128(pb + 32 * kk, 16, 1024),
-                                tc::desc_sw128(vst + kk * 2048, kTcRegion, 1024), kIdO,
-                                t > 0 || kk > 0);
+                        tc::mma_ts(tmem + 256 * u + 128, tp + 8 * kk,
+                                   tc::desc_sw128(vst + kk * 2048, kTcRegion, 1024), kIdO,
+                                   t > 0 || kk > 0);
                     tc::commit(o_done(u, t & 1));
                 }
                 tc::commit(v_empty0 + 8 * (t % kTcStages));
@@ -974,7 +970,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 const uint32_t kst = kring + s * kTcSlotBytes;
                 for (int u = 0; u < kTcTiles && ok; ++u) {
-                    if (j >= 2 && !mbar_wait_bounded(s_free(u, j & 1), ((j - 2) >> 1) & 1, misc,
+                    // the buffer holds P of stage j - 2 until its value product is done
+                    if (j >= 2 && !mbar_wait_bounded(o_done(u, j & 1), ((j - 2) >> 1) & 1, misc,
                                                      p.wait_cycles)) {
                         ok = false;
                         break;
@@ -1070,9 +1067,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     sc[32 + c] = __uint_as_float(v1[c]);
                 }
             }
-            tc::fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free(u, j & 1));
             const int kb = j * kTcKeys;
             if (kb + kTcKeys - 1 > lim) {
 #pragma unroll
@@ -1116,25 +1110,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc::fence_before();
                 }
             }
-            // P buffer j & 1 is free once the value product of stage j - 2 is done
-            if (j >= 2 && !wait_all(o_done(u, j & 1), ((j - 2) >> 1) & 1)) {
-                ok = false;
-                break;
-            }
-            uint8_t *pb = sm + kTcOffP + (2 * u + (j & 1)) * kTcPBytes;
+            // P as bf16 over the first 32 columns of the scores just read (a
+            // column holds two consecutive keys), the A operand of the value
+            // product
             float ps[4] = {0.f, 0.f, 0.f, 0.f};   // the row sum in four chains
+            uint32_t pw[kTcKeys / 2];
 #pragma unroll
-            for (int c = 0; c < kTcKeys / 8; ++c) {   // keys 8 c .. 8 c + 7
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = fast_exp2(sc[8 * c + 2 * e] - m);
-                    const float p1 = fast_exp2(sc[8 * c + 2 * e + 1] - m);
-                    ps[e] += p0 + p1;
-                    w[e] = pack_bf16x2(p0, p1);
-                }
-                *reinterpret_cast<uint4 *>(pb + sw128_off(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int c = 0; c < kTcKeys / 2; ++c) {
+                const float p0 = fast_exp2(sc[2 * c] - m);
+                const float p1 = fast_exp2(sc[2 * c + 1] - m);
+                ps[c & 3] += p0 + p1;
+                pw[c] = pack_bf16x2(p0, p1);
             }
+            tc::st32(trow + (j & 1) * kTcKeys, pw);
             l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
             // V rows of keys past the sequence (and of pages not brought there)
             // are zeroed once the slot has landed, by each tile's warps: both
@@ -1153,7 +1141,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                    ((c & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            fence_proxy_async_smem();  // P and the zeroed rows are read by the tensor core
+            tc::wait_st();
+            fence_proxy_async_smem();  // the zeroed rows are read by the tensor core
+            tc::fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full(u, j & 1));
         }

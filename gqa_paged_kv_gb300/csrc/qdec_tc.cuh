@@ -67,6 +67,18 @@ static __device__ __forceinline__ void mma(uint32_t dtmem, uint64_t adesc, uint6
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1 : 0)
         : "memory");
 }
+// D (+)= A B with A read from tensor memory (a_tmem: lane = row of A, each
+// 32-bit column two consecutive K elements, the lower half first) and B from
+// shared memory; one K = 16 step (8 columns of A).
+static __device__ __forceinline__ void mma_ts(uint32_t dtmem, uint32_t a_tmem, uint64_t bdesc,
+                                              uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(dtmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1 : 0)
+        : "memory");
+}
 // One arrival on `bar` once every tcgen05 operation this thread issued so
 // far has completed.
 static __device__ __forceinline__ void commit(uint32_t bar) {
