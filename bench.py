@@ -42,6 +42,7 @@ import subprocess
 import sys
 import tempfile
 import time
+from dataclasses import replace
 
 import numpy as np
 import torch
@@ -130,6 +131,9 @@ def parse_args():
                     help="launch each layer only after the previous one completed")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: run fewer layers than the workload has")
+    ap.add_argument("--pool-pages", type=int, default=0,
+                    help="profiling only: a smaller pool per layer (it must still hold every "
+                         "page the sequences reference; the work and traffic are the same)")
     return ap.parse_args()
 
 
@@ -711,6 +715,8 @@ def run_ours(args, dist: Dist):
     dev = dist.local
     torch.cuda.set_device(dev)
     spec = wl.WORKLOADS[args.workload]
+    if args.pool_pages:
+        spec = replace(spec, pool_pages=args.pool_pages)
     w = wl.build(spec, f"cuda:{dev}", layers=args.layers or None, kv=args.kv)
     spec = w.spec
     L = spec.layers
@@ -901,7 +907,7 @@ def run_ours(args, dist: Dist):
         cfg["plan"] = (f"planned for contexts up to {args.plan_bound} tokens (block-table rows "
                        f"of {layers.shape.max_blocks_per_seq} pages)")
     configs = []
-    if not args.qkv and not args.layers and not args.no_configs:
+    if not args.qkv and not args.layers and not args.no_configs and not args.pool_pages:
         # the other workloads of the benchmark plan, each on its own (the
         # headline's buffers are released first)
         del layers, run, w, step_in, flush

@@ -681,8 +681,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 // as two 8 KiB regions [dims 0-63][dims 64-127] of [64 keys][128 bytes],
 // 128-byte swizzled (one 2 KiB TMA box per page and region): a K slot is
 // refilled as soon as the stage's score products are done, while V is only
-// needed by the value products, one softmax later.  From one issuing thread
-// (warp 9), for each tile
+// needed by the value products, one softmax later.  For each tile, from its
+// own issuing thread (warps 9 and 11),
 //   S = Q K^T  (M 128, N 64, K 128: 8 MMAs of K 16; Q and K both K-major;
 //               q enters as bf16),
 //   O += P V   (M 128, N 128, K 64: 4 MMAs; P read from tensor memory, V
@@ -724,7 +724,8 @@ constexpr int kTcSoftmaxWarps = 4 * kTcTiles;
 constexpr int kTcProducerWarp = kTcSoftmaxWarps;           // K stages
 constexpr int kTcMmaWarp = kTcSoftmaxWarps + 1;
 constexpr int kTcVProducerWarp = kTcSoftmaxWarps + 2;      // V stages
-constexpr int kTcThreads = (kTcSoftmaxWarps + 3) * 32;
+constexpr int kTcMmaWarp1 = kTcSoftmaxWarps + 3;           // tile 1's products (tile 0: kTcMmaWarp)
+constexpr int kTcThreads = (kTcSoftmaxWarps + 4) * 32;
 // tile u: S buffers at columns 256 u + {0, 64}, O at 256 u + 128
 constexpr uint32_t kTcTmemCols = 256 * kTcTiles;
 static_assert(kTcSmemBytes <= 227 * 1024, "one CTA per SM");
@@ -829,9 +830,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             for (int s = 0; s < kTcStages; ++s) {
                 mbar_init(k_full0 + 8 * s, 1);    // the K producer's arrival + the bytes
-                mbar_init(k_empty0 + 8 * s, 1);   // the commit of the stage's score products
+                mbar_init(k_empty0 + 8 * s, kTcTiles);  // each tile's commit of its score product
                 mbar_init(v_full0 + 8 * s, 1);    // the V producer's arrival + the bytes
-                mbar_init(v_empty0 + 8 * s, 1);   // the commit of the stage's value products
+                mbar_init(v_empty0 + 8 * s, kTcTiles);  // each tile's commit of its value product
             }
             for (int u = 0; u < kTcTiles; ++u) {
                 for (int q = 0; q < 2; ++q) {
@@ -841,7 +842,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             mbar_init(q_ready, kTcSoftmaxWarps);
-            mbar_init(done_bar, 1);
+            mbar_init(done_bar, kTcTiles);  // each MMA issuer, once its products are done
             misc[0] = 0;
             misc[3] = 0;
             fence_mbar_init();
@@ -930,73 +931,69 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             issued = j + 1;
         }
         if (lane == 0) misc[isv ? 5 : 3] = issued;
-    } else if (warp == kTcMmaWarp) {
-        // --------------------------------------------- the MMA issuer --
+    } else if (warp == kTcMmaWarp || warp == kTcMmaWarp1) {
+        // ------------------------------------------- the MMA issuers --
+        // one thread per query tile issues its products, so neither tile
+        // waits for the other's softmax; the two meet only in the K and V
+        // rings, whose slots free once both tiles' commits have arrived
         if (lane == 0) {
-            const uint32_t qbase = smem_u32(sm + kTcOffQ);
+            const int u = warp == kTcMmaWarp ? 0 : 1;
+            const uint32_t qt = smem_u32(sm + kTcOffQ) + u * kTcQBytes;
             const uint32_t kring = smem_u32(sm + kTcOffKRing), vring = smem_u32(sm + kTcOffVRing);
             constexpr uint32_t kIdS = tc::idesc_bf16(kTcRows, kTcKeys, false);
             constexpr uint32_t kIdO = tc::idesc_bf16(kTcRows, kHeadDim, true);
-            // O_u += P_u,t V_t for both tiles once V_t has landed and their
-            // softmax warps have written P (over the scores of stage t, in
-            // tensor memory); the commits free that buffer for the scores of
-            // stage t + 2 (o_done) and the V slot (v_empty)
-            auto value_products = [&](int t) -> bool {
+            const uint32_t tile_tm = tmem + 256 * u;
+            // O += P_t V_t once V_t has landed and the tile's softmax warps
+            // have written P (over the scores of stage t, in tensor memory);
+            // the commits free that buffer for the scores of stage t + 2
+            // (o_done) and, with the other tile's, the V slot (v_empty)
+            auto value_product = [&](int t) -> bool {
                 if (!mbar_wait_bounded(v_full0 + 8 * (t % kTcStages), (t / kTcStages) & 1, misc,
-                                       p.wait_cycles))
+                                       p.wait_cycles) ||
+                    !mbar_wait_bounded(p_full(u, t & 1), (t >> 1) & 1, misc, p.wait_cycles))
                     return false;
+                tc::fence_after();
                 const uint32_t vst = vring + (t % kTcStages) * kTcSlotBytes;
-                for (int u = 0; u < kTcTiles; ++u) {
-                    if (!mbar_wait_bounded(p_full(u, t & 1), (t >> 1) & 1, misc, p.wait_cycles))
-                        return false;
-                    tc::fence_after();
-                    const uint32_t tp = tmem + 256 * u + (t & 1) * kTcKeys;  // P: 32 columns
+                const uint32_t tp = tile_tm + (t & 1) * kTcKeys;  // P: 32 columns
 #pragma unroll
-                    for (int kk = 0; kk < kTcKeys / 16; ++kk)
-                        tc::mma_ts(tmem + 256 * u + 128, tp + 8 * kk,
-                                   tc::desc_sw128(vst + kk * 2048, kTcRegion, 1024), kIdO,
-                                   t > 0 || kk > 0);
-                    tc::commit(o_done(u, t & 1));
-                }
+                for (int kk = 0; kk < kTcKeys / 16; ++kk)
+                    tc::mma_ts(tile_tm + 128, tp + 8 * kk,
+                               tc::desc_sw128(vst + kk * 2048, kTcRegion, 1024), kIdO,
+                               t > 0 || kk > 0);
+                tc::commit(o_done(u, t & 1));
                 tc::commit(v_empty0 + 8 * (t % kTcStages));
                 return true;
             };
             bool ok = mbar_wait_bounded(q_ready, 0, misc, p.wait_cycles);
             for (int j = 0; ok && j < ntiles; ++j) {
                 const int s = j % kTcStages;
-                if (!mbar_wait_bounded(k_full0 + 8 * s, (j / kTcStages) & 1, misc, p.wait_cycles)) {
+                // the buffer holds P of stage j - 2 until its value product is done
+                if (!mbar_wait_bounded(k_full0 + 8 * s, (j / kTcStages) & 1, misc, p.wait_cycles) ||
+                    (j >= 2 && !mbar_wait_bounded(o_done(u, j & 1), ((j - 2) >> 1) & 1, misc,
+                                                  p.wait_cycles))) {
                     ok = false;
                     break;
                 }
+                tc::fence_after();
                 const uint32_t kst = kring + s * kTcSlotBytes;
-                for (int u = 0; u < kTcTiles && ok; ++u) {
-                    // the buffer holds P of stage j - 2 until its value product is done
-                    if (j >= 2 && !mbar_wait_bounded(o_done(u, j & 1), ((j - 2) >> 1) & 1, misc,
-                                                     p.wait_cycles)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after();
-                    const uint32_t qt = qbase + u * kTcQBytes;
-                    const uint32_t tS = tmem + 256 * u + (j & 1) * kTcKeys;
+                const uint32_t tS = tile_tm + (j & 1) * kTcKeys;
 #pragma unroll
-                    for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-                        const uint32_t o = (kk >> 2) * kTcRegion + 32 * (kk & 3);
-                        const uint32_t qo = (kk >> 2) * kTcQHalf + 32 * (kk & 3);
-                        tc::mma(tS, tc::desc_sw128(qt + qo, 16, 1024),
-                                tc::desc_sw128(kst + o, 16, 1024), kIdS, kk > 0);
-                    }
-                    tc::commit(s_full(u, j & 1));
+                for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+                    const uint32_t o = (kk >> 2) * kTcRegion + 32 * (kk & 3);
+                    const uint32_t qo = (kk >> 2) * kTcQHalf + 32 * (kk & 3);
+                    tc::mma(tS, tc::desc_sw128(qt + qo, 16, 1024),
+                            tc::desc_sw128(kst + o, 16, 1024), kIdS, kk > 0);
                 }
-                if (ok) tc::commit(k_empty0 + 8 * s);  // the K slot frees once both products are done
-                if (ok && j >= 1 && !value_products(j - 1)) ok = false;
+                tc::commit(s_full(u, j & 1));
+                tc::commit(k_empty0 + 8 * s);  // with the other tile's: the K slot is free
+                if (j >= 1 && !value_product(j - 1)) ok = false;
             }
-            if (ok && !value_products(ntiles - 1)) ok = false;
+            if (ok && !value_product(ntiles - 1)) ok = false;
             if (!ok) {
                 misc[0] = 1;
                 flag_error(p.err, QDEC_FLAG_TIMEOUT);
             }
-            tc::commit(done_bar);  // every MMA issued above has completed
+            tc::commit(done_bar);  // every MMA this thread issued has completed
         }
         __syncwarp();
     } else {
