@@ -970,7 +970,8 @@ def prefill_config(P: int, L: int, fp8: bool) -> dict:
     """The `config` object of a --prefill line (the same for both arms)."""
     return {"workload": f"prefill-b1-prompt{P}-{L}layer" + ("-fp8kv" if fp8 else ""),
             "batch": 1, "prompt": P, "layers": L, "heads": "32 q / 8 kv, head_dim 128, page 16",
-            "launch": f"CUDA graph: {L} x (qdec_prefill_append_rope, qdec_prefill_attn)",
+            "launch": f"CUDA graph: {L} x (qdec_prefill_append_rope, qdec_prefill_attn), the "
+                      "bf16 attention a programmatic dependent of the append",
             "l2": "not flushed (compute-bound: each layer's K/V is re-read from L2 "
                   "by its query blocks by design)"}
 
@@ -1058,7 +1059,8 @@ def run_prefill(args, dist: Dist):
                  for l in range(L)]
     c0 = cases[0]
     shape = qdec.Shape(batch=1, num_pages=c0.num_pages, max_blocks_per_seq=c0.max_blocks,
-                       max_seq_len=c0.max_blocks * 16)
+                       max_seq_len=c0.max_blocks * 16,
+                       launch_flags=0 if args.no_overlap else qdec.QDEC_LAUNCH_OVERLAP_PREVIOUS)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     q_rot = torch.empty((P, 32, 128), dtype=torch.float32, device="cuda")
     out = torch.empty((L, P, 32, 128), dtype=torch.bfloat16, device="cuda")

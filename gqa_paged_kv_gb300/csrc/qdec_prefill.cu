@@ -786,6 +786,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     volatile int *pmask = misc + 6;
     const int g = blockIdx.x % p.Hkv;
     const int unit = blockIdx.x / p.Hkv;
+    if (p.pdl && tid == 0) launch_dependents();
 
     // ---- which (sequence, block) this CTA takes: units enumerate every
     // sequence's blocks from its last (most keys) to its first
@@ -885,6 +886,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             return pg < npg ? p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg] : -1;
         };
         int cur = lookup(0), nxt = lookup(1);
+        // the chunk's keys and values were appended by the kernel before
+        if (p.pdl) grid_dependency_wait();
         for (int j = 0; j < ntiles; ++j) {
             const int s = j % kTcStages;
             if (j > 0 && (j * kTcPagesPerStage) % 32 == 0) {
@@ -1014,6 +1017,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             return ok;
         };
+        if (p.pdl) grid_dependency_wait();  // q_rot, the pool and out of the kernel before
         {
             // Q of the tile, scaled to log2 units, as bf16: warp w converts
             // rows w % 4, w % 4 + 4, ..., lane l taking dims 4 l .. 4 l + 3 of
@@ -1243,11 +1247,19 @@ cudaError_t launch_prefill_attention_tc(const Params &p, const CUtensorMap &regi
             g_pf_tc_smem_set[dev] = true;
         }
     }
-    // units: at most T / 32 + B blocks of 32 chunk rows, times the KV heads
+    // units: at most T / 64 + B blocks of 64 chunk rows, times the KV heads
     const int64_t units = (static_cast<int64_t>(p.T) + kTcTok - 1) / kTcTok + p.B;
-    prefill_attention_tc_kernel<<<static_cast<unsigned>(units * p.Hkv), kTcThreads, kTcSmemBytes,
-                                  s>>>(region_map, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(units * p.Hkv));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = kTcSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = p.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, prefill_attention_tc_kernel, region_map, p);
 }
 
 cudaError_t launch_prefill_attention(const Params &p, const CUtensorMap &kv_map, bool fp8,

@@ -333,3 +333,30 @@ def test_prefill_full_prompt_sampled(kv):
     else:
         ref_out, _ = oracle.attention(pool, bt_r, lens, qr, 1 / math.sqrt(128))
     parity.assert_out_close(out[torch.as_tensor(rows, device="cuda")], ref_out)
+
+
+def test_prefill_attention_as_a_programmatic_dependent_gives_the_same_bits():
+    """With QDEC_LAUNCH_OVERLAP_PREVIOUS the tensor-core attention may start
+    while the append before it finishes, waiting for it before it reads q_rot
+    or the pool: several layers launched that way on one stream (each
+    layer's append, then its attention) give the serial launches' bits."""
+    q = parity.qdec()
+    seq_lens, chunks = [300, 17, 1000, 2048], [20, 17, 200, 2048]
+    layers = [wl.prefill_case(seq_lens, chunks, seed=40 + l) for l in range(3)]
+    T = layers[0].q.shape[0]
+    outs = []
+    for flags in (0, q.QDEC_LAUNCH_OVERLAP_PREVIOUS):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        q_rot = torch.empty((T, 32, 128), dtype=torch.float32, device="cuda")
+        out = torch.full((3, T, 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        for l, c in enumerate(layers):
+            pool = c.pool.clone()
+            shape = _shape(c, len(seq_lens), flags)
+            q.qdec_prefill_append_rope(shape, c.q, c.k, c.v, c.w_q, c.w_k, c.positions,
+                                       c.qo_indptr, c.seq_lens, c.block_table, pool, q_rot, err)
+            q.qdec_prefill_attn(shape, q_rot, c.qo_indptr, c.seq_lens, c.block_table, pool,
+                                out[l], err)
+        st, fl = q.qdec_check_error(err)
+        assert st == 0 and fl == 0, (st, fl)
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
