@@ -383,6 +383,27 @@ qdec_status encode_pool_map_fp8(CUtensorMap *map, const qdec_shape *s, const voi
     return r == CUDA_SUCCESS ? QDEC_OK : QDEC_ERR_CUDA;
 }
 
+// The FP8 pool's 4-D view with a box of one (page, plane): 16 tokens x 128
+// codes, 2 KiB (the tensor-core prefill brings K and V separately).
+qdec_status encode_pool_plane_map_fp8(CUtensorMap *map, const qdec_shape *s, const void *pool8) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return QDEC_ERR_CUDA;
+    const cuuint64_t plane = static_cast<cuuint64_t>(qdec::kFp8PlaneBytes);
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(qdec::kHeadDim),
+                                static_cast<cuuint64_t>(qdec::kPageSize), 2,
+                                static_cast<cuuint64_t>(s->num_pages) * 2 * s->num_kv_heads};
+    const cuuint64_t strides[3] = {qdec::kHeadDim,
+                                   static_cast<cuuint64_t>(s->num_kv_heads) * plane, plane};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(qdec::kHeadDim),
+                               static_cast<cuuint32_t>(qdec::kPageSize), 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(pool8), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? QDEC_OK : QDEC_ERR_CUDA;
+}
+
 // A row-major bf16 matrix [rows][cols] (row stride `stride` elements) as a
 // 2-D tensor with box_rows x 64 boxes, 128-byte swizzled.
 qdec_status encode_rows_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols,
@@ -622,12 +643,9 @@ qdec_status prefill_attn_impl(const qdec_shape *shape, int32_t num_tokens, const
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
     p.err = err_flag;
     CUtensorMap map;
-    if (!pool.fp8) {  // bf16 pool: the tensor-core kernel
-        if ((st = encode_pool_region_map(&map, shape, pool.data)) != QDEC_OK) return st;
-        return cuda_status(
-            qdec::launch_prefill_attention_tc(p, map, static_cast<cudaStream_t>(stream)));
-    }
-    if ((st = encode_map(&map, shape, pool)) != QDEC_OK) return st;
+    if ((st = pool.fp8 ? encode_pool_plane_map_fp8(&map, shape, pool.data)
+                       : encode_pool_region_map(&map, shape, pool.data)) != QDEC_OK)
+        return st;
     return cuda_status(
         qdec::launch_prefill_attention(p, map, pool.fp8, static_cast<cudaStream_t>(stream)));
 }

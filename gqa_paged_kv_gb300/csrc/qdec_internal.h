@@ -121,15 +121,12 @@ cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, AttnMod
 cudaError_t launch_merge(const Params &p, cudaStream_t s);
 
 // Chunked prefill (qdec_prefill.cu): steps 1-3 for every chunk row, and the
-// causal paged attention of the chunk (kv_map: the pool's page-tile map, of
-// the FP8 pool when fp8).
+// causal paged attention of the chunk on the 5th-generation tensor core
+// (kv_map: for a bf16 pool one (page, plane, half of D) region per box, for
+// an FP8 pool one (page, plane) per box).
 cudaError_t launch_prefill_append(const Params &p, bool fp8, cudaStream_t s);
 cudaError_t launch_prefill_attention(const Params &p, const CUtensorMap &kv_map, bool fp8,
                                      cudaStream_t s);
-// The same attention over a bf16 pool on the 5th-generation tensor core;
-// region_map views the pool with one (page, plane, half of D) region per box.
-cudaError_t launch_prefill_attention_tc(const Params &p, const CUtensorMap &region_map,
-                                        cudaStream_t s);
 
 // The merged QKV projection fused with steps 1-3 (qdec_qkv.cu): the weight
 // comes packed (qdec_qkv_pack_weights), x_map views x [B][hidden] with boxes

@@ -9,25 +9,18 @@
 //   key rows, then bf16(k_rot) and v into slot L_b - n_b + j of the pool.
 //   One CTA per token (the angles taken once), one warp per KV head.
 //
-// prefill_attention_kernel -- causal paged attention of the chunk (article
+// prefill_attention_tc_kernel -- causal paged attention of the chunk (article
 //   "扔掉 vLLM！从零构建 Qwen3-8B 推理引擎" (news.rkmt.cn), section 4.4.1:
 //   FlashAttention-2 prefill, the queries in blocks that each see only the
-//   keys at or before them, never forming the whole score matrix).  One CTA
-//   per (sequence, KV head, block of 16 chunk tokens), the blocks with the
-//   most keys first.  A producer warp streams the sequence's page tiles (K
-//   and V of one page and KV head, 8 KiB, one TMA box) up to the block's last
-//   query into a ring; each of the four consumer warps owns one query head
-//   of the group for the block's 16 tokens and, per tile, forms S = Q K^T
-//   with mma.sync (q as bf16 hi + lo, ~16-bit mantissa), masks keys after
-//   each query, keeps the online softmax in fp32 (log2 units) and adds
-//   P V with P taken straight from the score accumulators as bf16.
+//   keys at or before them, never forming the whole score matrix) on the
+//   5th-generation tensor core; see the kernel's own comment below.
 //
 // Over an FP8 (E4M3) pool the append stores codes, each row element divided
 // by its (page, plane, head) scale in fp32 and rounded to nearest-even with
-// saturation (the decode step's rule), and the attention brings each page
-// tile as codes plus its two scales, converts the codes to bf16 in shared
-// memory (exact: every E4M3 value is a bf16 value), multiplies the scores by
-// the K scale and folds the V scale into the weights of the value product.
+// saturation (the decode step's rule), and the attention converts each
+// stage's codes to f16 in shared memory (exact: every E4M3 value is an f16
+// value) for f16 tensor-core products, multiplies the scores by the K scale
+// of their page and folds the V scale into the weights of the value product.
 #include "qdec_internal.h"
 #include "qdec_ptx.cuh"
 #include "qdec_ff.cuh"
@@ -44,28 +37,6 @@ namespace qdec {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kPfRows = 16;                 // chunk tokens per work unit (one m16 tile)
-constexpr int kPfStages = 8;                // page tiles in flight per CTA
-// shared memory: [ring of page tiles][FP8: scale windows of every slot, two
-// converted bf16 tiles][full[8], empty[8], slot_ok[8], the abort flag, the unit]
-template <bool kFp8>
-__host__ __device__ constexpr int pf_ring_bytes() {
-    return kPfStages * (kFp8 ? kFp8TileBytes : kTileBytes);
-}
-template <bool kFp8>
-__host__ __device__ constexpr int pf_extra_bytes() {
-    return kFp8 ? kPfStages * kFp8SlotExtra + 2 * kTileBytes : 0;
-}
-// the tail: full and empty barriers (128 B), slot_ok (32 B), misc (16 B, then
-// 16 B unused), the FP8 conversion barriers (32 B), the slot scale indices
-// (32 B); plus up to 1 KiB lost aligning the base
-constexpr int kPfTailBytes = 2 * kPfStages * 8 + kPfStages * 4 + 32 + 32 + kPfStages * 4;
-static_assert(kPfTailBytes == 256, "tail layout");
-template <bool kFp8>
-__host__ __device__ constexpr int pf_smem_bytes() {
-    return pf_ring_bytes<kFp8>() + pf_extra_bytes<kFp8>() + kPfTailBytes + 1024;
-}
-
 __device__ __forceinline__ void flag_error(int32_t *err, int bits) {
     if (err) atomicOr(err, bits);
 }
@@ -224,449 +195,12 @@ __global__ void __launch_bounds__(kPfAppendThreads) prefill_append_kernel(
     }
 }
 
-// --------------------------------------------------------------- attention --
-// One page tile (K and V of one page and KV head, 8 KiB): the pool's 5-D
-// tensor map (64 dims, 16 tokens, 2 halves of D, K/V plane, page*2*Hkv +
-// head) lands it as [plane][half][token][64 dims], 128-byte rows swizzled by
-// (token % 8).
-__device__ __forceinline__ void tma_load_page_tile(uint32_t dst, const CUtensorMap *map,
-                                                   int plane_row, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %2, %2, %2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(plane_row), "r"(bar)
-        : "memory");
-}
-
-// One FP8 page tile: [plane][token][128 bytes of D], 4 KiB, 128-byte
-// swizzled rows (the pool's 4-D tensor map: bytes of D, token, plane,
-// page*2*Hkv + head).
-__device__ __forceinline__ void tma_load_page_tile_fp8(uint32_t dst, const CUtensorMap *map,
-                                                       int plane_row, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %2, %2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(plane_row), "r"(bar)
-        : "memory");
-}
-
-// Two E4M3 codes (low byte first) as a bf16 pair: exact (every E4M3 value
-// is a bf16 value; NaN stays NaN).
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_codes) {
+// Two E4M3 codes (the low byte first) as an f16 pair: exact (every E4M3
+// value is an f16 value; NaN stays NaN).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
     const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
         static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
-    const float lo = __half2float(__half(__half_raw{h.x}));
-    const float hi = __half2float(__half(__half_raw{h.y}));
-    return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xffff0000u);
-}
-
-template <bool kFp8>
-__global__ void __launch_bounds__(kThreads, 2)
-    prefill_attention_kernel(const __grid_constant__ CUtensorMap kv_map,
-                             const __grid_constant__ Params p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    constexpr int kSlot = kFp8 ? kFp8TileBytes : kTileBytes;  // ring slot
-    // FP8: after the ring, the scale windows of every slot, then two bf16
-    // tiles the codes are converted into
-    uint8_t *extra = sm + pf_ring_bytes<kFp8>();
-    uint8_t *conv = extra + kPfStages * kFp8SlotExtra;
-    uint8_t *tail = extra + pf_extra_bytes<kFp8>();
-    const uint32_t full0 = smem_u32(tail);
-    const uint32_t empty0 = full0 + kPfStages * 8;
-    volatile int *slot_ok = reinterpret_cast<volatile int *>(tail + 2 * kPfStages * 8);
-    volatile int *misc = reinterpret_cast<volatile int *>(tail + 2 * kPfStages * 8 + kPfStages * 4);
-    // misc: [0] abort, [1] sequence, [2] query block, [3] pages issued;
-    // FP8: [4] conv_full[2], conv_empty[2] barriers (8-byte aligned), then
-    // the scale index of every slot
-    const uint32_t convb0 = smem_u32(tail + 2 * kPfStages * 8 + kPfStages * 4 + 32);
-    volatile int *slot_si =
-        reinterpret_cast<volatile int *>(tail + 2 * kPfStages * 8 + kPfStages * 4 + 64);
-    const int g = blockIdx.x % p.Hkv;
-    const int unit = blockIdx.x / p.Hkv;
-
-    // ---- which (sequence, block) this CTA takes: units enumerate every
-    // sequence's blocks from its last (most keys) to its first
-    if (warp == 0) {
-        const int per = (p.B + 31) / 32;
-        int cnt = 0;
-        for (int i = 0; i < per; ++i) {
-            const int b = lane * per + i;
-            int n, L;
-            if (b < p.B && chunk_ok(p, b, n, L)) cnt += (n + kPfRows - 1) / kPfRows;
-        }
-        int incl = cnt;  // inclusive prefix over the lanes
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += v;
-        }
-        const int excl = incl - cnt;
-        if (lane == 0) misc[1] = -1;
-        __syncwarp();
-        if (unit >= excl && unit < incl) {
-            int k = unit - excl;
-            for (int i = 0; i < per; ++i) {
-                const int b = lane * per + i;
-                int n, L;
-                if (b >= p.B || !chunk_ok(p, b, n, L)) continue;
-                const int nb = (n + kPfRows - 1) / kPfRows;
-                if (k < nb) {
-                    misc[1] = b;
-                    misc[2] = nb - 1 - k;
-                    break;
-                }
-                k -= nb;
-            }
-        }
-        if (blockIdx.x == 0) {  // report malformed chunks once
-            for (int b = lane; b < p.B; b += 32) {
-                int n, L;
-                if (!chunk_ok(p, b, n, L)) flag_error(p.err, QDEC_FLAG_BAD_SEQLEN);
-            }
-        }
-        if (tid == 0) {
-            for (int s = 0; s < kPfStages; ++s) {
-                mbar_init(full0 + 8 * s, 1);
-                mbar_init(empty0 + 8 * s, kConsumerWarps);  // every warp reads every tile
-            }
-            if (kFp8)
-                for (int i = 0; i < 4; ++i) mbar_init(convb0 + 8 * i, kConsumerWarps);
-            misc[0] = 0;
-            misc[3] = 0;
-            misc[5] = 0;
-            fence_mbar_init();
-        }
-    }
-    __syncthreads();
-    const int b = misc[1];
-    if (b < 0) return;  // no unit for this CTA (the grid is an upper bound)
-    const int qb = misc[2];
-    int n, L;
-    chunk_ok(p, b, n, L);
-    const int row0 = p.qo_indptr[b] + qb * kPfRows;             // first packed row
-    const int nrows = min(kPfRows, n - qb * kPfRows);           // rows of this block
-    const int t0 = L - n + qb * kPfRows;                        // token index of row 0
-    const int npages = (t0 + nrows - 1) / kPageSize + 1;        // pages up to the last query
-
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------ TMA producer --
-        uint32_t i = 0;
-        bool stop = false;
-        for (int base = 0; base < npages && !stop; base += 32) {
-            int page = -1;
-            if (base + lane < npages)
-                page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + base + lane];
-            const int cnt = min(32, npages - base);
-            for (int j = 0; j < cnt; ++j, ++i) {
-                const int pj = __shfl_sync(kFull, page, j);
-                if (lane == 0) {
-                    const int slot = i % kPfStages;
-                    const uint32_t full = full0 + 8 * slot;
-                    if (misc[0]) {
-                        stop = true;
-                    } else if (i >= static_cast<uint32_t>(kPfStages) &&
-                               !mbar_wait_bounded(empty0 + 8 * slot, ((i / kPfStages) - 1) & 1,
-                                                  misc, p.wait_cycles)) {
-                        misc[0] = 1;
-                        flag_error(p.err, QDEC_FLAG_TIMEOUT);
-                        stop = true;
-                    } else if (p.withhold_first && i == 0) {
-                        // test hook: this tile's barrier phase never completes
-                    } else if (pj >= 0 && pj < p.num_pages) {
-                        slot_ok[slot] = 1;
-                        if constexpr (kFp8) {
-                            // the tile and the two 16-byte windows of kv_scale
-                            // holding its K and V scales (Hkv even: a window
-                            // never straddles pages)
-                            const int64_t si = static_cast<int64_t>(pj) * 2 * p.Hkv + g;
-                            slot_si[slot] = static_cast<int>(((si & 3) | (((si + p.Hkv) & 3) << 2)));
-                            const uint32_t win = smem_u32(extra + slot * kFp8SlotExtra);
-                            mbar_arrive_expect_tx(full, kFp8TileBytes + kFp8SlotExtra);
-                            tma_load_page_tile_fp8(smem_u32(sm + slot * kSlot), &kv_map,
-                                                   pj * 2 * p.Hkv + g, full);
-                            bulk_load(win, p.kv_scale + (si & ~3ll), kScaleWindowBytes, full);
-                            bulk_load(win + kScaleWindowBytes, p.kv_scale + ((si + p.Hkv) & ~3ll),
-                                      kScaleWindowBytes, full);
-                        } else {
-                            mbar_arrive_expect_tx(full, kTileBytes);
-                            tma_load_page_tile(smem_u32(sm + slot * kSlot), &kv_map,
-                                               pj * 2 * p.Hkv + g, full);
-                        }
-                    } else {
-                        slot_ok[slot] = 0;
-                        flag_error(p.err, QDEC_FLAG_BAD_PAGE);
-                        mbar_arrive(full);
-                    }
-                }
-                stop = __shfl_sync(kFull, stop, 0);
-                if (stop) break;
-            }
-        }
-        if (lane == 0) misc[3] = static_cast<int>(i);
-    } else {
-        // ------------------------------------------- consumer warps --
-        const int h = g * kGroup + warp;
-        const int gq = lane >> 2, tq = lane & 3;  // fragment row group, column pair
-        // Q fragments (A of m16n8k16, 16 tokens x 128 dims in 8 k-steps),
-        // scaled to log2 units, as bf16 hi + lo
-        uint32_t qh[8][4], ql[8][4];
-        {
-            const float *q0 = p.q_rot_in + (static_cast<int64_t>(row0 + gq) * p.Hq + h) * kHeadDim;
-            const float *q1 = q0 + 8 * static_cast<int64_t>(p.Hq) * kHeadDim;
-            const bool v0 = gq < nrows, v1 = gq + 8 < nrows;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float *src = (e & 1) ? q1 : q0;
-                    const bool valid = (e & 1) ? v1 : v0;
-                    const int col = 16 * kk + 2 * tq + ((e >> 1) << 3);
-                    float2 x = valid ? *reinterpret_cast<const float2 *>(src + col)
-                                     : make_float2(0.f, 0.f);
-                    x.x *= p.qscale;
-                    x.y *= p.qscale;
-                    const __nv_bfloat16 hx = __float2bfloat16_rn(x.x), hy = __float2bfloat16_rn(x.y);
-                    qh[kk][e] = static_cast<uint32_t>(__bfloat16_as_ushort(hx)) |
-                                (static_cast<uint32_t>(__bfloat16_as_ushort(hy)) << 16);
-                    ql[kk][e] = pack_bf16x2(x.x - __bfloat162float(hx), x.y - __bfloat162float(hy));
-                }
-            }
-        }
-        // the last key each of this thread's two rows may see (causal, and
-        // never past the sequence)
-        const int lim0 = min(t0 + gq, L - 1), lim1 = min(t0 + gq + 8, L - 1);
-        float o[16][4];
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        const int mi = lane >> 3, r8 = lane & 7;
-        // this lane's matrix-load offsets within a tile: K (keys (mi >> 1) * 8
-        // + r8, dim chunk 2 kk + (mi & 1)) and V (keys (mi & 1) * 8 + r8, dim
-        // chunk 2 pr + (mi >> 1)), for chunk pairs j = kk, pr mod 4 (the
-        // halves of D add 2 KiB)
-        uint32_t koff[4], voff[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int kt = (mi >> 1) * 8 + r8, vt = (mi & 1) * 8 + r8;
-            koff[j] = kt * 128 + (((2 * j + (mi & 1)) ^ (kt & 7)) << 4);
-            voff[j] = kPlaneBytes + vt * 128 + (((2 * j + (mi >> 1)) ^ (vt & 7)) << 4);
-        }
-        bool aborted = false;
-        for (int pg = 0; pg < npages; ++pg) {
-            const int slot = pg % kPfStages;
-            if (!mbar_wait_bounded(full0 + 8 * slot, (pg / kPfStages) & 1, misc, p.wait_cycles)) {
-                if (lane == 0) {
-                    misc[0] = 1;
-                    flag_error(p.err, QDEC_FLAG_TIMEOUT);
-                }
-                aborted = true;
-                break;
-            }
-            const bool ok = slot_ok[slot];
-            uint32_t tile = smem_u32(sm + slot * kSlot);
-            float sk = 1.f, sv = 1.f;  // FP8: the tile's K and V scales
-            if constexpr (kFp8) {
-                // convert this warp's quarter of the codes into buffer pg & 1
-                // (once its previous tile has been read by every warp), hand
-                // the ring slot back, wait for the other quarters
-                const int cb = pg & 1;
-                if (pg >= 2 && !mbar_wait_bounded(convb0 + 8 * (2 + cb), ((pg >> 1) - 1) & 1,
-                                                  misc, p.wait_cycles)) {
-                    if (lane == 0) {
-                        misc[0] = 1;
-                        flag_error(p.err, QDEC_FLAG_TIMEOUT);
-                    }
-                    aborted = true;
-                    break;
-                }
-                uint8_t *cvt = conv + cb * kTileBytes;
-                if (ok) {
-                    const int si = slot_si[slot];
-                    const float *win = reinterpret_cast<const float *>(extra + slot * kFp8SlotExtra);
-                    sk = win[si & 3];
-                    sv = win[4 + (si >> 2)];
-#pragma unroll
-                    for (int it = 0; it < 2; ++it) {
-                        // item: plane, token, 16 codes of dims 16 c .. 16 c + 15
-                        const int item = (warp * 32 + lane) + 128 * it;
-                        const int plane = item >> 7, tok = (item >> 3) & 15, c = item & 7;
-                        const uint4 codes = *reinterpret_cast<const uint4 *>(
-                            sm + slot * kSlot + plane * kFp8PlaneBytes + tok * 128 +
-                            ((c ^ (tok & 7)) << 4));
-                        const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
-                        uint32_t bf[8];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            bf[2 * q] = e4m3x2_to_bf16x2(w[q]);
-                            bf[2 * q + 1] = e4m3x2_to_bf16x2(w[q] >> 16);
-                        }
-                        // bf16 chunks 2c, 2c + 1 of the token: half c / 4
-                        uint8_t *dst = cvt + plane * kPlaneBytes + (c >> 2) * kTileHalfBytes + tok * 128;
-                        *reinterpret_cast<uint4 *>(dst + ((((2 * c) & 7) ^ (tok & 7)) << 4)) =
-                            make_uint4(bf[0], bf[1], bf[2], bf[3]);
-                        *reinterpret_cast<uint4 *>(dst + ((((2 * c + 1) & 7) ^ (tok & 7)) << 4)) =
-                            make_uint4(bf[4], bf[5], bf[6], bf[7]);
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(empty0 + 8 * slot);     // the codes are no longer needed
-                    mbar_arrive(convb0 + 8 * cb);       // this warp's quarter is in place
-                }
-                if (!mbar_wait_bounded(convb0 + 8 * cb, (pg >> 1) & 1, misc, p.wait_cycles)) {
-                    if (lane == 0) {
-                        misc[0] = 1;
-                        flag_error(p.err, QDEC_FLAG_TIMEOUT);
-                    }
-                    aborted = true;
-                    break;
-                }
-                tile = smem_u32(cvt);
-            }
-            if (ok) {
-                // ---- S = Q K^T: 16 tokens x 16 keys (two n-tiles of 8 keys)
-                // (the hi and lo products in separate accumulators: four
-                // independent chains of 8 MMAs instead of two of 16)
-                float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                float sl[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    uint32_t kb[4];
-                    // matrices: keys 0-7 / 8-15 (mi >> 1) x dims 16kk.. / 16kk+8.. (mi & 1)
-                    ldmatrix_x4(kb, tile + (kk >> 2) * kTileHalfBytes + koff[kk & 3]);
-                    mma_bf16(s[0], qh[kk], kb[0], kb[1]);
-                    mma_bf16(s[1], qh[kk], kb[2], kb[3]);
-                    mma_bf16(sl[0], ql[kk], kb[0], kb[1]);
-                    mma_bf16(sl[1], ql[kk], kb[2], kb[3]);
-                }
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) s[j][e] = (s[j][e] + sl[j][e]) * sk;
-                // ---- causal mask: key 16 pg + 8 j + 2 tq + e against each
-                // row's limit (only tiles that reach past a limit need it)
-                const int kbase = pg * kPageSize + 2 * tq;
-                if (pg * kPageSize + kPageSize - 1 > lim0) {
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int key = kbase + 8 * j + e;
-                            if (key > lim0) s[j][e] = -INFINITY;
-                            if (key > lim1) s[j][2 + e] = -INFINITY;
-                        }
-                    }
-                }
-                // ---- online softmax (log2 units), rows gq and gq + 8.  The
-                // running maximum is kept until a tile's maximum exceeds it
-                // by more than 2^8 (weights then stay below 256, exact enough
-                // in bf16 and fp32), so most tiles rescale nothing.
-                float mx0 = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-                float mx1 = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-#pragma unroll
-                for (int off = 1; off < 4; off <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, off));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, off));
-                }
-                // a row that has seen no key yet keeps m = -inf, weights 0
-                if (mx0 > m0 + 8.f || mx1 > m1 + 8.f) {
-                    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-                    const float a0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
-                    const float a1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
-                    l0 *= a0;
-                    l1 *= a1;
-                    m0 = n0;
-                    m1 = n1;
-#pragma unroll
-                    for (int nt = 0; nt < 16; ++nt) {
-                        o[nt][0] *= a0;
-                        o[nt][1] *= a0;
-                        o[nt][2] *= a1;
-                        o[nt][3] *= a1;
-                    }
-                }
-                float pw[2][4];
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        pw[j][e] = m0 == -INFINITY ? 0.f : exp2f(s[j][e] - m0);
-                        pw[j][2 + e] = m1 == -INFINITY ? 0.f : exp2f(s[j][2 + e] - m1);
-                    }
-                }
-                l0 += pw[0][0] + pw[0][1] + pw[1][0] + pw[1][1];
-                l1 += pw[0][2] + pw[0][3] + pw[1][2] + pw[1][3];
-                // ---- O += P V: P (16 tokens x 16 keys) from the score
-                // accumulators as the A operand; V rows past the sequence
-                // (possibly not finite) are zeroed in the B fragments
-                // (FP8: the V scale folded into the weights)
-                uint32_t pa[4];
-                pa[0] = pack_bf16x2(pw[0][0] * sv, pw[0][1] * sv);
-                pa[1] = pack_bf16x2(pw[0][2] * sv, pw[0][3] * sv);
-                pa[2] = pack_bf16x2(pw[1][0] * sv, pw[1][1] * sv);
-                pa[3] = pack_bf16x2(pw[1][2] * sv, pw[1][3] * sv);
-                const int ntok = min(kPageSize, L - pg * kPageSize);  // keys of this page in the sequence
-                // this thread's B elements hold keys 2 tq, 2 tq + 1 (b0) and +8 (b1)
-                const uint32_t keep0 = (2 * tq < ntok ? 0x0000ffffu : 0u) |
-                                       (2 * tq + 1 < ntok ? 0xffff0000u : 0u);
-                const uint32_t keep1 = (2 * tq + 8 < ntok ? 0x0000ffffu : 0u) |
-                                       (2 * tq + 9 < ntok ? 0xffff0000u : 0u);
-#pragma unroll
-                for (int pr = 0; pr < 8; ++pr) {
-                    uint32_t vb[4];
-                    // matrices: keys 0-7 / 8-15 (mi & 1) x dims 16pr.. / 16pr+8.. (mi >> 1)
-                    ldmatrix_x4_trans(vb, tile + (pr >> 2) * kTileHalfBytes + voff[pr & 3]);
-                    if (ntok < kPageSize) {  // the sequence's last page
-                        vb[0] &= keep0;
-                        vb[1] &= keep1;
-                        vb[2] &= keep0;
-                        vb[3] &= keep1;
-                    }
-                    mma_bf16(o[2 * pr], pa, vb[0], vb[1]);
-                    mma_bf16(o[2 * pr + 1], pa, vb[2], vb[3]);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) {
-                if (kFp8)
-                    mbar_arrive(convb0 + 8 * (2 + (pg & 1)));  // buffer pg & 1 read
-                else
-                    mbar_arrive(empty0 + 8 * slot);
-            }
-        }
-        // ---- normalise and write the block's rows of head h
-#pragma unroll
-        for (int off = 1; off < 4; off <<= 1) {
-            l0 += __shfl_xor_sync(kFull, l0, off);
-            l1 += __shfl_xor_sync(kFull, l1, off);
-        }
-        if (!aborted && !misc[0]) {
-            const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
-            __nv_bfloat16 *d0 = p.out + (static_cast<int64_t>(row0 + gq) * p.Hq + h) * kHeadDim;
-            __nv_bfloat16 *d1 = d0 + 8 * static_cast<int64_t>(p.Hq) * kHeadDim;
-#pragma unroll
-            for (int nt = 0; nt < 16; ++nt) {
-                const int col = 8 * nt + 2 * tq;
-                if (gq < nrows)
-                    *reinterpret_cast<uint32_t *>(d0 + col) = pack_bf16x2(o[nt][0] * i0, o[nt][1] * i0);
-                if (gq + 8 < nrows)
-                    *reinterpret_cast<uint32_t *>(d1 + col) = pack_bf16x2(o[nt][2] * i1, o[nt][3] * i1);
-            }
-        }
-    }
-    __syncthreads();
-    // a wait that gave up may leave copies in flight: let them land (bounded)
-    if (tid == 0 && misc[0]) {
-        const uint32_t issued = static_cast<uint32_t>(misc[3]);
-        const uint32_t first = issued > static_cast<uint32_t>(kPfStages) ? issued - kPfStages : 0;
-        volatile int never = 0;
-        for (uint32_t t = first; t < issued; ++t)
-            mbar_wait_bounded(full0 + 8 * (t % kPfStages), (t / kPfStages) & 1, &never,
-                              p.wait_cycles);
-    }
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
 // ------------------------------------- attention on the 5th-gen tensor core --
@@ -698,28 +232,22 @@ __global__ void __launch_bounds__(kThreads, 2)
 // product reads them.  The epilogue reads O out of tensor memory, divides by
 // the row sum and stores the row.  Every wait is bounded; the decisions that
 // lead to warp-collective tensor-memory loads and stores are warp-uniform.
+// Over an FP8 pool each producer brings its plane's codes into a staging
+// ring (one 2 KiB box per page) and converts them, exactly, to f16 into its
+// ring slot, zeroing the rows of keys past the sequence; Q and P are then f16
+// and the products of kind f16; the K scale of a key's page multiplies its
+// score and the V scale its weight in P (the row sum keeps the unscaled
+// weights).
 constexpr int kTcTiles = 2;                                // query tiles per CTA
 constexpr int kTcTileTok = 32;                             // chunk tokens per tile
 constexpr int kTcTok = kTcTiles * kTcTileTok;              // chunk tokens per CTA
 constexpr int kTcRows = kTcTileTok * kGroup;               // M = 128 rows per tile
 constexpr int kTcKeys = 64;                                // keys per stage
 constexpr int kTcPagesPerStage = kTcKeys / kPageSize;      // 4
-constexpr int kTcStages = 4;
-constexpr int kTcRegion = kTcKeys * 128;                   // [64 keys][64 dims] bf16, 8 KiB
+constexpr int kTcRegion = kTcKeys * 128;                   // [64 keys][64 dims] 16-bit, 8 KiB
 constexpr int kTcSlotBytes = 2 * kTcRegion;                // K (or V): dims 0-63, dims 64-127
-constexpr int kTcQHalf = kTcRows * 128;                    // [128 rows][64 dims] bf16, 16 KiB
+constexpr int kTcQHalf = kTcRows * 128;                    // [128 rows][64 dims] 16-bit, 16 KiB
 constexpr int kTcQBytes = 2 * kTcQHalf;                    // one tile's Q
-constexpr int kTcOffQ = 0;                                 // Q of tile u at u * kTcQBytes
-constexpr int kTcOffKRing = kTcOffQ + kTcTiles * kTcQBytes;
-constexpr int kTcOffVRing = kTcOffKRing + kTcStages * kTcSlotBytes;
-constexpr int kTcOffTail = kTcOffVRing + kTcStages * kTcSlotBytes;
-// tail: barriers k_full[S], k_empty[S], v_full[S], v_empty[S]; per tile
-// s_full[2], (unused)[2], p_full[2], o_done[2]; q_ready, done; then ints:
-// abort, sequence, block, K stages issued, tensor-memory address, V stages
-// issued, and the mask of pages brought into every V slot
-constexpr int kTcBars = 4 * kTcStages + kTcTiles * 8 + 2;
-constexpr int kTcTailBytes = kTcBars * 8 + (6 + kTcStages) * 4;
-constexpr int kTcSmemBytes = kTcOffTail + kTcTailBytes + 1024;
 constexpr int kTcSoftmaxWarps = 4 * kTcTiles;
 constexpr int kTcProducerWarp = kTcSoftmaxWarps;           // K stages
 constexpr int kTcMmaWarp = kTcSoftmaxWarps + 1;
@@ -728,14 +256,47 @@ constexpr int kTcMmaWarp1 = kTcSoftmaxWarps + 3;           // tile 1's products 
 constexpr int kTcThreads = (kTcSoftmaxWarps + 4) * 32;
 // tile u: S buffers at columns 256 u + {0, 64}, O at 256 u + 128
 constexpr uint32_t kTcTmemCols = 256 * kTcTiles;
-static_assert(kTcSmemBytes <= 227 * 1024, "one CTA per SM");
-static_assert(kTcOffKRing % 1024 == 0 && kTcOffVRing % 1024 == 0,
-              "swizzled operands start on 1024-byte boundaries");
 static_assert(kTcTmemCols <= 512, "tensor memory");
+// FP8 pool: the K and V scales of a stage's four pages, written by the V
+// producer when it issues the stage's copies and read by the softmax warps
+// once the stage's V slot is full; kept per stage in rings deep enough that
+// an entry is rewritten only after its softmax has read it (the V producer
+// issues stage j + 8 only after converting stage j + 5, i.e. after the value
+// products of stage j + 2, i.e. after every softmax of stage j + 2)
+constexpr int kTcKScaleRing = 8, kTcVScaleRing = 8;
 
-// One (page, plane, half of D) region of a page: 16 tokens x 64 dims, 2 KiB,
-// with the pool's region map (5-D: 64 dims, token, half, plane, page*2*Hkv +
-// head; box 64 x 16 x 1 x 1 x 1).
+// Shared-memory layout of the tensor-core prefill, per pool type: Q of both
+// tiles, the K and V rings of 16-bit slots, and for an FP8 pool the staging
+// rings of codes (per plane, a stage is four 2 KiB page boxes) and the scale
+// rings; then the barriers and a few ints.
+template <bool kFp8>
+struct TcLayout {
+    static constexpr int kStages = kFp8 ? 3 : 4;           // K and V ring depth
+    static constexpr int kStg = kFp8 ? 3 : 0;              // FP8 staging slots per plane
+    static constexpr int kStgSlot = kTcPagesPerStage * kFp8PlaneBytes;  // 8 KiB
+    static constexpr int kOffQ = 0;                        // Q of tile u at u * kTcQBytes
+    static constexpr int kOffKRing = kOffQ + kTcTiles * kTcQBytes;
+    static constexpr int kOffVRing = kOffKRing + kStages * kTcSlotBytes;
+    static constexpr int kOffStg = kOffVRing + kStages * kTcSlotBytes;  // [plane][kStg] slots
+    static constexpr int kOffScale = kOffStg + 2 * kStg * kStgSlot;     // K [16][4], V [8][4] floats
+    static constexpr int kScaleBytes = kFp8 ? (kTcKScaleRing + kTcVScaleRing) * 4 * 4 : 0;
+    static constexpr int kOffTail = kOffScale + kScaleBytes;
+    // tail: barriers k_full[S], k_empty[S], v_full[S], v_empty[S], staging
+    // full[2][kStg]; per tile s_full[2], (unused)[2], p_full[2], o_done[2];
+    // q_ready, done; then ints: abort, sequence, block, K stages issued,
+    // tensor-memory address, V stages issued, the pages brought into every
+    // V slot (bf16 pool) or every staging slot (FP8 pool)
+    static constexpr int kBars = 4 * kStages + 2 * kStg + kTcTiles * 8 + 2;
+    static constexpr int kTailBytes = kBars * 8 + (6 + kStages + 2 * kStg) * 4;
+    static constexpr int kSmemBytes = kOffTail + kTailBytes + 1024;
+    static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
+    static_assert(kOffKRing % 1024 == 0 && kOffVRing % 1024 == 0 && kOffStg % 1024 == 0,
+                  "swizzled operands and TMA boxes start on 1024-byte boundaries");
+};
+
+// One (page, plane, half of D) region of a bf16 page: 16 tokens x 64 dims,
+// 2 KiB, with the pool's region map (5-D: 64 dims, token, half, plane,
+// page*2*Hkv + head; box 64 x 16 x 1 x 1 x 1).
 __device__ __forceinline__ void tma_load_region(uint32_t dst, const CUtensorMap *map, int half,
                                                 int plane, int row, uint32_t bar) {
     asm volatile(
@@ -744,9 +305,20 @@ __device__ __forceinline__ void tma_load_region(uint32_t dst, const CUtensorMap 
         "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(half), "r"(plane), "r"(row), "r"(bar)
         : "memory");
 }
+// One (page, plane) of an FP8 page: 16 tokens x 128 codes, 2 KiB, with the
+// FP8 pool's plane map (4-D: 128 bytes of D, token, plane, page*2*Hkv +
+// head; box 128 x 16 x 1 x 1).
+__device__ __forceinline__ void tma_load_plane8(uint32_t dst, const CUtensorMap *map, int plane,
+                                                int row, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(plane), "r"(row), "r"(bar)
+        : "memory");
+}
 
 // 2^x by the hardware's approximation (one instruction; relative error
-// about 2^-22, far below the bf16 rounding of the weights it feeds;
+// about 2^-22, far below the 16-bit rounding of the weights it feeds;
 // 2^-inf = 0).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -760,30 +332,50 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
     return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// Two floats as the 16-bit operand type of the pool's products: bf16 over a
+// bf16 pool, f16 over an FP8 pool (whose E4M3 codes are exact in f16).
+template <bool kFp8>
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi) {
+    if constexpr (kFp8) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    } else {
+        return pack_bf16x2(lo, hi);
+    }
+}
+
+template <bool kFp8>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    prefill_attention_tc_kernel(const __grid_constant__ CUtensorMap region_map,
+    prefill_attention_tc_kernel(const __grid_constant__ CUtensorMap kv_map,
                                 const __grid_constant__ Params p) {
+    using Ly = TcLayout<kFp8>;
+    constexpr int S = Ly::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    uint8_t *tail = sm + kTcOffTail;
+    uint8_t *tail = sm + Ly::kOffTail;
     const uint32_t k_full0 = smem_u32(tail);
-    const uint32_t k_empty0 = k_full0 + 8 * kTcStages;
-    const uint32_t v_full0 = k_empty0 + 8 * kTcStages;
-    const uint32_t v_empty0 = v_full0 + 8 * kTcStages;
+    const uint32_t k_empty0 = k_full0 + 8 * S;
+    const uint32_t v_full0 = k_empty0 + 8 * S;
+    const uint32_t v_empty0 = v_full0 + 8 * S;
+    const uint32_t stg_full0 = v_empty0 + 8 * S;             // FP8: [plane][kStg]
     // per tile u: s_full, p_full, o_done, two of each (buffer q)
-    const uint32_t tile_bar0 = v_empty0 + 8 * kTcStages;
+    const uint32_t tile_bar0 = stg_full0 + 16 * Ly::kStg;
     auto s_full = [&](int u, int q) { return tile_bar0 + 64 * u + 8 * q; };
     auto p_full = [&](int u, int q) { return tile_bar0 + 64 * u + 32 + 8 * q; };
     auto o_done = [&](int u, int q) { return tile_bar0 + 64 * u + 48 + 8 * q; };
     const uint32_t q_ready = tile_bar0 + 64 * kTcTiles;
     const uint32_t done_bar = q_ready + 8;
     // misc: [0] abort, [1] sequence, [2] query block, [3] K stages issued,
-    // [4] tensor-memory address, [5] V stages issued; pmask[s]: pages
-    // brought into V slot s
-    volatile int *misc = reinterpret_cast<volatile int *>(tail + kTcBars * 8);
+    // [4] tensor-memory address, [5] V stages issued; pmask[s]: pages brought
+    // into V slot s (bf16 pool); smask[plane][q]: pages brought into staging
+    // slot q (FP8 pool)
+    volatile int *misc = reinterpret_cast<volatile int *>(tail + Ly::kBars * 8);
     volatile int *pmask = misc + 6;
+    volatile int *smask = misc + 6 + S;
+    float *kscale = reinterpret_cast<float *>(sm + Ly::kOffScale);          // [16][4]
+    float *vscale = kscale + kTcKScaleRing * kTcPagesPerStage;              // [8][4]
     const int g = blockIdx.x % p.Hkv;
     const int unit = blockIdx.x / p.Hkv;
     if (p.pdl && tid == 0) launch_dependents();
@@ -829,12 +421,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         }
         if (lane == 0) {
-            for (int s = 0; s < kTcStages; ++s) {
-                mbar_init(k_full0 + 8 * s, 1);    // the K producer's arrival + the bytes
+            for (int s = 0; s < S; ++s) {
+                // bf16 pool: the producer's arrival + the bytes; FP8 pool: the
+                // producer's arrival once the slot holds the converted codes
+                mbar_init(k_full0 + 8 * s, 1);
                 mbar_init(k_empty0 + 8 * s, kTcTiles);  // each tile's commit of its score product
-                mbar_init(v_full0 + 8 * s, 1);    // the V producer's arrival + the bytes
+                mbar_init(v_full0 + 8 * s, 1);
                 mbar_init(v_empty0 + 8 * s, kTcTiles);  // each tile's commit of its value product
             }
+            for (int q = 0; q < 2 * Ly::kStg; ++q) mbar_init(stg_full0 + 8 * q, 1);
             for (int u = 0; u < kTcTiles; ++u) {
                 for (int q = 0; q < 2; ++q) {
                     mbar_init(s_full(u, q), 1);   // commit of the score product
@@ -846,6 +441,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(done_bar, kTcTiles);  // each MMA issuer, once its products are done
             misc[0] = 0;
             misc[3] = 0;
+            misc[5] = 0;
             fence_mbar_init();
         }
     }
@@ -870,70 +466,153 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == kTcProducerWarp || warp == kTcVProducerWarp) {
         // ----------------------------------------------- TMA producers --
-        // One warp brings the K halves of every stage, the other the V
-        // halves, each into its own ring: a K slot frees as soon as the
-        // stage's score products are done, a V slot once its value products
-        // are.  Lanes 0-3 each bring one page of the stage (its two regions);
-        // the block-table entries are looked up 32 pages (8 stages) at a time,
-        // one group ahead.
+        // One warp brings the K half of every stage, the other the V half,
+        // each into its own ring: a K slot frees as soon as the stage's score
+        // products are done, a V slot once its value products are.
         const bool isv = warp == kTcVProducerWarp;
+        const int plane = isv ? 1 : 0;
         const uint32_t full0 = isv ? v_full0 : k_full0;
         const uint32_t empty0 = isv ? v_empty0 : k_empty0;
-        uint8_t *ringp = sm + (isv ? kTcOffVRing : kTcOffKRing);
+        uint8_t *ringp = sm + (isv ? Ly::kOffVRing : Ly::kOffKRing);
         int issued = 0;
-        auto lookup = [&](int grp) {  // lane l: page index 32 grp + l of the sequence
-            const int pg = 32 * grp + lane;
-            return pg < npg ? p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg] : -1;
-        };
-        int cur = lookup(0), nxt = lookup(1);
-        // the chunk's keys and values were appended by the kernel before
-        if (p.pdl) grid_dependency_wait();
-        for (int j = 0; j < ntiles; ++j) {
-            const int s = j % kTcStages;
-            if (j > 0 && (j * kTcPagesPerStage) % 32 == 0) {
-                cur = nxt;
-                nxt = lookup(j * kTcPagesPerStage / 32 + 1);
-            }
-            bool stop = false;
+        // waits only lane 0 makes (its outcome is shared with the warp)
+        auto lane0_wait = [&](uint32_t bar, uint32_t parity) {
+            bool ok = true;
             if (lane == 0) {
                 if (misc[0]) {
-                    stop = true;
-                } else if (j >= kTcStages &&
-                           !mbar_wait_bounded(empty0 + 8 * s, ((j / kTcStages) - 1) & 1, misc,
-                                              p.wait_cycles)) {
+                    ok = false;
+                } else if (!mbar_wait_bounded(bar, parity, misc, p.wait_cycles)) {
                     misc[0] = 1;
                     flag_error(p.err, QDEC_FLAG_TIMEOUT);
-                    stop = true;
+                    ok = false;
                 }
             }
-            if (__shfl_sync(kFull, stop, 0)) break;
-            const int pg = j * kTcPagesPerStage + lane;
-            const int page = __shfl_sync(kFull, cur, (j * kTcPagesPerStage + (lane & 3)) & 31);
-            const bool ok = lane < kTcPagesPerStage && pg < npg && page >= 0 && page < p.num_pages;
-            if (!isv && lane < kTcPagesPerStage && pg < npg && !ok) flag_error(p.err, QDEC_FLAG_BAD_PAGE);
-            const unsigned mask = __ballot_sync(kFull, ok) & 0xFu;
-            const bool withheld = !isv && p.withhold_first && j == 0;  // test hook: never lands
-            if (lane == 0) {
-                if (isv) pmask[s] = static_cast<int>(mask);
-                if (!withheld) {
-                    if (mask == 0)
-                        mbar_arrive(full0 + 8 * s);
-                    else
-                        mbar_arrive_expect_tx(full0 + 8 * s, __popc(mask) * 2 * (kPageSize * 128));
+            return __shfl_sync(kFull, ok, 0) != 0;
+        };
+        if constexpr (!kFp8) {
+            // lanes 0-3 each bring one page of the stage (its two regions);
+            // the block-table entries are looked up 32 pages (8 stages) at a
+            // time, one group ahead
+            auto lookup = [&](int grp) {  // lane l: page index 32 grp + l of the sequence
+                const int pg = 32 * grp + lane;
+                return pg < npg ? p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg] : -1;
+            };
+            int cur = lookup(0), nxt = lookup(1);
+            // the chunk's keys and values were appended by the kernel before
+            if (p.pdl) grid_dependency_wait();
+            for (int j = 0; j < ntiles; ++j) {
+                const int s = j % S;
+                if (j > 0 && (j * kTcPagesPerStage) % 32 == 0) {
+                    cur = nxt;
+                    nxt = lookup(j * kTcPagesPerStage / 32 + 1);
                 }
-            }
-            __syncwarp();
-            if (ok && !withheld) {
-                const uint32_t dst = smem_u32(ringp + s * kTcSlotBytes) + lane * (kPageSize * 128);
-                const int row = page * 2 * p.Hkv + g;
+                if (j >= S && !lane0_wait(empty0 + 8 * s, ((j / S) - 1) & 1)) break;
+                const int pg = j * kTcPagesPerStage + lane;
+                const int page = __shfl_sync(kFull, cur, (j * kTcPagesPerStage + (lane & 3)) & 31);
+                const bool ok = lane < kTcPagesPerStage && pg < npg && page >= 0 && page < p.num_pages;
+                if (!isv && lane < kTcPagesPerStage && pg < npg && !ok)
+                    flag_error(p.err, QDEC_FLAG_BAD_PAGE);
+                const unsigned mask = __ballot_sync(kFull, ok) & 0xFu;
+                const bool withheld = !isv && p.withhold_first && j == 0;  // test hook: never lands
+                if (lane == 0) {
+                    if (isv) pmask[s] = static_cast<int>(mask);
+                    if (!withheld) {
+                        if (mask == 0)
+                            mbar_arrive(full0 + 8 * s);
+                        else
+                            mbar_arrive_expect_tx(full0 + 8 * s, __popc(mask) * 2 * (kPageSize * 128));
+                    }
+                }
+                __syncwarp();
+                if (ok && !withheld) {
+                    const uint32_t dst = smem_u32(ringp + s * kTcSlotBytes) + lane * (kPageSize * 128);
+                    const int row = page * 2 * p.Hkv + g;
 #pragma unroll
-                for (int h = 0; h < 2; ++h)  // region h: dims 64 h .. 64 h + 63 of the plane
-                    tma_load_region(dst + h * kTcRegion, &region_map, h, isv ? 1 : 0, row,
-                                    full0 + 8 * s);
+                    for (int h = 0; h < 2; ++h)  // region h: dims 64 h .. 64 h + 63 of the plane
+                        tma_load_region(dst + h * kTcRegion, &kv_map, h, plane, row, full0 + 8 * s);
+                }
+                issued = j + 1;
             }
-            issued = j + 1;
+        } else {
+            // FP8 pool: each stage's codes land in a staging slot (lanes 0-3
+            // each bring one page's plane, 2 KiB, and its scale); the warp
+            // then converts them to f16 (exact) into the ring slot, zeroing
+            // the rows of keys past the sequence or on pages not brought.
+            constexpr int Q = Ly::kStg;
+            uint8_t *stg = sm + Ly::kOffStg + plane * Q * Ly::kStgSlot;
+            const uint32_t sfull0 = stg_full0 + 8 * Q * plane;
+            volatile int *sm_mask = smask + Q * plane;
+            // the chunk's keys and values were appended by the kernel before
+            if (p.pdl) grid_dependency_wait();
+            auto issue = [&](int jj) {
+                const int q = jj % Q;
+                const int pg = jj * kTcPagesPerStage + lane;
+                int page = -1;
+                if (lane < kTcPagesPerStage && pg < npg)
+                    page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg];
+                const bool ok = lane < kTcPagesPerStage && pg < npg && page >= 0 && page < p.num_pages;
+                if (!isv && lane < kTcPagesPerStage && pg < npg && !ok)
+                    flag_error(p.err, QDEC_FLAG_BAD_PAGE);
+                const unsigned mask = __ballot_sync(kFull, ok) & 0xFu;
+                if (isv && lane < kTcPagesPerStage) {  // both scales of each page of the stage
+                    const int64_t si = static_cast<int64_t>(page) * 2 * p.Hkv + g;
+                    kscale[(jj % kTcKScaleRing) * kTcPagesPerStage + lane] = ok ? p.kv_scale[si] : 0.f;
+                    vscale[(jj % kTcVScaleRing) * kTcPagesPerStage + lane] =
+                        ok ? p.kv_scale[si + p.Hkv] : 0.f;
+                }
+                const bool withheld = !isv && p.withhold_first && jj == 0;  // test hook
+                if (lane == 0) {
+                    sm_mask[q] = static_cast<int>(mask);
+                    if (!withheld) {
+                        if (mask == 0)
+                            mbar_arrive(sfull0 + 8 * q);
+                        else
+                            mbar_arrive_expect_tx(sfull0 + 8 * q, __popc(mask) * kFp8PlaneBytes);
+                    }
+                }
+                __syncwarp();
+                if (ok && !withheld)
+                    tma_load_plane8(smem_u32(stg + q * Ly::kStgSlot) + lane * kFp8PlaneBytes, &kv_map,
+                                    plane, page * 2 * p.Hkv + g, sfull0 + 8 * q);
+            };
+            int staged = 0;
+            for (; staged < Q && staged < ntiles; ++staged) issue(staged);
+            for (int j = 0; j < ntiles; ++j) {
+                const int s = j % S, q = j % Q;
+                if (!lane0_wait(sfull0 + 8 * q, (j / Q) & 1)) break;
+                if (j >= S && !lane0_wait(empty0 + 8 * s, ((j / S) - 1) & 1)) break;
+                const int mask = sm_mask[q];
+                const uint8_t *src = stg + q * Ly::kStgSlot;
+                uint8_t *dst = ringp + s * kTcSlotBytes;
+#pragma unroll 4
+                for (int i = 0; i < 16; ++i) {
+                    // key row kr (page kr / 16), codes 16 c .. 16 c + 15: the
+                    // f16 chunks 2 c' and 2 c' + 1 (c' = c % 4) of region c / 4
+                    const int e = lane + 32 * i, kr = e >> 3, c = e & 7, tr = kr & 15;
+                    const bool zero = j * kTcKeys + kr >= L || !((mask >> (kr >> 4)) & 1);
+                    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+                    if (!zero) {
+                        const uint4 codes = *reinterpret_cast<const uint4 *>(
+                            src + (kr >> 4) * kFp8PlaneBytes + tr * 128 + ((c ^ (tr & 7)) << 4));
+                        lo = make_uint4(e4m3x2_to_f16x2(codes.x), e4m3x2_to_f16x2(codes.x >> 16),
+                                        e4m3x2_to_f16x2(codes.y), e4m3x2_to_f16x2(codes.y >> 16));
+                        hi = make_uint4(e4m3x2_to_f16x2(codes.z), e4m3x2_to_f16x2(codes.z >> 16),
+                                        e4m3x2_to_f16x2(codes.w), e4m3x2_to_f16x2(codes.w >> 16));
+                    }
+                    uint8_t *reg = dst + (c >> 2) * kTcRegion;
+                    *reinterpret_cast<uint4 *>(reg + sw128_off(kr, 2 * (c & 3))) = lo;
+                    *reinterpret_cast<uint4 *>(reg + sw128_off(kr, 2 * (c & 3) + 1)) = hi;
+                }
+                fence_proxy_async_smem();  // read next by the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full0 + 8 * s);
+                issued = j + 1;
+                if (staged < ntiles) issue(staged++);  // into the staging slot just read
+            }
+            if (lane == 0) misc[isv ? 5 : 3] = staged;  // staging copies issued
         }
-        if (lane == 0) misc[isv ? 5 : 3] = issued;
+        if constexpr (!kFp8)
+            if (lane == 0) misc[isv ? 5 : 3] = issued;
     } else if (warp == kTcMmaWarp || warp == kTcMmaWarp1) {
         // ------------------------------------------- the MMA issuers --
         // one thread per query tile issues its products, so neither tile
@@ -941,22 +620,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // rings, whose slots free once both tiles' commits have arrived
         if (lane == 0) {
             const int u = warp == kTcMmaWarp ? 0 : 1;
-            const uint32_t qt = smem_u32(sm + kTcOffQ) + u * kTcQBytes;
-            const uint32_t kring = smem_u32(sm + kTcOffKRing), vring = smem_u32(sm + kTcOffVRing);
-            constexpr uint32_t kIdS = tc::idesc_bf16(kTcRows, kTcKeys, false);
-            constexpr uint32_t kIdO = tc::idesc_bf16(kTcRows, kHeadDim, true);
+            const uint32_t qt = smem_u32(sm + Ly::kOffQ) + u * kTcQBytes;
+            const uint32_t kring = smem_u32(sm + Ly::kOffKRing), vring = smem_u32(sm + Ly::kOffVRing);
+            constexpr uint32_t kIdS = kFp8 ? tc::idesc_f16(kTcRows, kTcKeys, false)
+                                           : tc::idesc_bf16(kTcRows, kTcKeys, false);
+            constexpr uint32_t kIdO = kFp8 ? tc::idesc_f16(kTcRows, kHeadDim, true)
+                                           : tc::idesc_bf16(kTcRows, kHeadDim, true);
             const uint32_t tile_tm = tmem + 256 * u;
             // O += P_t V_t once V_t has landed and the tile's softmax warps
             // have written P (over the scores of stage t, in tensor memory);
             // the commits free that buffer for the scores of stage t + 2
             // (o_done) and, with the other tile's, the V slot (v_empty)
             auto value_product = [&](int t) -> bool {
-                if (!mbar_wait_bounded(v_full0 + 8 * (t % kTcStages), (t / kTcStages) & 1, misc,
-                                       p.wait_cycles) ||
+                if (!mbar_wait_bounded(v_full0 + 8 * (t % S), (t / S) & 1, misc, p.wait_cycles) ||
                     !mbar_wait_bounded(p_full(u, t & 1), (t >> 1) & 1, misc, p.wait_cycles))
                     return false;
                 tc::fence_after();
-                const uint32_t vst = vring + (t % kTcStages) * kTcSlotBytes;
+                const uint32_t vst = vring + (t % S) * kTcSlotBytes;
                 const uint32_t tp = tile_tm + (t & 1) * kTcKeys;  // P: 32 columns
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk)
@@ -964,14 +644,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                tc::desc_sw128(vst + kk * 2048, kTcRegion, 1024), kIdO,
                                t > 0 || kk > 0);
                 tc::commit(o_done(u, t & 1));
-                tc::commit(v_empty0 + 8 * (t % kTcStages));
+                tc::commit(v_empty0 + 8 * (t % S));
                 return true;
             };
             bool ok = mbar_wait_bounded(q_ready, 0, misc, p.wait_cycles);
             for (int j = 0; ok && j < ntiles; ++j) {
-                const int s = j % kTcStages;
+                const int s = j % S;
                 // the buffer holds P of stage j - 2 until its value product is done
-                if (!mbar_wait_bounded(k_full0 + 8 * s, (j / kTcStages) & 1, misc, p.wait_cycles) ||
+                if (!mbar_wait_bounded(k_full0 + 8 * s, (j / S) & 1, misc, p.wait_cycles) ||
                     (j >= 2 && !mbar_wait_bounded(o_done(u, j & 1), ((j - 2) >> 1) & 1, misc,
                                                   p.wait_cycles))) {
                     ok = false;
@@ -1019,10 +699,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         };
         if (p.pdl) grid_dependency_wait();  // q_rot, the pool and out of the kernel before
         {
-            // Q of the tile, scaled to log2 units, as bf16: warp w converts
-            // rows w % 4, w % 4 + 4, ..., lane l taking dims 4 l .. 4 l + 3 of
-            // each (one coalesced 512-byte row per warp load, all in flight)
-            uint8_t *qt = sm + kTcOffQ + u * kTcQBytes;
+            // Q of the tile, scaled to log2 units, in the 16-bit operand type:
+            // warp w converts rows w % 4, w % 4 + 4, ..., lane l taking dims
+            // 4 l .. 4 l + 3 of each (one coalesced 512-byte row per warp
+            // load, all in flight)
+            uint8_t *qt = sm + Ly::kOffQ + u * kTcQBytes;
             const int half = lane >> 4, cc = (lane & 15) >> 1, sub = (lane & 1) * 8;
             float4 x[kTcRows / 4];
 #pragma unroll
@@ -1037,8 +718,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int k = 0; k < kTcRows / 4; ++k) {
                 const int rr = (warp & 3) + 4 * k;
-                const uint2 w = make_uint2(pack_bf16x2(x[k].x * p.qscale, x[k].y * p.qscale),
-                                           pack_bf16x2(x[k].z * p.qscale, x[k].w * p.qscale));
+                const uint2 w = make_uint2(pack16x2<kFp8>(x[k].x * p.qscale, x[k].y * p.qscale),
+                                           pack16x2<kFp8>(x[k].z * p.qscale, x[k].w * p.qscale));
                 *reinterpret_cast<uint2 *>(qt + half * kTcQHalf + sw128_off(rr, cc) + sub) = w;
             }
             fence_proxy_async_smem();  // read next by the tensor core
@@ -1050,7 +731,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            const int s = j % kTcStages;
+            const int s = j % S;
             if (!wait_all(s_full(u, j & 1), (j >> 1) & 1)) {
                 ok = false;
                 break;
@@ -1067,6 +748,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     sc[c] = __uint_as_float(v0[c]);
                     sc[32 + c] = __uint_as_float(v1[c]);
                 }
+            }
+            // FP8 pool: the stage's scales, once its V slot is full (the V
+            // producer wrote them before); the scores of page q of the stage
+            // times its K scale
+            float vs[kTcPagesPerStage] = {1.f, 1.f, 1.f, 1.f};
+            if constexpr (kFp8) {
+                if (!wait_all(v_full0 + 8 * s, (j / S) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const float *ks = kscale + (j % kTcKScaleRing) * kTcPagesPerStage;
+                const float *vsr = vscale + (j % kTcVScaleRing) * kTcPagesPerStage;
+#pragma unroll
+                for (int q = 0; q < kTcPagesPerStage; ++q) vs[q] = vsr[q];
+#pragma unroll
+                for (int c = 0; c < kTcKeys; ++c) sc[c] *= ks[c / kPageSize];
             }
             const int kb = j * kTcKeys;
             if (kb + kTcKeys - 1 > lim) {
@@ -1111,9 +808,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc::fence_before();
                 }
             }
-            // P as bf16 over the first 32 columns of the scores just read (a
-            // column holds two consecutive keys), the A operand of the value
-            // product
+            // P over the first 32 columns of the scores just read (a column
+            // holds two consecutive keys), the A operand of the value product;
+            // over an FP8 pool each weight times its page's V scale (the row
+            // sum keeps the unscaled weights)
             float ps[4] = {0.f, 0.f, 0.f, 0.f};   // the row sum in four chains
             uint32_t pw[kTcKeys / 2];
 #pragma unroll
@@ -1121,25 +819,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const float p0 = fast_exp2(sc[2 * c] - m);
                 const float p1 = fast_exp2(sc[2 * c + 1] - m);
                 ps[c & 3] += p0 + p1;
-                pw[c] = pack_bf16x2(p0, p1);
+                const float sv = vs[(2 * c) / kPageSize];
+                pw[c] = pack16x2<kFp8>(p0 * sv, p1 * sv);
             }
             tc::st32(trow + (j & 1) * kTcKeys, pw);
             l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-            // V rows of keys past the sequence (and of pages not brought there)
-            // are zeroed once the slot has landed, by each tile's warps: both
-            // value products read them
-            if (kb + kTcKeys > L) {
-                if (!wait_all(v_full0 + 8 * s, (j / kTcStages) & 1)) {
-                    ok = false;
-                    break;
-                }
-                const int pm = pmask[s];
-                uint8_t *vr = sm + kTcOffVRing + s * kTcSlotBytes;
-                for (int e = r; e < kTcKeys * 16; e += kTcRows) {
-                    const int kr = e >> 4, c = e & 15;
-                    if (kb + kr >= L || !((pm >> (kr / kPageSize)) & 1))
-                        *reinterpret_cast<uint4 *>(vr + (c >> 3) * kTcRegion + kr * 128 +
-                                                   ((c & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (!kFp8) {
+                // V rows of keys past the sequence (and of pages not brought
+                // there) are zeroed once the slot has landed, by each tile's
+                // warps: both value products read them
+                if (kb + kTcKeys > L) {
+                    if (!wait_all(v_full0 + 8 * s, (j / S) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    const int pm = pmask[s];
+                    uint8_t *vr = sm + Ly::kOffVRing + s * kTcSlotBytes;
+                    for (int e = r; e < kTcKeys * 16; e += kTcRows) {
+                        const int kr = e >> 4, c = e & 15;
+                        if (kb + kr >= L || !((pm >> (kr / kPageSize)) & 1))
+                            *reinterpret_cast<uint4 *>(vr + (c >> 3) * kTcRegion + kr * 128 +
+                                                       ((c & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
                 }
             }
             tc::wait_st();
@@ -1189,18 +890,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // a wait that gave up may leave copies in flight: let them land (bounded)
     if ((tid == kTcProducerWarp * 32 || tid == kTcVProducerWarp * 32) && misc[0]) {
         const bool isv = warp == kTcVProducerWarp;
-        const uint32_t full0 = isv ? v_full0 : k_full0;
         const int issued = misc[isv ? 5 : 3];
         volatile int never = 0;
-        for (int t = max(0, issued - kTcStages); t < issued; ++t)
-            mbar_wait_bounded(full0 + 8 * (t % kTcStages), (t / kTcStages) & 1, &never,
-                              p.wait_cycles);
+        if constexpr (kFp8) {
+            const uint32_t sfull0 = stg_full0 + 8 * Ly::kStg * (isv ? 1 : 0);
+            for (int t = max(0, issued - Ly::kStg); t < issued; ++t)
+                mbar_wait_bounded(sfull0 + 8 * (t % Ly::kStg), (t / Ly::kStg) & 1, &never,
+                                  p.wait_cycles);
+        } else {
+            const uint32_t full0 = isv ? v_full0 : k_full0;
+            for (int t = max(0, issued - S); t < issued; ++t)
+                mbar_wait_bounded(full0 + 8 * (t % S), (t / S) & 1, &never, p.wait_cycles);
+        }
     }
 }
 
 std::mutex g_pf_mu;
-bool g_pf_smem_set[2][64];
-bool g_pf_tc_smem_set[64];
+bool g_pf_tc_smem_set[2][64];
+
+template <bool kFp8>
+cudaError_t launch_tc(const Params &p, const CUtensorMap &kv_map, int dev, cudaStream_t s) {
+    using Ly = TcLayout<kFp8>;
+    {
+        std::lock_guard<std::mutex> lock(g_pf_mu);
+        if (!g_pf_tc_smem_set[kFp8 ? 1 : 0][dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(prefill_attention_tc_kernel<kFp8>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       Ly::kSmemBytes);
+            if (e != cudaSuccess) return e;
+            g_pf_tc_smem_set[kFp8 ? 1 : 0][dev] = true;
+        }
+    }
+    // units: at most T / 64 + B blocks of 64 chunk rows, times the KV heads
+    const int64_t units = (static_cast<int64_t>(p.T) + kTcTok - 1) / kTcTok + p.B;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(units * p.Hkv));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = Ly::kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = p.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, prefill_attention_tc_kernel<kFp8>, kv_map, p);
+}
 
 }  // namespace
 
@@ -1213,62 +947,13 @@ cudaError_t launch_prefill_append(const Params &p, bool fp8, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <bool kFp8>
-cudaError_t launch_attn(const Params &p, const CUtensorMap &kv_map, int dev, cudaStream_t s) {
-    {
-        std::lock_guard<std::mutex> lock(g_pf_mu);
-        if (!g_pf_smem_set[kFp8 ? 1 : 0][dev]) {
-            const cudaError_t e =
-                cudaFuncSetAttribute(prefill_attention_kernel<kFp8>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, pf_smem_bytes<kFp8>());
-            if (e != cudaSuccess) return e;
-            g_pf_smem_set[kFp8 ? 1 : 0][dev] = true;
-        }
-    }
-    // units: at most T / 16 + B blocks of 16 chunk rows, times the KV heads
-    const int64_t units = (static_cast<int64_t>(p.T) + kPfRows - 1) / kPfRows + p.B;
-    prefill_attention_kernel<kFp8>
-        <<<static_cast<unsigned>(units * p.Hkv), kThreads, pf_smem_bytes<kFp8>(), s>>>(kv_map, p);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_prefill_attention_tc(const Params &p, const CUtensorMap &region_map,
-                                        cudaStream_t s) {
-    if (p.T <= 0) return cudaSuccess;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 63;
-    {
-        std::lock_guard<std::mutex> lock(g_pf_mu);
-        if (!g_pf_tc_smem_set[dev]) {
-            const cudaError_t e = cudaFuncSetAttribute(
-                prefill_attention_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemBytes);
-            if (e != cudaSuccess) return e;
-            g_pf_tc_smem_set[dev] = true;
-        }
-    }
-    // units: at most T / 64 + B blocks of 64 chunk rows, times the KV heads
-    const int64_t units = (static_cast<int64_t>(p.T) + kTcTok - 1) / kTcTok + p.B;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(units * p.Hkv));
-    cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = kTcSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = p.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, prefill_attention_tc_kernel, region_map, p);
-}
-
 cudaError_t launch_prefill_attention(const Params &p, const CUtensorMap &kv_map, bool fp8,
                                      cudaStream_t s) {
     if (p.T <= 0) return cudaSuccess;
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 63;
-    return fp8 ? launch_attn<true>(p, kv_map, dev, s) : launch_attn<false>(p, kv_map, dev, s);
+    return fp8 ? launch_tc<true>(p, kv_map, dev, s) : launch_tc<false>(p, kv_map, dev, s);
 }
 
 }  // namespace qdec

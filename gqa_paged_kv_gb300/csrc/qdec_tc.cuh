@@ -56,6 +56,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same with f16 A and B (bits 7-9 = 0, 10-12 = 0).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
+    return (1u << 4) | (b_mn_major ? (1u << 16) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // D (+)= A B, one K = 16 step, issued by one thread (A: M x 16 from adesc,
 // B: 16 x N from bdesc).
 static __device__ __forceinline__ void mma(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
