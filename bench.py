@@ -61,30 +61,32 @@ PREFILL_METRIC = "prefill-attn TFLOP/s (causal, algorithmic) and µs/layer per p
 _CSRC = "gqa_paged_kv_gb300/csrc/"
 KERNEL_SOURCES = {
     "attention_kernel": tuple(_CSRC + f for f in ("qdec_kernels.cu", "qdec_internal.h",
-                                                  "qdec_ptx.cuh")),
+                                                  "qdec_ptx.cuh", "qdec_ff.cuh")),
     "qkv_append_kernel": tuple(_CSRC + f for f in ("qdec_qkv.cu", "qdec_internal.h",
                                                    "qdec_ptx.cuh")),
-    "prefill_attention_kernel": tuple(_CSRC + f for f in ("qdec_prefill.cu", "qdec_internal.h",
-                                                          "qdec_ptx.cuh", "qdec_tc.cuh")),
+    "prefill_attention_tc_kernel": tuple(_CSRC + f for f in ("qdec_prefill.cu",
+                                                             "qdec_internal.h", "qdec_ptx.cuh",
+                                                             "qdec_tc.cuh", "qdec_ff.cuh")),
 }
 
 # DRAM bytes per launch of the fused kernel measured with ncu (see
 # profiles/), keyed by workload; used only while the kernel source hash
 # still matches the one the counters were taken on.
 TRAFFIC = {
-    "b8-ctx256to384-36layer": {"kernel_sha": "db22c2a1a1b797eb", "bytes_per_launch": 10900023},
-    "b1-ctx8192-spikes-36layer": {"kernel_sha": "db22c2a1a1b797eb", "bytes_per_launch": 33634560},
-    "b64-ragged128to16384-sharedpool-36layer": {"kernel_sha": "db22c2a1a1b797eb",
-                                                "bytes_per_launch": 1038097364},
-    "b64-ragged128to16384-sharedpool-36layer-fp8kv": {"kernel_sha": "db22c2a1a1b797eb",
-                                                      "bytes_per_launch": 524764583},
+    "b8-ctx256to384-36layer": {"kernel_sha": "ebfd4d5815a4ad7c", "bytes_per_launch": 10899520},
+    "b1-ctx8192-spikes-36layer": {"kernel_sha": "ebfd4d5815a4ad7c", "bytes_per_launch": 33633536},
+    "b64-ragged128to16384-sharedpool-36layer": {"kernel_sha": "ebfd4d5815a4ad7c",
+                                                "bytes_per_launch": 1038094925},
+    "b64-ragged128to16384-sharedpool-36layer-fp8kv": {"kernel_sha": "ebfd4d5815a4ad7c",
+                                                      "bytes_per_launch": 525528576},
     # --prefill 2048: the causal prefill attention kernel
-    "prefill-b1-prompt2048-36layer": {"kernel_sha": "fb9a77aa27ecf581", "bytes_per_launch": 41995115},
-    "prefill-b1-prompt2048-36layer-fp8kv": {"kernel_sha": "fb9a77aa27ecf581", "bytes_per_launch": 37815019},
+    "prefill-b1-prompt2048-36layer": {"kernel_sha": "4cd71e6da03e48ef", "bytes_per_launch": 42007403},
+    "prefill-b1-prompt2048-36layer-fp8kv": {"kernel_sha": "4cd71e6da03e48ef",
+                                            "bytes_per_launch": 37826048},
     # --qkv: the projection kernel
-    "b8-ctx256to384-36layer-qkv2560": {"kernel_sha": "ba9a59823eb8e517", "bytes_per_launch": 31553185},
-    "b64-ragged128to16384-sharedpool-36layer-qkv2560": {"kernel_sha": "ba9a59823eb8e517",
-                                                        "bytes_per_launch": 31908342},
+    "b8-ctx256to384-36layer-qkv2560": {"kernel_sha": "bd321992338b6b31", "bytes_per_launch": 31554816},
+    "b64-ragged128to16384-sharedpool-36layer-qkv2560": {"kernel_sha": "bd321992338b6b31",
+                                                        "bytes_per_launch": 31906560},
 }
 
 # The CPU timings sample the first few layers of a workload (same shapes and
@@ -1183,7 +1185,7 @@ def run_prefill(args, dist: Dist):
 
     tr = TRAFFIC.get(name)
     traffic = (tr["bytes_per_launch"]
-               if tr and tr["kernel_sha"] == kernel_sha("prefill_attention_kernel") else None)
+               if tr and tr["kernel_sha"] == kernel_sha("prefill_attention_tc_kernel") else None)
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -1205,9 +1207,10 @@ def run_prefill(args, dist: Dist):
             "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,
-            "dtype": ("e4m3 KV converted to bf16 in shared memory (mma.sync bf16, q as hi+lo, "
-                      "f32 accumulate)" if fp8 else
-                      "bf16 (tcgen05 kind::f16, q as hi+lo, f32 accumulators in tensor memory)"),
+            "dtype": ("e4m3 KV converted exactly to f16 in shared memory (tcgen05 kind::f16 with "
+                      "f16 operands, f32 accumulators in tensor memory)" if fp8 else
+                      "bf16 (tcgen05 kind::f16 with bf16 operands, q rounded once to bf16, f32 "
+                      "accumulators in tensor memory)"),
             "data": "synthetic (seeded N(0,1) bf16 q/k/v, U(0.5,1.5) norm weights)",
             "us_per_layer_step": round(ms_step * 1e3 / L, 3),
             "config": prefill_config(P, L, fp8),
@@ -1215,8 +1218,8 @@ def run_prefill(args, dist: Dist):
                          "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, cuBLAS "
                                       f"burst)" if peak_kind == "measured" else "fallback",
-                         "kernel": ("prefill_attention_kernel<fp8>" if fp8
-                                    else "prefill_attention_tc_kernel"),
+                         "kernel": ("prefill_attention_tc_kernel<fp8>" if fp8
+                                    else "prefill_attention_tc_kernel<bf16>"),
                          "launch_us": round(launch_us, 3),
                          "launch_us_how": f"CUDA events around a graph of {L} attention "
                                           f"launches, {reps} replays",

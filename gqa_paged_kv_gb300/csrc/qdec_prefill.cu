@@ -204,9 +204,8 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
 }
 
 // ------------------------------------- attention on the 5th-gen tensor core --
-// prefill_attention_tc_kernel: the same causal paged attention (bf16 pool)
-// with both products on the tensor core (tcgen05, accumulators in tensor
-// memory).  One CTA per (sequence, KV head, block of 64 chunk tokens), the
+// prefill_attention_tc_kernel: causal paged attention of the chunk with both
+// products on the tensor core (tcgen05, accumulators in tensor memory).  One CTA per (sequence, KV head, block of 64 chunk tokens), the
 // blocks with the most keys first.  The block is two tiles of M = 128 rows:
 // tile u holds tokens 32 u .. 32 u + 31 of the block for the 4 query heads
 // of the group (row 32 j + i: head 4 g + j, token 32 u + i), so each K/V

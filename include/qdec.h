@@ -269,12 +269,12 @@ qdec_status qdec_qkv_pack_weights(const qdec_shape *shape, int32_t hidden,
  * block table must map every page up to token seq_lens[b] - 1.  Sequences
  * whose chunk is malformed are skipped and flagged QDEC_FLAG_BAD_SEQLEN.
  * shape->batch = B sequences; shape->num_ctas is ignored.  With
- * QDEC_LAUNCH_OVERLAP_PREVIOUS, qdec_prefill_attn over a bf16 pool may start
- * while the previous kernel on the stream finishes: it reads qo_indptr,
- * seq_lens and the block table at once, and waits for that kernel before it
- * reads q_rot or the pool or writes out (set the flag only when the previous
- * kernel writes none of the first three); the append and the FP8-pool
- * attention ignore the flag (each starts after the previous kernel).
+ * QDEC_LAUNCH_OVERLAP_PREVIOUS, qdec_prefill_attn (bf16 or FP8 pool) may
+ * start while the previous kernel on the stream finishes: it reads
+ * qo_indptr, seq_lens and the block table at once, and waits for that kernel
+ * before it reads q_rot, the pool or kv_scale or writes out (set the flag only
+ * when the previous kernel writes none of the first three); the append
+ * ignores the flag (it starts after the previous kernel).
  * FP8-pool forms follow the FP8 section below. */
 
 /* Steps 1-3 for every chunk row r: RMSNorm + NeoX RoPE at positions[r] of
