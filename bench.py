@@ -73,12 +73,14 @@ KERNEL_SOURCES = {
 # profiles/), keyed by workload; used only while the kernel source hash
 # still matches the one the counters were taken on.
 TRAFFIC = {
-    "b8-ctx256to384-36layer": {"kernel_sha": "ebfd4d5815a4ad7c", "bytes_per_launch": 10899520},
-    "b1-ctx8192-spikes-36layer": {"kernel_sha": "ebfd4d5815a4ad7c", "bytes_per_launch": 33633536},
+    "b8-ctx256to384-36layer": {"kernel_sha": "ebfd4d5815a4ad7c", "bytes_per_launch": 10899576},
+    "b16-ctx256to384-chanscale-36layer": {"kernel_sha": "ebfd4d5815a4ad7c",
+                                          "bytes_per_launch": 21779270},
+    "b1-ctx8192-spikes-36layer": {"kernel_sha": "ebfd4d5815a4ad7c", "bytes_per_launch": 33634251},
     "b64-ragged128to16384-sharedpool-36layer": {"kernel_sha": "ebfd4d5815a4ad7c",
-                                                "bytes_per_launch": 1038094925},
+                                                "bytes_per_launch": 1038103628},
     "b64-ragged128to16384-sharedpool-36layer-fp8kv": {"kernel_sha": "ebfd4d5815a4ad7c",
-                                                      "bytes_per_launch": 525528576},
+                                                      "bytes_per_launch": 524783838},
     # --prefill 2048: the causal prefill attention kernel
     "prefill-b1-prompt2048-36layer": {"kernel_sha": "4cd71e6da03e48ef", "bytes_per_launch": 42007403},
     "prefill-b1-prompt2048-36layer-fp8kv": {"kernel_sha": "4cd71e6da03e48ef",
@@ -129,6 +131,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the 36 calls eagerly")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--three-call", action="store_true",
+                    help="each layer as qdec_append_rope, qdec_attn_split, qdec_attn_merge "
+                         "(launched one after another) instead of the one-launch qdec_step")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch each layer only after the previous one completed")
     ap.add_argument("--layers", type=int, default=0,
@@ -268,9 +273,9 @@ def l2_bytes(dev=None) -> int:
     return L2_BYTES_NOMINAL
 
 
-def workload_name(spec, kv: str, qkv_hidden: int = 0) -> str:
+def workload_name(spec, kv: str, qkv_hidden: int = 0, three_call: bool = False) -> str:
     return (spec.name + ("-fp8kv" if kv == "fp8" else "")
-            + (f"-qkv{qkv_hidden}" if qkv_hidden else ""))
+            + (f"-qkv{qkv_hidden}" if qkv_hidden else "") + ("-threecall" if three_call else ""))
 
 
 def qkv_weight_bytes(spec, hidden: int) -> int:
@@ -324,6 +329,12 @@ def workload_config(w: wl.Workload, args, world: int, l2: int = L2_BYTES_NOMINAL
         cfg["hidden"] = qkv_hidden
         cfg["launch"] = (f"CUDA graphs: rope table + {L} x (qdec_qkv_append_rope, "
                          f"qdec_attn_decode)")
+    elif getattr(args, "three_call", False):
+        sfx = "_fp8" if w.kv == "fp8" else ""
+        cfg["workload"] = workload_name(spec, w.kv, 0, True)
+        cfg["launch"] = ("eager" if args.no_graph else "CUDA graphs") + (
+            f": rope table + {L} x (qdec_append_rope{sfx}, qdec_attn_split{sfx}, "
+            f"qdec_attn_merge), each launch after the previous one")
     return cfg
 
 
@@ -559,7 +570,7 @@ class DecodeLayers:
             bt = torch.full((spec.batch, mb), -1, dtype=torch.int32, device=w.block_table.device)
             bt[:, :w.max_blocks] = w.block_table
             self.block_table = bt
-        flags = 0 if args.no_overlap else qdec.QDEC_LAUNCH_OVERLAP_PREVIOUS
+        flags = 0 if args.no_overlap or args.three_call else qdec.QDEC_LAUNCH_OVERLAP_PREVIOUS
         self.shape = qdec.Shape(batch=spec.batch, num_pages=spec.pool_pages,
                                 max_blocks_per_seq=mb,
                                 max_seq_len=max(plan_bound, w.max_blocks * P) if plan_bound
@@ -571,6 +582,8 @@ class DecodeLayers:
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
         self.out = torch.empty((spec.layers, spec.batch, spec.num_q_heads, spec.head_dim),
                                dtype=torch.bfloat16, device="cuda")
+        self.q_rot = (torch.empty((spec.batch, spec.num_q_heads, spec.head_dim),
+                                  dtype=torch.float32, device="cuda") if args.three_call else None)
 
     def step_fn(self, qkv, seq_lens, positions, block_table, out_t):
         """One decode step (the rope table, then every layer) on these buffers."""
@@ -580,7 +593,22 @@ class DecodeLayers:
         def fn():
             qdec.qdec_rope_table(shape, positions, self.rope, stream=s)
             for l in range(w.spec.layers):
-                if w.kv == "fp8":
+                q, k, v = qkv[l, :, :Hq], qkv[l, :, Hq:Hq + Hkv], qkv[l, :, Hq + Hkv:]
+                if self.args.three_call and w.kv == "fp8":
+                    qdec.qdec_append_rope_fp8(shape, q, k, v, w.w_q[l], w.w_k[l], positions,
+                                              seq_lens, block_table, w.pool8(l), w.scale(l),
+                                              self.q_rot, self.err, stream=s, rope_table=self.rope)
+                    qdec.qdec_attn_split_fp8(shape, self.q_rot, w.pool8(l), w.scale(l), block_table,
+                                             seq_lens, self.ws, out_t[l], self.err, stream=s)
+                    qdec.qdec_attn_merge(shape, seq_lens, self.ws, out_t[l], self.err, stream=s)
+                elif self.args.three_call:
+                    qdec.qdec_append_rope(shape, q, k, v, w.w_q[l], w.w_k[l], positions, seq_lens,
+                                          block_table, w.pool(l), self.q_rot, self.err, stream=s,
+                                          rope_table=self.rope)
+                    qdec.qdec_attn_split(shape, self.q_rot, w.pool(l), block_table, seq_lens,
+                                         self.ws, out_t[l], self.err, stream=s)
+                    qdec.qdec_attn_merge(shape, seq_lens, self.ws, out_t[l], self.err, stream=s)
+                elif w.kv == "fp8":
                     qdec.qdec_step_fp8(shape, qkv[l, :, :Hq], qkv[l, :, Hq:Hq + Hkv],
                                        qkv[l, :, Hq + Hkv:], w.w_q[l], w.w_k[l], positions,
                                        seq_lens, block_table, w.pool8(l), w.scale(l), self.ws,
@@ -790,10 +818,13 @@ def run_ours(args, dist: Dist):
     # over its L launches, so an upper bound of the launch's duration
     launch_us = t_steps_ms / args.steps / L * 1e3
     achieved = bytes_layer / (launch_us * 1e-6) / 1e9
-    roof_bytes, roof_kernel = bytes_layer, ("attention_kernel<fused, fp8>" if w.kv == "fp8"
-                                            else "attention_kernel<fused>")
-    roof_how = (f"CUDA events around each step's graph (rope table + {L} launches, gaps "
-                f"included) / {L}")
+    mode = "split" if args.three_call else "fused"
+    roof_bytes, roof_kernel = bytes_layer, (f"attention_kernel<{mode}, fp8>" if w.kv == "fp8"
+                                            else f"attention_kernel<{mode}>")
+    per_layer = 3 if args.three_call else 1
+    roof_how = (f"CUDA events around each step's graph (rope table + {per_layer * L} launches, "
+                f"gaps included) / {L}" + (": the three launches of a layer together"
+                                           if args.three_call else ""))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if args.qkv:
         # the projection kernel alone: a graph of its L launches, timed the same way
@@ -876,7 +907,7 @@ def run_ours(args, dist: Dist):
     layers.check()
 
     traffic = None
-    tr = TRAFFIC.get(workload_name(spec, w.kv, args.hidden if args.qkv else 0))
+    tr = TRAFFIC.get(workload_name(spec, w.kv, args.hidden if args.qkv else 0, args.three_call))
     if tr and tr["kernel_sha"] == kernel_sha("qkv_append_kernel" if args.qkv
                                              else "attention_kernel"):
         traffic = tr["bytes_per_launch"]
@@ -909,7 +940,8 @@ def run_ours(args, dist: Dist):
         cfg["plan"] = (f"planned for contexts up to {args.plan_bound} tokens (block-table rows "
                        f"of {layers.shape.max_blocks_per_seq} pages)")
     configs = []
-    if not args.qkv and not args.layers and not args.no_configs and not args.pool_pages:
+    if (not args.qkv and not args.layers and not args.no_configs and not args.pool_pages
+            and not args.three_call):
         # the other workloads of the benchmark plan, each on its own (the
         # headline's buffers are released first)
         del layers, run, w, step_in, flush
@@ -948,7 +980,7 @@ def run_ours(args, dist: Dist):
             "e2e": {"value": e2e_value and round(e2e_value, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": k_e2e},
-            "gpu_launches": ((2 * L if args.qkv else L) + 1) * args.steps,
+            "gpu_launches": ((2 * L if args.qkv else per_layer * L) + 1) * args.steps,
             "clocks": ck,
             "cpu_baseline": cpu,
         }

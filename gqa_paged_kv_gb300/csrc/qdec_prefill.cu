@@ -220,13 +220,18 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
 //               q enters as bf16),
 //   O += P V   (M 128, N 128, K 64: 4 MMAs; P read from tensor memory, V
 //               read in place from shared memory as an MN-major operand).
-// S is double-buffered in tensor memory per tile, so the scores of stage
-// j + 1 are formed while the softmax warps (warps 4 u .. 4 u + 3 for tile u,
-// thread r of the group owning row r, its tensor-memory lane) work on stage
-// j: load the 64 scores, mask keys past each row's token, keep a stale
-// running maximum (O in tensor memory is rescaled only when a stage's
-// maximum exceeds it by more than 2^8, so the weights stay below 256), and
-// write P as bf16 into tensor memory over the scores just read.  V rows of
+// Per tile, tensor memory holds S (64 columns), P (32 columns: two 16-bit
+// weights per column) and O (128 columns).  The softmax warps (warps
+// 4 u .. 4 u + 3 for tile u, thread r of the group owning row r, its
+// tensor-memory lane) load the 64 scores of stage j and at once hand S back,
+// so the scores of stage j + 1 are formed while they mask keys past each
+// row's token, keep a stale running maximum (O in tensor memory is rescaled
+// only when a stage's maximum exceeds it by more than 2^8, so the weights
+// stay below 256), and write P into its own columns once the value product
+// of stage j - 1 has read the previous P.  Over a bf16 pool a weight is
+// rounded to the nearest bf16 (ties away from zero) by an integer add on
+// its bits, and the row sum adds the rounded weights, the same numbers the
+// value product multiplies.  V rows of
 // keys past the sequence (or of pages not brought) are zeroed before a value
 // product reads them.  The epilogue reads O out of tensor memory, divides by
 // the row sum and stores the row.  Every wait is bounded; the decisions that
@@ -253,7 +258,7 @@ constexpr int kTcMmaWarp = kTcSoftmaxWarps + 1;
 constexpr int kTcVProducerWarp = kTcSoftmaxWarps + 2;      // V stages
 constexpr int kTcMmaWarp1 = kTcSoftmaxWarps + 3;           // tile 1's products (tile 0: kTcMmaWarp)
 constexpr int kTcThreads = (kTcSoftmaxWarps + 4) * 32;
-// tile u: S buffers at columns 256 u + {0, 64}, O at 256 u + 128
+// tile u: S at columns 256 u .. +63, P at 256 u + 64 .. +95, O at 256 u + 128 .. +255
 constexpr uint32_t kTcTmemCols = 256 * kTcTiles;
 static_assert(kTcTmemCols <= 512, "tensor memory");
 // FP8 pool: the K and V scales of a stage's four pages, written by the V
@@ -281,7 +286,7 @@ struct TcLayout {
     static constexpr int kScaleBytes = kFp8 ? (kTcKScaleRing + kTcVScaleRing) * 4 * 4 : 0;
     static constexpr int kOffTail = kOffScale + kScaleBytes;
     // tail: barriers k_full[S], k_empty[S], v_full[S], v_empty[S], staging
-    // full[2][kStg]; per tile s_full[2], (unused)[2], p_full[2], o_done[2];
+    // full[2][kStg]; per tile s_full, s_free, p_full, o_done (and four unused);
     // q_ready, done; then ints: abort, sequence, block, K stages issued,
     // tensor-memory address, V stages issued, the pages brought into every
     // V slot (bf16 pool) or every staging slot (FP8 pool)
@@ -359,11 +364,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t v_full0 = k_empty0 + 8 * S;
     const uint32_t v_empty0 = v_full0 + 8 * S;
     const uint32_t stg_full0 = v_empty0 + 8 * S;             // FP8: [plane][kStg]
-    // per tile u: s_full, p_full, o_done, two of each (buffer q)
+    // per tile u: s_full (the scores are in tensor memory), s_free (the
+    // softmax warps have loaded them), p_full (P is written), o_done (the
+    // value product has completed); one phase per stage each
     const uint32_t tile_bar0 = stg_full0 + 16 * Ly::kStg;
-    auto s_full = [&](int u, int q) { return tile_bar0 + 64 * u + 8 * q; };
-    auto p_full = [&](int u, int q) { return tile_bar0 + 64 * u + 32 + 8 * q; };
-    auto o_done = [&](int u, int q) { return tile_bar0 + 64 * u + 48 + 8 * q; };
+    auto s_full = [&](int u) { return tile_bar0 + 64 * u; };
+    auto s_free = [&](int u) { return tile_bar0 + 64 * u + 8; };
+    auto p_full = [&](int u) { return tile_bar0 + 64 * u + 16; };
+    auto o_done = [&](int u) { return tile_bar0 + 64 * u + 24; };
     const uint32_t q_ready = tile_bar0 + 64 * kTcTiles;
     const uint32_t done_bar = q_ready + 8;
     // misc: [0] abort, [1] sequence, [2] query block, [3] K stages issued,
@@ -430,11 +438,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             for (int q = 0; q < 2 * Ly::kStg; ++q) mbar_init(stg_full0 + 8 * q, 1);
             for (int u = 0; u < kTcTiles; ++u) {
-                for (int q = 0; q < 2; ++q) {
-                    mbar_init(s_full(u, q), 1);   // commit of the score product
-                    mbar_init(p_full(u, q), 4);   // the tile's softmax warps have written P
-                    mbar_init(o_done(u, q), 1);   // commit of the value product
-                }
+                mbar_init(s_full(u), 1);   // commit of the score product
+                mbar_init(s_free(u), 4);   // the tile's softmax warps have loaded S
+                mbar_init(p_full(u), 4);   // the tile's softmax warps have written P
+                mbar_init(o_done(u), 1);   // commit of the value product
             }
             mbar_init(q_ready, kTcSoftmaxWarps);
             mbar_init(done_bar, kTcTiles);  // each MMA issuer, once its products are done
@@ -534,30 +541,62 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
         } else {
             // FP8 pool: each stage's codes land in a staging slot (lanes 0-3
-            // each bring one page's plane, 2 KiB, and its scale); the warp
-            // then converts them to f16 (exact) into the ring slot, zeroing
-            // the rows of keys past the sequence or on pages not brought.
+            // each bring one page's plane, 2 KiB, and the V producer the
+            // stage's scales); the warp then converts them to f16 (exact) into
+            // the ring slot, zeroing the rows of keys past the sequence or on
+            // pages not brought.  Page ids are looked up 32 at a time (lane l:
+            // page 32 G + l of the sequence) two groups ahead and their scales
+            // one group ahead, so no global load stalls the conversions.
             constexpr int Q = Ly::kStg;
             uint8_t *stg = sm + Ly::kOffStg + plane * Q * Ly::kStgSlot;
             const uint32_t sfull0 = stg_full0 + 8 * Q * plane;
             volatile int *sm_mask = smask + Q * plane;
+            auto lookup = [&](int grp) {
+                const int pg = 32 * grp + lane;
+                return pg < npg ? p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg] : -1;
+            };
+            // the K and V scale of page `page` (0 for an invalid id)
+            auto scales = [&](int page, float &ks, float &vs) {
+                ks = vs = 0.f;
+                if (page >= 0 && page < p.num_pages) {
+                    const int64_t si = static_cast<int64_t>(page) * 2 * p.Hkv + g;
+                    ks = p.kv_scale[si];
+                    vs = p.kv_scale[si + p.Hkv];
+                }
+            };
+            int pc = lookup(0), pn = lookup(1), pn2 = lookup(2), grp = 0;
             // the chunk's keys and values were appended by the kernel before
             if (p.pdl) grid_dependency_wait();
+            float ksc = 0.f, vsc = 0.f, ksn = 0.f, vsn = 0.f;
+            if (isv) {
+                scales(pc, ksc, vsc);
+                scales(pn, ksn, vsn);
+            }
             auto issue = [&](int jj) {
+                const int G = jj * kTcPagesPerStage / 32;
+                if (G != grp) {  // stages are issued in order: the next group
+                    pc = pn;
+                    pn = pn2;
+                    pn2 = lookup(G + 2);
+                    if (isv) {
+                        ksc = ksn;
+                        vsc = vsn;
+                        scales(pn, ksn, vsn);
+                    }
+                    grp = G;
+                }
                 const int q = jj % Q;
                 const int pg = jj * kTcPagesPerStage + lane;
-                int page = -1;
-                if (lane < kTcPagesPerStage && pg < npg)
-                    page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg];
+                const int src = (jj * kTcPagesPerStage + (lane & 3)) & 31;
+                const int page = __shfl_sync(kFull, pc, src);
                 const bool ok = lane < kTcPagesPerStage && pg < npg && page >= 0 && page < p.num_pages;
                 if (!isv && lane < kTcPagesPerStage && pg < npg && !ok)
                     flag_error(p.err, QDEC_FLAG_BAD_PAGE);
                 const unsigned mask = __ballot_sync(kFull, ok) & 0xFu;
+                const float ks = __shfl_sync(kFull, ksc, src), vs = __shfl_sync(kFull, vsc, src);
                 if (isv && lane < kTcPagesPerStage) {  // both scales of each page of the stage
-                    const int64_t si = static_cast<int64_t>(page) * 2 * p.Hkv + g;
-                    kscale[(jj % kTcKScaleRing) * kTcPagesPerStage + lane] = ok ? p.kv_scale[si] : 0.f;
-                    vscale[(jj % kTcVScaleRing) * kTcPagesPerStage + lane] =
-                        ok ? p.kv_scale[si + p.Hkv] : 0.f;
+                    kscale[(jj % kTcKScaleRing) * kTcPagesPerStage + lane] = ok ? ks : 0.f;
+                    vscale[(jj % kTcVScaleRing) * kTcPagesPerStage + lane] = ok ? vs : 0.f;
                 }
                 const bool withheld = !isv && p.withhold_first && jj == 0;  // test hook
                 if (lane == 0) {
@@ -583,24 +622,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int mask = sm_mask[q];
                 const uint8_t *src = stg + q * Ly::kStgSlot;
                 uint8_t *dst = ringp + s * kTcSlotBytes;
-#pragma unroll 4
-                for (int i = 0; i < 16; ++i) {
-                    // key row kr (page kr / 16), codes 16 c .. 16 c + 15: the
-                    // f16 chunks 2 c' and 2 c' + 1 (c' = c % 4) of region c / 4
-                    const int e = lane + 32 * i, kr = e >> 3, c = e & 7, tr = kr & 15;
-                    const bool zero = j * kTcKeys + kr >= L || !((mask >> (kr >> 4)) & 1);
-                    uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-                    if (!zero) {
-                        const uint4 codes = *reinterpret_cast<const uint4 *>(
-                            src + (kr >> 4) * kFp8PlaneBytes + tr * 128 + ((c ^ (tr & 7)) << 4));
-                        lo = make_uint4(e4m3x2_to_f16x2(codes.x), e4m3x2_to_f16x2(codes.x >> 16),
-                                        e4m3x2_to_f16x2(codes.y), e4m3x2_to_f16x2(codes.y >> 16));
-                        hi = make_uint4(e4m3x2_to_f16x2(codes.z), e4m3x2_to_f16x2(codes.z >> 16),
-                                        e4m3x2_to_f16x2(codes.w), e4m3x2_to_f16x2(codes.w >> 16));
+                // lane l, item i = 8 h + i': key row kr (page kr / 16), codes
+                // 16 c .. 16 c + 15, to the f16 chunks 2 c' and 2 c' + 1
+                // (c' = c % 4) of region c / 4.  Eight items' codes are
+                // loaded before any is stored (the stores could alias the
+                // loads as far as the compiler knows, which would serialise
+                // them item by item).
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint4 cv[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int e = lane + 32 * (8 * h + i), kr = e >> 3, c = e & 7, tr = kr & 15;
+                        const bool zero = j * kTcKeys + kr >= L || !((mask >> (kr >> 4)) & 1);
+                        cv[i] = zero ? make_uint4(0u, 0u, 0u, 0u)
+                                     : *reinterpret_cast<const uint4 *>(
+                                           src + (kr >> 4) * kFp8PlaneBytes + tr * 128 +
+                                           ((c ^ (tr & 7)) << 4));
                     }
-                    uint8_t *reg = dst + (c >> 2) * kTcRegion;
-                    *reinterpret_cast<uint4 *>(reg + sw128_off(kr, 2 * (c & 3))) = lo;
-                    *reinterpret_cast<uint4 *>(reg + sw128_off(kr, 2 * (c & 3) + 1)) = hi;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int e = lane + 32 * (8 * h + i), kr = e >> 3, c = e & 7;
+                        const uint4 w = cv[i];   // zero codes convert to +0
+                        const uint4 lo = make_uint4(e4m3x2_to_f16x2(w.x), e4m3x2_to_f16x2(w.x >> 16),
+                                                    e4m3x2_to_f16x2(w.y), e4m3x2_to_f16x2(w.y >> 16));
+                        const uint4 hi = make_uint4(e4m3x2_to_f16x2(w.z), e4m3x2_to_f16x2(w.z >> 16),
+                                                    e4m3x2_to_f16x2(w.w), e4m3x2_to_f16x2(w.w >> 16));
+                        uint8_t *reg = dst + (c >> 2) * kTcRegion;
+                        *reinterpret_cast<uint4 *>(reg + sw128_off(kr, 2 * (c & 3))) = lo;
+                        *reinterpret_cast<uint4 *>(reg + sw128_off(kr, 2 * (c & 3) + 1)) = hi;
+                    }
                 }
                 fence_proxy_async_smem();  // read next by the tensor core
                 __syncwarp();
@@ -627,38 +678,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                            : tc::idesc_bf16(kTcRows, kHeadDim, true);
             const uint32_t tile_tm = tmem + 256 * u;
             // O += P_t V_t once V_t has landed and the tile's softmax warps
-            // have written P (over the scores of stage t, in tensor memory);
-            // the commits free that buffer for the scores of stage t + 2
-            // (o_done) and, with the other tile's, the V slot (v_empty)
+            // have written P; the commits free P for the weights of stage
+            // t + 1 (o_done) and, with the other tile's, the V slot (v_empty)
             auto value_product = [&](int t) -> bool {
                 if (!mbar_wait_bounded(v_full0 + 8 * (t % S), (t / S) & 1, misc, p.wait_cycles) ||
-                    !mbar_wait_bounded(p_full(u, t & 1), (t >> 1) & 1, misc, p.wait_cycles))
+                    !mbar_wait_bounded(p_full(u), t & 1, misc, p.wait_cycles))
                     return false;
                 tc::fence_after();
                 const uint32_t vst = vring + (t % S) * kTcSlotBytes;
-                const uint32_t tp = tile_tm + (t & 1) * kTcKeys;  // P: 32 columns
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk)
-                    tc::mma_ts(tile_tm + 128, tp + 8 * kk,
+                    tc::mma_ts(tile_tm + 128, tile_tm + 64 + 8 * kk,
                                tc::desc_sw128(vst + kk * 2048, kTcRegion, 1024), kIdO,
                                t > 0 || kk > 0);
-                tc::commit(o_done(u, t & 1));
+                tc::commit(o_done(u));
                 tc::commit(v_empty0 + 8 * (t % S));
                 return true;
             };
             bool ok = mbar_wait_bounded(q_ready, 0, misc, p.wait_cycles);
             for (int j = 0; ok && j < ntiles; ++j) {
                 const int s = j % S;
-                // the buffer holds P of stage j - 2 until its value product is done
+                // S is free once the softmax warps have loaded the scores of
+                // stage j - 1
                 if (!mbar_wait_bounded(k_full0 + 8 * s, (j / S) & 1, misc, p.wait_cycles) ||
-                    (j >= 2 && !mbar_wait_bounded(o_done(u, j & 1), ((j - 2) >> 1) & 1, misc,
-                                                  p.wait_cycles))) {
+                    (j >= 1 && !mbar_wait_bounded(s_free(u), (j - 1) & 1, misc, p.wait_cycles))) {
                     ok = false;
                     break;
                 }
                 tc::fence_after();
                 const uint32_t kst = kring + s * kTcSlotBytes;
-                const uint32_t tS = tile_tm + (j & 1) * kTcKeys;
+                const uint32_t tS = tile_tm;
 #pragma unroll
                 for (int kk = 0; kk < kHeadDim / 16; ++kk) {
                     const uint32_t o = (kk >> 2) * kTcRegion + 32 * (kk & 3);
@@ -666,7 +715,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc::mma(tS, tc::desc_sw128(qt + qo, 16, 1024),
                             tc::desc_sw128(kst + o, 16, 1024), kIdS, kk > 0);
                 }
-                tc::commit(s_full(u, j & 1));
+                tc::commit(s_full(u));
                 tc::commit(k_empty0 + 8 * s);  // with the other tile's: the K slot is free
                 if (j >= 1 && !value_product(j - 1)) ok = false;
             }
@@ -731,7 +780,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
             const int s = j % S;
-            if (!wait_all(s_full(u, j & 1), (j >> 1) & 1)) {
+            if (!wait_all(s_full(u), j & 1)) {
                 ok = false;
                 break;
             }
@@ -739,8 +788,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float sc[kTcKeys];
             {
                 uint32_t v0[32], v1[32];
-                tc::ld32(v0, trow + (j & 1) * kTcKeys);
-                tc::ld32(v1, trow + (j & 1) * kTcKeys + 32);
+                tc::ld32(v0, trow);
+                tc::ld32(v1, trow + 32);
                 tc::wait_ld();
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
@@ -748,6 +797,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     sc[32 + c] = __uint_as_float(v1[c]);
                 }
             }
+            // the scores are in registers: S may take the next stage's
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free(u));
             // FP8 pool: the stage's scales, once its V slot is full (the V
             // producer wrote them before); the scores of page q of the stage
             // times its K scale
@@ -788,7 +841,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 m = mn;
                 if (j > 0) {
                     // O holds stages 0 .. j-1 once their last product is done
-                    if (!wait_all(o_done(u, (j - 1) & 1), ((j - 1) >> 1) & 1)) {
+                    if (!wait_all(o_done(u), (j - 1) & 1)) {
                         ok = false;
                         break;
                     }
@@ -807,21 +860,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc::fence_before();
                 }
             }
-            // P over the first 32 columns of the scores just read (a column
-            // holds two consecutive keys), the A operand of the value product;
-            // over an FP8 pool each weight times its page's V scale (the row
-            // sum keeps the unscaled weights)
+            // P (a column holds two consecutive keys), the A operand of the
+            // value product.  bf16 pool: each weight rounded to the nearest
+            // bf16 (ties away from zero: 0x8000 added to its bits, the upper
+            // half kept), the row sum over the rounded weights; FP8 pool:
+            // f16 weights times their page's V scale, the row sum over the
+            // unscaled weights
             float ps[4] = {0.f, 0.f, 0.f, 0.f};   // the row sum in four chains
             uint32_t pw[kTcKeys / 2];
 #pragma unroll
             for (int c = 0; c < kTcKeys / 2; ++c) {
                 const float p0 = fast_exp2(sc[2 * c] - m);
                 const float p1 = fast_exp2(sc[2 * c + 1] - m);
-                ps[c & 3] += p0 + p1;
-                const float sv = vs[(2 * c) / kPageSize];
-                pw[c] = pack16x2<kFp8>(p0 * sv, p1 * sv);
+                if constexpr (kFp8) {
+                    ps[c & 3] += p0 + p1;
+                    const float sv = vs[(2 * c) / kPageSize];
+                    pw[c] = pack16x2<kFp8>(p0 * sv, p1 * sv);
+                } else {
+                    const uint32_t r0 = __float_as_uint(p0) + 0x8000u;
+                    const uint32_t r1 = __float_as_uint(p1) + 0x8000u;
+                    ps[c & 3] += __uint_as_float(r0 & 0xFFFF0000u) + __uint_as_float(r1 & 0xFFFF0000u);
+                    pw[c] = __byte_perm(r0, r1, 0x7632);
+                }
             }
-            tc::st32(trow + (j & 1) * kTcKeys, pw);
+            // P of stage j - 1 stays until its value product is done
+            if (j > 0) {
+                if (!wait_all(o_done(u), (j - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after();
+            }
+            tc::st32(trow + 64, pw);
             l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
             if constexpr (!kFp8) {
                 // V rows of keys past the sequence (and of pages not brought
@@ -846,7 +916,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             fence_proxy_async_smem();  // the zeroed rows are read by the tensor core
             tc::fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full(u, j & 1));
+            if (lane == 0) mbar_arrive(p_full(u));
         }
         // ---- epilogue: O / l for this row, after every product has completed
         volatile int never = 0;
