@@ -65,14 +65,70 @@ static __device__ __forceinline__ __nv_bfloat16 ff_to_bf16(ff y) {
     return __float2bfloat16_rn(y.hi);
 }
 
+// Whether every value within err of y has the same nearest-even bf16 as y:
+// y is a normal float, no bf16 rounding boundary (the midpoint of two
+// consecutive bf16 values) lies within err of it, and err is below an eighth
+// of its bf16 spacing (so the boundaries of the neighbouring intervals, at
+// least a quarter spacing away, are out of reach too).
+static __device__ __forceinline__ bool bf16_rounding_certain(float y, float err) {
+    const uint32_t a = __float_as_uint(y) & 0x7FFFFFFFu;
+    if (a < 0x00800000u || a >= 0x7F800000u) return false;  // zero, subnormal, inf, NaN
+    const float mid = __uint_as_float((a & 0xFFFF0000u) | 0x8000u);
+    const float eighth = __uint_as_float(a & 0x7F800000u) * 0x1p-10f;  // 2^e x 2^-7 / 8
+    return fabsf(__uint_as_float(a) - mid) > err && err < eighth;  // the difference is exact
+}
+
 // The new key row (sequence b, KV head g) on one warp, lane l holding dims
-// 2l, 2l+1, 64+2l, 65+2l: RMSNorm and RoPE in float-float arithmetic, then
-// one rounding to bf16.  x*w is exact in fp32 (two bf16 values), so is x^2.
+// 2l, 2l+1, 64+2l, 65+2l: RMSNorm and RoPE, one rounding to bf16, the
+// nearest-even bf16 of the exact value.  x*w is exact in fp32 (two bf16
+// values), so is x^2.
+//
+// First in fp32, with an a-priori bound on the error (u = 2^-24): the sum of
+// squares passes through at most 7 roundings (8u relative, all terms
+// positive); v = ss/D + eps one more (9u); r = 1/sqrt(v) by IEEE square root
+// and division (6.5u); n = (x w) r one more (7.5u); the rotated element
+// y = n_a c - n_b s as fma(n_a, c, -fl(n_b s)) with c, s the float parts of
+// the angle (u each): |y32 - y| <= 9.6u (|n_a c| + |n_b s|) + 1.01u |y32|,
+// below 16u (|n_a c| + |n_b s| + |y32|) as computed.  When no element of the
+// row lies that close to a bf16 rounding boundary (most rows), its rounding
+// is final; otherwise the whole row is redone in float-float arithmetic
+// (about 48 significant bits).  Rows with a sum of squares under 2^-100 (or
+// not finite) take the float-float path as well, where the bound's premises
+// (no underflow in x^2 or x w) could fail.
 static __device__ void key_row(float eps, __nv_bfloat162 ka, __nv_bfloat162 kc, __nv_bfloat162 wa,
                         __nv_bfloat162 wc, const RopeEntry &e0, const RopeEntry &e1,
                         __nv_bfloat16 (&kb)[4]) {
     const float x[4] = {__low2float(ka), __high2float(ka), __low2float(kc), __high2float(kc)};
     const float wv[4] = {__low2float(wa), __high2float(wa), __low2float(wc), __high2float(wc)};
+    {
+        float sq = __fadd_rn(__fadd_rn(__fmul_rn(x[0], x[0]), __fmul_rn(x[1], x[1])),
+                             __fadd_rn(__fmul_rn(x[2], x[2]), __fmul_rn(x[3], x[3])));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, o));
+        const float v = fmaf(sq, 1.0f / kHeadDim, eps);
+        const float r = __fdiv_rn(1.0f, __fsqrt_rn(v));
+        float n[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) n[e] = __fmul_rn(__fmul_rn(x[e], wv[e]), r);
+        // element e rotates n[e] and n[e ^ 2] by angle e & 1
+        float y[4];
+        bool ok = sq >= 0x1p-100f && sq <= 0x1p100f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float c = (e & 1) ? e1.c_hi : e0.c_hi, sn = (e & 1) ? e1.s_hi : e0.s_hi;
+            const float a = n[e], b = n[e ^ 2];
+            // e < 2: a c - b s; e >= 2: a c + b s (b is the first half)
+            const float t = __fmul_rn(b, sn);
+            y[e] = fmaf(a, c, e < 2 ? -t : t);
+            const float mag = __fadd_rn(fabsf(__fmul_rn(a, c)), fabsf(t));
+            ok = ok && bf16_rounding_certain(y[e], 0x1p-20f * __fadd_rn(mag, fabsf(y[e])));
+        }
+        if (__all_sync(0xffffffffu, ok)) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) kb[e] = __float2bfloat16_rn(y[e]);
+            return;
+        }
+    }
     ff ss = {x[0] * x[0], 0.f};
 #pragma unroll
     for (int e = 1; e < 4; ++e) ss = ff_add(ss, ff{x[e] * x[e], 0.f});

@@ -230,8 +230,7 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
 // stay below 256), and write P into its own columns once the value product
 // of stage j - 1 has read the previous P.  Over a bf16 pool a weight is
 // rounded to the nearest bf16 (ties away from zero) by an integer add on
-// its bits, and the row sum adds the rounded weights, the same numbers the
-// value product multiplies.  V rows of
+// its bits (the conversion instruction costs more issue slots).  V rows of
 // keys past the sequence (or of pages not brought) are zeroed before a value
 // product reads them.  The epilogue reads O out of tensor memory, divides by
 // the row sum and stores the row.  Every wait is bounded; the decisions that
@@ -861,11 +860,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             // P (a column holds two consecutive keys), the A operand of the
-            // value product.  bf16 pool: each weight rounded to the nearest
-            // bf16 (ties away from zero: 0x8000 added to its bits, the upper
-            // half kept), the row sum over the rounded weights; FP8 pool:
-            // f16 weights times their page's V scale, the row sum over the
-            // unscaled weights
+            // value product, and the row sum of the fp32 weights.  bf16 pool:
+            // each weight rounded to the nearest bf16 (ties away from zero:
+            // 0x8000 added to its bits, the upper half kept); FP8 pool: f16
+            // weights times their page's V scale
             float ps[4] = {0.f, 0.f, 0.f, 0.f};   // the row sum in four chains
             uint32_t pw[kTcKeys / 2];
 #pragma unroll
@@ -877,10 +875,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const float sv = vs[(2 * c) / kPageSize];
                     pw[c] = pack16x2<kFp8>(p0 * sv, p1 * sv);
                 } else {
-                    const uint32_t r0 = __float_as_uint(p0) + 0x8000u;
-                    const uint32_t r1 = __float_as_uint(p1) + 0x8000u;
-                    ps[c & 3] += __uint_as_float(r0 & 0xFFFF0000u) + __uint_as_float(r1 & 0xFFFF0000u);
-                    pw[c] = __byte_perm(r0, r1, 0x7632);
+                    ps[c & 3] += p0 + p1;
+                    pw[c] = __byte_perm(__float_as_uint(p0) + 0x8000u, __float_as_uint(p1) + 0x8000u,
+                                        0x7632);
                 }
             }
             // P of stage j - 1 stays until its value product is done
