@@ -65,6 +65,65 @@ static __device__ __forceinline__ __nv_bfloat16 ff_to_bf16(ff y) {
     return __float2bfloat16_rn(y.hi);
 }
 
+// ---------------------------------------------- cos and sin, float-float --
+// (cos theta, sin theta) as normalised float pairs (about 46 significant
+// bits), from fp32 arithmetic after a double-precision argument reduction
+// (the GPU's fp64 rate makes a double sincos per angle the bound of a kernel
+// that needs many angles).  Reduction (Cody and Waite 1980): k = the integer
+// nearest theta * 2/pi, r = theta - k pi/2 with pi/2 the sum of two doubles,
+// both products through fused multiply-adds, so |r| <= pi/4 (plus rounding)
+// with an absolute error near 1e-16 for |k| < 2^31.  Then the Taylor series
+// about 0 in x = r (a float pair) and x^2: sin x = x + x x^2 P(x^2), cos x =
+// 1 + x^2 Q(x^2), P and Q with the coefficients (-1)^n / (2n+1)! and
+// (-1)^n / (2n+2)!; the terms whose magnitude stays below 1e-7 are summed in
+// float, the rest in float-float.  The remainders after x^17 and x^18 are
+// below 1e-19 for |x| <= pi/4.  The quadrant k mod 4 swaps and negates.
+static __device__ __forceinline__ ff ff_const(double d) {
+    const float h = static_cast<float>(d);
+    return {h, static_cast<float>(d - static_cast<double>(h))};
+}
+static __device__ RopeEntry ff_sincos(double theta) {
+    constexpr double kHalfPiHi = 1.5707963267948966;      // pi/2 rounded to a double
+    constexpr double kHalfPiLo = 6.123233995736766e-17;   // pi/2 minus that, rounded
+    constexpr double kTwoOverPi = 0.6366197723675814;
+    const double kq = rint(theta * kTwoOverPi);
+    double r = fma(-kq, kHalfPiHi, theta);
+    r = fma(-kq, kHalfPiLo, r);
+    const int q = static_cast<int>(static_cast<long long>(kq) & 3);
+    const float rh = static_cast<float>(r);
+    const ff x = {rh, static_cast<float>(r - static_cast<double>(rh))};
+    const ff x2 = ff_mul(x, x);
+    const float z = x2.hi;
+    // 1/n! for n = 2 .. 18
+    constexpr double f2 = 1.0 / 2, f3 = f2 / 3, f4 = f3 / 4, f5 = f4 / 5, f6 = f5 / 6,
+                     f7 = f6 / 7, f8 = f7 / 8, f9 = f8 / 9, f10 = f9 / 10, f11 = f10 / 11,
+                     f12 = f11 / 12, f13 = f12 / 13, f14 = f13 / 14, f15 = f14 / 15,
+                     f16 = f15 / 16, f17 = f16 / 17, f18 = f17 / 18;
+    // sin: P = -f3 + z (f5 + z (-f7 + z (f9 + z (-f11 + z (f13 + z (-f15 + z f17))))))
+    const float ts = static_cast<float>(-f11) +
+                     z * (static_cast<float>(f13) +
+                          z * (static_cast<float>(-f15) + z * static_cast<float>(f17)));
+    ff ps = ff_add(ff_const(f9), ff_mul_f(x2, ts));
+    ps = ff_add(ff_const(-f7), ff_mul(x2, ps));
+    ps = ff_add(ff_const(f5), ff_mul(x2, ps));
+    ps = ff_add(ff_const(-f3), ff_mul(x2, ps));
+    const ff sn = ff_add(x, ff_mul(x, ff_mul(x2, ps)));
+    // cos: Q = -f2 + z (f4 + z (-f6 + z (f8 + z (-f10 + z (f12 + z (-f14 + z (f16 - z f18)))))))
+    const float tc = static_cast<float>(f12) +
+                     z * (static_cast<float>(-f14) +
+                          z * (static_cast<float>(f16) + z * static_cast<float>(-f18)));
+    ff pc = ff_add(ff_const(-f10), ff_mul_f(x2, tc));
+    pc = ff_add(ff_const(f8), ff_mul(x2, pc));
+    pc = ff_add(ff_const(-f6), ff_mul(x2, pc));
+    pc = ff_add(ff_const(f4), ff_mul(x2, pc));
+    pc = ff_add(ff_const(-f2), ff_mul(x2, pc));
+    const ff cs = ff_add(ff{1.0f, 0.0f}, ff_mul(x2, pc));
+    // theta = r + q pi/2
+    const ff c = (q == 0) ? cs : (q == 1) ? ff_neg(sn) : (q == 2) ? ff_neg(cs) : sn;
+    const ff s = (q == 0) ? sn : (q == 1) ? cs : (q == 2) ? ff_neg(sn) : ff_neg(cs);
+    return {c.hi, c.lo, s.hi, s.lo};
+}
+
 // Whether every value within err of y has the same nearest-even bf16 as y:
 // y is a normal float, no bf16 rounding boundary (the midpoint of two
 // consecutive bf16 values) lies within err of it, and err is below an eighth

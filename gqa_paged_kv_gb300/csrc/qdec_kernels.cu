@@ -228,19 +228,15 @@ __device__ __forceinline__ uint32_t pack_bf16(__nv_bfloat16 lo, __nv_bfloat16 hi
 
 // ------------------------------------------------------------ RoPE angles --
 // Angle i of position pos is pos * theta^(-2i/D), formed in double (the
-// frequency comes in as a double).  precise: cos/sin from double sincos,
-// split into float pairs; otherwise the angle is reduced modulo 2 pi in
-// double and sin/cos are taken in fp32 (the lo parts are then zero).
+// frequency comes in as a double).  precise: cos/sin as float pairs from
+// ff_sincos (double reduction, float-float series); otherwise the angle is
+// reduced modulo 2 pi in double and sin/cos are taken in fp32 (the lo parts
+// are then zero).
 __device__ RopeEntry rope_entry(int pos, double inv_freq, bool precise) {
     const double th = static_cast<double>(pos) * inv_freq;
     RopeEntry e;
     if (precise) {
-        double sn, cn;
-        sincos(th, &sn, &cn);
-        e.c_hi = static_cast<float>(cn);
-        e.c_lo = static_cast<float>(cn - static_cast<double>(e.c_hi));
-        e.s_hi = static_cast<float>(sn);
-        e.s_lo = static_cast<float>(sn - static_cast<double>(e.s_hi));
+        e = ff_sincos(th);
     } else {
         const double kq = rint(th * kInvTwoPi);
         double red = fma(-kq, kTwoPiHi, th);
@@ -1450,9 +1446,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kCluster, kFp8))
 // ------------------------------------------------------------ rope table --
 constexpr int kRopeThreads = 32;
 // cos/sin of every (sequence, frequency) of the step, computed once and
-// shared by all layers (the angles depend on the positions only).  One
-// double-precision sincos per thread, spread over many small CTAs (fp64 is
-// slow per SM).  A following attention launch may start early: it reads the
+// shared by all layers (the angles depend on the positions only), one angle
+// per thread over many small CTAs.  A following attention launch may start early: it reads the
 // table only after its dependency wait.
 __global__ void __launch_bounds__(kRopeThreads) rope_table_kernel(const __grid_constant__ Params p) {
     launch_dependents();

@@ -81,7 +81,7 @@ __device__ __forceinline__ bool chunk_ok(const Params &p, int b, int &n, int &L)
 
 // ------------------------------------------------------------------ append --
 // One CTA per chunk row, 256 threads: the 64 angles of the row's position are
-// taken once (double sincos) into shared memory; warp w then handles KV head
+// taken once (ff_sincos: float pairs) into shared memory; warp w then handles KV head
 // w (and w + 8, ...): its four query rows in fp32 (q_rot's tolerance is
 // absolute), its key row in float-float arithmetic rounded once to bf16 (the
 // decode append's rule: the nearest-even bf16 of the exact value), and the
@@ -98,7 +98,7 @@ __device__ __forceinline__ uint16_t quantize_pair_e4m3(float a, float b, float s
 template <bool kFp8>
 __global__ void __launch_bounds__(kPfAppendThreads) prefill_append_kernel(
     const __grid_constant__ Params p) {
-    __shared__ double cs_d[kRotPairs], sn_d[kRotPairs];
+    __shared__ RopeEntry rs[kRotPairs];
     const int r = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = seq_of_row(p.qo_indptr, p.B, r);
@@ -109,14 +109,11 @@ __global__ void __launch_bounds__(kPfAppendThreads) prefill_append_kernel(
     }
     const int t = L - n + (r - p.qo_indptr[b]);  // token index in the sequence
     if (threadIdx.x < kRotPairs)  // angle i: positions[r] * theta^(-2i/D)
-        sincos(static_cast<double>(p.positions[r]) * p.inv_freq[threadIdx.x], &sn_d[threadIdx.x],
-               &cs_d[threadIdx.x]);
+        rs[threadIdx.x] = ff_sincos(static_cast<double>(p.positions[r]) * p.inv_freq[threadIdx.x]);
     __syncthreads();
     // this lane's rotate-half pairs i = 2 lane, 2 lane + 1: dims i and i + 64
-    const double c0 = cs_d[2 * lane], c1 = cs_d[2 * lane + 1];
-    const double s0 = sn_d[2 * lane], s1 = sn_d[2 * lane + 1];
-    const float fc0 = static_cast<float>(c0), fc1 = static_cast<float>(c1);
-    const float fs0 = static_cast<float>(s0), fs1 = static_cast<float>(s1);
+    const RopeEntry e0 = rs[2 * lane], e1 = rs[2 * lane + 1];
+    const float fc0 = e0.c_hi, fc1 = e1.c_hi, fs0 = e0.s_hi, fs1 = e1.s_hi;
     // RMSNorm (eps inside the root) of one 128-dim row; x w is exact in fp32
     // (a product of two bf16).  Returns the root; n holds x w for dims
     // 2 lane, 2 lane + 1, 64 + 2 lane, 64 + 2 lane + 1.
@@ -155,10 +152,6 @@ __global__ void __launch_bounds__(kPfAppendThreads) prefill_append_kernel(
             ((static_cast<int64_t>(page) * 2 * p.Hkv + g) * kPageSize + t % kPageSize) * kHeadDim;
         // the key: norm and rotation in float-float, one rounding to bf16
         const __nv_bfloat16 *krow = p.k + static_cast<int64_t>(r) * p.k_stride + g * kHeadDim;
-        const RopeEntry e0 = {fc0, static_cast<float>(c0 - static_cast<double>(fc0)), fs0,
-                              static_cast<float>(s0 - static_cast<double>(fs0))};
-        const RopeEntry e1 = {fc1, static_cast<float>(c1 - static_cast<double>(fc1)), fs1,
-                              static_cast<float>(s1 - static_cast<double>(fs1))};
         __nv_bfloat16 kb[4];
         key_row(p.eps, reinterpret_cast<const __nv_bfloat162 *>(krow)[lane],
                 reinterpret_cast<const __nv_bfloat162 *>(krow + 64)[lane],

@@ -167,6 +167,32 @@ def test_rope_table_values():
     assert np.max(np.abs(t[..., 2] + t[..., 3] - np.sin(ang))) < 1e-13
 
 
+def test_rope_table_values_at_large_positions():
+    """The float pairs (double reduction by pi/2, float-float series) stay
+    within 1e-13 of cos/sin of the double angle for positions far past any
+    context, where the reduction takes out up to ~10^6 quarter turns; the
+    bound adds pos x 2^-52 for a possible last-bit difference between the
+    host's and numpy's theta^(-2i/D)."""
+    q = parity.qdec()
+    pos = torch.tensor([0, 1, 2, 3, 1023, 40960, 65535, 131071, 777777, 1 << 20],
+                       dtype=torch.int32)
+    B = pos.numel()
+    shape = q.Shape(batch=B, num_pages=B, max_blocks_per_seq=1, max_seq_len=16)
+    rope = q.alloc_rope_table(shape)
+    q.qdec_rope_table(shape, pos.cuda(), rope)
+    torch.cuda.synchronize()
+    t = rope.view(torch.float32).view(B, 64, 4).double().cpu().numpy()
+    p = pos.numpy().astype(np.float64)
+    ang = p[:, None] * (1e6 ** (-2.0 * np.arange(64) / 128))[None, :]
+    tol = 1e-13 + p[:, None] * 2.0 ** -52
+    assert np.all(np.abs(t[..., 0] + t[..., 1] - np.cos(ang)) <= tol)
+    assert np.all(np.abs(t[..., 2] + t[..., 3] - np.sin(ang)) <= tol)
+    # the pairs are normalised: |lo| at most half an ulp of hi
+    for k in (0, 2):
+        hi, lo = t[..., k], t[..., k + 1]
+        assert np.all(np.abs(lo) <= np.spacing(np.abs(hi).astype(np.float32)).astype(np.float64) / 2 + 1e-45)
+
+
 @pytest.mark.parametrize("num_ctas", [0, 5])
 def test_overlapped_layers_match_serial_layers(num_ctas):
     """Programmatic dependent launch of consecutive layers changes no bit,
