@@ -131,6 +131,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the 36 calls eagerly")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--two-call", action="store_true",
+                    help="each layer as qdec_append_rope then qdec_attn_decode (step 4 and its "
+                         "merge in one launch) instead of the one-launch qdec_step")
     ap.add_argument("--three-call", action="store_true",
                     help="each layer as qdec_append_rope, qdec_attn_split, qdec_attn_merge "
                          "(launched one after another) instead of the one-launch qdec_step")
@@ -273,9 +276,16 @@ def l2_bytes(dev=None) -> int:
     return L2_BYTES_NOMINAL
 
 
-def workload_name(spec, kv: str, qkv_hidden: int = 0, three_call: bool = False) -> str:
+def workload_name(spec, kv: str, qkv_hidden: int = 0, calls: int = 1) -> str:
     return (spec.name + ("-fp8kv" if kv == "fp8" else "")
-            + (f"-qkv{qkv_hidden}" if qkv_hidden else "") + ("-threecall" if three_call else ""))
+            + (f"-qkv{qkv_hidden}" if qkv_hidden else "")
+            + {1: "", 2: "-twocall", 3: "-threecall"}[calls])
+
+
+def calls_per_layer(args) -> int:
+    """Launches of one decode layer-step: qdec_step, or the two- or
+    three-call decompositions."""
+    return 3 if getattr(args, "three_call", False) else 2 if getattr(args, "two_call", False) else 1
 
 
 def qkv_weight_bytes(spec, hidden: int) -> int:
@@ -329,12 +339,18 @@ def workload_config(w: wl.Workload, args, world: int, l2: int = L2_BYTES_NOMINAL
         cfg["hidden"] = qkv_hidden
         cfg["launch"] = (f"CUDA graphs: rope table + {L} x (qdec_qkv_append_rope, "
                          f"qdec_attn_decode)")
-    elif getattr(args, "three_call", False):
+    elif calls_per_layer(args) == 3:
         sfx = "_fp8" if w.kv == "fp8" else ""
-        cfg["workload"] = workload_name(spec, w.kv, 0, True)
+        cfg["workload"] = workload_name(spec, w.kv, 0, 3)
         cfg["launch"] = ("eager" if args.no_graph else "CUDA graphs") + (
             f": rope table + {L} x (qdec_append_rope{sfx}, qdec_attn_split{sfx}, "
             f"qdec_attn_merge), each launch after the previous one")
+    elif calls_per_layer(args) == 2:
+        sfx = "_fp8" if w.kv == "fp8" else ""
+        cfg["workload"] = workload_name(spec, w.kv, 0, 2)
+        cfg["launch"] = ("eager" if args.no_graph else "CUDA graphs") + (
+            f": rope table + {L} x (qdec_append_rope{sfx}, qdec_attn_decode{sfx})"
+            + ("" if args.no_overlap else ", programmatic dependent launch"))
     return cfg
 
 
@@ -570,7 +586,7 @@ class DecodeLayers:
             bt = torch.full((spec.batch, mb), -1, dtype=torch.int32, device=w.block_table.device)
             bt[:, :w.max_blocks] = w.block_table
             self.block_table = bt
-        flags = 0 if args.no_overlap or args.three_call else qdec.QDEC_LAUNCH_OVERLAP_PREVIOUS
+        flags = 0 if args.no_overlap or calls_per_layer(args) == 3 else qdec.QDEC_LAUNCH_OVERLAP_PREVIOUS
         self.shape = qdec.Shape(batch=spec.batch, num_pages=spec.pool_pages,
                                 max_blocks_per_seq=mb,
                                 max_seq_len=max(plan_bound, w.max_blocks * P) if plan_bound
@@ -583,7 +599,8 @@ class DecodeLayers:
         self.out = torch.empty((spec.layers, spec.batch, spec.num_q_heads, spec.head_dim),
                                dtype=torch.bfloat16, device="cuda")
         self.q_rot = (torch.empty((spec.batch, spec.num_q_heads, spec.head_dim),
-                                  dtype=torch.float32, device="cuda") if args.three_call else None)
+                                  dtype=torch.float32, device="cuda")
+                      if args.three_call or args.two_call else None)
 
     def step_fn(self, qkv, seq_lens, positions, block_table, out_t):
         """One decode step (the rope table, then every layer) on these buffers."""
@@ -601,6 +618,19 @@ class DecodeLayers:
                     qdec.qdec_attn_split_fp8(shape, self.q_rot, w.pool8(l), w.scale(l), block_table,
                                              seq_lens, self.ws, out_t[l], self.err, stream=s)
                     qdec.qdec_attn_merge(shape, seq_lens, self.ws, out_t[l], self.err, stream=s)
+                elif self.args.two_call and w.kv == "fp8":
+                    qdec.qdec_append_rope_fp8(shape, q, k, v, w.w_q[l], w.w_k[l], positions,
+                                              seq_lens, block_table, w.pool8(l), w.scale(l),
+                                              self.q_rot, self.err, stream=s, rope_table=self.rope)
+                    qdec.qdec_attn_decode_fp8(shape, self.q_rot, w.pool8(l), w.scale(l),
+                                              block_table, seq_lens, self.ws, out_t[l], self.err,
+                                              stream=s)
+                elif self.args.two_call:
+                    qdec.qdec_append_rope(shape, q, k, v, w.w_q[l], w.w_k[l], positions, seq_lens,
+                                          block_table, w.pool(l), self.q_rot, self.err, stream=s,
+                                          rope_table=self.rope)
+                    qdec.qdec_attn_decode(shape, self.q_rot, w.pool(l), block_table, seq_lens,
+                                          self.ws, out_t[l], self.err, stream=s)
                 elif self.args.three_call:
                     qdec.qdec_append_rope(shape, q, k, v, w.w_q[l], w.w_k[l], positions, seq_lens,
                                           block_table, w.pool(l), self.q_rot, self.err, stream=s,
@@ -818,13 +848,17 @@ def run_ours(args, dist: Dist):
     # over its L launches, so an upper bound of the launch's duration
     launch_us = t_steps_ms / args.steps / L * 1e3
     achieved = bytes_layer / (launch_us * 1e-6) / 1e9
-    mode = "split" if args.three_call else "fused"
+    per_layer = calls_per_layer(args)
+    # qdec_step itself runs in one launch or (bf16 pool, flat layout) two
+    step_launches = qdec.qdec_step_launches(layers.shape, w.kv == "fp8") if per_layer == 1 else 0
+    mode = {1: "fused" if step_launches == 1 else "decode", 2: "decode", 3: "split"}[per_layer]
+    launches_layer = max(per_layer, step_launches)
     roof_bytes, roof_kernel = bytes_layer, (f"attention_kernel<{mode}, fp8>" if w.kv == "fp8"
                                             else f"attention_kernel<{mode}>")
-    per_layer = 3 if args.three_call else 1
-    roof_how = (f"CUDA events around each step's graph (rope table + {per_layer * L} launches, "
-                f"gaps included) / {L}" + (": the three launches of a layer together"
-                                           if args.three_call else ""))
+    roof_how = (f"CUDA events around each step's graph (rope table + {launches_layer * L} "
+                f"launches, gaps included) / {L}"
+                + (f": the {launches_layer} launches of a layer together" if launches_layer > 1
+                   else ""))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if args.qkv:
         # the projection kernel alone: a graph of its L launches, timed the same way
@@ -907,7 +941,7 @@ def run_ours(args, dist: Dist):
     layers.check()
 
     traffic = None
-    tr = TRAFFIC.get(workload_name(spec, w.kv, args.hidden if args.qkv else 0, args.three_call))
+    tr = TRAFFIC.get(workload_name(spec, w.kv, args.hidden if args.qkv else 0, per_layer))
     if tr and tr["kernel_sha"] == kernel_sha("qkv_append_kernel" if args.qkv
                                              else "attention_kernel"):
         traffic = tr["bytes_per_launch"]
@@ -936,12 +970,15 @@ def run_ours(args, dist: Dist):
                       f"({host_cores()} host cores), fp64, {secs_all:.1f} s"}
 
     cfg = workload_config(w, args, dist.world, l2)
+    if step_launches == 2:
+        cfg["launch"] += (" (qdec_step runs as two launches here: the new-token kernel, then the "
+                          "decode-mode attention as its programmatic dependent)")
     if args.plan_bound:
         cfg["plan"] = (f"planned for contexts up to {args.plan_bound} tokens (block-table rows "
                        f"of {layers.shape.max_blocks_per_seq} pages)")
     configs = []
     if (not args.qkv and not args.layers and not args.no_configs and not args.pool_pages
-            and not args.three_call):
+            and per_layer == 1):
         # the other workloads of the benchmark plan, each on its own (the
         # headline's buffers are released first)
         del layers, run, w, step_in, flush
@@ -980,7 +1017,7 @@ def run_ours(args, dist: Dist):
             "e2e": {"value": e2e_value and round(e2e_value, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": k_e2e},
-            "gpu_launches": ((2 * L if args.qkv else per_layer * L) + 1) * args.steps,
+            "gpu_launches": ((2 * L if args.qkv else launches_layer * L) + 1) * args.steps,
             "clocks": ck,
             "cpu_baseline": cpu,
         }

@@ -233,14 +233,25 @@ int attention_grid(const qdec_shape *s) {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// qdec_step over a bf16 pool on the flat layout (many segments: each CTA
+// walks several) runs as two launches, the new-token kernel and then the
+// attention in decode mode as its programmatic dependent: there the fused
+// kernel's per-piece new-token work holds the consumer warps of a CTA while
+// its ring fills, which costs more than the extra launch (measured on 64
+// ragged sequences: 182.9 -> 172.6 us per layer-step).  On the cluster
+// layout (one piece per CTA, latency-bound) the single launch is faster.
+bool step_in_two_launches(const qdec_shape *s, bool fp8) {
+    return !fp8 && plan_for(s, true, false).cluster == 0;
+}
+
 struct WorkspaceLayout {
-    size_t cnt, lse, o, total;
+    size_t cnt, lse, o, o_end, qrot, total;
 };
 
 // counters [B*Hkv] int32 | partial lse [pieces][G] f32 | partial o [pieces][G][D] f32
 // with pieces <= grid + B*Hkv for either layout (flat: each CTA adds at most
 // one piece per segment it starts in, plus its first; cluster: one per
-// cluster).
+// cluster) | q_rot [B][Hq][D] f32 where qdec_step runs in two launches.
 WorkspaceLayout workspace_layout(const qdec_shape *s) {
     const size_t segs = static_cast<size_t>(s->batch) * s->num_kv_heads;
     const size_t pieces = static_cast<size_t>(attention_grid(s)) + segs;
@@ -248,7 +259,12 @@ WorkspaceLayout workspace_layout(const qdec_shape *s) {
     l.cnt = 0;
     l.lse = round256(segs * sizeof(int32_t));
     l.o = l.lse + round256(pieces * qdec::kGroup * sizeof(float));
-    l.total = l.o + pieces * qdec::kGroup * qdec::kHeadDim * sizeof(float);
+    l.o_end = l.o + pieces * qdec::kGroup * qdec::kHeadDim * sizeof(float);
+    l.qrot = round256(l.o_end);
+    l.total = l.qrot + (step_in_two_launches(s, false)
+                            ? static_cast<size_t>(s->batch) * s->num_q_heads * qdec::kHeadDim *
+                                  sizeof(float)
+                            : 0);
     return l;
 }
 
@@ -293,7 +309,7 @@ void bind_workspace(Params &p, const qdec_shape *s, void *ws) {
     p.ws_cnt = reinterpret_cast<int32_t *>(base + l.cnt);
     p.ws_lse = reinterpret_cast<float *>(base + l.lse);
     p.ws_o = reinterpret_cast<float *>(base + l.o);
-    p.ws_pieces = static_cast<long long>((l.total - l.o) /
+    p.ws_pieces = static_cast<long long>((l.o_end - l.o) /
                                          (qdec::kGroup * qdec::kHeadDim * sizeof(float)));
 }
 
@@ -567,9 +583,23 @@ qdec_status step_impl(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_str
     bind_workspace(p, shape, workspace);
     CUtensorMap map;
     if ((st = encode_map(&map, shape, pool)) != QDEC_OK) return st;
-    return cuda_status(
-        qdec::launch_attention(p, map, qdec::kAttnFused, pool.fp8,
-                               static_cast<cudaStream_t>(stream)));
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (step_in_two_launches(shape, pool.fp8)) {
+        // q_rot in the workspace's last region; the append with the shape's
+        // flags, the attention always as its programmatic dependent (it
+        // reads q_rot and the appended slots only after the append is done)
+        float *q_rot = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                                 workspace_layout(shape).qrot);
+        Params pa = p;
+        pa.q_rot_out = q_rot;
+        cudaError_t e = qdec::launch_append_rope(pa, false, s);
+        if (e != cudaSuccess) return cuda_status(e);
+        Params pd = p;
+        pd.q_rot_in = q_rot;
+        pd.pdl = 1;
+        return cuda_status(qdec::launch_attention(pd, map, qdec::kAttnDecode, false, s));
+    }
+    return cuda_status(qdec::launch_attention(p, map, qdec::kAttnFused, pool.fp8, s));
 }
 
 qdec_status attn_decode_impl(const qdec_shape *shape, const float *q_rot, const PoolArg &pool,
@@ -705,6 +735,11 @@ qdec_status qdec_rope_table(const qdec_shape *shape, const int32_t *positions, v
     p.positions = positions;
     p.rope_out = static_cast<qdec::RopeEntry *>(rope_table);
     return cuda_status(qdec::launch_rope_table(p, static_cast<cudaStream_t>(stream)));
+}
+
+int qdec_step_launches(const qdec_shape *shape, int fp8_pool) {
+    if (check_shape(shape) != QDEC_OK) return 0;
+    return step_in_two_launches(shape, fp8_pool != 0) ? 2 : 1;
 }
 
 size_t qdec_workspace_bytes(const qdec_shape *shape) {

@@ -1463,12 +1463,18 @@ __global__ void __launch_bounds__(kRopeThreads) rope_table_kernel(const __grid_c
 template <bool kFp8>
 __global__ void __launch_bounds__(128) append_rope_kernel(const __grid_constant__ Params p) {
     __shared__ __align__(16) uint8_t sm[kPrologueBytes];
+    // as a programmatic dependent (the flag's contract: the previous kernel
+    // writes neither seq_lens nor the block table): the attention after it
+    // may be scheduled at once, and q/k/v, the pool slot and q_rot are only
+    // touched once the previous kernel has completed
+    if (p.pdl) launch_dependents();
     const int g = blockIdx.x, b = blockIdx.y;
     const int L = p.seq_lens[b];
     if (L < 1 || L > p.max_blocks * kPageSize) {
         if (threadIdx.x == 0 && g == 0) flag_error(p.err, QDEC_FLAG_BAD_SEQLEN);
         return;
     }
+    if (p.pdl) grid_dependency_wait();
     new_token_rows<1, kFp8>(p, b, g, L, true, sm);
 }
 
@@ -1623,11 +1629,17 @@ cudaError_t launch_rope_table(const Params &p, cudaStream_t s) {
 }
 
 cudaError_t launch_append_rope(const Params &p, bool fp8, cudaStream_t s) {
-    if (fp8)
-        append_rope_kernel<true><<<dim3(p.Hkv, p.B), 128, 0, s>>>(p);
-    else
-        append_rope_kernel<false><<<dim3(p.Hkv, p.B), 128, 0, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.Hkv, p.B);
+    cfg.blockDim = dim3(128);
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = p.pdl ? 1 : 0;
+    return fp8 ? cudaLaunchKernelEx(&cfg, append_rope_kernel<true>, p)
+               : cudaLaunchKernelEx(&cfg, append_rope_kernel<false>, p);
 }
 
 cudaError_t launch_merge(const Params &p, cudaStream_t s) {

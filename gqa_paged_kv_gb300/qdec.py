@@ -35,8 +35,8 @@ QDEC_FLAG_BAD_INDEX = 8
 QDEC_LAUNCH_TEST_WITHHOLD_TILE = 1 << 30
 
 # Every symbol include/qdec.h declares.
-EXPORTS = ("qdec_workspace_bytes", "qdec_workspace_init", "qdec_rope_table_bytes",
-           "qdec_rope_table", "qdec_append_rope", "qdec_attn_split", "qdec_attn_merge",
+EXPORTS = ("qdec_workspace_bytes", "qdec_step_launches", "qdec_workspace_init",
+           "qdec_rope_table_bytes", "qdec_rope_table", "qdec_append_rope", "qdec_attn_split", "qdec_attn_merge",
            "qdec_attn_decode", "qdec_step", "qdec_qkv_append_rope", "qdec_qkv_pack_weights",
            "qdec_append_rope_fp8", "qdec_attn_split_fp8", "qdec_attn_decode_fp8",
            "qdec_prefill_append_rope", "qdec_prefill_attn", "qdec_prefill_append_rope_fp8",
@@ -95,6 +95,8 @@ def _load():
     st = ctypes.c_int
     lib.qdec_workspace_bytes.argtypes = [sp]
     lib.qdec_workspace_bytes.restype = sz
+    lib.qdec_step_launches.argtypes = [sp, ctypes.c_int]
+    lib.qdec_step_launches.restype = ctypes.c_int
     lib.qdec_workspace_init.argtypes = [sp, vp, sz, vp]
     lib.qdec_workspace_init.restype = st
     lib.qdec_rope_table_bytes.argtypes = [sp]
@@ -204,6 +206,10 @@ def _raise(status: int, what: str):
 
 def qdec_workspace_bytes(shape: Shape) -> int:
     return int(_lib.qdec_workspace_bytes(ctypes.byref(shape.c())))
+
+
+def qdec_step_launches(shape: Shape, fp8_pool: bool = False) -> int:
+    return int(_lib.qdec_step_launches(ctypes.byref(shape.c()), 1 if fp8_pool else 0))
 
 
 def qdec_workspace_init(shape: Shape, workspace: torch.Tensor, stream=None):

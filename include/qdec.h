@@ -97,6 +97,10 @@ typedef enum {
  * or writing anything.  Set it only when the immediately preceding kernel
  * does not write seq_lens, block_table or kv_pool pages other than the
  * append slots of this step (e.g. the previous layer's qdec_step).
+ * (Where qdec_step runs as two launches, see there, the first reads seq_lens
+ * before that wait, the second is always a programmatic dependent of the
+ * first.)  qdec_append_rope with the flag reads seq_lens before the wait and
+ * everything else after it.
  * qdec_attn_decode with the flag waits for the previous kernel before it
  * reads anything but its launch parameters.  qdec_qkv_append_rope with the
  * flag streams the first stages of its (packed) weight before that wait and
@@ -205,14 +209,22 @@ qdec_status qdec_attn_decode(const qdec_shape *shape, const float *q_rot,
                              size_t workspace_bytes, qdec_bf16 *out,
                              int32_t *err_flag, void *stream);
 
-/* The whole layer-step (steps 1-4) in ONE kernel launch: every CTA norms and
- * rotates the four query rows of the (sequence, KV head) it works on, the CTA
- * that holds the last page of a (sequence, KV head) also norms, rotates and
- * appends the new key/value, and the last CTA to finish a split (sequence,
- * KV head) merges its pieces.  Same arguments as qdec_append_rope plus the
- * workspace and `out`; no q_rot buffer is needed.  The workspace counters
- * must be zero on entry (qdec_workspace_init once).  See
- * QDEC_LAUNCH_OVERLAP_PREVIOUS for overlapping consecutive layers. */
+/* The whole layer-step (steps 1-4).  In ONE kernel launch where the work
+ * plan is the cluster layout (few (sequence, KV head) segments) or the pool
+ * is FP8: every CTA norms and rotates the four query rows of the (sequence,
+ * KV head) it works on, the CTA that holds the last page of a (sequence, KV
+ * head) also norms, rotates and appends the new key/value, and the last CTA
+ * to finish a split (sequence, KV head) merges its pieces.  Over a bf16 pool
+ * on the flat layout (many segments, each CTA walking several) in TWO: the
+ * kernel of qdec_append_rope (q_rot kept in the workspace), then the
+ * attention of qdec_attn_decode as its programmatic dependent -- there the
+ * per-segment new-token work inside the attention kernel costs more than
+ * the second launch.  qdec_step_launches tells which.  Either way the grid
+ * depends on the shape only (one captured graph serves every length).  Same
+ * arguments as qdec_append_rope plus the workspace and `out`; no q_rot
+ * buffer is needed.  The workspace counters must be zero on entry
+ * (qdec_workspace_init once).  See QDEC_LAUNCH_OVERLAP_PREVIOUS for
+ * overlapping consecutive layers. */
 qdec_status qdec_step(const qdec_shape *shape,
                       const qdec_bf16 *q, int64_t q_stride,
                       const qdec_bf16 *k, int64_t k_stride,
@@ -222,6 +234,11 @@ qdec_status qdec_step(const qdec_shape *shape,
                       const int32_t *block_table, const void *rope_table,
                       qdec_bf16 *kv_pool, void *workspace, size_t workspace_bytes,
                       qdec_bf16 *out, int32_t *err_flag, void *stream);
+
+/* Kernel launches of one qdec_step (fp8_pool = 0) or qdec_step_fp8
+ * (fp8_pool != 0) call for this shape on the current device: 1 or 2; 0 for
+ * an invalid shape.  Host only, no device work. */
+int qdec_step_launches(const qdec_shape *shape, int fp8_pool);
 
 /* The merged QKV projection fused with steps 1-3 (article "扔掉 vLLM！从零
  * 构建 Qwen3-8B 推理引擎" (news.rkmt.cn), section 4.4.3: the q, k and v

@@ -167,6 +167,30 @@ def test_rope_table_values():
     assert np.max(np.abs(t[..., 2] + t[..., 3] - np.sin(ang))) < 1e-13
 
 
+@pytest.mark.parametrize("lens,num_ctas", [([17, 1, 300, 64, 16, 2, 999], 7),
+                                           ([int(x) for x in np.linspace(1, 3000, 30)], 0)])
+def test_two_launch_step_is_append_then_decode(lens, num_ctas):
+    """Where qdec_step runs as two launches (bf16 pool, flat layout: a forced
+    grid, or 30 sequences = 240 segments, more than 60 % of the resident CTAs)
+    it is qdec_append_rope followed by qdec_attn_decode: the same bits, and
+    the oracle's result."""
+    q = parity.qdec()
+    spec = wl.custom(len(lens), lens, pool_pages=sum((l + 15) // 16 for l in lens) + 9, seed=23)
+    wa, wb = wl.build(spec, "cuda", poison=True), wl.build(spec, "cuda", poison=True)
+    ra = parity.Runner(wa, num_ctas=num_ctas)
+    rb = parity.Runner(wb, num_ctas=num_ctas)
+    assert q.qdec_step_launches(ra.shape) == 2
+    ref = parity.run_oracle(wl.oracle_inputs(wa, 0))
+    ra.step(0)
+    rb.two_calls(0)
+    ra.check_flags()
+    rb.check_flags()
+    assert torch.equal(ra.out[0].view(torch.int16), rb.out[0].view(torch.int16))
+    assert torch.equal(wa.pool(0).view(torch.int16), wb.pool(0).view(torch.int16))
+    parity.assert_out_close(ra.out[0], ref["out"])
+    parity.assert_slots(wa, 0, range(len(lens)), ref)
+
+
 def test_rope_table_values_at_large_positions():
     """The float pairs (double reduction by pi/2, float-float series) stay
     within 1e-13 of cos/sin of the double angle for positions far past any
