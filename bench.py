@@ -73,22 +73,28 @@ KERNEL_SOURCES = {
 # profiles/), keyed by workload; used only while the kernel source hash
 # still matches the one the counters were taken on.
 TRAFFIC = {
-    "b8-ctx256to384-36layer": {"kernel_sha": "ebfd4d5815a4ad7c", "bytes_per_launch": 10899576},
-    "b16-ctx256to384-chanscale-36layer": {"kernel_sha": "ebfd4d5815a4ad7c",
-                                          "bytes_per_launch": 21779270},
-    "b1-ctx8192-spikes-36layer": {"kernel_sha": "ebfd4d5815a4ad7c", "bytes_per_launch": 33634251},
-    "b64-ragged128to16384-sharedpool-36layer": {"kernel_sha": "ebfd4d5815a4ad7c",
-                                                "bytes_per_launch": 1038103628},
-    "b64-ragged128to16384-sharedpool-36layer-fp8kv": {"kernel_sha": "ebfd4d5815a4ad7c",
-                                                      "bytes_per_launch": 524783838},
+    # the attention kernel (workload 5 over bf16: the decode-mode kernel of the
+    # two-launch step)
+    "b8-ctx256to384-36layer":
+        {"kernel_sha": "e297049875109362", "bytes_per_launch": 10896197},
+    "b16-ctx256to384-chanscale-36layer":
+        {"kernel_sha": "e297049875109362", "bytes_per_launch": 21779787},
+    "b1-ctx8192-spikes-36layer":
+        {"kernel_sha": "e297049875109362", "bytes_per_launch": 33636040},
+    "b64-ragged128to16384-sharedpool-36layer":
+        {"kernel_sha": "e297049875109362", "bytes_per_launch": 1038141551},
+    "b64-ragged128to16384-sharedpool-36layer-fp8kv":
+        {"kernel_sha": "e297049875109362", "bytes_per_launch": 524804043},
     # --prefill 2048: the causal prefill attention kernel
-    "prefill-b1-prompt2048-36layer": {"kernel_sha": "4cd71e6da03e48ef", "bytes_per_launch": 42007403},
-    "prefill-b1-prompt2048-36layer-fp8kv": {"kernel_sha": "4cd71e6da03e48ef",
-                                            "bytes_per_launch": 37826048},
+    "prefill-b1-prompt2048-36layer":
+        {"kernel_sha": "b82e7ddbde5ad841", "bytes_per_launch": 42006848},
+    "prefill-b1-prompt2048-36layer-fp8kv":
+        {"kernel_sha": "b82e7ddbde5ad841", "bytes_per_launch": 37839509},
     # --qkv: the projection kernel
-    "b8-ctx256to384-36layer-qkv2560": {"kernel_sha": "bd321992338b6b31", "bytes_per_launch": 31554816},
-    "b64-ragged128to16384-sharedpool-36layer-qkv2560": {"kernel_sha": "bd321992338b6b31",
-                                                        "bytes_per_launch": 31906560},
+    "b8-ctx256to384-36layer-qkv2560":
+        {"kernel_sha": "bd321992338b6b31", "bytes_per_launch": 31553536},
+    "b64-ragged128to16384-sharedpool-36layer-qkv2560":
+        {"kernel_sha": "bd321992338b6b31", "bytes_per_launch": 31908314},
 }
 
 # The CPU timings sample the first few layers of a workload (same shapes and
