@@ -1459,9 +1459,12 @@ __global__ void __launch_bounds__(kRopeThreads) rope_table_kernel(const __grid_c
 
 // ---------------------------------------------------------- append kernel --
 // Steps 1-3 for (KV head blockIdx.x, sequence blockIdx.y): q rows to
-// q_rot_out, k and v into the pool.
+// q_rot_out, k and v into the pool.  Warps 0-3 produce the four query rows,
+// warp 4 the key/value row, so the key's loads do not wait behind a query
+// row's (the attention launched after this kernel waits for all of it).
+constexpr int kAppendThreads = 5 * 32;
 template <bool kFp8>
-__global__ void __launch_bounds__(128) append_rope_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const __grid_constant__ Params p) {
     __shared__ __align__(16) uint8_t sm[kPrologueBytes];
     // as a programmatic dependent (the flag's contract: the previous kernel
     // writes neither seq_lens nor the block table): the attention after it
@@ -1475,7 +1478,12 @@ __global__ void __launch_bounds__(128) append_rope_kernel(const __grid_constant_
         return;
     }
     if (p.pdl) grid_dependency_wait();
-    new_token_rows<1, kFp8>(p, b, g, L, true, sm);
+    if (threadIdx.x >= kGroup * 32) {
+        if (new_token_in_bounds(p, b, g, L))
+            key_value_row<kFp8>(p, b, g, L, sm, load_kv_inputs(p, b, g, L));
+        return;
+    }
+    new_token_rows<1, kFp8>(p, b, g, L, false, sm);
 }
 
 // ----------------------------------------------------------- merge kernel --
@@ -1631,7 +1639,7 @@ cudaError_t launch_rope_table(const Params &p, cudaStream_t s) {
 cudaError_t launch_append_rope(const Params &p, bool fp8, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.Hkv, p.B);
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(kAppendThreads);
     cfg.stream = s;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;

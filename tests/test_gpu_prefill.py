@@ -360,3 +360,30 @@ def test_prefill_attention_as_a_programmatic_dependent_gives_the_same_bits():
         assert st == 0 and fl == 0, (st, fl)
         outs.append(out)
     assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_prefill_fp8_attention_as_a_programmatic_dependent_gives_the_same_bits():
+    """The same over FP8 pools: the tensor-core attention launched as a
+    programmatic dependent of each layer's append (it reads q_rot, the codes
+    and the scales only after its wait) gives the serial launches' bits."""
+    q = parity.qdec()
+    seq_lens, chunks = [300, 17, 1000, 2048], [20, 17, 200, 2048]
+    layers = [wl.prefill_case_fp8(seq_lens, chunks, seed=50 + l) for l in range(3)]
+    T = layers[0][0].q.shape[0]
+    outs = []
+    for flags in (0, q.QDEC_LAUNCH_OVERLAP_PREVIOUS):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        q_rot = torch.empty((T, 32, 128), dtype=torch.float32, device="cuda")
+        out = torch.full((3, T, 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        for l, (c, codes, sc) in enumerate(layers):
+            codes = codes.clone()
+            shape = _shape(c, len(seq_lens), flags)
+            q.qdec_prefill_append_rope_fp8(shape, c.q, c.k, c.v, c.w_q, c.w_k, c.positions,
+                                           c.qo_indptr, c.seq_lens, c.block_table, codes, sc,
+                                           q_rot, err)
+            q.qdec_prefill_attn_fp8(shape, q_rot, c.qo_indptr, c.seq_lens, c.block_table, codes,
+                                    sc, out[l], err)
+        st, fl = q.qdec_check_error(err)
+        assert st == 0 and fl == 0, (st, fl)
+        outs.append(out)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
