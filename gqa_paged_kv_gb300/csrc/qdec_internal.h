@@ -24,13 +24,12 @@ constexpr int kTileHalfBytes = kPageSize * 64 * 2;         // 16 rows x 64 dims 
 constexpr int kPlaneBytes = 2 * kTileHalfBytes;            // one (page, plane, head) = 4 KiB
 constexpr int kTileBytes = 2 * kPlaneBytes;                // K + V = 8 KiB
 // FP8 (E4M3) pool: one byte per element, so a (page, plane, head) is 16
-// rows of 128 bytes and a page tile K + V is 4 KiB.  Each tile also brings
-// two 16-byte windows of kv_scale (the aligned 4-float groups holding its K
-// and its V scale).
+// rows of 128 bytes and a page tile K + V is 4 KiB.  Each ring slot also
+// holds the tile's K and V scale (two floats the producer stores with the
+// page lookup, so a tile is one copy).
 constexpr int kFp8PlaneBytes = kPageSize * kHeadDim;       // 2 KiB
 constexpr int kFp8TileBytes = 2 * kFp8PlaneBytes;          // 4 KiB
-constexpr int kScaleWindowBytes = 16;
-constexpr int kFp8SlotExtra = 2 * kScaleWindowBytes;       // per ring slot
+constexpr int kFp8SlotExtra = 16;                          // per ring slot
 // Cluster layout: the largest cluster whose peers' pieces get their own
 // receive buffer; larger clusters receive in rank 0's drained ring.
 constexpr int kMaxDirectRecv = 6;

@@ -104,7 +104,7 @@ static_assert(kOffKvNew % 16 == 0 && kOffRope % 16 == 0 && kOffBar % 8 == 0 &&
 static_assert(kOsBytes <= kTileBytes, "the warp-combine scratch fits in one ring slot");
 static_assert(kOsBytes + (kMaxCluster - 1) * kRecvSlotBytes <= 4 * kTileBytes,
               "scratch and receive buffer fit in a 4-slot bf16 ring");
-// bytes of one ring slot (the FP8 scale windows live after the ring)
+// bytes of one ring slot (the FP8 tiles' scales live after the ring)
 template <bool kFp8>
 __host__ __device__ constexpr int slot_bytes() {
     return kFp8 ? kFp8TileBytes : kTileBytes;
@@ -1039,15 +1039,13 @@ __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint3
             if constexpr (kFp8) {
                 if (patch || ntok < kPageSize)
                     fix_tile_fp8(tile, ntok, patch, reinterpret_cast<const uint8_t *>(kv_new), lane);
-                // this slot's scale windows: the K scale of head g sits at
-                // float g % 4 of its window (2 Hkv scales per page, Hkv even),
-                // the V scale at (Hkv + g) % 4 of the next
+                // this slot's K and V scale, stored by the producer
                 const float *win = reinterpret_cast<const float *>(
                     ring + NS * kFp8TileBytes + slot * kFp8SlotExtra);
-                const float sk = win[g & 3];
+                const float sk = win[0];
                 tile_math_fp8(ks, ks + kFp8PlaneBytes, qf, ntok, lane, st,
                               reinterpret_cast<__half *>(pbuf), qunA * sk, qunB * sk,
-                              win[4 + ((p.Hkv + g) & 3)]);
+                              win[1]);
             } else {
                 if (patch || ntok < kPageSize) fix_tile(tile, ntok, patch, kv_new, lane);
                 tile_math(ks, ks + kPlaneBytes, qf, ntok, lane, st, pbuf);
@@ -1271,6 +1269,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kCluster, kFp8))
         bool stop = false;
         for (long long base = 0; base < ntiles && !stop; base += 32) {
             int page = -1, g = cg;
+            float sck = 0.f, scv = 0.f;  // FP8: the tile's K and V scale
             if (base + lane < ntiles) {
                 int b, pg;
                 if (kCluster) {
@@ -1282,11 +1281,17 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kCluster, kFp8))
                 if (in_bounds(p, b >= 0 && b < p.B && pg >= 0 && pg < p.max_blocks && g >= 0 &&
                                      g < p.Hkv))
                     page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg];
+                if (kFp8 && page >= 0 && page < p.num_pages) {
+                    const int64_t si = static_cast<int64_t>(page) * 2 * p.Hkv + g;
+                    sck = p.kv_scale[si];
+                    scv = p.kv_scale[si + p.Hkv];
+                }
             }
             const int cnt = static_cast<int>(min(32ll, ntiles - base));
             for (int j = 0; j < cnt; ++j, ++i) {
                 const int pj = __shfl_sync(kFull, page, j);
                 const int gj = __shfl_sync(kFull, g, j);
+                const float skj = __shfl_sync(kFull, sck, j), svj = __shfl_sync(kFull, scv, j);
                 if (lane == 0) {
                     const int slot = i % NS;
                     const uint32_t full = full0 + 8 * slot;
@@ -1303,18 +1308,16 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kCluster, kFp8))
                     } else if (pj >= 0 && pj < p.num_pages && gj >= 0 && gj < p.Hkv) {
                         slot_ok[slot] = 1;
                         if constexpr (kFp8) {
-                            // the tile and the two 4-float windows of kv_scale
-                            // holding its K and V scales (2 Hkv scales per
-                            // page with Hkv even: windows never straddle pages)
-                            const int64_t si = static_cast<int64_t>(pj) * 2 * p.Hkv + gj;
-                            const uint32_t win = smem_u32(ring + NS * kFp8TileBytes +
-                                                          slot * kFp8SlotExtra);
-                            mbar_arrive_expect_tx(full, kFp8TileBytes + kFp8SlotExtra);
+                            // the tile's scales by plain stores (ordered before
+                            // the consumers' acquire by the arrive's release),
+                            // then the tile: one copy per slot
+                            float *win = reinterpret_cast<float *>(ring + NS * kFp8TileBytes +
+                                                                   slot * kFp8SlotExtra);
+                            win[0] = skj;
+                            win[1] = svj;
+                            mbar_arrive_expect_tx(full, kFp8TileBytes);
                             tma_load_tile_fp8(smem_u32(ring + slot * kFp8TileBytes), &kv_map,
                                               pj * 2 * p.Hkv + gj, full);
-                            bulk_load(win, p.kv_scale + (si & ~3ll), kScaleWindowBytes, full);
-                            bulk_load(win + kScaleWindowBytes, p.kv_scale + ((si + p.Hkv) & ~3ll),
-                                      kScaleWindowBytes, full);
                         } else {
                             mbar_arrive_expect_tx(full, kTileBytes);
                             tma_load_tile(smem_u32(ring + slot * kTileBytes), &kv_map,
