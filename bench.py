@@ -34,6 +34,7 @@ rank's time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -145,6 +146,9 @@ def parse_args():
                          "(launched one after another) instead of the one-launch qdec_step")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch each layer only after the previous one completed")
+    ap.add_argument("--fp8-in-kernel", action="store_true",
+                    help="--prefill --kv fp8: convert the codes inside the attention kernel "
+                         "instead of widening the pages once into a workspace")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: run fewer layers than the workload has")
     ap.add_argument("--pool-pages", type=int, default=0,
@@ -1043,12 +1047,21 @@ def prefill_flops(seq_lens, chunks, Hq=32, D=128) -> int:
     return 4 * D * Hq * tot
 
 
-def prefill_config(P: int, L: int, fp8: bool) -> dict:
+def prefill_config(P: int, L: int, fp8: bool, widen: bool = True) -> dict:
     """The `config` object of a --prefill line (the same for both arms)."""
+    if not fp8:
+        launch = (f"CUDA graph: {L} x (qdec_prefill_append_rope, qdec_prefill_attn), the "
+                  "attention a programmatic dependent of the append")
+    elif widen:
+        launch = (f"CUDA graph: {L} x (qdec_prefill_append_rope_fp8, qdec_prefill_attn_fp8 "
+                  "with a workspace: the pages dequantized to bf16 once, then the attention "
+                  "as a programmatic dependent of that pass)")
+    else:
+        launch = (f"CUDA graph: {L} x (qdec_prefill_append_rope_fp8, qdec_prefill_attn_fp8 "
+                  "without a workspace: the codes converted inside the attention kernel)")
     return {"workload": f"prefill-b1-prompt{P}-{L}layer" + ("-fp8kv" if fp8 else ""),
             "batch": 1, "prompt": P, "layers": L, "heads": "32 q / 8 kv, head_dim 128, page 16",
-            "launch": f"CUDA graph: {L} x (qdec_prefill_append_rope, qdec_prefill_attn), the "
-                      "bf16 attention a programmatic dependent of the append",
+            "launch": launch,
             "l2": "not flushed (compute-bound: each layer's K/V is re-read from L2 "
                   "by its query blocks by design)"}
 
@@ -1126,6 +1139,7 @@ def run_prefill(args, dist: Dist):
     P = args.prefill
     L = args.layers or 36
     fp8 = args.kv == "fp8"
+    widen = fp8 and not args.fp8_in_kernel
     name = prefill_config(P, L, fp8)["workload"]
     if fp8:   # E4M3 codes and per-(page, plane, head) scales of the same draws
         made = [wl.prefill_case_fp8([P], [P], seed=1000 + l, device="cuda") for l in range(L)]
@@ -1143,6 +1157,10 @@ def run_prefill(args, dist: Dist):
     out = torch.empty((L, P, 32, 128), dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.Stream()
     flops_layer = prefill_flops([P], [P])
+    # one workspace serves every layer: each call's widening waits for the
+    # calls before it on the stream
+    ws8 = (torch.empty(qdec.qdec_prefill_fp8_workspace_bytes(shape), dtype=torch.uint8,
+                       device="cuda") if widen else None)
 
     def step_fn(ins, outs):
         def fn():
@@ -1155,7 +1173,7 @@ def run_prefill(args, dist: Dist):
                                                       codes, sc, q_rot, err, stream=stream)
                     qdec.qdec_prefill_attn_fp8(shape, q_rot, c.qo_indptr, c.seq_lens,
                                                c.block_table, codes, sc, outs[l], err,
-                                               stream=stream)
+                                               stream=stream, workspace=ws8)
                     continue
                 qdec.qdec_prefill_append_rope(shape, q, k, v, c.w_q, c.w_k, c.positions,
                                               c.qo_indptr, c.seq_lens, c.block_table, c.pool,
@@ -1200,27 +1218,53 @@ def run_prefill(args, dist: Dist):
     ms_step = t_ms / args.steps
     value = dist.world * flops_layer * L * args.steps / (t_ms * 1e-3) / 1e12
 
-    # the attention kernel alone: a graph of its L launches
-    ga = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(ga, stream=stream):
+    # the attention kernel alone: a graph of its L launches.  Over an FP8 pool
+    # with a workspace each layer gets its own workspace, dequantized once
+    # beforehand by a full call, and the timed calls are told the pages are
+    # ready; the full call (dequantizing pass + attention) is timed as well.
+    def attn_graph(fn):
+        g_ = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g_, stream=stream):
+                fn()
+        return g_
+
+    def time_graph(g_, reps):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g_.replay()
+            e0.record(stream)
+            for _ in range(reps):
+                g_.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps / L * 1e3
+
+    def attn_calls(shape_, wss):
+        def fn():
             for l, c in enumerate(cases):
                 if fp8:
-                    qdec.qdec_prefill_attn_fp8(shape, q_rot, c.qo_indptr, c.seq_lens,
+                    qdec.qdec_prefill_attn_fp8(shape_, q_rot, c.qo_indptr, c.seq_lens,
                                                c.block_table, *pools8[l], out[l], err,
-                                               stream=stream)
+                                               stream=stream, workspace=wss[l])
                 else:
-                    qdec.qdec_prefill_attn(shape, q_rot, c.qo_indptr, c.seq_lens, c.block_table,
+                    qdec.qdec_prefill_attn(shape_, q_rot, c.qo_indptr, c.seq_lens, c.block_table,
                                            c.pool, out[l], err, stream=stream)
-        for _ in range(3):
-            ga.replay()
-        reps = max(5, args.steps // 4)
-        e0.record(stream)
-        for _ in range(reps):
-            ga.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    launch_us = e0.elapsed_time(e1) / reps / L * 1e3
+        return fn
+
+    reps = max(5, args.steps // 4)
+    call_us = None
+    if widen:
+        call_us = time_graph(attn_graph(attn_calls(shape, [ws8] * L)), reps)
+        ws_l = [torch.empty_like(ws8) for _ in range(L)]
+        with torch.cuda.stream(stream):
+            attn_calls(shape, ws_l)()
+        ready = dataclasses.replace(
+            shape, launch_flags=shape.launch_flags | qdec.QDEC_LAUNCH_PREFILL_PAGES_READY)
+        launch_us = time_graph(attn_graph(attn_calls(ready, ws_l)), reps)
+        del ws_l
+    else:
+        launch_us = time_graph(attn_graph(attn_calls(shape, [None] * L)), reps)
     achieved = flops_layer / (launch_us * 1e-6) / 1e12
     peak, peak_kind = measured_bf16_tflops()
 
@@ -1282,26 +1326,36 @@ def run_prefill(args, dist: Dist):
             "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,
-            "dtype": ("e4m3 KV converted exactly to f16 in shared memory (tcgen05 kind::f16 with "
-                      "f16 operands, f32 accumulators in tensor memory)" if fp8 else
+            "dtype": ("e4m3 KV dequantized once to bf16 (code x scale) in a workspace, then "
+                      "the bf16-pool attention (tcgen05 kind::f16 with bf16 operands, f32 "
+                      "accumulators in tensor memory)" if widen else
+                      "e4m3 KV converted exactly to f16 in shared memory (tcgen05 kind::f16 "
+                      "with f16 operands, f32 accumulators in tensor memory)" if fp8 else
                       "bf16 (tcgen05 kind::f16 with bf16 operands, q rounded once to bf16, f32 "
                       "accumulators in tensor memory)"),
             "data": "synthetic (seeded N(0,1) bf16 q/k/v, U(0.5,1.5) norm weights)",
             "us_per_layer_step": round(ms_step * 1e3 / L, 3),
-            "config": prefill_config(P, L, fp8),
+            "config": prefill_config(P, L, fp8, widen),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json bf16_tflops, cuBLAS "
                                       f"burst)" if peak_kind == "measured" else "fallback",
-                         "kernel": ("prefill_attention_tc_kernel<fp8>" if fp8
+                         "kernel": ("prefill_attention_tc_kernel<widened>"
+                                    if widen else "prefill_attention_tc_kernel<fp8>" if fp8
                                     else "prefill_attention_tc_kernel<bf16>"),
                          "launch_us": round(launch_us, 3),
                          "launch_us_how": f"CUDA events around a graph of {L} attention "
-                                          f"launches, {reps} replays",
+                                          f"launches, {reps} replays" +
+                                          (" (each layer's pages dequantized beforehand into "
+                                           "its own workspace)" if widen else ""),
+                         "call_us": call_us and round(call_us, 3),
+                         "call_us_how": ("the same graph of full qdec_prefill_attn_fp8 calls "
+                                         "(dequantizing pass + attention) on one shared "
+                                         "workspace" if widen else None),
                          "flops_per_launch": flops_layer},
             "e2e": {"value": e2e_value and round(e2e_value, 3), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k_e2e},
-            "gpu_launches": 2 * L * args.steps,
+            "gpu_launches": (3 if widen else 2) * L * args.steps,
             "clocks": ck,
             "cpu_baseline": cpu,
         }

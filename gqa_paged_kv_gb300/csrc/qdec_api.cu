@@ -46,7 +46,8 @@ qdec_status check_shape(const qdec_shape *s) {
         s->page_size < 1 || s->num_pages < 1 || s->max_blocks_per_seq < 1 ||
         s->max_seq_len < 1 || s->num_ctas < 0)
         return QDEC_ERR_INVALID_ARG;
-    if ((s->launch_flags & ~(QDEC_LAUNCH_OVERLAP_PREVIOUS | QDEC_LAUNCH_TEST_WITHHOLD_TILE)) != 0)
+    if ((s->launch_flags & ~(QDEC_LAUNCH_OVERLAP_PREVIOUS | QDEC_LAUNCH_PREFILL_PAGES_READY |
+                             QDEC_LAUNCH_TEST_WITHHOLD_TILE)) != 0)
         return QDEC_ERR_INVALID_ARG;
     if (!(s->rope_theta > 0.f) || !(s->eps >= 0.f) || !(s->sm_scale >= 0.f) ||
         !isfinite(s->rope_theta) || !isfinite(s->eps) || !isfinite(s->sm_scale))
@@ -652,10 +653,18 @@ qdec_status prefill_append_impl(const qdec_shape *shape, int32_t num_tokens, con
         qdec::launch_prefill_append(p, pool.fp8, static_cast<cudaStream_t>(stream)));
 }
 
+// Scratch of the FP8 prefill's widened pool: every page slot of every
+// sequence as 16-bit values (the bf16 pool's page size).
+size_t prefill_fp8_scratch_bytes(const qdec_shape *s) {
+    return static_cast<size_t>(s->batch) * s->max_blocks_per_seq * 2 * s->num_kv_heads *
+           qdec::kPageSize * qdec::kHeadDim * 2;
+}
+
 qdec_status prefill_attn_impl(const qdec_shape *shape, int32_t num_tokens, const float *q_rot,
                               const int32_t *qo_indptr, const int32_t *seq_lens,
                               const int32_t *block_table, const PoolArg &pool, qdec_bf16 *out,
-                              int32_t *err_flag, void *stream) {
+                              int32_t *err_flag, void *stream, void *workspace = nullptr,
+                              size_t workspace_bytes = 0) {
     qdec_status st = check_shape(shape);
     if (st != QDEC_OK) return st;
     if ((st = check_pool(shape, pool)) != QDEC_OK) return st;
@@ -672,12 +681,31 @@ qdec_status prefill_attn_impl(const qdec_shape *shape, int32_t num_tokens, const
     bind_pool(p, pool);
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
     p.err = err_flag;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
     CUtensorMap map;
+    if (pool.fp8 && workspace) {
+        // dequantize the sequences' pages once, then attend over the scratch
+        // as over a bf16 pool (the attention a programmatic dependent of the
+        // dequantizing pass, whose output it reads only after its wait)
+        if (!aligned16(workspace) || workspace_bytes < prefill_fp8_scratch_bytes(shape))
+            return QDEC_ERR_WORKSPACE;
+        qdec_shape ws_shape = *shape;
+        ws_shape.num_pages = shape->batch * shape->max_blocks_per_seq;
+        if ((st = encode_pool_region_map(&map, &ws_shape, workspace)) != QDEC_OK) return st;
+        p.wide = static_cast<__nv_bfloat16 *>(workspace);
+        Params pa = p;
+        if (!(shape->launch_flags & QDEC_LAUNCH_PREFILL_PAGES_READY)) {
+            cudaError_t e = qdec::launch_prefill_widen(p, cs);
+            if (e != cudaSuccess) return cuda_status(e);
+            pa.pdl = 1;
+        }
+        return cuda_status(qdec::launch_prefill_attention(pa, map, qdec::kPrefillPoolWide, cs));
+    }
     if ((st = pool.fp8 ? encode_pool_plane_map_fp8(&map, shape, pool.data)
                        : encode_pool_region_map(&map, shape, pool.data)) != QDEC_OK)
         return st;
-    return cuda_status(
-        qdec::launch_prefill_attention(p, map, pool.fp8, static_cast<cudaStream_t>(stream)));
+    return cuda_status(qdec::launch_prefill_attention(
+        p, map, pool.fp8 ? qdec::kPrefillPoolFp8 : qdec::kPrefillPoolBf16, cs));
 }
 
 qdec_status qkv_impl(const qdec_shape *shape, int32_t hidden, const qdec_bf16 *x,
@@ -854,9 +882,16 @@ qdec_status qdec_prefill_attn_fp8(const qdec_shape *shape, int32_t num_tokens,
                                   const float *q_rot, const int32_t *qo_indptr,
                                   const int32_t *seq_lens, const int32_t *block_table,
                                   const uint8_t *kv_pool_fp8, const float *kv_scale,
-                                  qdec_bf16 *out, int32_t *err_flag, void *stream) {
+                                  void *workspace, size_t workspace_bytes, qdec_bf16 *out,
+                                  int32_t *err_flag, void *stream) {
     return prefill_attn_impl(shape, num_tokens, q_rot, qo_indptr, seq_lens, block_table,
-                             PoolArg{kv_pool_fp8, kv_scale, true}, out, err_flag, stream);
+                             PoolArg{kv_pool_fp8, kv_scale, true}, out, err_flag, stream,
+                             workspace, workspace_bytes);
+}
+
+size_t qdec_prefill_fp8_workspace_bytes(const qdec_shape *shape) {
+    if (check_shape(shape) != QDEC_OK) return 0;
+    return prefill_fp8_scratch_bytes(shape);
 }
 
 qdec_status qdec_attn_merge(const qdec_shape *shape, const int32_t *seq_lens,

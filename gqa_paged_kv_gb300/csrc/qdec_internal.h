@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -88,6 +89,7 @@ struct Params {
     int qkv_boxes;           // QKV projection: 64-element blocks along hidden per stage
     const __nv_bfloat16 *w_packed;  // QKV projection: the weight in the packed order
     const int32_t *qo_indptr;  // prefill: [B+1] packed chunk rows of each sequence
+    __nv_bfloat16 *wide;       // prefill over FP8: the dequantised bf16 scratch pool
     int T;                     // prefill: rows the caller's buffers hold (qo_indptr[B] <= T)
     double inv_freq[kRotPairs];  // rope_theta^(-2i/D), i < D/2
 };
@@ -120,12 +122,17 @@ cudaError_t launch_attention(const Params &p, const CUtensorMap &kv_map, AttnMod
 cudaError_t launch_merge(const Params &p, cudaStream_t s);
 
 // Chunked prefill (qdec_prefill.cu): steps 1-3 for every chunk row, and the
-// causal paged attention of the chunk on the 5th-generation tensor core
-// (kv_map: for a bf16 pool one (page, plane, half of D) region per box, for
-// an FP8 pool one (page, plane) per box).
+// causal paged attention of the chunk on the 5th-generation tensor core.
+// Pool kinds of the attention: a bf16 pool (kv_map: one (page, plane, half
+// of D) region per box), an FP8 pool converted as it arrives (one (page,
+// plane) per box), or an FP8 pool dequantised beforehand by
+// launch_prefill_widen into the bf16 scratch p.wide (the bf16 region map
+// over that scratch).
+constexpr int kPrefillPoolBf16 = 0, kPrefillPoolFp8 = 1, kPrefillPoolWide = 2;
 cudaError_t launch_prefill_append(const Params &p, bool fp8, cudaStream_t s);
-cudaError_t launch_prefill_attention(const Params &p, const CUtensorMap &kv_map, bool fp8,
+cudaError_t launch_prefill_attention(const Params &p, const CUtensorMap &kv_map, int pool,
                                      cudaStream_t s);
+cudaError_t launch_prefill_widen(const Params &p, cudaStream_t s);
 
 // The merged QKV projection fused with steps 1-3 (qdec_qkv.cu): the weight
 // comes packed (qdec_qkv_pack_weights), x_map views x [B][hidden] with boxes

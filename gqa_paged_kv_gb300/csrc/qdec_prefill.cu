@@ -79,6 +79,19 @@ __device__ __forceinline__ bool chunk_ok(const Params &p, int b, int &n, int &L)
     return q0 >= 0 && q1 <= p.T && n >= 0 && L >= 1 && L <= p.max_blocks * kPageSize && n <= L;
 }
 
+// Pages sequence b occupies in a widened scratch: all its pages if its chunk
+// is well formed, none otherwise (both the widening and the attention use
+// this to number the scratch pages).
+__device__ __forceinline__ int widened_pages(const Params &p, int b) {
+    int n, L;
+    return chunk_ok(p, b, n, L) ? (L + kPageSize - 1) / kPageSize : 0;
+}
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    return v;
+}
+
 // ------------------------------------------------------------------ append --
 // One CTA per chunk row, 256 threads: the 64 angles of the row's position are
 // taken once (ff_sincos: float pairs) into shared memory; warp w then handles KV head
@@ -196,6 +209,97 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
     return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
+// ------------------------------------------------------- FP8 widening --
+// The E4M3 pages of every well-formed chunk's sequence dequantised once into
+// a bf16 scratch laid out as a bf16 pool ([page][plane][head][16][128]):
+// sequence b's page pg at scratch page base(b) + pg, base(b) = the widened
+// pages of the sequences before b.  Each value is code x scale of its
+// (page, plane, head), the exact product rounded to fp32 and then to the
+// nearest bf16 (an error of at most 2^-8 of the value, well below the 2^-4
+// of the E4M3 code itself; bf16 keeps fp32's range, so no scale overflows
+// it).  Rows of tokens past the sequence, and pages whose block-table entry
+// is not a valid page (flagged), are zero.  The tensor-core attention then
+// reads the scratch exactly as it reads a bf16 pool (kPoolWide: only the
+// page numbering differs), so each page is dequantised once instead of once
+// per query block, and no scale enters the softmax.  One CTA of 256 threads
+// per (sequence, page slot); a thread takes 16 codes at a time, issuing
+// kWidenBatch loads before it converts and stores any.
+constexpr int kWidenThreads = 256, kWidenBatch = 8;
+
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint32_t two_codes, float scale) {
+    const float2 f = __half22float2(__half2(__half2_raw(__nv_cvt_fp8x2_to_halfraw2(
+        static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3))));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+    return *reinterpret_cast<const uint32_t *>(&b);
+}
+
+__global__ void __launch_bounds__(kWidenThreads) prefill_widen_kernel(const __grid_constant__ Params p) {
+    // the attention after this launch may start its prologue at once; it
+    // waits for this grid's completion before it reads the scratch
+    if (p.pdl) launch_dependents();
+    const int b = blockIdx.x / p.max_blocks, pg = blockIdx.x % p.max_blocks;
+    __shared__ int base_s;
+    if (threadIdx.x < 32) {  // base(b): a warp sum over the sequences before b
+        const int lane = threadIdx.x;
+        int before = 0;
+        for (int b2 = lane; b2 < b; b2 += 32) before += widened_pages(p, b2);
+        before = warp_sum_int(before);
+        if (lane == 0) base_s = before;
+    }
+    __syncthreads();
+    int n, L;
+    if (b >= p.B || !chunk_ok(p, b, n, L)) return;  // uniform over the CTA
+    const int npg = (L + kPageSize - 1) / kPageSize;
+    if (pg >= npg) return;
+    const int page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg];
+    const bool valid = page >= 0 && page < p.num_pages;
+    if (!valid && threadIdx.x == 0) flag_error(p.err, QDEC_FLAG_BAD_PAGE);
+    // the append before wrote the chunk's slots, and the attention before
+    // may still read the scratch: codes are read and the scratch written
+    // only past this point
+    if (p.pdl) grid_dependency_wait();
+    const int64_t dst_page = static_cast<int64_t>(base_s) + pg;
+    // 2 Hkv (plane, head) blocks of 16 rows x 128 codes; 16 codes per item
+    constexpr int kItemsPerBlk = kPageSize * kHeadDim / 16;
+    const int items = 2 * p.Hkv * kItemsPerBlk;
+    for (int e0 = 0; e0 < items; e0 += kWidenThreads * kWidenBatch) {
+        uint4 w[kWidenBatch];
+        float sc[kWidenBatch];
+#pragma unroll
+        for (int k = 0; k < kWidenBatch; ++k) {
+            const int e = e0 + k * kWidenThreads + threadIdx.x;
+            const int blk = e / kItemsPerBlk;                      // plane * Hkv + head
+            const int r = (e / (kHeadDim / 16)) % kPageSize, c = e % (kHeadDim / 16);
+            w[k] = make_uint4(0u, 0u, 0u, 0u);
+            sc[k] = 0.f;
+            if (valid && e < items && pg * kPageSize + r < L) {
+                const int64_t pb = static_cast<int64_t>(page) * 2 * p.Hkv + blk;
+                w[k] = *reinterpret_cast<const uint4 *>(p.pool8 + (pb * kPageSize + r) * kHeadDim + 16 * c);
+                sc[k] = p.kv_scale[pb];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kWidenBatch; ++k) {
+            const int e = e0 + k * kWidenThreads + threadIdx.x;
+            if (e >= items) break;
+            const int blk = e / kItemsPerBlk;
+            const int r = (e / (kHeadDim / 16)) % kPageSize, c = e % (kHeadDim / 16);
+            const uint4 lo = make_uint4(e4m3x2_to_bf16x2_scaled(w[k].x, sc[k]),
+                                        e4m3x2_to_bf16x2_scaled(w[k].x >> 16, sc[k]),
+                                        e4m3x2_to_bf16x2_scaled(w[k].y, sc[k]),
+                                        e4m3x2_to_bf16x2_scaled(w[k].y >> 16, sc[k]));
+            const uint4 hi = make_uint4(e4m3x2_to_bf16x2_scaled(w[k].z, sc[k]),
+                                        e4m3x2_to_bf16x2_scaled(w[k].z >> 16, sc[k]),
+                                        e4m3x2_to_bf16x2_scaled(w[k].w, sc[k]),
+                                        e4m3x2_to_bf16x2_scaled(w[k].w >> 16, sc[k]));
+            uint4 *dst = reinterpret_cast<uint4 *>(
+                p.wide + ((dst_page * 2 * p.Hkv + blk) * kPageSize + r) * kHeadDim + 16 * c);
+            dst[0] = lo;
+            dst[1] = hi;
+        }
+    }
+}
+
 // ------------------------------------- attention on the 5th-gen tensor core --
 // prefill_attention_tc_kernel: causal paged attention of the chunk with both
 // products on the tensor core (tcgen05, accumulators in tensor memory).  One CTA per (sequence, KV head, block of 64 chunk tokens), the
@@ -265,25 +369,34 @@ constexpr int kTcKScaleRing = 8, kTcVScaleRing = 8;
 // tiles, the K and V rings of 16-bit slots, and for an FP8 pool the staging
 // rings of codes (per plane, a stage is four 2 KiB page boxes) and the scale
 // rings; then the barriers and a few ints.
-template <bool kFp8>
+// Pool kinds of the tensor-core prefill: a bf16 pool; an FP8 pool whose
+// codes each CTA converts to f16 as they arrive; an FP8 pool dequantised to
+// bf16 once beforehand (prefill_widen_kernel) into a scratch laid out as a
+// bf16 pool, its pages renumbered in sequence order.
+constexpr int kPoolBf16 = 0, kPoolFp8 = 1, kPoolWide = 2;
+
+template <int kPool>
 struct TcLayout {
-    static constexpr int kStages = kFp8 ? 3 : 4;           // K and V ring depth
-    static constexpr int kStg = kFp8 ? 3 : 0;              // FP8 staging slots per plane
+    static constexpr bool kStage = kPool == kPoolFp8;      // codes staged and converted
+    static constexpr bool kF16 = kStage;                   // f16 operands, per-page scales
+    static constexpr int kStages = kStage ? 3 : 4;         // K and V ring depth
+    static constexpr int kStg = kStage ? 3 : 0;            // FP8 staging slots per plane
     static constexpr int kStgSlot = kTcPagesPerStage * kFp8PlaneBytes;  // 8 KiB
     static constexpr int kOffQ = 0;                        // Q of tile u at u * kTcQBytes
     static constexpr int kOffKRing = kOffQ + kTcTiles * kTcQBytes;
     static constexpr int kOffVRing = kOffKRing + kStages * kTcSlotBytes;
     static constexpr int kOffStg = kOffVRing + kStages * kTcSlotBytes;  // [plane][kStg] slots
     static constexpr int kOffScale = kOffStg + 2 * kStg * kStgSlot;     // K [16][4], V [8][4] floats
-    static constexpr int kScaleBytes = kFp8 ? (kTcKScaleRing + kTcVScaleRing) * 4 * 4 : 0;
+    static constexpr int kScaleBytes = kF16 ? (kTcKScaleRing + kTcVScaleRing) * 4 * 4 : 0;
     static constexpr int kOffTail = kOffScale + kScaleBytes;
     // tail: barriers k_full[S], k_empty[S], v_full[S], v_empty[S], staging
     // full[2][kStg]; per tile s_full, s_free, p_full, o_done (and four unused);
     // q_ready, done; then ints: abort, sequence, block, K stages issued,
-    // tensor-memory address, V stages issued, the pages brought into every
-    // V slot (bf16 pool) or every staging slot (FP8 pool)
+    // tensor-memory address, V stages issued, the sequence's first page in
+    // a widened scratch, the pages brought into every V slot (bf16 pool) or
+    // every staging slot (FP8 pool)
     static constexpr int kBars = 4 * kStages + 2 * kStg + kTcTiles * 8 + 2;
-    static constexpr int kTailBytes = kBars * 8 + (6 + kStages + 2 * kStg) * 4;
+    static constexpr int kTailBytes = kBars * 8 + (7 + kStages + 2 * kStg) * 4;
     static constexpr int kSmemBytes = kOffTail + kTailBytes + 1024;
     static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
     static_assert(kOffKRing % 1024 == 0 && kOffVRing % 1024 == 0 && kOffStg % 1024 == 0,
@@ -340,11 +453,12 @@ __device__ __forceinline__ uint32_t pack16x2(float lo, float hi) {
     }
 }
 
-template <bool kFp8>
+template <int kPool>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_attention_tc_kernel(const __grid_constant__ CUtensorMap kv_map,
                                 const __grid_constant__ Params p) {
-    using Ly = TcLayout<kFp8>;
+    using Ly = TcLayout<kPool>;
+    constexpr bool kF16 = Ly::kF16, kStage = Ly::kStage;
     constexpr int S = Ly::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
@@ -367,12 +481,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t q_ready = tile_bar0 + 64 * kTcTiles;
     const uint32_t done_bar = q_ready + 8;
     // misc: [0] abort, [1] sequence, [2] query block, [3] K stages issued,
-    // [4] tensor-memory address, [5] V stages issued; pmask[s]: pages brought
-    // into V slot s (bf16 pool); smask[plane][q]: pages brought into staging
+    // [4] tensor-memory address, [5] V stages issued, [6] the sequence's
+    // first page in a widened scratch; pmask[s]: pages brought into V slot s
+    // (bf16 or widened pool); smask[plane][q]: pages brought into staging
     // slot q (FP8 pool)
     volatile int *misc = reinterpret_cast<volatile int *>(tail + Ly::kBars * 8);
-    volatile int *pmask = misc + 6;
-    volatile int *smask = misc + 6 + S;
+    volatile int *pmask = misc + 7;
+    volatile int *smask = misc + 7 + S;
     float *kscale = reinterpret_cast<float *>(sm + Ly::kOffScale);          // [16][4]
     float *vscale = kscale + kTcKScaleRing * kTcPagesPerStage;              // [8][4]
     const int g = blockIdx.x % p.Hkv;
@@ -418,6 +533,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 int n, L;
                 if (!chunk_ok(p, b, n, L)) flag_error(p.err, QDEC_FLAG_BAD_SEQLEN);
             }
+        }
+        if constexpr (kPool == kPoolWide) {
+            __syncwarp();
+            const int bb = misc[1];
+            int before = 0;  // widened pages of the sequences before bb
+            for (int i = 0; i < per; ++i) {
+                const int b2 = lane * per + i;
+                if (bb >= 0 && b2 < bb) before += widened_pages(p, b2);
+            }
+            before = warp_sum_int(before);
+            if (lane == 0) misc[6] = before;
         }
         if (lane == 0) {
             for (int s = 0; s < S; ++s) {
@@ -487,28 +613,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             return __shfl_sync(kFull, ok, 0) != 0;
         };
-        if constexpr (!kFp8) {
+        if constexpr (!kStage) {
             // lanes 0-3 each bring one page of the stage (its two regions);
             // the block-table entries are looked up 32 pages (8 stages) at a
-            // time, one group ahead
+            // time, one group ahead.  A widened pool is read at the sequence's
+            // scratch pages, which need no lookup (every page below npg is
+            // there, zero where the block table has no valid entry)
+            constexpr bool kWide = kPool == kPoolWide;
             auto lookup = [&](int grp) {  // lane l: page index 32 grp + l of the sequence
                 const int pg = 32 * grp + lane;
-                return pg < npg ? p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg] : -1;
+                return !kWide && pg < npg ? p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg]
+                                          : -1;
             };
             int cur = lookup(0), nxt = lookup(1);
+            const int wbase = kWide ? misc[6] : 0;
             // the chunk's keys and values were appended by the kernel before
             if (p.pdl) grid_dependency_wait();
             for (int j = 0; j < ntiles; ++j) {
                 const int s = j % S;
-                if (j > 0 && (j * kTcPagesPerStage) % 32 == 0) {
+                if (!kWide && j > 0 && (j * kTcPagesPerStage) % 32 == 0) {
                     cur = nxt;
                     nxt = lookup(j * kTcPagesPerStage / 32 + 1);
                 }
                 if (j >= S && !lane0_wait(empty0 + 8 * s, ((j / S) - 1) & 1)) break;
                 const int pg = j * kTcPagesPerStage + lane;
                 const int page = __shfl_sync(kFull, cur, (j * kTcPagesPerStage + (lane & 3)) & 31);
-                const bool ok = lane < kTcPagesPerStage && pg < npg && page >= 0 && page < p.num_pages;
-                if (!isv && lane < kTcPagesPerStage && pg < npg && !ok)
+                const bool valid = kWide || (page >= 0 && page < p.num_pages);
+                const bool ok = lane < kTcPagesPerStage && pg < npg && valid;
+                if (!isv && lane < kTcPagesPerStage && pg < npg && !valid)
                     flag_error(p.err, QDEC_FLAG_BAD_PAGE);
                 const unsigned mask = __ballot_sync(kFull, ok) & 0xFu;
                 const bool withheld = !isv && p.withhold_first && j == 0;  // test hook: never lands
@@ -524,7 +656,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 __syncwarp();
                 if (ok && !withheld) {
                     const uint32_t dst = smem_u32(ringp + s * kTcSlotBytes) + lane * (kPageSize * 128);
-                    const int row = page * 2 * p.Hkv + g;
+                    const int row = (kWide ? wbase + pg : page) * 2 * p.Hkv + g;
 #pragma unroll
                     for (int h = 0; h < 2; ++h)  // region h: dims 64 h .. 64 h + 63 of the plane
                         tma_load_region(dst + h * kTcRegion, &kv_map, h, plane, row, full0 + 8 * s);
@@ -653,7 +785,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (lane == 0) misc[isv ? 5 : 3] = staged;  // staging copies issued
         }
-        if constexpr (!kFp8)
+        if constexpr (!kStage)
             if (lane == 0) misc[isv ? 5 : 3] = issued;
     } else if (warp == kTcMmaWarp || warp == kTcMmaWarp1) {
         // ------------------------------------------- the MMA issuers --
@@ -664,9 +796,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int u = warp == kTcMmaWarp ? 0 : 1;
             const uint32_t qt = smem_u32(sm + Ly::kOffQ) + u * kTcQBytes;
             const uint32_t kring = smem_u32(sm + Ly::kOffKRing), vring = smem_u32(sm + Ly::kOffVRing);
-            constexpr uint32_t kIdS = kFp8 ? tc::idesc_f16(kTcRows, kTcKeys, false)
+            constexpr uint32_t kIdS = kF16 ? tc::idesc_f16(kTcRows, kTcKeys, false)
                                            : tc::idesc_bf16(kTcRows, kTcKeys, false);
-            constexpr uint32_t kIdO = kFp8 ? tc::idesc_f16(kTcRows, kHeadDim, true)
+            constexpr uint32_t kIdO = kF16 ? tc::idesc_f16(kTcRows, kHeadDim, true)
                                            : tc::idesc_bf16(kTcRows, kHeadDim, true);
             const uint32_t tile_tm = tmem + 256 * u;
             // O += P_t V_t once V_t has landed and the tile's softmax warps
@@ -758,8 +890,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int k = 0; k < kTcRows / 4; ++k) {
                 const int rr = (warp & 3) + 4 * k;
-                const uint2 w = make_uint2(pack16x2<kFp8>(x[k].x * p.qscale, x[k].y * p.qscale),
-                                           pack16x2<kFp8>(x[k].z * p.qscale, x[k].w * p.qscale));
+                const uint2 w = make_uint2(pack16x2<kF16>(x[k].x * p.qscale, x[k].y * p.qscale),
+                                           pack16x2<kF16>(x[k].z * p.qscale, x[k].w * p.qscale));
                 *reinterpret_cast<uint2 *>(qt + half * kTcQHalf + sw128_off(rr, cc) + sub) = w;
             }
             fence_proxy_async_smem();  // read next by the tensor core
@@ -797,7 +929,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // producer wrote them before); the scores of page q of the stage
             // times its K scale
             float vs[kTcPagesPerStage] = {1.f, 1.f, 1.f, 1.f};
-            if constexpr (kFp8) {
+            if constexpr (kF16) {
                 if (!wait_all(v_full0 + 8 * s, (j / S) & 1)) {
                     ok = false;
                     break;
@@ -863,10 +995,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int c = 0; c < kTcKeys / 2; ++c) {
                 const float p0 = fast_exp2(sc[2 * c] - m);
                 const float p1 = fast_exp2(sc[2 * c + 1] - m);
-                if constexpr (kFp8) {
+                if constexpr (kF16) {
                     ps[c & 3] += p0 + p1;
                     const float sv = vs[(2 * c) / kPageSize];
-                    pw[c] = pack16x2<kFp8>(p0 * sv, p1 * sv);
+                    pw[c] = pack16x2<kF16>(p0 * sv, p1 * sv);
                 } else {
                     ps[c & 3] += p0 + p1;
                     pw[c] = __byte_perm(__float_as_uint(p0) + 0x8000u, __float_as_uint(p1) + 0x8000u,
@@ -883,7 +1015,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             tc::st32(trow + 64, pw);
             l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-            if constexpr (!kFp8) {
+            if constexpr (!kStage) {
                 // V rows of keys past the sequence (and of pages not brought
                 // there) are zeroed once the slot has landed, by each tile's
                 // warps: both value products read them
@@ -951,7 +1083,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const bool isv = warp == kTcVProducerWarp;
         const int issued = misc[isv ? 5 : 3];
         volatile int never = 0;
-        if constexpr (kFp8) {
+        if constexpr (kStage) {
             const uint32_t sfull0 = stg_full0 + 8 * Ly::kStg * (isv ? 1 : 0);
             for (int t = max(0, issued - Ly::kStg); t < issued; ++t)
                 mbar_wait_bounded(sfull0 + 8 * (t % Ly::kStg), (t / Ly::kStg) & 1, &never,
@@ -965,19 +1097,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 std::mutex g_pf_mu;
-bool g_pf_tc_smem_set[2][64];
+bool g_pf_tc_smem_set[3][64];
 
-template <bool kFp8>
+template <int kPool>
 cudaError_t launch_tc(const Params &p, const CUtensorMap &kv_map, int dev, cudaStream_t s) {
-    using Ly = TcLayout<kFp8>;
+    using Ly = TcLayout<kPool>;
     {
         std::lock_guard<std::mutex> lock(g_pf_mu);
-        if (!g_pf_tc_smem_set[kFp8 ? 1 : 0][dev]) {
-            const cudaError_t e = cudaFuncSetAttribute(prefill_attention_tc_kernel<kFp8>,
+        if (!g_pf_tc_smem_set[kPool][dev]) {
+            const cudaError_t e = cudaFuncSetAttribute(prefill_attention_tc_kernel<kPool>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                        Ly::kSmemBytes);
             if (e != cudaSuccess) return e;
-            g_pf_tc_smem_set[kFp8 ? 1 : 0][dev] = true;
+            g_pf_tc_smem_set[kPool][dev] = true;
         }
     }
     // units: at most T / 64 + B blocks of 64 chunk rows, times the KV heads
@@ -992,7 +1124,7 @@ cudaError_t launch_tc(const Params &p, const CUtensorMap &kv_map, int dev, cudaS
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = p.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, prefill_attention_tc_kernel<kFp8>, kv_map, p);
+    return cudaLaunchKernelEx(&cfg, prefill_attention_tc_kernel<kPool>, kv_map, p);
 }
 
 }  // namespace
@@ -1006,13 +1138,31 @@ cudaError_t launch_prefill_append(const Params &p, bool fp8, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_attention(const Params &p, const CUtensorMap &kv_map, bool fp8,
+cudaError_t launch_prefill_attention(const Params &p, const CUtensorMap &kv_map, int pool,
                                      cudaStream_t s) {
     if (p.T <= 0) return cudaSuccess;
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 63;
-    return fp8 ? launch_tc<true>(p, kv_map, dev, s) : launch_tc<false>(p, kv_map, dev, s);
+    switch (pool) {
+    case kPrefillPoolFp8: return launch_tc<kPoolFp8>(p, kv_map, dev, s);
+    case kPrefillPoolWide: return launch_tc<kPoolWide>(p, kv_map, dev, s);
+    default: return launch_tc<kPoolBf16>(p, kv_map, dev, s);
+    }
+}
+
+cudaError_t launch_prefill_widen(const Params &p, cudaStream_t s) {
+    if (p.T <= 0) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.B) * static_cast<unsigned>(p.max_blocks));
+    cfg.blockDim = dim3(kWidenThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = p.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, prefill_widen_kernel, p);
 }
 
 }  // namespace qdec

@@ -27,6 +27,7 @@ QDEC_ERR_DEVICE_BOUNDS = 5
 QDEC_ERR_TIMEOUT = 6
 
 QDEC_LAUNCH_OVERLAP_PREVIOUS = 1
+QDEC_LAUNCH_PREFILL_PAGES_READY = 2
 
 QDEC_FLAG_BAD_PAGE = 1
 QDEC_FLAG_BAD_SEQLEN = 2
@@ -40,7 +41,7 @@ EXPORTS = ("qdec_workspace_bytes", "qdec_step_launches", "qdec_workspace_init",
            "qdec_attn_decode", "qdec_step", "qdec_qkv_append_rope", "qdec_qkv_pack_weights",
            "qdec_append_rope_fp8", "qdec_attn_split_fp8", "qdec_attn_decode_fp8",
            "qdec_prefill_append_rope", "qdec_prefill_attn", "qdec_prefill_append_rope_fp8",
-           "qdec_prefill_attn_fp8", "qdec_qkv_append_rope_fp8",
+           "qdec_prefill_attn_fp8", "qdec_prefill_fp8_workspace_bytes", "qdec_qkv_append_rope_fp8",
            "qdec_step_fp8",
            "qdec_step_static_scratch", "qdec_check_error", "qdec_status_string", "qdec_version")
 
@@ -120,8 +121,11 @@ def _load():
     lib.qdec_prefill_append_rope_fp8.argtypes = [sp, ctypes.c_int32, vp, i64, vp, i64, vp, i64,
                                                  vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.qdec_prefill_append_rope_fp8.restype = st
-    lib.qdec_prefill_attn_fp8.argtypes = [sp, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.qdec_prefill_attn_fp8.argtypes = [sp, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, sz, vp,
+                                          vp, vp]
     lib.qdec_prefill_attn_fp8.restype = st
+    lib.qdec_prefill_fp8_workspace_bytes.argtypes = [sp]
+    lib.qdec_prefill_fp8_workspace_bytes.restype = sz
     lib.qdec_step.argtypes = [sp, vp, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                               vp, vp, vp]
     lib.qdec_step.restype = st
@@ -283,12 +287,20 @@ def qdec_prefill_append_rope_fp8(shape: Shape, q, k, v, q_norm_w, k_norm_w, posi
 
 
 def qdec_prefill_attn_fp8(shape: Shape, q_rot, qo_indptr, seq_lens, block_table, kv_pool_fp8,
-                          kv_scale, out, err_flag=None, stream=None):
+                          kv_scale, out, err_flag=None, stream=None, workspace=None):
+    """workspace: None (each query block converts the codes it reads) or a
+    device buffer of at least qdec_prefill_fp8_workspace_bytes(shape) bytes
+    (the pages are dequantized to bf16 once, then attended as a bf16 pool)."""
     pool, scale = _fp8_pool(kv_pool_fp8, kv_scale)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _raise(_lib.qdec_prefill_attn_fp8(
         ctypes.byref(shape.c()), q_rot.shape[0], _ptr(q_rot), _ptr(qo_indptr), _ptr(seq_lens),
-        _ptr(block_table), pool, scale, _ptr(out), _ptr(err_flag), _stream(stream)),
-        "qdec_prefill_attn_fp8")
+        _ptr(block_table), pool, scale, _ptr(workspace), nbytes, _ptr(out), _ptr(err_flag),
+        _stream(stream)), "qdec_prefill_attn_fp8")
+
+
+def qdec_prefill_fp8_workspace_bytes(shape: Shape) -> int:
+    return int(_lib.qdec_prefill_fp8_workspace_bytes(ctypes.byref(shape.c())))
 
 
 def qdec_attn_merge(shape: Shape, seq_lens, workspace, out, err_flag=None, stream=None):

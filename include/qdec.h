@@ -79,6 +79,14 @@ typedef enum {
 
 /* qdec_shape.launch_flags */
 #define QDEC_LAUNCH_OVERLAP_PREVIOUS 1
+/* qdec_prefill_attn_fp8 with a workspace: the workspace already holds the
+ * dequantized pages of this call's sequences, written by an earlier
+ * qdec_prefill_attn_fp8 call with the same shape, qo_indptr, seq_lens,
+ * block_table and workspace, and neither the pool's pages of those
+ * sequences nor kv_scale have changed since (e.g. attending several query
+ * sets over one context): the dequantizing pass is skipped and the call is
+ * one launch.  Other calls ignore it. */
+#define QDEC_LAUNCH_PREFILL_PAGES_READY 2
 /* Test hook for the failure path, not for production use: in every CTA of
  * the paged attention kernels (qdec_step, qdec_attn_split, qdec_attn_decode,
  * qdec_prefill_attn and their FP8 forms) the first page tile is never
@@ -130,7 +138,7 @@ typedef struct {
     int32_t num_ctas;            /* attention grid size; 0 = automatic (a whole
                                     number of CTAs per SM).  Results do not
                                     depend on it beyond fp32 rounding.          */
-    int32_t launch_flags;        /* QDEC_LAUNCH_* bits (qdec_step only)          */
+    int32_t launch_flags;        /* QDEC_LAUNCH_* bits                           */
 } qdec_shape;
 
 /* Bytes of device workspace that qdec_attn_split / qdec_attn_merge /
@@ -371,7 +379,19 @@ qdec_status qdec_attn_decode_fp8(const qdec_shape *shape, const float *q_rot,
 /* Chunked prefill over an FP8 pool: qdec_prefill_append_rope storing the
  * chunk rows' codes (the append rule above, each row with the scales of its
  * slot's (page, plane, head)), and qdec_prefill_attn over the dequantized
- * pool.  kv_scale is read only. */
+ * pool.  kv_scale is read only.
+ * qdec_prefill_attn_fp8 with a workspace (device memory, 16-byte aligned, at
+ * least qdec_prefill_fp8_workspace_bytes(shape) bytes, caller-owned, no
+ * initialisation needed) first dequantizes every page of the chunks'
+ * sequences once into it, each value code x scale rounded to bf16 (a
+ * relative error of at most 2^-8, against the 2^-4 of the E4M3 code), then
+ * runs the bf16-pool attention over that copy: two launches, each page
+ * dequantized once instead of once per 64-row query block, and no scale in
+ * the softmax (the faster form).  With workspace NULL (workspace_bytes
+ * ignored) each block converts the codes it reads exactly to f16 and
+ * applies the scales in the softmax: one launch, no memory.  The two agree
+ * to within the bf16 rounding of the dequantized values;
+ * QDEC_ERR_WORKSPACE if the workspace is too small or misaligned. */
 qdec_status qdec_prefill_append_rope_fp8(const qdec_shape *shape, int32_t num_tokens,
                                          const qdec_bf16 *q, int64_t q_stride,
                                          const qdec_bf16 *k, int64_t k_stride,
@@ -385,7 +405,12 @@ qdec_status qdec_prefill_attn_fp8(const qdec_shape *shape, int32_t num_tokens,
                                   const float *q_rot, const int32_t *qo_indptr,
                                   const int32_t *seq_lens, const int32_t *block_table,
                                   const uint8_t *kv_pool_fp8, const float *kv_scale,
-                                  qdec_bf16 *out, int32_t *err_flag, void *stream);
+                                  void *workspace, size_t workspace_bytes, qdec_bf16 *out,
+                                  int32_t *err_flag, void *stream);
+/* Bytes of the workspace that qdec_prefill_attn_fp8 dequantizes into:
+ * batch * max_blocks_per_seq pages of 2 * Hkv * 16 * 128 bf16 values
+ * (0 for an invalid shape).  Host only. */
+size_t qdec_prefill_fp8_workspace_bytes(const qdec_shape *shape);
 
 /* qdec_qkv_append_rope with an FP8 pool: the projected key and value rows,
  * rounded to bf16 as the bf16 pool would hold them, are divided by their

@@ -201,7 +201,14 @@ def test_prefill_wait_that_runs_out_returns_timeout_and_device_stays_usable():
 
 # ------------------------------------------------------------------- FP8 pool --
 
-def _run_fp8(c, codes, sc, B):
+def _fp8_workspace(shape):
+    """A scratch for the widened-pages path, poisoned so a read of a byte the
+    widening pass did not write shows up."""
+    n = parity.qdec().qdec_prefill_fp8_workspace_bytes(shape)
+    return torch.full((n,), 0x7F, dtype=torch.uint8, device="cuda")
+
+
+def _run_fp8(c, codes, sc, B, widen=False):
     q = parity.qdec()
     shape = _shape(c, B)
     T = c.q.shape[0]
@@ -210,8 +217,9 @@ def _run_fp8(c, codes, sc, B):
     out = torch.full((T, 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
     q.qdec_prefill_append_rope_fp8(shape, c.q, c.k, c.v, c.w_q, c.w_k, c.positions, c.qo_indptr,
                                    c.seq_lens, c.block_table, codes, sc, q_rot, err)
+    ws = _fp8_workspace(shape) if widen else None
     q.qdec_prefill_attn_fp8(shape, q_rot, c.qo_indptr, c.seq_lens, c.block_table, codes, sc, out,
-                            err)
+                            err, workspace=ws)
     return q_rot, out, err
 
 
@@ -219,12 +227,15 @@ FP8_CASES = [([37], [37]), ([300, 17, 1000], [20, 17, 1]), ([64, 65, 31], [48, 1
              ([500, 40, 77, 250], [0, 40, 33, 0]), ([2048], [200])]
 
 
+@pytest.mark.parametrize("widen", [False, True], ids=["in-kernel", "widened"])
 @pytest.mark.parametrize("seq_lens,chunks", FP8_CASES, ids=lambda x: str(x)[:40])
-def test_prefill_fp8_matches_oracle(seq_lens, chunks):
+def test_prefill_fp8_matches_oracle(seq_lens, chunks, widen):
     """FP8 pool: q_rot and out as for bf16; the appended K and V codes equal
     the oracle's bit for bit (the bf16 key is the nearest-even rounding of the
     exact value on both sides; both divide in fp32 by the scale and round
-    once); nothing outside the chunk's slots changes."""
+    once); nothing outside the chunk's slots changes.  Both ways of reading
+    the codes are checked: converted inside the attention kernel, and
+    widened once into a caller's workspace beforehand."""
     c, codes, sc = wl.prefill_case_fp8(seq_lens, chunks, seed=sum(seq_lens) % 89)
     before = codes.cpu().numpy().copy()
     pool = before.copy()
@@ -236,7 +247,7 @@ def test_prefill_fp8_matches_oracle(seq_lens, chunks):
                                     float(np.float32(1e-6)))
     ref_out, _ = oracle.prefill_attention_fp8(pool, sc_h, bt, qo, L, res["q_rot"],
                                               1 / math.sqrt(128))
-    q_rot, out, err = _run_fp8(c, codes, sc, len(seq_lens))
+    q_rot, out, err = _run_fp8(c, codes, sc, len(seq_lens), widen)
     st, flags = parity.qdec().qdec_check_error(err)
     assert st == 0 and flags == 0, (st, flags)
     g = q_rot.double().cpu().numpy()
@@ -255,23 +266,132 @@ def test_prefill_fp8_matches_oracle(seq_lens, chunks):
     assert np.array_equal(got[~changed], before[~changed]), "append touched another slot"
 
 
-def test_prefill_fp8_wait_that_runs_out_returns_timeout_and_device_stays_usable():
+def _oracle_fp8(c, codes, sc):
+    """The oracle's append over a host copy of the FP8 pool, then its
+    attention over the appended pool."""
+    pool = codes.cpu().numpy().copy()
+    sc_h = sc.cpu().numpy()
+    qo, L, bt = c.qo_indptr.cpu().numpy(), c.seq_lens.cpu().numpy(), c.block_table.cpu().numpy()
+    res = oracle.prefill_append_fp8(wl.bf16_bits(c.q), wl.bf16_bits(c.k), wl.bf16_bits(c.v),
+                                    wl.bf16_bits(c.w_q), wl.bf16_bits(c.w_k),
+                                    c.positions.cpu().numpy(), qo, L, bt, pool, sc_h, 1e6,
+                                    float(np.float32(1e-6)))
+    ref_out, _ = oracle.prefill_attention_fp8(pool, sc_h, bt, qo, L, res["q_rot"],
+                                              1 / math.sqrt(128))
+    return ref_out
+
+
+@pytest.mark.parametrize("seq_lens,chunks", [([300, 17, 1000], [20, 17, 1]),
+                                             ([2048, 64, 5], [2048, 48, 5]),
+                                             ([129, 4000], [129, 31])],
+                         ids=lambda x: str(x)[:40])
+def test_prefill_fp8_widened_equals_bf16_pool_of_the_dequantized_values(seq_lens, chunks):
+    """The workspace path dequantizes each code once (code x scale in fp32,
+    rounded to the nearest-even bf16) and then attends exactly as over a bf16
+    pool: its output equals, bit for bit, the bf16-pool attention over a
+    pool dequantized that way on the host, on a poisoned workspace.  The
+    in-kernel conversion path (exact f16 codes, scales in the softmax) stays
+    within the output tolerance of it."""
+    q = parity.qdec()
+    c, codes, sc = wl.prefill_case_fp8(seq_lens, chunks, seed=len(seq_lens) + sum(chunks) % 61)
+    shape = _shape(c, len(seq_lens))
+    q_rot, out, err = _run_fp8(c, codes, sc, len(seq_lens))
+    st, flags = q.qdec_check_error(err)
+    assert st == 0 and flags == 0, (st, flags)
+    wide = torch.full_like(out, float("nan"))
+    q.qdec_prefill_attn_fp8(shape, q_rot, c.qo_indptr, c.seq_lens, c.block_table, codes, sc,
+                            wide, err, workspace=_fp8_workspace(shape))
+    st, flags = q.qdec_check_error(err)
+    assert st == 0 and flags == 0, (st, flags)
+    vals = codes.cpu().view(torch.float8_e4m3fn).float() * sc.cpu()[..., None, None]
+    pool16 = vals.to(torch.bfloat16).cuda()
+    ref = torch.full_like(out, float("nan"))
+    q.qdec_prefill_attn(shape, q_rot, c.qo_indptr, c.seq_lens, c.block_table, pool16, ref, err)
+    st, flags = q.qdec_check_error(err)
+    assert st == 0 and flags == 0, (st, flags)
+    assert torch.equal(wide.view(torch.int16), ref.view(torch.int16))
+    parity.assert_out_close(out, parity.to_f64(wide), "in-kernel vs workspace")
+
+
+def test_prefill_fp8_pages_ready_attends_over_the_workspace_as_left():
+    """With QDEC_LAUNCH_PREFILL_PAGES_READY the call skips the dequantizing
+    pass and attends over what an earlier call left in the workspace: the
+    same bits as that call, both as a plain launch and as a programmatic
+    dependent."""
+    q = parity.qdec()
+    c, codes, sc = wl.prefill_case_fp8([700, 129, 40], [300, 129, 7], seed=19)
+    shape = _shape(c, 3)
+    T = c.q.shape[0]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q_rot = torch.empty((T, 32, 128), dtype=torch.float32, device="cuda")
+    q.qdec_prefill_append_rope_fp8(shape, c.q, c.k, c.v, c.w_q, c.w_k, c.positions, c.qo_indptr,
+                                   c.seq_lens, c.block_table, codes, sc, q_rot, err)
+    ws = _fp8_workspace(shape)
+    first = torch.full((T, 32, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    q.qdec_prefill_attn_fp8(shape, q_rot, c.qo_indptr, c.seq_lens, c.block_table, codes, sc,
+                            first, err, workspace=ws)
+    for extra in (0, q.QDEC_LAUNCH_OVERLAP_PREVIOUS):
+        again = torch.full_like(first, float("nan"))
+        q.qdec_prefill_attn_fp8(_shape(c, 3, q.QDEC_LAUNCH_PREFILL_PAGES_READY | extra), q_rot,
+                                c.qo_indptr, c.seq_lens, c.block_table, codes, sc, again, err,
+                                workspace=ws)
+        st, flags = q.qdec_check_error(err)
+        assert st == 0 and flags == 0, (st, flags)
+        assert torch.equal(again.view(torch.int16), first.view(torch.int16))
+
+
+@pytest.mark.parametrize("widen", [False, True], ids=["in-kernel", "widened"])
+def test_prefill_fp8_bad_prefix_page_is_flagged(widen):
+    """A block-table entry outside the pool among one sequence's prefix pages
+    (which the append does not touch) is flagged by the attention call; the
+    other sequences are exact."""
+    q = parity.qdec()
+    c, codes, sc = wl.prefill_case_fp8([60, 70, 80], [20, 30, 40], seed=16)
+    ref_out = _oracle_fp8(c, codes.clone(), sc)
+    c.block_table[1, 0] = 10 ** 6                       # tokens 0-15 of sequence 1: prefix
+    q_rot, out, err = _run_fp8(c, codes, sc, 3, widen)
+    st, flags = q.qdec_check_error(err)
+    assert st == q.QDEC_ERR_DEVICE_BOUNDS and flags & q.QDEC_FLAG_BAD_PAGE, (st, flags)
+    rows = np.r_[0:20, 50:90]
+    parity.assert_out_close(out[rows], ref_out[rows])
+
+
+def test_prefill_fp8_widened_workspace_too_small_is_refused():
+    """A workspace one alignment unit short is refused before any launch
+    and the output is left untouched."""
+    q = parity.qdec()
+    c, codes, sc = wl.prefill_case_fp8([300, 17], [20, 17], seed=18)
+    shape = _shape(c, 2)
+    q_rot, out, err = _run_fp8(c, codes, sc, 2)
+    short = _fp8_workspace(shape)[:-16]
+    again = torch.full_like(out, float("nan"))
+    with pytest.raises(q.QdecError) as e:
+        q.qdec_prefill_attn_fp8(shape, q_rot, c.qo_indptr, c.seq_lens, c.block_table, codes, sc,
+                                again, err, workspace=short)
+    assert e.value.status == q.QDEC_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.isnan(again.float()).all()
+
+
+@pytest.mark.parametrize("widen", [False, True], ids=["in-kernel", "widened"])
+def test_prefill_fp8_wait_that_runs_out_returns_timeout_and_device_stays_usable(widen):
     """FP8 pool: as for bf16, the withheld tile's wait gives up with a timeout
     (the conversion barriers are never reached) and the next normal call
     gives the verified result bit for bit."""
     q = parity.qdec()
     c, codes, sc = wl.prefill_case_fp8([300, 17, 1000], [20, 17, 200], seed=17)
-    q_rot, out, err = _run_fp8(c, codes, sc, 3)
+    q_rot, out, err = _run_fp8(c, codes, sc, 3, widen)
     st, flags = q.qdec_check_error(err)
     assert st == 0 and flags == 0, (st, flags)
+    ws = _fp8_workspace(_shape(c, 3)) if widen else None
     withheld = torch.empty_like(out)
     q.qdec_prefill_attn_fp8(_shape(c, 3, q.QDEC_LAUNCH_TEST_WITHHOLD_TILE), q_rot, c.qo_indptr,
-                            c.seq_lens, c.block_table, codes, sc, withheld, err)
+                            c.seq_lens, c.block_table, codes, sc, withheld, err, workspace=ws)
     st, flags = q.qdec_check_error(err)
     assert st == q.QDEC_ERR_TIMEOUT and flags & q.QDEC_FLAG_TIMEOUT, (st, flags)
     again = torch.empty_like(out)
     q.qdec_prefill_attn_fp8(_shape(c, 3), q_rot, c.qo_indptr, c.seq_lens, c.block_table, codes,
-                            sc, again, err)
+                            sc, again, err, workspace=ws)
     st, flags = q.qdec_check_error(err)
     assert st == 0 and flags == 0, (st, flags)
     assert torch.equal(again, out)

@@ -128,7 +128,7 @@ def test_entry_points_reject_null_and_misaligned_arguments(q):
     # unsupported group size; unknown launch flag
     sh2 = ctypes.byref(_shape(q, num_q_heads=8, num_kv_heads=8).c())
     assert step(shape=sh2) == q.QDEC_ERR_UNSUPPORTED
-    sh3 = ctypes.byref(_shape(q, launch_flags=2).c())
+    sh3 = ctypes.byref(_shape(q, launch_flags=4).c())
     assert step(shape=sh3) == q.QDEC_ERR_INVALID_ARG
 
 
@@ -166,10 +166,17 @@ def test_fp8_entry_points_reject_bad_arguments(q):
     # an odd number of KV heads unsupported
     assert lib.qdec_prefill_append_rope_fp8(sh, 4, ok, S, ok, S, ok, S, ok, ok, ok, ok, ok, ok,
                                             ok, z, ok, z, z) == q.QDEC_ERR_INVALID_ARG
-    assert lib.qdec_prefill_attn_fp8(odd, 4, ok, ok, ok, ok, ok, ok, ok, z,
+    assert lib.qdec_prefill_attn_fp8(odd, 4, ok, ok, ok, ok, ok, ok, z, 0, ok, z,
                                      z) == q.QDEC_ERR_UNSUPPORTED
-    assert lib.qdec_prefill_attn_fp8(sh, 4, ok, ok, ok, ok, ok, bad, ok, z,
+    assert lib.qdec_prefill_attn_fp8(sh, 4, ok, ok, ok, ok, ok, bad, z, 0, ok, z,
                                      z) == q.QDEC_ERR_INVALID_ARG
+    # the widening workspace: too small or misaligned is refused before any launch
+    need = lib.qdec_prefill_fp8_workspace_bytes(sh)
+    assert need > 0 and lib.qdec_prefill_fp8_workspace_bytes(None) == 0
+    assert lib.qdec_prefill_attn_fp8(sh, 4, ok, ok, ok, ok, ok, ok, ok, need - 16, ok, z,
+                                     z) == q.QDEC_ERR_WORKSPACE
+    assert lib.qdec_prefill_attn_fp8(sh, 4, ok, ok, ok, ok, ok, ok, bad, need, ok, z,
+                                     z) == q.QDEC_ERR_WORKSPACE
     assert lib.qdec_qkv_append_rope_fp8(sh, 256, ok, 256, ok, ok, ok, ok, ok, ok, ok, ok, z, ok,
                                         z, z) == q.QDEC_ERR_INVALID_ARG
     assert lib.qdec_qkv_append_rope_fp8(odd, 256, ok, 256, ok, ok, ok, ok, ok, ok, ok, ok, ok, ok,
