@@ -62,7 +62,6 @@
 #include "qdec.h"
 
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <math.h>
 
 #include <mutex>
@@ -180,19 +179,10 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// Two E4M3 codes (low byte -> low half) as an f16 pair; exact, since every
-// E4M3 value is an f16 value.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    const __half2_raw h =
-        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-}
 // E4M3 codes of a / s and b / s (fp32 division, one rounding each, then
 // nearest-even with saturation to +-448), a in the low byte.
 __device__ __forceinline__ uint32_t quantize2_e4m3(float a, float b, float s) {
-    return static_cast<uint32_t>(
-        __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s)), __NV_SATFINITE,
-                                 __NV_E4M3));
+    return f32x2_to_e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s));
 }
 __device__ __forceinline__ void consumer_sync() {  // the 128 consumer threads only
     asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -463,9 +453,9 @@ static_assert(16 * kQ8Stride <= kOffKvNew - kOffQb, "FP8 q operand fits the q bu
 static_assert(kOffQScale + kGroup * 4 <= kOffRope, "unscale slots fit the kv_new buffer");
 
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_codes) {
-    const __half2_raw h =
-        __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
-    return make_float2(__half2float(__ushort_as_half(h.x)), __half2float(__ushort_as_half(h.y)));
+    const uint32_t h = e4m3x2_to_f16x2(two_codes);
+    return make_float2(__half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu))),
+                       __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16))));
 }
 
 __device__ void store_q_e4m3(uint8_t *sm, int w, int lane, const float (&ys)[4]) {
@@ -480,10 +470,8 @@ __device__ void store_q_e4m3(uint8_t *sm, int w, int lane, const float (&ys)[4])
     uint8_t *q8 = sm + kOffQb;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t c01 = static_cast<uint32_t>(
-            __nv_cvt_float2_to_fp8x2(make_float2(x[0], x[1]), __NV_SATFINITE, __NV_E4M3));
-        const uint32_t c23 = static_cast<uint32_t>(
-            __nv_cvt_float2_to_fp8x2(make_float2(x[2], x[3]), __NV_SATFINITE, __NV_E4M3));
+        const uint32_t c01 = f32x2_to_e4m3x2(x[0], x[1]);
+        const uint32_t c23 = f32x2_to_e4m3x2(x[2], x[3]);
         uint16_t *col = reinterpret_cast<uint16_t *>(q8 + (4 * i + w) * kQ8Stride);
         col[lane] = static_cast<uint16_t>(c01);
         col[32 + lane] = static_cast<uint16_t>(c23);

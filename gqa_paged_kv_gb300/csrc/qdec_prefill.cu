@@ -28,7 +28,6 @@
 #include "qdec.h"
 
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <math.h>
 
 #include <mutex>
@@ -104,8 +103,7 @@ constexpr int kPfAppendThreads = 256;
 // E4M3 codes of a / s and b / s (fp32 division, one rounding each, then
 // nearest-even with saturation to +-448), a in the low byte.
 __device__ __forceinline__ uint16_t quantize_pair_e4m3(float a, float b, float s) {
-    return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(
-        make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s)), __NV_SATFINITE, __NV_E4M3));
+    return f32x2_to_e4m3x2(__fdiv_rn(a, s), __fdiv_rn(b, s));
 }
 
 template <bool kFp8>
@@ -201,13 +199,6 @@ __global__ void __launch_bounds__(kPfAppendThreads) prefill_append_kernel(
     }
 }
 
-// Two E4M3 codes (the low byte first) as an f16 pair: exact (every E4M3
-// value is an f16 value; NaN stays NaN).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-        static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-}
 
 // ------------------------------------------------------- FP8 widening --
 // The E4M3 pages of every well-formed chunk's sequence dequantised once into
@@ -227,8 +218,8 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
 constexpr int kWidenThreads = 256, kWidenBatch = 8;
 
 __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint32_t two_codes, float scale) {
-    const float2 f = __half22float2(__half2(__half2_raw(__nv_cvt_fp8x2_to_halfraw2(
-        static_cast<__nv_fp8x2_storage_t>(two_codes & 0xFFFFu), __NV_E4M3))));
+    const uint32_t h = e4m3x2_to_f16x2(two_codes);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
     const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
     return *reinterpret_cast<const uint32_t *>(&b);
 }

@@ -10,6 +10,21 @@ namespace qdec {
 static __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// Two E4M3 codes (the low 16 bits of `two_codes`, the low byte first) as an
+// f16 pair (low byte -> low half): one conversion instruction; exact, since
+// every E4M3 value is an f16 value (NaN stays NaN).
+static __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(static_cast<unsigned short>(two_codes)));
+    return d;
+}
+// E4M3 codes of lo and hi (nearest-even, saturated to +-448; NaN stays NaN)
+// as two bytes, lo in the low byte: one conversion instruction.
+static __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+    unsigned short d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
 static __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }

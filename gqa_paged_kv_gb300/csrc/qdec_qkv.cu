@@ -40,7 +40,6 @@
 #include "qdec_ptx.cuh"
 #include "qdec.h"
 
-#include <cuda_fp8.h>
 #include <math.h>
 
 #include <algorithm>
@@ -201,10 +200,8 @@ __device__ __forceinline__ void store_row4(const Params &p, int64_t slot, int d0
     auto codes = [s](uint2 v) {  // four bf16 -> four E4M3 codes, low dim first
         const float2 f0 = make_float2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
         const float2 f1 = make_float2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
-        const uint32_t c0 = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f0.x, s), __fdiv_rn(f0.y, s)),
-                                                     __NV_SATFINITE, __NV_E4M3);
-        const uint32_t c1 = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f1.x, s), __fdiv_rn(f1.y, s)),
-                                                     __NV_SATFINITE, __NV_E4M3);
+        const uint32_t c0 = f32x2_to_e4m3x2(__fdiv_rn(f0.x, s), __fdiv_rn(f0.y, s));
+        const uint32_t c1 = f32x2_to_e4m3x2(__fdiv_rn(f1.x, s), __fdiv_rn(f1.y, s));
         return (c0 & 0xffffu) | (c1 << 16);
     };
     *reinterpret_cast<uint32_t *>(p.pool8 + slot + d0) = codes(lo);
