@@ -605,8 +605,8 @@ __device__ __forceinline__ void tile_math(uint32_t ks, uint32_t vs, const uint32
             tB = fmaxf(tB, __shfl_xor_sync(kFull, tB, o));
         }
         const float nA = fmaxf(st.mA, tA), nB = fmaxf(st.mB, tB);
-        const float aA = st.mA == kNegInf ? 0.f : exp2f(st.mA - nA);
-        const float aB = st.mB == kNegInf ? 0.f : exp2f(st.mB - nB);
+        const float aA = st.mA == kNegInf ? 0.f : fast_exp2(st.mA - nA);
+        const float aB = st.mB == kNegInf ? 0.f : fast_exp2(st.mB - nB);
         st.mA = nA;
         st.mB = nB;
         st.lA *= aA;
@@ -621,8 +621,8 @@ __device__ __forceinline__ void tile_math(uint32_t ks, uint32_t vs, const uint32
     }
     const float bA = st.mA == kNegInf ? 0.f : st.mA;
     const float bB = st.mB == kNegInf ? 0.f : st.mB;
-    const float pA0 = exp2f(sA0 - bA), pA1 = exp2f(sA1 - bA);
-    const float pB0 = exp2f(sB0 - bB), pB1 = exp2f(sB1 - bB);
+    const float pA0 = fast_exp2(sA0 - bA), pA1 = fast_exp2(sA1 - bA);
+    const float pB0 = fast_exp2(sB0 - bB), pB1 = fast_exp2(sB1 - bB);
     st.lA += pA0 + pA1;
     st.lB += pB0 + pB1;
 
@@ -735,8 +735,8 @@ __device__ __forceinline__ void tile_math_fp8(uint32_t ks, uint32_t vs, const ui
             tB = fmaxf(tB, __shfl_xor_sync(kFull, tB, o));
         }
         const float nA = fmaxf(st.mA, tA), nB = fmaxf(st.mB, tB);
-        const float aA = st.mA == kNegInf ? 0.f : exp2f(st.mA - nA);
-        const float aB = st.mB == kNegInf ? 0.f : exp2f(st.mB - nB);
+        const float aA = st.mA == kNegInf ? 0.f : fast_exp2(st.mA - nA);
+        const float aB = st.mB == kNegInf ? 0.f : fast_exp2(st.mB - nB);
         st.mA = nA;
         st.mB = nB;
         st.lA *= aA;
@@ -751,8 +751,8 @@ __device__ __forceinline__ void tile_math_fp8(uint32_t ks, uint32_t vs, const ui
     }
     const float bA = st.mA == kNegInf ? 0.f : st.mA;
     const float bB = st.mB == kNegInf ? 0.f : st.mB;
-    const float pA0 = exp2f(sA0 - bA), pA1 = exp2f(sA1 - bA);
-    const float pB0 = exp2f(sB0 - bB), pB1 = exp2f(sB1 - bB);
+    const float pA0 = fast_exp2(sA0 - bA), pA1 = fast_exp2(sA1 - bA);
+    const float pB0 = fast_exp2(sB0 - bB), pB1 = fast_exp2(sB1 - bB);
     st.lA += pA0 + pA1;
     st.lB += pB0 + pB1;
 
@@ -790,20 +790,24 @@ __device__ __forceinline__ void tile_math_fp8(uint32_t ks, uint32_t vs, const ui
         hi01[w] = __byte_perm(wc[w], wd[w], 0x5140);
         hi23[w] = __byte_perm(wc[w], wd[w], 0x7362);
     }
+    // m-tiles 4w + 2ip and 4w + 2ip + 1 from the halves of one permuted word
+    // each: dims 16tg + mt (t: tokens 2c, 2c+1; t8: tokens 2c+8, 2c+9) and
+    // 16tg + 8 + mt (u, u8)
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-        const int w = mt >> 2, i = mt & 3;
-        const int sh = (i & 1) * 16;
-        const uint32_t t01 = (i < 2 ? lo01[w] : lo23[w]) >> sh;       // dim 16tg + mt, tokens 2c, 2c+1
-        const uint32_t t89 = (i < 2 ? hi01[w] : hi23[w]) >> sh;       // tokens 2c+8, 2c+9
-        const uint32_t u01 = (i < 2 ? lo01[w + 2] : lo23[w + 2]) >> sh;  // dim 16tg + 8 + mt
-        const uint32_t u89 = (i < 2 ? hi01[w + 2] : hi23[w + 2]) >> sh;
-        uint32_t a[4];
-        a[0] = e4m3x2_to_f16x2(t01);
-        a[1] = e4m3x2_to_f16x2(u01);
-        a[2] = e4m3x2_to_f16x2(t89);
-        a[3] = e4m3x2_to_f16x2(u89);
-        mma_f16(st.o[mt], a, b0, b1);
+    for (int w = 0; w < 2; ++w) {
+#pragma unroll
+        for (int ip = 0; ip < 2; ++ip) {
+            uint32_t t[2], t8[2], u[2], u8[2];
+            e4m3x4_to_f16x2x2(ip ? lo23[w] : lo01[w], t[0], t[1]);
+            e4m3x4_to_f16x2x2(ip ? hi23[w] : hi01[w], t8[0], t8[1]);
+            e4m3x4_to_f16x2x2(ip ? lo23[w + 2] : lo01[w + 2], u[0], u[1]);
+            e4m3x4_to_f16x2x2(ip ? hi23[w + 2] : hi01[w + 2], u8[0], u8[1]);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t a[4] = {t[h], u[h], t8[h], u8[h]};
+                mma_f16(st.o[4 * w + 2 * ip + h], a, b0, b1);
+            }
+        }
     }
     __syncwarp();
 }
@@ -1003,18 +1007,31 @@ __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint3
         }
         ++kv_uses;
     }
-    for (int k = 0; k < cnt; ++k, ++i) {
-        if (static_cast<int>(i & 3) != warp) continue;
-        const int slot = i % NS;
-        const bool ok = mbar_wait_bounded(full0 + 8 * slot, (i / NS) & 1, misc, p.wait_cycles);
+    // this warp's tiles of the piece: ring positions i0 + k with (i0 + k) % 4
+    // == warp; as NS is a multiple of 4, each step of 4 advances the slot by
+    // 4 and flips the phase when it wraps
+    const uint32_t i0 = i;
+    const int kfirst = (warp - static_cast<int>(i0 & 3)) & 3;
+    int slot = static_cast<int>((i0 + kfirst) % NS);
+    uint32_t phase = ((i0 + kfirst) / NS) & 1;
+    i = i0 + cnt;
+    for (int k = kfirst; k < cnt; k += 4) {
+        const int cur = slot;
+        const uint32_t par = phase;
+        slot += 4;
+        if (slot >= NS) {
+            slot -= NS;
+            phase ^= 1;
+        }
+        const bool ok = mbar_wait_bounded(full0 + 8 * cur, par, misc, p.wait_cycles);
         if (!ok && lane == 0) {
             misc[0] = 1;
             flag_error(p.err, QDEC_FLAG_TIMEOUT);
         }
         const int pg = pg0 + k;
         const int ntok = min(kPageSize, L - pg * kPageSize);
-        if (ok && slot_ok[slot]) {
-            uint8_t *tile = ring + slot * slot_bytes<kFp8>();
+        if (ok && slot_ok[cur]) {
+            uint8_t *tile = ring + cur * slot_bytes<kFp8>();
             bool patch = kFused && pg == n - 1;
             if (patch && !mbar_wait_bounded(kv_bar, kv_parity, misc, p.wait_cycles)) {
                 if (lane == 0) {
@@ -1029,7 +1046,7 @@ __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint3
                     fix_tile_fp8(tile, ntok, patch, reinterpret_cast<const uint8_t *>(kv_new), lane);
                 // this slot's K and V scale, stored by the producer
                 const float *win = reinterpret_cast<const float *>(
-                    ring + NS * kFp8TileBytes + slot * kFp8SlotExtra);
+                    ring + NS * kFp8TileBytes + cur * kFp8SlotExtra);
                 const float sk = win[0];
                 tile_math_fp8(ks, ks + kFp8PlaneBytes, qf, ntok, lane, st,
                               reinterpret_cast<__half *>(pbuf), qunA * sk, qunB * sk,
@@ -1041,7 +1058,7 @@ __device__ void process_piece(const Params &p, uint8_t *sm, uint8_t *ring, uint3
         }
         __syncwarp();
         // a slot whose copy may still be landing is never handed back
-        if (ok && lane == 0) mbar_arrive(empty0 + 8 * slot);
+        if (ok && lane == 0) mbar_arrive(empty0 + 8 * cur);
     }
 }
 
@@ -1254,6 +1271,8 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kCluster, kFp8))
         if (kMode == kAttnDecode && p.pdl) grid_dependency_wait();
         const long long ntiles = kCluster ? pg_hi - pg_lo : hi - lo;
         uint32_t i = 0;
+        int next_slot = 0;   // i % NS
+        uint32_t wraps = 0;  // i / NS
         bool stop = false;
         for (long long base = 0; base < ntiles && !stop; base += 32) {
             int page = -1, g = cg;
@@ -1280,13 +1299,18 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kCluster, kFp8))
                 const int pj = __shfl_sync(kFull, page, j);
                 const int gj = __shfl_sync(kFull, g, j);
                 const float skj = __shfl_sync(kFull, sck, j), svj = __shfl_sync(kFull, scv, j);
+                const int slot = next_slot;
+                const uint32_t wr = wraps;
+                if (++next_slot == NS) {
+                    next_slot = 0;
+                    ++wraps;
+                }
                 if (lane == 0) {
-                    const int slot = i % NS;
                     const uint32_t full = full0 + 8 * slot;
                     if (misc[0]) {
                         stop = true;  // another thread gave up: issue nothing more
-                    } else if (i >= static_cast<uint32_t>(NS) &&
-                        !mbar_wait_bounded(empty0 + 8 * slot, ((i / NS) - 1) & 1, misc,
+                    } else if (wr > 0 &&
+                        !mbar_wait_bounded(empty0 + 8 * slot, (wr - 1) & 1, misc,
                                            p.wait_cycles)) {
                         misc[0] = 1;
                         flag_error(p.err, QDEC_FLAG_TIMEOUT);

@@ -417,15 +417,6 @@ __device__ __forceinline__ void tma_load_plane8(uint32_t dst, const CUtensorMap 
         : "memory");
 }
 
-// 2^x by the hardware's approximation (one instruction; relative error
-// about 2^-22, far below the 16-bit rounding of the weights it feeds;
-// 2^-inf = 0).
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // Offset of 16-byte chunk c of row r in a [rows][128 bytes] 128-byte
 // swizzled block starting on a 1024-byte boundary.
 __device__ __forceinline__ uint32_t sw128_off(int r, int c) {

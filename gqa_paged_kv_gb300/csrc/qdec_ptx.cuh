@@ -10,6 +10,24 @@ namespace qdec {
 static __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// 2^x by the hardware's approximation (one instruction; relative error
+// about 2^-22, far below the 16-bit rounding of the weights it feeds;
+// 2^-inf = 0; results below 2^-126 flush to zero).
+static __device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// The four E4M3 codes of `four_codes` (byte i = code i) as two f16 pairs:
+// lo = codes 0, 1 and hi = codes 2, 3 (the lower code in the lower half);
+// two conversion instructions on the word's halves, exact.
+static __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_codes, uint32_t &lo,
+                                                        uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four_codes));
+}
 // Two E4M3 codes (the low 16 bits of `two_codes`, the low byte first) as an
 // f16 pair (low byte -> low half): one conversion instruction; exact, since
 // every E4M3 value is an f16 value (NaN stays NaN).
