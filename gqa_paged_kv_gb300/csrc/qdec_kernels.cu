@@ -1266,33 +1266,59 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kCluster, kFp8))
     if (warp == kConsumerWarps) {
         // ------------------------------------------------ TMA producer --
         // 32 tiles at a time: every lane looks up one tile's page, lane 0
-        // issues the copies in order as ring slots come free.  In decode
-        // mode the previous kernel may have written the pages' new slots.
+        // issues the copies in order as ring slots come free.  Over an FP8
+        // pool the page ids are looked up two groups ahead and their scales
+        // one group ahead, so no global load of the lookup stalls the
+        // copies.  In decode mode the previous kernel may have written the
+        // pages' new slots.
         if (kMode == kAttnDecode && p.pdl) grid_dependency_wait();
         const long long ntiles = kCluster ? pg_hi - pg_lo : hi - lo;
         uint32_t i = 0;
         int next_slot = 0;   // i % NS
         uint32_t wraps = 0;  // i / NS
         bool stop = false;
+        // lane's tile `base + lane`: its page (-1 if none or out of range) and head
+        auto page_of = [&](long long base, int &g) {
+            g = cg;
+            if (base + lane >= ntiles) return -1;
+            int b, pg;
+            if (kCluster) {
+                b = cb;
+                pg = pg_lo + static_cast<int>(base) + lane;
+            } else {
+                tile_coords(pre, p.B, p.Hkv, lo + base + lane, b, g, pg);
+            }
+            if (!in_bounds(p, b >= 0 && b < p.B && pg >= 0 && pg < p.max_blocks && g >= 0 &&
+                                  g < p.Hkv))
+                return -1;
+            return p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg];
+        };
+        auto scales_of = [&](int page, int g, float &sk, float &sv) {
+            sk = sv = 0.f;
+            if (kFp8 && page >= 0 && page < p.num_pages) {
+                const int64_t si = static_cast<int64_t>(page) * 2 * p.Hkv + g;
+                sk = p.kv_scale[si];
+                sv = p.kv_scale[si + p.Hkv];
+            }
+        };
+        int g_c = cg, g_n = cg, page_c = -1, page_n = -1;
+        float sck = 0.f, scv = 0.f;  // FP8: the current group's K and V scale
+        if constexpr (kFp8) {
+            page_c = page_of(0, g_c);
+            page_n = page_of(32, g_n);
+            scales_of(page_c, g_c, sck, scv);
+        }
         for (long long base = 0; base < ntiles && !stop; base += 32) {
-            int page = -1, g = cg;
-            float sck = 0.f, scv = 0.f;  // FP8: the tile's K and V scale
-            if (base + lane < ntiles) {
-                int b, pg;
-                if (kCluster) {
-                    b = cb;
-                    pg = pg_lo + static_cast<int>(base) + lane;
-                } else {
-                    tile_coords(pre, p.B, p.Hkv, lo + base + lane, b, g, pg);
-                }
-                if (in_bounds(p, b >= 0 && b < p.B && pg >= 0 && pg < p.max_blocks && g >= 0 &&
-                                     g < p.Hkv))
-                    page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + pg];
-                if (kFp8 && page >= 0 && page < p.num_pages) {
-                    const int64_t si = static_cast<int64_t>(page) * 2 * p.Hkv + g;
-                    sck = p.kv_scale[si];
-                    scv = p.kv_scale[si + p.Hkv];
-                }
+            // bf16 pool: the group's pages looked up in place (the lookahead
+            // measured slower there)
+            int g = g_c, g_n2 = cg, page_n2 = -1;
+            float sck_n = 0.f, scv_n = 0.f;
+            int page = page_c;
+            if constexpr (kFp8) {
+                page_n2 = page_of(base + 64, g_n2);
+                scales_of(page_n, g_n, sck_n, scv_n);
+            } else {
+                page = page_of(base, g);
             }
             const int cnt = static_cast<int>(min(32ll, ntiles - base));
             for (int j = 0; j < cnt; ++j, ++i) {
@@ -1343,6 +1369,14 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm(kCluster, kFp8))
                 }
                 stop = __shfl_sync(kFull, stop, 0);
                 if (stop) break;
+            }
+            if constexpr (kFp8) {
+                page_c = page_n;
+                g_c = g_n;
+                sck = sck_n;
+                scv = scv_n;
+                page_n = page_n2;
+                g_n = g_n2;
             }
         }
         if (lane == 0) misc[2] = static_cast<int>(i);
