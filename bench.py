@@ -77,25 +77,26 @@ TRAFFIC = {
     # the attention kernel (workload 5 over bf16: the decode-mode kernel of the
     # two-launch step)
     "b8-ctx256to384-36layer":
-        {"kernel_sha": "e297049875109362", "bytes_per_launch": 10896197},
+        {"kernel_sha": "73aea732eca75c00", "bytes_per_launch": 10899452},
     "b16-ctx256to384-chanscale-36layer":
-        {"kernel_sha": "e297049875109362", "bytes_per_launch": 21779787},
+        {"kernel_sha": "73aea732eca75c00", "bytes_per_launch": 21779602},
     "b1-ctx8192-spikes-36layer":
-        {"kernel_sha": "e297049875109362", "bytes_per_launch": 33636040},
+        {"kernel_sha": "73aea732eca75c00", "bytes_per_launch": 33636209},
     "b64-ragged128to16384-sharedpool-36layer":
-        {"kernel_sha": "e297049875109362", "bytes_per_launch": 1038141551},
+        {"kernel_sha": "73aea732eca75c00", "bytes_per_launch": 1038110797},
     "b64-ragged128to16384-sharedpool-36layer-fp8kv":
-        {"kernel_sha": "e297049875109362", "bytes_per_launch": 524804043},
-    # --prefill 2048: the causal prefill attention kernel
+        {"kernel_sha": "73aea732eca75c00", "bytes_per_launch": 524673314},
+    # --prefill 2048: the causal prefill attention kernel (over an FP8 pool the
+    # kernel that reads the dequantized workspace)
     "prefill-b1-prompt2048-36layer":
-        {"kernel_sha": "b82e7ddbde5ad841", "bytes_per_launch": 42006848},
+        {"kernel_sha": "114528391bb37fc1", "bytes_per_launch": 42007749},
     "prefill-b1-prompt2048-36layer-fp8kv":
-        {"kernel_sha": "b82e7ddbde5ad841", "bytes_per_launch": 37839509},
+        {"kernel_sha": "114528391bb37fc1", "bytes_per_launch": 42010114},
     # --qkv: the projection kernel
     "b8-ctx256to384-36layer-qkv2560":
-        {"kernel_sha": "bd321992338b6b31", "bytes_per_launch": 31553536},
+        {"kernel_sha": "d083545efb834ee5", "bytes_per_launch": 31553438},
     "b64-ragged128to16384-sharedpool-36layer-qkv2560":
-        {"kernel_sha": "bd321992338b6b31", "bytes_per_launch": 31908314},
+        {"kernel_sha": "d083545efb834ee5", "bytes_per_launch": 31908697},
 }
 
 # The CPU timings sample the first few layers of a workload (same shapes and
@@ -1302,9 +1303,10 @@ def run_prefill(args, dist: Dist):
     st, flags = qdec.qdec_check_error(err, stream)
     assert st == 0, f"device error flags {flags:#x}"
 
-    tr = TRAFFIC.get(name)
+    tr = TRAFFIC.get(name)   # over an FP8 pool: counters of the workspace form
     traffic = (tr["bytes_per_launch"]
-               if tr and tr["kernel_sha"] == kernel_sha("prefill_attention_tc_kernel") else None)
+               if tr and tr["kernel_sha"] == kernel_sha("prefill_attention_tc_kernel")
+               and widen == fp8 else None)
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
