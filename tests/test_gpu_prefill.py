@@ -414,14 +414,17 @@ def test_prefill_fp8_chunk_of_one_equals_fp8_decode():
 
 # ------------------------------------------------------------ full size --
 
-@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("kv", ["bf16", "fp8", "fp8-workspace"])
 def test_prefill_full_prompt_sampled(kv):
     """The benchmark's size: one fresh 2048-token prompt in one chunk, run as
-    the benchmark runs it.  The oracle appends on its own copy of the pool
+    the benchmark runs it (over an FP8 pool both forms; the benchmark times
+    the workspace form).  The oracle appends on its own copy of the pool
     (taken before the GPU runs) and gives q_rot for every row; the attention
     is compared on sampled rows: row r's causal attention is the (pinned)
     decode attention of the oracle's q_rot[r] over the first r + 1 tokens of
     the oracle-appended pool."""
+    widen = kv == "fp8-workspace"
+    kv = "fp8" if widen else kv
     P = 2048
     rows = np.array([0, 1, 15, 16, 17, 255, 1000, 1023, 1024, 2046, 2047])
     if kv == "fp8":
@@ -437,7 +440,7 @@ def test_prefill_full_prompt_sampled(kv):
            wl.bf16_bits(c.w_k), c.positions.cpu().numpy(), qo, L, bt)
     if kv == "fp8":
         ref = oracle.prefill_append_fp8(*ins, pool, sc_h, 1e6, float(np.float32(1e-6)))
-        q_rot, out, err = _run_fp8(c, codes, sc, 1)
+        q_rot, out, err = _run_fp8(c, codes, sc, 1, widen)
     else:
         ref = oracle.prefill_append(*ins, pool, 1e6, float(np.float32(1e-6)))
         q_rot, out, err = _run(c, 1)
