@@ -983,7 +983,9 @@ def run_ours(args, dist: Dist):
     cfg = workload_config(w, args, dist.world, l2)
     if step_launches == 2:
         cfg["launch"] += (" (qdec_step runs as two launches here: the new-token kernel, then the "
-                          "decode-mode attention as its programmatic dependent)")
+                          "decode-mode attention as its programmatic dependent"
+                          + ("; over an FP8 pool the new-token kernel starts after the previous "
+                             "layer's attention has finished)" if w.kv == "fp8" else ")"))
     if args.plan_bound:
         cfg["plan"] = (f"planned for contexts up to {args.plan_bound} tokens (block-table rows "
                        f"of {layers.shape.max_blocks_per_seq} pages)")

@@ -234,15 +234,15 @@ int attention_grid(const qdec_shape *s) {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// qdec_step over a bf16 pool on the flat layout (many segments: each CTA
-// walks several) runs as two launches, the new-token kernel and then the
-// attention in decode mode as its programmatic dependent: there the fused
-// kernel's per-piece new-token work holds the consumer warps of a CTA while
-// its ring fills, which costs more than the extra launch (measured on 64
-// ragged sequences: 182.9 -> 172.6 us per layer-step).  On the cluster
-// layout (one piece per CTA, latency-bound) the single launch is faster.
+// qdec_step on the flat layout (many segments: each CTA walks several) runs
+// as two launches, the new-token kernel and then the attention in decode
+// mode as its programmatic dependent: there the fused kernel's per-piece
+// new-token work holds the consumer warps of a CTA while its ring fills,
+// which costs more than the extra launch (measured on 64 ragged sequences:
+// bf16 pool 182.9 -> 172.6 us per layer-step).  On the cluster layout (one
+// piece per CTA, latency-bound) the single launch is faster.
 bool step_in_two_launches(const qdec_shape *s, bool fp8) {
-    return !fp8 && plan_for(s, true, false).cluster == 0;
+    return plan_for(s, true, fp8).cluster == 0;
 }
 
 struct WorkspaceLayout {
@@ -262,8 +262,9 @@ WorkspaceLayout workspace_layout(const qdec_shape *s) {
     l.o = l.lse + round256(pieces * qdec::kGroup * sizeof(float));
     l.o_end = l.o + pieces * qdec::kGroup * qdec::kHeadDim * sizeof(float);
     l.qrot = round256(l.o_end);
-    l.total = l.qrot + (step_in_two_launches(s, false)
-                            ? static_cast<size_t>(s->batch) * s->num_q_heads * qdec::kHeadDim *
+    const bool two = step_in_two_launches(s, false) ||
+                     (fp8_supported(s) && step_in_two_launches(s, true));
+    l.total = l.qrot + (two ? static_cast<size_t>(s->batch) * s->num_q_heads * qdec::kHeadDim *
                                   sizeof(float)
                             : 0);
     return l;
@@ -593,12 +594,17 @@ qdec_status step_impl(const qdec_shape *shape, const qdec_bf16 *q, int64_t q_str
                                                  workspace_layout(shape).qrot);
         Params pa = p;
         pa.q_rot_out = q_rot;
-        cudaError_t e = qdec::launch_append_rope(pa, false, s);
+        // over an FP8 pool the new-token kernel starts only once the kernel
+        // before it is done: launched early, its CTAs slowed the previous
+        // layer's attention (64 ragged sequences: 220.8 against 131.0 us per
+        // layer-step)
+        if (pool.fp8) pa.pdl = 0;
+        cudaError_t e = qdec::launch_append_rope(pa, pool.fp8, s);
         if (e != cudaSuccess) return cuda_status(e);
         Params pd = p;
         pd.q_rot_in = q_rot;
         pd.pdl = 1;
-        return cuda_status(qdec::launch_attention(pd, map, qdec::kAttnDecode, false, s));
+        return cuda_status(qdec::launch_attention(pd, map, qdec::kAttnDecode, pool.fp8, s));
     }
     return cuda_status(qdec::launch_attention(p, map, qdec::kAttnFused, pool.fp8, s));
 }

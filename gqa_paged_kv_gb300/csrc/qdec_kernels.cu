@@ -490,27 +490,17 @@ __device__ __forceinline__ bool new_token_in_bounds(const Params &p, int b, int 
                             (L - 1) / kPageSize < p.max_blocks);
 }
 
-// The new-token query rows of (sequence b, KV head g), on the 128 consumer
-// threads: warp w norms and rotates query row 4g + w in fp32.  Lane l holds
-// dims 2l, 2l+1, 64+2l, 65+2l: both members of two rotate-half pairs.  With
-// need_k, warp 0 then also produces and appends the key/value row.
-//
-// Q_OUT = 0: scaled hi/lo operand rows into shared memory (qb), bf16 (or
-// f16 for an FP8 pool, whose tiles are multiplied in f16);
+// Query row w of the group (head 4g + w) of sequence b, on one warp: normed
+// and rotated in fp32 with the angles `rope` (the sequence's 64 entries).
+// Lane l holds dims 2l, 2l+1, 64+2l, 65+2l: both members of two rotate-half
+// pairs.
+// Q_OUT = 0: scaled operand rows into shared memory (bf16 hi/lo rows over a
+// bf16 pool, four E4M3 terms over an FP8 pool);
 // Q_OUT = 1: fp32 rows to p.q_rot_out (unscaled).
 template <int Q_OUT, bool kFp8>
-__device__ void new_token_rows(const Params &p, int b, int g, int L, bool need_k, uint8_t *sm) {
-    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
-    if (!new_token_in_bounds(p, b, g, L)) return;  // uniform over the CTA
-    const RopeEntry *rope;
-    if (p.rope) {
-        rope = p.rope + static_cast<int64_t>(b) * kRotPairs;
-    } else {
-        RopeEntry *rs = reinterpret_cast<RopeEntry *>(sm + kOffRope);
-        if (t < kRotPairs) rs[t] = rope_entry(p.positions[b], p.inv_freq[t], false);
-        consumer_sync();
-        rope = rs;
-    }
+__device__ void new_token_row(const Params &p, int b, int g, int w, const RopeEntry *rope,
+                              uint8_t *sm) {
+    const int lane = threadIdx.x & 31;
     const RopeEntry e0 = rope[2 * lane], e1 = rope[2 * lane + 1];
 
     const int hq = g * kGroup + w;
@@ -553,6 +543,29 @@ __device__ void new_token_rows(const Params &p, int b, int g, int L, bool need_k
         reinterpret_cast<float2 *>(dst)[lane] = make_float2(y0, y1);
         reinterpret_cast<float2 *>(dst + 64)[lane] = make_float2(y2, y3);
     }
+}
+
+// The sequence's angles: from the step's table, or computed into shared
+// memory by the first kRotPairs of `nthreads` threads that then meet on
+// named barrier `bar`.
+__device__ __forceinline__ const RopeEntry *rope_of(const Params &p, int b, uint8_t *sm, int bar,
+                                                    int nthreads) {
+    if (p.rope) return p.rope + static_cast<int64_t>(b) * kRotPairs;
+    RopeEntry *rs = reinterpret_cast<RopeEntry *>(sm + kOffRope);
+    if (threadIdx.x < kRotPairs) rs[threadIdx.x] = rope_entry(p.positions[b], p.inv_freq[threadIdx.x], false);
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nthreads) : "memory");
+    return rs;
+}
+
+// The new-token query rows of (sequence b, KV head g), on the 128 consumer
+// threads: warp w takes query row 4g + w.  With need_k, warp 0 then also
+// produces and appends the key/value row.
+template <int Q_OUT, bool kFp8>
+__device__ void new_token_rows(const Params &p, int b, int g, int L, bool need_k, uint8_t *sm) {
+    const int w = threadIdx.x >> 5;
+    if (!new_token_in_bounds(p, b, g, L)) return;  // uniform over the CTA
+    const RopeEntry *rope = rope_of(p, b, sm, 1, kConsumerWarps * 32);  // the consumer barrier
+    new_token_row<Q_OUT, kFp8>(p, b, g, w, rope, sm);
     if (need_k && w == 0) key_value_row<kFp8>(p, b, g, L, sm, load_kv_inputs(p, b, g, L));
 }
 
@@ -1527,12 +1540,15 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const __gri
         return;
     }
     if (p.pdl) grid_dependency_wait();
-    if (threadIdx.x >= kGroup * 32) {
+    const int warp = threadIdx.x >> 5;
+    if (warp >= kGroup) {
         if (new_token_in_bounds(p, b, g, L))
             key_value_row<kFp8>(p, b, g, L, sm, load_kv_inputs(p, b, g, L));
         return;
     }
-    new_token_rows<1, kFp8>(p, b, g, L, false, sm);
+    if (!new_token_in_bounds(p, b, g, L)) return;  // uniform over the CTA
+    const RopeEntry *rope = rope_of(p, b, sm, 2, kGroup * 32);
+    new_token_row<1, kFp8>(p, b, g, warp, rope, sm);
 }
 
 // ----------------------------------------------------------- merge kernel --

@@ -218,16 +218,18 @@ qdec_status qdec_attn_decode(const qdec_shape *shape, const float *q_rot,
                              int32_t *err_flag, void *stream);
 
 /* The whole layer-step (steps 1-4).  In ONE kernel launch where the work
- * plan is the cluster layout (few (sequence, KV head) segments) or the pool
- * is FP8: every CTA norms and rotates the four query rows of the (sequence,
- * KV head) it works on, the CTA that holds the last page of a (sequence, KV
- * head) also norms, rotates and appends the new key/value, and the last CTA
- * to finish a split (sequence, KV head) merges its pieces.  Over a bf16 pool
- * on the flat layout (many segments, each CTA walking several) in TWO: the
- * kernel of qdec_append_rope (q_rot kept in the workspace), then the
- * attention of qdec_attn_decode as its programmatic dependent -- there the
- * per-segment new-token work inside the attention kernel costs more than
- * the second launch.  qdec_step_launches tells which.  Either way the grid
+ * plan is the cluster layout (few (sequence, KV head) segments): every CTA
+ * norms and rotates the four query rows of the (sequence, KV head) it works
+ * on, the CTA that holds the last page of a (sequence, KV head) also norms,
+ * rotates and appends the new key/value, and the last CTA to finish a split
+ * (sequence, KV head) merges its pieces.  On the flat layout (many
+ * segments, each CTA walking several) in TWO: the kernel of
+ * qdec_append_rope (q_rot kept in the workspace), then the attention of
+ * qdec_attn_decode as its programmatic dependent -- there the per-segment
+ * new-token work inside the attention kernel costs more than the second
+ * launch.  (Over an FP8 pool the first of the two is never launched as a
+ * programmatic dependent, whatever the flags: started early, its CTAs slowed
+ * the previous attention.)  qdec_step_launches tells which.  Either way the grid
  * depends on the shape only (one captured graph serves every length).  Same
  * arguments as qdec_append_rope plus the workspace and `out`; no q_rot
  * buffer is needed.  The workspace counters must be zero on entry
@@ -424,9 +426,10 @@ qdec_status qdec_qkv_append_rope_fp8(const qdec_shape *shape, int32_t hidden,
                                      uint8_t *kv_pool_fp8, const float *kv_scale, float *q_rot,
                                      int32_t *err_flag, void *stream);
 
-/* qdec_step over an FP8 pool: one launch for steps 1-4, the new key and
- * value quantized into their slot as above.  Same launch flags, workspace
- * and error reporting as qdec_step. */
+/* qdec_step over an FP8 pool: steps 1-4, the new key and value quantized
+ * into their slot as above; one or two launches by the same rule as
+ * qdec_step (qdec_step_launches with fp8_pool != 0 tells which).  Same
+ * launch flags, workspace and error reporting as qdec_step. */
 qdec_status qdec_step_fp8(const qdec_shape *shape,
                           const qdec_bf16 *q, int64_t q_stride,
                           const qdec_bf16 *k, int64_t k_stride,

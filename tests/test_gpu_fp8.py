@@ -75,6 +75,30 @@ def test_append_then_decode_fp8(lens, num_ctas):
     assert torch.count_nonzero(r.ws[:4 * n].view(torch.int32)).item() == 0
 
 
+@pytest.mark.parametrize("lens,num_ctas", [([5, 300, 17, 1000, 64, 3], 7),
+                                           ([200 + 37 * i for i in range(30)], 0)],
+                         ids=["forced_grid", "30_sequences"])
+def test_two_launch_step_is_append_then_decode_fp8(lens, num_ctas):
+    """Where qdec_step_fp8 runs as two launches (the flat layout: a forced
+    grid, or 30 sequences = 240 segments) it is qdec_append_rope_fp8
+    followed by qdec_attn_decode_fp8: the same bits, and the oracle's
+    result."""
+    q = parity.qdec()
+    wa, wb = _small(lens, seed=46), _small(lens, seed=46)
+    ra = parity.Runner(wa, num_ctas=num_ctas)
+    rb = parity.Runner(wb, num_ctas=num_ctas)
+    assert q.qdec_step_launches(ra.shape, fp8_pool=True) == 2
+    ref = parity.run_oracle(wl.oracle_inputs(wa, 0))
+    ra.step(0)
+    rb.two_calls(0)
+    ra.check_flags()
+    rb.check_flags()
+    assert torch.equal(ra.out[0].view(torch.int16), rb.out[0].view(torch.int16))
+    assert torch.equal(wa.pool8(0), wb.pool8(0))
+    parity.assert_out_close(ra.out[0], ref["out"])
+    parity.assert_slots_fp8(wa, 0, range(len(lens)), ref)
+
+
 def test_decode_overlapped_layers_match_serial_fp8():
     spec = wl.custom(5, [17, 1, 300, 64, 1000], pool_pages=120, layers=4, seed=45)
     w = wl.build(spec, "cuda", poison=True, kv="fp8")

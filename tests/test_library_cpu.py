@@ -56,21 +56,22 @@ def test_workspace_bytes_rejects_bad_shapes(q):
 
 
 def test_step_launch_count(q):
-    """qdec_step runs in one launch or, over a bf16 pool on the flat layout,
-    two (the new-token kernel, then the decode-mode attention); its FP8 form
-    always in one; bad shapes give 0.  The two-launch form keeps q_rot in
-    the workspace, so the workspace is at least that large then."""
+    """qdec_step (either pool type) runs in one launch or, on the flat
+    layout, two (the new-token kernel, then the decode-mode attention); bad
+    shapes give 0.  The two-launch form keeps q_rot in the workspace, so the
+    workspace is at least that large then."""
     assert q.qdec_step_launches(_shape(q, batch=0)) == 0
     assert q._lib.qdec_step_launches(None, 0) == 0
     for kw in (dict(), dict(batch=64, num_pages=4096, max_blocks_per_seq=64,
                             max_seq_len=1024), dict(num_ctas=7)):
         sh = _shape(q, **kw)
-        n = q.qdec_step_launches(sh)
-        assert n in (1, 2), kw
-        assert q.qdec_step_launches(sh, fp8_pool=True) == 1
-        if n == 2:
-            assert q.qdec_workspace_bytes(sh) >= sh.batch * sh.num_q_heads * 128 * 4
-    assert q.qdec_step_launches(_shape(q, num_ctas=7)) == 2  # forced grids are flat
+        for fp8 in (False, True):
+            n = q.qdec_step_launches(sh, fp8_pool=fp8)
+            assert n in (1, 2), kw
+            if n == 2:
+                assert q.qdec_workspace_bytes(sh) >= sh.batch * sh.num_q_heads * 128 * 4
+    for fp8 in (False, True):  # forced grids are flat
+        assert q.qdec_step_launches(_shape(q, num_ctas=7), fp8_pool=fp8) == 2
 
 
 def test_entry_points_reject_null_and_misaligned_arguments(q):
