@@ -74,18 +74,18 @@ KERNEL_SOURCES = {
 # profiles/), keyed by workload; used only while the kernel source hash
 # still matches the one the counters were taken on.
 TRAFFIC = {
-    # the attention kernel (workload 5 over bf16: the decode-mode kernel of the
+    # the attention kernel (workload 5: the decode-mode kernel of the
     # two-launch step)
     "b8-ctx256to384-36layer":
-        {"kernel_sha": "73aea732eca75c00", "bytes_per_launch": 10899452},
+        {"kernel_sha": "fec73a2c7746cf7a", "bytes_per_launch": 10899880},
     "b16-ctx256to384-chanscale-36layer":
-        {"kernel_sha": "73aea732eca75c00", "bytes_per_launch": 21779602},
+        {"kernel_sha": "fec73a2c7746cf7a", "bytes_per_launch": 21779612},
     "b1-ctx8192-spikes-36layer":
-        {"kernel_sha": "73aea732eca75c00", "bytes_per_launch": 33636209},
+        {"kernel_sha": "fec73a2c7746cf7a", "bytes_per_launch": 33636451},
     "b64-ragged128to16384-sharedpool-36layer":
-        {"kernel_sha": "73aea732eca75c00", "bytes_per_launch": 1038110797},
+        {"kernel_sha": "fec73a2c7746cf7a", "bytes_per_launch": 1038109092},
     "b64-ragged128to16384-sharedpool-36layer-fp8kv":
-        {"kernel_sha": "73aea732eca75c00", "bytes_per_launch": 524673314},
+        {"kernel_sha": "fec73a2c7746cf7a", "bytes_per_launch": 524977074},
     # --prefill 2048: the causal prefill attention kernel (over an FP8 pool the
     # kernel that reads the dequantized workspace)
     "prefill-b1-prompt2048-36layer":
