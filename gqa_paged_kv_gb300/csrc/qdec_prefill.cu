@@ -119,62 +119,81 @@ __global__ void __launch_bounds__(kPfAppendThreads) prefill_append_kernel(
         return;  // uniform over the CTA
     }
     const int t = L - n + (r - p.qo_indptr[b]);  // token index in the sequence
+    // A warp's inputs, loaded before the angles are ready so that their
+    // latency overlaps the angle computation: the four query rows, the key
+    // row and the value row of KV head g (lane l: dims 2l, 2l+1, 64+2l,
+    // 65+2l; the value as two 4-byte words), and the page of the row's slot.
+    struct RowIn {
+        __nv_bfloat162 q[kGroup][2], k[2];
+        uint32_t v[2];
+        int page;
+    };
+    auto load_in = [&](int g) {
+        RowIn in;
+#pragma unroll
+        for (int j = 0; j < kGroup; ++j) {
+            const __nv_bfloat162 *qr = reinterpret_cast<const __nv_bfloat162 *>(
+                p.q + static_cast<int64_t>(r) * p.q_stride + (g * kGroup + j) * kHeadDim);
+            in.q[j][0] = qr[lane];
+            in.q[j][1] = qr[32 + lane];
+        }
+        const __nv_bfloat162 *kr = reinterpret_cast<const __nv_bfloat162 *>(
+            p.k + static_cast<int64_t>(r) * p.k_stride + g * kHeadDim);
+        in.k[0] = kr[lane];
+        in.k[1] = kr[32 + lane];
+        const uint32_t *vr = reinterpret_cast<const uint32_t *>(
+            p.v + static_cast<int64_t>(r) * p.v_stride + g * kHeadDim);
+        in.v[0] = vr[lane];
+        in.v[1] = vr[32 + lane];
+        in.page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + t / kPageSize];
+        return in;
+    };
+    const __nv_bfloat162 wqa = reinterpret_cast<const __nv_bfloat162 *>(p.w_q)[lane];
+    const __nv_bfloat162 wqc = reinterpret_cast<const __nv_bfloat162 *>(p.w_q + 64)[lane];
+    const __nv_bfloat162 wka = reinterpret_cast<const __nv_bfloat162 *>(p.w_k)[lane];
+    const __nv_bfloat162 wkc = reinterpret_cast<const __nv_bfloat162 *>(p.w_k + 64)[lane];
+    RowIn in{};
+    if (warp < p.Hkv) in = load_in(warp);
     if (threadIdx.x < kRotPairs)  // angle i: positions[r] * theta^(-2i/D)
         rs[threadIdx.x] = ff_sincos(static_cast<double>(p.positions[r]) * p.inv_freq[threadIdx.x]);
     __syncthreads();
     // this lane's rotate-half pairs i = 2 lane, 2 lane + 1: dims i and i + 64
     const RopeEntry e0 = rs[2 * lane], e1 = rs[2 * lane + 1];
     const float fc0 = e0.c_hi, fc1 = e1.c_hi, fs0 = e0.s_hi, fs1 = e1.s_hi;
-    // RMSNorm (eps inside the root) of one 128-dim row; x w is exact in fp32
-    // (a product of two bf16).  Returns the root; n holds x w for dims
-    // 2 lane, 2 lane + 1, 64 + 2 lane, 64 + 2 lane + 1.
-    auto norm = [&](const __nv_bfloat16 *x, const __nv_bfloat16 *w, float (&nv)[4]) {
-        const float2 a = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(x)[lane]);
-        const float2 c = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(x + 64)[lane]);
-        const float ss = warp_sum(a.x * a.x + a.y * a.y + c.x * c.x + c.y * c.y);
-        const float2 wa = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(w)[lane]);
-        const float2 wc = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(w + 64)[lane]);
-        nv[0] = a.x * wa.x;
-        nv[1] = a.y * wa.y;
-        nv[2] = c.x * wc.x;
-        nv[3] = c.y * wc.y;
-        return rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
-    };
+    const float2 wa = __bfloat1622float2(wqa), wc = __bfloat1622float2(wqc);
     for (int g = warp; g < p.Hkv; g += kPfAppendThreads / 32) {
+        if (g != warp) in = load_in(g);
 #pragma unroll
-        for (int j = 0; j < kGroup; ++j) {  // unrolled: the four rows' loads overlap
-            const int h = g * kGroup + j;
-            float nv[4];
-            const float rn = norm(p.q + static_cast<int64_t>(r) * p.q_stride + h * kHeadDim,
-                                  p.w_q, nv);
-            const float n1a = nv[0] * rn, n1b = nv[1] * rn, n2a = nv[2] * rn, n2b = nv[3] * rn;
-            float *dst = p.q_rot_out + (static_cast<int64_t>(r) * p.Hq + h) * kHeadDim;
+        for (int j = 0; j < kGroup; ++j) {
+            // RMSNorm (eps inside the root; x w exact in fp32, a product of
+            // two bf16), then the rotation
+            const float2 a = __bfloat1622float2(in.q[j][0]);
+            const float2 c = __bfloat1622float2(in.q[j][1]);
+            const float ss = warp_sum(a.x * a.x + a.y * a.y + c.x * c.x + c.y * c.y);
+            const float rn = rsqrtf(ss * (1.0f / kHeadDim) + p.eps);
+            const float n1a = a.x * wa.x * rn, n1b = a.y * wa.y * rn;
+            const float n2a = c.x * wc.x * rn, n2b = c.y * wc.y * rn;
+            float *dst = p.q_rot_out + (static_cast<int64_t>(r) * p.Hq + g * kGroup + j) * kHeadDim;
             reinterpret_cast<float2 *>(dst)[lane] =
                 make_float2(n1a * fc0 - n2a * fs0, n1b * fc1 - n2b * fs1);
             reinterpret_cast<float2 *>(dst + 64)[lane] =
                 make_float2(n2a * fc0 + n1a * fs0, n2b * fc1 + n1b * fs1);
         }
-        const int page = p.block_table[static_cast<int64_t>(b) * p.max_blocks + t / kPageSize];
+        const int page = in.page;
         if (page < 0 || page >= p.num_pages) {
             if (lane == 0) flag_error(p.err, QDEC_FLAG_BAD_PAGE);
             continue;
         }
         const int64_t slot =
             ((static_cast<int64_t>(page) * 2 * p.Hkv + g) * kPageSize + t % kPageSize) * kHeadDim;
-        // the key: norm and rotation in float-float, one rounding to bf16
-        const __nv_bfloat16 *krow = p.k + static_cast<int64_t>(r) * p.k_stride + g * kHeadDim;
+        // the key: norm and rotation rounded once to bf16 (exactly)
         __nv_bfloat16 kb[4];
-        key_row(p.eps, reinterpret_cast<const __nv_bfloat162 *>(krow)[lane],
-                reinterpret_cast<const __nv_bfloat162 *>(krow + 64)[lane],
-                reinterpret_cast<const __nv_bfloat162 *>(p.w_k)[lane],
-                reinterpret_cast<const __nv_bfloat162 *>(p.w_k + 64)[lane], e0, e1, kb);
+        key_row(p.eps, in.k[0], in.k[1], wka, wkc, e0, e1, kb);
         const uint32_t k01 = static_cast<uint32_t>(__bfloat16_as_ushort(kb[0])) |
                              (static_cast<uint32_t>(__bfloat16_as_ushort(kb[1])) << 16);
         const uint32_t k23 = static_cast<uint32_t>(__bfloat16_as_ushort(kb[2])) |
                              (static_cast<uint32_t>(__bfloat16_as_ushort(kb[3])) << 16);
-        const uint32_t *vs = reinterpret_cast<const uint32_t *>(
-            p.v + static_cast<int64_t>(r) * p.v_stride + g * kHeadDim);
-        const uint32_t v01 = vs[lane], v23 = vs[32 + lane];
+        const uint32_t v01 = in.v[0], v23 = in.v[1];
         const int64_t vslot = slot + static_cast<int64_t>(p.Hkv) * kPageSize * kHeadDim;
         if constexpr (kFp8) {
             // the bf16 rows the bf16 pool would hold, divided by the scales
@@ -198,7 +217,6 @@ __global__ void __launch_bounds__(kPfAppendThreads) prefill_append_kernel(
         }
     }
 }
-
 
 // ------------------------------------------------------- FP8 widening --
 // The E4M3 pages of every well-formed chunk's sequence dequantised once into
