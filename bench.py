@@ -1053,15 +1053,17 @@ def prefill_flops(seq_lens, chunks, Hq=32, D=128) -> int:
 def prefill_config(P: int, L: int, fp8: bool, widen: bool = True) -> dict:
     """The `config` object of a --prefill line (the same for both arms)."""
     if not fp8:
-        launch = (f"CUDA graph: {L} x (qdec_prefill_append_rope, qdec_prefill_attn), the "
-                  "attention a programmatic dependent of the append")
+        launch = (f"CUDA graph: qdec_prefill_rope_table, then {L} x (qdec_prefill_append_rope, "
+                  "qdec_prefill_attn), the attention a programmatic dependent of the append")
     elif widen:
-        launch = (f"CUDA graph: {L} x (qdec_prefill_append_rope_fp8, qdec_prefill_attn_fp8 "
-                  "with a workspace: the pages dequantized to bf16 once, then the attention "
-                  "as a programmatic dependent of that pass)")
+        launch = (f"CUDA graph: qdec_prefill_rope_table, then {L} x "
+                  "(qdec_prefill_append_rope_fp8, qdec_prefill_attn_fp8 with a workspace: the "
+                  "pages dequantized to bf16 once, then the attention as a programmatic "
+                  "dependent of that pass)")
     else:
-        launch = (f"CUDA graph: {L} x (qdec_prefill_append_rope_fp8, qdec_prefill_attn_fp8 "
-                  "without a workspace: the codes converted inside the attention kernel)")
+        launch = (f"CUDA graph: qdec_prefill_rope_table, then {L} x "
+                  "(qdec_prefill_append_rope_fp8, qdec_prefill_attn_fp8 without a workspace: "
+                  "the codes converted inside the attention kernel)")
     return {"workload": f"prefill-b1-prompt{P}-{L}layer" + ("-fp8kv" if fp8 else ""),
             "batch": 1, "prompt": P, "layers": L, "heads": "32 q / 8 kv, head_dim 128, page 16",
             "launch": launch,
@@ -1165,22 +1167,28 @@ def run_prefill(args, dist: Dist):
     ws8 = (torch.empty(qdec.qdec_prefill_fp8_workspace_bytes(shape), dtype=torch.uint8,
                        device="cuda") if widen else None)
 
+    # the chunk rows' RoPE angles, once per step for all layers (the same
+    # positions in every layer)
+    rope = qdec.alloc_prefill_rope_table(P)
+
     def step_fn(ins, outs):
         def fn():
+            qdec.qdec_prefill_rope_table(shape, c0.positions, rope, stream=stream)
             for l, c in enumerate(cases):
                 q, k, v = ins[l]
                 if fp8:
                     codes, sc = pools8[l]
                     qdec.qdec_prefill_append_rope_fp8(shape, q, k, v, c.w_q, c.w_k, c.positions,
                                                       c.qo_indptr, c.seq_lens, c.block_table,
-                                                      codes, sc, q_rot, err, stream=stream)
+                                                      codes, sc, q_rot, err, stream=stream,
+                                                      rope_table=rope)
                     qdec.qdec_prefill_attn_fp8(shape, q_rot, c.qo_indptr, c.seq_lens,
                                                c.block_table, codes, sc, outs[l], err,
                                                stream=stream, workspace=ws8)
                     continue
                 qdec.qdec_prefill_append_rope(shape, q, k, v, c.w_q, c.w_k, c.positions,
                                               c.qo_indptr, c.seq_lens, c.block_table, c.pool,
-                                              q_rot, err, stream=stream)
+                                              q_rot, err, stream=stream, rope_table=rope)
                 qdec.qdec_prefill_attn(shape, q_rot, c.qo_indptr, c.seq_lens, c.block_table,
                                        c.pool, outs[l], err, stream=stream)
         return fn
@@ -1359,7 +1367,7 @@ def run_prefill(args, dist: Dist):
                          "flops_per_launch": flops_layer},
             "e2e": {"value": e2e_value and round(e2e_value, 3), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k_e2e},
-            "gpu_launches": (3 if widen else 2) * L * args.steps,
+            "gpu_launches": ((3 if widen else 2) * L + 1) * args.steps,
             "clocks": ck,
             "cpu_baseline": cpu,
         }

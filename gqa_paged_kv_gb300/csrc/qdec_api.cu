@@ -638,18 +638,21 @@ qdec_status prefill_append_impl(const qdec_shape *shape, int32_t num_tokens, con
                                 int64_t q_stride, const qdec_bf16 *k, int64_t k_stride,
                                 const qdec_bf16 *v, int64_t v_stride, const qdec_bf16 *q_norm_w,
                                 const qdec_bf16 *k_norm_w, const int32_t *positions,
-                                const int32_t *qo_indptr, const int32_t *seq_lens,
-                                const int32_t *block_table, const PoolArg &pool, float *q_rot,
-                                int32_t *err_flag, void *stream) {
+                                const void *rope_table, const int32_t *qo_indptr,
+                                const int32_t *seq_lens, const int32_t *block_table,
+                                const PoolArg &pool, float *q_rot, int32_t *err_flag,
+                                void *stream) {
     qdec_status st = check_new_token_args(shape, q, q_stride, k, k_stride, v, v_stride, q_norm_w,
                                           k_norm_w, positions, seq_lens, block_table);
     if (st != QDEC_OK) return st;
     if ((st = check_pool(shape, pool)) != QDEC_OK) return st;
     if (num_tokens < 0 || !qo_indptr || !q_rot || !aligned16(q_rot)) return QDEC_ERR_INVALID_ARG;
+    if (rope_table && !aligned16(rope_table)) return QDEC_ERR_INVALID_ARG;
     Params p{};
     fill_common(p, shape, false, pool.fp8);
+    // the table's rows are the chunk rows (r), not the sequences
     bind_new_token(p, q, q_stride, k, k_stride, v, v_stride, q_norm_w, k_norm_w, positions,
-                   seq_lens, block_table, nullptr);
+                   seq_lens, block_table, rope_table);
     bind_pool(p, pool);
     p.qo_indptr = qo_indptr;
     p.T = num_tokens;
@@ -771,6 +774,26 @@ qdec_status qdec_rope_table(const qdec_shape *shape, const int32_t *positions, v
     return cuda_status(qdec::launch_rope_table(p, static_cast<cudaStream_t>(stream)));
 }
 
+size_t qdec_prefill_rope_table_bytes(int32_t num_tokens) {
+    return num_tokens > 0 ? static_cast<size_t>(num_tokens) * qdec::kRotPairs * sizeof(qdec::RopeEntry)
+                          : 0;
+}
+
+qdec_status qdec_prefill_rope_table(const qdec_shape *shape, int32_t num_tokens,
+                                    const int32_t *positions, void *rope_table, void *stream) {
+    qdec_status st = check_shape(shape);
+    if (st != QDEC_OK) return st;
+    if (num_tokens < 0 || !positions || !rope_table || !aligned16(rope_table))
+        return QDEC_ERR_INVALID_ARG;
+    if (num_tokens == 0) return QDEC_OK;
+    Params p{};
+    fill_common(p, shape, false);
+    p.B = num_tokens;  // one table row per chunk row
+    p.positions = positions;
+    p.rope_out = static_cast<qdec::RopeEntry *>(rope_table);
+    return cuda_status(qdec::launch_rope_table(p, static_cast<cudaStream_t>(stream)));
+}
+
 int qdec_step_launches(const qdec_shape *shape, int fp8_pool) {
     if (check_shape(shape) != QDEC_OK) return 0;
     return step_in_two_launches(shape, fp8_pool != 0) ? 2 : 1;
@@ -853,12 +876,12 @@ qdec_status qdec_prefill_append_rope(const qdec_shape *shape, int32_t num_tokens
                                      const qdec_bf16 *q, int64_t q_stride, const qdec_bf16 *k,
                                      int64_t k_stride, const qdec_bf16 *v, int64_t v_stride,
                                      const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
-                                     const int32_t *positions, const int32_t *qo_indptr,
-                                     const int32_t *seq_lens, const int32_t *block_table,
-                                     qdec_bf16 *kv_pool, float *q_rot, int32_t *err_flag,
-                                     void *stream) {
+                                     const int32_t *positions, const void *rope_table,
+                                     const int32_t *qo_indptr, const int32_t *seq_lens,
+                                     const int32_t *block_table, qdec_bf16 *kv_pool, float *q_rot,
+                                     int32_t *err_flag, void *stream) {
     return prefill_append_impl(shape, num_tokens, q, q_stride, k, k_stride, v, v_stride, q_norm_w,
-                               k_norm_w, positions, qo_indptr, seq_lens, block_table,
+                               k_norm_w, positions, rope_table, qo_indptr, seq_lens, block_table,
                                PoolArg{kv_pool, nullptr, false}, q_rot, err_flag, stream);
 }
 
@@ -867,12 +890,13 @@ qdec_status qdec_prefill_append_rope_fp8(const qdec_shape *shape, int32_t num_to
                                          const qdec_bf16 *k, int64_t k_stride,
                                          const qdec_bf16 *v, int64_t v_stride,
                                          const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
-                                         const int32_t *positions, const int32_t *qo_indptr,
-                                         const int32_t *seq_lens, const int32_t *block_table,
-                                         uint8_t *kv_pool_fp8, const float *kv_scale,
-                                         float *q_rot, int32_t *err_flag, void *stream) {
+                                         const int32_t *positions, const void *rope_table,
+                                         const int32_t *qo_indptr, const int32_t *seq_lens,
+                                         const int32_t *block_table, uint8_t *kv_pool_fp8,
+                                         const float *kv_scale, float *q_rot, int32_t *err_flag,
+                                         void *stream) {
     return prefill_append_impl(shape, num_tokens, q, q_stride, k, k_stride, v, v_stride, q_norm_w,
-                               k_norm_w, positions, qo_indptr, seq_lens, block_table,
+                               k_norm_w, positions, rope_table, qo_indptr, seq_lens, block_table,
                                PoolArg{kv_pool_fp8, kv_scale, true}, q_rot, err_flag, stream);
 }
 

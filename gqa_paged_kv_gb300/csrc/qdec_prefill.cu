@@ -154,11 +154,17 @@ __global__ void __launch_bounds__(kPfAppendThreads) prefill_append_kernel(
     const __nv_bfloat162 wkc = reinterpret_cast<const __nv_bfloat162 *>(p.w_k + 64)[lane];
     RowIn in{};
     if (warp < p.Hkv) in = load_in(warp);
-    if (threadIdx.x < kRotPairs)  // angle i: positions[r] * theta^(-2i/D)
-        rs[threadIdx.x] = ff_sincos(static_cast<double>(p.positions[r]) * p.inv_freq[threadIdx.x]);
-    __syncthreads();
-    // this lane's rotate-half pairs i = 2 lane, 2 lane + 1: dims i and i + 64
-    const RopeEntry e0 = rs[2 * lane], e1 = rs[2 * lane + 1];
+    // this lane's rotate-half pairs i = 2 lane, 2 lane + 1: dims i and i + 64;
+    // angle i is positions[r] * theta^(-2i/D), from the step's table (row r)
+    // or computed here once per row
+    const RopeEntry *rope = p.rope + static_cast<int64_t>(r) * kRotPairs;
+    if (!p.rope) {  // uniform over the CTA
+        if (threadIdx.x < kRotPairs)
+            rs[threadIdx.x] = ff_sincos(static_cast<double>(p.positions[r]) * p.inv_freq[threadIdx.x]);
+        __syncthreads();
+        rope = rs;
+    }
+    const RopeEntry e0 = rope[2 * lane], e1 = rope[2 * lane + 1];
     const float fc0 = e0.c_hi, fc1 = e1.c_hi, fs0 = e0.s_hi, fs1 = e1.s_hi;
     const float2 wa = __bfloat1622float2(wqa), wc = __bfloat1622float2(wqc);
     for (int g = warp; g < p.Hkv; g += kPfAppendThreads / 32) {

@@ -42,7 +42,7 @@ EXPORTS = ("qdec_workspace_bytes", "qdec_step_launches", "qdec_workspace_init",
            "qdec_append_rope_fp8", "qdec_attn_split_fp8", "qdec_attn_decode_fp8",
            "qdec_prefill_append_rope", "qdec_prefill_attn", "qdec_prefill_append_rope_fp8",
            "qdec_prefill_attn_fp8", "qdec_prefill_fp8_workspace_bytes", "qdec_qkv_append_rope_fp8",
-           "qdec_step_fp8",
+           "qdec_step_fp8", "qdec_prefill_rope_table_bytes", "qdec_prefill_rope_table",
            "qdec_step_static_scratch", "qdec_check_error", "qdec_status_string", "qdec_version")
 
 QDEC_STATIC_SCRATCH_BYTES = 4 << 20
@@ -114,12 +114,16 @@ def _load():
     lib.qdec_attn_decode.argtypes = [sp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     lib.qdec_attn_decode.restype = st
     lib.qdec_prefill_append_rope.argtypes = [sp, ctypes.c_int32, vp, i64, vp, i64, vp, i64, vp,
-                                             vp, vp, vp, vp, vp, vp, vp, vp, vp]
+                                             vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.qdec_prefill_append_rope.restype = st
     lib.qdec_prefill_attn.argtypes = [sp, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.qdec_prefill_attn.restype = st
     lib.qdec_prefill_append_rope_fp8.argtypes = [sp, ctypes.c_int32, vp, i64, vp, i64, vp, i64,
-                                                 vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+                                                 vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.qdec_prefill_rope_table_bytes.argtypes = [ctypes.c_int32]
+    lib.qdec_prefill_rope_table_bytes.restype = sz
+    lib.qdec_prefill_rope_table.argtypes = [sp, ctypes.c_int32, vp, vp, vp]
+    lib.qdec_prefill_rope_table.restype = st
     lib.qdec_prefill_append_rope_fp8.restype = st
     lib.qdec_prefill_attn_fp8.argtypes = [sp, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, sz, vp,
                                           vp, vp]
@@ -256,13 +260,34 @@ def qdec_attn_decode(shape: Shape, q_rot, kv_pool, block_table, seq_lens, worksp
         _ptr(err_flag), _stream(stream)), "qdec_attn_decode")
 
 
+def qdec_prefill_rope_table_bytes(num_tokens: int) -> int:
+    return int(_lib.qdec_prefill_rope_table_bytes(num_tokens))
+
+
+def qdec_prefill_rope_table(shape: Shape, positions, rope_table, stream=None):
+    """The angles of the chunk rows at `positions` [T] into `rope_table`
+    (qdec_prefill_rope_table_bytes(T) bytes)."""
+    _raise(_lib.qdec_prefill_rope_table(ctypes.byref(shape.c()), positions.numel(),
+                                        _ptr(positions), _ptr(rope_table), _stream(stream)),
+           "qdec_prefill_rope_table")
+
+
+def alloc_prefill_rope_table(num_tokens: int, device=None) -> torch.Tensor:
+    """A device buffer for qdec_prefill_rope_table (caller owns it)."""
+    return torch.empty(max(1, qdec_prefill_rope_table_bytes(num_tokens)), dtype=torch.uint8,
+                       device=device or "cuda")
+
+
 def qdec_prefill_append_rope(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, qo_indptr,
-                             seq_lens, block_table, kv_pool, q_rot, err_flag=None, stream=None):
+                             seq_lens, block_table, kv_pool, q_rot, err_flag=None, stream=None,
+                             rope_table=None):
     """Chunk rows q [T][Hq][D], k/v [T][Hkv][D] (row-strided views allowed),
-    positions [T], qo_indptr [B+1]; q_rot [T][Hq][D] float32 out."""
+    positions [T], qo_indptr [B+1]; q_rot [T][Hq][D] float32 out; rope_table
+    None or from qdec_prefill_rope_table over the same positions."""
     _raise(_lib.qdec_prefill_append_rope(
         ctypes.byref(shape.c()), q.shape[0], _ptr(q), _rows(q, "q"), _ptr(k), _rows(k, "k"),
-        _ptr(v), _rows(v, "v"), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions), _ptr(qo_indptr),
+        _ptr(v), _rows(v, "v"), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions),
+        _ptr(rope_table), _ptr(qo_indptr),
         _ptr(seq_lens), _ptr(block_table), _ptr(kv_pool), _ptr(q_rot), _ptr(err_flag),
         _stream(stream)), "qdec_prefill_append_rope")
 
@@ -277,11 +302,12 @@ def qdec_prefill_attn(shape: Shape, q_rot, qo_indptr, seq_lens, block_table, kv_
 
 def qdec_prefill_append_rope_fp8(shape: Shape, q, k, v, q_norm_w, k_norm_w, positions, qo_indptr,
                                  seq_lens, block_table, kv_pool_fp8, kv_scale, q_rot,
-                                 err_flag=None, stream=None):
+                                 err_flag=None, stream=None, rope_table=None):
     pool, scale = _fp8_pool(kv_pool_fp8, kv_scale)
     _raise(_lib.qdec_prefill_append_rope_fp8(
         ctypes.byref(shape.c()), q.shape[0], _ptr(q), _rows(q, "q"), _ptr(k), _rows(k, "k"),
-        _ptr(v), _rows(v, "v"), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions), _ptr(qo_indptr),
+        _ptr(v), _rows(v, "v"), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions),
+        _ptr(rope_table), _ptr(qo_indptr),
         _ptr(seq_lens), _ptr(block_table), pool, scale, _ptr(q_rot), _ptr(err_flag),
         _stream(stream)), "qdec_prefill_append_rope_fp8")
 

@@ -304,17 +304,30 @@ qdec_status qdec_qkv_pack_weights(const qdec_shape *shape, int32_t hidden,
  * ignores the flag (it starts after the previous kernel).
  * FP8-pool forms follow the FP8 section below. */
 
+/* The RoPE angles of num_tokens chunk rows (row r at positions[r]) into
+ * rope_table (device, 16-byte aligned, qdec_prefill_rope_table_bytes):
+ * computed once per step, they serve every layer's qdec_prefill_append_rope
+ * (the angles depend on the positions only), as qdec_rope_table does for
+ * decode.  One launch. */
+size_t qdec_prefill_rope_table_bytes(int32_t num_tokens);
+qdec_status qdec_prefill_rope_table(const qdec_shape *shape, int32_t num_tokens,
+                                    const int32_t *positions, void *rope_table, void *stream);
+
 /* Steps 1-3 for every chunk row r: RMSNorm + NeoX RoPE at positions[r] of
  * its query rows (q [num_tokens][Hq][D], row stride q_stride) into q_rot
  * [num_tokens][Hq][D] fp32 (unscaled), and of its key rows; bf16(k_rot) and v
  * (k, v [num_tokens][Hkv][D], row strides k_stride, v_stride) into slot t of
- * its sequence.  positions [num_tokens] int32.  Errors as qdec_append_rope. */
+ * its sequence.  positions [num_tokens] int32.  rope_table: NULL (each row's
+ * angles computed in the kernel) or the rows' angles from
+ * qdec_prefill_rope_table over the same positions (the same bits, fewer
+ * instructions per layer).  Errors as qdec_append_rope. */
 qdec_status qdec_prefill_append_rope(const qdec_shape *shape, int32_t num_tokens,
                                      const qdec_bf16 *q, int64_t q_stride,
                                      const qdec_bf16 *k, int64_t k_stride,
                                      const qdec_bf16 *v, int64_t v_stride,
                                      const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
-                                     const int32_t *positions, const int32_t *qo_indptr,
+                                     const int32_t *positions, const void *rope_table,
+                                     const int32_t *qo_indptr,
                                      const int32_t *seq_lens, const int32_t *block_table,
                                      qdec_bf16 *kv_pool, float *q_rot, int32_t *err_flag,
                                      void *stream);
@@ -399,7 +412,8 @@ qdec_status qdec_prefill_append_rope_fp8(const qdec_shape *shape, int32_t num_to
                                          const qdec_bf16 *k, int64_t k_stride,
                                          const qdec_bf16 *v, int64_t v_stride,
                                          const qdec_bf16 *q_norm_w, const qdec_bf16 *k_norm_w,
-                                         const int32_t *positions, const int32_t *qo_indptr,
+                                         const int32_t *positions, const void *rope_table,
+                                         const int32_t *qo_indptr,
                                          const int32_t *seq_lens, const int32_t *block_table,
                                          uint8_t *kv_pool_fp8, const float *kv_scale,
                                          float *q_rot, int32_t *err_flag, void *stream);

@@ -412,6 +412,45 @@ def test_prefill_fp8_chunk_of_one_equals_fp8_decode():
     assert torch.allclose(out.float(), out_d.float(), rtol=2 ** -7, atol=8e-3)
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_prefill_rope_table_gives_the_same_bits(kv):
+    """The append with the step's angle table (qdec_prefill_rope_table over
+    the chunk rows' positions, away from the token index) writes the same
+    q_rot and pool bits as the append that computes each row's angles
+    itself: both take them from the same float-float routine."""
+    q = parity.qdec()
+    seq_lens, chunks = [300, 17, 1000], [20, 17, 200]
+    outs = []
+    for table in (False, True):
+        if kv == "fp8":
+            c, codes, sc = wl.prefill_case_fp8(seq_lens, chunks, seed=21, pos_offset=4093)
+        else:
+            c = wl.prefill_case(seq_lens, chunks, seed=21, pos_offset=4093)
+        shape = _shape(c, 3)
+        T = c.q.shape[0]
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        q_rot = torch.full((T, 32, 128), float("nan"), dtype=torch.float32, device="cuda")
+        rope = None
+        if table:
+            rope = q.alloc_prefill_rope_table(T)
+            q.qdec_prefill_rope_table(shape, c.positions, rope)
+        if kv == "fp8":
+            q.qdec_prefill_append_rope_fp8(shape, c.q, c.k, c.v, c.w_q, c.w_k, c.positions,
+                                           c.qo_indptr, c.seq_lens, c.block_table, codes, sc,
+                                           q_rot, err, rope_table=rope)
+            pool = codes
+        else:
+            q.qdec_prefill_append_rope(shape, c.q, c.k, c.v, c.w_q, c.w_k, c.positions,
+                                       c.qo_indptr, c.seq_lens, c.block_table, c.pool, q_rot, err,
+                                       rope_table=rope)
+            pool = c.pool
+        st, flags = q.qdec_check_error(err)
+        assert st == 0 and flags == 0, (st, flags)
+        outs.append((q_rot.clone(), pool.clone()))
+    assert torch.equal(outs[0][0].view(torch.int32), outs[1][0].view(torch.int32))
+    assert torch.equal(outs[0][1].view(torch.uint8), outs[1][1].view(torch.uint8))
+
+
 # ------------------------------------------------------------ full size --
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8", "fp8-workspace"])

@@ -108,13 +108,21 @@ def test_entry_points_reject_null_and_misaligned_arguments(q):
     assert lib.qdec_attn_decode(None, ok, ok, ok, ok, ok, 1 << 30, ok, z,
                                 z) == q.QDEC_ERR_INVALID_ARG
     # prefill: missing qo_indptr / q_rot / out, misaligned q_rot, negative row count
-    def pre_append(n=4, qo=ok, qr=ok):
-        return lib.qdec_prefill_append_rope(sh, n, ok, S, ok, S, ok, S, ok, ok, ok, qo, ok, ok, ok,
-                                            qr, z, z)
+    def pre_append(n=4, qo=ok, qr=ok, rt=z):
+        return lib.qdec_prefill_append_rope(sh, n, ok, S, ok, S, ok, S, ok, ok, ok, rt, qo, ok, ok,
+                                            ok, qr, z, z)
     assert pre_append(qo=z) == q.QDEC_ERR_INVALID_ARG
     assert pre_append(qr=z) == q.QDEC_ERR_INVALID_ARG
     assert pre_append(qr=bad) == q.QDEC_ERR_INVALID_ARG
     assert pre_append(n=-1) == q.QDEC_ERR_INVALID_ARG
+    assert pre_append(rt=bad) == q.QDEC_ERR_INVALID_ARG   # a misaligned angle table
+    # the prefill angle table: size, and missing or misaligned buffers
+    assert lib.qdec_prefill_rope_table_bytes(2048) == 2048 * 64 * 16
+    assert lib.qdec_prefill_rope_table_bytes(0) == 0 and lib.qdec_prefill_rope_table_bytes(-3) == 0
+    assert lib.qdec_prefill_rope_table(sh, 4, z, ok, z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_prefill_rope_table(sh, 4, ok, bad, z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_prefill_rope_table(sh, -1, ok, ok, z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_prefill_rope_table(None, 4, ok, ok, z) == q.QDEC_ERR_INVALID_ARG
     assert lib.qdec_prefill_attn(sh, 4, z, ok, ok, ok, ok, ok, z, z) == q.QDEC_ERR_INVALID_ARG
     assert lib.qdec_prefill_attn(sh, 4, ok, z, ok, ok, ok, ok, z, z) == q.QDEC_ERR_INVALID_ARG
     assert lib.qdec_prefill_attn(sh, 4, ok, ok, ok, ok, ok, z, z, z) == q.QDEC_ERR_INVALID_ARG
@@ -165,8 +173,8 @@ def test_fp8_entry_points_reject_bad_arguments(q):
                                     z) == q.QDEC_ERR_INVALID_ARG
     # prefill and the fused projection over an FP8 pool: scales required,
     # an odd number of KV heads unsupported
-    assert lib.qdec_prefill_append_rope_fp8(sh, 4, ok, S, ok, S, ok, S, ok, ok, ok, ok, ok, ok,
-                                            ok, z, ok, z, z) == q.QDEC_ERR_INVALID_ARG
+    assert lib.qdec_prefill_append_rope_fp8(sh, 4, ok, S, ok, S, ok, S, ok, ok, ok, z, ok, ok,
+                                            ok, ok, z, ok, z, z) == q.QDEC_ERR_INVALID_ARG
     assert lib.qdec_prefill_attn_fp8(odd, 4, ok, ok, ok, ok, ok, ok, z, 0, ok, z,
                                      z) == q.QDEC_ERR_UNSUPPORTED
     assert lib.qdec_prefill_attn_fp8(sh, 4, ok, ok, ok, ok, ok, bad, z, 0, ok, z,
