@@ -63,7 +63,7 @@ struct Params {
     int64_t q_stride, k_stride, v_stride;   // elements between sequences
     const __nv_bfloat16 *w_q, *w_k;
     const int32_t *positions, *seq_lens, *block_table;
-    const RopeEntry *rope;   // per-step table ([B][D/2]; prefill: [T][D/2]), or null: in-kernel angles
+    const RopeEntry *rope;   // [B][D/2] per-step table, or null: angles computed in-kernel
     RopeEntry *rope_out;     // rope-table kernel output
     __nv_bfloat16 *pool;
     uint8_t *pool8;          // E4M3 pool (FP8 entry points), same layout as pool
