@@ -89,9 +89,9 @@ TRAFFIC = {
     # --prefill 2048: the causal prefill attention kernel (over an FP8 pool the
     # kernel that reads the dequantized workspace)
     "prefill-b1-prompt2048-36layer":
-        {"kernel_sha": "647ba138eb681338", "bytes_per_launch": 42007496},
+        {"kernel_sha": "7ac9fd35607ab740", "bytes_per_launch": 42005519},
     "prefill-b1-prompt2048-36layer-fp8kv":
-        {"kernel_sha": "647ba138eb681338", "bytes_per_launch": 42010600},
+        {"kernel_sha": "7ac9fd35607ab740", "bytes_per_launch": 42008950},
     # --qkv: the projection kernel
     "b8-ctx256to384-36layer-qkv2560":
         {"kernel_sha": "d083545efb834ee5", "bytes_per_launch": 31553438},

@@ -441,6 +441,29 @@ __device__ __forceinline__ void tma_load_plane8(uint32_t dst, const CUtensorMap 
         : "memory");
 }
 
+// Packed fp32 pairs: one instruction does the work of two (the softmax
+// warps are issue-bound, not bound by the exponential unit).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+__device__ __forceinline__ float f2_lo(uint64_t a) { return __uint_as_float(static_cast<uint32_t>(a)); }
+__device__ __forceinline__ float f2_hi(uint64_t a) { return __uint_as_float(static_cast<uint32_t>(a >> 32)); }
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // Offset of 16-byte chunk c of row r in a [rows][128 bytes] 128-byte
 // swizzled block starting on a 1024-byte boundary.
 __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
@@ -945,7 +968,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int q = 0; q < kTcPagesPerStage; ++q) vs[q] = vsr[q];
 #pragma unroll
-                for (int c = 0; c < kTcKeys; ++c) sc[c] *= ks[c / kPageSize];
+                for (int c = 0; c < kTcKeys; c += 2) {  // a pair shares its page
+                    const float k = ks[c / kPageSize];
+                    const uint64_t q = f2_mul(f2_pack(sc[c], sc[c + 1]), f2_pack(k, k));
+                    sc[c] = f2_lo(q);
+                    sc[c + 1] = f2_hi(q);
+                }
             }
             const int kb = j * kTcKeys;
             if (kb + kTcKeys - 1 > lim) {
@@ -995,22 +1023,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // each weight rounded to the nearest bf16 (ties away from zero:
             // 0x8000 added to its bits, the upper half kept); FP8 pool: f16
             // weights times their page's V scale
-            float ps[4] = {0.f, 0.f, 0.f, 0.f};   // the row sum in four chains
+            // (pairs of keys in packed fp32: the subtraction of the maximum
+            // and the row sum, two chains per packed accumulator)
+            uint64_t ps2[2] = {0ull, 0ull};
+            const uint64_t mm = f2_pack(m, m);
             uint32_t pw[kTcKeys / 2];
 #pragma unroll
             for (int c = 0; c < kTcKeys / 2; ++c) {
-                const float p0 = fast_exp2(sc[2 * c] - m);
-                const float p1 = fast_exp2(sc[2 * c + 1] - m);
+                const uint64_t d = f2_sub(f2_pack(sc[2 * c], sc[2 * c + 1]), mm);
+                const float p0 = fast_exp2(f2_lo(d));
+                const float p1 = fast_exp2(f2_hi(d));
+                const uint64_t pp = f2_pack(p0, p1);
+                ps2[c & 1] = f2_add(ps2[c & 1], pp);
                 if constexpr (kF16) {
-                    ps[c & 3] += p0 + p1;
                     const float sv = vs[(2 * c) / kPageSize];
-                    pw[c] = pack16x2<kF16>(p0 * sv, p1 * sv);
+                    const uint64_t q = f2_mul(pp, f2_pack(sv, sv));
+                    pw[c] = pack16x2<kF16>(f2_lo(q), f2_hi(q));
                 } else {
-                    ps[c & 3] += p0 + p1;
                     pw[c] = __byte_perm(__float_as_uint(p0) + 0x8000u, __float_as_uint(p1) + 0x8000u,
                                         0x7632);
                 }
             }
+            const float ps[4] = {f2_lo(ps2[0]), f2_hi(ps2[0]), f2_lo(ps2[1]), f2_hi(ps2[1])};
             // P of stage j - 1 stays until its value product is done
             if (j > 0) {
                 if (!wait_all(o_done(u), (j - 1) & 1)) {
