@@ -720,6 +720,20 @@ def timed_steps(run, stream, steps: int, warmup: int, dist: Dist, flush=None, cl
     return t_ms, dist.max(t_ms), per
 
 
+def step_spread(per_ms, layers: int) -> dict:
+    """Median and 10th / 90th percentiles (nearest rank) of the per-step
+    CUDA-event times, as µs per layer-step."""
+    xs = sorted(per_ms)
+    if not xs:
+        return {}
+
+    def rank(f):
+        return xs[min(len(xs) - 1, int(round(f * (len(xs) - 1))))] * 1e3 / layers
+
+    return {"median": round(rank(0.5), 4), "p10": round(rank(0.1), 4),
+            "p90": round(rank(0.9), 4)}
+
+
 def l2_flush_buffer(bytes_step: int, l2: int):
     """A buffer of twice the L2 size when a step's inputs would fit in it."""
     if bytes_step < 2 * l2:
@@ -748,10 +762,10 @@ def config_record(qdec, workload_id: int, args, dist: Dist, dev: int, peak: floa
             with torch.cuda.stream(stream):
                 step()   # first launch configures the kernels
         ck = Clocks(dev) if with_clocks else None
-        t_ms, t_max, _ = timed_steps(run, stream, args.steps, max(3, args.warmup), dist, fl, ck)
+        t_ms, t_max, per = timed_steps(run, stream, args.steps, max(3, args.warmup), dist, fl, ck)
         layers.check()
         us = t_max / args.steps / L * 1e3
-        rec = {"us_per_layer_step": round(us, 4),
+        rec = {"us_per_layer_step": round(us, 4), "spread": step_spread(per, L),
                "gbs": round(dist.world * bytes_layer / (us * 1e-6) / 1e9, 2),
                "frac_of_hbm": round(bytes_layer / (us * 1e-6) / 1e9 / peak, 4)}
         if ck:
@@ -1017,6 +1031,7 @@ def run_ours(args, dist: Dist):
                      + (", pages cast to E4M3 with amax/448 scales)" if args.kv == "fp8"
                         else ")")),
             "us_per_layer_step": round(ms_step * 1e3 / L, 4),
+            "us_per_layer_step_spread": step_spread(per, L),
             "pct_of_hbm_peak": round(100 * value / dist.world / peak, 2),
             "config": cfg,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,

@@ -114,3 +114,13 @@ def test_reference_arm_prepares_its_steps_outside_the_clock():
     assert [b for _, b in prepared] == [0, 1, 0, 1, 0]
     assert bench.oracle_run_steps(w, prepared) == sum(
         bench.sample_bytes(w, [L]) for L in (40, 17, 40, 17, 40))
+
+
+def test_step_spread_percentiles_by_nearest_rank():
+    """Per-step ms over 4 layers: median, p10 and p90 by nearest rank, in µs
+    per layer-step; an empty list gives no figures."""
+    per = [float(x) for x in range(1, 12)]          # 1 .. 11 ms
+    got = bench.step_spread(per, 4)
+    assert got == {"median": 6 * 1e3 / 4, "p10": 2 * 1e3 / 4, "p90": 10 * 1e3 / 4}
+    assert bench.step_spread([], 4) == {}
+    assert bench.step_spread([2.0], 2) == {"median": 1000.0, "p10": 1000.0, "p90": 1000.0}
