@@ -16,7 +16,7 @@ namespace {
 
 using qdec::Params;
 
-constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kVersion = 20000;  // 2.0.0: the prefill entry points gained a workspace and an angle table
 
 // ----------------------------------------------------------- device info --
 // Per-device attribute caches: calls may come from several host threads, so

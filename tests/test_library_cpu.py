@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(q):
 
 
 def test_version_and_status_strings(q):
-    assert q.qdec_version() == 10000
+    assert q.qdec_version() == 20000
     for st in range(7):
         assert q.status_string(st) and q.status_string(st) != "unknown status"
     assert q.status_string(99) == "unknown status"
